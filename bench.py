@@ -1,0 +1,363 @@
+"""Throughput of the stale-weight SGD hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config smlps|tiny|vgg_c|vgg_i|ps]
+
+A step is one pass of the whole hot path over one batch per logical replica:
+every replica's forward, softmax cross-entropy and backward (gradients fused
+into its GradBuf), then the parameter-server update that writes the next
+weight version. Default workload: the SMLPs MLP (3072 -> 5000 x5 -> 10),
+batch 512 per replica, 4 replicas with seeded delays in {0..3}, eta = 0.01.
+
+Prints one JSON line (rank 0). `value` is images/s with inputs resident in HBM;
+`e2e` is the same metric with every step's inputs copied from pinned host
+memory and the loss read back inside the timed region. `roofline` is the
+dominant kernel's achieved TF32 FLOP/s (or HBM GB/s for the update sweep)
+from CUDA events around its launches, against the measured peak.
+`--impl reference` times the FP64 CPU oracle on the same workload (bounded
+sample per step). Multi-GPU (torchrun): every rank runs an independent replica
+of the workload (no data-path collective); value = the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor ratio (tf32 1.1 PF vs bf16 2.25 PF)
+
+CONFIGS = {
+    "smlps": dict(net="smlps", batch=512, replicas=4, max_delay=3, optimizer="sgd", eta=0.01,
+                  desc="SMLPs MLP 3072-5000x5-10 fp32, batch 512/replica, ASGD 4 replicas, delays {0..3}, SGD eta=0.01"),
+    "tiny": dict(net="tiny", batch=8, replicas=1, max_delay=0, optimizer="sgd", eta=0.01,
+                 desc="tiny CNN (conv16-pool-conv32-pool-fc10), batch 8, SGD eta=0.01"),
+    "vgg_c": dict(net="vgg_c", batch=128, replicas=1, max_delay=0, optimizer="momentum", eta=0.01,
+                  stage_delays=[3, 2, 1, 0],
+                  desc="VGG-16 CIFAR-shaped fp32, batch 128, momentum 0.9, 4 pipeline stages s_k=3,2,1,0"),
+    "vgg_i": dict(net="vgg_i", batch=64, replicas=8, max_delay=7, optimizer="sgd", eta=0.005,
+                  desc="VGG-16 ILSVRC-shaped fp32, batch 64/replica, ASGD 8 replicas, delays {0..7}, SGD eta=0.005"),
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class GemmProbe:
+    """Records CUDA events, on the launching stream, around the forward FC
+    GEMM launches of the given (in, out) shapes (one tensor-core kernel per
+    call). Installed by the bench only; the library is untouched."""
+
+    def __init__(self, sprint_mod, torch, shapes):
+        self.S = sprint_mod
+        self.torch = torch
+        self.shapes = set(shapes)
+        self.active = False
+        self.events = []
+        self.flops = None
+        self.orig = sprint_mod.sprint_fc_fwd
+        probe = self
+
+        def fc_fwd(x, w, b, y, N, i, o, relu, stream=None):
+            if not (probe.active and (i, o) in probe.shapes):
+                return probe.orig(x, w, b, y, N, i, o, relu, stream)
+            st = torch.cuda.ExternalStream(stream) if isinstance(stream, int) else torch.cuda.current_stream()
+            a = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            r = probe.orig(x, w, b, y, N, i, o, relu, stream)
+            e.record(st)
+            probe.events.append((a, e, 2.0 * N * i * o))
+            return r
+        sprint_mod.sprint_fc_fwd = fc_fwd
+
+    def summary(self):
+        if not self.events:
+            return None
+        ms = np.array([a.elapsed_time(e) for a, e, _ in self.events])
+        fl = np.array([f for _, _, f in self.events])
+        return {"launches": len(ms), "mean_ms": float(ms.mean()), "total_ms": float(ms.sum()),
+                "tflops": float((fl / (ms / 1e3)).mean() / 1e12), "flops_per_launch": float(fl.mean())}
+
+
+def dense_init(shapes, seed):
+    import synth
+    return np.concatenate([np.concatenate([synth.normal(seed, f"w{i}", (L.w_numel,), np.sqrt(2.0 / L.fan_in)),
+                                           np.zeros(L.cout, np.float32)]) for i, L in enumerate(shapes)])
+
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+
+    from stale_weight_sgd_gb300 import model, sprint
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    net = model.NETWORKS[cfg["net"]]
+    shapes = model.layer_shapes(net)
+    N, R = cfg["batch"], cfg["replicas"]
+    c, h, w = net["input"]
+    feat = c * h * w
+    classes = shapes[-1].cout
+    P = max(2 * R, 8)
+    kw = dict(replicas=R, max_delay=cfg["max_delay"], schedule_seed=1234, optimizer=cfg["optimizer"], eta=cfg["eta"])
+    if "stage_delays" in cfg:
+        kw = dict(stage_of_layer=model.VGG_C_STAGES, stage_delays=cfg["stage_delays"], optimizer=cfg["optimizer"],
+                  eta=cfg["eta"])
+    tr = StaleSGD(net, N, **kw)
+    # synthetic data generated on the device (seeded), weights He-normal
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    xs = torch.randn((P, N, feat), generator=g, device=dev, dtype=torch.float32)
+    ys = torch.randint(0, classes, (P, N), generator=g, device=dev, dtype=torch.int32)
+    tr.set_batch_pool(xs, ys)
+    wd = dense_init(shapes, 7)
+    tr.load_weights(wd)
+
+    big = [(L.cin, L.cout) for L in shapes if L.kind == "fc" and L.cin * L.cout >= 20_000_000]
+    probe = GemmProbe(sprint, torch, big)
+
+    for _ in range(args.warmup):
+        tr.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    probe.active = True
+    launches0 = sprint.sprint_launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(tr.main_stream)
+    for _ in range(args.steps):
+        tr.step()
+    end.record(tr.main_stream)
+    torch.cuda.synchronize()
+    probe.active = False
+    launches = sprint.sprint_launch_count() - launches0
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    ms_max = allreduce_max(ms, world)
+    barrier(world)
+    loss = tr.step_loss()
+
+    # end to end: inputs from pinned host memory every step, loss read back
+    hx = torch.empty((R, N, feat), dtype=torch.float32).pin_memory()
+    hy = torch.empty((R, N), dtype=torch.int32).pin_memory()
+    hx.copy_(xs[:R].cpu())
+    hy.copy_(ys[:R].cpu())
+    dx = torch.empty((R, N, feat), dtype=torch.float32, device=dev)
+    dy = torch.empty((R, N), dtype=torch.int32, device=dev)
+    tr.set_batch_pool(dx, dy)
+    hloss = torch.empty((R,), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        main = tr.main_stream
+        tr.main_stream.wait_event(tr.ev_update)
+        with torch.cuda.stream(main):
+            dx.copy_(hx, non_blocking=True)
+            dy.copy_(hy, non_blocking=True)
+        tr.ev_update.record(main)
+        tr.step()
+        with torch.cuda.stream(main):
+            hloss.copy_(tr.loss[:, 0], non_blocking=True)
+        main.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = allreduce_max(e2e_s, world)
+
+    imgs = R * N * args.steps * world
+    value = imgs / (ms_max / 1e3)
+    e2e_value = imgs / e2e_s
+    peaks, peak_src = load_peaks()
+    summ = probe.summary()
+    roof = None
+    if summ:
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
+        achieved = summ["flops_per_launch"] / (summ["mean_ms"] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "tc_gemm_kernel (FC forward 512x5000x5000, TF32)",
+                "peak_source": f"{peak_src}: bf16 sustained x 1.1/2.25 (nominal tf32/bf16 dense ratio)",
+                "launches": summ["launches"], "mean_ms": round(summ["mean_ms"], 4)}
+    flops_step = model.train_flops_per_image(net) * R * N
+    out = {
+        "metric": "CNN train images/s on 1 GB300; conv-GEMM % TF32 peak; update GB/s vs HBM peak",
+        "value": round(value, 1), "unit": "images/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (tf32 tensor-core GEMMs, fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) inputs, uniform labels, He-normal init)",
+        "config": {"workload": cfg["desc"], "global_batch": R * N * world, "replicas_per_gpu": R,
+                   "parallelism": f"replicas only x{world}" if world > 1 else "1 GPU",
+                   "l2": "working set (weights, 4 GradBufs) far larger than L2; no flush needed"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "images/s",
+                "h2d_bytes_per_step": int(hx.numel() * 4 + hy.numel() * 4), "d2h_bytes_per_step": int(R * 4)},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "achieved_step_tflops": round(flops_step * args.steps / (ms_max / 1e3) / 1e12 * world, 1),
+        "clocks": clk,
+        "loss_last": loss,
+        "kernels_per_step": int(launches // args.steps),
+    }
+    return out
+
+
+def cpu_oracle_rate(cfg, budget_s=12.0):
+    """Images/s of the FP64 oracle's forward+backward for one replica batch,
+    on a bounded sample of images at the workload's full layer sizes."""
+    import oracle as O
+    import synth
+    arch = O.ARCHS[cfg["net"]]
+    layers = O.build_layers(arch)
+    c, h, w = arch["input"]
+    w0 = np.concatenate([np.concatenate([synth.normal(7, f"w{i}", (int(np.prod(L.w_shape)),), O.he_std(L)),
+                                         np.zeros(L.cout, np.float32)]) for i, L in enumerate(layers)]).astype(np.float64)
+    n = 2
+    done, elapsed = 0, 0.0
+    while True:
+        x = synth.images_nhwc(3, f"cpu{n}", n, c, h, w)
+        if layers[0].kind == "fc":
+            x = x.reshape(n, -1)
+        y = synth.labels(3, f"cpuy{n}", n, layers[-1].cout)
+        t0 = time.perf_counter()
+        O.gradient(layers, w0, x, y)
+        dt = time.perf_counter() - t0
+        done += n
+        elapsed += dt
+        if elapsed >= budget_s or dt * 4 + elapsed > budget_s * 2:
+            break
+        n = min(n * 2, cfg["batch"])
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return done / elapsed, cores, f"{done} images of one replica's forward+backward at full layer sizes ({elapsed:.1f} s)"
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="smlps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    cfg = CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, cores, sample = cpu_oracle_rate(cfg, budget_s=8.0)
+        step_imgs = cfg["replicas"] * cfg["batch"]
+        out = {"impl": "reference", "metric": "CNN train images/s on 1 GB300; conv-GEMM % TF32 peak; update GB/s vs HBM peak",
+               "value": round(rate, 3), "unit": "images/s", "n_gpus": args.gpus, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": round(step_imgs / rate * 1e3, 1), "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+               "config": {"workload": cfg["desc"], "global_batch": step_imgs},
+               "cpu_baseline": {"value": round(rate, 3), "unit": "images/s", "cores": cores, "kind": "oracle",
+                                "sample": sample},
+               "e2e": {"value": round(rate, 3), "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    out = run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            rate, cores, sample = cpu_oracle_rate(cfg)
+            out["cpu_baseline"] = {"value": round(rate, 3), "unit": "images/s", "cores": cores, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

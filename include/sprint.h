@@ -1,0 +1,241 @@
+/*
+ * sprint.h — C ABI of the GB300 (sm_103a) stale-weight SGD hot path.
+ *
+ * One process drives one GPU. The library computes the minibatch-SGD worker
+ * step of a CNN/MLP (forward pass, dE/dW, dE/db, dE/dX by implicit-GEMM /
+ * im2col convolution, FC GEMMs, 2x2 max-pooling, ReLU, softmax cross-entropy)
+ * and the gradient-buffer / parameter-server update (GradBuf accumulation,
+ * then plain SGD, momentum or per-parameter Adagrad), as set out in:
+ *
+ *   [S]  IPSJ SIG Technical Report Vol.2016-HPC-155 No.8, "SPRINT" ASGD CNN
+ *        framework: Eq. (1) minibatch SGD; Eq. (2)-(3) network shapes;
+ *        Sec. 3.3, Eq. (4)-(6) and the SGEMM role table that follows Eq. (6)
+ *        (convolution, fc, dedw, dedb, dedx fc, dedx conv, im2col);
+ *        Algorithm 1 (GPU thread: ComputeGradient, ComputeUpdateVal,
+ *        UpdateGradient into GradBuf_t); Algorithm 2 (update thread:
+ *        SumGradient, momentum via DeltaWeights, UpdateWeights).
+ *   [PB] "Pipelined training of deep CNNs with stale weights", Sec. 4.1.
+ *   [DB] "Google DistBelief Paper: Large Scale Distributed Deep Networks"
+ *        (parameter-server update w' := w - eta*dw, Adagrad, n_push).
+ *
+ * Conventions for every entry point
+ *  - Return value: a sprint_status (0 = SPRINT_OK). On error nothing is
+ *    launched, and sprint_last_error() returns a message (thread-local).
+ *  - Arguments are validated on the host before any launch.
+ *  - Device pointers are caller-owned (the library never allocates, frees or
+ *    keeps them past the call) and must be 16-byte aligned, else
+ *    SPRINT_ERR_ALIGN. Host pointers are marked "host".
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream). Output buffers must not alias inputs unless the
+ *    entry point says so.
+ *  - All tensors are fp32. GEMM-shaped work runs on the tensor cores as TF32
+ *    with FP32 accumulation; every other operation is exact fp32 arithmetic.
+ *  - Layouts: activations NHWC [N][H][W][C]; conv weights [Cout][3][3][Cin]
+ *    (GEMM K index = (kh*3 + kw)*Cin + ci); FC weights [out][in]; row-major.
+ *  - Convolutions are 3x3, stride 1 ([S] Sec. 3.2, c = 3); `pad` is 0 or 1;
+ *    the output is (H + 2*pad - 2) x (W + 2*pad - 2).
+ *  - Kernels never trap. A bounded wait inside a kernel that gives up sets a
+ *    device status word; sprint_device_status() reads it (SPRINT_ERR_DEVICE_FLAG).
+ */
+#ifndef SPRINT_H
+#define SPRINT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* sprint_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    SPRINT_OK = 0,
+    SPRINT_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad flag    */
+    SPRINT_ERR_SHAPE = 2,       /* inconsistent or out-of-range dimensions   */
+    SPRINT_ERR_ALIGN = 3,       /* device pointer not 16-byte aligned        */
+    SPRINT_ERR_UNSUPPORTED = 4, /* valid but not implemented (e.g. k > 16)   */
+    SPRINT_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed         */
+    SPRINT_ERR_DEVICE_FLAG = 6, /* a kernel reported a failed bounded wait   */
+    SPRINT_ERR_WORKSPACE = 7    /* caller workspace missing or too small     */
+} sprint_status;
+
+/* Message of the last failed call on this thread ("" if none). Never NULL. */
+const char* sprint_last_error(void);
+
+/* ABI version (major*100 + minor). */
+int sprint_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads). Host-side counter; no device call. */
+uint64_t sprint_launch_count(void);
+
+/* Reads (and with reset != 0 clears) the device status word that kernels set
+ * when a bounded wait gives up. *flags_out = 0 means no kernel reported a
+ * failure. Synchronises the device. Returns SPRINT_ERR_DEVICE_FLAG if a flag
+ * was set, SPRINT_OK otherwise. */
+int sprint_device_status(int* flags_out, int reset);
+
+/* ------------------------------------------------------------------------
+ * im2col — the explicit unrolling of [S] Sec. 3.3, Eq. (5): rows x_l^2 * N,
+ * columns c^2 * m_{l-1}.
+ * x:   device [N][H][W][C]
+ * col: device [N*Ho*Wo][9*C]; row (n,oh,ow), column (kh*3+kw)*C + ci holds
+ *      x[n][oh+kh-pad][ow+kw-pad][ci], or 0 outside the image.
+ * src_index: device [N*Ho*Wo][9*C] int32 or NULL; the flat NHWC index of the
+ *      source element in x, or -1 for padding. Bit-exact by construction.
+ * Errors: SHAPE if any size < 1, pad not in {0,1}, or N*Ho*Wo*9*C >= 2^31.
+ */
+int sprint_im2col(const float* x, int N, int H, int W, int C, int pad, float* col, int32_t* src_index,
+                  sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Convolution forward — the "convolution" SGEMM role of [S] Sec. 3.3
+ * (m = x_l^2 N, n = m_l, k = c^2 m_{l-1}), with the bias and ReLU of Sec. 3.2
+ * fused into the epilogue:
+ *   y[n,oh,ow,co] = act(b[co] + sum_{kh,kw,ci} x[n,oh+kh-pad,ow+kw-pad,ci] * w[co,kh,kw,ci])
+ * act = ReLU if relu != 0, identity otherwise. b may be NULL (no bias).
+ * x: device [N][H][W][Cin]; w: device [Cout][3][3][Cin]; b: device [Cout];
+ * y: device [N][Ho][Wo][Cout] (written, must not alias x).
+ * Implicit GEMM: no im2col buffer is formed. Layers whose channel counts the
+ * tensor-core loader cannot tile (Cin or Cout not a multiple of 32, e.g. the
+ * RGB input layer) run on a CUDA-core direct-convolution kernel instead.
+ * ws: see sprint_conv_workspace_size(SPRINT_CONV_FWD, ...).
+ */
+int sprint_conv_fwd(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
+                    int Cout, int pad, int relu, void* ws, size_t ws_bytes, sprint_stream_t stream);
+
+/* Convolution input gradient — the "dedx conv" role of [S] Sec. 3.3:
+ *   dx[n,i,j,ci] = mask(n,i,j,ci) * sum_{kh,kw,co} dy[n,i-kh+pad,j-kw+pad,co] * w[co,kh,kw,ci]
+ * mask = (relu_src > 0) if relu_src != NULL (relu_src is this layer's input,
+ * i.e. the previous layer's ReLU output, [N][H][W][Cin]), else 1.
+ * dy: device [N][Ho][Wo][Cout]; dx: device [N][H][W][Cin] (fully written).
+ * wT: device [3][3][Cin][Cout] = w transposed (sprint_transpose of w viewed as
+ * [Cout][9*Cin]), or NULL: the tensor cores read both operands k-contiguous,
+ * so without wT the call transposes w into its workspace first.
+ * ws: see sprint_conv_workspace_size(SPRINT_CONV_DX, ...) (sized for wT == NULL). */
+int sprint_conv_dX(const float* dy, const float* w, const float* wT, const float* relu_src, float* dx, int N, int H,
+                   int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes, sprint_stream_t stream);
+
+/* Convolution operations, for sprint_conv_workspace_size(). */
+enum { SPRINT_CONV_FWD = 0, SPRINT_CONV_DX = 1, SPRINT_CONV_DW = 2 };
+
+/* Workspace bytes the convolution `op` needs for this shape (split-K partial
+ * sums, partial bias sums); 0 means none. Every conv entry point takes a
+ * caller-owned device workspace `ws` of at least this many bytes (contents on
+ * entry ignored, clobbered by the call; NULL allowed when the size is 0, else
+ * SPRINT_ERR_WORKSPACE). Calls that may overlap on the GPU need separate
+ * workspaces. */
+size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Cin, int Cout, int pad);
+
+/* Convolution weight and bias gradients — the "dedw" and "dedb" roles of
+ * [S] Sec. 3.3 (dedw: m = c^2 m_{l-1}, n = m_l, k = x_l^2 N), fused with
+ * UpdateGradient of Algorithm 1 (GradBuf_t <- Grad, or += Grad):
+ *   dw[co,kh,kw,ci] = (accumulate ? dw : 0) + alpha * sum_{n,oh,ow} dy[n,oh,ow,co] x[n,oh+kh-pad,ow+kw-pad,ci]
+ *   db[co]          = (accumulate ? db : 0) + alpha * sum_{n,oh,ow} dy[n,oh,ow,co]   (db may be NULL)
+ * dy is the gradient w.r.t. the pre-activation (the ReLU mask already applied).
+ * ws: see sprint_conv_workspace_size(SPRINT_CONV_DW, ...). */
+int sprint_conv_dW(const float* x, const float* dy, float* dw, float* db, float alpha, int accumulate, int N, int H,
+                   int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * FC forward — the "fc" role of [S] Sec. 3.3 (m = N, n = m_l, k = m_{l-1}):
+ *   y[n][o] = act(b[o] + sum_i x[n][i] * w[o][i]), act = ReLU if relu != 0.
+ * x: device [N][in]; w: device [out][in]; b: device [out] or NULL;
+ * y: device [N][out] (must not alias x). */
+int sprint_fc_fwd(const float* x, const float* w, const float* b, float* y, int N, int in, int out, int relu,
+                  sprint_stream_t stream);
+
+/* FC backward — the "dedx fc", "dedw" and "dedb" roles of [S] Sec. 3.3,
+ * with UpdateGradient of Algorithm 1 fused into the dW/db epilogue:
+ *   dx[n][i] = mask[n][i] * sum_o dy[n][o] * w[o][i]       (skipped if dx == NULL)
+ *   dw[o][i] = (accumulate ? dw : 0) + alpha * sum_n dy[n][o] * x[n][i]
+ *   db[o]    = (accumulate ? db : 0) + alpha * sum_n dy[n][o]  (skipped if db == NULL)
+ * mask = (relu_src > 0) when relu_src != NULL (this layer's input [N][in]),
+ * else 1. dy is the gradient w.r.t. this layer's pre-activation output.
+ * x [N][in], w [out][in], dy [N][out], relu_src: device inputs;
+ * wT: device [in][out] = w transposed (sprint_transpose), or NULL (then
+ * transposed into the workspace); dx [N][in], dw [out][in], db [out]: outputs.
+ * The weight-gradient GEMM contracts over the batch; its operands are
+ * transposed into the workspace (k contiguous for the tensor cores).
+ * ws: device workspace of at least sprint_fc_workspace_size(N, in, out,
+ * wT != NULL) bytes (caller-owned scratch, clobbered; NULL if that is 0). */
+int sprint_fc_bwd(const float* x, const float* w, const float* wT, const float* dy, const float* relu_src, float* dx,
+                  float* dw, float* db, float alpha, int accumulate, int N, int in, int out, void* ws, size_t ws_bytes,
+                  sprint_stream_t stream);
+
+/* Workspace bytes sprint_fc_bwd needs (have_wT: whether wT will be passed). */
+size_t sprint_fc_workspace_size(int N, int in, int out, int have_wT);
+
+/* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
+ * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must
+ * not alias. */
+int sprint_transpose(const float* src, float* dst, int rows, int cols, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 2x2 stride-2 max-pool forward — the pooling p_l = 2 of [S] Sec. 3.2/Eq. (2).
+ * x: device [N][H][W][C]; y: device [N][H/2][W/2][C] (floor; a trailing odd
+ * row/column is ignored); argmax: device [N][H/2][W/2][C] uint8, code
+ * 2*dy + dx of the first window element (row-major) that is strictly greater
+ * than every element before it. Bit-exact on identical inputs. */
+int sprint_pool_fwd(const float* x, float* y, uint8_t* argmax, int N, int H, int W, int C, sprint_stream_t stream);
+
+/* Max-pool backward with the ReLU derivative of the pooled layer:
+ *   dx[n, 2i+dy, 2j+dx, c] = dy[n,i,j,c] * (pooled[n,i,j,c] > 0)  at the argmax code, else 0.
+ * pooled: the forward output y (device [N][H/2][W/2][C]) or NULL for no mask.
+ * (The selected element of the ReLU output equals pooled, so this is the ReLU
+ * derivative of the conv layer feeding the pool.)
+ * dx: device [N][H][W][C], fully written (zeros off the argmax). */
+int sprint_pool_bwd(const float* dy, const uint8_t* argmax, const float* pooled, float* dx, int N, int H, int W,
+                    int C, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Softmax cross-entropy — the softmax output layer of [S] Sec. 3.2:
+ *   loss    = (1/N) sum_n [log sum_c exp(z[n][c]) - z[n][label[n]]]
+ *   dlogits = (softmax(z) - onehot(label)) / N
+ * With reduction_sum != 0 the 1/N factors are dropped (literal Eq. (1) sum).
+ * logits: device [N][C]; labels: device int32 [N], each in [0, C) (not
+ * checked on the device: a label out of range gives an undefined row);
+ * loss: device fp32 scalar; dlogits: device [N][C] (may alias logits). */
+int sprint_softmax_xent(const float* logits, const int32_t* labels, int N, int C, float* loss, float* dlogits,
+                        int reduction_sum, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * GradBuf accumulation — ComputeUpdateVal + UpdateGradient of Algorithm 1:
+ *   buf[i] = (first ? 0 : buf[i]) + alpha * grad[i],  i < n.
+ * alpha = 1 stores raw gradients (eta applied at the update); alpha = -eta is
+ * the report's own form. buf and grad: device fp32 [n]. */
+int sprint_gradbuf_accumulate(float* buf, const float* grad, size_t n, float alpha, int first, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Parameter-server apply — SumGradient + UpdateWeights of Algorithm 2 and
+ * the DistBelief rule w' := w - eta*dw, over k pending gradient buffers
+ * (n_push accumulation). With S[i] = sum_{j<k} bufs[j][i] (summed in j order):
+ *   sgd:      w_out = w_in - eta*S
+ *   momentum: v = nu*v - eta*S;             w_out = w_in + v
+ *   adagrad:  G = G + S*S;                  w_out = w_in - eta*S/(sqrt(G) + eps)
+ * bufs: HOST array of k device pointers, 1 <= k <= 16. w_in == w_out is
+ * allowed (in place); writing a new ring slot (w_out != w_in) is the
+ * versioned-weights use. v and G are updated in place. n may be 0. */
+int sprint_apply_update_sgd(const float* w_in, float* w_out, const float* const* bufs, int k, size_t n, float eta,
+                            sprint_stream_t stream);
+int sprint_apply_update_momentum(const float* w_in, float* w_out, float* v, const float* const* bufs, int k,
+                                 size_t n, float eta, float nu, sprint_stream_t stream);
+int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const float* const* bufs, int k, size_t n,
+                                float eta, float eps, sprint_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Staleness schedule (host only) — the delays of asynchronous SGD ([S] Sec. 1,
+ * Fig. 1; [DB]: replicas fetch w, push dw). out[t*replicas + r] = delay of
+ * replica r at step t, in {0..max_delay}: z = the (t*replicas + r)-th output of
+ * SplitMix64 seeded with `seed` (Steele, Lea & Flood 2014), delay =
+ * ((z >> 32) * (max_delay + 1)) >> 32. Replica r then computes its gradient
+ * on W(max(0, t - delay)).
+ * out: HOST int32 [steps*replicas]. */
+int sprint_staleness_schedule(uint64_t seed, int steps, int replicas, int max_delay, int32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPRINT_H */

@@ -334,14 +334,15 @@ def softmax_xent(z, labels, reduction="mean"):
 # Worker step: forward, loss, backward (Algorithm 1 'ComputeGradient' of [S])
 # ---------------------------------------------------------------------------
 
-def forward_backward(layers: list[Layer], params, x, labels, reduction="mean"):
-    """Loss and per-layer (dW, db) for one batch.
+def forward(layers: list[Layer], params, x):
+    """Forward pass; returns (logits, saved) with saved[i] = (input of layer i,
+    its output after ReLU (before pooling), pool argmax or None).
 
     ``params`` is a list of (W, b) per layer; each layer may come from a
     different weight version (pipeline stages, R8). Conv layers: y = ReLU(conv + b),
     then optional 2x2 max-pool. FC layers: y = xW^T + b, ReLU unless the layer
     says otherwise. The input of the first FC layer is the NHWC activation
-    flattened in (h, w, c) order. Pinned by central finite differences."""
+    flattened in (h, w, c) order."""
     a = np.asarray(x, F64)
     n = a.shape[0]
     if layers[0].kind == "fc":
@@ -364,13 +365,21 @@ def forward_backward(layers: list[Layer], params, x, labels, reduction="mean"):
             y = relu(z) if L.relu else z
             saved.append((a, y, None))
             a = y
-    loss, g = softmax_xent(a, labels, reduction)
+    return a, saved
 
+
+def backward(layers: list[Layer], params, saved, g):
+    """Backward pass by hand, layer by layer, from dE/dlogits ``g``; returns
+    the per-layer (dW, db). Every decision it takes (ReLU derivative = 1 where
+    the saved output is > 0, R11; the pool argmax, R10) is read from ``saved``,
+    so it can be replayed on another implementation's saved activations."""
     grads = [None] * len(layers)
+    g = np.asarray(g, F64)
     for i in range(len(layers) - 1, -1, -1):
         L = layers[i]
         w, _ = params[i]
         xin, y, arg = saved[i]
+        xin = np.asarray(xin, F64)
         if L.kind == "fc":
             if L.relu:
                 g = g * relu_mask(y)
@@ -378,7 +387,7 @@ def forward_backward(layers: list[Layer], params, x, labels, reduction="mean"):
             grads[i] = (dw, db)
             g = dx
             if i > 0 and layers[i - 1].kind == "conv":
-                g = g.reshape(saved[i - 1][0].shape[0], *_out_hw(layers[i - 1]), layers[i - 1].cout)
+                g = g.reshape(xin.shape[0], *_out_hw(layers[i - 1]), layers[i - 1].cout)
         else:
             if L.pool:
                 g = maxpool2x2_bwd(g, arg, y.shape[1], y.shape[2])
@@ -387,7 +396,15 @@ def forward_backward(layers: list[Layer], params, x, labels, reduction="mean"):
             grads[i] = (dw, db)
             if i > 0:
                 g = conv3x3_dx(g, w, xin.shape[1], xin.shape[2])
-    return loss, grads
+    return grads
+
+
+def forward_backward(layers: list[Layer], params, x, labels, reduction="mean"):
+    """Loss and per-layer (dW, db) for one batch (forward, softmax
+    cross-entropy, backward). Pinned by central finite differences."""
+    logits, saved = forward(layers, params, x)
+    loss, g = softmax_xent(logits, labels, reduction)
+    return loss, backward(layers, params, saved, g)
 
 
 def _out_hw(L: Layer):
@@ -476,48 +493,80 @@ def version_used(t: int, s: int) -> int:
 # Stale-weight training driver (ASGD replicas [S] Fig. 1 / [DB]; pipeline [PB] 4.1)
 # ---------------------------------------------------------------------------
 
+def replica_params(layers, hist, t, r, *, schedule=None, stage_delays=None, stage_of_layer=None):
+    """Per-layer (W, b) that replica r uses at step t: W(max(0, t - s[t, r]))
+    for asynchronous replicas (R7), or W_l(max(0, t - s_k)) for the layers of
+    pipeline stage k (R8)."""
+    offs, _ = param_offsets(layers)
+    params = []
+    for li, L in enumerate(layers):
+        if stage_delays is not None:
+            ver = version_used(t, stage_delays[stage_of_layer[li]])
+        else:
+            ver = version_used(t, 0 if schedule is None else int(schedule[t, r]))
+        a, b = offs[li]
+        params.append((hist[ver][a:b].reshape(L.w_shape), hist[ver][b:b + L.cout]))
+    return params
+
+
+def step_gradients(layers, hist, t, batches, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
+                   reduction="mean"):
+    """Per-replica (loss, flat gradient) of global step t, given the weight
+    history hist[0..t] (hist[v] = W(v)).
+
+    Replica r draws batch (t*R + r) mod len(batches) and computes its gradient
+    at W(max(0, t - s[t, r])) (``schedule``), or, for a pipeline, every layer l
+    of stage k at W_l(max(0, t - s_k)) (``stage_delays``, ``stage_of_layer``)."""
+    losses, grads = [], []
+    for r in range(replicas):
+        x, y = batches[(t * replicas + r) % len(batches)]
+        params = replica_params(layers, hist, t, r, schedule=schedule, stage_delays=stage_delays,
+                                stage_of_layer=stage_of_layer)
+        loss, gl = forward_backward(layers, params, x, y, reduction)
+        losses.append(loss)
+        grads.append(flatten(gl))
+    return losses, grads
+
+
+def apply_update(w, grads, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None):
+    """The parameter-server apply of the summed gradients; returns (W', state')."""
+    if optimizer == "sgd":
+        return update_sgd(w, grads, eta), state
+    if optimizer == "momentum":
+        return update_momentum(w, state, grads, eta, nu)
+    if optimizer == "adagrad":
+        return update_adagrad(w, state, grads, eta, eps)
+    raise ValueError(optimizer)
+
+
+def train_step(layers, hist, t, batches, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
+               optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None, reduction="mean"):
+    """One global step: the R replica gradients (step_gradients), summed in
+    replica order and applied once (apply_update) with the optimizer state
+    before the step (momentum v or Adagrad G; ignored for SGD).
+    Returns (mean loss over replicas, W(t+1), new state)."""
+    losses, grads = step_gradients(layers, hist, t, batches, replicas=replicas, schedule=schedule,
+                                   stage_delays=stage_delays, stage_of_layer=stage_of_layer, reduction=reduction)
+    w_new, state = apply_update(hist[t], grads, optimizer, eta, nu, eps, state)
+    return sum(losses) / replicas, w_new, state
+
+
 def train(arch, w0, batches, steps, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
           optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, reduction="mean"):
-    """Simulated asynchronous training; returns (per-step mean loss, final W, history).
-
-    At step t replica r draws batch (t*R + r) mod len(batches), computes its
-    gradient at weights W(max(0, t - s[t, r])) (``schedule``) or, for a
-    pipeline, each layer l of stage k at W_l(max(0, t - s_k)) (``stage_delays``,
-    ``stage_of_layer``). The R gradients are summed in replica order and
-    applied once: W(t+1) = update(W(t), sum). The full history of W is kept,
-    which is the plain brute-force way to look up old versions."""
+    """Simulated asynchronous training from W(0) = w0; returns (per-step mean
+    loss, final W, history). The full history of W is kept, which is the plain
+    brute-force way to look up old versions (v0 = 0 for momentum, G0 = g0 for
+    Adagrad)."""
     layers = build_layers(arch)
-    offs, n = param_offsets(layers)
+    _, n = param_offsets(layers)
     hist = [np.asarray(w0, F64).copy()]
-    v = np.zeros(n, F64)
-    g2 = np.full(n, g0, F64)
+    state = np.zeros(n, F64) if optimizer == "momentum" else (np.full(n, g0, F64) if optimizer == "adagrad" else None)
     losses = []
     for t in range(steps):
-        grads, lsum = [], 0.0
-        for r in range(replicas):
-            x, y = batches[(t * replicas + r) % len(batches)]
-            if stage_delays is not None:
-                params = []
-                for li, L in enumerate(layers):
-                    ver = version_used(t, stage_delays[stage_of_layer[li]])
-                    a, b = offs[li]
-                    params.append((hist[ver][a:b].reshape(L.w_shape), hist[ver][b:b + L.cout]))
-                loss, gl = forward_backward(layers, params, x, y, reduction)
-                g = flatten(gl)
-            else:
-                s = 0 if schedule is None else int(schedule[t, r])
-                loss, g = gradient(layers, hist[version_used(t, s)], x, y, reduction)
-            grads.append(g)
-            lsum += loss
-        losses.append(lsum / replicas)
-        if optimizer == "sgd":
-            w_new = update_sgd(hist[t], grads, eta)
-        elif optimizer == "momentum":
-            w_new, v = update_momentum(hist[t], v, grads, eta, nu)
-        elif optimizer == "adagrad":
-            w_new, g2 = update_adagrad(hist[t], g2, grads, eta, eps)
-        else:
-            raise ValueError(optimizer)
+        loss, w_new, state = train_step(layers, hist, t, batches, replicas=replicas, schedule=schedule,
+                                        stage_delays=stage_delays, stage_of_layer=stage_of_layer, optimizer=optimizer,
+                                        eta=eta, nu=nu, eps=eps, state=state, reduction=reduction)
+        losses.append(loss)
         hist.append(w_new)
     return losses, hist[-1], hist
 

@@ -1,0 +1,398 @@
+// Memory-bound layers of the worker step: 2x2 max-pool forward/backward
+// ([S] Sec. 3.2, pooling p_l = 2), softmax cross-entropy (the softmax output
+// layer), the explicit im2col of [S] Eq. (5), and the column reduction that
+// forms dE/db (the "dedb" role, m = 1) with the GradBuf accumulate fused.
+#include "common.cuh"
+
+namespace sprint {
+
+// Column sums with the GradBuf epilogue: out[c] = (accumulate ? out[c] : 0) + alpha * sum_r in[r*cols + c].
+// Launched as (ceil(cols/32), chunks) blocks of 32x8 threads. With chunks == 1
+// the epilogue is applied directly; otherwise each chunk writes its partial
+// sum to partial[chunk*cols + c] and colsum_finish adds them in chunk order.
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ in, long long rows, int cols,
+                                                     long long rows_per_chunk, float* __restrict__ partial,
+                                                     float* __restrict__ out, float alpha, int accumulate) {
+    __shared__ float red[8][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + tx;
+    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_chunk;
+    long long r1 = r0 + rows_per_chunk;
+    if (r1 > rows) r1 = rows;
+    float s = 0.f;
+    if (c < cols)
+        for (long long r = r0 + ty; r < r1; r += 8) s += in[r * cols + c];
+    red[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && c < cols) {
+        float t = red[0][tx];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) t += red[k][tx];
+        if (gridDim.y == 1)
+            out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
+        else
+            partial[static_cast<long long>(blockIdx.y) * cols + c] = t;
+    }
+}
+
+__global__ void colsum_finish(const float* __restrict__ partial, int chunks, int cols, float* __restrict__ out,
+                              float alpha, int accumulate) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float t = 0.f;
+    for (int k = 0; k < chunks; ++k) t += partial[static_cast<long long>(k) * cols + c];
+    out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
+}
+
+// Number of chunks colsum uses for `rows` rows (1 means no workspace).
+int colsum_chunks(long long rows, int cols) {
+    if (rows <= 4096) return 1;
+    long long want = rows / 2048;
+    const long long col_blocks = (cols + 31) / 32;
+    const long long cap = (static_cast<long long>(num_sms()) * 8 + col_blocks - 1) / col_blocks;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    return static_cast<int>(want);
+}
+
+// With partial == nullptr the sum runs as one chunk (no workspace).
+int launch_colsum(const float* in, long long rows, int cols, float* partial, float* out, float alpha, int accumulate,
+                  cudaStream_t s) {
+    const int chunks = partial ? colsum_chunks(rows, cols) : 1;
+    const long long per = (rows + chunks - 1) / chunks;
+    dim3 grid((cols + 31) / 32, chunks);
+    colsum_kernel<<<grid, 256, 0, s>>>(in, rows, cols, per, partial, out, alpha, accumulate);
+    if (chunks > 1) colsum_finish<<<(cols + 127) / 128, 128, 0, s>>>(partial, chunks, cols, out, alpha, accumulate);
+    return check_launch("colsum", chunks > 1 ? 2 : 1);
+}
+
+// Strided batched transpose through 32x32 shared-memory tiles, coalesced on
+// both sides: dst[b*db + c*dc + r] = src[b*sb + r*sr + c] for r < R, c < C,
+// b = blockIdx.z. Used for w -> w^T (one batch) and NHWC -> [C][H][W][N]
+// (batch = pixel).
+__global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int R,
+                                                        int C, long long sb, long long sr, long long db, long long dc) {
+    __shared__ float tile[32][33];
+    const long long b = blockIdx.z;
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int r = r0 + j, c = c0 + tx;
+        if (r < R && c < C) tile[j][tx] = src[b * sb + static_cast<long long>(r) * sr + c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int c = c0 + j, r = r0 + tx;
+        if (r < R && c < C) dst[b * db + static_cast<long long>(c) * dc + r] = tile[tx][j];
+    }
+}
+
+int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
+                     long long dc, cudaStream_t s) {
+    if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
+    if (batch > 65535 || (R + 31) / 32 > 65535)
+        return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
+    dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
+    transpose_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc);
+    return check_launch("transpose_kernel");
+}
+
+namespace {
+
+// ------------------------------------------------------------------ pooling
+template <int V>
+__global__ void __launch_bounds__(256) pool_fwd_kernel(const float* __restrict__ x, float* __restrict__ y,
+                                                       uint8_t* __restrict__ arg, int N, int H, int W, int C) {
+    const int Ho = H / 2, Wo = W / 2, Cv = C / V;
+    const long long total = static_cast<long long>(N) * Ho * Wo * Cv;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int cv = static_cast<int>(idx % Cv);
+        long long p = idx / Cv;
+        const int ow = static_cast<int>(p % Wo);
+        p /= Wo;
+        const int oh = static_cast<int>(p % Ho);
+        const long long n = p / Ho;
+        const long long base = ((n * H + 2 * oh) * W + 2 * ow) * C + static_cast<long long>(cv) * V;
+        const long long ob = ((n * Ho + oh) * Wo + ow) * C + static_cast<long long>(cv) * V;
+        const long long off[4] = {0, C, static_cast<long long>(W) * C, static_cast<long long>(W) * C + C};
+        if constexpr (V == 4) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const float4*>(x + base + off[q]);
+            float b[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+            uint8_t a[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int q = 1; q < 4; ++q) {
+                const float e[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int l = 0; l < 4; ++l)
+                    if (e[l] > b[l]) {  // strict: the first maximum in row-major order wins
+                        b[l] = e[l];
+                        a[l] = static_cast<uint8_t>(q);
+                    }
+            }
+            *reinterpret_cast<float4*>(y + ob) = make_float4(b[0], b[1], b[2], b[3]);
+            *reinterpret_cast<uchar4*>(arg + ob) = make_uchar4(a[0], a[1], a[2], a[3]);
+        } else {
+            float b = x[base];
+            uint8_t a = 0;
+#pragma unroll
+            for (int q = 1; q < 4; ++q) {
+                const float e = x[base + off[q]];
+                if (e > b) {
+                    b = e;
+                    a = static_cast<uint8_t>(q);
+                }
+            }
+            y[ob] = b;
+            arg[ob] = a;
+        }
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) pool_bwd_kernel(const float* __restrict__ dy, const uint8_t* __restrict__ arg,
+                                                       const float* __restrict__ pooled, float* __restrict__ dx, int N,
+                                                       int H, int W, int C) {
+    const int Ho = H / 2, Wo = W / 2, Cv = C / V;
+    const long long total = static_cast<long long>(N) * Ho * Wo * Cv;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int cv = static_cast<int>(idx % Cv);
+        long long p = idx / Cv;
+        const int ow = static_cast<int>(p % Wo);
+        p /= Wo;
+        const int oh = static_cast<int>(p % Ho);
+        const long long n = p / Ho;
+        const long long base = ((n * H + 2 * oh) * W + 2 * ow) * C + static_cast<long long>(cv) * V;
+        const long long ob = ((n * Ho + oh) * Wo + ow) * C + static_cast<long long>(cv) * V;
+        const long long off[4] = {0, C, static_cast<long long>(W) * C, static_cast<long long>(W) * C + C};
+        if constexpr (V == 4) {
+            float4 g = *reinterpret_cast<const float4*>(dy + ob);
+            const uchar4 a = *reinterpret_cast<const uchar4*>(arg + ob);
+            if (pooled) {
+                const float4 m = *reinterpret_cast<const float4*>(pooled + ob);
+                g.x = m.x > 0.f ? g.x : 0.f;
+                g.y = m.y > 0.f ? g.y : 0.f;
+                g.z = m.z > 0.f ? g.z : 0.f;
+                g.w = m.w > 0.f ? g.w : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 o;
+                o.x = a.x == q ? g.x : 0.f;
+                o.y = a.y == q ? g.y : 0.f;
+                o.z = a.z == q ? g.z : 0.f;
+                o.w = a.w == q ? g.w : 0.f;
+                *reinterpret_cast<float4*>(dx + base + off[q]) = o;
+            }
+        } else {
+            float g = dy[ob];
+            if (pooled && !(pooled[ob] > 0.f)) g = 0.f;
+            const uint8_t a = arg[ob];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dx[base + off[q]] = (a == q) ? g : 0.f;
+        }
+    }
+}
+
+// zeroes the trailing odd row (H odd) and column (W odd) that the pool ignores
+__global__ void pool_bwd_edges(float* __restrict__ dx, int N, int H, int W, int C) {
+    const long long row_elems = (H & 1) ? static_cast<long long>(W) * C : 0;
+    const long long col_elems = (W & 1) ? static_cast<long long>(H) * C : 0;
+    const long long per_img = row_elems + col_elems;
+    const long long total = per_img * N;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long n = idx / per_img;
+        long long r = idx % per_img;
+        long long off;
+        if (r < row_elems) {
+            off = (n * H + (H - 1)) * static_cast<long long>(W) * C + r;
+        } else {
+            r -= row_elems;
+            const long long h = r / C, c = r % C;
+            off = ((n * H + h) * W + (W - 1)) * static_cast<long long>(C) + c;
+        }
+        dx[off] = 0.f;
+    }
+}
+
+int grid_for(long long work, int threads = 256) {
+    long long g = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(num_sms()) * 16;
+    if (g > cap) g = cap;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+// ------------------------------------------------------------------ softmax
+// One CTA; warp w handles rows w, w+32, ... Per-row losses are added in row
+// order within a warp and the 32 warp sums in warp order, so the loss is
+// deterministic.
+__global__ void __launch_bounds__(1024) softmax_xent_kernel(const float* logits, const int32_t* __restrict__ labels,
+                                                            int N, int C, float* __restrict__ loss, float* dlogits,
+                                                            float scale) {
+    __shared__ float warp_loss[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float acc = 0.f;
+    for (int r = warp; r < N; r += 32) {
+        const float* z = logits + static_cast<long long>(r) * C;
+        float m = -INFINITY;
+        for (int c = lane; c < C; c += 32) m = fmaxf(m, z[c]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float s = 0.f;
+        for (int c = lane; c < C; c += 32) s += expf(z[c] - m);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const int y = labels[r];
+        const float zy = z[y];
+        const float lse = m + logf(s);
+        const float inv = 1.f / s;
+        float* d = dlogits + static_cast<long long>(r) * C;
+        __syncwarp();
+        for (int c = lane; c < C; c += 32) {
+            const float p = expf(z[c] - m) * inv;
+            d[c] = (p - (c == y ? 1.f : 0.f)) * scale;
+        }
+        __syncwarp();
+        acc += lse - zy;
+    }
+    if (lane == 0) warp_loss[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 32; ++w) t += warp_loss[w];
+        *loss = t * scale;
+    }
+}
+
+// ------------------------------------------------------------------ im2col
+template <int V>
+__global__ void __launch_bounds__(256) im2col_kernel(const float* __restrict__ x, int N, int H, int W, int C, int pad,
+                                                     float* __restrict__ col, int32_t* __restrict__ src) {
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const int Kv = 9 * C / V, Cv = C / V;
+    const long long total = static_cast<long long>(N) * Ho * Wo * Kv;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int kv = static_cast<int>(idx % Kv);
+        long long p = idx / Kv;  // output pixel (n, oh, ow)
+        const int ow = static_cast<int>(p % Wo);
+        const long long q = p / Wo;
+        const int oh = static_cast<int>(q % Ho);
+        const long long n = q / Ho;
+        const int tap = kv / Cv, ci = (kv % Cv) * V;
+        const int ih = oh + tap / 3 - pad, iw = ow + tap % 3 - pad;
+        const bool in = ih >= 0 && ih < H && iw >= 0 && iw < W;
+        const long long s0 = ((n * H + ih) * W + iw) * C + ci;
+        const long long d0 = p * 9 * C + static_cast<long long>(tap) * C + ci;
+        if constexpr (V == 4) {
+            const float4 v = in ? *reinterpret_cast<const float4*>(x + s0) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(col + d0) = v;
+            if (src) {
+                const int b = in ? static_cast<int>(s0) : -1;
+                *reinterpret_cast<int4*>(src + d0) = in ? make_int4(b, b + 1, b + 2, b + 3) : make_int4(-1, -1, -1, -1);
+            }
+        } else {
+            col[d0] = in ? x[s0] : 0.f;
+            if (src) src[d0] = in ? static_cast<int32_t>(s0) : -1;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace sprint
+
+using namespace sprint;
+
+extern "C" int sprint_pool_fwd(const float* x, float* y, uint8_t* argmax, int N, int H, int W, int C,
+                               sprint_stream_t stream) {
+    SPRINT_REQUIRE(N >= 1 && H >= 2 && W >= 2 && C >= 1, SPRINT_ERR_SHAPE, "%s: bad shape N=%d H=%d W=%d C=%d", __func__,
+                   N, H, W, C);
+    SPRINT_NONNULL(x, "x");
+    SPRINT_NONNULL(y, "y");
+    SPRINT_NONNULL(argmax, "argmax");
+    SPRINT_ALIGNED(x, "x");
+    SPRINT_ALIGNED(y, "y");
+    SPRINT_ALIGNED(argmax, "argmax");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long outs = static_cast<long long>(N) * (H / 2) * (W / 2) * C;
+    if (C % 4 == 0)
+        pool_fwd_kernel<4><<<grid_for(outs / 4), 256, 0, s>>>(x, y, argmax, N, H, W, C);
+    else
+        pool_fwd_kernel<1><<<grid_for(outs), 256, 0, s>>>(x, y, argmax, N, H, W, C);
+    return check_launch(__func__);
+}
+
+extern "C" int sprint_pool_bwd(const float* dy, const uint8_t* argmax, const float* pooled, float* dx, int N, int H,
+                               int W, int C, sprint_stream_t stream) {
+    SPRINT_REQUIRE(N >= 1 && H >= 2 && W >= 2 && C >= 1, SPRINT_ERR_SHAPE, "%s: bad shape N=%d H=%d W=%d C=%d", __func__,
+                   N, H, W, C);
+    SPRINT_NONNULL(dy, "dy");
+    SPRINT_NONNULL(argmax, "argmax");
+    SPRINT_NONNULL(dx, "dx");
+    SPRINT_ALIGNED(dy, "dy");
+    SPRINT_ALIGNED(argmax, "argmax");
+    SPRINT_ALIGNED(pooled, "pooled");
+    SPRINT_ALIGNED(dx, "dx");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long outs = static_cast<long long>(N) * (H / 2) * (W / 2) * C;
+    if (C % 4 == 0)
+        pool_bwd_kernel<4><<<grid_for(outs / 4), 256, 0, s>>>(dy, argmax, pooled, dx, N, H, W, C);
+    else
+        pool_bwd_kernel<1><<<grid_for(outs), 256, 0, s>>>(dy, argmax, pooled, dx, N, H, W, C);
+    const bool odd = (H & 1) || (W & 1);
+    if (odd) {
+        const long long edge = static_cast<long long>(N) * (((H & 1) ? W : 0) + ((W & 1) ? H : 0)) * C;
+        pool_bwd_edges<<<grid_for(edge), 256, 0, s>>>(dx, N, H, W, C);
+    }
+    return check_launch(__func__, odd ? 2 : 1);
+}
+
+extern "C" int sprint_softmax_xent(const float* logits, const int32_t* labels, int N, int C, float* loss,
+                                   float* dlogits, int reduction_sum, sprint_stream_t stream) {
+    SPRINT_REQUIRE(N >= 1 && C >= 1, SPRINT_ERR_SHAPE, "%s: need N >= 1 and C >= 1 (got %d, %d)", __func__, N, C);
+    SPRINT_NONNULL(logits, "logits");
+    SPRINT_NONNULL(labels, "labels");
+    SPRINT_NONNULL(loss, "loss");
+    SPRINT_NONNULL(dlogits, "dlogits");
+    SPRINT_ALIGNED(logits, "logits");
+    SPRINT_ALIGNED(labels, "labels");
+    SPRINT_ALIGNED(loss, "loss");
+    SPRINT_ALIGNED(dlogits, "dlogits");
+    const float scale = reduction_sum ? 1.f : 1.f / static_cast<float>(N);
+    softmax_xent_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss, dlogits, scale);
+    return check_launch(__func__);
+}
+
+extern "C" int sprint_im2col(const float* x, int N, int H, int W, int C, int pad, float* col, int32_t* src_index,
+                             sprint_stream_t stream) {
+    SPRINT_REQUIRE(N >= 1 && C >= 1 && (pad == 0 || pad == 1) && H + 2 * pad >= 3 && W + 2 * pad >= 3, SPRINT_ERR_SHAPE,
+                   "%s: bad shape N=%d H=%d W=%d C=%d pad=%d", __func__, N, H, W, C, pad);
+    const long long total = static_cast<long long>(N) * (H + 2 * pad - 2) * (W + 2 * pad - 2) * 9 * C;
+    SPRINT_REQUIRE(total < (1ll << 31), SPRINT_ERR_SHAPE, "%s: output has %lld >= 2^31 elements", __func__, total);
+    SPRINT_NONNULL(x, "x");
+    SPRINT_NONNULL(col, "col");
+    SPRINT_ALIGNED(x, "x");
+    SPRINT_ALIGNED(col, "col");
+    SPRINT_ALIGNED(src_index, "src_index");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (C % 4 == 0)
+        im2col_kernel<4><<<grid_for(total / 4), 256, 0, s>>>(x, N, H, W, C, pad, col, src_index);
+    else
+        im2col_kernel<1><<<grid_for(total), 256, 0, s>>>(x, N, H, W, C, pad, col, src_index);
+    return check_launch(__func__);
+}
+
+extern "C" int sprint_transpose(const float* src, float* dst, int rows, int cols, sprint_stream_t stream) {
+    SPRINT_REQUIRE(rows >= 0 && cols >= 0, SPRINT_ERR_SHAPE, "%s: negative size", __func__);
+    if (rows == 0 || cols == 0) return SPRINT_OK;
+    SPRINT_NONNULL(src, "src");
+    SPRINT_NONNULL(dst, "dst");
+    SPRINT_REQUIRE(src != dst, SPRINT_ERR_INVALID_ARG, "%s: src and dst must not alias", __func__);
+    return launch_transpose(src, dst, 1, rows, cols, 0, cols, 0, rows, static_cast<cudaStream_t>(stream));
+}

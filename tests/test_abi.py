@@ -1,0 +1,89 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+function include/sprint.h declares, and its host-side validation returns the
+documented status codes before touching the device."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+
+@pytest.fixture(scope="module")
+def S():
+    from stale_weight_sgd_gb300 import build, sprint
+    build.build()
+    sprint.lib()
+    return sprint
+
+
+def test_exports_every_declared_function(S):
+    names = S.header_functions()
+    assert len(names) >= 20
+    L = S.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding wraps each one under the same name
+    assert not [n for n in names if not hasattr(S, n)]
+
+
+def test_version(S):
+    assert S.sprint_version() == 100
+
+
+@pytest.mark.parametrize("seed,steps,R,Smax", [(0, 7, 1, 0), (1234, 50, 8, 7), (2 ** 63 + 5, 13, 4, 3)])
+def test_schedule_matches_oracle_bit_exact(S, seed, steps, R, Smax):
+    # two independent implementations of the same published generator
+    assert (S.sprint_staleness_schedule(seed, steps, R, Smax) == O.staleness_schedule(seed, steps, R, Smax)).all()
+
+
+P = ctypes.c_void_p
+
+
+def test_update_rejects_bad_arguments(S):
+    L = S.lib()
+    arr = (P * 17)(*([16] * 17))
+    assert L.sprint_apply_update_sgd(16, 16, arr, 17, 100, ctypes.c_float(0.1), None) == 4   # k > 16
+    assert L.sprint_apply_update_sgd(16, 16, arr, 0, 100, ctypes.c_float(0.1), None) == 2    # k < 1
+    assert L.sprint_apply_update_sgd(None, 16, arr, 2, 100, ctypes.c_float(0.1), None) == 1  # NULL w_in
+    assert L.sprint_apply_update_sgd(20, 16, arr, 2, 100, ctypes.c_float(0.1), None) == 3    # misaligned
+    assert L.sprint_apply_update_sgd(16, 16, arr, 2, 0, ctypes.c_float(0.1), None) == 0      # n == 0: no-op
+    assert "aligned" in S.sprint_last_error()   # the message of the last failed call
+    bad = (P * 2)(16, 24)
+    assert L.sprint_apply_update_momentum(16, 16, 16, bad, 2, 10, ctypes.c_float(0.1), ctypes.c_float(0.9), None) == 3
+    assert L.sprint_apply_update_adagrad(16, 16, None, arr, 2, 10, ctypes.c_float(0.1), ctypes.c_float(1e-8), None) == 1
+
+
+def test_shape_and_workspace_errors(S):
+    L = S.lib()
+    assert L.sprint_fc_fwd(16, 16, None, 16, 0, 8, 8, 0, None) == 2
+    assert L.sprint_pool_fwd(16, 16, 16, 1, 1, 4, 4, None) == 2
+    assert L.sprint_softmax_xent(16, 16, 0, 10, 16, 16, 0, None) == 2
+    assert L.sprint_im2col(16, 1, 4, 4, 3, 2, 16, None, None) == 2          # pad 2
+    assert L.sprint_conv_fwd(16, 16, None, 16, 1, 4, 4, 3, 8, 5, 1, None, 0, None) == 2
+    need = S.sprint_fc_workspace_size(64, 256, 512, 0)
+    assert need > 0
+    rc = L.sprint_fc_bwd(16, 16, None, 16, None, 16, 16, None, ctypes.c_float(1), 0, 64, 256, 512, 16, need - 16, None)
+    assert rc == 7 and "workspace" in S.sprint_last_error()
+    assert S.sprint_fc_workspace_size(64, 256, 512, 1) < need       # wT supplied: no transposed copy needed
+    assert S.sprint_conv_workspace_size(2, 8, 16, 16, 64, 64, 1) > 0  # dedw: transposed copies
+    assert S.sprint_conv_workspace_size(9, 8, 16, 16, 64, 64, 1) == 0
+    assert L.sprint_transpose(16, 16, 4, 4, None) == 1               # aliasing
+
+
+def test_binding_raises_with_message(S):
+    with pytest.raises(S.SprintError) as e:
+        S.sprint_apply_update_sgd(16, 16, [16] * 17, 10, 0.1, stream=0)
+    assert "SPRINT_ERR_UNSUPPORTED" in str(e.value)
+
+
+def test_no_cpu_fallback_in_product_path():
+    import os
+    import re
+    root = os.path.join(os.path.dirname(os.path.dirname(__file__)), "stale_weight_sgd_gb300")
+    for dirpath, _, files in os.walk(root):
+        for f in files:
+            if f.endswith(".py"):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), f
+                assert not re.search(r"^\s*(import|from)\s+synth", src, re.M), f

@@ -1,0 +1,280 @@
+"""Kernel-by-kernel parity of the CUDA path (through the C ABI) against the FP64 oracle."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from helpers import TOL_FP32, TOL_TF32, TOL_UPDATE, dev, host, rel_inf
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def S():
+    from stale_weight_sgd_gb300 import sprint
+    sprint.lib()
+    return sprint
+
+
+def _f32(seed, tag, shape, std=1.0):
+    return synth.normal(seed, tag, shape, std)
+
+
+def _status_clean(S):
+    assert S.sprint_device_status(reset=True) == 0
+
+
+# ---------------------------------------------------------------- parameter-server update
+
+@pytest.mark.parametrize("k", [1, 3, 4, 16])
+@pytest.mark.parametrize("n", [0, 1, 7, 1000, 65537])
+@pytest.mark.parametrize("opt", ["sgd", "momentum", "adagrad"])
+def test_update(S, k, n, opt):
+    w = _f32(1, f"w{n}", n, 0.01)
+    bufs = [_f32(1, f"g{j}/{n}", n, 1e-3) for j in range(k)]
+    eta, nu, eps = 0.01, 0.9, 1e-8
+    dw = dev(w)
+    dout = torch.empty_like(dw)
+    dbufs = [dev(b) for b in bufs]
+    if opt == "sgd":
+        S.sprint_apply_update_sgd(dw, dout, dbufs, n, eta)
+        ref = O.update_sgd(w, bufs, eta)
+    elif opt == "momentum":
+        v = _f32(1, f"v{n}", n, 1e-4)
+        dv = dev(v)
+        S.sprint_apply_update_momentum(dw, dout, dv, dbufs, n, eta, nu)
+        ref, vref = O.update_momentum(w, v, bufs, eta, nu)
+        assert rel_inf(host(dv), vref) <= TOL_UPDATE
+    else:
+        G = np.full(n, 0.1, np.float32)
+        dG = dev(G)
+        S.sprint_apply_update_adagrad(dw, dout, dG, dbufs, n, eta, eps)
+        ref, Gref = O.update_adagrad(w, G, bufs, eta, eps)
+        assert rel_inf(host(dG), Gref) <= TOL_UPDATE
+    assert rel_inf(host(dout), ref) <= TOL_UPDATE
+
+
+def test_update_in_place_and_order_invariance_exact(S):
+    n, k = 4099, 8
+    w = synth.dyadic(2, "w", n)
+    bufs = [synth.dyadic(2, f"g{j}", n) for j in range(k)]
+    dw = dev(w)
+    S.sprint_apply_update_sgd(dw, dw, [dev(b) for b in bufs], n, 2.0 ** -3)
+    perm = synth.rng(2, "perm").permutation(k)
+    dw2 = dev(w)
+    S.sprint_apply_update_sgd(dw2, dw2, [dev(bufs[i]) for i in perm], n, 2.0 ** -3)
+    a, b = host(dw), host(dw2)
+    assert (a == b).all()
+    assert (a.astype(np.float64) == O.update_sgd(w, bufs, 2.0 ** -3)).all()
+
+
+@pytest.mark.parametrize("first", [0, 1])
+def test_gradbuf_accumulate(S, first):
+    n = 10003
+    buf = _f32(3, "buf", n)
+    g = _f32(3, "g", n)
+    d = dev(buf)
+    S.sprint_gradbuf_accumulate(d, dev(g), n, -0.01, first)
+    assert rel_inf(host(d), O.gradbuf_accumulate(buf, g, -0.01, bool(first))) <= TOL_UPDATE
+
+
+# ---------------------------------------------------------------- pool / softmax / im2col
+
+@pytest.mark.parametrize("shape", [(2, 8, 6, 8), (3, 7, 5, 3), (1, 4, 4, 16), (2, 2, 2, 5)])
+def test_pool_fwd_bwd_bit_exact(S, shape):
+    N, H, W, C = shape
+    x = _f32(4, f"x{shape}", shape)
+    x[0, 0:2, 0:2, 0] = 0.0       # tie: all-zero window
+    x = np.maximum(x, 0.0)        # pool sees ReLU outputs: many exact zero ties
+    y_ref, a_ref = O.maxpool2x2_fwd(x)
+    dx_ = dev(x)
+    y = torch.empty((N, H // 2, W // 2, C), dtype=torch.float32, device="cuda")
+    a = torch.empty(y.shape, dtype=torch.uint8, device="cuda")
+    S.sprint_pool_fwd(dx_, y, a, N, H, W, C)
+    assert (host(a) == a_ref).all()
+    assert (host(y) == y_ref.astype(np.float32)).all()
+    dy = _f32(4, f"dy{shape}", y.shape)
+    out = torch.full((N, H, W, C), 7.0, dtype=torch.float32, device="cuda")
+    S.sprint_pool_bwd(dev(dy), a, y, out, N, H, W, C)
+    ref = O.maxpool2x2_bwd(dy * (y_ref > 0), a_ref, H, W)
+    assert (host(out) == ref.astype(np.float32)).all()
+
+
+@pytest.mark.parametrize("N,C", [(8, 10), (512, 10), (64, 1000), (33, 7)])
+def test_softmax_xent(S, N, C):
+    z = _f32(5, f"z{N}", (N, C), 3.0)
+    y = synth.labels(5, f"y{N}", N, C)
+    loss_ref, dz_ref = O.softmax_xent(z, y)
+    dz = torch.empty((N, C), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(4, dtype=torch.float32, device="cuda")
+    S.sprint_softmax_xent(dev(z), dev(y), N, C, loss, dz)
+    assert abs(host(loss)[0] - loss_ref) <= 1e-6 * abs(loss_ref)
+    assert rel_inf(host(dz), dz_ref) <= TOL_FP32
+
+
+def test_softmax_uniform_is_ln_c(S):
+    z = np.full((16, 1000), 2.5, np.float32)
+    loss = torch.zeros(4, dtype=torch.float32, device="cuda")
+    dz = torch.empty((16, 1000), dtype=torch.float32, device="cuda")
+    S.sprint_softmax_xent(dev(z), dev(np.arange(16, dtype=np.int32)), 16, 1000, loss, dz)
+    assert abs(host(loss)[0] - np.log(1000.0)) < 1e-5
+
+
+@pytest.mark.parametrize("shape,pad", [((2, 5, 4, 3), 1), ((1, 6, 6, 8), 1), ((2, 4, 5, 4), 0)])
+def test_im2col_bit_exact(S, shape, pad):
+    N, H, W, C = shape
+    x = _f32(6, f"x{shape}", shape)
+    col_ref, src_ref = O.im2col(x, pad)
+    rows = N * (H + 2 * pad - 2) * (W + 2 * pad - 2)
+    col = torch.empty((rows, 9 * C), dtype=torch.float32, device="cuda")
+    src = torch.empty((rows, 9 * C), dtype=torch.int32, device="cuda")
+    S.sprint_im2col(dev(x), N, H, W, C, pad, col, src)
+    assert (host(src) == src_ref).all()
+    assert (host(col) == col_ref).all()
+
+
+# ---------------------------------------------------------------- FC (tcgen05 TF32 and CUDA-core paths)
+
+FC_CASES = [
+    (300, 200, 136),    # tensor cores: ragged M, N and K tiles
+    (512, 320, 384),    # several full tiles, N-tile 128/256
+    (64, 256, 512),     # M below one tile
+    (37, 50, 10),       # CUDA-core path (widths not multiples of 4)
+    (512, 5000, 10),    # classifier of SMLPs
+]
+
+
+@pytest.mark.parametrize("N,fin,fout", FC_CASES)
+@pytest.mark.parametrize("relu", [0, 1])
+def test_fc_fwd(S, N, fin, fout, relu):
+    x = _f32(7, f"x{N}{fin}", (N, fin))
+    w = _f32(7, f"w{fin}{fout}", (fout, fin), np.sqrt(2.0 / fin))
+    b = _f32(7, f"b{fout}", fout, 0.1)
+    ref = O.fc_fwd(x, w, b)
+    if relu:
+        ref = O.relu(ref)
+    y = torch.empty((N, fout), dtype=torch.float32, device="cuda")
+    S.sprint_fc_fwd(dev(x), dev(w), dev(b), y, N, fin, fout, relu)
+    assert rel_inf(host(y), ref) <= TOL_TF32
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("N,fin,fout", FC_CASES)
+@pytest.mark.parametrize("accumulate", [0, 1])
+@pytest.mark.parametrize("with_wT", [0, 1])
+def test_fc_bwd(S, N, fin, fout, accumulate, with_wT):
+    x = np.maximum(_f32(8, f"x{N}{fin}", (N, fin)), 0)   # a ReLU output: mask source
+    w = _f32(8, f"w{fin}{fout}", (fout, fin), np.sqrt(2.0 / fin))
+    dy = _f32(8, f"dy{N}{fout}", (N, fout))
+    dw0 = _f32(8, "dw0", (fout, fin))
+    db0 = _f32(8, "db0", fout)
+    dx_ref, dw_ref, db_ref = O.fc_bwd(x, w, dy)
+    dx_ref = dx_ref * O.relu_mask(x)
+    alpha = 0.5
+    dw_ref = O.gradbuf_accumulate(dw0, dw_ref, alpha, not accumulate)
+    db_ref = O.gradbuf_accumulate(db0, db_ref, alpha, not accumulate)
+    dx = torch.empty((N, fin), dtype=torch.float32, device="cuda")
+    dw = dev(dw0)
+    db = dev(db0)
+    xd = dev(x)
+    wT = dev(np.ascontiguousarray(w.T)) if with_wT else None
+    nb = S.sprint_fc_workspace_size(N, fin, fout, with_wT)
+    ws = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
+    S.sprint_fc_bwd(xd, dev(w), wT, dev(dy), xd, dx, dw, db, alpha, accumulate, N, fin, fout, ws, nb)
+    assert rel_inf(host(dx), dx_ref) <= TOL_TF32
+    assert rel_inf(host(dw), dw_ref) <= TOL_TF32
+    assert rel_inf(host(db), db_ref) <= TOL_FP32
+    _status_clean(S)
+
+
+# ---------------------------------------------------------------- convolution
+
+CONV_CASES = [
+    (2, 8, 8, 32, 64),      # tensor cores, one pixel tile per image pair
+    (3, 10, 6, 64, 32),     # ragged pixel tiles (boxes overhang the image)
+    (2, 16, 16, 32, 128),   # several pixel tiles, N-tile 128
+    (2, 4, 4, 64, 256),     # small spatial, wide channels
+    (2, 6, 5, 3, 16),       # RGB input layer: CUDA-core path
+    (1, 8, 8, 16, 32),      # Cin not a multiple of 32: CUDA-core path
+    (8, 16, 16, 16, 32),    # batch % 4 == 0: tensor-core weight gradient (the tiny CNN's conv2)
+    (4, 8, 8, 32, 64),      # tensor-core weight gradient, W*N = 32 per row
+    (12, 7, 5, 64, 32),     # ragged rows (W*N = 60), Cout < 128
+    (32, 4, 4, 128, 256),   # wide channels, split-K
+]
+
+
+def _conv_inputs(seed, N, H, W, Cin, Cout):
+    x = np.maximum(_f32(seed, f"x{N}{H}{W}{Cin}", (N, H, W, Cin)), 0)
+    w = _f32(seed, f"w{Cin}{Cout}", (Cout, 3, 3, Cin), np.sqrt(2.0 / (9 * Cin)))
+    b = _f32(seed, f"b{Cout}", Cout, 0.1)
+    return x, w, b
+
+
+def _ws(S, op, *shape):
+    n = S.sprint_conv_workspace_size(op, *shape, 1)
+    return (torch.empty(max(n // 4, 1) + 64, dtype=torch.float32, device="cuda"), n)
+
+
+@pytest.mark.parametrize("N,H,W,Cin,Cout", CONV_CASES)
+def test_conv_fwd(S, N, H, W, Cin, Cout):
+    x, w, b = _conv_inputs(9, N, H, W, Cin, Cout)
+    ref = O.relu(O.conv3x3_fwd(x, w, b))
+    y = torch.empty((N, H, W, Cout), dtype=torch.float32, device="cuda")
+    ws, nb = _ws(S, S.SPRINT_CONV_FWD, N, H, W, Cin, Cout)
+    S.sprint_conv_fwd(dev(x), dev(w), dev(b), y, N, H, W, Cin, Cout, 1, 1, ws, nb)
+    assert rel_inf(host(y), ref) <= TOL_TF32
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("N,H,W,Cin,Cout", CONV_CASES)
+def test_conv_dx(S, N, H, W, Cin, Cout):
+    x, w, _ = _conv_inputs(10, N, H, W, Cin, Cout)
+    dy = _f32(10, "dy", (N, H, W, Cout))
+    ref = O.conv3x3_dx(dy, w, H, W) * O.relu_mask(x)
+    dx = torch.full((N, H, W, Cin), 3.0, dtype=torch.float32, device="cuda")
+    ws, nb = _ws(S, S.SPRINT_CONV_DX, N, H, W, Cin, Cout)
+    xd = dev(x)
+    S.sprint_conv_dX(dev(dy), dev(w), None, xd, dx, N, H, W, Cin, Cout, 1, ws, nb)
+    assert rel_inf(host(dx), ref) <= TOL_TF32
+    # with a caller-provided w^T ([3][3][Cin][Cout])
+    wT = np.ascontiguousarray(w.reshape(Cout, 9 * Cin).T)
+    dx.fill_(5.0)
+    S.sprint_conv_dX(dev(dy), dev(w), dev(wT), xd, dx, N, H, W, Cin, Cout, 1, ws, nb)
+    assert rel_inf(host(dx), ref) <= TOL_TF32
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("N,H,W,Cin,Cout", CONV_CASES)
+@pytest.mark.parametrize("accumulate", [0, 1])
+def test_conv_dw(S, N, H, W, Cin, Cout, accumulate):
+    x, _, _ = _conv_inputs(11, N, H, W, Cin, Cout)
+    dy = _f32(11, "dy", (N, H, W, Cout))
+    dw0 = _f32(11, "dw0", (Cout, 3, 3, Cin))
+    db0 = _f32(11, "db0", Cout)
+    dw_ref, db_ref = O.conv3x3_dw(x, dy)
+    dw_ref = O.gradbuf_accumulate(dw0, dw_ref, 1.0, not accumulate)
+    db_ref = O.gradbuf_accumulate(db0, db_ref, 1.0, not accumulate)
+    dw, db = dev(dw0), dev(db0)
+    ws, nb = _ws(S, S.SPRINT_CONV_DW, N, H, W, Cin, Cout)
+    S.sprint_conv_dW(dev(x), dev(dy), dw, db, 1.0, accumulate, N, H, W, Cin, Cout, 1, ws, nb)
+    assert rel_inf(host(dw), dw_ref) <= TOL_TF32
+    assert rel_inf(host(db), db_ref) <= TOL_FP32
+    _status_clean(S)
+
+
+def test_transpose(S):
+    a = _f32(13, "a", (70, 45))
+    out = torch.empty((45, 70), dtype=torch.float32, device="cuda")
+    S.sprint_transpose(dev(a), out, 70, 45)
+    assert (host(out) == a.T).all()
+
+
+def test_conv_pad0(S):
+    N, H, W, Cin, Cout = 2, 9, 10, 32, 32
+    x, w, b = _conv_inputs(12, N, H, W, Cin, Cout)
+    ref = O.conv3x3_fwd(x, w, b, pad=0)
+    y = torch.empty((N, H - 2, W - 2, Cout), dtype=torch.float32, device="cuda")
+    S.sprint_conv_fwd(dev(x), dev(w), dev(b), y, N, H, W, Cin, Cout, 0, 0, None, 0)
+    assert rel_inf(host(y), ref) <= TOL_TF32
