@@ -167,6 +167,30 @@ int sprint_fc_bwd(const float* x, const float* w, const float* wT, const float* 
 /* Workspace bytes sprint_fc_bwd needs (have_wT: whether wT will be passed). */
 size_t sprint_fc_workspace_size(int N, int in, int out, int have_wT);
 
+/* FC backward without any allocation: the same computation and arguments as
+ * sprint_fc_bwd, minus the workspace, which comes from a fixed scratch array
+ * compiled into the library (the pages have no counterpart; this serves
+ * callers that cannot allocate device memory: code under a memory manager
+ * that owns all device memory, or paths that must not call cudaMalloc or
+ * cudaFree because those may synchronise the device).
+ *  - Limit: sprint_fc_bwd_static_scratch_bytes() bytes (24 MiB) per device. A
+ *    shape whose sprint_fc_workspace_size(N, in, out, wT != NULL || dx == NULL)
+ *    exceeds it is rejected with SPRINT_ERR_WORKSPACE before any launch.
+ *  - The array is held by every GPU that loads the library until the process
+ *    exits. The first call on a device looks up the array's device address on
+ *    that device (cudaGetSymbolAddress) and caches it; make that first call
+ *    before any stream capture.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero (each call writes what it reads).
+ *    Calls that overlap on the GPU (e.g. on two streams) race on it. */
+int sprint_fc_bwd_static_scratch(const float* x, const float* w, const float* wT, const float* dy,
+                                 const float* relu_src, float* dx, float* dw, float* db, float alpha, int accumulate,
+                                 int N, int in, int out, sprint_stream_t stream);
+
+/* Size in bytes of the static scratch array sprint_fc_bwd_static_scratch uses. */
+size_t sprint_fc_bwd_static_scratch_bytes(void);
+
 /* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
  * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must
  * not alias. */

@@ -50,6 +50,8 @@ _SIGS = {
     "sprint_fc_fwd": ([P, P, P, P, I, I, I, I, P], I),
     "sprint_fc_bwd": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P, SZ, P], I),
     "sprint_fc_workspace_size": ([I, I, I, I], SZ),
+    "sprint_fc_bwd_static_scratch": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P], I),
+    "sprint_fc_bwd_static_scratch_bytes": ([], SZ),
     "sprint_transpose": ([P, P, I, I, P], I),
     "sprint_pool_fwd": ([P, P, P, I, I, I, I, P], I),
     "sprint_pool_bwd": ([P, P, P, P, I, I, I, I, P], I),
@@ -161,6 +163,16 @@ def sprint_fc_bwd(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, in_,
     return _check("sprint_fc_bwd", lib().sprint_fc_bwd(_p(x), _p(w), _p(wT), _p(dy), _p(relu_src), _p(dx), _p(dw),
                                                        _p(db), float(alpha), int(accumulate), N, in_, out, _p(ws),
                                                        ws_bytes, _s(stream)))
+
+
+def sprint_fc_bwd_static_scratch(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, in_, out, stream=None):
+    return _check("sprint_fc_bwd_static_scratch", lib().sprint_fc_bwd_static_scratch(
+        _p(x), _p(w), _p(wT), _p(dy), _p(relu_src), _p(dx), _p(dw), _p(db), float(alpha), int(accumulate), N, in_, out,
+        _s(stream)))
+
+
+def sprint_fc_bwd_static_scratch_bytes() -> int:
+    return int(lib().sprint_fc_bwd_static_scratch_bytes())
 
 
 def sprint_fc_workspace_size(N, in_, out, have_wT) -> int:
