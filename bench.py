@@ -294,6 +294,105 @@ def cpu_oracle_rate(cfg, budget_s=12.0):
     return done / elapsed, cores, f"{done} images of one replica's forward+backward at full layer sizes ({elapsed:.1f} s)"
 
 
+KERNELS = {
+    # name: description; every case holds well under a few GB on the device
+    "fc_fwd": "FC forward GEMM of an SMLPs hidden layer, 512 x 5000 x 5000 (TF32)",
+    "fc_bwd": "FC backward (dX + dW + db) of an SMLPs hidden layer, 512 x 5000 x 5000, with w^T given",
+    "conv_fwd": "conv forward, VGG conv3_2 shape 56x56x256->256, batch 16 (TF32 implicit GEMM)",
+    "conv_dx": "conv input gradient, VGG conv3_2 shape, batch 16",
+    "conv_dw": "conv weight gradient, VGG conv3_2 shape, batch 16",
+    "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
+    "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
+}
+
+
+def run_kernel(args):
+    """Times one hot kernel at a workload shape with CUDA events (on the
+    launching stream), after warm-up; prints one JSON line."""
+    import torch
+
+    from stale_weight_sgd_gb300 import sprint as S
+    S.lib()
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    rnd = lambda *shape, std=1.0: torch.randn(shape, generator=g, device="cuda") * std
+    k = args.kernel
+    peaks, src = load_peaks()
+    if k.startswith("fc"):
+        M, K, N = 512, 5000, 5000
+        x = rnd(M, K).relu_()
+        w = [rnd(N, K, std=0.02) for _ in range(2)]     # two weight matrices: > L2 between launches
+        wT = [t.t().contiguous() for t in w]
+        y = torch.empty(M, N, device="cuda")
+        dy = rnd(M, N)
+        dx = torch.empty(M, K, device="cuda")
+        dw = torch.empty(N, K, device="cuda")
+        db = torch.empty(N, device="cuda")
+        nb = S.sprint_fc_workspace_size(M, K, N, 1)
+        ws = torch.empty(nb // 4 + 64, device="cuda")
+        if k == "fc_fwd":
+            fn = lambda i: S.sprint_fc_fwd(x, w[i % 2], None, y, M, K, N, 1)
+            work, unit = 2.0 * M * N * K, "TFLOP/s"
+        else:
+            fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
+            work, unit = 4.0 * M * N * K, "TFLOP/s"
+    elif k.startswith("conv"):
+        Nb, H, W, C = 16, 56, 56, 256
+        x = rnd(Nb, H, W, C).relu_()
+        w = rnd(C, 3, 3, C, std=(2.0 / (9 * C)) ** 0.5)
+        wT = w.reshape(C, 9 * C).t().contiguous()
+        b = torch.zeros(C, device="cuda")
+        y = torch.empty(Nb, H, W, C, device="cuda")
+        dy = rnd(Nb, H, W, C)
+        nbytes = max(S.sprint_conv_workspace_size(op, Nb, H, W, C, C, 1) for op in range(3))
+        ws = torch.empty(nbytes // 4 + 64, device="cuda")
+        dwt = torch.empty(C, 3, 3, C, device="cuda")
+        dbt = torch.empty(C, device="cuda")
+        work, unit = 2.0 * Nb * H * W * C * 9 * C, "TFLOP/s"
+        if k == "conv_fwd":
+            fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, C, C, 1, 1, ws, nbytes)
+        elif k == "conv_dx":
+            fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, y, Nb, H, W, C, C, 1, ws, nbytes)
+        else:
+            fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
+    else:
+        n = 16_000_000
+        kb = 16 if k == "update_sgd" else 4
+        wv = rnd(n, std=0.01)
+        bufs = [rnd(n, std=1e-3) for _ in range(kb)]
+        st = torch.zeros(n, device="cuda")
+        if k == "update_sgd":
+            fn = lambda i: S.sprint_apply_update_sgd(wv, wv, bufs, n, 0.01)
+            work = (4.0 * kb + 8) * n
+        else:
+            fn = lambda i: S.sprint_apply_update_momentum(wv, wv, st, bufs, n, 0.01, 0.9)
+            work = (4.0 * kb + 16) * n
+        unit = "GB/s"
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(args.steps):
+        fn(i)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / args.steps
+    achieved = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    if unit == "TFLOP/s":
+        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+        psrc = f"{src}: bf16 burst x 1.1/2.25"
+    else:
+        peak = peaks["hbm_gbs"]
+        psrc = f"{src}: hbm copy"
+    print(json.dumps({"kernel": k, "workload": KERNELS[k], "ms": round(ms, 4), "achieved": round(achieved, 1),
+                      "unit": unit, "peak": round(peak, 1), "frac": round(achieved / peak, 4), "peak_source": psrc,
+                      "flags": S.sprint_device_status()}))
+    return 0
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -318,7 +417,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(CONFIGS), default="smlps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=sorted(KERNELS), default=None,
+                    help="time one hot kernel at a workload shape instead of the training step")
     args = ap.parse_args(argv)
+    if args.kernel:
+        return run_kernel(args)
     cfg = CONFIGS[args.config]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

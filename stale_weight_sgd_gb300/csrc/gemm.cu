@@ -170,11 +170,17 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemm g) {
     const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
     float acc[4][4] = {};
     for (int k0 = 0; k0 < g.K; k0 += 16) {
+        // consecutive threads walk the operand's contiguous dimension (k when
+        // its k-stride is 1, else m / n), so the loads coalesce
         for (int e = threadIdx.x; e < 16 * 64; e += 256) {
-            const int kk = e / 64, mm = e % 64;
-            const int m = m0 + mm, n = n0 + mm, k = k0 + kk;
+            const int kk = g.a_sk == 1 ? e % 16 : e / 64, mm = g.a_sk == 1 ? e / 16 : e % 64;
+            const int m = m0 + mm, k = k0 + kk;
             As[kk][mm] = (m < g.M && k < g.K) ? g.A[m * g.a_sm + k * g.a_sk] : 0.f;
-            Bs[kk][mm] = (n < g.N && k < g.K) ? g.B[n * g.b_sn + k * g.b_sk] : 0.f;
+        }
+        for (int e = threadIdx.x; e < 16 * 64; e += 256) {
+            const int kk = g.b_sk == 1 ? e % 16 : e / 64, nn = g.b_sk == 1 ? e / 16 : e % 64;
+            const int n = n0 + nn, k = k0 + kk;
+            Bs[kk][nn] = (n < g.N && k < g.K) ? g.B[n * g.b_sn + k * g.b_sk] : 0.f;
         }
         __syncthreads();
 #pragma unroll
