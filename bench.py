@@ -165,7 +165,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if "stage_delays" in cfg:
         kw = dict(stage_of_layer=model.VGG_C_STAGES, stage_delays=cfg["stage_delays"], optimizer=cfg["optimizer"],
                   eta=cfg["eta"])
-    tr = StaleSGD(net, N, **kw)
+    tr = StaleSGD(net, N, concurrent=not args.serial_replicas, **kw)
     # synthetic data generated on the device (seeded), weights He-normal
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + rank)
@@ -417,6 +417,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(CONFIGS), default="smlps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial-replicas", action="store_true",
+                    help="run the replicas one after another on one stream instead of concurrently")
     ap.add_argument("--kernel", choices=sorted(KERNELS), default=None,
                     help="time one hot kernel at a workload shape instead of the training step")
     args = ap.parse_args(argv)

@@ -42,7 +42,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // operands instead of truncating the low mantissa bits itself (measured: 3.6x
 // smaller median relative error of the products, no systematic bias).
 bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-               const uint32_t* box) {
+               const uint32_t* box, bool tf32_load = true) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gd[5], gs[4];
@@ -53,7 +53,9 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
         es[i] = 1;
     }
     for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_TFLOAT32, rank, const_cast<void*>(base), gd, gs, bx, es,
+    // loads: TFLOAT32 (round to nearest on the way in); stores: FLOAT32 (bit-exact)
+    CUresult r = fn(m, tf32_load ? CU_TENSOR_MAP_DATA_TYPE_TFLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
+                    const_cast<void*>(base), gd, gs, bx, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -61,7 +63,8 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
 
 // ------------------------------------------------------------------ tcgen05 launches
 template <int ROLE, int BN>
-int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, dim3 grid, cudaStream_t s) {
+int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const TcParams& p,
+                 cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -71,17 +74,26 @@ int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, 
             return check_cuda("cudaFuncSetAttribute(tc_gemm_kernel)");
         attr_done[dev] = true;
     }
-    tc_gemm_kernel<ROLE, BN><<<grid, TC_THREADS, tc_smem_bytes(BN), s>>>(a, b, p);
+    // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
+    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+    tc_gemm_kernel<ROLE, BN><<<grid, TC_THREADS, tc_smem_bytes(BN), s>>>(a, b, d, p);
     return check_launch("tc_gemm_kernel");
 }
 
 template <int ROLE>
-int launch_tc(int bn, const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, dim3 grid, cudaStream_t s) {
-    if (grid.y > 65535 || grid.z > 65535) return fail(SPRINT_ERR_SHAPE, "tc_gemm: grid %u x %u x %u too large", grid.x, grid.y, grid.z);
+int launch_tc(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, TcParams p, long long m_tiles,
+              long long n_tiles, long long z_tiles, cudaStream_t s) {
+    const long long tiles = m_tiles * n_tiles * z_tiles;
+    if (tiles <= 0) return SPRINT_OK;
+    if (tiles > (1ll << 31) - 1) return fail(SPRINT_ERR_SHAPE, "tc_gemm: %lld tiles is too many", tiles);
+    p.m_tiles = static_cast<int>(m_tiles);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.z_tiles = static_cast<int>(z_tiles);
+    p.num_tiles = static_cast<int>(tiles);
     switch (bn) {
-        case 64: return launch_tc_bn<ROLE, 64>(a, b, p, grid, s);
-        case 128: return launch_tc_bn<ROLE, 128>(a, b, p, grid, s);
-        case 256: return launch_tc_bn<ROLE, 256>(a, b, p, grid, s);
+        case 64: return launch_tc_bn<ROLE, 64>(a, b, d, p, s);
+        case 128: return launch_tc_bn<ROLE, 128>(a, b, d, p, s);
+        case 256: return launch_tc_bn<ROLE, 256>(a, b, d, p, s);
         default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", bn);
     }
 }
@@ -449,16 +461,24 @@ bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int
                cudaStream_t s, int* rc) {
     const long long m_tiles = (M + TC_BM - 1) / TC_BM;
     const int bn = pick_bn(m_tiles, N, 1, N >= 256 ? 256 : (N >= 128 ? 128 : 64));
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 4};
     const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)ldb * 4};
     const uint32_t ba[2] = {32, 128}, bb[2] = {32, (uint32_t)bn};
     if (!make_tmap(&ta, A, 2, da, sa, ba) || !make_tmap(&tb, B, 2, db, sb, bb)) return false;
+    // TMA store of D when its row pitch is a multiple of 16 bytes, else direct stores
+    p.store = ST_DIRECT;
+    td = ta;
+    if ((p.ldd & 3) == 0 && aligned16(p.D)) {
+        const uint64_t dd[2] = {(uint64_t)N, (uint64_t)M}, sd[1] = {(uint64_t)p.ldd * 4};
+        const uint32_t bd[2] = {32, 32};
+        if (make_tmap(&td, p.D, 2, dd, sd, bd, false)) p.store = ST_2D;
+    }
     p.M = M;
     p.N = N;
     p.num_kt = (K + TC_BK - 1) / TC_BK;
     p.kt_per_split = p.num_kt;
-    *rc = launch_tc<ROLE_GEMM_2D>(bn, ta, tb, p, dim3(m_tiles, (N + bn - 1) / bn, 1), s);
+    *rc = launch_tc<ROLE_GEMM_2D>(bn, ta, tb, td, p, m_tiles, (N + bn - 1) / bn, 1, s);
     return true;
 }
 
@@ -584,12 +604,22 @@ extern "C" size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Ci
 
 static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, const CUtensorMap* tb,
                         TcParams p, int ncols, cudaStream_t s, bool* done) {
-    CUtensorMap ta;
+    CUtensorMap ta, td;
     const uint64_t da[4] = {(uint64_t)act_c, (uint64_t)act_w, (uint64_t)act_h, (uint64_t)p.img_n};
     const uint64_t sa[3] = {(uint64_t)act_c * 4, (uint64_t)act_w * act_c * 4, (uint64_t)act_h * act_w * act_c * 4};
     const uint32_t ba[4] = {32, (uint32_t)pl.box.bw, (uint32_t)pl.box.bh, (uint32_t)pl.box.bimg};
     *done = false;
     if (!make_tmap(&ta, act, 4, da, sa, ba)) return SPRINT_OK;
+    // the output's 32-row sub-box that one epilogue warp stores (rows are w-fastest pixels)
+    const int sbw = pl.box.bw < 32 ? pl.box.bw : 32;
+    const int sbh = pl.box.bh < 32 / sbw ? pl.box.bh : 32 / sbw;
+    const int sbimg = 32 / (sbw * sbh);
+    const uint64_t dd[4] = {(uint64_t)ncols, (uint64_t)p.out_w, (uint64_t)p.out_h, (uint64_t)p.img_n};
+    const uint64_t sd[3] = {(uint64_t)p.ldd * 4, (uint64_t)p.out_w * p.ldd * 4, (uint64_t)p.out_h * p.out_w * p.ldd * 4};
+    const uint32_t bd[4] = {32, (uint32_t)sbw, (uint32_t)sbh, (uint32_t)sbimg};
+    p.store = ST_DIRECT;
+    td = ta;
+    if ((p.ldd & 3) == 0 && aligned16(p.D) && make_tmap(&td, p.D, 4, dd, sd, bd, false)) p.store = ST_PIX4D;
     p.N = ncols;
     p.num_kt = pl.num_kt;
     p.kt_per_split = pl.num_kt;
@@ -600,7 +630,7 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
     p.tiles_h = pl.box.th;
     p.chunks = pl.num_kt / 9;
     *done = true;
-    return launch_tc<ROLE_CONV_IMPL>(pl.bn, ta, *tb, p, dim3(pl.box.tiles(), (ncols + pl.bn - 1) / pl.bn, 1), s);
+    return launch_tc<ROLE_CONV_IMPL>(pl.bn, ta, *tb, td, p, pl.box.tiles(), (ncols + pl.bn - 1) / pl.bn, 1, s);
 }
 
 extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
@@ -754,8 +784,22 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
             p.alpha = alpha;
             p.accumulate = accumulate;
             p.partial = pl.splits > 1 ? part : nullptr;
-            dim3 grid((Cout + TC_BM - 1) / TC_BM, (Cin + pl.bn - 1) / pl.bn, 9 * pl.splits);
-            if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.bn, ta, tb, p, grid, s))) return rc;
+            CUtensorMap td = ta;
+            p.store = ST_DIRECT;
+            if (pl.splits > 1) {
+                const uint64_t dd[3] = {(uint64_t)Cin, (uint64_t)Cout, (uint64_t)9 * pl.splits};
+                const uint64_t sd[2] = {(uint64_t)Cin * 4, (uint64_t)Cout * Cin * 4};
+                const uint32_t bd[3] = {32, 32, 1};
+                if (aligned16(part) && make_tmap(&td, part, 3, dd, sd, bd, false)) p.store = ST_PARTIAL3D;
+            } else {
+                const uint64_t dd[3] = {(uint64_t)Cin, 9, (uint64_t)Cout};
+                const uint64_t sd[2] = {(uint64_t)Cin * 4, (uint64_t)9 * Cin * 4};
+                const uint32_t bd[3] = {32, 1, 32};
+                if (make_tmap(&td, dw, 3, dd, sd, bd, false)) p.store = ST_WGRAD3D;
+            }
+            if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.bn, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
+                                                 (Cin + pl.bn - 1) / pl.bn, 9ll * pl.splits, s)))
+                return rc;
             if (pl.splits > 1) {
                 dw_split_reduce<<<grid_cap(9ll * Cout * Cin), 256, 0, s>>>(part, pl.splits, Cout, Cin, dw, alpha,
                                                                          accumulate);

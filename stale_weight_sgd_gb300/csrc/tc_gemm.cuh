@@ -1,20 +1,30 @@
 // tcgen05 TF32 GEMM engine for the contractions of the worker step.
 //
-// One CTA computes a 128 x BN tile of D = sum_k A(m,k) * B(n,k) over a range
-// of 32-wide k-tiles (split-K over blockIdx.z where asked):
+// Persistent kernel: gridDim.x CTAs (at most one per SM) walk a static list of
+// 128 x BN output tiles (m fastest, so CTAs running together share the B
+// panel in L2). Within a CTA:
 //   warp 4   : TMA producer (one lane) — fills a STAGES-deep ring of shared-
 //              memory stages, 128 B (32 fp32) wide along k, 128-byte swizzled;
-//   warp 5   : allocates the TMEM accumulator (BN fp32 columns x 128 lanes)
-//              and issues tcgen05.mma.kind::tf32 (M=128, N=BN, K=8) from one
-//              lane; tcgen05.commit frees a stage once its MMAs are done;
+//              the ring runs on across tiles;
+//   warp 5   : allocates two TMEM accumulators (2 x BN fp32 columns) and issues
+//              tcgen05.mma.kind::tf32 (M=128, N=BN, K=8) from one lane, tile
+//              after tile, alternating accumulators; tcgen05.commit frees a
+//              stage once its MMAs are done and hands a finished accumulator
+//              to the epilogue;
 //   warps 0-3: epilogue — tcgen05.ld the accumulator (warp w owns TMEM lanes
-//              32w..32w+31 = tile rows), apply bias/ReLU, the ReLU mask of the
-//              backward pass, or the GradBuf accumulate, and store.
-// Both operands are K-major (k contiguous in shared memory): the TF32 kind of
-// tcgen05.mma reads no MN-major operand on this part, so transposed operands
-// are formed in global memory by the callers (tc dispatch in gemm.cu).
-// Every wait is bounded: one that gives up sets a bit in the device status
-// word and the CTA runs to completion without hanging.
+//              32w..32w+31 = tile rows), release it to the MMA warp, apply
+//              bias/ReLU, the ReLU mask of the backward pass or the GradBuf
+//              scale, stage each 32 x 32 chunk in 128B-swizzled shared memory
+//              and write it with a TMA store (or a TMA add-reduction for the
+//              GradBuf accumulate); ragged edges are clipped by TMA. Outputs TMA
+//              cannot describe (row pitch not a multiple of 16 bytes) are
+//              written by the threads directly instead.
+// So the epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Both operands are K-major: the TF32 kind of tcgen05.mma reads no MN-major
+// operand on this part, so transposed operands are formed in global memory by
+// the callers (gemm.cu). Every wait is bounded: one that gives up sets a bit
+// in the device status word and the CTA finishes without hanging.
 //
 // Roles (the SGEMM roles of the SPRINT report, Sec. 3.3):
 //   GEMM_2D   : A [M][K], B [N][K] row-major (fc, dedx fc with B = w^T,
@@ -35,24 +45,28 @@ namespace sprint {
 
 enum Role : int { ROLE_GEMM_2D = 0, ROLE_CONV_IMPL = 1, ROLE_CONV_WGRAD = 2 };
 enum Epi : int { EPI_STORE = 0, EPI_MASK = 1, EPI_ACCUM = 2 };
+// how the epilogue writes: direct stores, or TMA through a store map of shape
+enum Store : int { ST_DIRECT = 0, ST_2D = 1, ST_PIX4D = 2, ST_WGRAD3D = 3, ST_PARTIAL3D = 4 };
 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 32;                      // fp32 elements per 128-byte swizzle row
 constexpr int TC_THREADS = 192;
 constexpr int TC_A_STAGE = TC_BM * TC_BK * 4;  // 16 KB
+constexpr int TC_STAGING = 4 * 4096;           // one 32 x 32 fp32 staging chunk per epilogue warp
 
 __host__ __device__ constexpr int tc_stages(int bn) { return bn >= 256 ? 4 : (bn >= 128 ? 6 : 8); }
 __host__ __device__ constexpr int tc_b_stage(int bn) { return bn * TC_BK * 4; }
-__host__ __device__ constexpr int tc_tmem_cols(int bn) { return bn <= 32 ? 32 : (bn <= 64 ? 64 : (bn <= 128 ? 128 : 256)); }
+__host__ __device__ constexpr int tc_tmem_cols(int bn) { return bn <= 32 ? 64 : (bn <= 64 ? 128 : (bn <= 128 ? 256 : 512)); }
 __host__ __device__ constexpr int tc_smem_bytes(int bn) {
-    return 1024 /* alignment slack */ + tc_stages(bn) * (TC_A_STAGE + tc_b_stage(bn)) + 256 /* barriers */;
+    return 1024 /* alignment slack */ + tc_stages(bn) * (TC_A_STAGE + tc_b_stage(bn)) + TC_STAGING + 256 /* barriers */;
 }
 
 struct TcParams {
     int M, N;            // GEMM_2D / CONV_WGRAD: output rows, columns; CONV_IMPL: N = columns
+    int m_tiles, n_tiles, z_tiles, num_tiles;  // tile space: m fastest, then n, then z
     int num_kt;          // k-tiles in the full reduction
     int kt_per_split;    // k-tiles per split
-    int splits;          // CONV_WGRAD: blockIdx.z = tap * splits + split
+    int splits;          // CONV_WGRAD: z = tap * splits + split
     // convolution geometry: pixel boxes (bw x bh x bimg) tile the output grid
     int img_n, out_h, out_w, pad;
     int bw, bh, bimg, tiles_w, tiles_h;
@@ -61,6 +75,7 @@ struct TcParams {
     int b_tap_outer;     // CONV_IMPL: B map dims {k, n, 9} (1) or {k, 9, n} (0)
     // epilogue
     int epi;
+    int store;           // Store
     float* D;
     long long ldd;
     const float* bias;   // [N] or null
@@ -75,10 +90,23 @@ struct TcParams {
 
 #if defined(__CUDACC__)
 
+struct TileCoord {
+    int mt, nt, z;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& p) {
+    TileCoord c;
+    c.mt = t % p.m_tiles;
+    const int r = t / p.m_tiles;
+    c.nt = r % p.n_tiles;
+    c.z = r / p.n_tiles;
+    return c;
+}
+
 template <int ROLE, int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmD, const TcParams p) {
     constexpr int STAGES = tc_stages(BN);
     constexpr int B_STAGE = tc_b_stage(BN);
     constexpr uint32_t IDESC = idesc_tf32(BN, false, false);
@@ -91,44 +119,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * TC_A_STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+    uint8_t* sStage = sB + STAGES * B_STAGE;   // 4 x 4 KB epilogue staging, 1024-aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(sStage + TC_STAGING);
     uint64_t* empty = full + STAGES;
-    uint64_t* accum_full = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_full + 1);
+    uint64_t* tmem_full = empty + STAGES;     // [2]
+    uint64_t* tmem_empty = tmem_full + 2;     // [2]
+    uint64_t* mma_done = tmem_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    int split = blockIdx.z, tap = 0;
-    if constexpr (ROLE == ROLE_CONV_WGRAD) {
-        tap = blockIdx.z / p.splits;
-        split = blockIdx.z % p.splits;
-    }
-    const int kt_begin = split * p.kt_per_split;
-    int kt_end = kt_begin + p.kt_per_split;
-    if (kt_end > p.num_kt) kt_end = p.num_kt;
-    const int nkt = kt_end > kt_begin ? kt_end - kt_begin : 0;
-    const int n0 = blockIdx.y * BN;
-    const int m0 = blockIdx.x * TC_BM;
-
-    // CONV_IMPL: the 128 output pixels of this tile
-    int pw0 = 0, ph0 = 0, pn0 = 0;
-    if constexpr (ROLE == ROLE_CONV_IMPL) {
-        const int mt = blockIdx.x;
-        pw0 = (mt % p.tiles_w) * p.bw;
-        ph0 = ((mt / p.tiles_w) % p.tiles_h) * p.bh;
-        pn0 = (mt / (p.tiles_w * p.tiles_h)) * p.bimg;
-    }
 
     if (warp == 4 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], 4);   // one arrival per epilogue warp
+        }
+        mbar_init(mma_done, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.store != ST_DIRECT) tma_prefetch_desc(&tmD);
     }
     if (warp == 5) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -137,172 +152,279 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = *tmem_slot;
+    const uint32_t tmem_base = *tmem_slot;
+
+    // per-tile k range (split-K over z for the weight gradient)
+    auto k_range = [&](const TileCoord& tc, int& kt0, int& nkt, int& tap) {
+        int split = tc.z;
+        tap = 0;
+        if constexpr (ROLE == ROLE_CONV_WGRAD) {
+            tap = tc.z / p.splits;
+            split = tc.z % p.splits;
+        }
+        kt0 = split * p.kt_per_split;
+        int kt1 = kt0 + p.kt_per_split;
+        if (kt1 > p.num_kt) kt1 = p.num_kt;
+        nkt = kt1 > kt0 ? kt1 - kt0 : 0;
+    };
 
     if (warp == 4) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            for (int i = 0; i < nkt; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) break;
-                const int kt = kt_begin + i;
-                uint8_t* a_dst = sA + s * TC_A_STAGE;
-                uint8_t* b_dst = sB + s * B_STAGE;
-                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                if constexpr (ROLE == ROLE_GEMM_2D) {
-                    tma_load_2d(a_dst, &tmA, kt * TC_BK, m0, &full[s]);
-                    tma_load_2d(b_dst, &tmB, kt * TC_BK, n0, &full[s]);
-                } else if constexpr (ROLE == ROLE_CONV_IMPL) {
-                    const int t = kt / p.chunks;
-                    const int c0 = (kt % p.chunks) * TC_BK;
-                    const int dh = (t / 3 - p.pad) * p.tap_sign, dw = (t % 3 - p.pad) * p.tap_sign;
-                    tma_load_4d(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
-                    if (p.b_tap_outer)
-                        tma_load_3d(b_dst, &tmB, c0, n0, t, &full[s]);
-                    else
-                        tma_load_3d(b_dst, &tmB, c0, t, n0, &full[s]);
-                } else {  // CONV_WGRAD: k-tile = 32 consecutive (w, n) of one output row h
-                    // dy^T viewed as {Wo*N, Ho, Cout}, x^T as {W*N, H, Cin}: a tap shifts x by
-                    // (kw - pad)*N along the inner dimension and by kh - pad rows; positions
-                    // outside the image fall outside the tensor and are zero-filled.
-                    const int h = kt / p.tiles_w;
-                    const int c0 = (kt % p.tiles_w) * TC_BK;
-                    tma_load_3d(a_dst, &tmA, c0, h, m0, &full[s]);
-                    tma_load_3d(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0, &full[s]);
+            uint32_t it = 0;
+            bool alive = true;
+            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
+                const TileCoord tc = tile_coord(t, p);
+                int kt0, nkt, tap;
+                k_range(tc, kt0, nkt, tap);
+                const int n0 = tc.nt * BN, m0 = tc.mt * TC_BM;
+                int pw0 = 0, ph0 = 0, pn0 = 0;
+                if constexpr (ROLE == ROLE_CONV_IMPL) {
+                    pw0 = (tc.mt % p.tiles_w) * p.bw;
+                    ph0 = ((tc.mt / p.tiles_w) % p.tiles_h) * p.bh;
+                    pn0 = (tc.mt / (p.tiles_w * p.tiles_h)) * p.bimg;
+                }
+                for (int i = 0; i < nkt; ++i, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) {
+                        alive = false;
+                        break;
+                    }
+                    const int kt = kt0 + i;
+                    uint8_t* a_dst = sA + s * TC_A_STAGE;
+                    uint8_t* b_dst = sB + s * B_STAGE;
+                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    if constexpr (ROLE == ROLE_GEMM_2D) {
+                        tma_load_2d(a_dst, &tmA, kt * TC_BK, m0, &full[s]);
+                        tma_load_2d(b_dst, &tmB, kt * TC_BK, n0, &full[s]);
+                    } else if constexpr (ROLE == ROLE_CONV_IMPL) {
+                        const int tp = kt / p.chunks;
+                        const int c0 = (kt % p.chunks) * TC_BK;
+                        const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
+                        tma_load_4d(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
+                        if (p.b_tap_outer)
+                            tma_load_3d(b_dst, &tmB, c0, n0, tp, &full[s]);
+                        else
+                            tma_load_3d(b_dst, &tmB, c0, tp, n0, &full[s]);
+                    } else {  // CONV_WGRAD: dy^T {Wo*N, Ho, Cout}, x^T {W*N, H, Cin}
+                        const int h = kt / p.tiles_w;
+                        const int c0 = (kt % p.tiles_w) * TC_BK;
+                        tma_load_3d(a_dst, &tmA, c0, h, m0, &full[s]);
+                        tma_load_3d(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
+                                    &full[s]);
+                    }
                 }
             }
         }
     } else if (warp == 5) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            for (int i = 0; i < nkt; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (!mbar_wait_bounded(&full[s], ph, p.status, DEV_FLAG_WAIT_MMA)) break;
+            uint32_t it = 0, j = 0;
+            bool alive = true;
+            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x, ++j) {
+                const TileCoord tc = tile_coord(t, p);
+                int kt0, nkt, tap;
+                k_range(tc, kt0, nkt, tap);
+                const uint32_t b = j & 1, tph = (j >> 1) & 1;
+                if (!mbar_wait_bounded(&tmem_empty[b], tph ^ 1, p.status, DEV_FLAG_WAIT_MMA)) break;
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(sA + s * TC_A_STAGE);
-                const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int i = 0; i < nkt; ++i, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait_bounded(&full[s], ph, p.status, DEV_FLAG_WAIT_MMA)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + s * TC_A_STAGE);
+                    const uint32_t b_base = smem_u32(sB + s * B_STAGE);
 #pragma unroll
-                for (int kk = 0; kk < TC_BK / 8; ++kk) {
-                    // K-major, 128-byte swizzle: 8 rows of 128 B per 1024-byte group (SBO);
-                    // each K=8 step advances 32 bytes inside the swizzled row.
-                    const uint64_t da = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                    const uint64_t db = smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                    mma_tf32(tmem_d, da, db, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < TC_BK / 8; ++kk) {
+                        // K-major, 128-byte swizzle: 8 rows of 128 B per 1024-byte group (SBO);
+                        // each K=8 step advances 32 bytes inside the swizzled row.
+                        const uint64_t da = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t db = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                        mma_tf32(d_tmem, da, db, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&tmem_full[b]);
             }
-            mma_commit(accum_full);
+            // every MMA issued above has completed once this commit arrives
+            mma_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, p.status, DEV_FLAG_WAIT_MMA);
         }
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- epilogue (warps 0-3)
-        const bool ok = mbar_wait_bounded(accum_full, 0, p.status, DEV_FLAG_WAIT_EPILOGUE);
-        tc_fence_after();
-        const int r = warp * 32 + lane;  // tile row = TMEM lane
-        long long row_off = -1, mask_off = -1, part_off = -1;
-        if constexpr (ROLE == ROLE_CONV_IMPL) {
-            const int ow = pw0 + r % p.bw;
-            const int oh = ph0 + (r / p.bw) % p.bh;
-            const int on = pn0 + r / (p.bw * p.bh);
-            if (ow < p.out_w && oh < p.out_h && on < p.img_n) {
-                const long long pix = (static_cast<long long>(on) * p.out_h + oh) * p.out_w + ow;
-                row_off = pix * p.ldd;
-                mask_off = pix * p.ldm;
+        uint8_t* stage = sStage + warp * 4096;
+        bool pending = false;     // a TMA store of this warp may still read `stage`
+        uint32_t j = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++j) {
+            const TileCoord tc = tile_coord(t, p);
+            int kt0, nkt, tap;
+            k_range(tc, kt0, nkt, tap);
+            const uint32_t b = j & 1, tph = (j >> 1) & 1;
+            if (!mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE)) break;
+            tc_fence_after();
+            const int n0 = tc.nt * BN, m0 = tc.mt * TC_BM;
+            const int r = warp * 32 + lane;  // tile row = TMEM lane
+            // output row of this thread (direct stores, mask loads); -1 if outside
+            long long row_off = -1, mask_off = -1;
+            int pw0 = 0, ph0 = 0, pn0 = 0;
+            if constexpr (ROLE == ROLE_CONV_IMPL) {
+                pw0 = (tc.mt % p.tiles_w) * p.bw;
+                ph0 = ((tc.mt / p.tiles_w) % p.tiles_h) * p.bh;
+                pn0 = (tc.mt / (p.tiles_w * p.tiles_h)) * p.bimg;
+                const int ow = pw0 + r % p.bw;
+                const int oh = ph0 + (r / p.bw) % p.bh;
+                const int on = pn0 + r / (p.bw * p.bh);
+                if (ow < p.out_w && oh < p.out_h && on < p.img_n) {
+                    const long long pix = (static_cast<long long>(on) * p.out_h + oh) * p.out_w + ow;
+                    row_off = pix * p.ldd;
+                    mask_off = pix * p.ldm;
+                }
+            } else {
+                const int m = m0 + r;
+                if (m < p.M) {
+                    row_off = static_cast<long long>(m) * p.ldd;
+                    mask_off = static_cast<long long>(m) * p.ldm;
+                }
             }
-        } else {
-            const int m = m0 + r;
-            if (m < p.M) {
-                row_off = static_cast<long long>(m) * p.ldd;
-                mask_off = static_cast<long long>(m) * p.ldm;
-                if (p.partial) part_off = (static_cast<long long>(blockIdx.z) * p.M + m) * p.N;
-            }
-        }
-        long long col_shift = 0;
-        if constexpr (ROLE == ROLE_CONV_WGRAD) col_shift = static_cast<long long>(tap) * p.N;
+            const bool to_partial = p.partial != nullptr;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem_d + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
-            tmem_wait_ld();
-            const int ncol0 = n0 + c;
-            if (!ok || row_off < 0 || nkt == 0 || ncol0 >= p.N) continue;
-            const bool full4 = (ncol0 + 32 <= p.N);
-            if (part_off >= 0) {
-                float* dst = p.partial + part_off + ncol0;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    if (full4) {
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                                          __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (ncol0 + j + q < p.N) dst[j + q] = __uint_as_float(v[j + q]);
-                    }
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + b * BN + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+                tmem_wait_ld();
+                if (c + 32 >= BN) {  // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tmem_empty[b]);
                 }
-                continue;
-            }
-            float* dst = p.D + row_off + col_shift + ncol0;
+                const int ncol0 = n0 + c;
+                if (ncol0 >= p.N) continue;  // whole chunk outside the output (warp-uniform)
+                float o[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float o[4];
+                for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(v[q]);
+                if (!to_partial) {
+                    if (p.epi == EPI_STORE) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = __uint_as_float(v[j + q]);
-                if (p.epi == EPI_STORE) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float t = o[q];
-                        if (p.bias && ncol0 + j + q < p.N) t += p.bias[ncol0 + j + q];
-                        if (p.relu) t = fmaxf(t, 0.f);
-                        o[q] = t;
-                    }
-                } else if (p.epi == EPI_MASK) {
-                    if (p.mask) {
-                        const float* ms = p.mask + mask_off + ncol0 + j;
-                        if (full4) {
-                            const float4 mv = *reinterpret_cast<const float4*>(ms);
-                            o[0] = mv.x > 0.f ? o[0] : 0.f;
-                            o[1] = mv.y > 0.f ? o[1] : 0.f;
-                            o[2] = mv.z > 0.f ? o[2] : 0.f;
-                            o[3] = mv.w > 0.f ? o[3] : 0.f;
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (ncol0 + j + q < p.N) o[q] = ms[q] > 0.f ? o[q] : 0.f;
+                        for (int q = 0; q < 32; ++q) {
+                            float x = o[q];
+                            if (p.bias && ncol0 + q < p.N) x += p.bias[ncol0 + q];
+                            if (p.relu) x = fmaxf(x, 0.f);
+                            o[q] = x;
                         }
-                    }
-                } else {  // EPI_ACCUM: GradBuf <- (accumulate ? GradBuf : 0) + alpha * acc
-                    if (full4) {
-                        float4 prev = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.accumulate) prev = *reinterpret_cast<const float4*>(dst + j);
-                        o[0] = prev.x + p.alpha * o[0];
-                        o[1] = prev.y + p.alpha * o[1];
-                        o[2] = prev.z + p.alpha * o[2];
-                        o[3] = prev.w + p.alpha * o[3];
+                    } else if (p.epi == EPI_MASK) {
+                        if (p.mask && mask_off >= 0) {
+                            const float* ms = p.mask + mask_off + ncol0;
+                            if (ncol0 + 32 <= p.N && (p.ldm & 3) == 0) {
+#pragma unroll
+                                for (int q = 0; q < 32; q += 4) {
+                                    const float4 mv = *reinterpret_cast<const float4*>(ms + q);
+                                    o[q] = mv.x > 0.f ? o[q] : 0.f;
+                                    o[q + 1] = mv.y > 0.f ? o[q + 1] : 0.f;
+                                    o[q + 2] = mv.z > 0.f ? o[q + 2] : 0.f;
+                                    o[q + 3] = mv.w > 0.f ? o[q + 3] : 0.f;
+                                }
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 32; ++q)
+                                    if (ncol0 + q < p.N) o[q] = ms[q] > 0.f ? o[q] : 0.f;
+                            }
+                        }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (ncol0 + j + q < p.N) o[q] = (p.accumulate ? dst[j + q] : 0.f) + p.alpha * o[q];
+                        for (int q = 0; q < 32; ++q) o[q] *= p.alpha;
                     }
                 }
-                if (full4) {
-                    *reinterpret_cast<float4*>(dst + j) = make_float4(o[0], o[1], o[2], o[3]);
+                if (p.store != ST_DIRECT) {
+                    // stage the 32 x 32 chunk (128B-swizzled rows) and hand it to TMA
+                    if (pending) {
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float4* dst = reinterpret_cast<float4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4));
+                        *dst = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    // a box whose origin lies past the output (all 32 rows outside) is not issued
+                    bool inside;
+                    if constexpr (ROLE == ROLE_CONV_IMPL) {
+                        const int row0 = warp * 32;
+                        inside = pw0 + row0 % p.bw < p.out_w && ph0 + (row0 / p.bw) % p.bh < p.out_h &&
+                                 pn0 + row0 / (p.bw * p.bh) < p.img_n;
+                    } else {
+                        inside = m0 + warp * 32 < p.M;
+                    }
+                    if (lane == 0 && inside) {
+                        const bool add = (p.epi == EPI_ACCUM) && p.accumulate && !to_partial;
+                        if (p.store == ST_2D) {
+                            if (add)
+                                tma_reduce_add_2d(&tmD, ncol0, m0 + warp * 32, stage);
+                            else
+                                tma_store_2d(&tmD, ncol0, m0 + warp * 32, stage);
+                        } else if (p.store == ST_PIX4D) {
+                            const int row0 = warp * 32;
+                            const int wo = row0 % p.bw, ho = (row0 / p.bw) % p.bh, no = row0 / (p.bw * p.bh);
+                            tma_store_4d(&tmD, ncol0, pw0 + wo, ph0 + ho, pn0 + no, stage);
+                        } else if (p.store == ST_WGRAD3D) {
+                            if (add)
+                                tma_reduce_add_3d(&tmD, ncol0, tap, m0 + warp * 32, stage);
+                            else
+                                tma_store_3d(&tmD, ncol0, tap, m0 + warp * 32, stage);
+                        } else {  // ST_PARTIAL3D
+                            tma_store_3d(&tmD, ncol0, m0 + warp * 32, tc.z, stage);
+                        }
+                        bulk_commit();
+                    }
+                    pending = true;
+                    continue;
+                }
+                // direct stores (outputs TMA cannot describe)
+                if (row_off < 0) continue;
+                if (to_partial) {
+                    float* dst = p.partial + (static_cast<long long>(tc.z) * p.M + (m0 + r)) * p.N + ncol0;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (ncol0 + q < p.N) dst[q] = o[q];
+                    continue;
+                }
+                long long col_shift = 0;
+                if constexpr (ROLE == ROLE_CONV_WGRAD) col_shift = static_cast<long long>(tap) * p.N;
+                float* dst = p.D + row_off + col_shift + ncol0;
+                const bool vec = (ncol0 + 32 <= p.N) && (p.ldd & 3) == 0;
+                if (p.epi == EPI_ACCUM && p.accumulate) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (ncol0 + q < p.N) o[q] += dst[q];
+                }
+                if (vec) {
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(dst + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (ncol0 + j + q < p.N) dst[j + q] = o[q];
+                    for (int q = 0; q < 32; ++q)
+                        if (ncol0 + q < p.N) dst[q] = o[q];
                 }
             }
         }
+        if (lane == 0) bulk_wait0();   // every TMA store of this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem_d, TMEM_COLS);
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
