@@ -191,8 +191,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(tr.main_stream)
+    host_t0 = time.perf_counter()
     for _ in range(args.steps):
         tr.step()
+    host_issue_ms = (time.perf_counter() - host_t0) * 1e3 / args.steps
     end.record(tr.main_stream)
     torch.cuda.synchronize()
     probe.active = False
@@ -211,21 +213,30 @@ def run_ours(args, cfg, rank, world, local_rank):
     dx = torch.empty((R, N, feat), dtype=torch.float32, device=dev)
     dy = torch.empty((R, N), dtype=torch.int32, device=dev)
     tr.set_batch_pool(dx, dy)
-    hloss = torch.empty((R,), dtype=torch.float32).pin_memory()
+    hloss = torch.empty(tuple(tr.loss.shape), dtype=torch.float32).pin_memory()
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
+    ph = {"h2d": 0.0, "step": 0.0, "d2h_sync": 0.0}
     for _ in range(args.steps):
         main = tr.main_stream
+        e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
         tr.main_stream.wait_event(tr.ev_update)
+        e0.record(main)
         with torch.cuda.stream(main):
             dx.copy_(hx, non_blocking=True)
             dy.copy_(hy, non_blocking=True)
+        e1.record(main)
         tr.ev_update.record(main)
         tr.step()
+        e2.record(main)
         with torch.cuda.stream(main):
-            hloss.copy_(tr.loss[:, 0], non_blocking=True)
+            hloss.copy_(tr.loss, non_blocking=True)   # contiguous [R][4]; column 0 = replica loss
+        e3.record(main)
         main.synchronize()
+        ph["h2d"] += e0.elapsed_time(e1)
+        ph["step"] += e1.elapsed_time(e2)
+        ph["d2h_sync"] += e2.elapsed_time(e3)
     e2e_s = time.perf_counter() - t0
     e2e_s = allreduce_max(e2e_s, world)
 
@@ -254,13 +265,15 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "parallelism": f"replicas only x{world}" if world > 1 else "1 GPU",
                    "l2": "working set (weights, 4 GradBufs) far larger than L2; no flush needed"},
         "e2e": {"value": round(e2e_value, 1), "unit": "images/s",
-                "h2d_bytes_per_step": int(hx.numel() * 4 + hy.numel() * 4), "d2h_bytes_per_step": int(R * 4)},
+                "h2d_bytes_per_step": int(hx.numel() * 4 + hy.numel() * 4), "d2h_bytes_per_step": int(hloss.numel() * 4),
+                "phase_ms_per_step": {k: round(v / args.steps, 3) for k, v in ph.items()}},
         "gpu_launches": int(launches),
         "roofline": roof,
         "achieved_step_tflops": round(flops_step * args.steps / (ms_max / 1e3) / 1e12 * world, 1),
         "clocks": clk,
         "loss_last": loss,
         "kernels_per_step": int(launches // args.steps),
+        "host_issue_ms_per_step": round(host_issue_ms, 3),
     }
     return out
 

@@ -239,6 +239,62 @@ int launch_simt_gemm(const SimtGemm& g, cudaStream_t s) {
     return check_launch("simt_gemm_kernel");
 }
 
+// Skinny product for few output columns (N <= 16), both operands k-contiguous:
+// D[m][n] = act(bias[n] + sum_k A[m*lda + k] * B[n*ldb + k]). Two rows per
+// block; the 256 threads split k, keep every partial sum in registers, and
+// reduce in a fixed order (warp shuffles, then the 8 warps in order).
+constexpr int kSkinnyN = 16;
+__global__ void __launch_bounds__(256) skinny_nt_kernel(const float* __restrict__ A, long long lda,
+                                                        const float* __restrict__ B, long long ldb,
+                                                        const float* __restrict__ bias, float* __restrict__ D,
+                                                        long long ldd, int M, int N, int K, int relu) {
+    __shared__ float red[8][2][kSkinnyN];
+    const int m0 = blockIdx.x * 2;
+    const bool two = m0 + 1 < M;
+    const float* a0 = A + static_cast<long long>(m0) * lda;
+    const float* a1 = A + static_cast<long long>(two ? m0 + 1 : m0) * lda;
+    float acc0[kSkinnyN], acc1[kSkinnyN];
+#pragma unroll
+    for (int n = 0; n < kSkinnyN; ++n) acc0[n] = acc1[n] = 0.f;
+    for (int k = threadIdx.x; k < K; k += 256) {
+        const float x0 = a0[k], x1 = a1[k];
+#pragma unroll
+        for (int n = 0; n < kSkinnyN; ++n) {
+            if (n < N) {
+                const float w = B[static_cast<long long>(n) * ldb + k];
+                acc0[n] = fmaf(x0, w, acc0[n]);
+                acc1[n] = fmaf(x1, w, acc1[n]);
+            }
+        }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int n = 0; n < kSkinnyN; ++n) {
+        float u = acc0[n], v = acc1[n];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            u += __shfl_xor_sync(0xffffffffu, u, o);
+            v += __shfl_xor_sync(0xffffffffu, v, o);
+        }
+        if (lane == 0) {
+            red[warp][0][n] = u;
+            red[warp][1][n] = v;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * kSkinnyN) {
+        const int r = threadIdx.x / kSkinnyN, n = threadIdx.x % kSkinnyN;
+        if (n < N && (r == 0 || two)) {
+            float t = red[0][r][n];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) t += red[w][r][n];
+            if (bias) t += bias[n];
+            if (relu) t = fmaxf(t, 0.f);
+            D[static_cast<long long>(m0 + r) * ldd + n] = t;
+        }
+    }
+}
+
 // direct convolution, one thread per output element (co fastest)
 __global__ void __launch_bounds__(256) simt_conv_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ b, float* __restrict__ y, int N,
@@ -426,7 +482,8 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     pl.box = PixBox{0, 0, 0, static_cast<int>((static_cast<long long>(Wo) * N + TC_BK - 1) / TC_BK), Ho, 1};
     pl.num_kt = pl.box.tw * Ho;   // per output row: ceil(Wo*N / 32) k-tiles
     const long long m_tiles = (Cout + TC_BM - 1) / TC_BM;
-    pl.bn = pick_bn(m_tiles, Cin, 9, Cin >= 256 ? 256 : (Cin >= 128 ? 128 : 64));
+    // split-K below fills the machine, so the widest tile (best MMA shape) is used
+    pl.bn = Cin > 128 ? 256 : (Cin > 64 ? 128 : 64);
     const long long base = m_tiles * ((Cin + pl.bn - 1) / pl.bn) * 9;
     long long want = (2ll * num_sms() + base - 1) / base;
     long long maxs = pl.num_kt / 8;
@@ -515,6 +572,10 @@ extern "C" int sprint_fc_fwd(const float* x, const float* w, const float* b, flo
         p.relu = relu;
         int rc = SPRINT_OK;
         if (gemm2d_tc(x, in, w, in, N, out, in, p, s, &rc)) return rc;
+    }
+    if (out <= kSkinnyN) {
+        skinny_nt_kernel<<<(N + 1) / 2, 256, 0, s>>>(x, in, w, in, b, y, out, N, out, in, relu);
+        return check_launch("skinny_nt_kernel");
     }
     SimtGemm g{N, out, in, x, in, 1, w, in, 1, y, out, b, nullptr, 0, 1.f, 0, relu, SIMT_STORE};
     return launch_simt_gemm(g, s);

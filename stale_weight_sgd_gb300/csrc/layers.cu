@@ -44,13 +44,67 @@ __global__ void colsum_finish(const float* __restrict__ partial, int chunks, int
     out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
 }
 
+// Column sums for cols % 4 == 0: a block of 32 x 32 threads covers 128 columns
+// (tx: a float4 of 4 columns) and one chunk of rows (ty: every 32nd row, four
+// independent loads in flight per thread); the 32 row stripes are then added
+// in stripe order. Same epilogue / partial convention as colsum_kernel.
+__global__ void __launch_bounds__(1024) colsum4_kernel(const float* __restrict__ in, long long rows, int cols,
+                                                       long long rows_per_chunk, float* __restrict__ partial,
+                                                       float* __restrict__ out, float alpha, int accumulate) {
+    __shared__ float4 red[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int col = (blockIdx.x * 32 + tx) * 4;
+    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_chunk;
+    long long r1 = r0 + rows_per_chunk;
+    if (r1 > rows) r1 = rows;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
+    if (col < cols) {
+        const float* base = in + col;
+        long long r = r0 + ty;
+        for (; r + 96 < r1; r += 128) {
+            const float4 a = *reinterpret_cast<const float4*>(base + r * cols);
+            const float4 b = *reinterpret_cast<const float4*>(base + (r + 32) * cols);
+            const float4 c = *reinterpret_cast<const float4*>(base + (r + 64) * cols);
+            const float4 d = *reinterpret_cast<const float4*>(base + (r + 96) * cols);
+            s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+            s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
+            s2.x += c.x; s2.y += c.y; s2.z += c.z; s2.w += c.w;
+            s3.x += d.x; s3.y += d.y; s3.z += d.z; s3.w += d.w;
+        }
+        for (; r < r1; r += 32) {
+            const float4 a = *reinterpret_cast<const float4*>(base + r * cols);
+            s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+        }
+    }
+    red[ty][tx] = make_float4(s0.x + s1.x + s2.x + s3.x, s0.y + s1.y + s2.y + s3.y, s0.z + s1.z + s2.z + s3.z,
+                              s0.w + s1.w + s2.w + s3.w);
+    __syncthreads();
+    if (ty == 0 && col < cols) {
+        float4 t = red[0][tx];
+        for (int k = 1; k < 32; ++k) {
+            const float4 u = red[k][tx];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        if (gridDim.y == 1) {
+            float4 o = make_float4(alpha * t.x, alpha * t.y, alpha * t.z, alpha * t.w);
+            if (accumulate) {
+                const float4 prev = *reinterpret_cast<const float4*>(out + col);
+                o.x += prev.x; o.y += prev.y; o.z += prev.z; o.w += prev.w;
+            }
+            *reinterpret_cast<float4*>(out + col) = o;
+        } else {
+            *reinterpret_cast<float4*>(partial + static_cast<long long>(blockIdx.y) * cols + col) = t;
+        }
+    }
+}
+
 // Number of chunks colsum uses for `rows` rows (1 means no workspace).
 int colsum_chunks(long long rows, int cols) {
-    if (rows <= 4096) return 1;
-    long long want = rows / 2048;
-    const long long col_blocks = (cols + 31) / 32;
-    const long long cap = (static_cast<long long>(num_sms()) * 8 + col_blocks - 1) / col_blocks;
-    if (want > cap) want = cap;
+    if (rows <= 8192) return 1;
+    const long long col_blocks = (cols + 127) / 128;
+    long long want = (2ll * num_sms() + col_blocks - 1) / col_blocks;   // ~2 blocks per SM
+    const long long by_rows = rows / 1024;
+    if (want > by_rows) want = by_rows;
     if (want < 1) want = 1;
     return static_cast<int>(want);
 }
@@ -60,8 +114,14 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
                   cudaStream_t s) {
     const int chunks = partial ? colsum_chunks(rows, cols) : 1;
     const long long per = (rows + chunks - 1) / chunks;
-    dim3 grid((cols + 31) / 32, chunks);
-    colsum_kernel<<<grid, 256, 0, s>>>(in, rows, cols, per, partial, out, alpha, accumulate);
+    const bool vec = (cols % 4 == 0) && aligned16(in) && aligned16(out) && (!partial || aligned16(partial));
+    if (vec) {
+        dim3 grid((cols + 127) / 128, chunks);
+        colsum4_kernel<<<grid, 1024, 0, s>>>(in, rows, cols, per, partial, out, alpha, accumulate);
+    } else {
+        dim3 grid((cols + 31) / 32, chunks);
+        colsum_kernel<<<grid, 256, 0, s>>>(in, rows, cols, per, partial, out, alpha, accumulate);
+    }
     if (chunks > 1) colsum_finish<<<(cols + 127) / 128, 128, 0, s>>>(partial, chunks, cols, out, alpha, accumulate);
     return check_launch("colsum", chunks > 1 ? 2 : 1);
 }
