@@ -295,6 +295,39 @@ __global__ void __launch_bounds__(256) skinny_nt_kernel(const float* __restrict_
     }
 }
 
+// im2col with the k dimension padded to kp (>= 9*C, a multiple of 32) with
+// zeros: col[p][k] = x[n][oh+kh-pad][ow+kw-pad][ci] for k = (kh*3+kw)*C + ci < 9C.
+// Used for input layers whose channel count TMA cannot tile (e.g. RGB).
+__global__ void __launch_bounds__(256) im2col_pad_kernel(const float* __restrict__ x, int N, int H, int W, int C,
+                                                         int pad, int kp, float* __restrict__ col) {
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const long long total = static_cast<long long>(N) * Ho * Wo * kp;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int k = static_cast<int>(idx % kp);
+        const long long pix = idx / kp;
+        float v = 0.f;
+        if (k < 9 * C) {
+            const int ow = static_cast<int>(pix % Wo);
+            const int oh = static_cast<int>((pix / Wo) % Ho);
+            const long long n = pix / (static_cast<long long>(Wo) * Ho);
+            const int tap = k / C, ci = k % C;
+            const int ih = oh + tap / 3 - pad, iw = ow + tap % 3 - pad;
+            if (ih >= 0 && ih < H && iw >= 0 && iw < W) v = x[((n * H + ih) * W + iw) * C + ci];
+        }
+        col[idx] = v;
+    }
+}
+
+// wp[co][k] = w[co][k] for k < K, 0 for K <= k < kp
+__global__ void pad_cols_kernel(const float* __restrict__ w, int rows, int K, int kp, float* __restrict__ wp) {
+    const int total = rows * kp;
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+        const int k = idx % kp, r = idx / kp;
+        wp[idx] = k < K ? w[r * K + k] : 0.f;
+    }
+}
+
 // direct convolution, one thread per output element (co fastest)
 __global__ void __launch_bounds__(256) simt_conv_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ b, float* __restrict__ y, int N,
@@ -442,6 +475,9 @@ FcPlan plan_fc(int N, int in, int out, bool have_wT) {
 
 struct ConvPlan {
     bool tc = false;
+    bool im2col = false;    // forward through an explicit padded im2col + 2-D GEMM
+    int kp = 0;             // padded k of that im2col
+    size_t ws_col = 0, ws_wpad = 0;
     int bn = 0;
     PixBox box{};
     int splits = 1, kt_per_split = 0, num_kt = 0;
@@ -449,13 +485,21 @@ struct ConvPlan {
     size_t ws_xT = 0, ws_dyT = 0;   // dedw: [C][H][W][N] copies
     size_t ws_partial = 0;  // dedw: split-K partial sums
     size_t ws_colsum = 0;   // dedw: partial bias sums
-    size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum; }
+    size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad; }
 };
 
 ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool have_wT) {
     ConvPlan pl;
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const long long P = static_cast<long long>(N) * Ho * Wo;
+    if (op == SPRINT_CONV_FWD && Cin % 4 != 0 && Cout % 4 == 0 && Cout >= 16 && 9 * Cin <= 64) {
+        // few input channels (the RGB layer): explicit im2col, k padded to 32 or 64
+        pl.tc = pl.im2col = true;
+        pl.kp = (9 * Cin + 31) / 32 * 32;
+        pl.ws_col = fbytes(P * pl.kp);
+        pl.ws_wpad = fbytes(static_cast<long long>(Cout) * pl.kp);
+        return pl;
+    }
     if (op == SPRINT_CONV_FWD || op == SPRINT_CONV_DX) {
         pl.tc = (Cin % 4 == 0) && (Cout % 4 == 0) && Cin >= 8 && Cout >= 16;
         if (!pl.tc) return pl;
@@ -471,7 +515,9 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     // dedw
     const int chunks = colsum_chunks(P, Cout);
     pl.ws_colsum = chunks > 1 ? fbytes(static_cast<long long>(chunks) * Cout) : 0;
-    pl.tc = (N % 4 == 0) && (Cin % 4 == 0) && (Cout % 4 == 0) && Cin >= 8 && Cout >= 16;
+    // x^T puts channels outermost, so any Cin works; outputs with Cin % 4 != 0
+    // are written with direct stores
+    pl.tc = (N % 4 == 0) && (Cout % 4 == 0) && Cout >= 16;
     if (!pl.tc) {
         const long long nchunk = (P + kDwChunk - 1) / kDwChunk;
         pl.ws_partial = fbytes(nchunk * Cout * 9 * Cin);
@@ -709,6 +755,24 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total()))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    if (pl.tc && pl.im2col) {
+        float* col = static_cast<float*>(ws);
+        float* wpad = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_col);
+        const long long P = static_cast<long long>(N) * Ho * Wo;
+        im2col_pad_kernel<<<grid_cap(P * pl.kp), 256, 0, s>>>(x, N, H, W, Cin, pad, pl.kp, col);
+        if ((rc = check_launch("im2col_pad_kernel"))) return rc;
+        pad_cols_kernel<<<(Cout * pl.kp + 255) / 256, 256, 0, s>>>(w, Cout, 9 * Cin, pl.kp, wpad);
+        if ((rc = check_launch("pad_cols_kernel"))) return rc;
+        SPRINT_REQUIRE(P < (1ll << 31), SPRINT_ERR_SHAPE, "%s: too many output pixels", __func__);
+        TcParams p = base_params();
+        p.epi = EPI_STORE;
+        p.D = y;
+        p.ldd = Cout;
+        p.bias = b;
+        p.relu = relu;
+        if (gemm2d_tc(col, pl.kp, wpad, pl.kp, static_cast<int>(P), Cout, pl.kp, p, s, &rc)) return rc;
+        return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
+    }
     if (pl.tc) {
         CUtensorMap tb;
         const uint64_t db[3] = {(uint64_t)Cin, 9, (uint64_t)Cout};

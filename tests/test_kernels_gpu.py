@@ -202,6 +202,8 @@ CONV_CASES = [
     (4, 8, 8, 32, 64),      # tensor-core weight gradient, W*N = 32 per row
     (12, 7, 5, 64, 32),     # ragged rows (W*N = 60), Cout < 128
     (32, 4, 4, 128, 256),   # wide channels, split-K
+    (4, 12, 12, 3, 64),     # RGB layer, batch % 4 == 0: padded im2col forward, tensor-core weight gradient
+    (8, 9, 7, 3, 16),       # RGB layer, ragged spatial size
 ]
 
 
