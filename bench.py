@@ -221,13 +221,12 @@ def run_ours(args, cfg, rank, world, local_rank):
     for _ in range(args.steps):
         main = tr.main_stream
         e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
-        tr.main_stream.wait_event(tr.ev_update)
         e0.record(main)
         with torch.cuda.stream(main):
             dx.copy_(hx, non_blocking=True)
             dy.copy_(hy, non_blocking=True)
         e1.record(main)
-        tr.ev_update.record(main)
+        tr.mark_inputs(main)
         tr.step()
         e2.record(main)
         with torch.cuda.stream(main):

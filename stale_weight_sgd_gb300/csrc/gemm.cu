@@ -93,28 +93,31 @@ int launch_tc(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensor
     switch (bn) {
         case 64: return launch_tc_bn<ROLE, 64>(a, b, d, p, s);
         case 128: return launch_tc_bn<ROLE, 128>(a, b, d, p, s);
+        case 160: return launch_tc_bn<ROLE, 160>(a, b, d, p, s);
+        case 192: return launch_tc_bn<ROLE, 192>(a, b, d, p, s);
         case 256: return launch_tc_bn<ROLE, 256>(a, b, d, p, s);
         default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", bn);
     }
 }
 
-// Picks the tile width: the one whose last wave leaves the fewest SM slots idle,
-// weighted by the per-instruction MMA efficiency of narrow tiles.
+// Picks the tile width for a persistent launch: each SM runs ceil(tiles / SMs)
+// tiles one after another, and a tile's time grows with its width and shrinks
+// with the MMA efficiency of that width (narrow tiles are bound by shared-
+// memory operand traffic), so minimise ceil(tiles / SMs) * bn / efficiency.
 int pick_bn(long long m_tiles, long long n, long long z, int max_bn) {
-    const int cands[3] = {256, 128, 64};
-    const double eff[3] = {1.0, 0.95, 0.7};
+    const int cands[5] = {256, 192, 160, 128, 64};
+    const double eff[5] = {1.0, 0.97, 0.95, 0.92, 0.7};
     const long long sms = num_sms();
     int best = 64;
-    double best_score = -1.0;
-    for (int i = 0; i < 3; ++i) {
+    double best_cost = 1e300;
+    for (int i = 0; i < 5; ++i) {
         const int bn = cands[i];
         if (bn > max_bn) continue;
         const long long tiles = m_tiles * ((n + bn - 1) / bn) * z;
-        const long long waves = (tiles + sms - 1) / sms;
-        const double used = static_cast<double>(m_tiles * n * z) / static_cast<double>(waves * sms * bn);
-        const double score = used * eff[i];
-        if (score > best_score + 1e-9) {
-            best_score = score;
+        const long long rounds = (tiles + sms - 1) / sms;
+        const double cost = static_cast<double>(rounds) * bn / eff[i];
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
             best = bn;
         }
     }
@@ -328,6 +331,28 @@ __global__ void pad_cols_kernel(const float* __restrict__ w, int rows, int K, in
     }
 }
 
+// dx[m][n] = mask(m, n) * sum_{k < K} dy[m][k] * w[k][n] for a short reduction
+// (K <= 32, e.g. the input gradient of a 10-way classifier): one thread per
+// output, dy row broadcast within the warp, w read coalesced along n.
+__global__ void __launch_bounds__(256) smallk_dx_kernel(const float* __restrict__ dy, const float* __restrict__ w,
+                                                        const float* __restrict__ mask, float* __restrict__ dx, int M,
+                                                        int N, int K) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(idx % N);
+        const long long m = idx / N;
+        if (mask && !(mask[idx] > 0.f)) {
+            dx[idx] = 0.f;
+            continue;
+        }
+        const float* d = dy + m * K;
+        float acc = 0.f;
+        for (int k = 0; k < K; ++k) acc = fmaf(d[k], w[static_cast<long long>(k) * N + n], acc);
+        dx[idx] = acc;
+    }
+}
+
 // direct convolution, one thread per output element (co fastest)
 __global__ void __launch_bounds__(256) simt_conv_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ b, float* __restrict__ y, int N,
@@ -466,7 +491,8 @@ FcPlan plan_fc(int N, int in, int out, bool have_wT) {
     const bool al = (in % 4 == 0) && (out % 4 == 0);
     pl.fwd_tc = al && in >= 8 && out >= 16;
     pl.dx_tc = al && out >= 8 && in >= 16;
-    pl.dw_tc = al && (N % 4 == 0) && N >= 8 && in >= 16 && out >= 16;
+    // dW reads the transposed copies (pitch = batch) and writes dw (pitch = in): out may be anything
+    pl.dw_tc = (in % 4 == 0) && (N % 4 == 0) && N >= 8 && in >= 16;
     pl.ws_wT = (pl.dx_tc && !have_wT) ? fbytes(static_cast<long long>(in) * out) : 0;
     pl.ws_xT = pl.dw_tc ? fbytes(static_cast<long long>(N) * in) : 0;
     pl.ws_dyT = pl.dw_tc ? fbytes(static_cast<long long>(N) * out) : 0;
@@ -671,6 +697,11 @@ extern "C" int sprint_fc_bwd(const float* x, const float* w, const float* wT, co
             p.ldm = in;
             done = gemm2d_tc(dy, out, wt, out, N, in, out, p, s, &rc);
             if (rc) return rc;
+        }
+        if (!done && out <= 32) {
+            smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(dy, w, relu_src, dx, N, in, out);
+            if ((rc = check_launch("smallk_dx_kernel"))) return rc;
+            done = true;
         }
         if (!done) {
             SimtGemm g{N, in, out, dy, out, 1, w, 1, in, dx, in, nullptr, relu_src, in, 1.f, 0, 0, SIMT_MASK};

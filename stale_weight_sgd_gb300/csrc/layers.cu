@@ -330,6 +330,47 @@ __global__ void __launch_bounds__(1024) softmax_xent_kernel(const float* logits,
     }
 }
 
+// Few classes (C <= 32): one row per thread; per-row losses are added by each
+// warp in row order and the warp sums in warp order (deterministic).
+__global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(const float* logits, const int32_t* __restrict__ labels,
+                                                                 int N, int C, float* __restrict__ loss, float* dlogits,
+                                                                 float scale) {
+    __shared__ float warp_loss[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float acc = 0.f;
+    for (int base = 0; base < N; base += 1024) {
+        const int r = base + threadIdx.x;
+        float row_loss = 0.f;
+        if (r < N) {
+            const float* z = logits + static_cast<long long>(r) * C;
+            float* d = dlogits + static_cast<long long>(r) * C;
+            float m = -INFINITY;
+            for (int c = 0; c < C; ++c) m = fmaxf(m, z[c]);
+            float s = 0.f;
+            for (int c = 0; c < C; ++c) s += expf(z[c] - m);
+            const int y = labels[r];
+            const float zy = z[y];
+            const float inv = 1.f / s;
+            row_loss = m + logf(s) - zy;
+            for (int c = 0; c < C; ++c) d[c] = (expf(z[c] - m) * inv - (c == y ? 1.f : 0.f)) * scale;
+        }
+        // add this pass's 32 rows of the warp in row order
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, row_loss, o);
+            if (lane >= o) row_loss += t;
+        }
+        acc += __shfl_sync(0xffffffffu, row_loss, 31);
+    }
+    if (lane == 0) warp_loss[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 32; ++w) t += warp_loss[w];
+        *loss = t * scale;
+    }
+}
+
 // ------------------------------------------------------------------ im2col
 template <int V>
 __global__ void __launch_bounds__(256) im2col_kernel(const float* __restrict__ x, int N, int H, int W, int C, int pad,
@@ -425,7 +466,12 @@ extern "C" int sprint_softmax_xent(const float* logits, const int32_t* labels, i
     SPRINT_ALIGNED(loss, "loss");
     SPRINT_ALIGNED(dlogits, "dlogits");
     const float scale = reduction_sum ? 1.f : 1.f / static_cast<float>(N);
-    softmax_xent_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss, dlogits, scale);
+    if (C <= 32)
+        softmax_xent_rows_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss,
+                                                                                   dlogits, scale);
+    else
+        softmax_xent_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss, dlogits,
+                                                                              scale);
     return check_launch(__func__);
 }
 

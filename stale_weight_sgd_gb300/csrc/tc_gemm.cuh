@@ -6,7 +6,7 @@
 //   warp 4   : TMA producer (one lane) — fills a STAGES-deep ring of shared-
 //              memory stages, 128 B (32 fp32) wide along k, 128-byte swizzled;
 //              the ring runs on across tiles;
-//   warp 5   : allocates two TMEM accumulators (2 x BN fp32 columns) and issues
+//   warp 5   : allocates two TMEM accumulators (BN fp32 columns each) and issues
 //              tcgen05.mma.kind::tf32 (M=128, N=BN, K=8) from one lane, tile
 //              after tile, alternating accumulators; tcgen05.commit frees a
 //              stage once its MMAs are done and hands a finished accumulator
@@ -54,7 +54,12 @@ constexpr int TC_THREADS = 192;
 constexpr int TC_A_STAGE = TC_BM * TC_BK * 4;  // 16 KB
 constexpr int TC_STAGING = 4 * 4096;           // one 32 x 32 fp32 staging chunk per epilogue warp
 
-__host__ __device__ constexpr int tc_stages(int bn) { return bn >= 256 ? 4 : (bn >= 128 ? 6 : 8); }
+// as many stages as fit next to the staging buffers in 227 KB of shared memory (at most 8)
+__host__ __device__ constexpr int tc_stages(int bn) {
+    return (232448 - 1024 - 4 * 4096 - 1024) / (128 * 32 * 4 + bn * 32 * 4) > 8
+               ? 8
+               : (232448 - 1024 - 4 * 4096 - 1024) / (128 * 32 * 4 + bn * 32 * 4);
+}
 __host__ __device__ constexpr int tc_b_stage(int bn) { return bn * TC_BK * 4; }
 __host__ __device__ constexpr int tc_tmem_cols(int bn) { return bn <= 32 ? 64 : (bn <= 64 ? 128 : (bn <= 128 ? 256 : 512)); }
 __host__ __device__ constexpr int tc_smem_bytes(int bn) {
@@ -113,6 +118,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
     constexpr uint32_t STAGE_BYTES = TC_A_STAGE + B_STAGE;
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+    static_assert(tc_smem_bytes(BN) <= 232448, "shared memory budget exceeded");
+    constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;   // second accumulator at a power-of-two column offset
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t b = j & 1, tph = (j >> 1) & 1;
                 if (!mbar_wait_bounded(&tmem_empty[b], tph ^ 1, p.status, DEV_FLAG_WAIT_MMA)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + b * BN;
+                const uint32_t d_tmem = tmem_base + b * ACC_STRIDE;
                 for (int i = 0; i < nkt; ++i, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + b * BN + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+                tmem_ld_32x32b_x32(tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
                 tmem_wait_ld();
                 if (c + 32 >= BN) {  // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();

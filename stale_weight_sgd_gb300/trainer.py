@@ -24,9 +24,11 @@ blog summary: replicas fetch w, push dw, the server applies w' := w - eta*dw):
 
 Replica r draws batch (t*R + r) mod P from a pool of P device-resident
 batches. Replicas run on their own CUDA streams (independent work that fills
-the GPU together); the update waits for all of them, and the next step's
-replicas wait for the update. Nothing here computes: every operation is a
-libsprint call.
+the GPU together); the update of step t waits for all of them. A replica of
+step t waits only for the newest weight version it reads (so a replica with
+delay >= 1 need not wait for update t-1) and for update t-2, the last reader
+of its GradBuf set: GradBufs are double-buffered by step parity. Nothing here
+computes: every operation is a libsprint call.
 """
 from __future__ import annotations
 
@@ -63,7 +65,8 @@ class StaleSGD:
 
         self.ring = torch.zeros((self.S + 1, self.n), **f32)
         self.ringT = torch.zeros((self.S + 1, self.n), **f32)   # W^T of every layer that needs dX
-        self.gradbuf = torch.zeros((self.R, self.n), **f32)
+        self.gradbuf_sets = torch.zeros((2, self.R, self.n), **f32)   # step t writes set t % 2
+        self.gradbuf = self.gradbuf_sets[0]
         if optimizer == "momentum":
             self.opt_state = torch.zeros(self.n, **f32)
         elif optimizer == "adagrad":
@@ -81,9 +84,13 @@ class StaleSGD:
         main = torch.cuda.current_stream(self.dev)
         self.main_stream = main
         self.streams = [torch.cuda.Stream(self.dev) for _ in range(self.R)] if concurrent else [main] * self.R
-        self.ev_update = torch.cuda.Event()
+        self.ev_update = torch.cuda.Event()      # the latest update has finished
         self.ev_done = [torch.cuda.Event() for _ in range(self.R)]
+        self.ev_ver = [torch.cuda.Event() for _ in range(self.S + 3)]  # version v exists: ev_ver[v % (S+3)]
         self.ev_update.record(main)
+        self.ev_ver[0].record(main)
+        self.ev_inputs = torch.cuda.Event()
+        self.inputs_pending = False
         self._sched = np.zeros((0, self.R), np.int32)
         self.batches_x = None
         self.batches_y = None
@@ -133,6 +140,7 @@ class StaleSGD:
         self.t = 0
         torch.cuda.synchronize(self.dev)
         self.ev_update.record(self.main_stream)
+        self.ev_ver[0].record(self.main_stream)
 
     def load_batches(self, batches):
         """Uploads the pool of (x, labels) batches; x is NHWC (or [N][features])."""
@@ -145,6 +153,12 @@ class StaleSGD:
         """Uses device tensors [P][N][...] and [P][N] (int32) as the batch pool."""
         self.batches_x = x.reshape(x.shape[0], self.N, -1)
         self.batches_y = y
+
+    def mark_inputs(self, stream):
+        """The batch pool was (re)written on `stream`: the next step's replicas
+        wait for that work before reading it."""
+        self.ev_inputs.record(stream)
+        self.inputs_pending = True
 
     def weights(self, version=None) -> np.ndarray:
         """Dense copy of W(version) (default: the current version)."""
@@ -179,7 +193,7 @@ class StaleSGD:
         N = self.N
         ring_ptr = self.ring.data_ptr()
         row = self.n * 4
-        gb = self.gradbuf[r].data_ptr()
+        gb = self.gradbuf_sets[t % 2][r].data_ptr()
         bi = (t * self.R + r) % self.batches_x.shape[0]
         x = self.batches_x[bi]
         y = self.batches_y[bi]
@@ -241,7 +255,7 @@ class StaleSGD:
         """SumGradient + UpdateWeights (Algorithm 2): W(t+1) into ring slot t+1."""
         w_in = self.ring[t % (self.S + 1)]
         w_out = self.ring[(t + 1) % (self.S + 1)]
-        bufs = [self.gradbuf[r] for r in range(self.R)]
+        bufs = [self.gradbuf_sets[t % 2][r] for r in range(self.R)]
         sh = stream.cuda_stream
         if self.optimizer == "sgd":
             S.sprint_apply_update_sgd(w_in, w_out, bufs, self.n, self.eta, sh)
@@ -254,15 +268,23 @@ class StaleSGD:
     def step(self):
         """One global step: every replica's gradient, then one update. Asynchronous."""
         t = self.t
+        L = len(self.ev_ver)
         for r in range(self.R):
             st = self.streams[r]
-            st.wait_event(self.ev_update)
+            newest = max(self._version(t, r, li) for li in range(len(self.shapes)))
+            # the newest version this replica reads, and update t-2 (last reader of GradBuf set t % 2)
+            st.wait_event(self.ev_ver[max(newest, t - 1, 0) % L])
+            if self.inputs_pending:
+                st.wait_event(self.ev_inputs)
             self._replica(t, r, st)
             self.ev_done[r].record(st)
         for r in range(self.R):
             self.main_stream.wait_event(self.ev_done[r])
         self._update(t, self.main_stream)
         self.ev_update.record(self.main_stream)
+        self.ev_ver[(t + 1) % L].record(self.main_stream)
+        self.gradbuf = self.gradbuf_sets[t % 2]   # the GradBufs of the step just issued
+        self.inputs_pending = False
         self.t = t + 1
 
     def step_loss(self) -> float:

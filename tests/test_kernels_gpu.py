@@ -102,7 +102,7 @@ def test_pool_fwd_bwd_bit_exact(S, shape):
     assert (host(out) == ref.astype(np.float32)).all()
 
 
-@pytest.mark.parametrize("N,C", [(8, 10), (512, 10), (64, 1000), (33, 7)])
+@pytest.mark.parametrize("N,C", [(8, 10), (512, 10), (64, 1000), (33, 7), (1500, 10), (20, 32), (20, 33)])
 def test_softmax_xent(S, N, C):
     z = _f32(5, f"z{N}", (N, C), 3.0)
     y = synth.labels(5, f"y{N}", N, C)
@@ -143,6 +143,8 @@ FC_CASES = [
     (64, 256, 512),     # M below one tile
     (37, 50, 10),       # CUDA-core path (widths not multiples of 4)
     (512, 5000, 10),    # classifier of SMLPs
+    (64, 48, 10),       # 10 outputs: tensor-core dW with a partial M tile, short-reduction dX
+    (16, 40, 33),       # 33 outputs: tensor-core dW, CUDA-core dX
 ]
 
 
