@@ -62,63 +62,146 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
 }
 
 // ------------------------------------------------------------------ tcgen05 launches
+// Tile shape of one launch: BN output columns per tile; pair = clusters of two
+// CTAs sharing M = 256 MMAs (each CTA loads BN/2 rows of B).
+struct Tile {
+    int bn = 64;
+    bool pair = false;
+    uint32_t b_rows() const { return static_cast<uint32_t>(pair ? bn / 2 : bn); }
+};
+
+// CTA pairs that can be resident at once for this kernel (clusters are placed
+// within one GPC, so this can be below half the SM count)
 template <int ROLE, int BN>
+int pair_slots() {
+    static int slots[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!slots[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+        cfg.blockDim = dim3(TC_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = tc_smem_bytes(BN, true);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<ROLE, BN, true>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        slots[dev] = n;
+    }
+    return slots[dev];
+}
+
+template <int ROLE, int BN, bool PAIR>
 int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const TcParams& p,
                  cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel<ROLE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc_smem_bytes(BN)) != cudaSuccess)
+        if (cudaFuncSetAttribute(tc_gemm_kernel<ROLE, BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc_smem_bytes(BN, PAIR)) != cudaSuccess)
             return check_cuda("cudaFuncSetAttribute(tc_gemm_kernel)");
         attr_done[dev] = true;
     }
-    // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
-    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-    tc_gemm_kernel<ROLE, BN><<<grid, TC_THREADS, tc_smem_bytes(BN), s>>>(a, b, d, p);
-    return check_launch("tc_gemm_kernel");
-}
-
-template <int ROLE>
-int launch_tc(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, TcParams p, long long m_tiles,
-              long long n_tiles, long long z_tiles, cudaStream_t s) {
-    const long long tiles = m_tiles * n_tiles * z_tiles;
-    if (tiles <= 0) return SPRINT_OK;
-    if (tiles > (1ll << 31) - 1) return fail(SPRINT_ERR_SHAPE, "tc_gemm: %lld tiles is too many", tiles);
-    p.m_tiles = static_cast<int>(m_tiles);
-    p.n_tiles = static_cast<int>(n_tiles);
-    p.z_tiles = static_cast<int>(z_tiles);
-    p.num_tiles = static_cast<int>(tiles);
-    switch (bn) {
-        case 64: return launch_tc_bn<ROLE, 64>(a, b, d, p, s);
-        case 128: return launch_tc_bn<ROLE, 128>(a, b, d, p, s);
-        case 160: return launch_tc_bn<ROLE, 160>(a, b, d, p, s);
-        case 192: return launch_tc_bn<ROLE, 192>(a, b, d, p, s);
-        case 256: return launch_tc_bn<ROLE, 256>(a, b, d, p, s);
-        default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", bn);
+    if constexpr (!PAIR) {
+        // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
+        const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+        tc_gemm_kernel<ROLE, BN, false><<<grid, TC_THREADS, tc_smem_bytes(BN, false), s>>>(a, b, d, p);
+        return check_launch("tc_gemm_kernel");
+    } else {
+        // persistent pairs: at most as many clusters as can be resident together
+        const int slots = pair_slots<ROLE, BN>();
+        const int pairs = p.num_tiles < slots ? p.num_tiles : slots;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        cfg.blockDim = dim3(TC_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = tc_smem_bytes(BN, true);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, tc_gemm_kernel<ROLE, BN, true>, a, b, d, p);
+        return check_launch("tc_gemm_kernel(pair)");
     }
 }
 
-// Picks the tile width for a persistent launch: each SM runs ceil(tiles / SMs)
-// tiles one after another, and a tile's time grows with its width and shrinks
-// with the MMA efficiency of that width (narrow tiles are bound by shared-
-// memory operand traffic), so minimise ceil(tiles / SMs) * bn / efficiency.
-int pick_bn(long long m_tiles, long long n, long long z, int max_bn) {
+// m_tiles counts 128-row tiles; a pair launch walks ceil(m_tiles / 2) units.
+template <int ROLE>
+int launch_tc(Tile tl, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, TcParams p,
+              long long m_tiles, long long n_tiles, long long z_tiles, cudaStream_t s) {
+    const long long m_units = tl.pair ? (m_tiles + 1) / 2 : m_tiles;
+    const long long tiles = m_units * n_tiles * z_tiles;
+    if (tiles <= 0) return SPRINT_OK;
+    if (tiles > (1ll << 31) - 1) return fail(SPRINT_ERR_SHAPE, "tc_gemm: %lld tiles is too many", tiles);
+    p.m_tiles = static_cast<int>(m_units);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.z_tiles = static_cast<int>(z_tiles);
+    p.num_tiles = static_cast<int>(tiles);
+    if (tl.pair) {
+        switch (tl.bn) {
+            case 64: return launch_tc_bn<ROLE, 64, true>(a, b, d, p, s);
+            case 128: return launch_tc_bn<ROLE, 128, true>(a, b, d, p, s);
+            case 160: return launch_tc_bn<ROLE, 160, true>(a, b, d, p, s);
+            case 192: return launch_tc_bn<ROLE, 192, true>(a, b, d, p, s);
+            case 256: return launch_tc_bn<ROLE, 256, true>(a, b, d, p, s);
+            default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", tl.bn);
+        }
+    }
+    switch (tl.bn) {
+        case 64: return launch_tc_bn<ROLE, 64, false>(a, b, d, p, s);
+        case 128: return launch_tc_bn<ROLE, 128, false>(a, b, d, p, s);
+        case 160: return launch_tc_bn<ROLE, 160, false>(a, b, d, p, s);
+        case 192: return launch_tc_bn<ROLE, 192, false>(a, b, d, p, s);
+        case 256: return launch_tc_bn<ROLE, 256, false>(a, b, d, p, s);
+        default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", tl.bn);
+    }
+}
+
+// Picks the tile shape of a persistent launch. Each slot (an SM, or a pair of
+// SMs) runs ceil(units / slots) work units one after another; a unit's time
+// grows with its width and shrinks with the MMA efficiency of that shape, so
+// minimise ceil(units / slots) * bn / efficiency. A pair unit is two 128-row
+// tiles on two SMs, so it takes as long as one single-CTA tile of the same
+// width at the same efficiency. The efficiencies are measured (8192^3 TF32
+// GEMM, relative to the pair of width 256 at ~940 TFLOP/s): a TF32 k-tile is
+// bound by shared-memory bandwidth (the TMA writes plus the tensor core's
+// operand reads, ~128 B/clk per SM), which only the pair-256 shape, loading half
+// of B per SM and reading A once per 256 columns, brings under its MMA time.
+Tile pick_tile(long long m_tiles, long long n, long long z, int max_bn) {
     const int cands[5] = {256, 192, 160, 128, 64};
-    const double eff[5] = {1.0, 0.97, 0.95, 0.92, 0.7};
+    const double eff[5] = {0.86, 0.72, 0.68, 0.58, 0.36};
+    const double eff_pair[5] = {1.0, 0.79, 0.86, 0.74, 0.40};
     const long long sms = num_sms();
-    int best = 64;
+    Tile best;
     double best_cost = 1e300;
-    for (int i = 0; i < 5; ++i) {
-        const int bn = cands[i];
-        if (bn > max_bn) continue;
-        const long long tiles = m_tiles * ((n + bn - 1) / bn) * z;
-        const long long rounds = (tiles + sms - 1) / sms;
-        const double cost = static_cast<double>(rounds) * bn / eff[i];
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = bn;
+    for (int pair = 0; pair < 2; ++pair) {
+        if (pair && m_tiles < 2) continue;
+        const long long mu = pair ? (m_tiles + 1) / 2 : m_tiles;
+        const long long slots = pair ? sms / 2 : sms;
+        for (int i = 0; i < 5; ++i) {
+            const int bn = cands[i];
+            if (bn > max_bn) continue;
+            const long long units = mu * ((n + bn - 1) / bn) * z;
+            const long long rounds = (units + slots - 1) / slots;
+            const double cost = static_cast<double>(rounds) * bn / (pair ? eff_pair[i] : eff[i]);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.bn = bn;
+                best.pair = pair != 0;
+            }
         }
     }
     return best;
@@ -504,7 +587,7 @@ struct ConvPlan {
     bool im2col = false;    // forward through an explicit padded im2col + 2-D GEMM
     int kp = 0;             // padded k of that im2col
     size_t ws_col = 0, ws_wpad = 0;
-    int bn = 0;
+    Tile tile{};
     PixBox box{};
     int splits = 1, kt_per_split = 0, num_kt = 0;
     size_t ws_wT = 0;       // dedx: transposed weights when the caller has none
@@ -532,7 +615,7 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         const int gw = op == SPRINT_CONV_FWD ? Wo : W, gh = op == SPRINT_CONV_FWD ? Ho : H;
         pl.box = pick_box(TC_BM, gw, gh, N);
         const int ncols = op == SPRINT_CONV_FWD ? Cout : Cin;
-        pl.bn = pick_bn(pl.box.tiles(), ncols, 1, ncols >= 256 ? 256 : (ncols >= 128 ? 128 : 64));
+        pl.tile = pick_tile(pl.box.tiles(), ncols, 1, ncols >= 256 ? 256 : (ncols >= 128 ? 128 : 64));
         pl.num_kt = 9 * (((op == SPRINT_CONV_FWD ? Cin : Cout) + 31) / 32);
         pl.kt_per_split = pl.num_kt;
         if (op == SPRINT_CONV_DX && !have_wT) pl.ws_wT = fbytes(9ll * Cin * Cout);
@@ -554,10 +637,14 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     pl.box = PixBox{0, 0, 0, static_cast<int>((static_cast<long long>(Wo) * N + TC_BK - 1) / TC_BK), Ho, 1};
     pl.num_kt = pl.box.tw * Ho;   // per output row: ceil(Wo*N / 32) k-tiles
     const long long m_tiles = (Cout + TC_BM - 1) / TC_BM;
-    // split-K below fills the machine, so the widest tile (best MMA shape) is used
-    pl.bn = Cin > 128 ? 256 : (Cin > 64 ? 128 : 64);
-    const long long base = m_tiles * ((Cin + pl.bn - 1) / pl.bn) * 9;
-    long long want = (2ll * num_sms() + base - 1) / base;
+    // split-K below fills the machine, so the widest tile (best MMA shape) is used,
+    // on CTA pairs when Cout spans an even number of 128-row tiles (or many)
+    pl.tile.bn = Cin > 128 ? 256 : (Cin > 64 ? 128 : 64);
+    pl.tile.pair = m_tiles >= 2 && (m_tiles % 2 == 0 || m_tiles >= 6);
+    const long long m_units = pl.tile.pair ? (m_tiles + 1) / 2 : m_tiles;
+    const long long slots = pl.tile.pair ? num_sms() / 2 : num_sms();
+    const long long base = m_units * ((Cin + pl.tile.bn - 1) / pl.tile.bn) * 9;
+    long long want = (2ll * slots + base - 1) / base;
     long long maxs = pl.num_kt / 8;
     if (want > maxs) want = maxs;
     if (want < 1) want = 1;
@@ -589,11 +676,11 @@ int check_ws(const char* fn, const void* ws, size_t ws_bytes, size_t need) {
 bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int M, int N, int K, TcParams p,
                cudaStream_t s, int* rc) {
     const long long m_tiles = (M + TC_BM - 1) / TC_BM;
-    const int bn = pick_bn(m_tiles, N, 1, N >= 256 ? 256 : (N >= 128 ? 128 : 64));
+    const Tile tl = pick_tile(m_tiles, N, 1, N >= 256 ? 256 : (N >= 128 ? 128 : 64));
     CUtensorMap ta, tb, td;
     const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 4};
     const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)ldb * 4};
-    const uint32_t ba[2] = {32, 128}, bb[2] = {32, (uint32_t)bn};
+    const uint32_t ba[2] = {32, 128}, bb[2] = {32, tl.b_rows()};
     if (!make_tmap(&ta, A, 2, da, sa, ba) || !make_tmap(&tb, B, 2, db, sb, bb)) return false;
     // TMA store of D when its row pitch is a multiple of 16 bytes, else direct stores
     p.store = ST_DIRECT;
@@ -607,7 +694,7 @@ bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int
     p.N = N;
     p.num_kt = (K + TC_BK - 1) / TC_BK;
     p.kt_per_split = p.num_kt;
-    *rc = launch_tc<ROLE_GEMM_2D>(bn, ta, tb, td, p, m_tiles, (N + bn - 1) / bn, 1, s);
+    *rc = launch_tc<ROLE_GEMM_2D>(tl, ta, tb, td, p, m_tiles, (N + tl.bn - 1) / tl.bn, 1, s);
     return true;
 }
 
@@ -768,7 +855,8 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
     p.tiles_h = pl.box.th;
     p.chunks = pl.num_kt / 9;
     *done = true;
-    return launch_tc<ROLE_CONV_IMPL>(pl.bn, ta, *tb, td, p, pl.box.tiles(), (ncols + pl.bn - 1) / pl.bn, 1, s);
+    return launch_tc<ROLE_CONV_IMPL>(pl.tile, ta, *tb, td, p, pl.box.tiles(), (ncols + pl.tile.bn - 1) / pl.tile.bn,
+                                     1, s);
 }
 
 extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
@@ -808,7 +896,7 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
         CUtensorMap tb;
         const uint64_t db[3] = {(uint64_t)Cin, 9, (uint64_t)Cout};
         const uint64_t sb[2] = {(uint64_t)Cin * 4, (uint64_t)9 * Cin * 4};
-        const uint32_t bb[3] = {32, 1, (uint32_t)pl.bn};
+        const uint32_t bb[3] = {32, 1, pl.tile.b_rows()};
         if (make_tmap(&tb, w, 3, db, sb, bb)) {
             TcParams p = base_params();
             p.img_n = N;
@@ -859,7 +947,7 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
         CUtensorMap tb;
         const uint64_t db[3] = {(uint64_t)Cout, (uint64_t)Cin, 9};
         const uint64_t sb[2] = {(uint64_t)Cout * 4, (uint64_t)Cin * Cout * 4};
-        const uint32_t bb[3] = {32, (uint32_t)pl.bn, 1};
+        const uint32_t bb[3] = {32, pl.tile.b_rows(), 1};
         if (make_tmap(&tb, wt, 3, db, sb, bb)) {
             TcParams p = base_params();
             p.img_n = N;
@@ -920,7 +1008,7 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         const uint64_t dbm[3] = {(uint64_t)W * N, (uint64_t)H, (uint64_t)Cin};
         const uint64_t sbm[2] = {(uint64_t)W * N * 4, (uint64_t)H * W * N * 4};
         const uint32_t ba[3] = {32, 1, 128};
-        const uint32_t bb[3] = {32, 1, (uint32_t)pl.bn};
+        const uint32_t bb[3] = {32, 1, pl.tile.b_rows()};
         if (make_tmap(&ta, dyT, 3, da, sa, ba) && make_tmap(&tb, xT, 3, dbm, sbm, bb)) {
             TcParams p = base_params();
             p.M = Cout;
@@ -953,8 +1041,8 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
                 const uint32_t bd[3] = {32, 1, 32};
                 if (make_tmap(&td, dw, 3, dd, sd, bd, false)) p.store = ST_WGRAD3D;
             }
-            if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.bn, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
-                                                 (Cin + pl.bn - 1) / pl.bn, 9ll * pl.splits, s)))
+            if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
+                                                 (Cin + pl.tile.bn - 1) / pl.tile.bn, 9ll * pl.splits, s)))
                 return rc;
             if (pl.splits > 1) {
                 dw_split_reduce<<<grid_cap(9ll * Cout * Cin), 256, 0, s>>>(part, pl.splits, Cout, Cin, dw, alpha,

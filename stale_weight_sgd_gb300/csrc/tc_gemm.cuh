@@ -4,8 +4,8 @@
 // 128 x BN output tiles (m fastest, so CTAs running together share the B
 // panel in L2). Within a CTA:
 //   warp 4   : TMA producer (one lane) — fills a STAGES-deep ring of shared-
-//              memory stages, 128 B (32 fp32) wide along k, 128-byte swizzled;
-//              the ring runs on across tiles;
+//              memory stages, each one or two k-tiles of 128 B (32 fp32) along
+//              k, 128-byte swizzled; the ring runs on across tiles;
 //   warp 5   : allocates two TMEM accumulators (BN fp32 columns each) and issues
 //              tcgen05.mma.kind::tf32 (M=128, N=BN, K=8) from one lane, tile
 //              after tile, alternating accumulators; tcgen05.commit frees a
@@ -20,6 +20,15 @@
 //              cannot describe (row pitch not a multiple of 16 bytes) are
 //              written by the threads directly instead.
 // So the epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// CTA pairs (PAIR = true, clusters of two): a work unit is two vertically
+// adjacent tiles (m-tiles 2u and 2u+1) computed by one tcgen05.mma of M = 256
+// (cta_group::2) that the even CTA issues. Each CTA loads its own 128 rows of A
+// and half of the BN rows of B, so a pair moves 3/4 of the operand bytes two
+// single CTAs would for the same FLOPs; both CTAs' loads complete on the even
+// CTA's stage barrier, commits free the stage in both CTAs, and each CTA's
+// epilogue drains its own TMEM (rows 0-127 of the pair tile in the even CTA,
+// 128-255 in the odd one) and hands it back to the even CTA's MMA thread.
 //
 // Both operands are K-major: the TF32 kind of tcgen05.mma reads no MN-major
 // operand on this part, so transposed operands are formed in global memory by
@@ -54,21 +63,36 @@ constexpr int TC_THREADS = 192;
 constexpr int TC_A_STAGE = TC_BM * TC_BK * 4;  // 16 KB
 constexpr int TC_STAGING = 4 * 4096;           // one 32 x 32 fp32 staging chunk per epilogue warp
 
-// as many stages as fit next to the staging buffers in 227 KB of shared memory (at most 8)
-__host__ __device__ constexpr int tc_stages(int bn) {
-    return (232448 - 1024 - 4 * 4096 - 1024) / (128 * 32 * 4 + bn * 32 * 4) > 8
-               ? 8
-               : (232448 - 1024 - 4 * 4096 - 1024) / (128 * 32 * 4 + bn * 32 * 4);
+// B rows one CTA holds per k-tile (a pair splits the BN rows between its CTAs)
+__host__ __device__ constexpr int tc_b_rows(int bn, bool pair) { return pair ? bn / 2 : bn; }
+__host__ __device__ constexpr int tc_b_stage(int bn, bool pair) { return tc_b_rows(bn, pair) * TC_BK * 4; }
+constexpr int TC_RING_BYTES = 232448 - 1024 - 4 * 4096 - 1024;   // shared memory left for the operand ring
+// k-tiles per pipeline stage. Every stage hand-off (full barrier, MMA batch,
+// commit) costs a roughly fixed ~100 cycles, which narrow tiles cannot hide
+// behind their MMAs, so they take two k-tiles per stage as long as the ring
+// still holds at least four stages (measured: +20-30% for pair tiles of width
+// <= 160 and single tiles of width 64; wide tiles lose more from the shorter
+// ring than they gain).
+__host__ __device__ constexpr int tc_ks(int bn, bool pair) {
+    return TC_RING_BYTES / (2 * (TC_A_STAGE + tc_b_stage(bn, pair))) >= 4 ? 2 : 1;
 }
-__host__ __device__ constexpr int tc_b_stage(int bn) { return bn * TC_BK * 4; }
+// as many stages as fit next to the staging buffers in 227 KB of shared memory (at most 8)
+__host__ __device__ constexpr int tc_stages(int bn, bool pair) {
+    return TC_RING_BYTES / (tc_ks(bn, pair) * (TC_A_STAGE + tc_b_stage(bn, pair))) > 8
+               ? 8
+               : TC_RING_BYTES / (tc_ks(bn, pair) * (TC_A_STAGE + tc_b_stage(bn, pair)));
+}
 __host__ __device__ constexpr int tc_tmem_cols(int bn) { return bn <= 32 ? 64 : (bn <= 64 ? 128 : (bn <= 128 ? 256 : 512)); }
-__host__ __device__ constexpr int tc_smem_bytes(int bn) {
-    return 1024 /* alignment slack */ + tc_stages(bn) * (TC_A_STAGE + tc_b_stage(bn)) + TC_STAGING + 256 /* barriers */;
+__host__ __device__ constexpr int tc_smem_bytes(int bn, bool pair) {
+    return 1024 /* alignment slack */ +
+           tc_stages(bn, pair) * tc_ks(bn, pair) * (TC_A_STAGE + tc_b_stage(bn, pair)) + TC_STAGING +
+           256 /* barriers */;
 }
 
 struct TcParams {
     int M, N;            // GEMM_2D / CONV_WGRAD: output rows, columns; CONV_IMPL: N = columns
-    int m_tiles, n_tiles, z_tiles, num_tiles;  // tile space: m fastest, then n, then z
+    int m_tiles, n_tiles, z_tiles, num_tiles;  // work units: m fastest, then n, then z (a pair's
+                                               // unit covers m-tiles 2m and 2m+1)
     int num_kt;          // k-tiles in the full reduction
     int kt_per_split;    // k-tiles per split
     int splits;          // CONV_WGRAD: z = tap * splits + split
@@ -108,25 +132,29 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& p) {
     return c;
 }
 
-template <int ROLE, int BN>
+template <int ROLE, int BN, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const TcParams p) {
-    constexpr int STAGES = tc_stages(BN);
-    constexpr int B_STAGE = tc_b_stage(BN);
-    constexpr uint32_t IDESC = idesc_tf32(BN, false, false);
+    constexpr int STAGES = tc_stages(BN, PAIR);
+    constexpr int KS = tc_ks(BN, PAIR);          // k-tiles per stage
+    constexpr int B_ROWS = tc_b_rows(BN, PAIR);
+    constexpr int B_STAGE = tc_b_stage(BN, PAIR);  // one k-tile of B
+    constexpr uint32_t IDESC = idesc_tf32(BN, false, false, PAIR ? 256 : 128);
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
-    constexpr uint32_t STAGE_BYTES = TC_A_STAGE + B_STAGE;
+    // bytes of one k-tile on the barrier the MMA thread waits on (both CTAs' loads for a pair)
+    constexpr uint32_t KTILE_BYTES = (TC_A_STAGE + B_STAGE) * (PAIR ? 2 : 1);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
-    static_assert(tc_smem_bytes(BN) <= 232448, "shared memory budget exceeded");
+    static_assert(!PAIR || BN >= 64, "a pair splits BN into two halves of at least 32 rows");
+    static_assert(tc_smem_bytes(BN, PAIR) <= 232448, "shared memory budget exceeded");
     constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;   // second accumulator at a power-of-two column offset
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * TC_A_STAGE;
-    uint8_t* sStage = sB + STAGES * B_STAGE;   // 4 x 4 KB epilogue staging, 1024-aligned
+    uint8_t* sB = smem + STAGES * KS * TC_A_STAGE;
+    uint8_t* sStage = sB + STAGES * KS * B_STAGE;   // 4 x 4 KB epilogue staging, 1024-aligned
     uint64_t* full = reinterpret_cast<uint64_t*>(sStage + TC_STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* tmem_full = empty + STAGES;     // [2]
@@ -136,6 +164,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // position in the pair (0 = the CTA that issues the MMAs); work unit walk
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (warp == 4 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -144,7 +176,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tmem_full[b], 1);
-            mbar_init(&tmem_empty[b], 4);   // one arrival per epilogue warp
+            mbar_init(&tmem_empty[b], PAIR ? 8 : 4);   // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(mma_done, 1);
         fence_mbar_init();
@@ -153,13 +185,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (p.store != ST_DIRECT) tma_prefetch_desc(&tmD);
     }
     if (warp == 5) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
+    // this CTA's tile of work unit t
+    auto own_coord = [&](int t) {
+        TileCoord c = tile_coord(t, p);
+        if constexpr (PAIR) c.mt = 2 * c.mt + static_cast<int>(rank);
+        return c;
+    };
 
     // per-tile k range (split-K over z for the weight gradient)
     auto k_range = [&](const TileCoord& tc, int& kt0, int& nkt, int& tap) {
@@ -180,64 +225,98 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool alive = true;
-            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
-                const TileCoord tc = tile_coord(t, p);
+            for (int t = unit0; t < p.num_tiles && alive; t += units) {
+                const TileCoord tc = own_coord(t);
                 int kt0, nkt, tap;
                 k_range(tc, kt0, nkt, tap);
-                const int n0 = tc.nt * BN, m0 = tc.mt * TC_BM;
+                // B rows this CTA loads: all BN, or its half of them in a pair
+                const int n0 = tc.nt * BN + static_cast<int>(rank) * B_ROWS, m0 = tc.mt * TC_BM;
                 int pw0 = 0, ph0 = 0, pn0 = 0;
                 if constexpr (ROLE == ROLE_CONV_IMPL) {
                     pw0 = (tc.mt % p.tiles_w) * p.bw;
                     ph0 = ((tc.mt / p.tiles_w) % p.tiles_h) * p.bh;
                     pn0 = (tc.mt / (p.tiles_w * p.tiles_h)) * p.bimg;
                 }
-                for (int i = 0; i < nkt; ++i, ++it) {
+                for (int i = 0; i < nkt; i += KS, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) {
                         alive = false;
                         break;
                     }
-                    const int kt = kt0 + i;
-                    uint8_t* a_dst = sA + s * TC_A_STAGE;
-                    uint8_t* b_dst = sB + s * B_STAGE;
-                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                    if constexpr (ROLE == ROLE_GEMM_2D) {
-                        tma_load_2d(a_dst, &tmA, kt * TC_BK, m0, &full[s]);
-                        tma_load_2d(b_dst, &tmB, kt * TC_BK, n0, &full[s]);
-                    } else if constexpr (ROLE == ROLE_CONV_IMPL) {
-                        const int tp = kt / p.chunks;
-                        const int c0 = (kt % p.chunks) * TC_BK;
-                        const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
-                        tma_load_4d(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
-                        if (p.b_tap_outer)
-                            tma_load_3d(b_dst, &tmB, c0, n0, tp, &full[s]);
-                        else
-                            tma_load_3d(b_dst, &tmB, c0, tp, n0, &full[s]);
-                    } else {  // CONV_WGRAD: dy^T {Wo*N, Ho, Cout}, x^T {W*N, H, Cin}
-                        const int h = kt / p.tiles_w;
-                        const int c0 = (kt % p.tiles_w) * TC_BK;
-                        tma_load_3d(a_dst, &tmA, c0, h, m0, &full[s]);
-                        tma_load_3d(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
-                                    &full[s]);
+                    const int nq = nkt - i < KS ? nkt - i : KS;   // k-tiles in this stage
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], nq * KTILE_BYTES);
+                    for (int q = 0; q < nq; ++q) {
+                        const int kt = kt0 + i + q;
+                        uint8_t* a_dst = sA + (s * KS + q) * TC_A_STAGE;
+                        uint8_t* b_dst = sB + (s * KS + q) * B_STAGE;
+                        if constexpr (PAIR) {
+                            // both CTAs' copies complete on the even CTA's barrier
+                            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+                            if constexpr (ROLE == ROLE_GEMM_2D) {
+                                tma_load_2d_pair(a_dst, &tmA, kt * TC_BK, m0, bar);
+                                tma_load_2d_pair(b_dst, &tmB, kt * TC_BK, n0, bar);
+                            } else if constexpr (ROLE == ROLE_CONV_IMPL) {
+                                const int tp = kt / p.chunks;
+                                const int c0 = (kt % p.chunks) * TC_BK;
+                                const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
+                                tma_load_4d_pair(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, bar);
+                                if (p.b_tap_outer)
+                                    tma_load_3d_pair(b_dst, &tmB, c0, n0, tp, bar);
+                                else
+                                    tma_load_3d_pair(b_dst, &tmB, c0, tp, n0, bar);
+                            } else {
+                                const int h = kt / p.tiles_w;
+                                const int c0 = (kt % p.tiles_w) * TC_BK;
+                                tma_load_3d_pair(a_dst, &tmA, c0, h, m0, bar);
+                                tma_load_3d_pair(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad,
+                                                 n0, bar);
+                            }
+                        } else if constexpr (ROLE == ROLE_GEMM_2D) {
+                            tma_load_2d(a_dst, &tmA, kt * TC_BK, m0, &full[s]);
+                            tma_load_2d(b_dst, &tmB, kt * TC_BK, n0, &full[s]);
+                        } else if constexpr (ROLE == ROLE_CONV_IMPL) {
+                            const int tp = kt / p.chunks;
+                            const int c0 = (kt % p.chunks) * TC_BK;
+                            const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
+                            tma_load_4d(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
+                            if (p.b_tap_outer)
+                                tma_load_3d(b_dst, &tmB, c0, n0, tp, &full[s]);
+                            else
+                                tma_load_3d(b_dst, &tmB, c0, tp, n0, &full[s]);
+                        } else {  // CONV_WGRAD: dy^T {Wo*N, Ho, Cout}, x^T {W*N, H, Cin}
+                            const int h = kt / p.tiles_w;
+                            const int c0 = (kt % p.tiles_w) * TC_BK;
+                            tma_load_3d(a_dst, &tmA, c0, h, m0, &full[s]);
+                            tma_load_3d(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
+                                        &full[s]);
+                        }
                     }
                 }
+            }
+            // every copy issued above has landed before the CTA (and, for a pair,
+            // its peer, which waits at the final cluster barrier) may exit
+            if (rank == 0) {
+                const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+                for (uint32_t k = first; k < it; ++k)
+                    if (!mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1, p.status, DEV_FLAG_WAIT_PRODUCER))
+                        break;
             }
         }
     } else if (warp == 5) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             uint32_t it = 0, j = 0;
             bool alive = true;
-            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x, ++j) {
-                const TileCoord tc = tile_coord(t, p);
+            for (int t = unit0; t < p.num_tiles && alive; t += units, ++j) {
+                const TileCoord tc = own_coord(t);
                 int kt0, nkt, tap;
                 k_range(tc, kt0, nkt, tap);
                 const uint32_t b = j & 1, tph = (j >> 1) & 1;
                 if (!mbar_wait_bounded(&tmem_empty[b], tph ^ 1, p.status, DEV_FLAG_WAIT_MMA)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * ACC_STRIDE;
-                for (int i = 0; i < nkt; ++i, ++it) {
+                for (int i = 0; i < nkt; i += KS, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait_bounded(&full[s], ph, p.status, DEV_FLAG_WAIT_MMA)) {
@@ -245,22 +324,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + s * TC_A_STAGE);
-                    const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+                    const int nq = nkt - i < KS ? nkt - i : KS;
+                    for (int q = 0; q < nq; ++q) {
+                        const uint32_t a_base = smem_u32(sA + (s * KS + q) * TC_A_STAGE);
+                        const uint32_t b_base = smem_u32(sB + (s * KS + q) * B_STAGE);
 #pragma unroll
-                    for (int kk = 0; kk < TC_BK / 8; ++kk) {
-                        // K-major, 128-byte swizzle: 8 rows of 128 B per 1024-byte group (SBO);
-                        // each K=8 step advances 32 bytes inside the swizzled row.
-                        const uint64_t da = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        const uint64_t db = smem_desc_sw128(b_base + kk * 32, 16, 1024);
-                        mma_tf32(d_tmem, da, db, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < TC_BK / 8; ++kk) {
+                            // K-major, 128-byte swizzle: 8 rows of 128 B per 1024-byte group (SBO);
+                            // each K=8 step advances 32 bytes inside the swizzled row.
+                            const uint64_t da = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                            const uint64_t db = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                            const uint32_t acc = (i > 0 || q > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (PAIR)
+                                mma_tf32_pair(d_tmem, da, db, IDESC, acc);
+                            else
+                                mma_tf32(d_tmem, da, db, IDESC, acc);
+                        }
                     }
-                    mma_commit(&empty[s]);
+                    if constexpr (PAIR)
+                        mma_commit_pair(&empty[s], 0x3);
+                    else
+                        mma_commit(&empty[s]);
                 }
-                mma_commit(&tmem_full[b]);
+                if constexpr (PAIR)
+                    mma_commit_pair(&tmem_full[b], 0x3);
+                else
+                    mma_commit(&tmem_full[b]);
             }
             // every MMA issued above has completed once this commit arrives
-            mma_commit(mma_done);
+            if constexpr (PAIR)
+                mma_commit_pair(mma_done, 0x1);
+            else
+                mma_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, p.status, DEV_FLAG_WAIT_MMA);
         }
         __syncwarp();
@@ -269,8 +364,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint8_t* stage = sStage + warp * 4096;
         bool pending = false;     // a TMA store of this warp may still read `stage`
         uint32_t j = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++j) {
-            const TileCoord tc = tile_coord(t, p);
+        for (int t = unit0; t < p.num_tiles; t += units, ++j) {
+            const TileCoord tc = own_coord(t);
             int kt0, nkt, tap;
             k_range(tc, kt0, nkt, tap);
             const uint32_t b = j & 1, tph = (j >> 1) & 1;
@@ -309,7 +404,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (c + 32 >= BN) {  // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tmem_empty[b]);
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                        else
+                            mbar_arrive(&tmem_empty[b]);
+                    }
                 }
                 const int ncol0 = n0 + c;
                 if (ncol0 >= p.N) continue;  // whole chunk outside the output (warp-uniform)
@@ -429,9 +529,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // neither CTA leaves while the other may still signal it
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
