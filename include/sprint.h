@@ -191,6 +191,29 @@ int sprint_fc_bwd_static_scratch(const float* x, const float* w, const float* wT
 /* Size in bytes of the static scratch array sprint_fc_bwd_static_scratch uses. */
 size_t sprint_fc_bwd_static_scratch_bytes(void);
 
+/* ------------------------------------------------------------------------
+ * Batched FC: `batch` independent problems of one shape in as few launches as
+ * possible — the R logical replicas of one layer ([S] Algorithm 1 runs one
+ * GPU thread per replica; here the replicas of a layer are one grouped
+ * tensor-core launch, each problem with its own weight version).
+ * Every array argument is a HOST array of `batch` device pointers (read during
+ * the call only); problem g uses entry g of each. Each problem computes exactly
+ * what sprint_fc_fwd / sprint_fc_bwd compute for it. Arrays the single-problem
+ * call lets be NULL may be NULL arrays here (b, wT, relu_src, dx, db); entries
+ * of b and relu_src may also be NULL individually. batch = 0 is a no-op.
+ * Problems must not write the same memory. */
+int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b, float* const* y,
+                          int batch, int N, int in, int out, int relu, sprint_stream_t stream);
+
+/* Workspace bytes of sprint_fc_bwd_batched (0 if none needed): `batch` slices
+ * of sprint_fc_workspace_size(N, in, out, have_wT), each rounded up to 256. */
+size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int out, int have_wT);
+
+int sprint_fc_bwd_batched(const float* const* x, const float* const* w, const float* const* wT,
+                          const float* const* dy, const float* const* relu_src, float* const* dx, float* const* dw,
+                          float* const* db, float alpha, int accumulate, int batch, int N, int in, int out, void* ws,
+                          size_t ws_bytes, sprint_stream_t stream);
+
 /* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
  * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must
  * not alias. */
@@ -223,6 +246,13 @@ int sprint_pool_bwd(const float* dy, const uint8_t* argmax, const float* pooled,
  * loss: device fp32 scalar; dlogits: device [N][C] (may alias logits). */
 int sprint_softmax_xent(const float* logits, const int32_t* labels, int N, int C, float* loss, float* dlogits,
                         int reduction_sum, sprint_stream_t stream);
+
+/* The same for `batch` replicas of one shape in one launch (one block per
+ * problem): logits, labels, loss, dlogits are HOST arrays of `batch` device
+ * pointers; problem g writes *loss[g] and dlogits[g]. batch = 0 is a no-op. */
+int sprint_softmax_xent_batched(const float* const* logits, const int32_t* const* labels, float* const* loss,
+                                float* const* dlogits, int batch, int N, int C, int reduction_sum,
+                                sprint_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * GradBuf accumulation — ComputeUpdateVal + UpdateGradient of Algorithm 1:

@@ -40,6 +40,10 @@ enum : int {
     DEV_FLAG_WAIT_EPILOGUE = 4,   // epilogue gave up waiting for the accumulator
 };
 
+// largest number of problems one grouped launch takes (batched entry points
+// split longer lists into launches of this many)
+constexpr int kMaxGroup = 16;
+
 // ---------------------------------------------------------------- device side
 #if defined(__CUDACC__)
 

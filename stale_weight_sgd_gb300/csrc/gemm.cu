@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "tc_gemm.cuh"
 
@@ -17,6 +18,9 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
 int colsum_chunks(long long rows, int cols);
 int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
                      long long dc, cudaStream_t s);
+int launch_transpose_group(const float* const* src, float* const* dst, int G, int R, int C, cudaStream_t s);
+int launch_colsum_group(const float* const* in, float* const* out, int G, long long rows, int cols, float alpha,
+                        int accumulate, cudaStream_t s);
 
 namespace {
 
@@ -72,7 +76,7 @@ struct Tile {
 
 // CTA pairs that can be resident at once for this kernel (clusters are placed
 // within one GPC, so this can be below half the SM count)
-template <int ROLE, int BN>
+template <int ROLE, int BN, int G>
 int pair_slots() {
     static int slots[64] = {};
     int dev = 0;
@@ -91,7 +95,7 @@ int pair_slots() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<ROLE, BN, true>, &cfg) != cudaSuccess || n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<ROLE, BN, true, G>, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
             n = num_sms() / 2;
         }
@@ -100,14 +104,13 @@ int pair_slots() {
     return slots[dev];
 }
 
-template <int ROLE, int BN, bool PAIR>
-int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const TcParams& p,
-                 cudaStream_t s) {
+template <int ROLE, int BN, bool PAIR, int G>
+int launch_tc_bn(const TcMaps<G>& maps, const TcParams& p, cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(tc_gemm_kernel<ROLE, BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tc_gemm_kernel<ROLE, BN, PAIR, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tc_smem_bytes(BN, PAIR)) != cudaSuccess)
             return check_cuda("cudaFuncSetAttribute(tc_gemm_kernel)");
         attr_done[dev] = true;
@@ -115,11 +118,11 @@ int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& 
     if constexpr (!PAIR) {
         // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
         const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-        tc_gemm_kernel<ROLE, BN, false><<<grid, TC_THREADS, tc_smem_bytes(BN, false), s>>>(a, b, d, p);
+        tc_gemm_kernel<ROLE, BN, false, G><<<grid, TC_THREADS, tc_smem_bytes(BN, false), s>>>(maps, p);
         return check_launch("tc_gemm_kernel");
     } else {
         // persistent pairs: at most as many clusters as can be resident together
-        const int slots = pair_slots<ROLE, BN>();
+        const int slots = pair_slots<ROLE, BN, G>();
         const int pairs = p.num_tiles < slots ? p.num_tiles : slots;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -133,15 +136,16 @@ int launch_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& 
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, tc_gemm_kernel<ROLE, BN, true>, a, b, d, p);
+        cudaLaunchKernelEx(&cfg, tc_gemm_kernel<ROLE, BN, true, G>, maps, p);
         return check_launch("tc_gemm_kernel(pair)");
     }
 }
 
 // m_tiles counts 128-row tiles; a pair launch walks ceil(m_tiles / 2) units.
-template <int ROLE>
-int launch_tc(Tile tl, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, TcParams p,
-              long long m_tiles, long long n_tiles, long long z_tiles, cudaStream_t s) {
+// For a grouped launch (G > 1) z_tiles is the number of problems.
+template <int ROLE, int G>
+int launch_tc_maps(Tile tl, const TcMaps<G>& maps, TcParams p, long long m_tiles, long long n_tiles,
+                   long long z_tiles, cudaStream_t s) {
     const long long m_units = tl.pair ? (m_tiles + 1) / 2 : m_tiles;
     const long long tiles = m_units * n_tiles * z_tiles;
     if (tiles <= 0) return SPRINT_OK;
@@ -152,22 +156,32 @@ int launch_tc(Tile tl, const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     p.num_tiles = static_cast<int>(tiles);
     if (tl.pair) {
         switch (tl.bn) {
-            case 64: return launch_tc_bn<ROLE, 64, true>(a, b, d, p, s);
-            case 128: return launch_tc_bn<ROLE, 128, true>(a, b, d, p, s);
-            case 160: return launch_tc_bn<ROLE, 160, true>(a, b, d, p, s);
-            case 192: return launch_tc_bn<ROLE, 192, true>(a, b, d, p, s);
-            case 256: return launch_tc_bn<ROLE, 256, true>(a, b, d, p, s);
+            case 64: return launch_tc_bn<ROLE, 64, true, G>(maps, p, s);
+            case 128: return launch_tc_bn<ROLE, 128, true, G>(maps, p, s);
+            case 160: return launch_tc_bn<ROLE, 160, true, G>(maps, p, s);
+            case 192: return launch_tc_bn<ROLE, 192, true, G>(maps, p, s);
+            case 256: return launch_tc_bn<ROLE, 256, true, G>(maps, p, s);
             default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", tl.bn);
         }
     }
     switch (tl.bn) {
-        case 64: return launch_tc_bn<ROLE, 64, false>(a, b, d, p, s);
-        case 128: return launch_tc_bn<ROLE, 128, false>(a, b, d, p, s);
-        case 160: return launch_tc_bn<ROLE, 160, false>(a, b, d, p, s);
-        case 192: return launch_tc_bn<ROLE, 192, false>(a, b, d, p, s);
-        case 256: return launch_tc_bn<ROLE, 256, false>(a, b, d, p, s);
+        case 64: return launch_tc_bn<ROLE, 64, false, G>(maps, p, s);
+        case 128: return launch_tc_bn<ROLE, 128, false, G>(maps, p, s);
+        case 160: return launch_tc_bn<ROLE, 160, false, G>(maps, p, s);
+        case 192: return launch_tc_bn<ROLE, 192, false, G>(maps, p, s);
+        case 256: return launch_tc_bn<ROLE, 256, false, G>(maps, p, s);
         default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", tl.bn);
     }
+}
+
+template <int ROLE>
+int launch_tc(Tile tl, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, TcParams p,
+              long long m_tiles, long long n_tiles, long long z_tiles, cudaStream_t s) {
+    TcMaps<1> maps;
+    maps.a[0] = a;
+    maps.b[0] = b;
+    maps.d[0] = d;
+    return launch_tc_maps<ROLE, 1>(tl, maps, p, m_tiles, n_tiles, z_tiles, s);
 }
 
 // Picks the tile shape of a persistent launch. Each slot (an SM, or a pair of
@@ -698,6 +712,71 @@ bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int
     return true;
 }
 
+// Grouped form: D_g (epilogue) = A_g . B_g^T for g < G, every problem of the
+// same shape, kMaxGroup problems per launch; per-problem bias / mask / D come
+// from the arrays (bias and mask may be null arrays). Every tensor map is made
+// before the first launch; false if one cannot be (nothing launched then).
+bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B, long long ldb, int M, int N, int K,
+                     TcParams p, const float* const* bias, const float* const* mask, float* const* D, int G,
+                     cudaStream_t s, int* rc) {
+    *rc = SPRINT_OK;
+    if (G <= 0) return true;
+    const long long m_tiles = (M + TC_BM - 1) / TC_BM;
+    const int per_launch = G < kMaxGroup ? G : kMaxGroup;
+    const Tile tl = pick_tile(m_tiles, N, per_launch, N >= 256 ? 256 : (N >= 128 ? 128 : 64));
+    const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 4};
+    const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)ldb * 4};
+    const uint32_t ba[2] = {32, 128}, bb[2] = {32, tl.b_rows()};
+    const uint64_t dd[2] = {(uint64_t)N, (uint64_t)M}, sd[1] = {(uint64_t)p.ldd * 4};
+    const uint32_t bd[2] = {32, 32};
+    bool tma_store = (p.ldd & 3) == 0;
+    for (int g = 0; g < G && tma_store; ++g) tma_store = aligned16(D[g]);
+    const int chunks = (G + kMaxGroup - 1) / kMaxGroup;
+    std::vector<TcMaps<kMaxGroup>> maps(chunks);
+    for (int g = 0; g < G; ++g) {
+        TcMaps<kMaxGroup>& m = maps[g / kMaxGroup];
+        const int i = g % kMaxGroup;
+        if (!make_tmap(&m.a[i], A[g], 2, da, sa, ba) || !make_tmap(&m.b[i], B[g], 2, db, sb, bb)) return false;
+        if (tma_store) {
+            if (!make_tmap(&m.d[i], D[g], 2, dd, sd, bd, false)) return false;
+        } else {
+            m.d[i] = m.a[i];
+        }
+    }
+    p.store = tma_store ? ST_2D : ST_DIRECT;
+    p.M = M;
+    p.N = N;
+    p.num_kt = (K + TC_BK - 1) / TC_BK;
+    p.kt_per_split = p.num_kt;
+    for (int c = 0; c < chunks; ++c) {
+        const int g0 = c * kMaxGroup, n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        for (int i = 0; i < kMaxGroup; ++i) {
+            p.g_bias[i] = (i < n && bias) ? bias[g0 + i] : nullptr;
+            p.g_mask[i] = (i < n && mask) ? mask[g0 + i] : nullptr;
+            p.g_D[i] = i < n ? D[g0 + i] : nullptr;
+        }
+        *rc = launch_tc_maps<ROLE_GEMM_2D, kMaxGroup>(tl, maps[c], p, m_tiles, (N + tl.bn - 1) / tl.bn, n, s);
+        if (*rc) return true;
+    }
+    return true;
+}
+
+// pointer-array arguments of the batched entry points
+int check_ptr_array(const char* fn, const char* what, const void* const* arr, int batch, bool array_nullable,
+                    bool entries_nullable) {
+    if (!arr) {
+        SPRINT_REQUIRE(array_nullable, SPRINT_ERR_INVALID_ARG, "%s: %s is NULL", fn, what);
+        return SPRINT_OK;
+    }
+    for (int g = 0; g < batch; ++g) {
+        SPRINT_REQUIRE(entries_nullable || arr[g], SPRINT_ERR_INVALID_ARG, "%s: %s[%d] is NULL", fn, what, g);
+        SPRINT_REQUIRE(!arr[g] || aligned16(arr[g]), SPRINT_ERR_ALIGN, "%s: %s[%d] not 16-byte aligned", fn, what, g);
+    }
+    return SPRINT_OK;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
 }  // namespace
 }  // namespace sprint
 
@@ -817,6 +896,129 @@ extern "C" int sprint_fc_bwd(const float* x, const float* w, const float* wT, co
     }
     // dedb
     if (db && (rc = launch_colsum(dy, N, out, nullptr, db, alpha, accumulate, s))) return rc;
+    return SPRINT_OK;
+}
+
+// ====================================================================== FC, batched over problems
+extern "C" size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int out, int have_wT) {
+    if (batch < 1 || N < 1 || in < 1 || out < 1) return 0;
+    return static_cast<size_t>(batch) * round256(plan_fc(N, in, out, have_wT != 0).total());
+}
+
+extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b,
+                                     float* const* y, int batch, int N, int in, int out, int relu,
+                                     sprint_stream_t stream) {
+    SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
+                   "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", __func__, batch, N, in, out);
+    if (batch == 0) return SPRINT_OK;
+    int rc;
+    if ((rc = check_ptr_array(__func__, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "b", reinterpret_cast<const void* const*>(b), batch, true, true)) ||
+        (rc = check_ptr_array(__func__, "y", reinterpret_cast<const void* const*>(y), batch, false, false)))
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (batch > 1 && plan_fc(N, in, out, true).fwd_tc) {
+        TcParams p = base_params();
+        p.epi = EPI_STORE;
+        p.ldd = out;
+        p.relu = relu;
+        if (gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc)) return rc;
+    }
+    for (int g = 0; g < batch; ++g)
+        if ((rc = sprint_fc_fwd(x[g], w[g], b ? b[g] : nullptr, y[g], N, in, out, relu, stream))) return rc;
+    return SPRINT_OK;
+}
+
+extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* w, const float* const* wT,
+                                     const float* const* dy, const float* const* relu_src, float* const* dx,
+                                     float* const* dw, float* const* db, float alpha, int accumulate, int batch, int N,
+                                     int in, int out, void* ws, size_t ws_bytes, sprint_stream_t stream) {
+    SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
+                   "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", __func__, batch, N, in, out);
+    if (batch == 0) return SPRINT_OK;
+    int rc;
+    if ((rc = check_ptr_array(__func__, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "wT", reinterpret_cast<const void* const*>(wT), batch, true, false)) ||
+        (rc = check_ptr_array(__func__, "dy", reinterpret_cast<const void* const*>(dy), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "relu_src", reinterpret_cast<const void* const*>(relu_src), batch, true,
+                              true)) ||
+        (rc = check_ptr_array(__func__, "dx", reinterpret_cast<const void* const*>(dx), batch, true, false)) ||
+        (rc = check_ptr_array(__func__, "dw", reinterpret_cast<const void* const*>(dw), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "db", reinterpret_cast<const void* const*>(db), batch, true, false)))
+        return rc;
+    FcPlan pl = plan_fc(N, in, out, wT != nullptr);
+    if (!dx) pl.ws_wT = 0;
+    const size_t per = round256(pl.total());
+    if ((rc = check_ws(__func__, ws, ws_bytes, per * batch))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (batch == 1)
+        return sprint_fc_bwd(x[0], w[0], wT ? wT[0] : nullptr, dy[0], relu_src ? relu_src[0] : nullptr,
+                             dx ? dx[0] : nullptr, dw[0], db ? db[0] : nullptr, alpha, accumulate, N, in, out, ws,
+                             ws_bytes, stream);
+    char* wsb = static_cast<char*>(ws);
+    std::vector<float*> ws_wT(batch), xT(batch), dyT(batch);
+    for (int g = 0; g < batch; ++g) {
+        ws_wT[g] = reinterpret_cast<float*>(wsb + g * per);
+        xT[g] = reinterpret_cast<float*>(wsb + g * per + pl.ws_wT);
+        dyT[g] = reinterpret_cast<float*>(wsb + g * per + pl.ws_wT + pl.ws_xT);
+    }
+
+    // dedx fc: dx_g = mask_g * (dy_g . (w_g^T)^T)
+    if (dx) {
+        bool done = false;
+        if (pl.dx_tc) {
+            const float* const* wt = wT;
+            if (!wt) {
+                if ((rc = launch_transpose_group(w, ws_wT.data(), batch, out, in, s))) return rc;
+                wt = ws_wT.data();
+            }
+            TcParams p = base_params();
+            p.epi = EPI_MASK;
+            p.ldd = in;
+            p.ldm = in;
+            done = gemm2d_tc_group(dy, out, wt, out, N, in, out, p, nullptr, relu_src, dx, batch, s, &rc);
+            if (rc) return rc;
+        }
+        if (!done) {
+            for (int g = 0; g < batch; ++g) {
+                if (out <= 32) {
+                    smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(
+                        dy[g], w[g], relu_src ? relu_src[g] : nullptr, dx[g], N, in, out);
+                    if ((rc = check_launch("smallk_dx_kernel"))) return rc;
+                } else {
+                    SimtGemm q{N, in, out, dy[g], out, 1, w[g], 1, in, dx[g], in, nullptr,
+                               relu_src ? relu_src[g] : nullptr, in, 1.f, 0, 0, SIMT_MASK};
+                    if ((rc = launch_simt_gemm(q, s))) return rc;
+                }
+            }
+        }
+    }
+    // dedw: dw_g = acc*dw_g + alpha * (dy_g^T) . (x_g^T)^T
+    {
+        bool done = false;
+        if (pl.dw_tc) {
+            if ((rc = launch_transpose_group(x, xT.data(), batch, N, in, s))) return rc;
+            if ((rc = launch_transpose_group(dy, dyT.data(), batch, N, out, s))) return rc;
+            TcParams p = base_params();
+            p.epi = EPI_ACCUM;
+            p.ldd = in;
+            p.alpha = alpha;
+            p.accumulate = accumulate;
+            done = gemm2d_tc_group(dyT.data(), N, xT.data(), N, out, in, N, p, nullptr, nullptr, dw, batch, s, &rc);
+            if (rc) return rc;
+        }
+        if (!done) {
+            for (int g = 0; g < batch; ++g) {
+                SimtGemm q{out, in, N, dy[g], 1, out, x[g], 1, in, dw[g], in, nullptr, nullptr, 0, alpha, accumulate,
+                           0, SIMT_ACCUM};
+                if ((rc = launch_simt_gemm(q, s))) return rc;
+            }
+        }
+    }
+    // dedb
+    if (db) return launch_colsum_group(dy, db, batch, N, out, alpha, accumulate, s);
     return SPRINT_OK;
 }
 

@@ -159,6 +159,122 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
     return check_launch("transpose_kernel");
 }
 
+// One launch over up to kMaxGroup problems (blockIdx.z = problem g):
+// out[g] = in[g]^T, in[g] being R x C row-major.
+struct GroupPtrs {
+    const float* in[kMaxGroup];
+    float* out[kMaxGroup];
+};
+
+__global__ void __launch_bounds__(256) transpose_group_kernel(GroupPtrs t, int R, int C) {
+    __shared__ float tile[32][33];
+    const float* __restrict__ src = t.in[blockIdx.z];
+    float* __restrict__ dst = t.out[blockIdx.z];
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int r = r0 + j, c = c0 + tx;
+        if (r < R && c < C) tile[j][tx] = src[static_cast<long long>(r) * C + c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int c = c0 + j, r = r0 + tx;
+        if (r < R && c < C) dst[static_cast<long long>(c) * R + r] = tile[tx][j];
+    }
+}
+
+int launch_transpose_group(const float* const* src, float* const* dst, int G, int R, int C, cudaStream_t s) {
+    if (G <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
+    if ((R + 31) / 32 > 65535) return fail(SPRINT_ERR_SHAPE, "transpose: %d rows exceed the grid limits", R);
+    for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+        const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        GroupPtrs t{};
+        for (int i = 0; i < n; ++i) {
+            t.in[i] = src[g0 + i];
+            t.out[i] = dst[g0 + i];
+        }
+        transpose_group_kernel<<<dim3((C + 31) / 32, (R + 31) / 32, n), 256, 0, s>>>(t, R, C);
+        int rc = check_launch("transpose_group_kernel");
+        if (rc) return rc;
+    }
+    return SPRINT_OK;
+}
+
+// Column sums of up to kMaxGroup row-major [rows][cols] matrices (cols % 4 == 0,
+// one chunk of rows: the FC bias gradient), blockIdx.y = problem; same
+// arithmetic order and epilogue as colsum4_kernel with one chunk.
+__global__ void __launch_bounds__(1024) colsum4_group_kernel(GroupPtrs t, long long rows, int cols, float alpha,
+                                                             int accumulate) {
+    __shared__ float4 red[32][33];
+    const float* __restrict__ in = t.in[blockIdx.y];
+    float* __restrict__ out = t.out[blockIdx.y];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int col = (blockIdx.x * 32 + tx) * 4;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
+    if (col < cols) {
+        const float* base = in + col;
+        long long r = ty;
+        for (; r + 96 < rows; r += 128) {
+            const float4 a = *reinterpret_cast<const float4*>(base + r * cols);
+            const float4 b = *reinterpret_cast<const float4*>(base + (r + 32) * cols);
+            const float4 c = *reinterpret_cast<const float4*>(base + (r + 64) * cols);
+            const float4 d = *reinterpret_cast<const float4*>(base + (r + 96) * cols);
+            s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+            s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
+            s2.x += c.x; s2.y += c.y; s2.z += c.z; s2.w += c.w;
+            s3.x += d.x; s3.y += d.y; s3.z += d.z; s3.w += d.w;
+        }
+        for (; r < rows; r += 32) {
+            const float4 a = *reinterpret_cast<const float4*>(base + r * cols);
+            s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+        }
+    }
+    red[ty][tx] = make_float4(s0.x + s1.x + s2.x + s3.x, s0.y + s1.y + s2.y + s3.y, s0.z + s1.z + s2.z + s3.z,
+                              s0.w + s1.w + s2.w + s3.w);
+    __syncthreads();
+    if (ty == 0 && col < cols) {
+        float4 u = red[0][tx];
+        for (int k = 1; k < 32; ++k) {
+            const float4 v = red[k][tx];
+            u.x += v.x; u.y += v.y; u.z += v.z; u.w += v.w;
+        }
+        float4 o = make_float4(alpha * u.x, alpha * u.y, alpha * u.z, alpha * u.w);
+        if (accumulate) {
+            const float4 prev = *reinterpret_cast<const float4*>(out + col);
+            o.x += prev.x; o.y += prev.y; o.z += prev.z; o.w += prev.w;
+        }
+        *reinterpret_cast<float4*>(out + col) = o;
+    }
+}
+
+// out[g][c] = (accumulate ? out[g][c] : 0) + alpha * sum_r in[g][r][c], one chunk per problem
+int launch_colsum_group(const float* const* in, float* const* out, int G, long long rows, int cols, float alpha,
+                        int accumulate, cudaStream_t s) {
+    bool vec = cols % 4 == 0;
+    for (int g = 0; g < G && vec; ++g) vec = aligned16(in[g]) && aligned16(out[g]);
+    if (!vec) {
+        for (int g = 0; g < G; ++g) {
+            const int rc = launch_colsum(in[g], rows, cols, nullptr, out[g], alpha, accumulate, s);
+            if (rc) return rc;
+        }
+        return SPRINT_OK;
+    }
+    for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+        const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        GroupPtrs t{};
+        for (int i = 0; i < n; ++i) {
+            t.in[i] = in[g0 + i];
+            t.out[i] = out[g0 + i];
+        }
+        colsum4_group_kernel<<<dim3((cols + 127) / 128, n), 1024, 0, s>>>(t, rows, cols, alpha, accumulate);
+        const int rc = check_launch("colsum4_group_kernel");
+        if (rc) return rc;
+    }
+    return SPRINT_OK;
+}
+
 namespace {
 
 // ------------------------------------------------------------------ pooling
@@ -292,9 +408,19 @@ int grid_for(long long work, int threads = 256) {
 // One CTA; warp w handles rows w, w+32, ... Per-row losses are added in row
 // order within a warp and the 32 warp sums in warp order, so the loss is
 // deterministic.
-__global__ void __launch_bounds__(1024) softmax_xent_kernel(const float* logits, const int32_t* __restrict__ labels,
-                                                            int N, int C, float* __restrict__ loss, float* dlogits,
-                                                            float scale) {
+// one problem per block: blockIdx.x selects the replica's tensors
+struct XentTable {
+    const float* logits[kMaxGroup];
+    const int32_t* labels[kMaxGroup];
+    float* loss[kMaxGroup];
+    float* dlogits[kMaxGroup];
+};
+
+__global__ void __launch_bounds__(1024) softmax_xent_kernel(XentTable tab, int N, int C, float scale) {
+    const float* logits = tab.logits[blockIdx.x];
+    const int32_t* __restrict__ labels = tab.labels[blockIdx.x];
+    float* __restrict__ loss = tab.loss[blockIdx.x];
+    float* dlogits = tab.dlogits[blockIdx.x];
     __shared__ float warp_loss[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float acc = 0.f;
@@ -332,9 +458,11 @@ __global__ void __launch_bounds__(1024) softmax_xent_kernel(const float* logits,
 
 // Few classes (C <= 32): one row per thread; per-row losses are added by each
 // warp in row order and the warp sums in warp order (deterministic).
-__global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(const float* logits, const int32_t* __restrict__ labels,
-                                                                 int N, int C, float* __restrict__ loss, float* dlogits,
-                                                                 float scale) {
+__global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(XentTable tab, int N, int C, float scale) {
+    const float* logits = tab.logits[blockIdx.x];
+    const int32_t* __restrict__ labels = tab.labels[blockIdx.x];
+    float* __restrict__ loss = tab.loss[blockIdx.x];
+    float* dlogits = tab.dlogits[blockIdx.x];
     __shared__ float warp_loss[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float acc = 0.f;
@@ -454,6 +582,32 @@ extern "C" int sprint_pool_bwd(const float* dy, const uint8_t* argmax, const flo
     return check_launch(__func__, odd ? 2 : 1);
 }
 
+namespace sprint {
+namespace {
+int launch_xent(const float* const* logits, const int32_t* const* labels, float* const* loss, float* const* dlogits,
+                int G, int N, int C, int reduction_sum, cudaStream_t s) {
+    const float scale = reduction_sum ? 1.f : 1.f / static_cast<float>(N);
+    for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+        const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        XentTable t{};
+        for (int i = 0; i < n; ++i) {
+            t.logits[i] = logits[g0 + i];
+            t.labels[i] = labels[g0 + i];
+            t.loss[i] = loss[g0 + i];
+            t.dlogits[i] = dlogits[g0 + i];
+        }
+        if (C <= 32)
+            softmax_xent_rows_kernel<<<n, 1024, 0, s>>>(t, N, C, scale);
+        else
+            softmax_xent_kernel<<<n, 1024, 0, s>>>(t, N, C, scale);
+        const int rc = check_launch("softmax_xent");
+        if (rc) return rc;
+    }
+    return SPRINT_OK;
+}
+}  // namespace
+}  // namespace sprint
+
 extern "C" int sprint_softmax_xent(const float* logits, const int32_t* labels, int N, int C, float* loss,
                                    float* dlogits, int reduction_sum, sprint_stream_t stream) {
     SPRINT_REQUIRE(N >= 1 && C >= 1, SPRINT_ERR_SHAPE, "%s: need N >= 1 and C >= 1 (got %d, %d)", __func__, N, C);
@@ -465,14 +619,23 @@ extern "C" int sprint_softmax_xent(const float* logits, const int32_t* labels, i
     SPRINT_ALIGNED(labels, "labels");
     SPRINT_ALIGNED(loss, "loss");
     SPRINT_ALIGNED(dlogits, "dlogits");
-    const float scale = reduction_sum ? 1.f : 1.f / static_cast<float>(N);
-    if (C <= 32)
-        softmax_xent_rows_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss,
-                                                                                   dlogits, scale);
-    else
-        softmax_xent_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(logits, labels, N, C, loss, dlogits,
-                                                                              scale);
-    return check_launch(__func__);
+    return launch_xent(&logits, &labels, &loss, &dlogits, 1, N, C, reduction_sum, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int sprint_softmax_xent_batched(const float* const* logits, const int32_t* const* labels, float* const* loss,
+                                           float* const* dlogits, int batch, int N, int C, int reduction_sum,
+                                           sprint_stream_t stream) {
+    SPRINT_REQUIRE(batch >= 0 && N >= 1 && C >= 1, SPRINT_ERR_SHAPE,
+                   "%s: need batch >= 0, N >= 1 and C >= 1 (got %d, %d, %d)", __func__, batch, N, C);
+    if (batch == 0) return SPRINT_OK;
+    SPRINT_REQUIRE(logits && labels && loss && dlogits, SPRINT_ERR_INVALID_ARG, "%s: NULL pointer array", __func__);
+    for (int g = 0; g < batch; ++g) {
+        SPRINT_REQUIRE(logits[g] && labels[g] && loss[g] && dlogits[g], SPRINT_ERR_INVALID_ARG,
+                       "%s: NULL pointer for problem %d", __func__, g);
+        SPRINT_REQUIRE(aligned16(logits[g]) && aligned16(labels[g]) && aligned16(loss[g]) && aligned16(dlogits[g]),
+                       SPRINT_ERR_ALIGN, "%s: pointer of problem %d not 16-byte aligned", __func__, g);
+    }
+    return launch_xent(logits, labels, loss, dlogits, batch, N, C, reduction_sum, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int sprint_im2col(const float* x, int N, int H, int W, int C, int pad, float* col, int32_t* src_index,

@@ -89,6 +89,14 @@ __host__ __device__ constexpr int tc_smem_bytes(int bn, bool pair) {
            256 /* barriers */;
 }
 
+// Up to TC_MAX_GROUP independent GEMMs of one shape in one launch (the work
+// units of problem g have z = g): one tensor-map triple per problem.
+constexpr int TC_MAX_GROUP = kMaxGroup;
+template <int G>
+struct TcMaps {
+    CUtensorMap a[G], b[G], d[G];
+};
+
 struct TcParams {
     int M, N;            // GEMM_2D / CONV_WGRAD: output rows, columns; CONV_IMPL: N = columns
     int m_tiles, n_tiles, z_tiles, num_tiles;  // work units: m fastest, then n, then z (a pair's
@@ -115,6 +123,10 @@ struct TcParams {
     int relu;
     float* partial;      // split-K partial sums [z][M][N] or null
     int* status;
+    // grouped launches: per-problem bias, mask and output (direct stores)
+    const float* g_bias[TC_MAX_GROUP];
+    const float* g_mask[TC_MAX_GROUP];
+    float* g_D[TC_MAX_GROUP];
 };
 
 #if defined(__CUDACC__)
@@ -132,10 +144,10 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& p) {
     return c;
 }
 
-template <int ROLE, int BN, bool PAIR>
+template <int ROLE, int BN, bool PAIR, int G>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const TcParams p) {
+    tc_gemm_kernel(const __grid_constant__ TcMaps<G> maps, const TcParams p) {
+    static_assert(G == 1 || ROLE == ROLE_GEMM_2D, "only plain GEMMs are grouped");
     constexpr int STAGES = tc_stages(BN, PAIR);
     constexpr int KS = tc_ks(BN, PAIR);          // k-tiles per stage
     constexpr int B_ROWS = tc_b_rows(BN, PAIR);
@@ -180,9 +192,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         mbar_init(mma_done, 1);
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        if (p.store != ST_DIRECT) tma_prefetch_desc(&tmD);
+        for (int g = 0; g < G && g < p.z_tiles; ++g) {
+            tma_prefetch_desc(&maps.a[g]);
+            tma_prefetch_desc(&maps.b[g]);
+            if (p.store != ST_DIRECT) tma_prefetch_desc(&maps.d[g]);
+        }
     }
     if (warp == 5) {
         if constexpr (PAIR) {
@@ -208,7 +222,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     // per-tile k range (split-K over z for the weight gradient)
     auto k_range = [&](const TileCoord& tc, int& kt0, int& nkt, int& tap) {
-        int split = tc.z;
+        int split = G > 1 ? 0 : tc.z;   // grouped: z is the problem, not a k split
         tap = 0;
         if constexpr (ROLE == ROLE_CONV_WGRAD) {
             tap = tc.z / p.splits;
@@ -229,6 +243,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const TileCoord tc = own_coord(t);
                 int kt0, nkt, tap;
                 k_range(tc, kt0, nkt, tap);
+                const CUtensorMap* mA = &maps.a[G > 1 ? tc.z : 0];
+                const CUtensorMap* mB = &maps.b[G > 1 ? tc.z : 0];
                 // B rows this CTA loads: all BN, or its half of them in a pair
                 const int n0 = tc.nt * BN + static_cast<int>(rank) * B_ROWS, m0 = tc.mt * TC_BM;
                 int pw0 = 0, ph0 = 0, pn0 = 0;
@@ -254,41 +270,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             // both CTAs' copies complete on the even CTA's barrier
                             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
                             if constexpr (ROLE == ROLE_GEMM_2D) {
-                                tma_load_2d_pair(a_dst, &tmA, kt * TC_BK, m0, bar);
-                                tma_load_2d_pair(b_dst, &tmB, kt * TC_BK, n0, bar);
+                                tma_load_2d_pair(a_dst, mA, kt * TC_BK, m0, bar);
+                                tma_load_2d_pair(b_dst, mB, kt * TC_BK, n0, bar);
                             } else if constexpr (ROLE == ROLE_CONV_IMPL) {
                                 const int tp = kt / p.chunks;
                                 const int c0 = (kt % p.chunks) * TC_BK;
                                 const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
-                                tma_load_4d_pair(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, bar);
+                                tma_load_4d_pair(a_dst, mA, c0, pw0 + dw, ph0 + dh, pn0, bar);
                                 if (p.b_tap_outer)
-                                    tma_load_3d_pair(b_dst, &tmB, c0, n0, tp, bar);
+                                    tma_load_3d_pair(b_dst, mB, c0, n0, tp, bar);
                                 else
-                                    tma_load_3d_pair(b_dst, &tmB, c0, tp, n0, bar);
+                                    tma_load_3d_pair(b_dst, mB, c0, tp, n0, bar);
                             } else {
                                 const int h = kt / p.tiles_w;
                                 const int c0 = (kt % p.tiles_w) * TC_BK;
-                                tma_load_3d_pair(a_dst, &tmA, c0, h, m0, bar);
-                                tma_load_3d_pair(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad,
+                                tma_load_3d_pair(a_dst, mA, c0, h, m0, bar);
+                                tma_load_3d_pair(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad,
                                                  n0, bar);
                             }
                         } else if constexpr (ROLE == ROLE_GEMM_2D) {
-                            tma_load_2d(a_dst, &tmA, kt * TC_BK, m0, &full[s]);
-                            tma_load_2d(b_dst, &tmB, kt * TC_BK, n0, &full[s]);
+                            tma_load_2d(a_dst, mA, kt * TC_BK, m0, &full[s]);
+                            tma_load_2d(b_dst, mB, kt * TC_BK, n0, &full[s]);
                         } else if constexpr (ROLE == ROLE_CONV_IMPL) {
                             const int tp = kt / p.chunks;
                             const int c0 = (kt % p.chunks) * TC_BK;
                             const int dh = (tp / 3 - p.pad) * p.tap_sign, dw = (tp % 3 - p.pad) * p.tap_sign;
-                            tma_load_4d(a_dst, &tmA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
+                            tma_load_4d(a_dst, mA, c0, pw0 + dw, ph0 + dh, pn0, &full[s]);
                             if (p.b_tap_outer)
-                                tma_load_3d(b_dst, &tmB, c0, n0, tp, &full[s]);
+                                tma_load_3d(b_dst, mB, c0, n0, tp, &full[s]);
                             else
-                                tma_load_3d(b_dst, &tmB, c0, tp, n0, &full[s]);
+                                tma_load_3d(b_dst, mB, c0, tp, n0, &full[s]);
                         } else {  // CONV_WGRAD: dy^T {Wo*N, Ho, Cout}, x^T {W*N, H, Cin}
                             const int h = kt / p.tiles_w;
                             const int c0 = (kt % p.tiles_w) * TC_BK;
-                            tma_load_3d(a_dst, &tmA, c0, h, m0, &full[s]);
-                            tma_load_3d(b_dst, &tmB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
+                            tma_load_3d(a_dst, mA, c0, h, m0, &full[s]);
+                            tma_load_3d(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
                                         &full[s]);
                         }
                     }
@@ -372,6 +388,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE)) break;
             tc_fence_after();
             const int n0 = tc.nt * BN, m0 = tc.mt * TC_BM;
+            const CUtensorMap* mD = &maps.d[G > 1 ? tc.z : 0];
+            const float* bias = G > 1 ? p.g_bias[tc.z] : p.bias;
+            const float* mask = G > 1 ? p.g_mask[tc.z] : p.mask;
+            float* Dout = G > 1 ? p.g_D[tc.z] : p.D;
             const int r = warp * 32 + lane;  // tile row = TMEM lane
             // output row of this thread (direct stores, mask loads); -1 if outside
             long long row_off = -1, mask_off = -1;
@@ -421,13 +441,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             float x = o[q];
-                            if (p.bias && ncol0 + q < p.N) x += p.bias[ncol0 + q];
+                            if (bias && ncol0 + q < p.N) x += bias[ncol0 + q];
                             if (p.relu) x = fmaxf(x, 0.f);
                             o[q] = x;
                         }
                     } else if (p.epi == EPI_MASK) {
-                        if (p.mask && mask_off >= 0) {
-                            const float* ms = p.mask + mask_off + ncol0;
+                        if (mask && mask_off >= 0) {
+                            const float* ms = mask + mask_off + ncol0;
                             if (ncol0 + 32 <= p.N && (p.ldm & 3) == 0) {
 #pragma unroll
                                 for (int q = 0; q < 32; q += 4) {
@@ -474,20 +494,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const bool add = (p.epi == EPI_ACCUM) && p.accumulate && !to_partial;
                         if (p.store == ST_2D) {
                             if (add)
-                                tma_reduce_add_2d(&tmD, ncol0, m0 + warp * 32, stage);
+                                tma_reduce_add_2d(mD, ncol0, m0 + warp * 32, stage);
                             else
-                                tma_store_2d(&tmD, ncol0, m0 + warp * 32, stage);
+                                tma_store_2d(mD, ncol0, m0 + warp * 32, stage);
                         } else if (p.store == ST_PIX4D) {
                             const int row0 = warp * 32;
                             const int wo = row0 % p.bw, ho = (row0 / p.bw) % p.bh, no = row0 / (p.bw * p.bh);
-                            tma_store_4d(&tmD, ncol0, pw0 + wo, ph0 + ho, pn0 + no, stage);
+                            tma_store_4d(mD, ncol0, pw0 + wo, ph0 + ho, pn0 + no, stage);
                         } else if (p.store == ST_WGRAD3D) {
                             if (add)
-                                tma_reduce_add_3d(&tmD, ncol0, tap, m0 + warp * 32, stage);
+                                tma_reduce_add_3d(mD, ncol0, tap, m0 + warp * 32, stage);
                             else
-                                tma_store_3d(&tmD, ncol0, tap, m0 + warp * 32, stage);
+                                tma_store_3d(mD, ncol0, tap, m0 + warp * 32, stage);
                         } else {  // ST_PARTIAL3D
-                            tma_store_3d(&tmD, ncol0, m0 + warp * 32, tc.z, stage);
+                            tma_store_3d(mD, ncol0, m0 + warp * 32, tc.z, stage);
                         }
                         bulk_commit();
                     }
@@ -505,7 +525,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 long long col_shift = 0;
                 if constexpr (ROLE == ROLE_CONV_WGRAD) col_shift = static_cast<long long>(tap) * p.N;
-                float* dst = p.D + row_off + col_shift + ncol0;
+                float* dst = Dout + row_off + col_shift + ncol0;
                 const bool vec = (ncol0 + 32 <= p.N) && (p.ldd & 3) == 0;
                 if (p.epi == EPI_ACCUM && p.accumulate) {
 #pragma unroll

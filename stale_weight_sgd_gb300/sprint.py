@@ -52,10 +52,14 @@ _SIGS = {
     "sprint_fc_workspace_size": ([I, I, I, I], SZ),
     "sprint_fc_bwd_static_scratch": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P], I),
     "sprint_fc_bwd_static_scratch_bytes": ([], SZ),
+    "sprint_fc_fwd_batched": ([P, P, P, P, I, I, I, I, I, P], I),
+    "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
+    "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
     "sprint_pool_fwd": ([P, P, P, I, I, I, I, P], I),
     "sprint_pool_bwd": ([P, P, P, P, I, I, I, I, P], I),
     "sprint_softmax_xent": ([P, P, I, I, P, P, I, P], I),
+    "sprint_softmax_xent_batched": ([P, P, P, P, I, I, I, I, P], I),
     "sprint_gradbuf_accumulate": ([P, P, SZ, F, I, P], I),
     "sprint_apply_update_sgd": ([P, P, P, I, SZ, F, P], I),
     "sprint_apply_update_momentum": ([P, P, P, P, I, SZ, F, F, P], I),
@@ -205,6 +209,37 @@ def sprint_gradbuf_accumulate(buf, grad, n, alpha, first, stream=None):
 def _ptr_array(bufs):
     arr = (ctypes.c_void_p * len(bufs))(*[_p(b) for b in bufs])
     return arr
+
+
+def _opt_array(items):
+    """Host pointer array for a batched call, or NULL for None (entries may be None)."""
+    return None if items is None else _ptr_array(items)
+
+
+def sprint_fc_fwd_batched(x, w, b, y, N, fin, fout, relu, stream=None):
+    n = len(x)
+    return _check("sprint_fc_fwd_batched", lib().sprint_fc_fwd_batched(
+        _ptr_array(x), _ptr_array(w), _opt_array(b), _ptr_array(y), n, N, fin, fout, int(relu), _s(stream)))
+
+
+def sprint_fc_batched_workspace_size(batch, N, fin, fout, have_wT) -> int:
+    return lib().sprint_fc_batched_workspace_size(batch, N, fin, fout, int(have_wT))
+
+
+def sprint_fc_bwd_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, fin, fout, ws=None, ws_bytes=0,
+                          stream=None):
+    n = len(x)
+    return _check("sprint_fc_bwd_batched", lib().sprint_fc_bwd_batched(
+        _ptr_array(x), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(relu_src), _opt_array(dx),
+        _ptr_array(dw), _opt_array(db), float(alpha), int(accumulate), n, N, fin, fout, _p(ws), ws_bytes,
+        _s(stream)))
+
+
+def sprint_softmax_xent_batched(logits, labels, loss, dlogits, N, C, reduction_sum=0, stream=None):
+    n = len(logits)
+    return _check("sprint_softmax_xent_batched", lib().sprint_softmax_xent_batched(
+        _ptr_array(logits), _ptr_array(labels), _ptr_array(loss), _ptr_array(dlogits), n, N, C, int(reduction_sum),
+        _s(stream)))
 
 
 def sprint_apply_update_sgd(w_in, w_out, bufs, n, eta, stream=None):

@@ -71,6 +71,31 @@ def test_shape_and_workspace_errors(S):
     assert L.sprint_transpose(16, 16, 4, 4, None) == 1               # aliasing
 
 
+def test_batched_entry_points_validate(S):
+    L = S.lib()
+    f1 = ctypes.c_float(1)
+    ok = (P * 3)(16, 32, 48)
+    mis = (P * 3)(16, 36, 48)
+    nul = (P * 3)(16, None, 48)
+    # batch 0 is a no-op; shapes checked first
+    assert L.sprint_fc_fwd_batched(None, None, None, None, 0, 8, 8, 8, 0, None) == 0
+    assert L.sprint_fc_fwd_batched(ok, ok, None, ok, 3, 0, 8, 8, 0, None) == 2
+    assert L.sprint_fc_fwd_batched(None, ok, None, ok, 3, 8, 8, 8, 0, None) == 1      # NULL array
+    assert L.sprint_fc_fwd_batched(ok, nul, None, ok, 3, 8, 8, 8, 0, None) == 1       # NULL entry
+    assert L.sprint_fc_fwd_batched(ok, ok, mis, ok, 3, 8, 8, 8, 0, None) == 3         # misaligned bias entry
+    assert "b[1]" in S.sprint_last_error()
+    need = S.sprint_fc_batched_workspace_size(3, 64, 256, 512, 0)
+    assert need >= 3 * S.sprint_fc_workspace_size(64, 256, 512, 0)
+    assert S.sprint_fc_batched_workspace_size(0, 64, 256, 512, 0) == 0
+    rc = L.sprint_fc_bwd_batched(ok, ok, None, ok, None, ok, ok, None, f1, 0, 3, 64, 256, 512, 16, need - 16, None)
+    assert rc == 7 and "workspace" in S.sprint_last_error()
+    assert L.sprint_fc_bwd_batched(ok, ok, None, ok, None, ok, None, None, f1, 0, 3, 64, 256, 512, 16, need,
+                                   None) == 1   # dw array is required
+    assert L.sprint_softmax_xent_batched(ok, ok, ok, nul, 3, 8, 10, 0, None) == 1
+    assert L.sprint_softmax_xent_batched(ok, ok, mis, ok, 3, 8, 10, 0, None) == 3
+    assert L.sprint_softmax_xent_batched(None, None, None, None, 0, 8, 10, 0, None) == 0
+
+
 def test_binding_raises_with_message(S):
     with pytest.raises(S.SprintError) as e:
         S.sprint_apply_update_sgd(16, 16, [16] * 17, 10, 0.1, stream=0)

@@ -191,6 +191,88 @@ def test_fc_bwd(S, N, fin, fout, accumulate, with_wT):
     _status_clean(S)
 
 
+# ---------------------------------------------------------------- FC batched over replicas (grouped launches)
+
+FC_BATCHED_CASES = [
+    (3, 300, 200, 136),    # grouped tensor-core launch, ragged tiles
+    (2, 512, 320, 384),    # grouped pair tiles
+    (17, 64, 96, 64),      # more problems than one launch takes
+    (3, 37, 50, 10),       # CUDA-core paths, looped per problem
+    (2, 64, 48, 10),       # grouped tensor-core dW, short-reduction dX
+]
+
+
+def _fc_problem(seed, g, N, fin, fout):
+    x = np.maximum(_f32(seed, f"bx{g}", (N, fin)), 0)
+    w = _f32(seed, f"bw{g}", (fout, fin), np.sqrt(2.0 / fin))
+    b = _f32(seed, f"bb{g}", fout, 0.1)
+    dy = _f32(seed, f"bdy{g}", (N, fout))
+    return x, w, b, dy
+
+
+@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES)
+@pytest.mark.parametrize("relu", [0, 1])
+def test_fc_fwd_batched(S, G, N, fin, fout, relu):
+    probs = [_fc_problem(11, g, N, fin, fout) for g in range(G)]
+    xs = [dev(p[0]) for p in probs]
+    ws = [dev(p[1]) for p in probs]
+    bs = [dev(p[2]) if g % 3 != 1 else None for g, p in enumerate(probs)]   # some problems without bias
+    ys = [torch.empty((N, fout), dtype=torch.float32, device="cuda") for _ in range(G)]
+    S.sprint_fc_fwd_batched(xs, ws, bs, ys, N, fin, fout, relu)
+    for g, (x, w, b, _) in enumerate(probs):
+        ref = O.fc_fwd(x, w, b if g % 3 != 1 else np.zeros_like(b))
+        if relu:
+            ref = O.relu(ref)
+        assert rel_inf(host(ys[g]), ref) <= TOL_TF32, g
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES)
+@pytest.mark.parametrize("with_wT,with_dx", [(0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("accumulate", [0, 1])
+def test_fc_bwd_batched(S, G, N, fin, fout, with_wT, with_dx, accumulate):
+    probs = [_fc_problem(12, g, N, fin, fout) for g in range(G)]
+    alpha = 0.5
+    xs = [dev(p[0]) for p in probs]
+    ws = [dev(p[1]) for p in probs]
+    wTs = [dev(np.ascontiguousarray(p[1].T)) for p in probs] if with_wT else None
+    dys = [dev(p[3]) for p in probs]
+    masks = [xs[g] if g % 2 == 0 else None for g in range(G)]      # odd problems: no ReLU mask
+    dxs = [torch.empty((N, fin), dtype=torch.float32, device="cuda") for _ in range(G)] if with_dx else None
+    dw0 = [_f32(12, f"dw0{g}", (fout, fin)) for g in range(G)]
+    db0 = [_f32(12, f"db0{g}", fout) for g in range(G)]
+    dws = [dev(a) for a in dw0]
+    dbs = [dev(a) for a in db0]
+    nb = S.sprint_fc_batched_workspace_size(G, N, fin, fout, with_wT or not with_dx)
+    wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
+    S.sprint_fc_bwd_batched(xs, ws, wTs, dys, masks, dxs, dws, dbs, alpha, accumulate, N, fin, fout, wsb, nb)
+    for g, (x, w, _, dy) in enumerate(probs):
+        dx_ref, dw_ref, db_ref = O.fc_bwd(x, w, dy)
+        if g % 2 == 0:
+            dx_ref = dx_ref * O.relu_mask(x)
+        dw_ref = O.gradbuf_accumulate(dw0[g], dw_ref, alpha, not accumulate)
+        db_ref = O.gradbuf_accumulate(db0[g], db_ref, alpha, not accumulate)
+        if with_dx:
+            assert rel_inf(host(dxs[g]), dx_ref) <= TOL_TF32, g
+        assert rel_inf(host(dws[g]), dw_ref) <= TOL_TF32, g
+        assert rel_inf(host(dbs[g]), db_ref) <= TOL_FP32, g
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("G,N,C", [(4, 512, 10), (3, 64, 1000), (17, 33, 7)])
+def test_softmax_xent_batched(S, G, N, C):
+    zs = [_f32(13, f"z{g}", (N, C), 3.0) for g in range(G)]
+    ys = [synth.labels(13, f"y{g}", N, C) for g in range(G)]
+    loss = torch.zeros((G, 4), dtype=torch.float32, device="cuda")
+    dz = [torch.empty((N, C), dtype=torch.float32, device="cuda") for _ in range(G)]
+    S.sprint_softmax_xent_batched([dev(z) for z in zs], [dev(y) for y in ys], [loss[g] for g in range(G)], dz, N, C)
+    lh = host(loss)
+    for g in range(G):
+        loss_ref, dz_ref = O.softmax_xent(zs[g], ys[g])
+        assert abs(lh[g, 0] - loss_ref) <= 1e-6 * abs(loss_ref), g
+        assert rel_inf(host(dz[g]), dz_ref) <= TOL_FP32, g
+
+
 # ---------------------------------------------------------------- convolution
 
 CONV_CASES = [
