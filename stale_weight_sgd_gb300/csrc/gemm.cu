@@ -428,6 +428,112 @@ __global__ void pad_cols_kernel(const float* __restrict__ w, int rows, int K, in
     }
 }
 
+// Narrow outputs (N <= 16, e.g. a 10-way classifier), K % 4 == 0, up to
+// kMaxGroup problems per launch (blockIdx.y = problem): a block of 256 threads
+// owns 4 rows of one problem; every thread walks k in float4 steps (stride
+// 256 * 4) for the 4 rows and all N outputs, so each w float4 it loads serves 4
+// rows; partial sums are reduced in a fixed order (warp shuffles, then the 8
+// warps in order).
+struct SkinnyGroup {
+    const float* x[kMaxGroup];
+    const float* w[kMaxGroup];
+    const float* b[kMaxGroup];
+    float* y[kMaxGroup];
+};
+
+template <int NO>
+__global__ void __launch_bounds__(256) skinny4_kernel(SkinnyGroup grp, int M, int N, int K, int relu) {
+    __shared__ float red[8][4][NO];
+    const int g = blockIdx.y;
+    const float* __restrict__ X = grp.x[g];
+    const float* __restrict__ Wt = grp.w[g];
+    const int m0 = blockIdx.x * 4;
+    const int K4 = K >> 2;
+    float acc[4][NO];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int n = 0; n < NO; ++n) acc[r][n] = 0.f;
+    const float4* xr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int m = m0 + r < M ? m0 + r : M - 1;   // rows past M repeat the last row (not stored)
+        xr[r] = reinterpret_cast<const float4*>(X + static_cast<long long>(m) * K);
+    }
+    for (int k4 = threadIdx.x; k4 < K4; k4 += 256) {
+        // every load of this k-step is issued before the first FMA uses one
+        float4 xv[4], wv[NO];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) xv[r] = __ldcs(xr[r] + k4);
+#pragma unroll
+        for (int n = 0; n < NO; ++n)
+            wv[n] = n < N ? __ldg(reinterpret_cast<const float4*>(Wt + static_cast<long long>(n) * K) + k4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int n = 0; n < NO; ++n)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float a = acc[r][n];
+                a = fmaf(xv[r].x, wv[n].x, a);
+                a = fmaf(xv[r].y, wv[n].y, a);
+                a = fmaf(xv[r].z, wv[n].z, a);
+                a = fmaf(xv[r].w, wv[n].w, a);
+                acc[r][n] = a;
+            }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int n = 0; n < NO; ++n) {
+            if (n < N) {
+                float v = acc[r][n];
+#pragma unroll
+                for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) red[warp][r][n] = v;
+            }
+        }
+    __syncthreads();
+    if (threadIdx.x < 4 * NO) {
+        const int r = threadIdx.x / NO, n = threadIdx.x % NO;
+        if (n < N && m0 + r < M) {
+            float t = red[0][r][n];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) t += red[w][r][n];
+            if (grp.b[g]) t += grp.b[g][n];
+            if (relu) t = fmaxf(t, 0.f);
+            grp.y[g][static_cast<long long>(m0 + r) * N + n] = t;
+        }
+    }
+}
+
+// y_g = x_g . w_g^T (+ b_g, ReLU) for narrow outputs (N <= 16, K % 4 == 0)
+int launch_skinny4(const float* const* x, const float* const* w, const float* const* b, float* const* y, int G,
+                   int M, int N, int K, int relu, cudaStream_t s) {
+    for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+        const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        SkinnyGroup t{};
+        for (int i = 0; i < n; ++i) {
+            t.x[i] = x[g0 + i];
+            t.w[i] = w[g0 + i];
+            t.b[i] = b ? b[g0 + i] : nullptr;
+            t.y[i] = y[g0 + i];
+        }
+        const dim3 grid((M + 3) / 4, n);
+        if (N <= 4)
+            skinny4_kernel<4><<<grid, 256, 0, s>>>(t, M, N, K, relu);
+        else if (N <= 8)
+            skinny4_kernel<8><<<grid, 256, 0, s>>>(t, M, N, K, relu);
+        else if (N <= 10)
+            skinny4_kernel<10><<<grid, 256, 0, s>>>(t, M, N, K, relu);
+        else
+            skinny4_kernel<kSkinnyN><<<grid, 256, 0, s>>>(t, M, N, K, relu);
+        const int rc = check_launch("skinny4_kernel");
+        if (rc) return rc;
+    }
+    return SPRINT_OK;
+}
+
 // dx[m][n] = mask(m, n) * sum_{k < K} dy[m][k] * w[k][n] for a short reduction
 // (K <= 32, e.g. the input gradient of a 10-way classifier): one thread per
 // output, dy row broadcast within the warp, w read coalesced along n.
@@ -448,6 +554,83 @@ __global__ void __launch_bounds__(256) smallk_dx_kernel(const float* __restrict_
         for (int k = 0; k < K; ++k) acc = fmaf(d[k], w[static_cast<long long>(k) * N + n], acc);
         dx[idx] = acc;
     }
+}
+
+// Grouped form for N % 4 == 0 (blockIdx.y = problem): a thread computes 4
+// consecutive outputs of one row from the row's K dy values (broadcast) and K
+// float4 loads of w, all issued before the FMAs.
+struct SmallkGroup {
+    const float* dy[kMaxGroup];
+    const float* w[kMaxGroup];
+    const float* mask[kMaxGroup];
+    float* dx[kMaxGroup];
+};
+
+template <int KM>
+__global__ void __launch_bounds__(256) smallk_dx4_kernel(SmallkGroup grp, int M, int N, int K) {
+    const int g = blockIdx.y;
+    const float* __restrict__ dy = grp.dy[g];
+    const float4* __restrict__ w4 = reinterpret_cast<const float4*>(grp.w[g]);
+    const float* __restrict__ mask = grp.mask[g];
+    float4* __restrict__ dx4 = reinterpret_cast<float4*>(grp.dx[g]);
+    const int N4 = N >> 2;
+    const long long total = static_cast<long long>(M) * N4;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int n4 = static_cast<int>(idx % N4);
+        const long long m = idx / N4;
+        float d[KM];
+        float4 wv[KM];
+#pragma unroll
+        for (int k = 0; k < KM; ++k) {
+            d[k] = k < K ? dy[m * K + k] : 0.f;
+            wv[k] = k < K ? __ldg(w4 + static_cast<long long>(k) * N4 + n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4 mk = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (mask) mk = __ldcs(reinterpret_cast<const float4*>(mask) + idx);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < KM; ++k) {
+            a.x = fmaf(d[k], wv[k].x, a.x);
+            a.y = fmaf(d[k], wv[k].y, a.y);
+            a.z = fmaf(d[k], wv[k].z, a.z);
+            a.w = fmaf(d[k], wv[k].w, a.w);
+        }
+        a.x = mk.x > 0.f ? a.x : 0.f;
+        a.y = mk.y > 0.f ? a.y : 0.f;
+        a.z = mk.z > 0.f ? a.z : 0.f;
+        a.w = mk.w > 0.f ? a.w : 0.f;
+        __stcs(dx4 + idx, a);
+    }
+}
+
+// dx_g = mask_g * (dy_g . w_g) for K <= 32, N % 4 == 0, all problems in as few launches as possible
+int launch_smallk_dx4(const float* const* dy, const float* const* w, const float* const* mask, float* const* dx,
+                      int G, int M, int N, int K, cudaStream_t s) {
+    const long long total = static_cast<long long>(M) * (N / 4);
+    long long blocks = (total + 255) / 256;
+    const long long cap = 8ll * num_sms();
+    if (blocks > cap) blocks = cap;
+    for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+        const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+        SmallkGroup t{};
+        for (int i = 0; i < n; ++i) {
+            t.dy[i] = dy[g0 + i];
+            t.w[i] = w[g0 + i];
+            t.mask[i] = mask ? mask[g0 + i] : nullptr;
+            t.dx[i] = dx[g0 + i];
+        }
+        const dim3 grid(static_cast<unsigned>(blocks), n);
+        if (K <= 8)
+            smallk_dx4_kernel<8><<<grid, 256, 0, s>>>(t, M, N, K);
+        else if (K <= 16)
+            smallk_dx4_kernel<16><<<grid, 256, 0, s>>>(t, M, N, K);
+        else
+            smallk_dx4_kernel<32><<<grid, 256, 0, s>>>(t, M, N, K);
+        const int rc = check_launch("smallk_dx4_kernel");
+        if (rc) return rc;
+    }
+    return SPRINT_OK;
 }
 
 // direct convolution, one thread per output element (co fastest)
@@ -658,10 +841,21 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     const long long m_units = pl.tile.pair ? (m_tiles + 1) / 2 : m_tiles;
     const long long slots = pl.tile.pair ? num_sms() / 2 : num_sms();
     const long long base = m_units * ((Cin + pl.tile.bn - 1) / pl.tile.bn) * 9;
-    long long want = (2ll * slots + base - 1) / base;
+    // split count: fewest (rounds of units) x (k-tiles per unit), counting each
+    // split's partial-sum write and read as ~8 k-tiles of work; splits keep >= 8 k-tiles
     long long maxs = pl.num_kt / 8;
-    if (want > maxs) want = maxs;
-    if (want < 1) want = 1;
+    if (maxs < 1) maxs = 1;
+    long long want = 1;
+    double best = 1e300;
+    for (long long sp = 1; sp <= maxs && sp <= 4 * slots; ++sp) {
+        const long long per = (pl.num_kt + sp - 1) / sp;
+        const long long rounds = (base * sp + slots - 1) / slots;
+        const double cost = static_cast<double>(rounds) * (per + (sp > 1 ? 8 : 0));
+        if (cost < best - 1e-9) {
+            best = cost;
+            want = sp;
+        }
+    }
     pl.kt_per_split = static_cast<int>((pl.num_kt + want - 1) / want);
     pl.splits = (pl.num_kt + pl.kt_per_split - 1) / pl.kt_per_split;
     if (pl.splits > 1) pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * 9 * Cout * Cin);
@@ -812,6 +1006,7 @@ extern "C" int sprint_fc_fwd(const float* x, const float* w, const float* b, flo
         if (gemm2d_tc(x, in, w, in, N, out, in, p, s, &rc)) return rc;
     }
     if (out <= kSkinnyN) {
+        if (in % 4 == 0) return launch_skinny4(&x, &w, &b, &y, 1, N, out, in, relu, s);
         skinny_nt_kernel<<<(N + 1) / 2, 256, 0, s>>>(x, in, w, in, b, y, out, N, out, in, relu);
         return check_launch("skinny_nt_kernel");
     }
@@ -865,8 +1060,14 @@ extern "C" int sprint_fc_bwd(const float* x, const float* w, const float* wT, co
             if (rc) return rc;
         }
         if (!done && out <= 32) {
-            smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(dy, w, relu_src, dx, N, in, out);
-            if ((rc = check_launch("smallk_dx_kernel"))) return rc;
+            if (in % 4 == 0) {
+                if ((rc = launch_smallk_dx4(&dy, &w, relu_src ? &relu_src : nullptr, &dx, 1, N, in, out, s)))
+                    return rc;
+            } else {
+                smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(dy, w, relu_src, dx, N,
+                                                                                         in, out);
+                if ((rc = check_launch("smallk_dx_kernel"))) return rc;
+            }
             done = true;
         }
         if (!done) {
@@ -925,6 +1126,7 @@ extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* 
         p.relu = relu;
         if (gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc)) return rc;
     }
+    if (out <= kSkinnyN && in % 4 == 0) return launch_skinny4(x, w, b, y, batch, N, out, in, relu, s);
     for (int g = 0; g < batch; ++g)
         if ((rc = sprint_fc_fwd(x[g], w[g], b ? b[g] : nullptr, y[g], N, in, out, relu, stream))) return rc;
     return SPRINT_OK;
@@ -980,6 +1182,10 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
             p.ldm = in;
             done = gemm2d_tc_group(dy, out, wt, out, N, in, out, p, nullptr, relu_src, dx, batch, s, &rc);
             if (rc) return rc;
+        }
+        if (!done && out <= 32 && in % 4 == 0) {
+            if ((rc = launch_smallk_dx4(dy, w, relu_src, dx, batch, N, in, out, s))) return rc;
+            done = true;
         }
         if (!done) {
             for (int g = 0; g < batch; ++g) {

@@ -249,11 +249,53 @@ __global__ void __launch_bounds__(1024) colsum4_group_kernel(GroupPtrs t, long l
     }
 }
 
+// Narrow column sums (cols <= 16, e.g. a classifier's bias gradient), one
+// block per problem (blockIdx.x): thread t adds rows t, t+256, ... for every
+// column, then the 256 partial sums of a column are added in thread order.
+__global__ void __launch_bounds__(256) colsum_narrow_group_kernel(GroupPtrs t, long long rows, int cols, float alpha,
+                                                                  int accumulate) {
+    __shared__ float red[16][257];
+    const float* __restrict__ in = t.in[blockIdx.x];
+    float* __restrict__ out = t.out[blockIdx.x];
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+    for (long long r = threadIdx.x; r < rows; r += 256) {
+        const float* row = in + r * cols;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            if (c < cols) acc[c] += row[c];
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) red[c][threadIdx.x] = acc[c];
+    __syncthreads();
+    if (threadIdx.x < cols) {
+        const int c = threadIdx.x;
+        float s = 0.f;
+        for (int i = 0; i < 256; ++i) s += red[c][i];
+        out[c] = (accumulate ? out[c] : 0.f) + alpha * s;
+    }
+}
+
 // out[g][c] = (accumulate ? out[g][c] : 0) + alpha * sum_r in[g][r][c], one chunk per problem
 int launch_colsum_group(const float* const* in, float* const* out, int G, long long rows, int cols, float alpha,
                         int accumulate, cudaStream_t s) {
     bool vec = cols % 4 == 0;
     for (int g = 0; g < G && vec; ++g) vec = aligned16(in[g]) && aligned16(out[g]);
+    if (!vec && cols <= 16) {
+        for (int g0 = 0; g0 < G; g0 += kMaxGroup) {
+            const int n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
+            GroupPtrs t{};
+            for (int i = 0; i < n; ++i) {
+                t.in[i] = in[g0 + i];
+                t.out[i] = out[g0 + i];
+            }
+            colsum_narrow_group_kernel<<<n, 256, 0, s>>>(t, rows, cols, alpha, accumulate);
+            const int rc = check_launch("colsum_narrow_group_kernel");
+            if (rc) return rc;
+        }
+        return SPRINT_OK;
+    }
     if (!vec) {
         for (int g = 0; g < G; ++g) {
             const int rc = launch_colsum(in[g], rows, cols, nullptr, out[g], alpha, accumulate, s);

@@ -20,15 +20,27 @@ blog summary: replicas fetch w, push dw, the server applies w' := w - eta*dw):
     version, written once when the version is created and shared by every
     replica that reads that version;
   * the update sums the R GradBufs in replica order and applies SGD, momentum
-    or Adagrad (Algorithm 2; one fused kernel).
+    or Adagrad (Algorithm 2; one fused kernel per layer).
 
+Execution is layer-major: the R replicas of a layer are one batch of
+problems. An FC layer is one grouped tensor-core launch for all replicas
+(each problem with its own weight version); a convolution runs replica after
+replica (each already fills the GPU); the softmax of all replicas is one
+launch. All of it is issued on one stream. The update is split by layer: as
+soon as the backward pass of layer l has finished for every replica, a second
+stream applies the update of layer l (and writes its W^T) while the backward
+pass of the layers below runs, so only the update of the first layer remains
+between two steps. Per-layer events order everything else:
+  * the forward pass of layer l at step t waits for the newest version of
+    layer l that any replica reads;
+  * the backward pass of layer l at step t waits for version t-1 of layer l,
+    i.e. for update t-2, the last reader of GradBuf set t mod 2 (GradBufs
+    are double-buffered by step parity);
+  * the update of layer l at step t overwrites ring slot (t+1) mod (S+1),
+    whose version t-S is read by nobody once layer l's backward pass of step
+    t is done.
 Replica r draws batch (t*R + r) mod P from a pool of P device-resident
-batches. Replicas run on their own CUDA streams (independent work that fills
-the GPU together); the update of step t waits for all of them. A replica of
-step t waits only for the newest weight version it reads (so a replica with
-delay >= 1 need not wait for update t-1) and for update t-2, the last reader
-of its GradBuf set: GradBufs are double-buffered by step parity. Nothing here
-computes: every operation is a libsprint call.
+batches. Nothing here computes: every operation is a libsprint call.
 """
 from __future__ import annotations
 
@@ -43,6 +55,8 @@ class StaleSGD:
     def __init__(self, net, batch, *, replicas=1, max_delay=0, schedule_seed=0, stage_of_layer=None,
                  stage_delays=None, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, concurrent=True,
                  device="cuda"):
+        """concurrent: run the per-layer updates on a second stream, overlapping
+        the rest of the backward pass (False: everything on one stream)."""
         S.lib()  # fail loudly if the CUDA library is missing
         self.net = net
         self.shapes = layer_shapes(net)
@@ -76,19 +90,31 @@ class StaleSGD:
         else:
             raise ValueError(optimizer)
         self.loss = torch.zeros((self.R, 4), **f32)  # row r, column 0 = replica r's loss
-
-        # per-replica activations, saved for the backward pass
-        self.acts = [self._alloc_acts() for _ in range(self.R)]
         self.classes = self.shapes[-1].cout
+        # parameter span of each layer (W then b, padded): the per-layer update range
+        ends = [L.w_off for L in self.shapes[1:]] + [self.n]
+        self.span = [(L.w_off, e - L.w_off) for L, e in zip(self.shapes, ends)]
+        self._alloc_acts()
 
         main = torch.cuda.current_stream(self.dev)
         self.main_stream = main
-        self.streams = [torch.cuda.Stream(self.dev) for _ in range(self.R)] if concurrent else [main] * self.R
-        self.ev_update = torch.cuda.Event()      # the latest update has finished
-        self.ev_done = [torch.cuda.Event() for _ in range(self.R)]
-        self.ev_ver = [torch.cuda.Event() for _ in range(self.S + 3)]  # version v exists: ev_ver[v % (S+3)]
-        self.ev_update.record(main)
-        self.ev_ver[0].record(main)
+        self.upd_stream = torch.cuda.Stream(self.dev) if concurrent else main
+        # convolutions of different replicas run side by side (each with its own
+        # workspace): the small late layers alone leave most SMs idle
+        self.fork = concurrent and self.R > 1 and any(L.kind == "conv" for L in self.shapes)
+        if self.fork:
+            self.rep_streams = [torch.cuda.Stream(self.dev) for _ in range(self.R)]
+            self.rep_ws = [torch.empty(max(self.conv_ws_bytes // 4 + 64, 64), **f32) for _ in range(self.R)]
+            self.ev_fork = torch.cuda.Event()
+            self.ev_join = [torch.cuda.Event() for _ in range(self.R)]
+        else:
+            self.rep_streams = [main] * self.R
+            self.rep_ws = [self.ws] * self.R
+        self.K = self.S + 3   # version v of layer l exists: ev_layer[l][v % K]
+        self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
+        self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
+        for evs in self.ev_layer:
+            evs[0].record(main)
         self.ev_inputs = torch.cuda.Event()
         self.inputs_pending = False
         self._sched = np.zeros((0, self.R), np.int32)
@@ -98,49 +124,69 @@ class StaleSGD:
 
     # ------------------------------------------------------------------ buffers
     def _alloc_acts(self):
+        """Per layer one [R][...] tensor (replica r's slice is row r), the
+        gradient ping-pong pair [R][big], and one workspace for the largest call."""
         f32 = dict(dtype=torch.float32, device=self.dev)
-        outs, pooled, argmax = [], [], []
-        big = 0       # largest activation / gradient tensor (elements)
-        ws_bytes = 0  # largest workspace any call of this replica needs
+        R, N = self.R, self.N
+
+        def rows(numel, dtype=torch.float32):
+            # [R][numel] with each replica's row starting on a 256-byte boundary
+            stride = (numel + 255) // 256 * 256
+            return torch.empty((R, stride), dtype=dtype, device=self.dev)[:, :numel]
+
+        self.outs, self.pooled, self.argmax = [], [], []
+        big = 0
+        ws_bytes = 0
+        conv_ws = 0
         for L in self.shapes:
             if L.kind == "conv":
-                numel = self.N * L.h * L.w * L.cout
-                big = max(big, numel, self.N * L.h * L.w * L.cin)
-                outs.append(torch.empty(numel, **f32))
+                numel = N * L.h * L.w * L.cout
+                big = max(big, numel, N * L.h * L.w * L.cin)
+                self.outs.append(rows(numel))
                 if L.pool:
                     ph, pw = L.out_hw
-                    pooled.append(torch.empty(self.N * ph * pw * L.cout, **f32))
-                    argmax.append(torch.empty(self.N * ph * pw * L.cout, dtype=torch.uint8, device=self.dev))
+                    self.pooled.append(rows(N * ph * pw * L.cout))
+                    self.argmax.append(rows(N * ph * pw * L.cout, torch.uint8))
                 else:
-                    pooled.append(None)
-                    argmax.append(None)
+                    self.pooled.append(None)
+                    self.argmax.append(None)
                 for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX, S.SPRINT_CONV_DW):
-                    ws_bytes = max(ws_bytes, S.sprint_conv_workspace_size(op, self.N, L.h, L.w, L.cin, L.cout, 1))
+                    conv_ws = max(conv_ws, S.sprint_conv_workspace_size(op, N, L.h, L.w, L.cin, L.cout, 1))
             else:
-                numel = self.N * L.cout
-                big = max(big, numel, self.N * L.cin)
-                outs.append(torch.empty(numel, **f32))
-                pooled.append(None)
-                argmax.append(None)
-                ws_bytes = max(ws_bytes, S.sprint_fc_workspace_size(self.N, L.cin, L.cout, 1))
-        g = [torch.empty(big, **f32), torch.empty(big, **f32)]
-        ws = torch.empty(max(ws_bytes // 4 + 64, 64), **f32)
-        return dict(outs=outs, pooled=pooled, argmax=argmax, g=g, ws=ws, ws_bytes=ws.numel() * 4)
+                numel = N * L.cout
+                big = max(big, numel, N * L.cin)
+                self.outs.append(rows(numel))
+                self.pooled.append(None)
+                self.argmax.append(None)
+                ws_bytes = max(ws_bytes, S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 1),
+                               S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 0))
+        self.g = rows(big)
+        self.h = rows(big)
+        self.ws = torch.empty(max(max(ws_bytes, conv_ws) // 4 + 64, 64), **f32)
+        self.ws_bytes = self.ws.numel() * 4
+        self.conv_ws_bytes = conv_ws
+        # per-replica views (what a replica's pass reads and writes)
+        self.acts = [dict(outs=[o[r] for o in self.outs],
+                          pooled=[p[r] if p is not None else None for p in self.pooled],
+                          argmax=[a[r] if a is not None else None for a in self.argmax])
+                     for r in range(R)]
 
     # ------------------------------------------------------------------ data / weights
     def load_weights(self, dense: np.ndarray):
         """Sets W(0) from a dense [W0 b0 W1 b1 ...] fp32 vector."""
+        torch.cuda.synchronize(self.dev)
         w = torch.from_numpy(pack(self.shapes, np.asarray(dense, np.float32)))
         self.ring[0].copy_(w.to(self.dev))
-        self._transpose_slot(0, self.main_stream)
+        for li in range(1, len(self.shapes)):
+            self._transpose_layer(li, 0, self.main_stream)
         if self.optimizer == "momentum":
             self.opt_state.zero_()
         elif self.optimizer == "adagrad":
             self.opt_state.fill_(self.g0)
         self.t = 0
         torch.cuda.synchronize(self.dev)
-        self.ev_update.record(self.main_stream)
-        self.ev_ver[0].record(self.main_stream)
+        for evs in self.ev_layer:
+            evs[0].record(self.main_stream)
 
     def load_batches(self, batches):
         """Uploads the pool of (x, labels) batches; x is NHWC (or [N][features])."""
@@ -155,8 +201,8 @@ class StaleSGD:
         self.batches_y = y
 
     def mark_inputs(self, stream):
-        """The batch pool was (re)written on `stream`: the next step's replicas
-        wait for that work before reading it."""
+        """The batch pool was (re)written on `stream`: the next step waits for
+        that work before reading it."""
         self.ev_inputs.record(stream)
         self.inputs_pending = True
 
@@ -166,13 +212,13 @@ class StaleSGD:
         torch.cuda.synchronize(self.dev)
         return unpack(self.shapes, self.ring[v % (self.S + 1)].cpu().numpy())
 
-    def _transpose_slot(self, slot, stream):
-        """W^T of every layer after the first (they need dE/dX) into ringT[slot]."""
-        src = self.ring[slot].data_ptr()
-        dst = self.ringT[slot].data_ptr()
-        for L in self.shapes[1:]:
-            rows, cols = (L.cout, 9 * L.cin) if L.kind == "conv" else (L.cout, L.cin)
-            S.sprint_transpose(src + 4 * L.w_off, dst + 4 * L.w_off, rows, cols, stream.cuda_stream)
+    def _transpose_layer(self, li, slot, stream):
+        """W_l^T of version slot `slot` into ringT (layers after the first need dE/dX)."""
+        L = self.shapes[li]
+        rows, cols = (L.cout, 9 * L.cin) if L.kind == "conv" else (L.cout, L.cin)
+        src = self.ring[slot].data_ptr() + 4 * L.w_off
+        dst = self.ringT[slot].data_ptr() + 4 * L.w_off
+        S.sprint_transpose(src, dst, rows, cols, stream.cuda_stream)
 
     def schedule(self, steps) -> np.ndarray:
         if self._sched.shape[0] < steps:
@@ -187,107 +233,154 @@ class StaleSGD:
         s = int(self.schedule(t + 1)[t, r]) if self.S > 0 else 0
         return max(0, t - s)
 
-    def _replica(self, t, r, stream):
-        """Forward, softmax cross-entropy and backward of replica r (Algorithm 1)."""
-        A = self.acts[r]
-        N = self.N
-        ring_ptr = self.ring.data_ptr()
-        row = self.n * 4
-        gb = self.gradbuf_sets[t % 2][r].data_ptr()
-        bi = (t * self.R + r) % self.batches_x.shape[0]
-        x = self.batches_x[bi]
-        y = self.batches_y[bi]
-        ringT_ptr = self.ringT.data_ptr()
-        wptr, wtptr = [], []
-        for li, L in enumerate(self.shapes):
-            slot = self._version(t, r, li) % (self.S + 1)
-            base = ring_ptr + slot * row
-            wptr.append((base + 4 * L.w_off, base + 4 * L.b_off))
-            wtptr.append(ringT_ptr + slot * row + 4 * L.w_off)
-        ws, wsb = A["ws"], A["ws_bytes"]
+    def _update_layer(self, t, li, stream):
+        """SumGradient + UpdateWeights (Algorithm 2) of layer li: W_l(t+1) into
+        ring slot t+1, then its transpose."""
+        off, cnt = self.span[li]
+        slot_in, slot_out = t % (self.S + 1), (t + 1) % (self.S + 1)
+        w_in = self.ring[slot_in].data_ptr() + 4 * off
+        w_out = self.ring[slot_out].data_ptr() + 4 * off
+        bufs = [self.gradbuf_sets[t % 2][r].data_ptr() + 4 * off for r in range(self.R)]
         sh = stream.cuda_stream
+        if self.optimizer == "sgd":
+            S.sprint_apply_update_sgd(w_in, w_out, bufs, cnt, self.eta, sh)
+        elif self.optimizer == "momentum":
+            S.sprint_apply_update_momentum(w_in, w_out, self.opt_state.data_ptr() + 4 * off, bufs, cnt, self.eta,
+                                           self.nu, sh)
+        else:
+            S.sprint_apply_update_adagrad(w_in, w_out, self.opt_state.data_ptr() + 4 * off, bufs, cnt, self.eta,
+                                          self.eps, sh)
+        if li > 0:
+            self._transpose_layer(li, slot_out, stream)
+
+    def _per_replica(self, fn):
+        """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica
+        streams (forked from and joined back into the main stream) or in order
+        on the main stream."""
+        main = self.main_stream
+        if not self.fork:
+            for r in range(self.R):
+                fn(r, main.cuda_stream, self.ws, self.ws_bytes)
+            return
+        self.ev_fork.record(main)
+        for r in range(self.R):
+            st = self.rep_streams[r]
+            st.wait_event(self.ev_fork)
+            fn(r, st.cuda_stream, self.rep_ws[r], self.rep_ws[r].numel() * 4)
+            self.ev_join[r].record(st)
+        for r in range(self.R):
+            main.wait_event(self.ev_join[r])
+
+    def step(self):
+        """One global step: every replica's gradient, then the update, layer by
+        layer. Asynchronous."""
+        t, R, N, K = self.t, self.R, self.N, self.K
+        main, upd = self.main_stream, self.upd_stream
+        sh = main.cuda_stream
+        nL = len(self.shapes)
+        row = self.n * 4
+        ring, ringT = self.ring.data_ptr(), self.ringT.data_ptr()
+        ver = [[self._version(t, r, li) for li in range(nL)] for r in range(R)]
+        slot = [[v % (self.S + 1) for v in vr] for vr in ver]
+        gb = [self.gradbuf_sets[t % 2][r].data_ptr() for r in range(R)]
+        P = self.batches_x.shape[0]
+        bidx = [(t * R + r) % P for r in range(R)]
+        if self.inputs_pending:
+            main.wait_event(self.ev_inputs)
+            self.inputs_pending = False
+        ws, wsb = self.ws, self.ws_bytes
+
+        def W(r, li):
+            return ring + slot[r][li] * row + 4 * self.shapes[li].w_off
+
+        def B(r, li):
+            return ring + slot[r][li] * row + 4 * self.shapes[li].b_off
+
+        def WT(r, li):
+            return ringT + slot[r][li] * row + 4 * self.shapes[li].w_off
 
         # forward
-        inp = [None] * len(self.shapes)
-        cur = x.data_ptr()
+        cur = [self.batches_x[b].data_ptr() for b in bidx]
+        inp = [None] * nL
         for li, L in enumerate(self.shapes):
+            main.wait_event(self.ev_layer[li][max(ver[r][li] for r in range(R)) % K])
             inp[li] = cur
-            out = A["outs"][li]
+            outs = [self.outs[li][r].data_ptr() for r in range(R)]
             if L.kind == "conv":
-                S.sprint_conv_fwd(cur, wptr[li][0], wptr[li][1], out, N, L.h, L.w, L.cin, L.cout, 1, 1, ws, wsb, sh)
-                if L.pool:
-                    S.sprint_pool_fwd(out, A["pooled"][li], A["argmax"][li], N, L.h, L.w, L.cout, sh)
-                    cur = A["pooled"][li].data_ptr()
-                else:
-                    cur = out.data_ptr()
+                def fwd(r, st, rws, rwsb, li=li, L=L, src=cur, outs=outs):
+                    S.sprint_conv_fwd(src[r], W(r, li), B(r, li), outs[r], N, L.h, L.w, L.cin, L.cout, 1, 1, rws,
+                                      rwsb, st)
+                    if L.pool:
+                        S.sprint_pool_fwd(outs[r], self.pooled[li][r], self.argmax[li][r], N, L.h, L.w, L.cout, st)
+                self._per_replica(fwd)
+                cur = [self.pooled[li][r].data_ptr() for r in range(R)] if L.pool else outs
             else:
-                S.sprint_fc_fwd(cur, wptr[li][0], wptr[li][1], out, N, L.cin, L.cout, int(L.relu), sh)
-                cur = out.data_ptr()
-        g, h = A["g"]
-        S.sprint_softmax_xent(cur, y, N, self.classes, self.loss[r], g, 0, sh)
+                S.sprint_fc_fwd_batched(cur, [W(r, li) for r in range(R)], [B(r, li) for r in range(R)], outs, N,
+                                        L.cin, L.cout, int(L.relu), sh)
+                cur = outs
+        g = [self.g[r].data_ptr() for r in range(R)]
+        h = [self.h[r].data_ptr() for r in range(R)]
+        S.sprint_softmax_xent_batched(cur, [self.batches_y[b].data_ptr() for b in bidx],
+                                      [self.loss[r].data_ptr() for r in range(R)], g, N, self.classes, 0, sh)
 
         # backward (g holds dE/d(pre-activation output) of layer li)
-        for li in range(len(self.shapes) - 1, -1, -1):
+        for li in range(nL - 1, -1, -1):
             L = self.shapes[li]
-            dw, db = gb + 4 * L.w_off, gb + 4 * L.b_off
             prev = self.shapes[li - 1] if li > 0 else None
+            # update t-2 (the last reader of GradBuf set t % 2) of this layer has finished
+            main.wait_event(self.ev_layer[li][max(t - 1, 0) % K])
+            dw = [gb[r] + 4 * L.w_off for r in range(R)]
+            db = [gb[r] + 4 * L.b_off for r in range(R)]
             if L.kind == "fc":
                 relu_src = None
                 if prev is not None and not (prev.kind == "conv" and prev.pool) and prev.relu:
                     relu_src = inp[li]
-                S.sprint_fc_bwd(inp[li], wptr[li][0], wtptr[li] if prev is not None else None, g, relu_src,
-                                h if prev is not None else None, dw, db, 1.0, 0, N, L.cin, L.cout, ws, wsb, sh)
+                S.sprint_fc_bwd_batched(inp[li], [W(r, li) for r in range(R)],
+                                        [WT(r, li) for r in range(R)] if prev is not None else None, g, relu_src,
+                                        h if prev is not None else None, dw, db, 1.0, 0, N, L.cin, L.cout, ws, wsb,
+                                        sh)
             else:
-                S.sprint_conv_dW(inp[li], g, dw, db, 1.0, 0, N, L.h, L.w, L.cin, L.cout, 1, ws, wsb, sh)
-                if prev is not None:
-                    relu_src = None if prev.pool else inp[li]
-                    S.sprint_conv_dX(g, wptr[li][0], wtptr[li], relu_src, h, N, L.h, L.w, L.cin, L.cout, 1, ws, wsb,
-                                     sh)
+                def bwd(r, st, rws, rwsb, li=li, L=L, prev=prev, g=g, h=h, dw=dw, db=db):
+                    S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, 0, N, L.h, L.w, L.cin, L.cout, 1, rws, rwsb,
+                                     st)
+                    if prev is not None:
+                        relu_src = None if prev.pool else inp[li][r]
+                        S.sprint_conv_dX(g[r], W(r, li), WT(r, li), relu_src, h[r], N, L.h, L.w, L.cin, L.cout, 1,
+                                         rws, rwsb, st)
+                        if prev.kind == "conv" and prev.pool:
+                            # g[r] (free) <- routed gradient of the pre-pool ReLU output, masked
+                            S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], g[r], N, prev.h,
+                                              prev.w, prev.cout, st)
+                self._per_replica(bwd)
+            # layer li's gradients are final: its update overlaps the layers below
+            self.ev_bwd[li].record(main)
+            upd.wait_event(self.ev_bwd[li])
+            self._update_layer(t, li, upd)
+            self.ev_layer[li][(t + 1) % K].record(upd)
             if prev is None:
                 break
-            g, h = h, g
             if prev.kind == "conv" and prev.pool:
-                # h (free) <- routed gradient of the pre-pool ReLU output, masked
-                S.sprint_pool_bwd(g, A["argmax"][li - 1], A["pooled"][li - 1], h, N, prev.h, prev.w, prev.cout, sh)
+                if L.kind == "fc":
+                    # the FC input gradient (in h) routed through the pool into g (free), masked
+                    for r in range(R):
+                        S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], g[r], N, prev.h,
+                                          prev.w, prev.cout, sh)
+                # the conv branch routed into g already: g holds the next layer's gradient
+            else:
                 g, h = h, g
-
-    def _update(self, t, stream):
-        """SumGradient + UpdateWeights (Algorithm 2): W(t+1) into ring slot t+1."""
-        w_in = self.ring[t % (self.S + 1)]
-        w_out = self.ring[(t + 1) % (self.S + 1)]
-        bufs = [self.gradbuf_sets[t % 2][r] for r in range(self.R)]
-        sh = stream.cuda_stream
-        if self.optimizer == "sgd":
-            S.sprint_apply_update_sgd(w_in, w_out, bufs, self.n, self.eta, sh)
-        elif self.optimizer == "momentum":
-            S.sprint_apply_update_momentum(w_in, w_out, self.opt_state, bufs, self.n, self.eta, self.nu, sh)
-        else:
-            S.sprint_apply_update_adagrad(w_in, w_out, self.opt_state, bufs, self.n, self.eta, self.eps, sh)
-        self._transpose_slot((t + 1) % (self.S + 1), stream)
-
-    def step(self):
-        """One global step: every replica's gradient, then one update. Asynchronous."""
-        t = self.t
-        L = len(self.ev_ver)
-        for r in range(self.R):
-            st = self.streams[r]
-            newest = max(self._version(t, r, li) for li in range(len(self.shapes)))
-            # the newest version this replica reads, and update t-2 (last reader of GradBuf set t % 2)
-            st.wait_event(self.ev_ver[max(newest, t - 1, 0) % L])
-            if self.inputs_pending:
-                st.wait_event(self.ev_inputs)
-            self._replica(t, r, st)
-            self.ev_done[r].record(st)
-        for r in range(self.R):
-            self.main_stream.wait_event(self.ev_done[r])
-        self._update(t, self.main_stream)
-        self.ev_update.record(self.main_stream)
-        self.ev_ver[(t + 1) % L].record(self.main_stream)
         self.gradbuf = self.gradbuf_sets[t % 2]   # the GradBufs of the step just issued
-        self.inputs_pending = False
         self.t = t + 1
+
+    def join(self, stream=None):
+        """Makes `stream` (default: the main stream) wait for every update
+        issued so far (the last step's updates may still run on the update
+        stream when step() returns)."""
+        st = self.main_stream if stream is None else stream
+        for evs in self.ev_layer:
+            st.wait_event(evs[self.t % self.K])
 
     def step_loss(self) -> float:
         """Mean over replicas of the last step's loss (synchronises)."""
+        self.join()
         self.main_stream.synchronize()
         return float(self.loss[:, 0].mean().item())

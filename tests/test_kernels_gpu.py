@@ -145,6 +145,9 @@ FC_CASES = [
     (512, 5000, 10),    # classifier of SMLPs
     (64, 48, 10),       # 10 outputs: tensor-core dW with a partial M tile, short-reduction dX
     (16, 40, 33),       # 33 outputs: tensor-core dW, CUDA-core dX
+    (41, 64, 3),        # 3 outputs: float4 skinny forward (4-wide accumulators), ragged row block
+    (24, 96, 13),       # 13 outputs: float4 skinny forward (16-wide accumulators)
+    (20, 64, 30),       # 30 outputs: short-reduction dX with 32 registers of dy, CUDA-core forward
 ]
 
 
@@ -199,6 +202,7 @@ FC_BATCHED_CASES = [
     (17, 64, 96, 64),      # more problems than one launch takes
     (3, 37, 50, 10),       # CUDA-core paths, looped per problem
     (2, 64, 48, 10),       # grouped tensor-core dW, short-reduction dX
+    (5, 42, 128, 7),       # grouped float4 skinny forward (8-wide accumulators), ragged row block
 ]
 
 
