@@ -103,6 +103,15 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the probed kernel, from one ncu capture of the same kernel on the same shape
+# (bench.py --kernel fc_fwd_grouped); must be re-measured whenever that kernel
+# or its tile choice changes (then None).
+PROFILED_TRAFFIC = {
+    "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 497.5e6,
+}
+
+
 class GemmProbe:
     """Records CUDA events, on the launching stream, around the forward FC
     GEMM launches of the given (in, out) shapes: one grouped tensor-core
@@ -258,7 +267,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
         achieved = summ["flops_per_launch"] / (summ["mean_ms"] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": PROFILED_TRAFFIC.get(summ["kernel"]),
                 "kernel": summ["kernel"],
                 "peak_source": f"{peak_src}: bf16 sustained x 1.1/2.25 (nominal tf32/bf16 dense ratio)",
                 "launches": summ["launches"], "mean_ms": round(summ["mean_ms"], 4)}
@@ -322,6 +331,8 @@ KERNELS = {
     "conv_fwd": "conv forward, VGG conv3_2 shape 56x56x256->256, batch 16 (TF32 implicit GEMM)",
     "conv_dx": "conv input gradient, VGG conv3_2 shape, batch 16",
     "conv_dw": "conv weight gradient, VGG conv3_2 shape, batch 16",
+    "fc_fwd_grouped": "grouped FC forward of the SMLPs hidden layer over 4 replicas, 4 x 512 x 5000 x 5000 (TF32)",
+    "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T given",
     "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
     "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
 }
@@ -340,7 +351,26 @@ def run_kernel(args):
     rnd = lambda *shape, std=1.0: torch.randn(shape, generator=g, device="cuda") * std
     k = args.kernel
     peaks, src = load_peaks()
-    if k.startswith("fc"):
+    if k.endswith("_grouped"):
+        M, K, N, G = 512, 5000, 5000, 4
+        x = [rnd(M, K).relu_() for _ in range(G)]
+        w = [[rnd(N, K, std=0.02) for _ in range(G)] for _ in range(2)]   # two sets: > L2 between launches
+        wT = [[t.t().contiguous() for t in ws_] for ws_ in w]
+        y = [torch.empty(M, N, device="cuda") for _ in range(G)]
+        dy = [rnd(M, N) for _ in range(G)]
+        dx = [torch.empty(M, K, device="cuda") for _ in range(G)]
+        dw = [torch.empty(N, K, device="cuda") for _ in range(G)]
+        db = [torch.empty(N, device="cuda") for _ in range(G)]
+        nb = S.sprint_fc_batched_workspace_size(G, M, K, N, 1)
+        ws = torch.empty(nb // 4 + 64, device="cuda")
+        if k == "fc_fwd_grouped":
+            fn = lambda i: S.sprint_fc_fwd_batched(x, w[i % 2], None, y, M, K, N, 1)
+            work = 2.0 * M * N * K * G
+        else:
+            fn = lambda i: S.sprint_fc_bwd_batched(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
+            work = 4.0 * M * N * K * G
+        unit = "TFLOP/s"
+    elif k.startswith("fc"):
         M, K, N = 512, 5000, 5000
         x = rnd(M, K).relu_()
         w = [rnd(N, K, std=0.02) for _ in range(2)]     # two weight matrices: > L2 between launches
