@@ -203,10 +203,19 @@ size_t sprint_fc_bwd_static_scratch_bytes(void);
  * of b and relu_src may also be NULL individually. batch = 0 is a no-op.
  * Problems must not write the same memory. */
 int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b, float* const* y,
-                          int batch, int N, int in, int out, int relu, sprint_stream_t stream);
+                          int batch, int N, int in, int out, int relu, void* ws, size_t ws_bytes,
+                          sprint_stream_t stream);
 
-/* Workspace bytes of sprint_fc_bwd_batched (0 if none needed): `batch` slices
- * of sprint_fc_workspace_size(N, in, out, have_wT), each rounded up to 256. */
+/* Optional workspace of sprint_fc_fwd_batched (device, 16-byte aligned): with
+ * at least this many bytes the tensor-core launch may split the k range of its
+ * last, partial round of tiles (partial sums parked in the workspace, then
+ * added in a fixed order: deterministic); with less (or ws = NULL) it does not. */
+size_t sprint_fc_fwd_batched_workspace_size(void);
+
+/* Workspace bytes of sprint_fc_bwd_batched: `batch` slices of
+ * sprint_fc_workspace_size(N, in, out, have_wT), each rounded up to 256, then
+ * sprint_fc_fwd_batched_workspace_size() bytes for the last-round k split of
+ * its GEMMs (optional: a workspace holding only the slices is accepted). */
 size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int out, int have_wT);
 
 int sprint_fc_bwd_batched(const float* const* x, const float* const* w, const float* const* wT,

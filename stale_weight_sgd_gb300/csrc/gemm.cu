@@ -147,8 +147,9 @@ template <int ROLE, int G>
 int launch_tc_maps(Tile tl, const TcMaps<G>& maps, TcParams p, long long m_tiles, long long n_tiles,
                    long long z_tiles, cudaStream_t s) {
     const long long m_units = tl.pair ? (m_tiles + 1) / 2 : m_tiles;
-    const long long tiles = m_units * n_tiles * z_tiles;
+    long long tiles = m_units * n_tiles * z_tiles;
     if (tiles <= 0) return SPRINT_OK;
+    if (p.tail_splits > 1) tiles = p.tail_start + (tiles - p.tail_start) * p.tail_splits;
     if (tiles > (1ll << 31) - 1) return fail(SPRINT_ERR_SHAPE, "tc_gemm: %lld tiles is too many", tiles);
     p.m_tiles = static_cast<int>(m_units);
     p.n_tiles = static_cast<int>(n_tiles);
@@ -219,6 +220,101 @@ Tile pick_tile(long long m_tiles, long long n, long long z, int max_bn) {
         }
     }
     return best;
+}
+
+// Shared memory slabs the tail split may use: at most one TM x BN slab per
+// slot of the last round (TM x slots = 128 x SMs rows, BN <= 256).
+size_t tail_bytes() { return static_cast<size_t>(num_sms()) * TC_BM * 256 * 4; }
+
+// A launch plan: tile shape, plus the k-split of the last, partial round's
+// tiles (tail_splits == 1: none). With the split the last round runs r * s
+// units of 1/s of the k range on the slots the r leftover tiles would leave
+// idle; the slabs are added afterwards (tc_tail_reduce).
+struct GemmPlan {
+    Tile tile;
+    int tail_splits = 1, tail_kt = 0;
+    long long tail_start = 0;
+};
+
+GemmPlan plan_gemm(long long m_tiles, long long n, long long z, int max_bn, int num_kt, bool allow_tail) {
+    const int cands[5] = {256, 192, 160, 128, 64};
+    const double eff[5] = {0.86, 0.72, 0.68, 0.58, 0.36};
+    const double eff_pair[5] = {1.0, 0.79, 0.86, 0.74, 0.40};
+    const long long sms = num_sms();
+    GemmPlan best;
+    double best_cost = 1e300;
+    for (int pair = 0; pair < 2; ++pair) {
+        if (pair && m_tiles < 2) continue;
+        const long long mu = pair ? (m_tiles + 1) / 2 : m_tiles;
+        const long long slots = pair ? sms / 2 : sms;
+        for (int i = 0; i < 5; ++i) {
+            const int bn = cands[i];
+            if (bn > max_bn) continue;
+            const long long units = mu * ((n + bn - 1) / bn) * z;
+            const long long full = units / slots, r = units % slots;
+            double rounds = static_cast<double>(full);
+            long long sp = 1;
+            if (r > 0) {
+                sp = allow_tail ? slots / r : 1;
+                if (sp > num_kt / 4) sp = num_kt / 4;
+                if (sp >= 2) {
+                    // equal k-ranges of ceil(num_kt / sp) k-tiles: no range may be empty
+                    const long long kt = (num_kt + sp - 1) / sp;
+                    sp = (num_kt + kt - 1) / kt;
+                }
+                if (sp >= 2)
+                    rounds += 1.0 / static_cast<double>(sp) + 0.03;   // + the slab reduction
+                else {
+                    sp = 1;
+                    rounds += 1.0;
+                }
+            }
+            const double cost = rounds * bn / (pair ? eff_pair[i] : eff[i]);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.tile.bn = bn;
+                best.tile.pair = pair != 0;
+                best.tail_splits = static_cast<int>(sp);
+                best.tail_kt = sp > 1 ? static_cast<int>((num_kt + sp - 1) / sp) : 0;
+                best.tail_start = full * slots;
+            }
+        }
+    }
+    return best;
+}
+
+// Launches tc_tail_reduce for the tail tiles of a GEMM_2D launch planned by
+// plan_gemm; m_units / n_tiles / z_tiles describe that launch's unit grid
+// (the kernel decomposes tile indices with them).
+int launch_tail_reduce(const GemmPlan& pl, TcParams p, long long m_units, long long n_tiles, long long z_tiles,
+                       cudaStream_t s) {
+    p.m_tiles = static_cast<int>(m_units);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.z_tiles = static_cast<int>(z_tiles);
+    const long long total_units = m_units * n_tiles * z_tiles;
+    if (p.m_tiles <= 0 || p.n_tiles <= 0 || total_units <= pl.tail_start) return SPRINT_OK;
+    const int tiles = static_cast<int>(total_units - pl.tail_start);
+    const long long work = static_cast<long long>(tiles) * (pl.tile.pair ? 256 : 128) * (pl.tile.bn / 4);
+    long long blocks = (work + 255) / 256;
+    if (blocks > 8ll * num_sms()) blocks = 8ll * num_sms();
+    const unsigned g = static_cast<unsigned>(blocks);
+#define SPRINT_TAIL(BNV)                                                              \
+    case BNV:                                                                         \
+        if (pl.tile.pair)                                                             \
+            tc_tail_reduce<BNV, 256><<<g, 256, 0, s>>>(p, tiles);                     \
+        else                                                                          \
+            tc_tail_reduce<BNV, 128><<<g, 256, 0, s>>>(p, tiles);                     \
+        break;
+    switch (pl.tile.bn) {
+        SPRINT_TAIL(64)
+        SPRINT_TAIL(128)
+        SPRINT_TAIL(160)
+        SPRINT_TAIL(192)
+        SPRINT_TAIL(256)
+        default: return fail(SPRINT_ERR_UNSUPPORTED, "tile width %d not built", pl.tile.bn);
+    }
+#undef SPRINT_TAIL
+    return check_launch("tc_tail_reduce");
 }
 
 TcParams base_params() {
@@ -912,12 +1008,16 @@ bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int
 // before the first launch; false if one cannot be (nothing launched then).
 bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B, long long ldb, int M, int N, int K,
                      TcParams p, const float* const* bias, const float* const* mask, float* const* D, int G,
-                     cudaStream_t s, int* rc) {
+                     cudaStream_t s, int* rc, float* tail_ws = nullptr, size_t tail_ws_bytes = 0) {
     *rc = SPRINT_OK;
     if (G <= 0) return true;
     const long long m_tiles = (M + TC_BM - 1) / TC_BM;
     const int per_launch = G < kMaxGroup ? G : kMaxGroup;
-    const Tile tl = pick_tile(m_tiles, N, per_launch, N >= 256 ? 256 : (N >= 128 ? 128 : 64));
+    const int num_kt = (K + TC_BK - 1) / TC_BK;
+    const bool tail_ok = tail_ws && tail_ws_bytes >= tail_bytes() && aligned16(tail_ws);
+    // the tail split is planned for a full launch of per_launch problems (the last chunk may hold fewer)
+    const GemmPlan plan = plan_gemm(m_tiles, N, per_launch, N >= 256 ? 256 : (N >= 128 ? 128 : 64), num_kt, tail_ok);
+    const Tile tl = plan.tile;
     const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 4};
     const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)ldb * 4};
     const uint32_t ba[2] = {32, 128}, bb[2] = {32, tl.b_rows()};
@@ -942,6 +1042,8 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
     p.N = N;
     p.num_kt = (K + TC_BK - 1) / TC_BK;
     p.kt_per_split = p.num_kt;
+    const long long n_tiles = (N + tl.bn - 1) / tl.bn;
+    const long long m_units = tl.pair ? (m_tiles + 1) / 2 : m_tiles;
     for (int c = 0; c < chunks; ++c) {
         const int g0 = c * kMaxGroup, n = G - g0 < kMaxGroup ? G - g0 : kMaxGroup;
         for (int i = 0; i < kMaxGroup; ++i) {
@@ -949,8 +1051,17 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
             p.g_mask[i] = (i < n && mask) ? mask[g0 + i] : nullptr;
             p.g_D[i] = i < n ? D[g0 + i] : nullptr;
         }
-        *rc = launch_tc_maps<ROLE_GEMM_2D, kMaxGroup>(tl, maps[c], p, m_tiles, (N + tl.bn - 1) / tl.bn, n, s);
+        const long long units = m_units * n_tiles * n;
+        p.tail_splits = 1;
+        if (plan.tail_splits > 1 && units > plan.tail_start) {
+            p.tail_splits = plan.tail_splits;
+            p.tail_kt = plan.tail_kt;
+            p.tail_start = static_cast<int>(plan.tail_start);
+            p.tail_part = tail_ws;
+        }
+        *rc = launch_tc_maps<ROLE_GEMM_2D, kMaxGroup>(tl, maps[c], p, m_tiles, n_tiles, n, s);
         if (*rc) return true;
+        if (p.tail_splits > 1 && (*rc = launch_tail_reduce(plan, p, m_units, n_tiles, n, s))) return true;
     }
     return true;
 }
@@ -1103,12 +1214,14 @@ extern "C" int sprint_fc_bwd(const float* x, const float* w, const float* wT, co
 // ====================================================================== FC, batched over problems
 extern "C" size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int out, int have_wT) {
     if (batch < 1 || N < 1 || in < 1 || out < 1) return 0;
-    return static_cast<size_t>(batch) * round256(plan_fc(N, in, out, have_wT != 0).total());
+    return static_cast<size_t>(batch) * round256(plan_fc(N, in, out, have_wT != 0).total()) + tail_bytes();
 }
 
+extern "C" size_t sprint_fc_fwd_batched_workspace_size(void) { return tail_bytes(); }
+
 extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b,
-                                     float* const* y, int batch, int N, int in, int out, int relu,
-                                     sprint_stream_t stream) {
+                                     float* const* y, int batch, int N, int in, int out, int relu, void* ws,
+                                     size_t ws_bytes, sprint_stream_t stream) {
     SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
                    "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", __func__, batch, N, in, out);
     if (batch == 0) return SPRINT_OK;
@@ -1124,7 +1237,9 @@ extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* 
         p.epi = EPI_STORE;
         p.ldd = out;
         p.relu = relu;
-        if (gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc)) return rc;
+        if (gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc, static_cast<float*>(ws),
+                            ws_bytes))
+            return rc;
     }
     if (out <= kSkinnyN && in % 4 == 0) return launch_skinny4(x, w, b, y, batch, N, out, in, relu, s);
     for (int g = 0; g < batch; ++g)
@@ -1154,6 +1269,9 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
     if (!dx) pl.ws_wT = 0;
     const size_t per = round256(pl.total());
     if ((rc = check_ws(__func__, ws, ws_bytes, per * batch))) return rc;
+    // what follows the per-problem slices serves the tail split of the GEMMs (optional)
+    float* tail_ws = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + per * batch) : nullptr;
+    const size_t tail_ws_bytes = ws ? ws_bytes - per * batch : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (batch == 1)
         return sprint_fc_bwd(x[0], w[0], wT ? wT[0] : nullptr, dy[0], relu_src ? relu_src[0] : nullptr,
@@ -1180,7 +1298,8 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
             p.epi = EPI_MASK;
             p.ldd = in;
             p.ldm = in;
-            done = gemm2d_tc_group(dy, out, wt, out, N, in, out, p, nullptr, relu_src, dx, batch, s, &rc);
+            done = gemm2d_tc_group(dy, out, wt, out, N, in, out, p, nullptr, relu_src, dx, batch, s, &rc, tail_ws,
+                                   tail_ws_bytes);
             if (rc) return rc;
         }
         if (!done && out <= 32 && in % 4 == 0) {
@@ -1212,7 +1331,8 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
             p.ldd = in;
             p.alpha = alpha;
             p.accumulate = accumulate;
-            done = gemm2d_tc_group(dyT.data(), N, xT.data(), N, out, in, N, p, nullptr, nullptr, dw, batch, s, &rc);
+            done = gemm2d_tc_group(dyT.data(), N, xT.data(), N, out, in, N, p, nullptr, nullptr, dw, batch, s, &rc,
+                                   tail_ws, tail_ws_bytes);
             if (rc) return rc;
         }
         if (!done) {

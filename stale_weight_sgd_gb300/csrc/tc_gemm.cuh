@@ -123,6 +123,12 @@ struct TcParams {
     int relu;
     float* partial;      // split-K partial sums [z][M][N] or null
     int* status;
+    // tail split (GEMM_2D): units from tail_start on are the last, partial
+    // round's tiles, each cut into tail_splits k-ranges of tail_kt k-tiles; their
+    // raw accumulators go to tail_part (one TM x BN fp32 slab per unit, TM = 256
+    // for a pair, 128 otherwise) and tc_tail_reduce finishes them
+    int tail_start, tail_splits, tail_kt;
+    float* tail_part;
     // grouped launches: per-problem bias, mask and output (direct stores)
     const float* g_bias[TC_MAX_GROUP];
     const float* g_mask[TC_MAX_GROUP];
@@ -133,12 +139,23 @@ struct TcParams {
 
 struct TileCoord {
     int mt, nt, z;
+    int tail;   // index of a tail-split unit (-1: a whole tile)
+    int split;  // its k-range
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& p) {
+__host__ __device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& p) {
     TileCoord c;
-    c.mt = t % p.m_tiles;
-    const int r = t / p.m_tiles;
+    c.tail = -1;
+    c.split = 0;
+    int tt = t;
+    if (p.tail_splits > 1 && t >= p.tail_start) {
+        const int u = t - p.tail_start;
+        tt = p.tail_start + u / p.tail_splits;
+        c.tail = u;
+        c.split = u % p.tail_splits;
+    }
+    c.mt = tt % p.m_tiles;
+    const int r = tt / p.m_tiles;
     c.nt = r % p.n_tiles;
     c.z = r / p.n_tiles;
     return c;
@@ -222,8 +239,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     // per-tile k range (split-K over z for the weight gradient)
     auto k_range = [&](const TileCoord& tc, int& kt0, int& nkt, int& tap) {
-        int split = G > 1 ? 0 : tc.z;   // grouped: z is the problem, not a k split
         tap = 0;
+        if (tc.tail >= 0) {
+            kt0 = tc.split * p.tail_kt;
+            const int kt1 = kt0 + p.tail_kt < p.num_kt ? kt0 + p.tail_kt : p.num_kt;
+            nkt = kt1 > kt0 ? kt1 - kt0 : 0;
+            return;
+        }
+        int split = G > 1 ? 0 : tc.z;   // grouped: z is the problem, not a k split
         if constexpr (ROLE == ROLE_CONV_WGRAD) {
             tap = tc.z / p.splits;
             split = tc.z % p.splits;
@@ -393,6 +416,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const float* mask = G > 1 ? p.g_mask[tc.z] : p.mask;
             float* Dout = G > 1 ? p.g_D[tc.z] : p.D;
             const int r = warp * 32 + lane;  // tile row = TMEM lane
+            if (tc.tail >= 0) {
+                // a k-range of a tail tile: park the raw accumulator rows in the slab
+                float* slab = p.tail_part +
+                              (static_cast<long long>(tc.tail) * (PAIR ? 2 * TC_BM : TC_BM) + rank * TC_BM + r) * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+                    tmem_wait_ld();
+                    if (c + 32 >= BN) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (PAIR)
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                            else
+                                mbar_arrive(&tmem_empty[b]);
+                        }
+                    }
+                    if (nkt == 0) {   // an empty k-range contributes zeros (the accumulator was never written)
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] = 0u;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(slab + c + q) =
+                            make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
+                                        __uint_as_float(v[q + 3]));
+                }
+                continue;
+            }
             // output row of this thread (direct stores, mask loads); -1 if outside
             long long row_off = -1, mask_off = -1;
             int pw0 = 0, ph0 = 0, pn0 = 0;
@@ -556,6 +610,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else
             tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// Finishes the tail-split tiles of a GEMM_2D launch: out = epilogue(sum of
+// the tile's tail_splits slabs, added in k-range order). One thread per 4
+// consecutive columns of a tile row; TM = 256 (pair) or 128.
+template <int BN, int TM>
+__global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail_tiles) {
+    if (p.m_tiles <= 0 || p.n_tiles <= 0) return;
+    const long long per_tile = static_cast<long long>(TM) * (BN / 4);
+    const long long total = per_tile * tail_tiles;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(idx / per_tile);
+        const int rem = static_cast<int>(idx % per_tile);
+        const int row = rem / (BN / 4), col = (rem % (BN / 4)) * 4;
+        // decompose the tile as the kernel did (units are m-fastest; a pair unit spans TM rows)
+        const int tt = p.tail_start + j;
+        const int mu = tt % p.m_tiles, rr = tt / p.m_tiles;
+        const int nt = rr % p.n_tiles, z = rr / p.n_tiles;
+        const int m = mu * TM + row, n0 = nt * BN + col;
+        if (m >= p.M || n0 >= p.N || z >= p.z_tiles || z >= TC_MAX_GROUP) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < p.tail_splits; ++sp) {
+            const float4 v = *reinterpret_cast<const float4*>(
+                p.tail_part + ((static_cast<long long>(j) * p.tail_splits + sp) * TM + row) * BN + col);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float o[4] = {acc.x, acc.y, acc.z, acc.w};
+        const bool grouped = p.z_tiles > 1 || p.g_D[0] != nullptr;
+        float* D = grouped ? p.g_D[z] : p.D;
+        const float* bias = grouped ? p.g_bias[z] : p.bias;
+        const float* mask = grouped ? p.g_mask[z] : p.mask;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = n0 + q;
+            if (n >= p.N) break;
+            float x = o[q];
+            float* d = D + static_cast<long long>(m) * p.ldd + n;
+            if (p.epi == EPI_STORE) {
+                if (bias) x += bias[n];
+                if (p.relu) x = fmaxf(x, 0.f);
+            } else if (p.epi == EPI_MASK) {
+                if (mask && !(mask[static_cast<long long>(m) * p.ldm + n] > 0.f)) x = 0.f;
+            } else {
+                x *= p.alpha;
+                if (p.accumulate) x += *d;
+            }
+            *d = x;
+        }
     }
 }
 

@@ -52,7 +52,8 @@ _SIGS = {
     "sprint_fc_workspace_size": ([I, I, I, I], SZ),
     "sprint_fc_bwd_static_scratch": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P], I),
     "sprint_fc_bwd_static_scratch_bytes": ([], SZ),
-    "sprint_fc_fwd_batched": ([P, P, P, P, I, I, I, I, I, P], I),
+    "sprint_fc_fwd_batched": ([P, P, P, P, I, I, I, I, I, P, SZ, P], I),
+    "sprint_fc_fwd_batched_workspace_size": ([], SZ),
     "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
     "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
@@ -216,10 +217,15 @@ def _opt_array(items):
     return None if items is None else _ptr_array(items)
 
 
-def sprint_fc_fwd_batched(x, w, b, y, N, fin, fout, relu, stream=None):
+def sprint_fc_fwd_batched(x, w, b, y, N, fin, fout, relu, ws=None, ws_bytes=0, stream=None):
     n = len(x)
     return _check("sprint_fc_fwd_batched", lib().sprint_fc_fwd_batched(
-        _ptr_array(x), _ptr_array(w), _opt_array(b), _ptr_array(y), n, N, fin, fout, int(relu), _s(stream)))
+        _ptr_array(x), _ptr_array(w), _opt_array(b), _ptr_array(y), n, N, fin, fout, int(relu), _p(ws), ws_bytes,
+        _s(stream)))
+
+
+def sprint_fc_fwd_batched_workspace_size() -> int:
+    return lib().sprint_fc_fwd_batched_workspace_size()
 
 
 def sprint_fc_batched_workspace_size(batch, N, fin, fout, have_wT) -> int:

@@ -316,7 +316,7 @@ class StaleSGD:
                 cur = [self.pooled[li][r].data_ptr() for r in range(R)] if L.pool else outs
             else:
                 S.sprint_fc_fwd_batched(cur, [W(r, li) for r in range(R)], [B(r, li) for r in range(R)], outs, N,
-                                        L.cin, L.cout, int(L.relu), sh)
+                                        L.cin, L.cout, int(L.relu), ws, wsb, sh)
                 cur = outs
         g = [self.g[r].data_ptr() for r in range(R)]
         h = [self.h[r].data_ptr() for r in range(R)]

@@ -214,15 +214,19 @@ def _fc_problem(seed, g, N, fin, fout):
     return x, w, b, dy
 
 
-@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES)
+@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES + [(4, 512, 3072, 5000)])
 @pytest.mark.parametrize("relu", [0, 1])
-def test_fc_fwd_batched(S, G, N, fin, fout, relu):
+@pytest.mark.parametrize("tail", [0, 1])
+def test_fc_fwd_batched(S, G, N, fin, fout, relu, tail):
     probs = [_fc_problem(11, g, N, fin, fout) for g in range(G)]
     xs = [dev(p[0]) for p in probs]
     ws = [dev(p[1]) for p in probs]
     bs = [dev(p[2]) if g % 3 != 1 else None for g, p in enumerate(probs)]   # some problems without bias
     ys = [torch.empty((N, fout), dtype=torch.float32, device="cuda") for _ in range(G)]
-    S.sprint_fc_fwd_batched(xs, ws, bs, ys, N, fin, fout, relu)
+    # with the workspace the last round's tiles may be split along k (partials added afterwards)
+    nb = S.sprint_fc_fwd_batched_workspace_size() if tail else 0
+    wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda") if tail else None
+    S.sprint_fc_fwd_batched(xs, ws, bs, ys, N, fin, fout, relu, wsb, nb)
     for g, (x, w, b, _) in enumerate(probs):
         ref = O.fc_fwd(x, w, b if g % 3 != 1 else np.zeros_like(b))
         if relu:
@@ -233,8 +237,8 @@ def test_fc_fwd_batched(S, G, N, fin, fout, relu):
 
 @pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES)
 @pytest.mark.parametrize("with_wT,with_dx", [(0, 1), (1, 1), (1, 0)])
-@pytest.mark.parametrize("accumulate", [0, 1])
-def test_fc_bwd_batched(S, G, N, fin, fout, with_wT, with_dx, accumulate):
+@pytest.mark.parametrize("accumulate,tail", [(0, 1), (1, 1), (1, 0)])
+def test_fc_bwd_batched(S, G, N, fin, fout, with_wT, with_dx, accumulate, tail):
     probs = [_fc_problem(12, g, N, fin, fout) for g in range(G)]
     alpha = 0.5
     xs = [dev(p[0]) for p in probs]
@@ -248,6 +252,8 @@ def test_fc_bwd_batched(S, G, N, fin, fout, with_wT, with_dx, accumulate):
     dws = [dev(a) for a in dw0]
     dbs = [dev(a) for a in db0]
     nb = S.sprint_fc_batched_workspace_size(G, N, fin, fout, with_wT or not with_dx)
+    if not tail:   # only the per-problem slices: no k split of the last round
+        nb -= S.sprint_fc_fwd_batched_workspace_size()
     wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
     S.sprint_fc_bwd_batched(xs, ws, wTs, dys, masks, dxs, dws, dbs, alpha, accumulate, N, fin, fout, wsb, nb)
     for g, (x, w, _, dy) in enumerate(probs):
