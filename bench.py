@@ -331,6 +331,8 @@ KERNELS = {
     "conv_dw": "conv weight gradient, VGG conv3_2 shape, batch 16",
     "fc_fwd_grouped": "grouped FC forward of the SMLPs hidden layer over 4 replicas, 4 x 512 x 5000 x 5000 (TF32)",
     "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T given",
+    "conv_dw_224x64": "conv weight gradient, VGG conv1_2 shape 224x224x64->64, batch 16",
+    "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
     "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
     "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
 }
@@ -386,6 +388,24 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
             work, unit = 4.0 * M * N * K, "TFLOP/s"
+    elif k in ("conv_dw_224x64", "conv_fwd_224x3"):
+        Nb, H, W = 16, 224, 224
+        Ci = 64 if k == "conv_dw_224x64" else 3
+        Co = 64
+        x = rnd(Nb, H, W, Ci).relu_()
+        w = rnd(Co, 3, 3, Ci, std=(2.0 / (9 * Ci)) ** 0.5)
+        b = torch.zeros(Co, device="cuda")
+        y = torch.empty(Nb, H, W, Co, device="cuda")
+        dy = rnd(Nb, H, W, Co)
+        nbytes = max(S.sprint_conv_workspace_size(op, Nb, H, W, Ci, Co, 1) for op in range(3))
+        ws = torch.empty(nbytes // 4 + 64, device="cuda")
+        dwt = torch.empty(Co, 3, 3, Ci, device="cuda")
+        dbt = torch.empty(Co, device="cuda")
+        work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
+        if k == "conv_dw_224x64":
+            fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
+        else:
+            fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
     elif k.startswith("conv"):
         Nb, H, W, C = 16, 56, 56, 256
         x = rnd(Nb, H, W, C).relu_()

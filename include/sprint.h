@@ -121,11 +121,15 @@ int sprint_conv_dX(const float* dy, const float* w, const float* wT, const float
 enum { SPRINT_CONV_FWD = 0, SPRINT_CONV_DX = 1, SPRINT_CONV_DW = 2 };
 
 /* Workspace bytes the convolution `op` needs for this shape (split-K partial
- * sums, partial bias sums); 0 means none. Every conv entry point takes a
- * caller-owned device workspace `ws` of at least this many bytes (contents on
- * entry ignored, clobbered by the call; NULL allowed when the size is 0, else
- * SPRINT_ERR_WORKSPACE). Calls that may overlap on the GPU need separate
- * workspaces. */
+ * sums, partial bias sums, transposed copies); 0 means none. Every conv entry
+ * point takes a caller-owned device workspace `ws` of this many bytes (contents
+ * on entry ignored, clobbered by the call; NULL allowed when the size is 0).
+ * For SPRINT_CONV_FWD and SPRINT_CONV_DX the last part of the size may be room
+ * for splitting the k range of the launch's last, partial round of tiles
+ * (partial sums added afterwards in a fixed order: deterministic); a smaller
+ * workspace that still holds the rest is accepted and that split is skipped.
+ * Too small a workspace gives SPRINT_ERR_WORKSPACE. Calls that may overlap on
+ * the GPU need separate workspaces. */
 size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Cin, int Cout, int pad);
 
 /* Convolution weight and bias gradients — the "dedw" and "dedb" roles of

@@ -286,6 +286,7 @@ GemmPlan plan_gemm(long long m_tiles, long long n, long long z, int max_bn, int 
 // Launches tc_tail_reduce for the tail tiles of a GEMM_2D launch planned by
 // plan_gemm; m_units / n_tiles / z_tiles describe that launch's unit grid
 // (the kernel decomposes tile indices with them).
+template <int ROLE>
 int launch_tail_reduce(const GemmPlan& pl, TcParams p, long long m_units, long long n_tiles, long long z_tiles,
                        cudaStream_t s) {
     p.m_tiles = static_cast<int>(m_units);
@@ -301,9 +302,9 @@ int launch_tail_reduce(const GemmPlan& pl, TcParams p, long long m_units, long l
 #define SPRINT_TAIL(BNV)                                                              \
     case BNV:                                                                         \
         if (pl.tile.pair)                                                             \
-            tc_tail_reduce<BNV, 256><<<g, 256, 0, s>>>(p, tiles);                     \
+            tc_tail_reduce<BNV, 256, ROLE><<<g, 256, 0, s>>>(p, tiles);               \
         else                                                                          \
-            tc_tail_reduce<BNV, 128><<<g, 256, 0, s>>>(p, tiles);                     \
+            tc_tail_reduce<BNV, 128, ROLE><<<g, 256, 0, s>>>(p, tiles);               \
         break;
     switch (pl.tile.bn) {
         SPRINT_TAIL(64)
@@ -835,6 +836,23 @@ __global__ void dw_split_reduce(const float* __restrict__ partial, int splits, i
     }
 }
 
+// dw[co][tap][ci] = (acc ? dw : 0) + alpha * sum_s partial[s][co][tap * rows + ci]
+// (taps packed along N, rows >= Cin channel rows per tap)
+__global__ void dw_packed_reduce(const float* __restrict__ partial, int splits, int Cout, int Cin, int rows,
+                                 float* __restrict__ dw, float alpha, int accumulate) {
+    const long long total = 9ll * Cout * Cin;
+    const long long np = 9ll * rows;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int ci = static_cast<int>(idx % Cin);
+        const int tap = static_cast<int>((idx / Cin) % 9);
+        const long long co = idx / (9ll * Cin);
+        float t = 0.f;
+        for (int s = 0; s < splits; ++s) t += partial[(s * static_cast<long long>(Cout) + co) * np + tap * rows + ci];
+        dw[idx] = (accumulate ? dw[idx] : 0.f) + alpha * t;
+    }
+}
+
 __global__ void colsum_finish_k(const float* __restrict__ partial, int chunks, int cols, float* __restrict__ out,
                                 float alpha, int accumulate) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
@@ -885,9 +903,12 @@ struct ConvPlan {
     int splits = 1, kt_per_split = 0, num_kt = 0;
     size_t ws_wT = 0;       // dedx: transposed weights when the caller has none
     size_t ws_xT = 0, ws_dyT = 0;   // dedw: [C][H][W][N] copies
-    size_t ws_partial = 0;  // dedw: split-K partial sums
+    size_t ws_partial = 0;  // dedw: split-K partial sums (or the padded output of packed taps)
     size_t ws_colsum = 0;   // dedw: partial bias sums
-    size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad; }
+    int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
+    GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
+    size_t ws_tail = 0;            // fwd / dedx: slabs of that split (last in the workspace)
+    size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad + ws_tail; }
 };
 
 ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool have_wT) {
@@ -908,8 +929,10 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         const int gw = op == SPRINT_CONV_FWD ? Wo : W, gh = op == SPRINT_CONV_FWD ? Ho : H;
         pl.box = pick_box(TC_BM, gw, gh, N);
         const int ncols = op == SPRINT_CONV_FWD ? Cout : Cin;
-        pl.tile = pick_tile(pl.box.tiles(), ncols, 1, ncols >= 256 ? 256 : (ncols >= 128 ? 128 : 64));
         pl.num_kt = 9 * (((op == SPRINT_CONV_FWD ? Cin : Cout) + 31) / 32);
+        pl.gp = plan_gemm(pl.box.tiles(), ncols, 1, ncols >= 256 ? 256 : (ncols >= 128 ? 128 : 64), pl.num_kt, true);
+        pl.tile = pl.gp.tile;
+        pl.ws_tail = pl.gp.tail_splits > 1 ? tail_bytes() : 0;
         pl.kt_per_split = pl.num_kt;
         if (op == SPRINT_CONV_DX && !have_wT) pl.ws_wT = fbytes(9ll * Cin * Cout);
         return pl;
@@ -930,13 +953,52 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     pl.box = PixBox{0, 0, 0, static_cast<int>((static_cast<long long>(Wo) * N + TC_BK - 1) / TC_BK), Ho, 1};
     pl.num_kt = pl.box.tw * Ho;   // per output row: ceil(Wo*N / 32) k-tiles
     const long long m_tiles = (Cout + TC_BM - 1) / TC_BM;
-    // split-K below fills the machine, so the widest tile (best MMA shape) is used,
-    // on CTA pairs when Cout spans an even number of 128-row tiles (or many)
-    pl.tile.bn = Cin > 128 ? 256 : (Cin > 64 ? 128 : 64);
-    pl.tile.pair = m_tiles >= 2 && (m_tiles % 2 == 0 || m_tiles >= 6);
-    const long long m_units = pl.tile.pair ? (m_tiles + 1) / 2 : m_tiles;
+    const bool pair_m = m_tiles >= 2 && (m_tiles % 2 == 0 || m_tiles >= 6);
+    long long base;
+    if (Cin <= 128 && (Cin % 8 == 0 || Cin < 8)) {
+        // Few input channels: an n-tile holds whole taps (rows of x^T at their
+        // shifts), wg_rows rows each (8 for Cin < 8: the box rows past Cin are TMA
+        // zero fill), instead of one tap of a few columns; D = [Cout][9 * wg_rows].
+        pl.wg_rows = Cin < 8 ? 8 : Cin;
+        const int rows = pl.wg_rows;
+        int bn = 0;
+        if (9 * rows <= 256) {   // every tap in one tile: the narrowest width that holds 9 * rows
+            const int cands[5] = {64, 128, 160, 192, 256};
+            for (int i = 0; i < 5 && !bn; ++i)
+                if (cands[i] >= 9 * rows && cands[i] % rows == 0) bn = cands[i];
+        }
+        bool pair = false;
+        if (!bn) {
+            // several tiles: least (tiles x width) / efficiency over the widths that hold whole taps
+            const int cands[4] = {256, 192, 160, 128};
+            const double eff[4] = {0.86, 0.72, 0.68, 0.58}, eff_pair[4] = {1.0, 0.79, 0.86, 0.74};
+            double best_c = 1e300;
+            for (int i = 0; i < 4; ++i) {
+                const int c = cands[i];
+                if (c % rows) continue;
+                const bool pr = pair_m && (c / 2) % rows == 0;
+                const double cost = static_cast<double>((9 + c / rows - 1) / (c / rows)) * c / (pr ? eff_pair[i] : eff[i]);
+                if (cost < best_c - 1e-9) {
+                    best_c = cost;
+                    bn = c;
+                    pair = pr;
+                }
+            }
+        } else {
+            pair = pair_m && (bn / 2) % rows == 0;
+        }
+        pl.tile.bn = bn;
+        pl.tile.pair = pair;
+        pl.wg_tpt = bn / rows;
+        base = (pl.tile.pair ? (m_tiles + 1) / 2 : m_tiles) * ((9 + pl.wg_tpt - 1) / pl.wg_tpt);
+    } else {
+        // split-K below fills the machine, so the widest tile (best MMA shape) is used,
+        // on CTA pairs when Cout spans an even number of 128-row tiles (or many)
+        pl.tile.bn = Cin > 128 ? 256 : (Cin > 64 ? 128 : 64);
+        pl.tile.pair = pair_m;
+        base = (pl.tile.pair ? (m_tiles + 1) / 2 : m_tiles) * ((Cin + pl.tile.bn - 1) / pl.tile.bn) * 9;
+    }
     const long long slots = pl.tile.pair ? num_sms() / 2 : num_sms();
-    const long long base = m_units * ((Cin + pl.tile.bn - 1) / pl.tile.bn) * 9;
     // split count: fewest (rounds of units) x (k-tiles per unit), counting each
     // split's partial-sum write and read as ~8 k-tiles of work; splits keep >= 8 k-tiles
     long long maxs = pl.num_kt / 8;
@@ -954,7 +1016,12 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     }
     pl.kt_per_split = static_cast<int>((pl.num_kt + want - 1) / want);
     pl.splits = (pl.num_kt + pl.kt_per_split - 1) / pl.kt_per_split;
-    if (pl.splits > 1) pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * 9 * Cout * Cin);
+    if (pl.wg_tpt > 0) {
+        if (pl.splits > 1 || pl.wg_rows != Cin)
+            pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * Cout * 9 * pl.wg_rows);
+    } else if (pl.splits > 1) {
+        pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * 9 * Cout * Cin);
+    }
     return pl;
 }
 
@@ -1061,7 +1128,8 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
         }
         *rc = launch_tc_maps<ROLE_GEMM_2D, kMaxGroup>(tl, maps[c], p, m_tiles, n_tiles, n, s);
         if (*rc) return true;
-        if (p.tail_splits > 1 && (*rc = launch_tail_reduce(plan, p, m_units, n_tiles, n, s))) return true;
+        if (p.tail_splits > 1 && (*rc = launch_tail_reduce<ROLE_GEMM_2D>(plan, p, m_units, n_tiles, n, s)))
+            return true;
     }
     return true;
 }
@@ -1356,7 +1424,7 @@ extern "C" size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Ci
 }
 
 static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, const CUtensorMap* tb,
-                        TcParams p, int ncols, cudaStream_t s, bool* done) {
+                        TcParams p, int ncols, cudaStream_t s, bool* done, float* tail_ws) {
     CUtensorMap ta, td;
     const uint64_t da[4] = {(uint64_t)act_c, (uint64_t)act_w, (uint64_t)act_h, (uint64_t)p.img_n};
     const uint64_t sa[3] = {(uint64_t)act_c * 4, (uint64_t)act_w * act_c * 4, (uint64_t)act_h * act_w * act_c * 4};
@@ -1383,8 +1451,19 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
     p.tiles_h = pl.box.th;
     p.chunks = pl.num_kt / 9;
     *done = true;
-    return launch_tc<ROLE_CONV_IMPL>(pl.tile, ta, *tb, td, p, pl.box.tiles(), (ncols + pl.tile.bn - 1) / pl.tile.bn,
-                                     1, s);
+    const long long n_tiles = (ncols + pl.tile.bn - 1) / pl.tile.bn;
+    const bool tail = pl.gp.tail_splits > 1 && tail_ws;
+    if (tail) {
+        p.tail_splits = pl.gp.tail_splits;
+        p.tail_kt = pl.gp.tail_kt;
+        p.tail_start = static_cast<int>(pl.gp.tail_start);
+        p.tail_part = tail_ws;
+    }
+    int rc = launch_tc<ROLE_CONV_IMPL>(pl.tile, ta, *tb, td, p, pl.box.tiles(), n_tiles, 1, s);
+    if (rc || !tail) return rc;
+    p.tiles_w = pl.box.tw;
+    const long long m_units = pl.tile.pair ? (pl.box.tiles() + 1) / 2 : pl.box.tiles();
+    return launch_tail_reduce<ROLE_CONV_IMPL>(pl.gp, p, m_units, n_tiles, 1, s);
 }
 
 extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
@@ -1399,7 +1478,10 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     SPRINT_ALIGNED(b, "b");
     SPRINT_ALIGNED(y, "y");
     const ConvPlan pl = plan_conv(SPRINT_CONV_FWD, N, H, W, Cin, Cout, pad, true);
-    if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total()))) return rc;
+    // the tail-split slabs (last in the workspace) are optional: without room for them the
+    // last round is not split
+    if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total() - pl.ws_tail))) return rc;
+    const bool tail_room = pl.ws_tail && ws && ws_bytes >= pl.ws_total();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     if (pl.tc && pl.im2col) {
@@ -1439,7 +1521,9 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
             p.bias = b;
             p.relu = relu;
             bool done = false;
-            rc = conv_impl_tc(pl, x, Cin, W, H, &tb, p, Cout, s, &done);
+            float* tail_ws =
+                tail_room ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_total() - pl.ws_tail) : nullptr;
+            rc = conv_impl_tc(pl, x, Cin, W, H, &tb, p, Cout, s, &done, tail_ws);
             if (rc || done) return rc;
         }
     }
@@ -1462,7 +1546,9 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
     SPRINT_ALIGNED(relu_src, "relu_src");
     SPRINT_ALIGNED(dx, "dx");
     const ConvPlan pl = plan_conv(SPRINT_CONV_DX, N, H, W, Cin, Cout, pad, wT != nullptr);
-    if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total()))) return rc;
+    // the tail-split slabs (last in the workspace) are optional
+    if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total() - pl.ws_tail))) return rc;
+    const bool tail_room = pl.ws_tail && ws && ws_bytes >= pl.ws_total();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     if (pl.tc) {
@@ -1490,7 +1576,9 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
             p.mask = relu_src;
             p.ldm = Cin;
             bool done = false;
-            rc = conv_impl_tc(pl, dy, Cout, Wo, Ho, &tb, p, Cin, s, &done);
+            float* tail_ws =
+                tail_room ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_total() - pl.ws_tail) : nullptr;
+            rc = conv_impl_tc(pl, dy, Cout, Wo, Ho, &tb, p, Cin, s, &done, tail_ws);
             if (rc || done) return rc;
         }
     }
@@ -1536,7 +1624,8 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         const uint64_t dbm[3] = {(uint64_t)W * N, (uint64_t)H, (uint64_t)Cin};
         const uint64_t sbm[2] = {(uint64_t)W * N * 4, (uint64_t)H * W * N * 4};
         const uint32_t ba[3] = {32, 1, 128};
-        const uint32_t bb[3] = {32, 1, pl.tile.b_rows()};
+        // packed taps: one box = one tap's wg_rows channel rows; else BN (or half) channel rows
+        const uint32_t bb[3] = {32, 1, pl.wg_tpt > 0 ? static_cast<uint32_t>(pl.wg_rows) : pl.tile.b_rows()};
         if (make_tmap(&ta, dyT, 3, da, sa, ba) && make_tmap(&tb, xT, 3, dbm, sbm, bb)) {
             TcParams p = base_params();
             p.M = Cout;
@@ -1558,7 +1647,35 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
             p.partial = pl.splits > 1 ? part : nullptr;
             CUtensorMap td = ta;
             p.store = ST_DIRECT;
-            if (pl.splits > 1) {
+            if (pl.wg_tpt > 0) {
+                // D = [Cout][9 * rows]: straight into dw when rows == Cin and one split, else partials
+                const int np = 9 * pl.wg_rows;
+                p.wg_tpt = pl.wg_tpt;
+                p.wg_rows = pl.wg_rows;
+                p.N = np;
+                const bool direct = pl.splits == 1 && pl.wg_rows == Cin;
+                p.partial = direct ? nullptr : part;
+                p.ldd = np;
+                if (direct) {
+                    const uint64_t dd[2] = {(uint64_t)np, (uint64_t)Cout}, sd[1] = {(uint64_t)np * 4};
+                    const uint32_t bd[2] = {32, 32};
+                    if ((np & 3) == 0 && make_tmap(&td, dw, 2, dd, sd, bd, false)) p.store = ST_2D;
+                } else {
+                    const uint64_t dd[3] = {(uint64_t)np, (uint64_t)Cout, (uint64_t)pl.splits};
+                    const uint64_t sd[2] = {(uint64_t)np * 4, (uint64_t)Cout * np * 4};
+                    const uint32_t bd[3] = {32, 32, 1};
+                    if (aligned16(part) && make_tmap(&td, part, 3, dd, sd, bd, false)) p.store = ST_PARTIAL3D;
+                }
+                if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
+                                                     (9 + pl.wg_tpt - 1) / pl.wg_tpt, pl.splits, s)))
+                    return rc;
+                if (!direct) {
+                    dw_packed_reduce<<<grid_cap(9ll * Cout * Cin), 256, 0, s>>>(part, pl.splits, Cout, Cin,
+                                                                              pl.wg_rows, dw, alpha, accumulate);
+                    if ((rc = check_launch("dw_packed_reduce"))) return rc;
+                }
+                done = true;
+            } else if (pl.splits > 1) {
                 const uint64_t dd[3] = {(uint64_t)Cin, (uint64_t)Cout, (uint64_t)9 * pl.splits};
                 const uint64_t sd[2] = {(uint64_t)Cin * 4, (uint64_t)Cout * Cin * 4};
                 const uint32_t bd[3] = {32, 32, 1};
@@ -1569,15 +1686,17 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
                 const uint32_t bd[3] = {32, 1, 32};
                 if (make_tmap(&td, dw, 3, dd, sd, bd, false)) p.store = ST_WGRAD3D;
             }
-            if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
-                                                 (Cin + pl.tile.bn - 1) / pl.tile.bn, 9ll * pl.splits, s)))
-                return rc;
-            if (pl.splits > 1) {
-                dw_split_reduce<<<grid_cap(9ll * Cout * Cin), 256, 0, s>>>(part, pl.splits, Cout, Cin, dw, alpha,
-                                                                         accumulate);
-                if ((rc = check_launch("dw_split_reduce"))) return rc;
+            if (!done) {   // one tap per tile: taps and splits in z
+                if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, td, p, (Cout + TC_BM - 1) / TC_BM,
+                                                     (Cin + pl.tile.bn - 1) / pl.tile.bn, 9ll * pl.splits, s)))
+                    return rc;
+                if (pl.splits > 1) {
+                    dw_split_reduce<<<grid_cap(9ll * Cout * Cin), 256, 0, s>>>(part, pl.splits, Cout, Cin, dw,
+                                                                             alpha, accumulate);
+                    if ((rc = check_launch("dw_split_reduce"))) return rc;
+                }
+                done = true;
             }
-            done = true;
         }
     }
     if (!done) {

@@ -129,6 +129,12 @@ struct TcParams {
     // for a pair, 128 otherwise) and tc_tail_reduce finishes them
     int tail_start, tail_splits, tail_kt;
     float* tail_part;
+    // CONV_WGRAD with taps packed along N (wg_tpt > 0): an n-tile holds wg_tpt
+    // taps of wg_rows channel rows each (wg_rows % 8 == 0: every tap's slice
+    // starts on a 1024-byte swizzle atom; rows past Cin are TMA zero fill), so
+    // D[co][tap * wg_rows + ci]; z is the k split only. wg_tpt == 0: one tap per
+    // n-tile column range, taps and splits in z.
+    int wg_tpt, wg_rows;
     // grouped launches: per-problem bias, mask and output (direct stores)
     const float* g_bias[TC_MAX_GROUP];
     const float* g_mask[TC_MAX_GROUP];
@@ -247,9 +253,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             return;
         }
         int split = G > 1 ? 0 : tc.z;   // grouped: z is the problem, not a k split
+        tap = 0;
         if constexpr (ROLE == ROLE_CONV_WGRAD) {
-            tap = tc.z / p.splits;
-            split = tc.z % p.splits;
+            if (p.wg_tpt == 0) {
+                tap = tc.z / p.splits;
+                split = tc.z % p.splits;
+            }
+            // interleaved splits: split s takes k-tiles s, s + splits, ... so the CTAs running
+            // together read one narrow k window (shared through L2, rows swept in order)
+            // instead of `splits` far-apart streams of the [C][H][W][N] copies
+            kt0 = split;
+            nkt = split < p.num_kt ? (p.num_kt - split + p.splits - 1) / p.splits : 0;
+            return;
         }
         kt0 = split * p.kt_per_split;
         int kt1 = kt0 + p.kt_per_split;
@@ -284,9 +299,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     const int nq = nkt - i < KS ? nkt - i : KS;   // k-tiles in this stage
-                    if (rank == 0) mbar_arrive_expect_tx(&full[s], nq * KTILE_BYTES);
+                    uint32_t ktile_bytes = KTILE_BYTES;
+                    if constexpr (ROLE == ROLE_CONV_WGRAD) {
+                        if (p.wg_tpt > 0) {   // A boxes of both CTAs + the taps that exist in this n-tile
+                            const int per = PAIR ? p.wg_tpt / 2 : p.wg_tpt;
+                            int taps = 0;
+                            for (int rk = 0; rk < (PAIR ? 2 : 1); ++rk) {
+                                const int first = tc.nt * p.wg_tpt + rk * per;
+                                taps += first >= 9 ? 0 : (9 - first < per ? 9 - first : per);
+                            }
+                            ktile_bytes = (PAIR ? 2u : 1u) * TC_A_STAGE + static_cast<uint32_t>(taps * p.wg_rows) * 128u;
+                        }
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], nq * ktile_bytes);
                     for (int q = 0; q < nq; ++q) {
-                        const int kt = kt0 + i + q;
+                        // the k-tile of this stage slot (interleaved splits for the weight gradient)
+                        const int kt = ROLE == ROLE_CONV_WGRAD ? kt0 + (i + q) * p.splits : kt0 + i + q;
                         uint8_t* a_dst = sA + (s * KS + q) * TC_A_STAGE;
                         uint8_t* b_dst = sB + (s * KS + q) * B_STAGE;
                         if constexpr (PAIR) {
@@ -308,8 +336,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 const int h = kt / p.tiles_w;
                                 const int c0 = (kt % p.tiles_w) * TC_BK;
                                 tma_load_3d_pair(a_dst, mA, c0, h, m0, bar);
-                                tma_load_3d_pair(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad,
-                                                 n0, bar);
+                                if (p.wg_tpt > 0) {
+                                    const int per = p.wg_tpt / 2, first = tc.nt * p.wg_tpt + static_cast<int>(rank) * per;
+                                    for (int j = 0; j < per && first + j < 9; ++j) {
+                                        const int tp = first + j;
+                                        tma_load_3d_pair(b_dst + j * p.wg_rows * 128, mB, c0 + (tp % 3 - p.pad) * p.img_n,
+                                                         h + tp / 3 - p.pad, 0, bar);
+                                    }
+                                } else {
+                                    tma_load_3d_pair(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad,
+                                                     n0, bar);
+                                }
                             }
                         } else if constexpr (ROLE == ROLE_GEMM_2D) {
                             tma_load_2d(a_dst, mA, kt * TC_BK, m0, &full[s]);
@@ -327,8 +364,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             const int h = kt / p.tiles_w;
                             const int c0 = (kt % p.tiles_w) * TC_BK;
                             tma_load_3d(a_dst, mA, c0, h, m0, &full[s]);
-                            tma_load_3d(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
-                                        &full[s]);
+                            if (p.wg_tpt > 0) {
+                                const int first = tc.nt * p.wg_tpt;
+                                for (int j = 0; j < p.wg_tpt && first + j < 9; ++j) {
+                                    const int tp = first + j;
+                                    tma_load_3d(b_dst + j * p.wg_rows * 128, mB, c0 + (tp % 3 - p.pad) * p.img_n,
+                                                h + tp / 3 - p.pad, 0, &full[s]);
+                                }
+                            } else {
+                                tma_load_3d(b_dst, mB, c0 + (tap % 3 - p.pad) * p.img_n, h + tap / 3 - p.pad, n0,
+                                            &full[s]);
+                            }
                         }
                     }
                 }
@@ -616,7 +662,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // Finishes the tail-split tiles of a GEMM_2D launch: out = epilogue(sum of
 // the tile's tail_splits slabs, added in k-range order). One thread per 4
 // consecutive columns of a tile row; TM = 256 (pair) or 128.
-template <int BN, int TM>
+template <int BN, int TM, int ROLE>
 __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail_tiles) {
     if (p.m_tiles <= 0 || p.n_tiles <= 0) return;
     const long long per_tile = static_cast<long long>(TM) * (BN / 4);
@@ -630,8 +676,21 @@ __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail
         const int tt = p.tail_start + j;
         const int mu = tt % p.m_tiles, rr = tt / p.m_tiles;
         const int nt = rr % p.n_tiles, z = rr / p.n_tiles;
-        const int m = mu * TM + row, n0 = nt * BN + col;
-        if (m >= p.M || n0 >= p.N || z >= p.z_tiles || z >= TC_MAX_GROUP) continue;
+        const int n0 = nt * BN + col;
+        if (n0 >= p.N || z >= p.z_tiles || z >= TC_MAX_GROUP) continue;
+        long long m;   // output row (GEMM_2D) or output pixel (CONV_IMPL) of this slab row
+        if constexpr (ROLE == ROLE_CONV_IMPL) {
+            // slab row = rank * 128 + r of the unit's box(es); the box decomposition of the epilogue
+            const int mt = TM == 256 ? 2 * mu + row / 128 : mu, r = row % 128;
+            const int ow = (mt % p.tiles_w) * p.bw + r % p.bw;
+            const int oh = ((mt / p.tiles_w) % p.tiles_h) * p.bh + (r / p.bw) % p.bh;
+            const int on = (mt / (p.tiles_w * p.tiles_h)) * p.bimg + r / (p.bw * p.bh);
+            if (ow >= p.out_w || oh >= p.out_h || on >= p.img_n) continue;
+            m = (static_cast<long long>(on) * p.out_h + oh) * p.out_w + ow;
+        } else {
+            m = static_cast<long long>(mu) * TM + row;
+            if (m >= p.M) continue;
+        }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int sp = 0; sp < p.tail_splits; ++sp) {
             const float4 v = *reinterpret_cast<const float4*>(
@@ -651,12 +710,12 @@ __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail
             const int n = n0 + q;
             if (n >= p.N) break;
             float x = o[q];
-            float* d = D + static_cast<long long>(m) * p.ldd + n;
+            float* d = D + m * p.ldd + n;
             if (p.epi == EPI_STORE) {
                 if (bias) x += bias[n];
                 if (p.relu) x = fmaxf(x, 0.f);
             } else if (p.epi == EPI_MASK) {
-                if (mask && !(mask[static_cast<long long>(m) * p.ldm + n] > 0.f)) x = 0.f;
+                if (mask && !(mask[m * p.ldm + n] > 0.f)) x = 0.f;
             } else {
                 x *= p.alpha;
                 if (p.accumulate) x += *d;
