@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
@@ -286,7 +287,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "roofline": roof,
         "achieved_step_tflops": round(flops_step * args.steps / (ms_max / 1e3) / 1e12 * world, 1),
         "clocks": clk,
-        "loss_last": loss,
+        # a diverged run (the ILSVRC-shaped config with 8 summed replica gradients at eta 0.005
+        # overflows after a few steps) has no finite loss: JSON has no NaN
+        "loss_last": loss if math.isfinite(loss) else None,
         "kernels_per_step": int(launches // args.steps),
         "host_issue_ms_per_step": round(host_issue_ms, 3),
     }
