@@ -730,6 +730,106 @@ int launch_smallk_dx4(const float* const* dy, const float* const* w, const float
     return SPRINT_OK;
 }
 
+// Forward convolution with very few input channels (the RGB layer, CIN <= 4,
+// Cout % 16 == 0). Its 9*CIN-long reduction makes it bound by writing y, not by
+// arithmetic (~14 FLOP per output byte), so it runs on the CUDA cores at
+// streaming speed: a thread owns one output pixel x 16 consecutive output
+// channels, loads the pixel's 3x3xCIN patch once (zero outside the image), and
+// reads the weights — staged per block in shared memory as [tap*CIN+ci][co] —
+// as four float4; bias and ReLU are fused and y is written as four float4.
+// The 32 lanes of a warp take 32 consecutive pixels of the same channel group,
+// so every weight read is one shared-memory broadcast (lanes of different
+// groups in one warp read rows 64 B apart: bank conflicts, measured 10x slower).
+template <int CIN>
+__global__ void __launch_bounds__(256) conv_smallc_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                              const float* __restrict__ b, float* __restrict__ y, int N,
+                                                              int H, int W, int Cout, int pad, int relu) {
+    extern __shared__ float4 smallc_smem[];
+    float* ws = reinterpret_cast<float*>(smallc_smem);   // [9*CIN][Cout], then bias [Cout]
+    constexpr int K = 9 * CIN;
+    for (int i = threadIdx.x; i < K * Cout; i += blockDim.x) ws[(i % K) * Cout + i / K] = w[i];
+    float* bs = ws + K * Cout;
+    for (int i = threadIdx.x; i < Cout; i += blockDim.x) bs[i] = b ? b[i] : 0.f;
+    __syncthreads();
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const int groups = Cout / 16;
+    const int P = N * Ho * Wo;                       // < 2^31 (checked by the caller)
+    const int pix_blocks = (P + 31) / 32;            // 32-pixel warp tasks per channel group
+    const int tasks = pix_blocks * groups;
+    const int warp_gid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int task = warp_gid; task < tasks; task += warps) {
+        const int g = task % groups;
+        const int pix = (task / groups) * 32 + lane;
+        if (pix >= P) continue;
+        const int ow = pix % Wo;
+        const int t = pix / Wo;
+        const int oh = t % Ho;
+        const long long n = t / Ho;
+        float in[K];
+#pragma unroll
+        for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+            for (int kw = 0; kw < 3; ++kw) {
+                const int ih = oh + kh - pad, iw = ow + kw - pad;
+                const bool ok = ih >= 0 && ih < H && iw >= 0 && iw < W;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) {
+                    float v = 0.f;
+                    if (ok) v = __ldg(x + ((n * H + ih) * W + iw) * CIN + ci);
+                    in[(kh * 3 + kw) * CIN + ci] = v;
+                }
+            }
+        const int co0 = g * 16;
+        float acc[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q] = bs[co0 + q];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const float4* wr = reinterpret_cast<const float4*>(ws + k * Cout + co0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+                const float4 wv = wr[v4];
+                acc[4 * v4 + 0] = fmaf(in[k], wv.x, acc[4 * v4 + 0]);
+                acc[4 * v4 + 1] = fmaf(in[k], wv.y, acc[4 * v4 + 1]);
+                acc[4 * v4 + 2] = fmaf(in[k], wv.z, acc[4 * v4 + 2]);
+                acc[4 * v4 + 3] = fmaf(in[k], wv.w, acc[4 * v4 + 3]);
+            }
+        }
+        float4* dst = reinterpret_cast<float4*>(y + static_cast<long long>(pix) * Cout + co0);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+            float4 o = make_float4(acc[4 * v4], acc[4 * v4 + 1], acc[4 * v4 + 2], acc[4 * v4 + 3]);
+            if (relu) {
+                o.x = fmaxf(o.x, 0.f);
+                o.y = fmaxf(o.y, 0.f);
+                o.z = fmaxf(o.z, 0.f);
+                o.w = fmaxf(o.w, 0.f);
+            }
+            __stcs(dst + v4, o);
+        }
+    }
+}
+
+int launch_conv_smallc(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
+                       int Cout, int pad, int relu, cudaStream_t s) {
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const long long P = static_cast<long long>(N) * Ho * Wo;
+    SPRINT_REQUIRE(P < (1ll << 31) - 32, SPRINT_ERR_SHAPE, "conv_fwd: %lld output pixels", P);
+    const long long total = ((P + 31) / 32) * 32 * (Cout / 16);
+    const size_t smem = (static_cast<size_t>(9) * Cin * Cout + Cout) * sizeof(float);
+    long long g = (total + 255) / 256;
+    if (g > 16ll * num_sms()) g = 16ll * num_sms();
+    const int grid = static_cast<int>(g < 1 ? 1 : g);
+    switch (Cin) {
+        case 1: conv_smallc_fwd_kernel<1><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        case 2: conv_smallc_fwd_kernel<2><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        case 3: conv_smallc_fwd_kernel<3><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        default: conv_smallc_fwd_kernel<4><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+    }
+    return check_launch("conv_smallc_fwd_kernel");
+}
+
 // direct convolution, one thread per output element (co fastest)
 __global__ void __launch_bounds__(256) simt_conv_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ b, float* __restrict__ y, int N,
@@ -896,6 +996,7 @@ FcPlan plan_fc(int N, int in, int out, bool have_wT) {
 struct ConvPlan {
     bool tc = false;
     bool im2col = false;    // forward through an explicit padded im2col + 2-D GEMM
+    bool smallc = false;    // forward with Cin <= 4: direct CUDA-core kernel (conv_smallc_fwd_kernel)
     int kp = 0;             // padded k of that im2col
     size_t ws_col = 0, ws_wpad = 0;
     Tile tile{};
@@ -915,6 +1016,11 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     ConvPlan pl;
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const long long P = static_cast<long long>(N) * Ho * Wo;
+    if (op == SPRINT_CONV_FWD && Cin <= 4 && Cout % 16 == 0 && (9 * Cin + 1) * Cout * 4 <= 48 * 1024) {
+        // the RGB layer: direct CUDA-core convolution at output-write speed (no workspace)
+        pl.smallc = true;
+        return pl;
+    }
     if (op == SPRINT_CONV_FWD && Cin % 4 != 0 && Cout % 4 == 0 && Cout >= 16 && 9 * Cin <= 64) {
         // few input channels (the RGB layer): explicit im2col, k padded to 32 or 64
         pl.tc = pl.im2col = true;
@@ -1484,6 +1590,7 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     const bool tail_room = pl.ws_tail && ws && ws_bytes >= pl.ws_total();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    if (pl.smallc) return launch_conv_smallc(x, w, b, y, N, H, W, Cin, Cout, pad, relu, s);
     if (pl.tc && pl.im2col) {
         float* col = static_cast<float*>(ws);
         float* wpad = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_col);

@@ -298,6 +298,8 @@ CONV_CASES = [
     (32, 4, 4, 128, 256),   # wide channels, split-K
     (4, 12, 12, 3, 64),     # RGB layer, batch % 4 == 0: padded im2col forward, tensor-core weight gradient
     (8, 9, 7, 3, 16),       # RGB layer, ragged spatial size
+    (3, 7, 6, 1, 16),       # one input channel: direct CUDA-core forward, zero-filled tap boxes in dW
+    (4, 8, 5, 4, 32),       # four input channels: direct forward (4-wide patch), CUDA-core dX
 ]
 
 
@@ -365,6 +367,16 @@ def test_transpose(S):
     out = torch.empty((45, 70), dtype=torch.float32, device="cuda")
     S.sprint_transpose(dev(a), out, 70, 45)
     assert (host(out) == a.T).all()
+
+
+def test_conv_rgb_pad0(S):
+    N, H, W, Cin, Cout = 2, 9, 10, 3, 32
+    x, w, b = _conv_inputs(14, N, H, W, Cin, Cout)
+    ref = O.relu(O.conv3x3_fwd(x, w, b, pad=0))
+    y = torch.empty((N, H - 2, W - 2, Cout), dtype=torch.float32, device="cuda")
+    S.sprint_conv_fwd(dev(x), dev(w), dev(b), y, N, H, W, Cin, Cout, 0, 1, None, 0)
+    assert rel_inf(host(y), ref) <= TOL_TF32
+    _status_clean(S)
 
 
 def test_conv_pad0(S):
