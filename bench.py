@@ -259,7 +259,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     e2e_s = allreduce_max(e2e_s, world)
 
     imgs = R * N * args.steps * world
-    value = imgs / (ms_max / 1e3)
+    value, _ = weak_scaling_value(R * N * args.steps, ms / 1e3, world)
     e2e_value = imgs / e2e_s
     peaks, peak_src = load_peaks()
     summ = probe.summary()
@@ -467,6 +467,27 @@ def run_kernel(args):
     return 0
 
 
+def init_dist(world, local_rank):
+    """One process per GPU (NCCL); on a machine without GPUs the same host
+    logic runs over gloo (the multi-process CPU tests)."""
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        dist.init_process_group("gloo")
+
+
+def weak_scaling_value(imgs_per_rank, seconds_local, world):
+    """Replicas-only scaling: every rank runs the whole workload; the job's
+    images/s are all ranks' images over the slowest rank's time."""
+    s_max = allreduce_max(seconds_local, world)
+    return imgs_per_rank * world / s_max, s_max
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -519,11 +540,7 @@ def main(argv=None):
         print(json.dumps(out))
         return 0
 
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
+    init_dist(world, local_rank)
     out = run_ours(args, cfg, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
