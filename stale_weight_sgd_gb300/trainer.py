@@ -54,9 +54,12 @@ from .model import layer_shapes, pack, padded_size, unpack
 class StaleSGD:
     def __init__(self, net, batch, *, replicas=1, max_delay=0, schedule_seed=0, stage_of_layer=None,
                  stage_delays=None, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, concurrent=True,
-                 device="cuda"):
+                 graphs="auto", device="cuda"):
         """concurrent: run the per-layer updates on a second stream, overlapping
-        the rest of the backward pass (False: everything on one stream)."""
+        the rest of the backward pass (False: everything on one stream).
+        graphs: replay captured CUDA graphs of the step ("auto": when the delay
+        schedule is periodic — pipeline stages or no delay — so the same few
+        steps recur; the seeded random ASGD schedule is issued step by step)."""
         S.lib()  # fail loudly if the CUDA library is missing
         self.net = net
         self.shapes = layer_shapes(net)
@@ -121,6 +124,14 @@ class StaleSGD:
         self.batches_x = None
         self.batches_y = None
         self.t = 0
+        periodic = self.pipeline or self.S == 0
+        self.use_graphs = periodic if graphs == "auto" else bool(graphs)
+        self._graphs = {}            # step key -> captured CUDA graph
+        self._graph_steps = False    # the last step ran as a graph replay
+        self._graph_kernels = {}     # step key -> kernels in the graph
+        self.graph_launch_adjust = 0  # kernels replayed minus kernels counted while capturing
+        self.ev_graph_upd = torch.cuda.Event()
+        self._cap_stream = None
 
     # ------------------------------------------------------------------ buffers
     def _alloc_acts(self):
@@ -184,6 +195,7 @@ class StaleSGD:
         elif self.optimizer == "adagrad":
             self.opt_state.fill_(self.g0)
         self.t = 0
+        self._graph_steps = False   # eager again until the schedule is periodic
         torch.cuda.synchronize(self.dev)
         for evs in self.ev_layer:
             evs[0].record(self.main_stream)
@@ -271,10 +283,81 @@ class StaleSGD:
         for r in range(self.R):
             main.wait_event(self.ev_join[r])
 
+    def _graph_key(self, t):
+        """Everything a captured step bakes in: weight slots, GradBuf parity, batches."""
+        nL = len(self.shapes)
+        P = self.batches_x.shape[0]
+        slots = tuple(self._version(t, r, li) % (self.S + 1) for r in range(self.R) for li in range(nL))
+        bx = tuple(self.batches_x[(t * self.R + r) % P].data_ptr() for r in range(self.R))
+        by = tuple(self.batches_y[(t * self.R + r) % P].data_ptr() for r in range(self.R))
+        return slots, t % 2, bx, by
+
+    def _capture(self, t, key):
+        """Captures step t's graph (not run): on a stream of our own (capture needs
+        a non-default stream), standing in for the main stream while it is issued."""
+        main = self.main_stream
+        if self._cap_stream is None:
+            self._cap_stream = torch.cuda.Stream(self.dev)
+        g = torch.cuda.CUDAGraph()
+        n0 = S.sprint_launch_count()
+        self.main_stream = self._cap_stream
+        try:
+            with torch.cuda.graph(g, stream=self._cap_stream, capture_error_mode="relaxed"):
+                self._issue(t, graph=True)
+        finally:
+            self.main_stream = main
+        self._graphs[key] = g
+        self._graph_kernels[key] = S.sprint_launch_count() - n0
+        self.graph_launch_adjust -= self._graph_kernels[key]   # captured, not run
+        return g
+
+    def prepare_graphs(self):
+        """Captures (without running them) the graphs of every step of one period of
+        the schedule from the current step on, so later steps only replay; returns
+        how many graphs are cached. No-op unless graphs are in use."""
+        if not self.use_graphs:
+            return 0
+        P = self.batches_x.shape[0]
+        period = np.lcm.reduce([self.S + 1, 2, P // np.gcd(P, self.R) if P else 1])
+        t0 = max(self.t, self.S)
+        for t in range(t0, t0 + int(period)):
+            key = self._graph_key(t)
+            if key not in self._graphs:
+                self._capture(t, key)
+        return len(self._graphs)
+
     def step(self):
         """One global step: every replica's gradient, then the update, layer by
         layer. Asynchronous."""
-        t, R, N, K = self.t, self.R, self.N, self.K
+        t = self.t
+        main = self.main_stream
+        if self.inputs_pending:
+            main.wait_event(self.ev_inputs)
+            self.inputs_pending = False
+        # Periodic schedules: once past the first S steps (whose versions are clamped
+        # at 0) a step is a replay of the graph captured for its key. A captured step
+        # ends with the update stream joined into the main stream, so replays are
+        # ordered by the main stream alone and need none of the per-layer events.
+        if self.use_graphs and t >= self.S:
+            if not self._graph_steps:
+                self.join()   # the eager steps' updates still in flight
+            key = self._graph_key(t)
+            g = self._graphs.get(key)
+            if g is None:
+                g = self._capture(t, key)
+            with torch.cuda.stream(main):
+                g.replay()
+            self.graph_launch_adjust += self._graph_kernels[key]
+            self._graph_steps = True
+            self.gradbuf = self.gradbuf_sets[t % 2]
+            self.t = t + 1
+            return
+        self._issue(t, graph=False)
+
+    def _issue(self, t, graph):
+        """Issues step t (graph: being captured — no waits on events recorded by
+        earlier steps, no per-layer version events, the update stream joined at the end)."""
+        R, N, K = self.R, self.N, self.K
         main, upd = self.main_stream, self.upd_stream
         sh = main.cuda_stream
         nL = len(self.shapes)
@@ -285,9 +368,6 @@ class StaleSGD:
         gb = [self.gradbuf_sets[t % 2][r].data_ptr() for r in range(R)]
         P = self.batches_x.shape[0]
         bidx = [(t * R + r) % P for r in range(R)]
-        if self.inputs_pending:
-            main.wait_event(self.ev_inputs)
-            self.inputs_pending = False
         ws, wsb = self.ws, self.ws_bytes
 
         def W(r, li):
@@ -303,7 +383,8 @@ class StaleSGD:
         cur = [self.batches_x[b].data_ptr() for b in bidx]
         inp = [None] * nL
         for li, L in enumerate(self.shapes):
-            main.wait_event(self.ev_layer[li][max(ver[r][li] for r in range(R)) % K])
+            if not graph:
+                main.wait_event(self.ev_layer[li][max(ver[r][li] for r in range(R)) % K])
             inp[li] = cur
             outs = [self.outs[li][r].data_ptr() for r in range(R)]
             if L.kind == "conv":
@@ -328,7 +409,8 @@ class StaleSGD:
             L = self.shapes[li]
             prev = self.shapes[li - 1] if li > 0 else None
             # update t-2 (the last reader of GradBuf set t % 2) of this layer has finished
-            main.wait_event(self.ev_layer[li][max(t - 1, 0) % K])
+            if not graph:
+                main.wait_event(self.ev_layer[li][max(t - 1, 0) % K])
             dw = [gb[r] + 4 * L.w_off for r in range(R)]
             db = [gb[r] + 4 * L.b_off for r in range(R)]
             if L.kind == "fc":
@@ -356,7 +438,8 @@ class StaleSGD:
             self.ev_bwd[li].record(main)
             upd.wait_event(self.ev_bwd[li])
             self._update_layer(t, li, upd)
-            self.ev_layer[li][(t + 1) % K].record(upd)
+            if not graph:
+                self.ev_layer[li][(t + 1) % K].record(upd)
             if prev is None:
                 break
             if prev.kind == "conv" and prev.pool:
@@ -368,6 +451,11 @@ class StaleSGD:
                 # the conv branch routed into g already: g holds the next layer's gradient
             else:
                 g, h = h, g
+        if graph:
+            # join the update stream: the next replay starts after this step's updates
+            self.ev_graph_upd.record(upd)
+            main.wait_event(self.ev_graph_upd)
+            return
         self.gradbuf = self.gradbuf_sets[t % 2]   # the GradBufs of the step just issued
         self.t = t + 1
 
@@ -376,6 +464,12 @@ class StaleSGD:
         issued so far (the last step's updates may still run on the update
         stream when step() returns)."""
         st = self.main_stream if stream is None else stream
+        if self._graph_steps:   # graph replays end with the update stream joined
+            if st is not self.main_stream:
+                ev = torch.cuda.Event()
+                ev.record(self.main_stream)
+                st.wait_event(ev)
+            return
         for evs in self.ev_layer:
             st.wait_event(evs[self.t % self.K])
 
