@@ -1406,7 +1406,10 @@ extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* 
         (rc = check_ptr_array(__func__, "y", reinterpret_cast<const void* const*>(y), batch, false, false)))
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (batch > 1 && plan_fc(N, in, out, true).fwd_tc) {
+    // grouped tensor-core launch; narrow outputs (e.g. a 10-way classifier, out % 4 != 0) too
+    // when the last-round k split is available (few tiles, long k): direct stores write y
+    const bool tail_room = ws && ws_bytes >= tail_bytes();
+    if (batch > 1 && (plan_fc(N, in, out, true).fwd_tc || (in % 4 == 0 && in >= 256 && tail_room))) {
         TcParams p = base_params();
         p.epi = EPI_STORE;
         p.ldd = out;

@@ -203,6 +203,8 @@ FC_BATCHED_CASES = [
     (3, 37, 50, 10),       # CUDA-core paths, looped per problem
     (2, 64, 48, 10),       # grouped tensor-core dW, short-reduction dX
     (5, 42, 128, 7),       # grouped float4 skinny forward (8-wide accumulators), ragged row block
+    (4, 96, 512, 10),      # narrow output, long k: grouped tensor cores + k-split last round (with workspace)
+    (3, 64, 300, 13),      # the same with a ragged k tile and 13 outputs
 ]
 
 
