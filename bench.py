@@ -129,15 +129,15 @@ class GemmProbe:
         self.orig = sprint_mod.sprint_fc_fwd_batched
         probe = self
 
-        def fc_fwd_batched(x, w, b, y, N, i, o, relu, ws=None, ws_bytes=0, stream=None):
+        def fc_fwd_batched(x, w, b, y, N, i, o, relu, ws=None, ws_bytes=0, stream=None, yT=None):
             if not (probe.active and (i, o) in probe.shapes):
-                return probe.orig(x, w, b, y, N, i, o, relu, ws, ws_bytes, stream)
+                return probe.orig(x, w, b, y, N, i, o, relu, ws, ws_bytes, stream, yT)
             st = (torch.cuda.ExternalStream(stream) if isinstance(stream, int) and stream != 0
                   else torch.cuda.current_stream())
             a = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             a.record(st)
-            r = probe.orig(x, w, b, y, N, i, o, relu, ws, ws_bytes, stream)
+            r = probe.orig(x, w, b, y, N, i, o, relu, ws, ws_bytes, stream, yT)
             e.record(st)
             probe.events.append((a, e, 2.0 * N * i * o * len(x)))
             probe.desc = f"tc_gemm_kernel (grouped FC forward, {len(x)} x {N}x{o}x{i}, TF32)"

@@ -207,8 +207,13 @@ size_t sprint_fc_bwd_static_scratch_bytes(void);
  * of b and relu_src may also be NULL individually. batch = 0 is a no-op.
  * Problems must not write the same memory. */
 int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b, float* const* y,
-                          int batch, int N, int in, int out, int relu, void* ws, size_t ws_bytes,
+                          float* const* yT, int batch, int N, int in, int out, int relu, void* ws, size_t ws_bytes,
                           sprint_stream_t stream);
+/* yT (nullable array): also write each output transposed, yT[g] = device
+ * [out][N] (row j = column j of y[g]), the k-contiguous operand a following
+ * layer's weight-gradient GEMM reads (the TF32 tensor-core MMA takes only
+ * k-contiguous operands). The tensor-core epilogue stores it next to y; other
+ * paths transpose y afterwards. Must not overlap y or x. */
 
 /* Optional workspace of sprint_fc_fwd_batched (device, 16-byte aligned): with
  * at least this many bytes the tensor-core launch may split the k range of its
@@ -222,10 +227,25 @@ size_t sprint_fc_fwd_batched_workspace_size(void);
  * its GEMMs (optional: a workspace holding only the slices is accepted). */
 size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int out, int have_wT);
 
-int sprint_fc_bwd_batched(const float* const* x, const float* const* w, const float* const* wT,
-                          const float* const* dy, const float* const* relu_src, float* const* dx, float* const* dw,
+int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const float* const* w,
+                          const float* const* wT, const float* const* dy, const float* const* dyT,
+                          const float* const* relu_src, float* const* dx, float* const* dxT, float* const* dw,
                           float* const* db, float alpha, int accumulate, int batch, int N, int in, int out, void* ws,
                           size_t ws_bytes, sprint_stream_t stream);
+/* Optional transposed operands and outputs (nullable arrays; with all three
+ * NULL the call is the plain batched backward):
+ *  xT1[g]: device [in + 1][N], x[g] transposed (row i = column i of x[g])
+ *    followed by one row of N ones. The weight-gradient GEMM reads it instead
+ *    of transposing x, and the row of ones gives that GEMM one more output
+ *    column, sum_n dy[g][n][o], which becomes db (alpha / accumulate as for
+ *    db): dedb is computed inside the dedw GEMM ([S] Sec. 3.2, dedb = the
+ *    column sums of dE/dy). x is still required (paths that do not take the
+ *    tensor cores read it).
+ *  dyT[g]: device [out][N], dy[g] transposed (read instead of transposing dy).
+ *  dxT[g]: device [in][N], written with dx[g] transposed (needs dx); what the
+ *    layer below passes as its dyT.
+ * Results are those of the plain call up to the rounding of db (a TF32 GEMM
+ * column instead of an fp32 sum when xT1 is given). */
 
 /* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
  * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must

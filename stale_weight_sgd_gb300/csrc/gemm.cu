@@ -324,6 +324,7 @@ TcParams base_params() {
     p.alpha = 1.f;
     p.splits = 1;
     p.tap_sign = 1;
+    p.vec_col = -1;
     p.status = device_status_ptr();
     return p;
 }
@@ -1181,7 +1182,8 @@ bool gemm2d_tc(const float* A, long long lda, const float* B, long long ldb, int
 // before the first launch; false if one cannot be (nothing launched then).
 bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B, long long ldb, int M, int N, int K,
                      TcParams p, const float* const* bias, const float* const* mask, float* const* D, int G,
-                     cudaStream_t s, int* rc, float* tail_ws = nullptr, size_t tail_ws_bytes = 0) {
+                     cudaStream_t s, int* rc, float* tail_ws = nullptr, size_t tail_ws_bytes = 0,
+                     float* const* DT = nullptr, float* const* vec = nullptr) {
     *rc = SPRINT_OK;
     if (G <= 0) return true;
     const long long m_tiles = (M + TC_BM - 1) / TC_BM;
@@ -1194,7 +1196,9 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
     const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 4};
     const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)ldb * 4};
     const uint32_t ba[2] = {32, 128}, bb[2] = {32, tl.b_rows()};
-    const uint64_t dd[2] = {(uint64_t)N, (uint64_t)M}, sd[1] = {(uint64_t)p.ldd * 4};
+    // D holds the columns before the vector column (p.vec_col, with vec), all N otherwise
+    if (!vec) p.vec_col = -1;
+    const uint64_t dd[2] = {(uint64_t)(p.vec_col >= 0 ? p.vec_col : N), (uint64_t)M}, sd[1] = {(uint64_t)p.ldd * 4};
     const uint32_t bd[2] = {32, 32};
     bool tma_store = (p.ldd & 3) == 0;
     for (int g = 0; g < G && tma_store; ++g) tma_store = aligned16(D[g]);
@@ -1223,6 +1227,8 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
             p.g_bias[i] = (i < n && bias) ? bias[g0 + i] : nullptr;
             p.g_mask[i] = (i < n && mask) ? mask[g0 + i] : nullptr;
             p.g_D[i] = i < n ? D[g0 + i] : nullptr;
+            p.g_DT[i] = (i < n && DT) ? DT[g0 + i] : nullptr;
+            p.g_vec[i] = (i < n && vec) ? vec[g0 + i] : nullptr;
         }
         const long long units = m_units * n_tiles * n;
         p.tail_splits = 1;
@@ -1394,8 +1400,8 @@ extern "C" size_t sprint_fc_batched_workspace_size(int batch, int N, int in, int
 extern "C" size_t sprint_fc_fwd_batched_workspace_size(void) { return tail_bytes(); }
 
 extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* w, const float* const* b,
-                                     float* const* y, int batch, int N, int in, int out, int relu, void* ws,
-                                     size_t ws_bytes, sprint_stream_t stream) {
+                                     float* const* y, float* const* yT, int batch, int N, int in, int out, int relu,
+                                     void* ws, size_t ws_bytes, sprint_stream_t stream) {
     SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
                    "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", __func__, batch, N, in, out);
     if (batch == 0) return SPRINT_OK;
@@ -1403,29 +1409,40 @@ extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* 
     if ((rc = check_ptr_array(__func__, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
         (rc = check_ptr_array(__func__, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
         (rc = check_ptr_array(__func__, "b", reinterpret_cast<const void* const*>(b), batch, true, true)) ||
-        (rc = check_ptr_array(__func__, "y", reinterpret_cast<const void* const*>(y), batch, false, false)))
+        (rc = check_ptr_array(__func__, "y", reinterpret_cast<const void* const*>(y), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "yT", reinterpret_cast<const void* const*>(yT), batch, true, false)))
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // grouped tensor-core launch; narrow outputs (e.g. a 10-way classifier, out % 4 != 0) too
     // when the last-round k split is available (few tiles, long k): direct stores write y
+    // (and the transposed copy, rows of N, when asked for)
     const bool tail_room = ws && ws_bytes >= tail_bytes();
+    bool done = false;
     if (batch > 1 && (plan_fc(N, in, out, true).fwd_tc || (in % 4 == 0 && in >= 256 && tail_room))) {
         TcParams p = base_params();
         p.epi = EPI_STORE;
         p.ldd = out;
         p.relu = relu;
-        if (gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc, static_cast<float*>(ws),
-                            ws_bytes))
-            return rc;
+        p.lddT = N;
+        done = gemm2d_tc_group(x, in, w, in, N, out, in, p, b, nullptr, y, batch, s, &rc, static_cast<float*>(ws),
+                               ws_bytes, yT);
+        if (rc) return rc;
+        if (done) return SPRINT_OK;
     }
-    if (out <= kSkinnyN && in % 4 == 0) return launch_skinny4(x, w, b, y, batch, N, out, in, relu, s);
-    for (int g = 0; g < batch; ++g)
-        if ((rc = sprint_fc_fwd(x[g], w[g], b ? b[g] : nullptr, y[g], N, in, out, relu, stream))) return rc;
+    if (out <= kSkinnyN && in % 4 == 0) {
+        if ((rc = launch_skinny4(x, w, b, y, batch, N, out, in, relu, s))) return rc;
+    } else {
+        for (int g = 0; g < batch; ++g)
+            if ((rc = sprint_fc_fwd(x[g], w[g], b ? b[g] : nullptr, y[g], N, in, out, relu, stream))) return rc;
+    }
+    // paths without the transposed store: transpose the result
+    if (yT) return launch_transpose_group(const_cast<const float* const*>(y), yT, batch, N, out, s);
     return SPRINT_OK;
 }
 
-extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* w, const float* const* wT,
-                                     const float* const* dy, const float* const* relu_src, float* const* dx,
+extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const float* const* w,
+                                     const float* const* wT, const float* const* dy, const float* const* dyT,
+                                     const float* const* relu_src, float* const* dx, float* const* dxT,
                                      float* const* dw, float* const* db, float alpha, int accumulate, int batch, int N,
                                      int in, int out, void* ws, size_t ws_bytes, sprint_stream_t stream) {
     SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
@@ -1433,15 +1450,19 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
     if (batch == 0) return SPRINT_OK;
     int rc;
     if ((rc = check_ptr_array(__func__, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "xT1", reinterpret_cast<const void* const*>(xT1), batch, true, false)) ||
         (rc = check_ptr_array(__func__, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
         (rc = check_ptr_array(__func__, "wT", reinterpret_cast<const void* const*>(wT), batch, true, false)) ||
         (rc = check_ptr_array(__func__, "dy", reinterpret_cast<const void* const*>(dy), batch, false, false)) ||
+        (rc = check_ptr_array(__func__, "dyT", reinterpret_cast<const void* const*>(dyT), batch, true, false)) ||
         (rc = check_ptr_array(__func__, "relu_src", reinterpret_cast<const void* const*>(relu_src), batch, true,
                               true)) ||
         (rc = check_ptr_array(__func__, "dx", reinterpret_cast<const void* const*>(dx), batch, true, false)) ||
+        (rc = check_ptr_array(__func__, "dxT", reinterpret_cast<const void* const*>(dxT), batch, true, false)) ||
         (rc = check_ptr_array(__func__, "dw", reinterpret_cast<const void* const*>(dw), batch, false, false)) ||
         (rc = check_ptr_array(__func__, "db", reinterpret_cast<const void* const*>(db), batch, true, false)))
         return rc;
+    SPRINT_REQUIRE(!dxT || dx, SPRINT_ERR_INVALID_ARG, "%s: dxT needs dx", __func__);
     FcPlan pl = plan_fc(N, in, out, wT != nullptr);
     if (!dx) pl.ws_wT = 0;
     const size_t per = round256(pl.total());
@@ -1450,19 +1471,20 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
     float* tail_ws = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + per * batch) : nullptr;
     const size_t tail_ws_bytes = ws ? ws_bytes - per * batch : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (batch == 1)
+    const bool extras = xT1 || dyT || dxT;
+    if (batch == 1 && !extras)
         return sprint_fc_bwd(x[0], w[0], wT ? wT[0] : nullptr, dy[0], relu_src ? relu_src[0] : nullptr,
                              dx ? dx[0] : nullptr, dw[0], db ? db[0] : nullptr, alpha, accumulate, N, in, out, ws,
                              ws_bytes, stream);
     char* wsb = static_cast<char*>(ws);
-    std::vector<float*> ws_wT(batch), xT(batch), dyT(batch);
+    std::vector<float*> ws_wT(batch), xT(batch), dyT_ws(batch);
     for (int g = 0; g < batch; ++g) {
         ws_wT[g] = reinterpret_cast<float*>(wsb + g * per);
         xT[g] = reinterpret_cast<float*>(wsb + g * per + pl.ws_wT);
-        dyT[g] = reinterpret_cast<float*>(wsb + g * per + pl.ws_wT + pl.ws_xT);
+        dyT_ws[g] = reinterpret_cast<float*>(wsb + g * per + pl.ws_wT + pl.ws_xT);
     }
 
-    // dedx fc: dx_g = mask_g * (dy_g . (w_g^T)^T)
+    // dedx fc: dx_g = mask_g * (dy_g . (w_g^T)^T) (and its transpose, rows of N, when asked for)
     if (dx) {
         bool done = false;
         if (pl.dx_tc) {
@@ -1475,42 +1497,58 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
             p.epi = EPI_MASK;
             p.ldd = in;
             p.ldm = in;
+            p.lddT = N;
             done = gemm2d_tc_group(dy, out, wt, out, N, in, out, p, nullptr, relu_src, dx, batch, s, &rc, tail_ws,
-                                   tail_ws_bytes);
+                                   tail_ws_bytes, dxT);
             if (rc) return rc;
         }
-        if (!done && out <= 32 && in % 4 == 0) {
-            if ((rc = launch_smallk_dx4(dy, w, relu_src, dx, batch, N, in, out, s))) return rc;
-            done = true;
-        }
         if (!done) {
-            for (int g = 0; g < batch; ++g) {
-                if (out <= 32) {
-                    smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(
-                        dy[g], w[g], relu_src ? relu_src[g] : nullptr, dx[g], N, in, out);
-                    if ((rc = check_launch("smallk_dx_kernel"))) return rc;
-                } else {
-                    SimtGemm q{N, in, out, dy[g], out, 1, w[g], 1, in, dx[g], in, nullptr,
-                               relu_src ? relu_src[g] : nullptr, in, 1.f, 0, 0, SIMT_MASK};
-                    if ((rc = launch_simt_gemm(q, s))) return rc;
+            if (out <= 32 && in % 4 == 0) {
+                if ((rc = launch_smallk_dx4(dy, w, relu_src, dx, batch, N, in, out, s))) return rc;
+            } else {
+                for (int g = 0; g < batch; ++g) {
+                    if (out <= 32) {
+                        smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(
+                            dy[g], w[g], relu_src ? relu_src[g] : nullptr, dx[g], N, in, out);
+                        if ((rc = check_launch("smallk_dx_kernel"))) return rc;
+                    } else {
+                        SimtGemm q{N, in, out, dy[g], out, 1, w[g], 1, in, dx[g], in, nullptr,
+                                   relu_src ? relu_src[g] : nullptr, in, 1.f, 0, 0, SIMT_MASK};
+                        if ((rc = launch_simt_gemm(q, s))) return rc;
+                    }
                 }
             }
+            if (dxT && (rc = launch_transpose_group(const_cast<const float* const*>(dx), dxT, batch, N, in, s)))
+                return rc;
         }
     }
-    // dedw: dw_g = acc*dw_g + alpha * (dy_g^T) . (x_g^T)^T
+    // dedw: dw_g = acc*dw_g + alpha * (dy_g^T) . (x_g^T)^T; with x^T followed by a row of
+    // ones (xT1) the same GEMM's column `in` is dedb = alpha * sum_i dy_g[i] (+ acc*db_g)
+    bool db_done = false;
     {
         bool done = false;
         if (pl.dw_tc) {
-            if ((rc = launch_transpose_group(x, xT.data(), batch, N, in, s))) return rc;
-            if ((rc = launch_transpose_group(dy, dyT.data(), batch, N, out, s))) return rc;
+            const float* const* bt = xT1;
+            if (!bt) {
+                if ((rc = launch_transpose_group(x, xT.data(), batch, N, in, s))) return rc;
+                bt = xT.data();
+            }
+            const float* const* at = dyT;
+            if (!at) {
+                if ((rc = launch_transpose_group(dy, dyT_ws.data(), batch, N, out, s))) return rc;
+                at = dyT_ws.data();
+            }
             TcParams p = base_params();
             p.epi = EPI_ACCUM;
             p.ldd = in;
             p.alpha = alpha;
             p.accumulate = accumulate;
-            done = gemm2d_tc_group(dyT.data(), N, xT.data(), N, out, in, N, p, nullptr, nullptr, dw, batch, s, &rc,
-                                   tail_ws, tail_ws_bytes);
+            const bool with_db = xT1 && db;
+            if (with_db) p.vec_col = in;
+            done = gemm2d_tc_group(at, N, bt, N, out, with_db ? in + 1 : in, N, p, nullptr, nullptr, dw, batch, s,
+                                   &rc, tail_ws, tail_ws_bytes, nullptr, with_db ? db : nullptr);
             if (rc) return rc;
+            db_done = done && with_db;
         }
         if (!done) {
             for (int g = 0; g < batch; ++g) {
@@ -1521,7 +1559,7 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
         }
     }
     // dedb
-    if (db) return launch_colsum_group(dy, db, batch, N, out, alpha, accumulate, s);
+    if (db && !db_done) return launch_colsum_group(dy, db, batch, N, out, alpha, accumulate, s);
     return SPRINT_OK;
 }
 

@@ -139,6 +139,17 @@ struct TcParams {
     const float* g_bias[TC_MAX_GROUP];
     const float* g_mask[TC_MAX_GROUP];
     float* g_D[TC_MAX_GROUP];
+    // grouped launches, direct stores by the thread that owns the row:
+    //  g_DT[z] (optional): a transposed copy of the output, DT[n * lddT + m]
+    //  (EPI_STORE, EPI_MASK);
+    //  vec_col >= 0 (EPI_ACCUM): GEMM column vec_col is not part of D (which
+    //  holds the vec_col columns before it) but lands in g_vec[z][m], with the
+    //  same alpha / accumulate epilogue (a column of ones appended to B turns
+    //  it into the row sums of A)
+    int vec_col;
+    long long lddT;
+    float* g_DT[TC_MAX_GROUP];
+    float* g_vec[TC_MAX_GROUP];
 };
 
 #if defined(__CUDACC__)
@@ -568,6 +579,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int q = 0; q < 32; ++q) o[q] *= p.alpha;
                     }
                 }
+                // columns of D (the vector column, if any, is stored apart)
+                const int ncols = (G > 1 && p.vec_col >= 0) ? p.vec_col : p.N;
+                if constexpr (G > 1) {
+                    if (!to_partial && row_off >= 0) {
+                        const long long m = m0 + r;
+                        if (p.vec_col >= ncol0 && p.vec_col < ncol0 + 32) {
+                            float x = 0.f;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q)
+                                if (ncol0 + q == p.vec_col) x = o[q];
+                            float* vp = p.g_vec[tc.z] + m;
+                            if (p.accumulate) x += *vp;
+                            *vp = x;
+                        }
+                        float* DT = p.g_DT[tc.z];
+                        if (DT) {
+                            // lanes hold consecutive rows: each column is one 128-byte warp store
+                            DT += static_cast<long long>(ncol0) * p.lddT + m;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q)
+                                if (ncol0 + q < ncols) DT[q * p.lddT] = o[q];
+                        }
+                    }
+                }
                 if (p.store != ST_DIRECT) {
                     // stage the 32 x 32 chunk (128B-swizzled rows) and hand it to TMA
                     if (pending) {
@@ -588,7 +623,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         inside = pw0 + row0 % p.bw < p.out_w && ph0 + (row0 / p.bw) % p.bh < p.out_h &&
                                  pn0 + row0 / (p.bw * p.bh) < p.img_n;
                     } else {
-                        inside = m0 + warp * 32 < p.M;
+                        inside = m0 + warp * 32 < p.M && ncol0 < ncols;
                     }
                     if (lane == 0 && inside) {
                         const bool add = (p.epi == EPI_ACCUM) && p.accumulate && !to_partial;
@@ -626,11 +661,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 long long col_shift = 0;
                 if constexpr (ROLE == ROLE_CONV_WGRAD) col_shift = static_cast<long long>(tap) * p.N;
                 float* dst = Dout + row_off + col_shift + ncol0;
-                const bool vec = (ncol0 + 32 <= p.N) && (p.ldd & 3) == 0;
+                const bool vec = (ncol0 + 32 <= ncols) && (p.ldd & 3) == 0;
                 if (p.epi == EPI_ACCUM && p.accumulate) {
 #pragma unroll
                     for (int q = 0; q < 32; ++q)
-                        if (ncol0 + q < p.N) o[q] += dst[q];
+                        if (ncol0 + q < ncols) o[q] += dst[q];
                 }
                 if (vec) {
 #pragma unroll
@@ -639,7 +674,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 } else {
 #pragma unroll
                     for (int q = 0; q < 32; ++q)
-                        if (ncol0 + q < p.N) dst[q] = o[q];
+                        if (ncol0 + q < ncols) dst[q] = o[q];
                 }
             }
         }
@@ -660,67 +695,102 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // Finishes the tail-split tiles of a GEMM_2D launch: out = epilogue(sum of
-// the tile's tail_splits slabs, added in k-range order). One thread per 4
-// consecutive columns of a tile row; TM = 256 (pair) or 128.
+// the tile's tail_splits slabs, added in k-range order). A block takes one
+// 32 x 32 patch of a tile at a time, a thread 4 consecutive columns of one
+// patch row (8 threads cover a 128-byte row segment); the transposed copy, if
+// any, goes out through shared memory so that its stores are row segments too.
+// TM = 256 (pair) or 128.
 template <int BN, int TM, int ROLE>
 __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail_tiles) {
+    __shared__ float patch[32][33];
     if (p.m_tiles <= 0 || p.n_tiles <= 0) return;
-    const long long per_tile = static_cast<long long>(TM) * (BN / 4);
-    const long long total = per_tile * tail_tiles;
-    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int j = static_cast<int>(idx / per_tile);
-        const int rem = static_cast<int>(idx % per_tile);
-        const int row = rem / (BN / 4), col = (rem % (BN / 4)) * 4;
+    constexpr int PR = TM / 32, PC = BN / 32;   // patches per tile: rows, columns
+    const long long patches = static_cast<long long>(tail_tiles) * PR * PC;
+    const int prow = threadIdx.x >> 3, pcol = (threadIdx.x & 7) * 4;
+    const bool grouped = p.z_tiles > 1 || p.g_D[0] != nullptr;
+    for (long long pi = blockIdx.x; pi < patches; pi += gridDim.x) {
+        const int j = static_cast<int>(pi / (PR * PC));
+        const int rem = static_cast<int>(pi % (PR * PC));
+        const int row0 = (rem / PC) * 32, col0 = (rem % PC) * 32;
         // decompose the tile as the kernel did (units are m-fastest; a pair unit spans TM rows)
         const int tt = p.tail_start + j;
         const int mu = tt % p.m_tiles, rr = tt / p.m_tiles;
         const int nt = rr % p.n_tiles, z = rr / p.n_tiles;
+        if (z >= p.z_tiles || z >= TC_MAX_GROUP || nt * BN + col0 >= p.N) continue;   // whole patch (uniform)
+        const int row = row0 + prow, col = col0 + pcol;
         const int n0 = nt * BN + col;
-        if (n0 >= p.N || z >= p.z_tiles || z >= TC_MAX_GROUP) continue;
-        long long m;   // output row (GEMM_2D) or output pixel (CONV_IMPL) of this slab row
+        long long m = -1;   // output row (GEMM_2D) or output pixel (CONV_IMPL) of this slab row; -1 outside
         if constexpr (ROLE == ROLE_CONV_IMPL) {
             // slab row = rank * 128 + r of the unit's box(es); the box decomposition of the epilogue
             const int mt = TM == 256 ? 2 * mu + row / 128 : mu, r = row % 128;
             const int ow = (mt % p.tiles_w) * p.bw + r % p.bw;
             const int oh = ((mt / p.tiles_w) % p.tiles_h) * p.bh + (r / p.bw) % p.bh;
             const int on = (mt / (p.tiles_w * p.tiles_h)) * p.bimg + r / (p.bw * p.bh);
-            if (ow >= p.out_w || oh >= p.out_h || on >= p.img_n) continue;
-            m = (static_cast<long long>(on) * p.out_h + oh) * p.out_w + ow;
+            if (ow < p.out_w && oh < p.out_h && on < p.img_n)
+                m = (static_cast<long long>(on) * p.out_h + oh) * p.out_w + ow;
         } else {
             m = static_cast<long long>(mu) * TM + row;
-            if (m >= p.M) continue;
+            if (m >= p.M) m = -1;
         }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 0; sp < p.tail_splits; ++sp) {
-            const float4 v = *reinterpret_cast<const float4*>(
-                p.tail_part + ((static_cast<long long>(j) * p.tail_splits + sp) * TM + row) * BN + col);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        float o[4] = {acc.x, acc.y, acc.z, acc.w};
-        const bool grouped = p.z_tiles > 1 || p.g_D[0] != nullptr;
         float* D = grouped ? p.g_D[z] : p.D;
         const float* bias = grouped ? p.g_bias[z] : p.bias;
         const float* mask = grouped ? p.g_mask[z] : p.mask;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int n = n0 + q;
-            if (n >= p.N) break;
-            float x = o[q];
-            float* d = D + m * p.ldd + n;
-            if (p.epi == EPI_STORE) {
-                if (bias) x += bias[n];
-                if (p.relu) x = fmaxf(x, 0.f);
-            } else if (p.epi == EPI_MASK) {
-                if (mask && !(mask[m * p.ldm + n] > 0.f)) x = 0.f;
-            } else {
-                x *= p.alpha;
-                if (p.accumulate) x += *d;
+        float* DT = (ROLE == ROLE_GEMM_2D && grouped) ? p.g_DT[z] : nullptr;
+        float* vec = (ROLE == ROLE_GEMM_2D && grouped && p.vec_col >= 0) ? p.g_vec[z] : nullptr;
+        const int ncols = vec ? p.vec_col : p.N;
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m >= 0 && n0 < p.N) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < p.tail_splits; ++sp) {
+                const float4 v = *reinterpret_cast<const float4*>(
+                    p.tail_part + ((static_cast<long long>(j) * p.tail_splits + sp) * TM + row) * BN + col);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
             }
-            *d = x;
+            o[0] = acc.x;
+            o[1] = acc.y;
+            o[2] = acc.z;
+            o[3] = acc.w;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = n0 + q;
+                if (n >= p.N || n > ncols) break;
+                float x = o[q];
+                float* d = (n < ncols) ? D + m * p.ldd + n : vec + m;
+                if (p.epi == EPI_STORE) {
+                    if (bias) x += bias[n];
+                    if (p.relu) x = fmaxf(x, 0.f);
+                } else if (p.epi == EPI_MASK) {
+                    if (mask && !(mask[m * p.ldm + n] > 0.f)) x = 0.f;
+                } else {
+                    x *= p.alpha;
+                    if (p.accumulate) x += *d;
+                }
+                o[q] = x;
+                *d = x;
+            }
+        }
+        if (DT) {   // uniform over the block
+#pragma unroll
+            for (int q = 0; q < 4; ++q) patch[prow][pcol + q] = o[q];
+            __syncthreads();
+            const int c = threadIdx.x >> 3, r0 = (threadIdx.x & 7) * 4;   // patch column, first of 4 rows
+            const int n = nt * BN + col0 + c;
+            const long long mb = static_cast<long long>(mu) * TM + row0 + r0;
+            if (n < ncols) {
+                float* dt = DT + static_cast<long long>(n) * p.lddT + mb;
+                if (mb + 4 <= p.M && (p.lddT & 3) == 0 && (mb & 3) == 0) {
+                    *reinterpret_cast<float4*>(dt) =
+                        make_float4(patch[r0][c], patch[r0 + 1][c], patch[r0 + 2][c], patch[r0 + 3][c]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (mb + q < p.M) dt[q] = patch[r0 + q][c];
+                }
+            }
+            __syncthreads();
         }
     }
 }

@@ -52,10 +52,10 @@ _SIGS = {
     "sprint_fc_workspace_size": ([I, I, I, I], SZ),
     "sprint_fc_bwd_static_scratch": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P], I),
     "sprint_fc_bwd_static_scratch_bytes": ([], SZ),
-    "sprint_fc_fwd_batched": ([P, P, P, P, I, I, I, I, I, P, SZ, P], I),
+    "sprint_fc_fwd_batched": ([P, P, P, P, P, I, I, I, I, I, P, SZ, P], I),
     "sprint_fc_fwd_batched_workspace_size": ([], SZ),
     "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
-    "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
+    "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
     "sprint_pool_fwd": ([P, P, P, I, I, I, I, P], I),
     "sprint_pool_bwd": ([P, P, P, P, I, I, I, I, P], I),
@@ -217,11 +217,11 @@ def _opt_array(items):
     return None if items is None else _ptr_array(items)
 
 
-def sprint_fc_fwd_batched(x, w, b, y, N, fin, fout, relu, ws=None, ws_bytes=0, stream=None):
+def sprint_fc_fwd_batched(x, w, b, y, N, fin, fout, relu, ws=None, ws_bytes=0, stream=None, yT=None):
     n = len(x)
     return _check("sprint_fc_fwd_batched", lib().sprint_fc_fwd_batched(
-        _ptr_array(x), _ptr_array(w), _opt_array(b), _ptr_array(y), n, N, fin, fout, int(relu), _p(ws), ws_bytes,
-        _s(stream)))
+        _ptr_array(x), _ptr_array(w), _opt_array(b), _ptr_array(y), _opt_array(yT), n, N, fin, fout, int(relu),
+        _p(ws), ws_bytes, _s(stream)))
 
 
 def sprint_fc_fwd_batched_workspace_size() -> int:
@@ -233,12 +233,12 @@ def sprint_fc_batched_workspace_size(batch, N, fin, fout, have_wT) -> int:
 
 
 def sprint_fc_bwd_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, fin, fout, ws=None, ws_bytes=0,
-                          stream=None):
+                          stream=None, xT1=None, dyT=None, dxT=None):
     n = len(x)
     return _check("sprint_fc_bwd_batched", lib().sprint_fc_bwd_batched(
-        _ptr_array(x), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(relu_src), _opt_array(dx),
-        _ptr_array(dw), _opt_array(db), float(alpha), int(accumulate), n, N, fin, fout, _p(ws), ws_bytes,
-        _s(stream)))
+        _ptr_array(x), _opt_array(xT1), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(dyT),
+        _opt_array(relu_src), _opt_array(dx), _opt_array(dxT), _ptr_array(dw), _opt_array(db), float(alpha),
+        int(accumulate), n, N, fin, fout, _p(ws), ws_bytes, _s(stream)))
 
 
 def sprint_softmax_xent_batched(logits, labels, loss, dlogits, N, C, reduction_sum=0, stream=None):

@@ -146,10 +146,14 @@ class StaleSGD:
             return torch.empty((R, stride), dtype=dtype, device=self.dev)[:, :numel]
 
         self.outs, self.pooled, self.argmax = [], [], []
+        # FC layers followed by an FC layer also keep their output transposed,
+        # [out + 1][N] with a last row of ones (the next layer's xT1 operand:
+        # its weight-gradient GEMM reads it as is and yields db in the same pass)
+        self.outsT = []
         big = 0
         ws_bytes = 0
         conv_ws = 0
-        for L in self.shapes:
+        for li, L in enumerate(self.shapes):
             if L.kind == "conv":
                 numel = N * L.h * L.w * L.cout
                 big = max(big, numel, N * L.h * L.w * L.cin)
@@ -171,8 +175,18 @@ class StaleSGD:
                 self.argmax.append(None)
                 ws_bytes = max(ws_bytes, S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 1),
                                S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 0))
+            nxt = self.shapes[li + 1] if li + 1 < len(self.shapes) else None
+            if L.kind == "fc" and nxt is not None and nxt.kind == "fc":
+                t = rows((L.cout + 1) * N)
+                t[:, L.cout * N:].fill_(1.0)
+                self.outsT.append(t)
+            else:
+                self.outsT.append(None)
         self.g = rows(big)
         self.h = rows(big)
+        # dE/dy of FC layers transposed ([out][N]), written by the dX GEMM of the layer above
+        self.gT = rows(big)
+        self.hT = rows(big)
         self.ws = torch.empty(max(max(ws_bytes, conv_ws) // 4 + 64, 64), **f32)
         self.ws_bytes = self.ws.numel() * 4
         self.conv_ws_bytes = conv_ws
@@ -396,11 +410,15 @@ class StaleSGD:
                 self._per_replica(fwd)
                 cur = [self.pooled[li][r].data_ptr() for r in range(R)] if L.pool else outs
             else:
+                yT = None if self.outsT[li] is None else [self.outsT[li][r].data_ptr() for r in range(R)]
                 S.sprint_fc_fwd_batched(cur, [W(r, li) for r in range(R)], [B(r, li) for r in range(R)], outs, N,
-                                        L.cin, L.cout, int(L.relu), ws, wsb, sh)
+                                        L.cin, L.cout, int(L.relu), ws, wsb, sh, yT=yT)
                 cur = outs
         g = [self.g[r].data_ptr() for r in range(R)]
         h = [self.h[r].data_ptr() for r in range(R)]
+        gT = None   # g transposed, when the layer above wrote it
+        hT_all = [self.hT[r].data_ptr() for r in range(R)]
+        gT_all = [self.gT[r].data_ptr() for r in range(R)]
         S.sprint_softmax_xent_batched(cur, [self.batches_y[b].data_ptr() for b in bidx],
                                       [self.loss[r].data_ptr() for r in range(R)], g, N, self.classes, 0, sh)
 
@@ -413,14 +431,19 @@ class StaleSGD:
                 main.wait_event(self.ev_layer[li][max(t - 1, 0) % K])
             dw = [gb[r] + 4 * L.w_off for r in range(R)]
             db = [gb[r] + 4 * L.b_off for r in range(R)]
+            hT = None
             if L.kind == "fc":
                 relu_src = None
                 if prev is not None and not (prev.kind == "conv" and prev.pool) and prev.relu:
                     relu_src = inp[li]
+                xT1 = None
+                if prev is not None and self.outsT[li - 1] is not None:
+                    xT1 = [self.outsT[li - 1][r].data_ptr() for r in range(R)]
+                    hT = hT_all   # the layer below is FC too: it reads dE/dy transposed
                 S.sprint_fc_bwd_batched(inp[li], [W(r, li) for r in range(R)],
                                         [WT(r, li) for r in range(R)] if prev is not None else None, g, relu_src,
                                         h if prev is not None else None, dw, db, 1.0, 0, N, L.cin, L.cout, ws, wsb,
-                                        sh)
+                                        sh, xT1=xT1, dyT=gT, dxT=hT)
             else:
                 def bwd(r, st, rws, rwsb, li=li, L=L, prev=prev, g=g, h=h, dw=dw, db=db):
                     S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, 0, N, L.h, L.w, L.cin, L.cout, 1, rws, rwsb,
@@ -451,6 +474,7 @@ class StaleSGD:
                 # the conv branch routed into g already: g holds the next layer's gradient
             else:
                 g, h = h, g
+                gT, hT_all, gT_all = hT, gT_all, hT_all
         if graph:
             # join the update stream: the next replay starts after this step's updates
             self.ev_graph_upd.record(upd)

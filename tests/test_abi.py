@@ -78,21 +78,29 @@ def test_batched_entry_points_validate(S):
     mis = (P * 3)(16, 36, 48)
     nul = (P * 3)(16, None, 48)
     # batch 0 is a no-op; shapes checked first
-    assert L.sprint_fc_fwd_batched(None, None, None, None, 0, 8, 8, 8, 0, None, 0, None) == 0
-    assert L.sprint_fc_fwd_batched(ok, ok, None, ok, 3, 0, 8, 8, 0,None, 0, None) == 2
-    assert L.sprint_fc_fwd_batched(None, ok, None, ok, 3, 8, 8, 8, 0,None, 0, None) == 1      # NULL array
-    assert L.sprint_fc_fwd_batched(ok, nul, None, ok, 3, 8, 8, 8, 0,None, 0, None) == 1       # NULL entry
-    assert L.sprint_fc_fwd_batched(ok, ok, mis, ok, 3, 8, 8, 8, 0,None, 0, None) == 3         # misaligned bias entry
+    assert L.sprint_fc_fwd_batched(None, None, None, None, None, 0, 8, 8, 8, 0, None, 0, None) == 0
+    assert L.sprint_fc_fwd_batched(ok, ok, None, ok, None, 3, 0, 8, 8, 0,None, 0, None) == 2
+    assert L.sprint_fc_fwd_batched(None, ok, None, ok, None, 3, 8, 8, 8, 0,None, 0, None) == 1      # NULL array
+    assert L.sprint_fc_fwd_batched(ok, nul, None, ok, None, 3, 8, 8, 8, 0,None, 0, None) == 1       # NULL entry
+    assert L.sprint_fc_fwd_batched(ok, ok, mis, ok, None, 3, 8, 8, 8, 0,None, 0, None) == 3         # misaligned bias entry
     assert "b[1]" in S.sprint_last_error()
     need = S.sprint_fc_batched_workspace_size(3, 64, 256, 512, 0)
     tail = S.sprint_fc_fwd_batched_workspace_size()
     assert tail > 0 and need >= 3 * S.sprint_fc_workspace_size(64, 256, 512, 0) + tail
     need -= tail   # the per-problem slices alone are accepted
     assert S.sprint_fc_batched_workspace_size(0, 64, 256, 512, 0) == 0
-    rc = L.sprint_fc_bwd_batched(ok, ok, None, ok, None, ok, ok, None, f1, 0, 3, 64, 256, 512, 16, need - 16, None)
+    # (x, xT1, w, wT, dy, dyT, relu_src, dx, dxT, dw, db, ...)
+    rc = L.sprint_fc_bwd_batched(ok, None, ok, None, ok, None, None, ok, None, ok, None, f1, 0, 3, 64, 256, 512, 16,
+                                 need - 16, None)
     assert rc == 7 and "workspace" in S.sprint_last_error()
-    assert L.sprint_fc_bwd_batched(ok, ok, None, ok, None, ok, None, None, f1, 0, 3, 64, 256, 512, 16, need,
-                                   None) == 1   # dw array is required
+    assert L.sprint_fc_bwd_batched(ok, None, ok, None, ok, None, None, ok, None, None, None, f1, 0, 3, 64, 256, 512,
+                                   16, need, None) == 1   # dw array is required
+    assert L.sprint_fc_bwd_batched(ok, mis, ok, None, ok, None, None, ok, None, ok, None, f1, 0, 3, 64, 256, 512,
+                                   16, need, None) == 3   # misaligned xT1 entry
+    assert "xT1[1]" in S.sprint_last_error()
+    assert L.sprint_fc_bwd_batched(ok, None, ok, None, ok, None, None, None, ok, ok, None, f1, 0, 3, 64, 256, 512,
+                                   16, need, None) == 1   # dxT without dx
+    assert L.sprint_fc_fwd_batched(ok, ok, None, ok, nul, 3, 8, 8, 8, 0, None, 0, None) == 1   # NULL yT entry
     assert L.sprint_softmax_xent_batched(ok, ok, ok, nul, 3, 8, 10, 0, None) == 1
     assert L.sprint_softmax_xent_batched(ok, ok, mis, ok, 3, 8, 10, 0, None) == 3
     assert L.sprint_softmax_xent_batched(None, None, None, None, 0, 8, 10, 0, None) == 0

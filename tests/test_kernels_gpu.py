@@ -271,6 +271,71 @@ def test_fc_bwd_batched(S, G, N, fin, fout, with_wT, with_dx, accumulate, tail):
     _status_clean(S)
 
 
+@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES + [(4, 512, 3072, 5000)])
+@pytest.mark.parametrize("tail", [0, 1])
+def test_fc_fwd_batched_transposed_copy(S, G, N, fin, fout, tail):
+    """yT: the same outputs as the plain call, bit for bit, and their exact transpose."""
+    probs = [_fc_problem(14, g, N, fin, fout) for g in range(G)]
+    xs = [dev(p[0]) for p in probs]
+    ws = [dev(p[1]) for p in probs]
+    bs = [dev(p[2]) for p in probs]
+    nb = S.sprint_fc_fwd_batched_workspace_size() if tail else 0
+    wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda") if tail else None
+    ys = [torch.empty((N, fout), dtype=torch.float32, device="cuda") for _ in range(G)]
+    ys2 = [torch.empty((N, fout), dtype=torch.float32, device="cuda") for _ in range(G)]
+    yTs = [torch.full((fout + 1, N), 7.0, dtype=torch.float32, device="cuda") for _ in range(G)]
+    S.sprint_fc_fwd_batched(xs, ws, bs, ys, N, fin, fout, 1, wsb, nb)
+    S.sprint_fc_fwd_batched(xs, ws, bs, ys2, N, fin, fout, 1, wsb, nb, yT=yTs)
+    for g, (x, w, b, _) in enumerate(probs):
+        y, y2, yT = host(ys[g]), host(ys2[g]), host(yTs[g])
+        assert np.array_equal(y, y2), g
+        assert np.array_equal(yT[:fout], y.T), g
+        assert np.all(yT[fout] == 7.0), g          # the row past the output is not written
+        assert rel_inf(y, O.relu(O.fc_fwd(x, w, b))) <= TOL_TF32, g
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("G,N,fin,fout", FC_BATCHED_CASES + [(4, 512, 5000, 5000)])
+@pytest.mark.parametrize("accumulate,tail", [(0, 1), (1, 1), (1, 0)])
+def test_fc_bwd_batched_transposed_operands(S, G, N, fin, fout, accumulate, tail):
+    """xT1 / dyT / dxT: x^T with a row of ones (dedb inside the dedw GEMM), dy^T read
+    as given, dx^T written next to dx; results as the oracle's, dxT the exact transpose."""
+    probs = [_fc_problem(15, g, N, fin, fout) for g in range(G)]
+    alpha = 0.5
+    xs = [dev(p[0]) for p in probs]
+    xT1 = [dev(np.concatenate([p[0].T, np.ones((1, N), np.float32)])) for p in probs]
+    ws = [dev(p[1]) for p in probs]
+    wTs = [dev(np.ascontiguousarray(p[1].T)) for p in probs]
+    dys = [dev(p[3]) for p in probs]
+    dyT = [dev(np.ascontiguousarray(p[3].T)) for p in probs]
+    masks = [xs[g] if g % 2 == 0 else None for g in range(G)]
+    dxs = [torch.empty((N, fin), dtype=torch.float32, device="cuda") for _ in range(G)]
+    dxT = [torch.empty((fin, N), dtype=torch.float32, device="cuda") for _ in range(G)]
+    dw0 = [_f32(15, f"dw0{g}", (fout, fin)) for g in range(G)]
+    db0 = [_f32(15, f"db0{g}", fout) for g in range(G)]
+    dws = [dev(a) for a in dw0]
+    dbs = [dev(a) for a in db0]
+    nb = S.sprint_fc_batched_workspace_size(G, N, fin, fout, 1)
+    if not tail:
+        nb -= S.sprint_fc_fwd_batched_workspace_size()
+    wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
+    S.sprint_fc_bwd_batched(xs, ws, wTs, dys, masks, dxs, dws, dbs, alpha, accumulate, N, fin, fout, wsb, nb,
+                            xT1=xT1, dyT=dyT, dxT=dxT)
+    for g, (x, w, _, dy) in enumerate(probs):
+        dx_ref, dw_ref, db_ref = O.fc_bwd(x, w, dy)
+        if g % 2 == 0:
+            dx_ref = dx_ref * O.relu_mask(x)
+        dw_ref = O.gradbuf_accumulate(dw0[g], dw_ref, alpha, not accumulate)
+        db_ref = O.gradbuf_accumulate(db0[g], db_ref, alpha, not accumulate)
+        dx = host(dxs[g])
+        assert rel_inf(dx, dx_ref) <= TOL_TF32, g
+        assert np.array_equal(host(dxT[g]), dx.T), g
+        assert rel_inf(host(dws[g]), dw_ref) <= TOL_TF32, g
+        # db: a column of the TF32 dedw GEMM when that runs on the tensor cores
+        assert rel_inf(host(dbs[g]), db_ref) <= TOL_TF32, g
+    _status_clean(S)
+
+
 @pytest.mark.parametrize("G,N,C", [(4, 512, 10), (3, 64, 1000), (17, 33, 7)])
 def test_softmax_xent_batched(S, G, N, C):
     zs = [_f32(13, f"z{g}", (N, C), 3.0) for g in range(G)]
