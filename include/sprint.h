@@ -247,6 +247,32 @@ int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const 
  * Results are those of the plain call up to the rounding of db (a TF32 GEMM
  * column instead of an fp32 sum when xT1 is given). */
 
+/* Update rules of the parameter-server apply (see sprint_apply_update_*). */
+typedef enum { SPRINT_OPT_SGD = 0, SPRINT_OPT_MOMENTUM = 1, SPRINT_OPT_ADAGRAD = 2 } sprint_opt;
+
+/* The batched FC backward of the R replicas of one layer (arguments as
+ * sprint_fc_bwd_batched; each dw[g] / db[g] is replica g's GradBuf, Algorithm 1)
+ * followed by the parameter-server apply of that layer over those `batch`
+ * GradBufs (SumGradient + UpdateWeights of Algorithm 2, [S] Sec. 3):
+ *   S = dw[0] + dw[1] + ... + dw[batch-1]  (added in g order, per element)
+ *   w_out = rule(w_in, S) with `opt` and eta, nu_or_eps exactly as
+ *   sprint_apply_update_sgd / _momentum / _adagrad compute it (bit for bit);
+ *   b_out = rule(b_in, db[0] + ... + db[batch-1]) when db is given;
+ *   wT_out (nullable): also w_out transposed, device [in][out].
+ * w_in, w_out, w_state: device [out][in] (w_state: the momentum v or the
+ * Adagrad G of w, updated in place; unused for SGD); b_in, b_out, b_state:
+ * device [out] (required when db is given). w_out may equal w_in (in place)
+ * but must not overlap any other argument. 1 <= batch <= 16.
+ * The update runs after the backward pass in stream order: W' (and W'^T in
+ * the same pass, as sprint_apply_update_t), then b'. */
+int sprint_fc_bwd_update_batched(const float* const* x, const float* const* xT1, const float* const* w,
+                                 const float* const* wT, const float* const* dy, const float* const* dyT,
+                                 const float* const* relu_src, float* const* dx, float* const* dxT, float* const* dw,
+                                 float* const* db, float alpha, int accumulate, int batch, int N, int in, int out,
+                                 int opt, const float* w_in, const float* b_in, float* w_out, float* b_out,
+                                 float* wT_out, float* w_state, float* b_state, float eta, float nu_or_eps, void* ws,
+                                 size_t ws_bytes, sprint_stream_t stream);
+
 /* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
  * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must
  * not alias. */
@@ -310,6 +336,18 @@ int sprint_apply_update_momentum(const float* w_in, float* w_out, float* v, cons
                                  size_t n, float eta, float nu, sprint_stream_t stream);
 int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const float* const* bufs, int k, size_t n,
                                 float eta, float eps, sprint_stream_t stream);
+
+/* The same update of a row-major [rows][cols] weight matrix (n = rows*cols)
+ * by rule `opt` (sprint_opt; nu_or_eps = nu for momentum, eps for Adagrad,
+ * unused for SGD), bit for bit what the rule's sprint_apply_update_* call
+ * computes, that also writes W' transposed: wT_out[c*rows + r] =
+ * w_out[r*cols + c] (device [cols][rows]: the copy the input-gradient GEMMs
+ * read, written in the same pass instead of reading W' back). state: v or G
+ * (device [rows][cols], in place; NULL for SGD). wT_out must not overlap the
+ * other arguments; w_out may equal w_in. 1 <= k <= 16. */
+int sprint_apply_update_t(int opt, const float* w_in, float* w_out, float* wT_out, float* state,
+                          const float* const* bufs, int k, int rows, int cols, float eta, float nu_or_eps,
+                          sprint_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Staleness schedule (host only) — the delays of asynchronous SGD ([S] Sec. 1,

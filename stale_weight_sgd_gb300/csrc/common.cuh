@@ -44,6 +44,17 @@ enum : int {
 // split longer lists into launches of this many)
 constexpr int kMaxGroup = 16;
 
+// parameter-server update rules (the values of sprint_opt)
+enum PsOpt : int { PS_SGD = 0, PS_MOMENTUM = 1, PS_ADAGRAD = 2 };
+
+// the standalone update kernels by rule over k GradBufs (update.cu); the _t
+// form updates a row-major [rows][cols] matrix and also writes W' transposed
+int launch_ps_update(int opt, const char* fn, const float* w_in, float* w_out, float* state, const float* const* bufs,
+                     int k, size_t n, float eta, float hp, sprint_stream_t stream);
+int launch_ps_update_t(int opt, const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
+                       const float* const* bufs, int k, int rows, int cols, float eta, float hp,
+                       sprint_stream_t stream);
+
 // ---------------------------------------------------------------- device side
 #if defined(__CUDACC__)
 
@@ -330,6 +341,27 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int n, bool a_mn_major, bool b
            | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(n >> 3) << 17)   // N >> 3
            | (static_cast<uint32_t>(m >> 4) << 24);  // M >> 4
+}
+
+// One parameter of the parameter-server update (UpdateWeights of Algorithm 2
+// in the SPRINT report; DistBelief's w' := w - eta*dw), given the summed
+// gradient s: SGD w' = w - eta*s; momentum v' = hp*v - eta*s, w' = w + v';
+// Adagrad G' = G + s*s, w' = w - eta*s/(sqrt(G') + hp). The standalone update
+// kernel and the update fused into the weight-gradient GEMM both call this, so
+// they round identically.
+template <int OPT>
+__device__ __forceinline__ void ps_apply1(float s, float w, float* state, float eta, float hp, float& w_new) {
+    if constexpr (OPT == PS_SGD) {
+        w_new = w - eta * s;
+    } else if constexpr (OPT == PS_MOMENTUM) {
+        const float v = hp * (*state) - eta * s;
+        *state = v;
+        w_new = w + v;
+    } else {
+        const float g = *state + s * s;
+        *state = g;
+        w_new = w - eta * s / (sqrtf(g) + hp);
+    }
 }
 
 #endif  // __CUDACC__

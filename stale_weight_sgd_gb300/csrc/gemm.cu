@@ -115,15 +115,16 @@ int launch_tc_bn(const TcMaps<G>& maps, const TcParams& p, cudaStream_t s) {
             return check_cuda("cudaFuncSetAttribute(tc_gemm_kernel)");
         attr_done[dev] = true;
     }
+    const int work = p.num_tiles;
     if constexpr (!PAIR) {
         // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
-        const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+        const int grid = work < num_sms() ? work : num_sms();
         tc_gemm_kernel<ROLE, BN, false, G><<<grid, TC_THREADS, tc_smem_bytes(BN, false), s>>>(maps, p);
         return check_launch("tc_gemm_kernel");
     } else {
         // persistent pairs: at most as many clusters as can be resident together
         const int slots = pair_slots<ROLE, BN, G>();
-        const int pairs = p.num_tiles < slots ? p.num_tiles : slots;
+        const int pairs = work < slots ? work : slots;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1440,42 +1441,91 @@ extern "C" int sprint_fc_fwd_batched(const float* const* x, const float* const* 
     return SPRINT_OK;
 }
 
-extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const float* const* w,
-                                     const float* const* wT, const float* const* dy, const float* const* dyT,
-                                     const float* const* relu_src, float* const* dx, float* const* dxT,
-                                     float* const* dw, float* const* db, float alpha, int accumulate, int batch, int N,
-                                     int in, int out, void* ws, size_t ws_bytes, sprint_stream_t stream) {
+// the parameter-server update of one FC layer over the batch's GradBufs
+struct PsArgs {
+    int opt;
+    const float* w_in;
+    const float* b_in;
+    float* w_out;
+    float* b_out;
+    float* wT_out;
+    float* w_state;
+    float* b_state;
+    float eta, hp;
+};
+
+static int fc_bwd_batched_impl(const char* fn, const float* const* x, const float* const* xT1, const float* const* w,
+                               const float* const* wT, const float* const* dy, const float* const* dyT,
+                               const float* const* relu_src, float* const* dx, float* const* dxT, float* const* dw,
+                               float* const* db, float alpha, int accumulate, int batch, int N, int in, int out,
+                               void* ws, size_t ws_bytes, sprint_stream_t stream, const PsArgs* ps) {
     SPRINT_REQUIRE(batch >= 0 && N >= 1 && in >= 1 && out >= 1, SPRINT_ERR_SHAPE,
-                   "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", __func__, batch, N, in, out);
+                   "%s: need batch >= 0 and N, in, out >= 1 (got %d, %d, %d, %d)", fn, batch, N, in, out);
     if (batch == 0) return SPRINT_OK;
     int rc;
-    if ((rc = check_ptr_array(__func__, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
-        (rc = check_ptr_array(__func__, "xT1", reinterpret_cast<const void* const*>(xT1), batch, true, false)) ||
-        (rc = check_ptr_array(__func__, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
-        (rc = check_ptr_array(__func__, "wT", reinterpret_cast<const void* const*>(wT), batch, true, false)) ||
-        (rc = check_ptr_array(__func__, "dy", reinterpret_cast<const void* const*>(dy), batch, false, false)) ||
-        (rc = check_ptr_array(__func__, "dyT", reinterpret_cast<const void* const*>(dyT), batch, true, false)) ||
-        (rc = check_ptr_array(__func__, "relu_src", reinterpret_cast<const void* const*>(relu_src), batch, true,
+    if ((rc = check_ptr_array(fn, "x", reinterpret_cast<const void* const*>(x), batch, false, false)) ||
+        (rc = check_ptr_array(fn, "xT1", reinterpret_cast<const void* const*>(xT1), batch, true, false)) ||
+        (rc = check_ptr_array(fn, "w", reinterpret_cast<const void* const*>(w), batch, false, false)) ||
+        (rc = check_ptr_array(fn, "wT", reinterpret_cast<const void* const*>(wT), batch, true, false)) ||
+        (rc = check_ptr_array(fn, "dy", reinterpret_cast<const void* const*>(dy), batch, false, false)) ||
+        (rc = check_ptr_array(fn, "dyT", reinterpret_cast<const void* const*>(dyT), batch, true, false)) ||
+        (rc = check_ptr_array(fn, "relu_src", reinterpret_cast<const void* const*>(relu_src), batch, true,
                               true)) ||
-        (rc = check_ptr_array(__func__, "dx", reinterpret_cast<const void* const*>(dx), batch, true, false)) ||
-        (rc = check_ptr_array(__func__, "dxT", reinterpret_cast<const void* const*>(dxT), batch, true, false)) ||
-        (rc = check_ptr_array(__func__, "dw", reinterpret_cast<const void* const*>(dw), batch, false, false)) ||
-        (rc = check_ptr_array(__func__, "db", reinterpret_cast<const void* const*>(db), batch, true, false)))
+        (rc = check_ptr_array(fn, "dx", reinterpret_cast<const void* const*>(dx), batch, true, false)) ||
+        (rc = check_ptr_array(fn, "dxT", reinterpret_cast<const void* const*>(dxT), batch, true, false)) ||
+        (rc = check_ptr_array(fn, "dw", reinterpret_cast<const void* const*>(dw), batch, false, false)) ||
+        (rc = check_ptr_array(fn, "db", reinterpret_cast<const void* const*>(db), batch, true, false)))
         return rc;
-    SPRINT_REQUIRE(!dxT || dx, SPRINT_ERR_INVALID_ARG, "%s: dxT needs dx", __func__);
+    SPRINT_REQUIRE(!dxT || dx, SPRINT_ERR_INVALID_ARG, "%s: dxT needs dx", fn);
     FcPlan pl = plan_fc(N, in, out, wT != nullptr);
     if (!dx) pl.ws_wT = 0;
     const size_t per = round256(pl.total());
-    if ((rc = check_ws(__func__, ws, ws_bytes, per * batch))) return rc;
+    if ((rc = check_ws(fn, ws, ws_bytes, per * batch))) return rc;
     // what follows the per-problem slices serves the tail split of the GEMMs (optional)
     float* tail_ws = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + per * batch) : nullptr;
     const size_t tail_ws_bytes = ws ? ws_bytes - per * batch : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ps) {
+        SPRINT_REQUIRE(ps->opt >= PS_SGD && ps->opt <= PS_ADAGRAD, SPRINT_ERR_INVALID_ARG, "%s: unknown update rule %d",
+                       fn, ps->opt);
+        SPRINT_REQUIRE(batch <= kMaxGroup, SPRINT_ERR_UNSUPPORTED, "%s: the update sums at most %d GradBufs (got %d)",
+                       fn, kMaxGroup, batch);
+        SPRINT_REQUIRE(ps->w_in && ps->w_out && (ps->opt == PS_SGD || ps->w_state), SPRINT_ERR_INVALID_ARG,
+                       "%s: NULL w_in, w_out or w_state", fn);
+        SPRINT_REQUIRE(!db || (ps->b_in && ps->b_out && (ps->opt == PS_SGD || ps->b_state)), SPRINT_ERR_INVALID_ARG,
+                       "%s: NULL b_in, b_out or b_state", fn);
+        SPRINT_REQUIRE(aligned16(ps->w_in) && aligned16(ps->w_out) && (!ps->w_state || aligned16(ps->w_state)) &&
+                           (!ps->wT_out || aligned16(ps->wT_out)) && (!ps->b_in || aligned16(ps->b_in)) &&
+                           (!ps->b_out || aligned16(ps->b_out)) && (!ps->b_state || aligned16(ps->b_state)),
+                       SPRINT_ERR_ALIGN, "%s: update pointers must be 16-byte aligned", fn);
+    }
+    // the update by the standalone kernels (what the weight-gradient GEMM did not fuse)
+    // the layer's update after its backward pass (in stream order): W' (and W'^T in
+    // the same pass), then b'
+    auto finish_ps = [&]() -> int {
+        if (!ps) return SPRINT_OK;
+        int r;
+        const float* const* bufs = const_cast<const float* const*>(dw);
+        if (ps->wT_out)
+            r = launch_ps_update_t(ps->opt, fn, ps->w_in, ps->w_out, ps->wT_out, ps->w_state, bufs, batch, out, in,
+                                   ps->eta, ps->hp, stream);
+        else
+            r = launch_ps_update(ps->opt, fn, ps->w_in, ps->w_out, ps->w_state, bufs, batch,
+                                 static_cast<size_t>(out) * in, ps->eta, ps->hp, stream);
+        if (r) return r;
+        if (db)
+            return launch_ps_update(ps->opt, fn, ps->b_in, ps->b_out, ps->b_state, const_cast<const float* const*>(db),
+                                    batch, static_cast<size_t>(out), ps->eta, ps->hp, stream);
+        return SPRINT_OK;
+    };
     const bool extras = xT1 || dyT || dxT;
-    if (batch == 1 && !extras)
-        return sprint_fc_bwd(x[0], w[0], wT ? wT[0] : nullptr, dy[0], relu_src ? relu_src[0] : nullptr,
-                             dx ? dx[0] : nullptr, dw[0], db ? db[0] : nullptr, alpha, accumulate, N, in, out, ws,
-                             ws_bytes, stream);
+    if (batch == 1 && !extras) {
+        if ((rc = sprint_fc_bwd(x[0], w[0], wT ? wT[0] : nullptr, dy[0], relu_src ? relu_src[0] : nullptr,
+                                dx ? dx[0] : nullptr, dw[0], db ? db[0] : nullptr, alpha, accumulate, N, in, out, ws,
+                                ws_bytes, stream)))
+            return rc;
+        return finish_ps();
+    }
     char* wsb = static_cast<char*>(ws);
     std::vector<float*> ws_wT(batch), xT(batch), dyT_ws(batch);
     for (int g = 0; g < batch; ++g) {
@@ -1559,8 +1609,30 @@ extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* 
         }
     }
     // dedb
-    if (db && !db_done) return launch_colsum_group(dy, db, batch, N, out, alpha, accumulate, s);
-    return SPRINT_OK;
+    if (db && !db_done && (rc = launch_colsum_group(dy, db, batch, N, out, alpha, accumulate, s))) return rc;
+    return finish_ps();
+}
+
+extern "C" int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const float* const* w,
+                                     const float* const* wT, const float* const* dy, const float* const* dyT,
+                                     const float* const* relu_src, float* const* dx, float* const* dxT,
+                                     float* const* dw, float* const* db, float alpha, int accumulate, int batch, int N,
+                                     int in, int out, void* ws, size_t ws_bytes, sprint_stream_t stream) {
+    return fc_bwd_batched_impl(__func__, x, xT1, w, wT, dy, dyT, relu_src, dx, dxT, dw, db, alpha, accumulate, batch,
+                               N, in, out, ws, ws_bytes, stream, nullptr);
+}
+
+extern "C" int sprint_fc_bwd_update_batched(const float* const* x, const float* const* xT1, const float* const* w,
+                                            const float* const* wT, const float* const* dy, const float* const* dyT,
+                                            const float* const* relu_src, float* const* dx, float* const* dxT,
+                                            float* const* dw, float* const* db, float alpha, int accumulate,
+                                            int batch, int N, int in, int out, int opt, const float* w_in,
+                                            const float* b_in, float* w_out, float* b_out, float* wT_out,
+                                            float* w_state, float* b_state, float eta, float nu_or_eps, void* ws,
+                                            size_t ws_bytes, sprint_stream_t stream) {
+    const PsArgs ps{opt, w_in, b_in, w_out, b_out, wT_out, w_state, b_state, eta, nu_or_eps};
+    return fc_bwd_batched_impl(__func__, x, xT1, w, wT, dy, dyT, relu_src, dx, dxT, dw, db, alpha, accumulate, batch,
+                               N, in, out, ws, ws_bytes, stream, &ps);
 }
 
 // ====================================================================== conv

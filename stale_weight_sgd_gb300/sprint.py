@@ -56,6 +56,9 @@ _SIGS = {
     "sprint_fc_fwd_batched_workspace_size": ([], SZ),
     "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
     "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
+    "sprint_apply_update_t": ([I, P, P, P, P, P, I, I, I, F, F, P], I),
+    "sprint_fc_bwd_update_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, I, P, P, P, P, P, P, P, F, F, P,
+                                      SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
     "sprint_pool_fwd": ([P, P, P, I, I, I, I, P], I),
     "sprint_pool_bwd": ([P, P, P, P, I, I, I, I, P], I),
@@ -239,6 +242,26 @@ def sprint_fc_bwd_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate,
         _ptr_array(x), _opt_array(xT1), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(dyT),
         _opt_array(relu_src), _opt_array(dx), _opt_array(dxT), _ptr_array(dw), _opt_array(db), float(alpha),
         int(accumulate), n, N, fin, fout, _p(ws), ws_bytes, _s(stream)))
+
+
+SPRINT_OPT = {"sgd": 0, "momentum": 1, "adagrad": 2}
+
+
+def sprint_apply_update_t(opt, w_in, w_out, wT_out, state, bufs, rows, cols, eta, nu_or_eps=0.0, stream=None):
+    return _check("sprint_apply_update_t", lib().sprint_apply_update_t(
+        SPRINT_OPT.get(opt, opt), _p(w_in), _p(w_out), _p(wT_out), _p(state), _ptr_array(bufs), len(bufs), rows, cols,
+        float(eta), float(nu_or_eps), _s(stream)))
+
+
+def sprint_fc_bwd_update_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, fin, fout, opt, w_in, b_in,
+                                 w_out, b_out, wT_out, w_state, b_state, eta, nu_or_eps, ws=None, ws_bytes=0,
+                                 stream=None, xT1=None, dyT=None, dxT=None):
+    n = len(x)
+    return _check("sprint_fc_bwd_update_batched", lib().sprint_fc_bwd_update_batched(
+        _ptr_array(x), _opt_array(xT1), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(dyT),
+        _opt_array(relu_src), _opt_array(dx), _opt_array(dxT), _ptr_array(dw), _opt_array(db), float(alpha),
+        int(accumulate), n, N, fin, fout, SPRINT_OPT.get(opt, opt), _p(w_in), _p(b_in), _p(w_out), _p(b_out),
+        _p(wT_out), _p(w_state), _p(b_state), float(eta), float(nu_or_eps), _p(ws), ws_bytes, _s(stream)))
 
 
 def sprint_softmax_xent_batched(logits, labels, loss, dlogits, N, C, reduction_sum=0, stream=None):

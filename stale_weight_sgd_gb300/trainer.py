@@ -261,23 +261,37 @@ class StaleSGD:
 
     def _update_layer(self, t, li, stream):
         """SumGradient + UpdateWeights (Algorithm 2) of layer li: W_l(t+1) into
-        ring slot t+1, then its transpose."""
+        ring slot t+1, with its transpose written in the same pass (layers after
+        the first), then b."""
         off, cnt = self.span[li]
         slot_in, slot_out = t % (self.S + 1), (t + 1) % (self.S + 1)
-        w_in = self.ring[slot_in].data_ptr() + 4 * off
-        w_out = self.ring[slot_out].data_ptr() + 4 * off
-        bufs = [self.gradbuf_sets[t % 2][r].data_ptr() + 4 * off for r in range(self.R)]
         sh = stream.cuda_stream
-        if self.optimizer == "sgd":
-            S.sprint_apply_update_sgd(w_in, w_out, bufs, cnt, self.eta, sh)
-        elif self.optimizer == "momentum":
-            S.sprint_apply_update_momentum(w_in, w_out, self.opt_state.data_ptr() + 4 * off, bufs, cnt, self.eta,
-                                           self.nu, sh)
-        else:
-            S.sprint_apply_update_adagrad(w_in, w_out, self.opt_state.data_ptr() + 4 * off, bufs, cnt, self.eta,
-                                          self.eps, sh)
-        if li > 0:
-            self._transpose_layer(li, slot_out, stream)
+        hp = self.eps if self.optimizer == "adagrad" else self.nu
+        gb = self.gradbuf_sets[t % 2]
+
+        def ptrs(o):
+            return (self.ring[slot_in].data_ptr() + 4 * o, self.ring[slot_out].data_ptr() + 4 * o,
+                    self.opt_state.data_ptr() + 4 * o if self.opt_state is not None else None,
+                    [gb[r].data_ptr() + 4 * o for r in range(self.R)])
+
+        def plain(o, n):
+            w_in, w_out, st, bufs = ptrs(o)
+            if self.optimizer == "sgd":
+                S.sprint_apply_update_sgd(w_in, w_out, bufs, n, self.eta, sh)
+            elif self.optimizer == "momentum":
+                S.sprint_apply_update_momentum(w_in, w_out, st, bufs, n, self.eta, self.nu, sh)
+            else:
+                S.sprint_apply_update_adagrad(w_in, w_out, st, bufs, n, self.eta, self.eps, sh)
+
+        if li == 0:   # no input gradient: no transpose; W, b and padding in one pass
+            plain(off, cnt)
+            return
+        L = self.shapes[li]
+        rows, cols = (L.cout, 9 * L.cin) if L.kind == "conv" else (L.cout, L.cin)
+        w_in, w_out, st, bufs = ptrs(L.w_off)
+        wT = self.ringT[slot_out].data_ptr() + 4 * L.w_off
+        S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh)
+        plain(L.b_off, L.cout)
 
     def _per_replica(self, fn):
         """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica

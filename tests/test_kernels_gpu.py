@@ -56,6 +56,40 @@ def test_update(S, k, n, opt):
     assert rel_inf(host(dout), ref) <= TOL_UPDATE
 
 
+@pytest.mark.parametrize("rows,cols", [(300, 136), (37, 27), (64, 4096), (129, 260)])
+@pytest.mark.parametrize("k", [1, 4, 16])
+@pytest.mark.parametrize("opt", ["sgd", "momentum", "adagrad"])
+def test_update_transposed(S, rows, cols, k, opt):
+    """sprint_apply_update_t: W', state bit for bit the flat update's; W'^T its exact transpose;
+    W' against the oracle's update."""
+    n = rows * cols
+    w = _f32(4, f"w{n}", n, 0.01)
+    bufs = [_f32(4, f"g{j}/{n}", n, 1e-3) for j in range(k)]
+    st0 = np.abs(_f32(4, f"s{n}", n, 1e-2)) + (0.1 if opt == "adagrad" else 0.0)
+    eta, hp = 0.01, (1e-8 if opt == "adagrad" else 0.9)
+    dbufs = [dev(b) for b in bufs]
+    dw = dev(w)
+    out_t, out_f = torch.empty_like(dw), torch.empty_like(dw)
+    wT = torch.empty(n, dtype=torch.float32, device="cuda")
+    st_t, st_f = (dev(st0), dev(st0)) if opt != "sgd" else (None, None)
+    S.sprint_apply_update_t(opt, dw, out_t, wT, st_t, dbufs, rows, cols, eta, hp)
+    if opt == "sgd":
+        S.sprint_apply_update_sgd(dw, out_f, dbufs, n, eta)
+        ref = O.update_sgd(w, bufs, eta)
+    elif opt == "momentum":
+        S.sprint_apply_update_momentum(dw, out_f, st_f, dbufs, n, eta, hp)
+        ref, _ = O.update_momentum(w, st0, bufs, eta, hp)
+    else:
+        S.sprint_apply_update_adagrad(dw, out_f, st_f, dbufs, n, eta, hp)
+        ref, _ = O.update_adagrad(w, st0, bufs, eta, hp)
+    a = host(out_t)
+    assert np.array_equal(a, host(out_f))
+    assert np.array_equal(host(wT).reshape(cols, rows), a.reshape(rows, cols).T)
+    if opt != "sgd":
+        assert np.array_equal(host(st_t), host(st_f))
+    assert rel_inf(a, ref) <= TOL_UPDATE
+
+
 def test_update_in_place_and_order_invariance_exact(S):
     n, k = 4099, 8
     w = synth.dyadic(2, "w", n)
@@ -333,6 +367,65 @@ def test_fc_bwd_batched_transposed_operands(S, G, N, fin, fout, accumulate, tail
         assert rel_inf(host(dws[g]), dw_ref) <= TOL_TF32, g
         # db: a column of the TF32 dedw GEMM when that runs on the tensor cores
         assert rel_inf(host(dbs[g]), db_ref) <= TOL_TF32, g
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("G,N,fin,fout", [c for c in FC_BATCHED_CASES if c[0] <= 16] + [(4, 512, 1000, 768), (1, 64, 256, 128)])
+@pytest.mark.parametrize("opt", ["sgd", "momentum", "adagrad"])
+@pytest.mark.parametrize("with_xT1", [0, 1])
+def test_fc_bwd_update_batched(S, G, N, fin, fout, opt, with_xT1):
+    """Backward + the parameter-server apply of the layer over the G GradBufs: GradBufs as
+    the oracle's; W', b' and the optimizer state bit for bit what the standalone update
+    computes from those GradBufs; W'^T the exact transpose of W'."""
+    probs = [_fc_problem(16, g, N, fin, fout) for g in range(G)]
+    xs = [dev(p[0]) for p in probs]
+    ws = [dev(p[1]) for p in probs]
+    wTs = [dev(np.ascontiguousarray(p[1].T)) for p in probs]
+    dys = [dev(p[3]) for p in probs]
+    xT1 = [dev(np.concatenate([p[0].T, np.ones((1, N), np.float32)])) for p in probs] if with_xT1 else None
+    dxs = [torch.empty((N, fin), dtype=torch.float32, device="cuda") for _ in range(G)]
+    dws = [torch.empty((fout, fin), dtype=torch.float32, device="cuda") for _ in range(G)]
+    dbs = [torch.empty(fout, dtype=torch.float32, device="cuda") for _ in range(G)]
+    w_in = dev(_f32(16, "win", (fout, fin), 0.05))
+    b_in = dev(_f32(16, "bin", fout, 0.05))
+    if opt == "adagrad":
+        st0 = np.abs(_f32(16, "st", fout * fin + fout)) + 0.1
+    else:
+        st0 = _f32(16, "st", fout * fin + fout, 0.01)
+    w_st, b_st = dev(st0[:fout * fin].reshape(fout, fin)), dev(st0[fout * fin:])
+    w_out = torch.full((fout, fin), 5.0, dtype=torch.float32, device="cuda")
+    b_out = torch.full((fout,), 5.0, dtype=torch.float32, device="cuda")
+    wT_out = torch.empty((fin, fout), dtype=torch.float32, device="cuda")
+    eta, hp = 0.05, (1e-6 if opt == "adagrad" else 0.9)
+    nb = S.sprint_fc_batched_workspace_size(G, N, fin, fout, 1)
+    wsb = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
+    S.sprint_fc_bwd_update_batched(xs, ws, wTs, dys, None, dxs, dws, dbs, 1.0, 0, N, fin, fout, opt, w_in, b_in, w_out,
+                                   b_out, wT_out, w_st if opt != "sgd" else None, b_st if opt != "sgd" else None, eta,
+                                   hp, wsb, nb, xT1=xT1)
+    for g, (x, w, _, dy) in enumerate(probs):
+        dx_ref, dw_ref, db_ref = O.fc_bwd(x, w, dy)
+        assert rel_inf(host(dxs[g]), dx_ref) <= TOL_TF32, g
+        assert rel_inf(host(dws[g]), dw_ref) <= TOL_TF32, g
+        assert rel_inf(host(dbs[g]), db_ref) <= TOL_TF32, g
+    # the standalone update on the GradBufs just written, from the same starting state
+    w_ref = torch.empty_like(w_out)
+    b_ref = torch.empty_like(b_out)
+    w_st2, b_st2 = dev(st0[:fout * fin].reshape(fout, fin)), dev(st0[fout * fin:])
+    if opt == "sgd":
+        S.sprint_apply_update_sgd(w_in, w_ref, dws, fout * fin, eta)
+        S.sprint_apply_update_sgd(b_in, b_ref, dbs, fout, eta)
+    elif opt == "momentum":
+        S.sprint_apply_update_momentum(w_in, w_ref, w_st2, dws, fout * fin, eta, hp)
+        S.sprint_apply_update_momentum(b_in, b_ref, b_st2, dbs, fout, eta, hp)
+    else:
+        S.sprint_apply_update_adagrad(w_in, w_ref, w_st2, dws, fout * fin, eta, hp)
+        S.sprint_apply_update_adagrad(b_in, b_ref, b_st2, dbs, fout, eta, hp)
+    assert np.array_equal(host(w_out), host(w_ref))
+    assert np.array_equal(host(b_out), host(b_ref))
+    assert np.array_equal(host(wT_out), host(w_out).T)
+    if opt != "sgd":
+        assert np.array_equal(host(w_st), host(w_st2))
+        assert np.array_equal(host(b_st), host(b_st2))
     _status_clean(S)
 
 
