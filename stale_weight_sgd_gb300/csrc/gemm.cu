@@ -663,7 +663,16 @@ struct SmallkGroup {
     const float* w[kMaxGroup];
     const float* mask[kMaxGroup];
     float* dx[kMaxGroup];
+    float* dxT[kMaxGroup];
 };
+
+// dx = mask * (dy . w) for a short reduction (K <= 32, e.g. the classifier's 10
+// outputs), optionally with dxT = dx^T ([N][M]). A thread owns one float4 of
+// columns for SK_ROWS consecutive rows: its K float4 of w are loaded once and
+// reused for every row; a warp covers 128 consecutive columns (512-byte rows
+// of dx, mask). dxT gets the thread's SK_ROWS-long column runs (32 bytes per
+// column, two float4 when M % 4 == 0).
+constexpr int SK_ROWS = 8;
 
 template <int KM>
 __global__ void __launch_bounds__(256) smallk_dx4_kernel(SmallkGroup grp, int M, int N, int K) {
@@ -672,41 +681,74 @@ __global__ void __launch_bounds__(256) smallk_dx4_kernel(SmallkGroup grp, int M,
     const float4* __restrict__ w4 = reinterpret_cast<const float4*>(grp.w[g]);
     const float* __restrict__ mask = grp.mask[g];
     float4* __restrict__ dx4 = reinterpret_cast<float4*>(grp.dx[g]);
+    float* __restrict__ dxT = grp.dxT[g];
     const int N4 = N >> 2;
-    const long long total = static_cast<long long>(M) * N4;
+    const int row_blocks = (M + SK_ROWS - 1) / SK_ROWS;
+    const long long total = static_cast<long long>(row_blocks) * N4;
     for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int n4 = static_cast<int>(idx % N4);
-        const long long m = idx / N4;
-        float d[KM];
+        const int m0 = static_cast<int>(idx / N4) * SK_ROWS;
         float4 wv[KM];
 #pragma unroll
-        for (int k = 0; k < KM; ++k) {
-            d[k] = k < K ? dy[m * K + k] : 0.f;
+        for (int k = 0; k < KM; ++k)
             wv[k] = k < K ? __ldg(w4 + static_cast<long long>(k) * N4 + n4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4 mk = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (mask) mk = __ldcs(reinterpret_cast<const float4*>(mask) + idx);
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 out[SK_ROWS];
 #pragma unroll
-        for (int k = 0; k < KM; ++k) {
-            a.x = fmaf(d[k], wv[k].x, a.x);
-            a.y = fmaf(d[k], wv[k].y, a.y);
-            a.z = fmaf(d[k], wv[k].z, a.z);
-            a.w = fmaf(d[k], wv[k].w, a.w);
+        for (int i = 0; i < SK_ROWS; ++i) {
+            const int m = m0 + i;
+            out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m >= M) continue;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < KM; ++k) {
+                if (k >= K) break;
+                const float d = dy[static_cast<long long>(m) * K + k];
+                a.x = fmaf(d, wv[k].x, a.x);
+                a.y = fmaf(d, wv[k].y, a.y);
+                a.z = fmaf(d, wv[k].z, a.z);
+                a.w = fmaf(d, wv[k].w, a.w);
+            }
+            const long long e = static_cast<long long>(m) * N4 + n4;
+            if (mask) {
+                const float4 mk = __ldcs(reinterpret_cast<const float4*>(mask) + e);
+                a.x = mk.x > 0.f ? a.x : 0.f;
+                a.y = mk.y > 0.f ? a.y : 0.f;
+                a.z = mk.z > 0.f ? a.z : 0.f;
+                a.w = mk.w > 0.f ? a.w : 0.f;
+            }
+            __stcs(dx4 + e, a);
+            out[i] = a;
         }
-        a.x = mk.x > 0.f ? a.x : 0.f;
-        a.y = mk.y > 0.f ? a.y : 0.f;
-        a.z = mk.z > 0.f ? a.z : 0.f;
-        a.w = mk.w > 0.f ? a.w : 0.f;
-        __stcs(dx4 + idx, a);
+        if (dxT) {
+            const int c = 4 * n4;
+            const float col[4][SK_ROWS] = {
+                {out[0].x, out[1].x, out[2].x, out[3].x, out[4].x, out[5].x, out[6].x, out[7].x},
+                {out[0].y, out[1].y, out[2].y, out[3].y, out[4].y, out[5].y, out[6].y, out[7].y},
+                {out[0].z, out[1].z, out[2].z, out[3].z, out[4].z, out[5].z, out[6].z, out[7].z},
+                {out[0].w, out[1].w, out[2].w, out[3].w, out[4].w, out[5].w, out[6].w, out[7].w}};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float* dst = dxT + static_cast<long long>(c + q) * M + m0;
+                if ((M & 3) == 0 && m0 + SK_ROWS <= M) {
+                    __stcs(reinterpret_cast<float4*>(dst), make_float4(col[q][0], col[q][1], col[q][2], col[q][3]));
+                    __stcs(reinterpret_cast<float4*>(dst + 4), make_float4(col[q][4], col[q][5], col[q][6], col[q][7]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < SK_ROWS; ++i)
+                        if (m0 + i < M) dst[i] = col[q][i];
+                }
+            }
+        }
     }
 }
 
-// dx_g = mask_g * (dy_g . w_g) for K <= 32, N % 4 == 0, all problems in as few launches as possible
+// dx_g = mask_g * (dy_g . w_g) (and dxT_g = dx_g^T when dxT is given) for K <= 32,
+// N % 4 == 0, all problems in as few launches as possible
 int launch_smallk_dx4(const float* const* dy, const float* const* w, const float* const* mask, float* const* dx,
-                      int G, int M, int N, int K, cudaStream_t s) {
-    const long long total = static_cast<long long>(M) * (N / 4);
+                      float* const* dxT, int G, int M, int N, int K, cudaStream_t s) {
+    static_assert(SK_ROWS == 8, "the transposed store is written for 8-row runs");
+    const long long total = static_cast<long long>((M + SK_ROWS - 1) / SK_ROWS) * (N / 4);
     long long blocks = (total + 255) / 256;
     const long long cap = 8ll * num_sms();
     if (blocks > cap) blocks = cap;
@@ -718,6 +760,7 @@ int launch_smallk_dx4(const float* const* dy, const float* const* w, const float
             t.w[i] = w[g0 + i];
             t.mask[i] = mask ? mask[g0 + i] : nullptr;
             t.dx[i] = dx[g0 + i];
+            t.dxT[i] = dxT ? dxT[g0 + i] : nullptr;
         }
         const dim3 grid(static_cast<unsigned>(blocks), n);
         if (K <= 8)
@@ -1353,7 +1396,7 @@ extern "C" int sprint_fc_bwd(const float* x, const float* w, const float* wT, co
         }
         if (!done && out <= 32) {
             if (in % 4 == 0) {
-                if ((rc = launch_smallk_dx4(&dy, &w, relu_src ? &relu_src : nullptr, &dx, 1, N, in, out, s)))
+                if ((rc = launch_smallk_dx4(&dy, &w, relu_src ? &relu_src : nullptr, &dx, nullptr, 1, N, in, out, s)))
                     return rc;
             } else {
                 smallk_dx_kernel<<<grid_cap(static_cast<long long>(N) * in), 256, 0, s>>>(dy, w, relu_src, dx, N,
@@ -1553,8 +1596,10 @@ static int fc_bwd_batched_impl(const char* fn, const float* const* x, const floa
             if (rc) return rc;
         }
         if (!done) {
+            bool transposed = false;
             if (out <= 32 && in % 4 == 0) {
-                if ((rc = launch_smallk_dx4(dy, w, relu_src, dx, batch, N, in, out, s))) return rc;
+                if ((rc = launch_smallk_dx4(dy, w, relu_src, dx, dxT, batch, N, in, out, s))) return rc;
+                transposed = true;
             } else {
                 for (int g = 0; g < batch; ++g) {
                     if (out <= 32) {
@@ -1568,7 +1613,8 @@ static int fc_bwd_batched_impl(const char* fn, const float* const* x, const floa
                     }
                 }
             }
-            if (dxT && (rc = launch_transpose_group(const_cast<const float* const*>(dx), dxT, batch, N, in, s)))
+            if (dxT && !transposed &&
+                (rc = launch_transpose_group(const_cast<const float* const*>(dx), dxT, batch, N, in, s)))
                 return rc;
         }
     }

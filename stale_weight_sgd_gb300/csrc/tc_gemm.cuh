@@ -740,10 +740,25 @@ __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail
         const int ncols = vec ? p.vec_col : p.N;
         float o[4] = {0.f, 0.f, 0.f, 0.f};
         if (m >= 0 && n0 < p.N) {
+            // the slabs in k-range order; eight loads in flight before their adds (same order)
+            const float* slab0 = p.tail_part + (static_cast<long long>(j) * p.tail_splits * TM + row) * BN + col;
+            const long long slab_step = static_cast<long long>(TM) * BN;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < p.tail_splits; ++sp) {
-                const float4 v = *reinterpret_cast<const float4*>(
-                    p.tail_part + ((static_cast<long long>(j) * p.tail_splits + sp) * TM + row) * BN + col);
+            int sp = 0;
+            for (; sp + 8 <= p.tail_splits; sp += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const float4*>(slab0 + (sp + u) * slab_step);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
+            for (; sp < p.tail_splits; ++sp) {
+                const float4 v = *reinterpret_cast<const float4*>(slab0 + sp * slab_step);
                 acc.x += v.x;
                 acc.y += v.y;
                 acc.z += v.z;
