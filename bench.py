@@ -169,8 +169,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     # a dedicated stream (not the legacy default stream) for the whole run: the
-    # trainer issues on it, and the probe's events are recorded on it
-    torch.cuda.set_stream(torch.cuda.Stream(dev))
+    # trainer issues on it, and the probe's events are recorded on it. It runs at
+    # high priority so that the training step's kernels (the critical path) are
+    # scheduled ahead of the trainer's low-priority update stream
+    torch.cuda.set_stream(torch.cuda.Stream(dev, priority=-1))
     net = model.NETWORKS[cfg["net"]]
     shapes = model.layer_shapes(net)
     N, R = cfg["batch"], cfg["replicas"]

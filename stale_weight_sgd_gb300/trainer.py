@@ -101,7 +101,9 @@ class StaleSGD:
 
         main = torch.cuda.current_stream(self.dev)
         self.main_stream = main
-        self.upd_stream = torch.cuda.Stream(self.dev) if concurrent else main
+        # lowest priority: on a higher-priority caller stream the backward GEMMs are
+        # scheduled first and the updates take what the GPU has left
+        self.upd_stream = torch.cuda.Stream(self.dev, priority=0) if concurrent else main
         # convolutions of different replicas run side by side (each with its own
         # workspace): the small late layers alone leave most SMs idle
         self.fork = concurrent and self.R > 1 and any(L.kind == "conv" for L in self.shapes)
