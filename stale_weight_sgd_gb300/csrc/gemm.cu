@@ -1263,6 +1263,13 @@ bool gemm2d_tc_group(const float* const* A, long long lda, const float* const* B
     p.N = N;
     p.num_kt = (K + TC_BK - 1) / TC_BK;
     p.kt_per_split = p.num_kt;
+    // problems that share B (replicas reading one weight version): units of one
+    // n-tile of all problems together, so a B tile is read from HBM once and then
+    // from L2 (A, re-read per n-tile, is the small operand here)
+    p.z_mid = 0;
+    for (int g = 1; g < G && !p.z_mid; ++g)
+        for (int h = 0; h < g; ++h)
+            if (B[g] == B[h]) p.z_mid = 1;
     const long long n_tiles = (N + tl.bn - 1) / tl.bn;
     const long long m_units = tl.pair ? (m_tiles + 1) / 2 : m_tiles;
     for (int c = 0; c < chunks; ++c) {

@@ -150,6 +150,10 @@ struct TcParams {
     long long lddT;
     float* g_DT[TC_MAX_GROUP];
     float* g_vec[TC_MAX_GROUP];
+    // unit order m, then z, then n (grouped problems that share B run their
+    // units of one n-tile together, so each B tile comes from HBM once);
+    // 0: m, then n, then z
+    int z_mid;
 };
 
 #if defined(__CUDACC__)
@@ -173,8 +177,13 @@ __host__ __device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& 
     }
     c.mt = tt % p.m_tiles;
     const int r = tt / p.m_tiles;
-    c.nt = r % p.n_tiles;
-    c.z = r / p.n_tiles;
+    if (p.z_mid) {
+        c.z = r % p.z_tiles;
+        c.nt = r / p.z_tiles;
+    } else {
+        c.nt = r % p.n_tiles;
+        c.z = r / p.n_tiles;
+    }
     return c;
 }
 
@@ -715,7 +724,8 @@ __global__ void __launch_bounds__(256) tc_tail_reduce(const TcParams p, int tail
         // decompose the tile as the kernel did (units are m-fastest; a pair unit spans TM rows)
         const int tt = p.tail_start + j;
         const int mu = tt % p.m_tiles, rr = tt / p.m_tiles;
-        const int nt = rr % p.n_tiles, z = rr / p.n_tiles;
+        const int nt = p.z_mid ? rr / p.z_tiles : rr % p.n_tiles;
+        const int z = p.z_mid ? rr % p.z_tiles : rr / p.n_tiles;
         if (z >= p.z_tiles || z >= TC_MAX_GROUP || nt * BN + col0 >= p.N) continue;   // whole patch (uniform)
         const int row = row0 + prow, col = col0 + pcol;
         const int n0 = nt * BN + col;
