@@ -109,7 +109,8 @@ class ClockSampler:
 # (bench.py --kernel fc_fwd_grouped); must be re-measured whenever that kernel
 # or its tile choice changes (then None).
 PROFILED_TRAFFIC = {
-    "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 484.9e6,
+    # one call: the GEMM kernel 461.8 + 47.0 MB and its tail reduction 17.1 MB (one ncu capture)
+    "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 525.9e6,
 }
 
 
@@ -351,8 +352,10 @@ KERNELS = {
     "conv_fwd": "conv forward, VGG conv3_2 shape 56x56x256->256, batch 16 (TF32 implicit GEMM)",
     "conv_dx": "conv input gradient, VGG conv3_2 shape, batch 16",
     "conv_dw": "conv weight gradient, VGG conv3_2 shape, batch 16",
-    "fc_fwd_grouped": "grouped FC forward of the SMLPs hidden layer over 4 replicas, 4 x 512 x 5000 x 5000 (TF32)",
-    "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T given",
+    "fc_fwd_grouped": "grouped FC forward of the SMLPs hidden layer over 4 replicas, 4 x 512 x 5000 x 5000 (TF32), "
+                      "with bias and the transposed output copy, as in the step",
+    "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T, "
+                      "x^T + ones row, dy^T given and dx^T written, as in the step",
     "conv_dw_224x64": "conv weight gradient, VGG conv1_2 shape 224x224x64->64, batch 16",
     "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
     "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
@@ -383,13 +386,21 @@ def run_kernel(args):
         dx = [torch.empty(M, K, device="cuda") for _ in range(G)]
         dw = [torch.empty(N, K, device="cuda") for _ in range(G)]
         db = [torch.empty(N, device="cuda") for _ in range(G)]
+        # the calls as the training step makes them: bias, transposed copies (y^T, dx^T),
+        # x^T with its row of ones (db from the weight-gradient GEMM), dy^T given
+        b = [rnd(N, std=0.1) for _ in range(G)]
+        yT = [torch.empty(N + 1, M, device="cuda") for _ in range(G)]
+        xT1 = [torch.cat([t.t(), torch.ones(1, M, device="cuda")]).contiguous() for t in x]
+        dyT = [t.t().contiguous() for t in dy]
+        dxT = [torch.empty(K, M, device="cuda") for _ in range(G)]
         nb = S.sprint_fc_batched_workspace_size(G, M, K, N, 1)
         ws = torch.empty(nb // 4 + 64, device="cuda")
         if k == "fc_fwd_grouped":
-            fn = lambda i: S.sprint_fc_fwd_batched(x, w[i % 2], None, y, M, K, N, 1, ws, nb)
+            fn = lambda i: S.sprint_fc_fwd_batched(x, w[i % 2], b, y, M, K, N, 1, ws, nb, yT=yT)
             work = 2.0 * M * N * K * G
         else:
-            fn = lambda i: S.sprint_fc_bwd_batched(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
+            fn = lambda i: S.sprint_fc_bwd_batched(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb,
+                                                   xT1=xT1, dyT=dyT, dxT=dxT)
             work = 4.0 * M * N * K * G
         unit = "TFLOP/s"
     elif k.startswith("fc"):
