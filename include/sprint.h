@@ -337,17 +337,20 @@ int sprint_apply_update_momentum(const float* w_in, float* w_out, float* v, cons
 int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const float* const* bufs, int k, size_t n,
                                 float eta, float eps, sprint_stream_t stream);
 
-/* The same update of a row-major [rows][cols] weight matrix (n = rows*cols)
- * by rule `opt` (sprint_opt; nu_or_eps = nu for momentum, eps for Adagrad,
- * unused for SGD), bit for bit what the rule's sprint_apply_update_* call
- * computes, that also writes W' transposed: wT_out[c*rows + r] =
- * w_out[r*cols + c] (device [cols][rows]: the copy the input-gradient GEMMs
- * read, written in the same pass instead of reading W' back). state: v or G
- * (device [rows][cols], in place; NULL for SGD). wT_out must not overlap the
- * other arguments; w_out may equal w_in. 1 <= k <= 16. */
+/* The same update over n_total elements by rule `opt` (sprint_opt; nu_or_eps
+ * = nu for momentum, eps for Adagrad, unused for SGD), bit for bit what the
+ * rule's sprint_apply_update_* call over n_total computes, whose first
+ * rows*cols elements are a row-major [rows][cols] weight matrix that is also
+ * written transposed: wT_out[c*rows + r] = w_out[r*cols + c] (device
+ * [cols][rows]: the copy the input-gradient GEMMs read, written in the same
+ * pass instead of reading W' back). The elements after the matrix (a layer's
+ * bias, following its weights) are updated without a transpose, in the same
+ * launch. state: v or G (device [n_total], in place; NULL for SGD). wT_out
+ * must not overlap the other arguments; w_out may equal w_in. 1 <= k <= 16,
+ * rows, cols >= 1, n_total >= rows*cols. */
 int sprint_apply_update_t(int opt, const float* w_in, float* w_out, float* wT_out, float* state,
-                          const float* const* bufs, int k, int rows, int cols, float eta, float nu_or_eps,
-                          sprint_stream_t stream);
+                          const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta,
+                          float nu_or_eps, sprint_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Staleness schedule (host only) — the delays of asynchronous SGD ([S] Sec. 1,

@@ -48,11 +48,12 @@ constexpr int kMaxGroup = 16;
 enum PsOpt : int { PS_SGD = 0, PS_MOMENTUM = 1, PS_ADAGRAD = 2 };
 
 // the standalone update kernels by rule over k GradBufs (update.cu); the _t
-// form updates a row-major [rows][cols] matrix and also writes W' transposed
+// form updates a row-major [rows][cols] matrix, also writing W' transposed,
+// and then the elements up to n_total after it without transposing
 int launch_ps_update(int opt, const char* fn, const float* w_in, float* w_out, float* state, const float* const* bufs,
                      int k, size_t n, float eta, float hp, sprint_stream_t stream);
 int launch_ps_update_t(int opt, const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
-                       const float* const* bufs, int k, int rows, int cols, float eta, float hp,
+                       const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
                        sprint_stream_t stream);
 
 // ---------------------------------------------------------------- device side

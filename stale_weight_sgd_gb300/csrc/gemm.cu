@@ -1558,7 +1558,7 @@ static int fc_bwd_batched_impl(const char* fn, const float* const* x, const floa
         const float* const* bufs = const_cast<const float* const*>(dw);
         if (ps->wT_out)
             r = launch_ps_update_t(ps->opt, fn, ps->w_in, ps->w_out, ps->wT_out, ps->w_state, bufs, batch, out, in,
-                                   ps->eta, ps->hp, stream);
+                                   static_cast<size_t>(out) * in, ps->eta, ps->hp, stream);
         else
             r = launch_ps_update(ps->opt, fn, ps->w_in, ps->w_out, ps->w_state, bufs, batch,
                                  static_cast<size_t>(out) * in, ps->eta, ps->hp, stream);

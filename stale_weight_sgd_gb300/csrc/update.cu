@@ -95,10 +95,23 @@ constexpr int kUtRows = 32, kUtCols = 128;
 
 template <int OPT, int K, bool VEC>
 __global__ void __launch_bounds__(256) update_t_kernel(const float* w_in, float* w_out, float* wT_out, float* state,
-                                                       BufPtrs bufs, int rows, int cols, float eta, float hp) {
+                                                       BufPtrs bufs, int rows, int cols, size_t n_total, float eta,
+                                                       float hp) {
     __shared__ float tile[kUtRows][kUtCols + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int r0 = blockIdx.y * kUtRows, c0 = blockIdx.x * kUtCols;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        // the elements after the matrix (a layer's bias): the flat update, no transpose
+        for (size_t i = static_cast<size_t>(rows) * cols + threadIdx.x; i < n_total; i += blockDim.x) {
+            float sm = bufs.p[0][i];
+            for (int b = 1; b < K; ++b) sm += bufs.p[b][i];
+            float st = (OPT != PS_SGD) ? state[i] : 0.f;
+            float o;
+            ps_apply1<OPT>(sm, w_in[i], &st, eta, hp, o);
+            if constexpr (OPT != PS_SGD) state[i] = st;
+            w_out[i] = o;
+        }
+    }
 #pragma unroll
     for (int j = 0; j < kUtRows / 8; ++j) {
         const int rr = ty + 8 * j, r = r0 + rr;
@@ -188,11 +201,14 @@ int launch_update(const char* fn, const float* w_in, float* w_out, float* state,
 
 template <int OPT>
 int launch_update_t(const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
-                    const float* const* bufs, int k, int rows, int cols, float eta, float hp, sprint_stream_t stream) {
+                    const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
+                    sprint_stream_t stream) {
     SPRINT_REQUIRE(k >= 1, SPRINT_ERR_SHAPE, "%s: k must be >= 1 (got %d)", fn, k);
     SPRINT_REQUIRE(k <= kMaxBufs, SPRINT_ERR_UNSUPPORTED, "%s: k = %d > %d buffers", fn, k, kMaxBufs);
-    SPRINT_REQUIRE(rows >= 0 && cols >= 0, SPRINT_ERR_SHAPE, "%s: negative size", fn);
-    if (rows == 0 || cols == 0) return SPRINT_OK;
+    SPRINT_REQUIRE(rows >= 1 && cols >= 1, SPRINT_ERR_SHAPE, "%s: rows and cols must be >= 1 (got %d, %d)", fn, rows,
+                   cols);
+    SPRINT_REQUIRE(n_total >= static_cast<size_t>(rows) * cols, SPRINT_ERR_SHAPE,
+                   "%s: n_total %zu is below rows * cols", fn, n_total);
     SPRINT_REQUIRE(rows <= 65535 * kUtRows, SPRINT_ERR_SHAPE, "%s: %d rows exceed the grid", fn, rows);
     SPRINT_REQUIRE(w_in && w_out && wT_out && bufs, SPRINT_ERR_INVALID_ARG, "%s: NULL w_in, w_out, wT_out or bufs",
                    fn);
@@ -210,9 +226,9 @@ int launch_update_t(const char* fn, const float* w_in, float* w_out, float* wT_o
 #define SPRINT_K(KK)                                                                                            \
     case KK:                                                                                                    \
         if (vec)                                                                                                \
-            update_t_kernel<OPT, KK, true><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, eta, hp); \
+            update_t_kernel<OPT, KK, true><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp); \
         else                                                                                                    \
-            update_t_kernel<OPT, KK, false><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, eta, hp); \
+            update_t_kernel<OPT, KK, false><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp); \
         break;
         SPRINT_K(1) SPRINT_K(2) SPRINT_K(3) SPRINT_K(4) SPRINT_K(5) SPRINT_K(6) SPRINT_K(7) SPRINT_K(8)
         SPRINT_K(9) SPRINT_K(10) SPRINT_K(11) SPRINT_K(12) SPRINT_K(13) SPRINT_K(14) SPRINT_K(15) SPRINT_K(16)
@@ -235,14 +251,18 @@ int launch_ps_update(int opt, const char* fn, const float* w_in, float* w_out, f
 }
 
 int launch_ps_update_t(int opt, const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
-                       const float* const* bufs, int k, int rows, int cols, float eta, float hp,
+                       const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
                        sprint_stream_t stream) {
     switch (opt) {
-        case PS_SGD: return launch_update_t<PS_SGD>(fn, w_in, w_out, wT_out, nullptr, bufs, k, rows, cols, eta, hp, stream);
+        case PS_SGD:
+            return launch_update_t<PS_SGD>(fn, w_in, w_out, wT_out, nullptr, bufs, k, rows, cols, n_total, eta, hp,
+                                           stream);
         case PS_MOMENTUM:
-            return launch_update_t<PS_MOMENTUM>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, eta, hp, stream);
+            return launch_update_t<PS_MOMENTUM>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, hp,
+                                                stream);
         case PS_ADAGRAD:
-            return launch_update_t<PS_ADAGRAD>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, eta, hp, stream);
+            return launch_update_t<PS_ADAGRAD>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, hp,
+                                               stream);
         default: return fail(SPRINT_ERR_INVALID_ARG, "%s: unknown update rule %d", fn, opt);
     }
 }
@@ -278,7 +298,8 @@ extern "C" int sprint_apply_update_adagrad(const float* w_in, float* w_out, floa
 }
 
 extern "C" int sprint_apply_update_t(int opt, const float* w_in, float* w_out, float* wT_out, float* state,
-                                     const float* const* bufs, int k, int rows, int cols, float eta, float nu_or_eps,
-                                     sprint_stream_t stream) {
-    return launch_ps_update_t(opt, __func__, w_in, w_out, wT_out, state, bufs, k, rows, cols, eta, nu_or_eps, stream);
+                                     const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta,
+                                     float nu_or_eps, sprint_stream_t stream) {
+    return launch_ps_update_t(opt, __func__, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, nu_or_eps,
+                              stream);
 }

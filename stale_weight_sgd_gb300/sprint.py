@@ -56,7 +56,7 @@ _SIGS = {
     "sprint_fc_fwd_batched_workspace_size": ([], SZ),
     "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
     "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
-    "sprint_apply_update_t": ([I, P, P, P, P, P, I, I, I, F, F, P], I),
+    "sprint_apply_update_t": ([I, P, P, P, P, P, I, I, I, SZ, F, F, P], I),
     "sprint_fc_bwd_update_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, I, P, P, P, P, P, P, P, F, F, P,
                                       SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
@@ -247,10 +247,12 @@ def sprint_fc_bwd_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate,
 SPRINT_OPT = {"sgd": 0, "momentum": 1, "adagrad": 2}
 
 
-def sprint_apply_update_t(opt, w_in, w_out, wT_out, state, bufs, rows, cols, eta, nu_or_eps=0.0, stream=None):
+def sprint_apply_update_t(opt, w_in, w_out, wT_out, state, bufs, rows, cols, eta, nu_or_eps=0.0, stream=None,
+                          n_total=None):
+    n = rows * cols if n_total is None else n_total
     return _check("sprint_apply_update_t", lib().sprint_apply_update_t(
         SPRINT_OPT.get(opt, opt), _p(w_in), _p(w_out), _p(wT_out), _p(state), _ptr_array(bufs), len(bufs), rows, cols,
-        float(eta), float(nu_or_eps), _s(stream)))
+        n, float(eta), float(nu_or_eps), _s(stream)))
 
 
 def sprint_fc_bwd_update_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, fin, fout, opt, w_in, b_in,

@@ -263,8 +263,8 @@ class StaleSGD:
 
     def _update_layer(self, t, li, stream):
         """SumGradient + UpdateWeights (Algorithm 2) of layer li: W_l(t+1) into
-        ring slot t+1, with its transpose written in the same pass (layers after
-        the first), then b."""
+        ring slot t+1 in one launch, with W's transpose written in the same pass
+        (layers after the first)."""
         off, cnt = self.span[li]
         slot_in, slot_out = t % (self.S + 1), (t + 1) % (self.S + 1)
         sh = stream.cuda_stream
@@ -290,10 +290,10 @@ class StaleSGD:
             return
         L = self.shapes[li]
         rows, cols = (L.cout, 9 * L.cin) if L.kind == "conv" else (L.cout, L.cin)
-        w_in, w_out, st, bufs = ptrs(L.w_off)
+        w_in, w_out, st, bufs = ptrs(off)
         wT = self.ringT[slot_out].data_ptr() + 4 * L.w_off
-        S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh)
-        plain(L.b_off, L.cout)
+        # W (transposed copy too), then the rest of the span (b and padding) in the same launch
+        S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh, n_total=cnt)
 
     def _per_replica(self, fn):
         """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica

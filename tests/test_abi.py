@@ -53,11 +53,13 @@ def test_update_rejects_bad_arguments(S):
     assert L.sprint_apply_update_momentum(16, 16, 16, bad, 2, 10, ctypes.c_float(0.1), ctypes.c_float(0.9), None) == 3
     assert L.sprint_apply_update_adagrad(16, 16, None, arr, 2, 10, ctypes.c_float(0.1), ctypes.c_float(1e-8), None) == 1
     f = ctypes.c_float
-    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 0, 8, f(0.1), f(0), None) == 0    # empty
-    assert L.sprint_apply_update_t(0, 16, 16, None, None, arr, 2, 4, 8, f(0.1), f(0), None) == 1  # NULL wT_out
-    assert L.sprint_apply_update_t(1, 16, 16, 16, None, arr, 2, 4, 8, f(0.1), f(0.9), None) == 1  # momentum, NULL v
-    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 17, 4, 8, f(0.1), f(0), None) == 4   # k > 16
-    assert L.sprint_apply_update_t(5, 16, 16, 16, None, arr, 2, 4, 8, f(0.1), f(0), None) == 1    # unknown rule
+    n = ctypes.c_size_t
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 0, 8, n(0), f(0.1), f(0), None) == 2     # no rows
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 4, 8, n(31), f(0.1), f(0), None) == 2    # n < 4*8
+    assert L.sprint_apply_update_t(0, 16, 16, None, None, arr, 2, 4, 8, n(32), f(0.1), f(0), None) == 1  # NULL wT
+    assert L.sprint_apply_update_t(1, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0.9), None) == 1  # NULL v
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 17, 4, 8, n(32), f(0.1), f(0), None) == 4   # k > 16
+    assert L.sprint_apply_update_t(5, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0), None) == 1    # rule
 
 
 def test_shape_and_workspace_errors(S):

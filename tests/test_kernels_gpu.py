@@ -56,13 +56,14 @@ def test_update(S, k, n, opt):
     assert rel_inf(host(dout), ref) <= TOL_UPDATE
 
 
-@pytest.mark.parametrize("rows,cols", [(300, 136), (37, 27), (64, 4096), (129, 260)])
+@pytest.mark.parametrize("rows,cols,tail", [(300, 136, 303), (37, 27, 0), (64, 4096, 64), (129, 260, 1)])
 @pytest.mark.parametrize("k", [1, 4, 16])
 @pytest.mark.parametrize("opt", ["sgd", "momentum", "adagrad"])
-def test_update_transposed(S, rows, cols, k, opt):
-    """sprint_apply_update_t: W', state bit for bit the flat update's; W'^T its exact transpose;
+def test_update_transposed(S, rows, cols, tail, k, opt):
+    """sprint_apply_update_t over a matrix plus `tail` elements after it (a bias and padding):
+    W', state bit for bit the flat update's; W'^T the exact transpose of the matrix part;
     W' against the oracle's update."""
-    n = rows * cols
+    n = rows * cols + tail
     w = _f32(4, f"w{n}", n, 0.01)
     bufs = [_f32(4, f"g{j}/{n}", n, 1e-3) for j in range(k)]
     st0 = np.abs(_f32(4, f"s{n}", n, 1e-2)) + (0.1 if opt == "adagrad" else 0.0)
@@ -70,9 +71,9 @@ def test_update_transposed(S, rows, cols, k, opt):
     dbufs = [dev(b) for b in bufs]
     dw = dev(w)
     out_t, out_f = torch.empty_like(dw), torch.empty_like(dw)
-    wT = torch.empty(n, dtype=torch.float32, device="cuda")
+    wT = torch.empty(rows * cols, dtype=torch.float32, device="cuda")
     st_t, st_f = (dev(st0), dev(st0)) if opt != "sgd" else (None, None)
-    S.sprint_apply_update_t(opt, dw, out_t, wT, st_t, dbufs, rows, cols, eta, hp)
+    S.sprint_apply_update_t(opt, dw, out_t, wT, st_t, dbufs, rows, cols, eta, hp, n_total=n)
     if opt == "sgd":
         S.sprint_apply_update_sgd(dw, out_f, dbufs, n, eta)
         ref = O.update_sgd(w, bufs, eta)
@@ -84,7 +85,7 @@ def test_update_transposed(S, rows, cols, k, opt):
         ref, _ = O.update_adagrad(w, st0, bufs, eta, hp)
     a = host(out_t)
     assert np.array_equal(a, host(out_f))
-    assert np.array_equal(host(wT).reshape(cols, rows), a.reshape(rows, cols).T)
+    assert np.array_equal(host(wT).reshape(cols, rows), a[:rows * cols].reshape(rows, cols).T)
     if opt != "sgd":
         assert np.array_equal(host(st_t), host(st_f))
     assert rel_inf(a, ref) <= TOL_UPDATE
