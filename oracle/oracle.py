@@ -37,6 +37,22 @@ its reason in the design notes):
   R7 staleness: replica r at step t uses W(max(0, t - s[t,r])), where W(t) is
      the version before step t's update; delays from SplitMix64.
   R8 pipeline stage k (forward and backward) uses W_k(max(0, t - s_k)).
+  R11 Nesterov momentum (the pipelined-training page's appendices train with
+     "SGD with Nesterov momentum" but print no formula): in R5's units,
+     v' = nu*v - eta*S, W' = W + nu*v' - eta*S.
+  R12 weight decay (same appendices, a coefficient only): L2 on the summed
+     gradient at the parameter server, S <- S + lambda*W, before any rule.
+  R13 hybrid pipelined/non-pipelined training ([PB] Sec. 4.2): the stage
+     delays s_k hold for steps t < N_p and are 0 from t = N_p on. Degree of
+     staleness of stage pair k = s_k (steps its weights lag); percentage of
+     stale weights = the parameters (W and b) of layers in stages with s_k > 0
+     over all parameters ([PB] Sec. 4.1).
+  R14 DistBelief n_fetch / n_push ([DB]): every replica refreshes a local copy
+     of the parameters from the server at steps t with t % n_fetch == 0 and
+     computes its gradients on that copy; it accumulates them in its GradBuf
+     (assigned at t % n_push == 0, added otherwise) and pushes at steps with
+     (t + 1) % n_push == 0, where the server applies the sum of the R pushed
+     buffers (replica order) once. All replicas run in phase.
   R10 max-pool argmax = first window offset in row-major order under strict >.
   R11 ReLU derivative at 0 is 0.
 
@@ -437,20 +453,35 @@ def sum_buffers(bufs):
     return s
 
 
-def update_sgd(w, bufs, eta):
+def decayed_sum(w, bufs, weight_decay=0.0):
+    """S = sum of the buffers, plus lambda*W when weight decay is on (R12)."""
+    s = sum_buffers(bufs)
+    if weight_decay:
+        s = s + weight_decay * np.asarray(w, F64)
+    return s
+
+
+def update_sgd(w, bufs, eta, weight_decay=0.0):
     """W' = W - eta * S   (Eq. (1) of [S] with S the summed gradient; [DB])."""
-    return np.asarray(w, F64) - eta * sum_buffers(bufs)
+    return np.asarray(w, F64) - eta * decayed_sum(w, bufs, weight_decay)
 
 
-def update_momentum(w, v, bufs, eta, nu):
+def update_momentum(w, v, bufs, eta, nu, weight_decay=0.0):
     """v' = nu*v - eta*S, W' = W + v'  (Algorithm 2 of [S] with DeltaWeights = v, R5)."""
-    v_new = nu * np.asarray(v, F64) - eta * sum_buffers(bufs)
+    v_new = nu * np.asarray(v, F64) - eta * decayed_sum(w, bufs, weight_decay)
     return np.asarray(w, F64) + v_new, v_new
 
 
-def update_adagrad(w, g2, bufs, eta, eps):
+def update_nesterov(w, v, bufs, eta, nu, weight_decay=0.0):
+    """v' = nu*v - eta*S, W' = W + nu*v' - eta*S  (Nesterov momentum, R11)."""
+    s = decayed_sum(w, bufs, weight_decay)
+    v_new = nu * np.asarray(v, F64) - eta * s
+    return np.asarray(w, F64) + nu * v_new - eta * s, v_new
+
+
+def update_adagrad(w, g2, bufs, eta, eps, weight_decay=0.0):
     """G' = G + S*S, W' = W - eta*S/(sqrt(G') + eps)  (per-parameter rate of [DB], R6)."""
-    s = sum_buffers(bufs)
+    s = decayed_sum(w, bufs, weight_decay)
     g_new = np.asarray(g2, F64) + s * s
     return np.asarray(w, F64) - eta * s / (np.sqrt(g_new) + eps), g_new
 
@@ -493,15 +524,40 @@ def version_used(t: int, s: int) -> int:
 # Stale-weight training driver (ASGD replicas [S] Fig. 1 / [DB]; pipeline [PB] 4.1)
 # ---------------------------------------------------------------------------
 
-def replica_params(layers, hist, t, r, *, schedule=None, stage_delays=None, stage_of_layer=None):
+def stage_delay(stage_delays, k, t, hybrid_switch=None):
+    """Delay of pipeline stage k at step t: s_k, or 0 from step N_p on in
+    hybrid training (R13)."""
+    if hybrid_switch is not None and t >= hybrid_switch:
+        return 0
+    return int(stage_delays[k])
+
+
+def staleness_degrees(stage_delays):
+    """Degree of staleness of each stage pair: the steps its weights lag (R13)."""
+    return [int(s) for s in stage_delays]
+
+
+def stale_weight_percent(layers, stage_of_layer, stage_delays):
+    """Percentage of the parameters (W and b) held by layers whose stage uses
+    stale weights (s_k > 0), R13 / [PB] Sec. 4.1."""
+    stale = total = 0
+    for li, L in enumerate(layers):
+        n = int(np.prod(L.w_shape)) + L.cout
+        total += n
+        if stage_delays[stage_of_layer[li]] > 0:
+            stale += n
+    return 100.0 * stale / total
+
+
+def replica_params(layers, hist, t, r, *, schedule=None, stage_delays=None, stage_of_layer=None, hybrid_switch=None):
     """Per-layer (W, b) that replica r uses at step t: W(max(0, t - s[t, r]))
     for asynchronous replicas (R7), or W_l(max(0, t - s_k)) for the layers of
-    pipeline stage k (R8)."""
+    pipeline stage k (R8; s_k = 0 from step N_p on in hybrid training, R13)."""
     offs, _ = param_offsets(layers)
     params = []
     for li, L in enumerate(layers):
         if stage_delays is not None:
-            ver = version_used(t, stage_delays[stage_of_layer[li]])
+            ver = version_used(t, stage_delay(stage_delays, stage_of_layer[li], t, hybrid_switch))
         else:
             ver = version_used(t, 0 if schedule is None else int(schedule[t, r]))
         a, b = offs[li]
@@ -510,7 +566,7 @@ def replica_params(layers, hist, t, r, *, schedule=None, stage_delays=None, stag
 
 
 def step_gradients(layers, hist, t, batches, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
-                   reduction="mean"):
+                   reduction="mean", hybrid_switch=None):
     """Per-replica (loss, flat gradient) of global step t, given the weight
     history hist[0..t] (hist[v] = W(v)).
 
@@ -521,54 +577,97 @@ def step_gradients(layers, hist, t, batches, *, replicas=1, schedule=None, stage
     for r in range(replicas):
         x, y = batches[(t * replicas + r) % len(batches)]
         params = replica_params(layers, hist, t, r, schedule=schedule, stage_delays=stage_delays,
-                                stage_of_layer=stage_of_layer)
+                                stage_of_layer=stage_of_layer, hybrid_switch=hybrid_switch)
         loss, gl = forward_backward(layers, params, x, y, reduction)
         losses.append(loss)
         grads.append(flatten(gl))
     return losses, grads
 
 
-def apply_update(w, grads, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None):
+def apply_update(w, grads, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None, weight_decay=0.0):
     """The parameter-server apply of the summed gradients; returns (W', state')."""
     if optimizer == "sgd":
-        return update_sgd(w, grads, eta), state
+        return update_sgd(w, grads, eta, weight_decay), state
     if optimizer == "momentum":
-        return update_momentum(w, state, grads, eta, nu)
+        return update_momentum(w, state, grads, eta, nu, weight_decay)
+    if optimizer == "nesterov":
+        return update_nesterov(w, state, grads, eta, nu, weight_decay)
     if optimizer == "adagrad":
-        return update_adagrad(w, state, grads, eta, eps)
+        return update_adagrad(w, state, grads, eta, eps, weight_decay)
     raise ValueError(optimizer)
 
 
 def train_step(layers, hist, t, batches, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
-               optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None, reduction="mean"):
+               optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, state=None, reduction="mean", hybrid_switch=None,
+               weight_decay=0.0):
     """One global step: the R replica gradients (step_gradients), summed in
     replica order and applied once (apply_update) with the optimizer state
-    before the step (momentum v or Adagrad G; ignored for SGD).
+    before the step (momentum / Nesterov v or Adagrad G; ignored for SGD).
     Returns (mean loss over replicas, W(t+1), new state)."""
     losses, grads = step_gradients(layers, hist, t, batches, replicas=replicas, schedule=schedule,
-                                   stage_delays=stage_delays, stage_of_layer=stage_of_layer, reduction=reduction)
-    w_new, state = apply_update(hist[t], grads, optimizer, eta, nu, eps, state)
+                                   stage_delays=stage_delays, stage_of_layer=stage_of_layer, reduction=reduction,
+                                   hybrid_switch=hybrid_switch)
+    w_new, state = apply_update(hist[t], grads, optimizer, eta, nu, eps, state, weight_decay)
     return sum(losses) / replicas, w_new, state
 
 
+def initial_state(optimizer, n, g0=0.1):
+    """v0 = 0 for momentum and Nesterov, G0 = g0 for Adagrad, none for SGD."""
+    if optimizer in ("momentum", "nesterov"):
+        return np.zeros(n, F64)
+    if optimizer == "adagrad":
+        return np.full(n, g0, F64)
+    return None
+
+
 def train(arch, w0, batches, steps, *, replicas=1, schedule=None, stage_delays=None, stage_of_layer=None,
-          optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, reduction="mean"):
+          optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, reduction="mean", hybrid_switch=None,
+          weight_decay=0.0):
     """Simulated asynchronous training from W(0) = w0; returns (per-step mean
     loss, final W, history). The full history of W is kept, which is the plain
-    brute-force way to look up old versions (v0 = 0 for momentum, G0 = g0 for
-    Adagrad)."""
+    brute-force way to look up old versions."""
     layers = build_layers(arch)
     _, n = param_offsets(layers)
     hist = [np.asarray(w0, F64).copy()]
-    state = np.zeros(n, F64) if optimizer == "momentum" else (np.full(n, g0, F64) if optimizer == "adagrad" else None)
+    state = initial_state(optimizer, n, g0)
     losses = []
     for t in range(steps):
         loss, w_new, state = train_step(layers, hist, t, batches, replicas=replicas, schedule=schedule,
                                         stage_delays=stage_delays, stage_of_layer=stage_of_layer, optimizer=optimizer,
-                                        eta=eta, nu=nu, eps=eps, state=state, reduction=reduction)
+                                        eta=eta, nu=nu, eps=eps, state=state, reduction=reduction,
+                                        hybrid_switch=hybrid_switch, weight_decay=weight_decay)
         losses.append(loss)
         hist.append(w_new)
     return losses, hist[-1], hist
+
+
+def train_fetch_push(arch, w0, batches, steps, *, replicas=1, n_fetch=1, n_push=1, optimizer="sgd", eta=0.01,
+                     nu=0.9, eps=1e-8, g0=0.1, reduction="mean", weight_decay=0.0):
+    """DistBelief-style training with n_fetch / n_push (R14), step by step as
+    the rule reads: refresh the local copies, compute and accumulate every
+    replica's gradient, and at a push step apply the R buffers. Returns
+    (per-step mean loss, final server W, the server W after each update)."""
+    layers = build_layers(arch)
+    _, n = param_offsets(layers)
+    w = np.asarray(w0, F64).copy()
+    state = initial_state(optimizer, n, g0)
+    local = [None] * replicas
+    bufs = [None] * replicas
+    losses, versions = [], [w]
+    for t in range(steps):
+        if t % n_fetch == 0:
+            local = [w.copy() for _ in range(replicas)]
+        step_losses = []
+        for r in range(replicas):
+            x, y = batches[(t * replicas + r) % len(batches)]
+            loss, gl = forward_backward(layers, unflatten(layers, local[r]), x, y, reduction)
+            step_losses.append(loss)
+            bufs[r] = gradbuf_accumulate(bufs[r], flatten(gl), 1.0, first=(t % n_push == 0))
+        losses.append(sum(step_losses) / replicas)
+        if (t + 1) % n_push == 0:
+            w, state = apply_update(w, bufs, optimizer, eta, nu, eps, state, weight_decay)
+            versions.append(w)
+    return losses, w, versions
 
 
 def flops_per_image(arch) -> float:

@@ -64,6 +64,30 @@ def _fc_bwd_half_db(x, w, dy):
     return dx, dw, db * 0.5
 
 
+def _nesterov_old_velocity(w, v, bufs, eta, nu, weight_decay=0.0):
+    s = OM.decayed_sum(w, bufs, weight_decay)
+    v_new = nu * np.asarray(v, float) - eta * s
+    return np.asarray(w, float) + nu * np.asarray(v, float) - eta * s, v_new
+
+
+def _decay_sign(w, bufs, weight_decay=0.0):
+    return OM.sum_buffers(bufs) - weight_decay * np.asarray(w, float)
+
+
+def _never_switch(stage_delays, k, t, hybrid_switch=None):
+    return int(stage_delays[k])
+
+
+def _stale_weights_only(layers, stage_of_layer, stage_delays):
+    stale = total = 0
+    for li, L in enumerate(layers):
+        n = int(np.prod(L.w_shape))
+        total += n + L.cout
+        if stage_delays[stage_of_layer[li]] > 0:
+            stale += n
+    return 100.0 * stale / total
+
+
 MUTANTS = [
     ("conv3x3_dx", _flipped_dx, P.test_conv_adjoint_identities, ()),
     ("conv3x3_fwd", _no_bias_fwd, P.test_conv_fwd_brute_force, (1,)),
@@ -74,6 +98,10 @@ MUTANTS = [
     ("maxpool2x2_fwd", _pool_last_max, P.test_pool_brute_force_with_ties, ()),
     ("version_used", _stale_off_by_one, P.test_constant_delay_matches_explicit_loop, ()),
     ("fc_bwd", _fc_bwd_half_db, P.test_network_gradient_finite_differences, (P.SMALL_MLP,)),
+    ("update_nesterov", _nesterov_old_velocity, P.test_nesterov_constant_gradient_closed_form, ()),
+    ("decayed_sum", _decay_sign, P.test_weight_decay_alone_is_geometric_shrink, ()),
+    ("stage_delay", _never_switch, P.test_hybrid_switch_endpoints_and_prefix, ()),
+    ("stale_weight_percent", _stale_weights_only, P.test_stale_weight_percent_vgg_by_hand, ()),
 ]
 
 

@@ -382,3 +382,134 @@ def test_pipeline_stage_delays_use_per_stage_versions():
         mixed = np.concatenate([old[:offs[2][0]], new[offs[2][0]:]])
         W.append(W[t] - eta * O.gradient(layers, mixed, *b[t % len(b)])[1])
     np.testing.assert_array_equal(wT, W[-1])
+
+
+# ---- Nesterov momentum, weight decay (pipelined-training page, Appendices A/B)
+
+def test_nesterov_constant_gradient_closed_form():
+    # v_t = -eta*g*(1 - nu^t)/(1 - nu); W_T = W_0 + sum_t (nu*v_t - eta*g)
+    w0, g, eta, nu, T = 0.4, -0.25, 0.02, 0.9, 30
+    w, v = np.array([w0]), np.array([0.0])
+    for _ in range(T):
+        w, v = O.update_nesterov(w, v, [np.array([g])], eta, nu)
+    closed = w0 - eta * g * sum(nu * (1 - nu ** t) / (1 - nu) + 1.0 for t in range(1, T + 1))
+    assert w[0] == pytest.approx(closed, rel=1e-13)
+    assert v[0] == pytest.approx(-eta * g * (1 - nu ** T) / (1 - nu), rel=1e-13)
+    # nu = 0 reduces to plain SGD
+    w1, _ = O.update_nesterov(np.array([w0]), np.array([3.0]), [np.array([g])], eta, 0.0)
+    assert w1[0] == pytest.approx(w0 - eta * g, rel=1e-15)
+
+
+def test_weight_decay_alone_is_geometric_shrink():
+    # zero gradient: S = lambda*W, so SGD gives W_T = W_0 * (1 - eta*lambda)^T
+    w0, eta, lam, T = np.array([1.5, -0.75, 0.0]), 0.05, 0.004, 40
+    w = w0.copy()
+    for _ in range(T):
+        w = O.update_sgd(w, [np.zeros(3)], eta, weight_decay=lam)
+    np.testing.assert_allclose(w, w0 * (1 - eta * lam) ** T, rtol=1e-13, atol=0)
+    # Adagrad, one step from G0: G' = G0 + (lambda*W)^2, W' = W - eta*lambda*W/(sqrt(G') + eps)
+    G0, eps = 0.1, 1e-8
+    w1, G1 = O.update_adagrad(np.array([2.0]), np.array([G0]), [np.array([0.0])], eta, eps, weight_decay=lam)
+    g = lam * 2.0
+    assert G1[0] == pytest.approx(G0 + g * g, rel=1e-15)
+    assert w1[0] == pytest.approx(2.0 - eta * g / (math.sqrt(G0 + g * g) + eps), rel=1e-15)
+
+
+def test_weight_decay_is_one_more_pushed_buffer():
+    # the decay term enters like an extra GradBuf holding lambda*W, for every rule
+    rng = np.random.default_rng(5)
+    w, v, b = rng.standard_normal(7), rng.standard_normal(7), [rng.standard_normal(7) for _ in range(3)]
+    lam = 0.01
+    extra = b + [lam * w]
+    np.testing.assert_allclose(O.update_sgd(w, b, 0.1, lam), O.update_sgd(w, extra, 0.1), rtol=0, atol=1e-15)
+    for fn in (O.update_momentum, O.update_nesterov):
+        a = fn(w, v, b, 0.1, 0.9, lam)
+        c = fn(w, v, extra, 0.1, 0.9)
+        np.testing.assert_allclose(a[0], c[0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(a[1], c[1], rtol=0, atol=1e-15)
+
+
+# ---- hybrid pipelined / non-pipelined training and stale-weight metrics (pipelined-training page, Sec. 4)
+
+# VGG-16 stage cut of the pipeline reading: block 1 | block 2 | block 3 | blocks 4-5 + FC
+VGG_STAGE_CUT = [0, 0, 1, 1, 2, 2, 2] + [3] * 9
+
+
+def test_stale_weight_percent_vgg_by_hand():
+    layers = O.build_layers(O.ARCHS["vgg_c"])
+    # stages 0-2 (delays 3, 2, 1) hold conv1_1 .. conv3_3: 9*Cin*Cout + Cout each
+    convs = [(3, 64), (64, 64), (64, 128), (128, 128), (128, 256), (256, 256), (256, 256)]
+    stale = sum(9 * ci * co + co for ci, co in convs)
+    assert stale == 1735488
+    total = O.param_count_eq3(O.ARCHS["vgg_c"])
+    assert O.stale_weight_percent(layers, VGG_STAGE_CUT, [3, 2, 1, 0]) == pytest.approx(100.0 * stale / total,
+                                                                                         rel=1e-15)
+    assert O.stale_weight_percent(layers, VGG_STAGE_CUT, [0, 0, 0, 0]) == 0.0
+    assert O.stale_weight_percent(layers, VGG_STAGE_CUT, [1, 1, 1, 1]) == 100.0
+    assert O.staleness_degrees([3, 2, 1, 0]) == [3, 2, 1, 0]
+
+
+def test_hybrid_switch_endpoints_and_prefix():
+    arch = SMALL_CNN
+    stages, delays = [0, 0, 1, 1, 1], [2, 0]
+    w0 = _init(arch)
+    b = _batches(arch, 5, 3)
+    T = 4
+    base = O.train(arch, w0, b, T, stage_delays=delays, stage_of_layer=stages)
+    plain = O.train(arch, w0, b, T, stage_delays=[0, 0], stage_of_layer=stages)
+    # switching at step 0 is plain SGD; never switching is the pipeline
+    h0 = O.train(arch, w0, b, T, stage_delays=delays, stage_of_layer=stages, hybrid_switch=0)
+    hT = O.train(arch, w0, b, T, stage_delays=delays, stage_of_layer=stages, hybrid_switch=T)
+    assert h0[0] == plain[0] and all((x == y).all() for x, y in zip(h0[2], plain[2]))
+    assert hT[0] == base[0] and all((x == y).all() for x, y in zip(hT[2], base[2]))
+    # switching at N_p = 2: the first two steps are the pipeline's, and from there every
+    # step uses the current weights (a brute-force loop over the same history)
+    h2 = O.train(arch, w0, b, T, stage_delays=delays, stage_of_layer=stages, hybrid_switch=2)
+    assert h2[0][:2] == base[0][:2] and all((x == y).all() for x, y in zip(h2[2][:3], base[2][:3]))
+    layers = O.build_layers(arch)
+    hist = list(h2[2][:3])
+    for t in range(2, T):
+        x, y = b[t % len(b)]
+        g = O.gradient(layers, hist[t], x, y)[1]
+        hist.append(hist[t] - 0.01 * g)
+    np.testing.assert_allclose(h2[2][T], hist[T], rtol=0, atol=1e-13)
+
+
+# ---- DistBelief n_fetch / n_push
+
+def test_fetch_push_every_step_is_synchronous_sgd():
+    arch = SMALL_MLP
+    w0 = _init(arch)
+    b = _batches(arch, 6, 4)
+    a = O.train(arch, w0, b, 5, replicas=3)
+    f = O.train_fetch_push(arch, w0, b, 5, replicas=3, n_fetch=1, n_push=1)
+    assert a[0] == f[0] and (a[1] == f[1]).all()
+
+
+@pytest.mark.parametrize("m", [2, 3])
+def test_fetch_push_windows_equal_a_bigger_synchronous_step(m):
+    # n_fetch = n_push = m: the m steps of a window use one copy of W and push their
+    # gradient sum once, i.e. one synchronous step with m*R replicas (same batches)
+    arch = SMALL_MLP
+    R = 2
+    w0 = _init(arch)
+    b = _batches(arch, 12, 3)
+    f = O.train_fetch_push(arch, w0, b, 2 * m, replicas=R, n_fetch=m, n_push=m, optimizer="momentum")
+    s = O.train(arch, w0, b, 2, replicas=m * R, optimizer="momentum")
+    np.testing.assert_allclose(f[1], s[1], rtol=0, atol=1e-12)
+    assert len(f[2]) == 3
+
+
+def test_fetch_slower_than_push_uses_stale_local_copies():
+    # n_fetch = 2, n_push = 1, one replica: step 2j+1 computes on W before step 2j's update
+    arch = SMALL_MLP
+    layers = O.build_layers(arch)
+    w0 = _init(arch)
+    b = _batches(arch, 4, 3)
+    f = O.train_fetch_push(arch, w0, b, 4, replicas=1, n_fetch=2, n_push=1)
+    w = w0.copy()
+    for t in range(4):
+        local = w if t % 2 == 0 else local
+        g = O.gradient(layers, local, *b[t % len(b)])[1]
+        w = w - 0.01 * g
+    np.testing.assert_allclose(f[1], w, rtol=0, atol=1e-13)
