@@ -247,16 +247,16 @@ int sprint_fc_bwd_batched(const float* const* x, const float* const* xT1, const 
  * Results are those of the plain call up to the rounding of db (a TF32 GEMM
  * column instead of an fp32 sum when xT1 is given). */
 
-/* Update rules of the parameter-server apply (see sprint_apply_update_*). */
-typedef enum { SPRINT_OPT_SGD = 0, SPRINT_OPT_MOMENTUM = 1, SPRINT_OPT_ADAGRAD = 2 } sprint_opt;
+/* Update rules of the parameter-server apply (see sprint_apply_update). */
+typedef enum { SPRINT_OPT_SGD = 0, SPRINT_OPT_MOMENTUM = 1, SPRINT_OPT_ADAGRAD = 2, SPRINT_OPT_NESTEROV = 3 } sprint_opt;
 
 /* The batched FC backward of the R replicas of one layer (arguments as
  * sprint_fc_bwd_batched; each dw[g] / db[g] is replica g's GradBuf, Algorithm 1)
  * followed by the parameter-server apply of that layer over those `batch`
  * GradBufs (SumGradient + UpdateWeights of Algorithm 2, [S] Sec. 3):
  *   S = dw[0] + dw[1] + ... + dw[batch-1]  (added in g order, per element)
- *   w_out = rule(w_in, S) with `opt` and eta, nu_or_eps exactly as
- *   sprint_apply_update_sgd / _momentum / _adagrad compute it (bit for bit);
+ *   w_out = rule(w_in, S) with `opt`, eta, nu_or_eps and weight_decay exactly
+ *   as sprint_apply_update computes it (bit for bit);
  *   b_out = rule(b_in, db[0] + ... + db[batch-1]) when db is given;
  *   wT_out (nullable): also w_out transposed, device [in][out].
  * w_in, w_out, w_state: device [out][in] (w_state: the momentum v or the
@@ -270,8 +270,8 @@ int sprint_fc_bwd_update_batched(const float* const* x, const float* const* xT1,
                                  const float* const* relu_src, float* const* dx, float* const* dxT, float* const* dw,
                                  float* const* db, float alpha, int accumulate, int batch, int N, int in, int out,
                                  int opt, const float* w_in, const float* b_in, float* w_out, float* b_out,
-                                 float* wT_out, float* w_state, float* b_state, float eta, float nu_or_eps, void* ws,
-                                 size_t ws_bytes, sprint_stream_t stream);
+                                 float* wT_out, float* w_state, float* b_state, float eta, float nu_or_eps,
+                                 float weight_decay, void* ws, size_t ws_bytes, sprint_stream_t stream);
 
 /* Transpose: dst[c][r] = src[r][c] for a row-major [rows][cols] matrix (the
  * w -> w^T copies the input-gradient GEMMs read). src and dst: device, must
@@ -337,9 +337,23 @@ int sprint_apply_update_momentum(const float* w_in, float* w_out, float* v, cons
 int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const float* const* bufs, int k, size_t n,
                                 float eta, float eps, sprint_stream_t stream);
 
+/* The parameter-server apply by rule: opt (sprint_opt) picks SGD, momentum,
+ * Adagrad (as above; nu_or_eps = nu or eps) or Nesterov momentum
+ *   v = nu*v - eta*S;   w_out = w_in + nu*v - eta*S
+ * (the pipelined-training page's appendices train with "SGD with Nesterov
+ * momentum" and print no formula: this is the usual form in the units of the
+ * momentum rule above). weight_decay (lambda) adds L2 decay at the server:
+ * S <- S + lambda*w_in before the rule (0: off, and the results equal the
+ * sprint_apply_update_sgd / _momentum / _adagrad calls bit for bit). state: v
+ * (momentum, Nesterov) or G (Adagrad), NULL for SGD. Arguments otherwise as
+ * the calls above. */
+int sprint_apply_update(int opt, const float* w_in, float* w_out, float* state, const float* const* bufs, int k,
+                        size_t n, float eta, float nu_or_eps, float weight_decay, sprint_stream_t stream);
+
 /* The same update over n_total elements by rule `opt` (sprint_opt; nu_or_eps
- * = nu for momentum, eps for Adagrad, unused for SGD), bit for bit what the
- * rule's sprint_apply_update_* call over n_total computes, whose first
+ * = nu for momentum and Nesterov, eps for Adagrad, unused for SGD; weight
+ * decay as sprint_apply_update), bit for bit what sprint_apply_update over
+ * n_total computes, whose first
  * rows*cols elements are a row-major [rows][cols] weight matrix that is also
  * written transposed: wT_out[c*rows + r] = w_out[r*cols + c] (device
  * [cols][rows]: the copy the input-gradient GEMMs read, written in the same
@@ -350,7 +364,7 @@ int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const
  * rows, cols >= 1, n_total >= rows*cols. */
 int sprint_apply_update_t(int opt, const float* w_in, float* w_out, float* wT_out, float* state,
                           const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta,
-                          float nu_or_eps, sprint_stream_t stream);
+                          float nu_or_eps, float weight_decay, sprint_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Staleness schedule (host only) — the delays of asynchronous SGD ([S] Sec. 1,

@@ -45,16 +45,16 @@ enum : int {
 constexpr int kMaxGroup = 16;
 
 // parameter-server update rules (the values of sprint_opt)
-enum PsOpt : int { PS_SGD = 0, PS_MOMENTUM = 1, PS_ADAGRAD = 2 };
+enum PsOpt : int { PS_SGD = 0, PS_MOMENTUM = 1, PS_ADAGRAD = 2, PS_NESTEROV = 3 };
 
 // the standalone update kernels by rule over k GradBufs (update.cu); the _t
 // form updates a row-major [rows][cols] matrix, also writing W' transposed,
 // and then the elements up to n_total after it without transposing
 int launch_ps_update(int opt, const char* fn, const float* w_in, float* w_out, float* state, const float* const* bufs,
-                     int k, size_t n, float eta, float hp, sprint_stream_t stream);
+                     int k, size_t n, float eta, float hp, float wd, sprint_stream_t stream);
 int launch_ps_update_t(int opt, const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
                        const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
-                       sprint_stream_t stream);
+                       float wd, sprint_stream_t stream);
 
 // ---------------------------------------------------------------- device side
 #if defined(__CUDACC__)
@@ -346,18 +346,26 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int n, bool a_mn_major, bool b
 
 // One parameter of the parameter-server update (UpdateWeights of Algorithm 2
 // in the SPRINT report; DistBelief's w' := w - eta*dw), given the summed
-// gradient s: SGD w' = w - eta*s; momentum v' = hp*v - eta*s, w' = w + v';
-// Adagrad G' = G + s*s, w' = w - eta*s/(sqrt(G') + hp). The standalone update
-// kernel and the update fused into the weight-gradient GEMM both call this, so
-// they round identically.
+// gradient s, with weight decay wd (s <- s + wd*w first, when wd != 0):
+//   SGD       w' = w - eta*s
+//   momentum  v' = hp*v - eta*s, w' = w + v'
+//   Nesterov  v' = hp*v - eta*s, w' = w + hp*v' - eta*s
+//   Adagrad   G' = G + s*s, w' = w - eta*s/(sqrt(G') + hp)
+// Every update kernel calls this one function, so they all round identically.
 template <int OPT>
-__device__ __forceinline__ void ps_apply1(float s, float w, float* state, float eta, float hp, float& w_new) {
+__device__ __forceinline__ void ps_apply1(float s, float w, float* state, float eta, float hp, float wd,
+                                          float& w_new) {
+    if (wd != 0.f) s = s + wd * w;
     if constexpr (OPT == PS_SGD) {
         w_new = w - eta * s;
     } else if constexpr (OPT == PS_MOMENTUM) {
         const float v = hp * (*state) - eta * s;
         *state = v;
         w_new = w + v;
+    } else if constexpr (OPT == PS_NESTEROV) {
+        const float v = hp * (*state) - eta * s;
+        *state = v;
+        w_new = w + hp * v - eta * s;
     } else {
         const float g = *state + s * s;
         *state = g;

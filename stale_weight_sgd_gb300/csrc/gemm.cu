@@ -1501,7 +1501,7 @@ struct PsArgs {
     float* wT_out;
     float* w_state;
     float* b_state;
-    float eta, hp;
+    float eta, hp, wd;
 };
 
 static int fc_bwd_batched_impl(const char* fn, const float* const* x, const float* const* xT1, const float* const* w,
@@ -1536,8 +1536,8 @@ static int fc_bwd_batched_impl(const char* fn, const float* const* x, const floa
     const size_t tail_ws_bytes = ws ? ws_bytes - per * batch : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (ps) {
-        SPRINT_REQUIRE(ps->opt >= PS_SGD && ps->opt <= PS_ADAGRAD, SPRINT_ERR_INVALID_ARG, "%s: unknown update rule %d",
-                       fn, ps->opt);
+        SPRINT_REQUIRE(ps->opt >= PS_SGD && ps->opt <= PS_NESTEROV, SPRINT_ERR_INVALID_ARG,
+                       "%s: unknown update rule %d", fn, ps->opt);
         SPRINT_REQUIRE(batch <= kMaxGroup, SPRINT_ERR_UNSUPPORTED, "%s: the update sums at most %d GradBufs (got %d)",
                        fn, kMaxGroup, batch);
         SPRINT_REQUIRE(ps->w_in && ps->w_out && (ps->opt == PS_SGD || ps->w_state), SPRINT_ERR_INVALID_ARG,
@@ -1558,14 +1558,14 @@ static int fc_bwd_batched_impl(const char* fn, const float* const* x, const floa
         const float* const* bufs = const_cast<const float* const*>(dw);
         if (ps->wT_out)
             r = launch_ps_update_t(ps->opt, fn, ps->w_in, ps->w_out, ps->wT_out, ps->w_state, bufs, batch, out, in,
-                                   static_cast<size_t>(out) * in, ps->eta, ps->hp, stream);
+                                   static_cast<size_t>(out) * in, ps->eta, ps->hp, ps->wd, stream);
         else
             r = launch_ps_update(ps->opt, fn, ps->w_in, ps->w_out, ps->w_state, bufs, batch,
-                                 static_cast<size_t>(out) * in, ps->eta, ps->hp, stream);
+                                 static_cast<size_t>(out) * in, ps->eta, ps->hp, ps->wd, stream);
         if (r) return r;
         if (db)
             return launch_ps_update(ps->opt, fn, ps->b_in, ps->b_out, ps->b_state, const_cast<const float* const*>(db),
-                                    batch, static_cast<size_t>(out), ps->eta, ps->hp, stream);
+                                    batch, static_cast<size_t>(out), ps->eta, ps->hp, ps->wd, stream);
         return SPRINT_OK;
     };
     const bool extras = xT1 || dyT || dxT;
@@ -1681,9 +1681,9 @@ extern "C" int sprint_fc_bwd_update_batched(const float* const* x, const float* 
                                             float* const* dw, float* const* db, float alpha, int accumulate,
                                             int batch, int N, int in, int out, int opt, const float* w_in,
                                             const float* b_in, float* w_out, float* b_out, float* wT_out,
-                                            float* w_state, float* b_state, float eta, float nu_or_eps, void* ws,
-                                            size_t ws_bytes, sprint_stream_t stream) {
-    const PsArgs ps{opt, w_in, b_in, w_out, b_out, wT_out, w_state, b_state, eta, nu_or_eps};
+                                            float* w_state, float* b_state, float eta, float nu_or_eps,
+                                            float weight_decay, void* ws, size_t ws_bytes, sprint_stream_t stream) {
+    const PsArgs ps{opt, w_in, b_in, w_out, b_out, wT_out, w_state, b_state, eta, nu_or_eps, weight_decay};
     return fc_bwd_batched_impl(__func__, x, xT1, w, wT, dy, dyT, relu_src, dx, dxT, dw, db, alpha, accumulate, batch,
                                N, in, out, ws, ws_bytes, stream, &ps);
 }

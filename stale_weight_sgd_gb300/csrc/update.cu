@@ -26,7 +26,7 @@ __device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpr
 // one float4 are in flight together.
 template <int OPT, int K>
 __global__ void __launch_bounds__(kThreads) update_kernel(const float* w_in, float* w_out, float* state, BufPtrs bufs,
-                                                          size_t n, float eta, float hp) {
+                                                          size_t n, float eta, float hp, float wd) {
     const size_t n4 = n / 4;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -45,10 +45,10 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const float* w_in, flo
             s.w += g[j].w;
         }
         float4 o;
-        ps_apply1<OPT>(s.x, w.x, &st.x, eta, hp, o.x);
-        ps_apply1<OPT>(s.y, w.y, &st.y, eta, hp, o.y);
-        ps_apply1<OPT>(s.z, w.z, &st.z, eta, hp, o.z);
-        ps_apply1<OPT>(s.w, w.w, &st.w, eta, hp, o.w);
+        ps_apply1<OPT>(s.x, w.x, &st.x, eta, hp, wd, o.x);
+        ps_apply1<OPT>(s.y, w.y, &st.y, eta, hp, wd, o.y);
+        ps_apply1<OPT>(s.z, w.z, &st.z, eta, hp, wd, o.z);
+        ps_apply1<OPT>(s.w, w.w, &st.w, eta, hp, wd, o.w);
         if constexpr (OPT != PS_SGD) st_stream(state + 4 * i, st);
         st_stream(w_out + 4 * i, o);
     }
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const float* w_in, flo
         for (int j = 1; j < K; ++j) s += bufs.p[j][i];
         float st = (OPT != PS_SGD) ? state[i] : 0.f;
         float o;
-        ps_apply1<OPT>(s, w_in[i], &st, eta, hp, o);
+        ps_apply1<OPT>(s, w_in[i], &st, eta, hp, wd, o);
         if constexpr (OPT != PS_SGD) state[i] = st;
         w_out[i] = o;
     }
@@ -96,7 +96,7 @@ constexpr int kUtRows = 32, kUtCols = 128;
 template <int OPT, int K, bool VEC>
 __global__ void __launch_bounds__(256) update_t_kernel(const float* w_in, float* w_out, float* wT_out, float* state,
                                                        BufPtrs bufs, int rows, int cols, size_t n_total, float eta,
-                                                       float hp) {
+                                                       float hp, float wd) {
     __shared__ float tile[kUtRows][kUtCols + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int r0 = blockIdx.y * kUtRows, c0 = blockIdx.x * kUtCols;
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256) update_t_kernel(const float* w_in, float*
             for (int b = 1; b < K; ++b) sm += bufs.p[b][i];
             float st = (OPT != PS_SGD) ? state[i] : 0.f;
             float o;
-            ps_apply1<OPT>(sm, w_in[i], &st, eta, hp, o);
+            ps_apply1<OPT>(sm, w_in[i], &st, eta, hp, wd, o);
             if constexpr (OPT != PS_SGD) state[i] = st;
             w_out[i] = o;
         }
@@ -134,10 +134,10 @@ __global__ void __launch_bounds__(256) update_t_kernel(const float* w_in, float*
                 sm.z += g[b].z;
                 sm.w += g[b].w;
             }
-            ps_apply1<OPT>(sm.x, w.x, &st.x, eta, hp, o[0]);
-            ps_apply1<OPT>(sm.y, w.y, &st.y, eta, hp, o[1]);
-            ps_apply1<OPT>(sm.z, w.z, &st.z, eta, hp, o[2]);
-            ps_apply1<OPT>(sm.w, w.w, &st.w, eta, hp, o[3]);
+            ps_apply1<OPT>(sm.x, w.x, &st.x, eta, hp, wd, o[0]);
+            ps_apply1<OPT>(sm.y, w.y, &st.y, eta, hp, wd, o[1]);
+            ps_apply1<OPT>(sm.z, w.z, &st.z, eta, hp, wd, o[2]);
+            ps_apply1<OPT>(sm.w, w.w, &st.w, eta, hp, wd, o[3]);
             if constexpr (OPT != PS_SGD) st_stream(state + off, st);
             st_stream(w_out + off, make_float4(o[0], o[1], o[2], o[3]));
         } else {
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) update_t_kernel(const float* w_in, float*
                 float sm = bufs.p[0][off + e];
                 for (int b = 1; b < K; ++b) sm += bufs.p[b][off + e];
                 float st = (OPT != PS_SGD) ? state[off + e] : 0.f;
-                ps_apply1<OPT>(sm, w_in[off + e], &st, eta, hp, o[e]);
+                ps_apply1<OPT>(sm, w_in[off + e], &st, eta, hp, wd, o[e]);
                 if constexpr (OPT != PS_SGD) state[off + e] = st;
                 w_out[off + e] = o[e];
             }
@@ -173,7 +173,7 @@ int stream_grid(size_t n) {
 
 template <int OPT>
 int launch_update(const char* fn, const float* w_in, float* w_out, float* state, const float* const* bufs, int k,
-                  size_t n, float eta, float hp, sprint_stream_t stream) {
+                  size_t n, float eta, float hp, float wd, sprint_stream_t stream) {
     SPRINT_REQUIRE(k >= 1, SPRINT_ERR_SHAPE, "%s: k must be >= 1 (got %d)", fn, k);
     SPRINT_REQUIRE(k <= kMaxBufs, SPRINT_ERR_UNSUPPORTED, "%s: k = %d > %d buffers", fn, k, kMaxBufs);
     if (n == 0) return SPRINT_OK;
@@ -191,7 +191,7 @@ int launch_update(const char* fn, const float* w_in, float* w_out, float* state,
     const int grid = stream_grid(n);
     switch (k) {
 #define SPRINT_K(KK) \
-    case KK: update_kernel<OPT, KK><<<grid, kThreads, 0, s>>>(w_in, w_out, state, bp, n, eta, hp); break;
+    case KK: update_kernel<OPT, KK><<<grid, kThreads, 0, s>>>(w_in, w_out, state, bp, n, eta, hp, wd); break;
         SPRINT_K(1) SPRINT_K(2) SPRINT_K(3) SPRINT_K(4) SPRINT_K(5) SPRINT_K(6) SPRINT_K(7) SPRINT_K(8)
         SPRINT_K(9) SPRINT_K(10) SPRINT_K(11) SPRINT_K(12) SPRINT_K(13) SPRINT_K(14) SPRINT_K(15) SPRINT_K(16)
 #undef SPRINT_K
@@ -201,7 +201,7 @@ int launch_update(const char* fn, const float* w_in, float* w_out, float* state,
 
 template <int OPT>
 int launch_update_t(const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
-                    const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
+                    const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp, float wd,
                     sprint_stream_t stream) {
     SPRINT_REQUIRE(k >= 1, SPRINT_ERR_SHAPE, "%s: k must be >= 1 (got %d)", fn, k);
     SPRINT_REQUIRE(k <= kMaxBufs, SPRINT_ERR_UNSUPPORTED, "%s: k = %d > %d buffers", fn, k, kMaxBufs);
@@ -226,9 +226,9 @@ int launch_update_t(const char* fn, const float* w_in, float* w_out, float* wT_o
 #define SPRINT_K(KK)                                                                                            \
     case KK:                                                                                                    \
         if (vec)                                                                                                \
-            update_t_kernel<OPT, KK, true><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp); \
+            update_t_kernel<OPT, KK, true><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp, wd); \
         else                                                                                                    \
-            update_t_kernel<OPT, KK, false><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp); \
+            update_t_kernel<OPT, KK, false><<<grid, 256, 0, s>>>(w_in, w_out, wT_out, state, bp, rows, cols, n_total, eta, hp, wd); \
         break;
         SPRINT_K(1) SPRINT_K(2) SPRINT_K(3) SPRINT_K(4) SPRINT_K(5) SPRINT_K(6) SPRINT_K(7) SPRINT_K(8)
         SPRINT_K(9) SPRINT_K(10) SPRINT_K(11) SPRINT_K(12) SPRINT_K(13) SPRINT_K(14) SPRINT_K(15) SPRINT_K(16)
@@ -241,28 +241,32 @@ int launch_update_t(const char* fn, const float* w_in, float* w_out, float* wT_o
 
 // the standalone update by rule (PsOpt), for callers in other files
 int launch_ps_update(int opt, const char* fn, const float* w_in, float* w_out, float* state, const float* const* bufs,
-                     int k, size_t n, float eta, float hp, sprint_stream_t stream) {
+                     int k, size_t n, float eta, float hp, float wd, sprint_stream_t stream) {
     switch (opt) {
-        case PS_SGD: return launch_update<PS_SGD>(fn, w_in, w_out, nullptr, bufs, k, n, eta, hp, stream);
-        case PS_MOMENTUM: return launch_update<PS_MOMENTUM>(fn, w_in, w_out, state, bufs, k, n, eta, hp, stream);
-        case PS_ADAGRAD: return launch_update<PS_ADAGRAD>(fn, w_in, w_out, state, bufs, k, n, eta, hp, stream);
+        case PS_SGD: return launch_update<PS_SGD>(fn, w_in, w_out, nullptr, bufs, k, n, eta, hp, wd, stream);
+        case PS_MOMENTUM: return launch_update<PS_MOMENTUM>(fn, w_in, w_out, state, bufs, k, n, eta, hp, wd, stream);
+        case PS_NESTEROV: return launch_update<PS_NESTEROV>(fn, w_in, w_out, state, bufs, k, n, eta, hp, wd, stream);
+        case PS_ADAGRAD: return launch_update<PS_ADAGRAD>(fn, w_in, w_out, state, bufs, k, n, eta, hp, wd, stream);
         default: return fail(SPRINT_ERR_INVALID_ARG, "%s: unknown update rule %d", fn, opt);
     }
 }
 
 int launch_ps_update_t(int opt, const char* fn, const float* w_in, float* w_out, float* wT_out, float* state,
                        const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta, float hp,
-                       sprint_stream_t stream) {
+                       float wd, sprint_stream_t stream) {
     switch (opt) {
         case PS_SGD:
             return launch_update_t<PS_SGD>(fn, w_in, w_out, wT_out, nullptr, bufs, k, rows, cols, n_total, eta, hp,
-                                           stream);
+                                           wd, stream);
         case PS_MOMENTUM:
             return launch_update_t<PS_MOMENTUM>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, hp,
-                                                stream);
+                                                wd, stream);
+        case PS_NESTEROV:
+            return launch_update_t<PS_NESTEROV>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, hp,
+                                                wd, stream);
         case PS_ADAGRAD:
             return launch_update_t<PS_ADAGRAD>(fn, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, hp,
-                                               stream);
+                                               wd, stream);
         default: return fail(SPRINT_ERR_INVALID_ARG, "%s: unknown update rule %d", fn, opt);
     }
 }
@@ -284,22 +288,28 @@ extern "C" int sprint_gradbuf_accumulate(float* buf, const float* grad, size_t n
 
 extern "C" int sprint_apply_update_sgd(const float* w_in, float* w_out, const float* const* bufs, int k, size_t n,
                                        float eta, sprint_stream_t stream) {
-    return launch_update<PS_SGD>(__func__, w_in, w_out, nullptr, bufs, k, n, eta, 0.f, stream);
+    return launch_update<PS_SGD>(__func__, w_in, w_out, nullptr, bufs, k, n, eta, 0.f, 0.f, stream);
 }
 
 extern "C" int sprint_apply_update_momentum(const float* w_in, float* w_out, float* v, const float* const* bufs, int k,
                                             size_t n, float eta, float nu, sprint_stream_t stream) {
-    return launch_update<PS_MOMENTUM>(__func__, w_in, w_out, v, bufs, k, n, eta, nu, stream);
+    return launch_update<PS_MOMENTUM>(__func__, w_in, w_out, v, bufs, k, n, eta, nu, 0.f, stream);
 }
 
 extern "C" int sprint_apply_update_adagrad(const float* w_in, float* w_out, float* G, const float* const* bufs, int k,
                                            size_t n, float eta, float eps, sprint_stream_t stream) {
-    return launch_update<PS_ADAGRAD>(__func__, w_in, w_out, G, bufs, k, n, eta, eps, stream);
+    return launch_update<PS_ADAGRAD>(__func__, w_in, w_out, G, bufs, k, n, eta, eps, 0.f, stream);
+}
+
+extern "C" int sprint_apply_update(int opt, const float* w_in, float* w_out, float* state, const float* const* bufs,
+                                   int k, size_t n, float eta, float nu_or_eps, float weight_decay,
+                                   sprint_stream_t stream) {
+    return launch_ps_update(opt, __func__, w_in, w_out, state, bufs, k, n, eta, nu_or_eps, weight_decay, stream);
 }
 
 extern "C" int sprint_apply_update_t(int opt, const float* w_in, float* w_out, float* wT_out, float* state,
                                      const float* const* bufs, int k, int rows, int cols, size_t n_total, float eta,
-                                     float nu_or_eps, sprint_stream_t stream) {
+                                     float nu_or_eps, float weight_decay, sprint_stream_t stream) {
     return launch_ps_update_t(opt, __func__, w_in, w_out, wT_out, state, bufs, k, rows, cols, n_total, eta, nu_or_eps,
-                              stream);
+                              weight_decay, stream);
 }

@@ -135,3 +135,18 @@ def train_flops_per_image(net) -> float:
         macs = L.h * L.w * L.cout * 9 * L.cin if L.kind == "conv" else L.cout * L.cin
         f += 2.0 * macs * (2 if i == 0 else 3)
     return f
+
+
+def staleness_degrees(stage_delays) -> list[int]:
+    """Degree of staleness of each pipeline stage pair: the number of steps its
+    weights lag ("Pipelined training of deep CNNs with stale weights", Sec. 4.1)."""
+    return [int(s) for s in stage_delays]
+
+
+def stale_weight_percent(shapes: list[LayerShape], stage_of_layer, stage_delays) -> float:
+    """Percentage of the parameters (weights and biases) that sit in stages
+    computing on stale weights (delay > 0), same section: every layer before
+    the last pipeline-register pair trains on old weights."""
+    counts = [L.w_numel + L.cout for L in shapes]
+    stale = sum(n for n, k in zip(counts, stage_of_layer) if stage_delays[k] > 0)
+    return 100.0 * stale / sum(counts)

@@ -56,9 +56,10 @@ _SIGS = {
     "sprint_fc_fwd_batched_workspace_size": ([], SZ),
     "sprint_fc_batched_workspace_size": ([I, I, I, I, I], SZ),
     "sprint_fc_bwd_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P], I),
-    "sprint_apply_update_t": ([I, P, P, P, P, P, I, I, I, SZ, F, F, P], I),
-    "sprint_fc_bwd_update_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, I, P, P, P, P, P, P, P, F, F, P,
-                                      SZ, P], I),
+    "sprint_apply_update": ([I, P, P, P, P, I, SZ, F, F, F, P], I),
+    "sprint_apply_update_t": ([I, P, P, P, P, P, I, I, I, SZ, F, F, F, P], I),
+    "sprint_fc_bwd_update_batched": ([P, P, P, P, P, P, P, P, P, P, P, F, I, I, I, I, I, I, P, P, P, P, P, P, P, F, F, F,
+                                      P, SZ, P], I),
     "sprint_transpose": ([P, P, I, I, P], I),
     "sprint_pool_fwd": ([P, P, P, I, I, I, I, P], I),
     "sprint_pool_bwd": ([P, P, P, P, I, I, I, I, P], I),
@@ -244,26 +245,33 @@ def sprint_fc_bwd_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate,
         int(accumulate), n, N, fin, fout, _p(ws), ws_bytes, _s(stream)))
 
 
-SPRINT_OPT = {"sgd": 0, "momentum": 1, "adagrad": 2}
+SPRINT_OPT = {"sgd": 0, "momentum": 1, "adagrad": 2, "nesterov": 3}
+
+
+def sprint_apply_update(opt, w_in, w_out, state, bufs, n, eta, nu_or_eps=0.0, weight_decay=0.0, stream=None):
+    return _check("sprint_apply_update", lib().sprint_apply_update(
+        SPRINT_OPT.get(opt, opt), _p(w_in), _p(w_out), _p(state), _ptr_array(bufs), len(bufs), n, float(eta),
+        float(nu_or_eps), float(weight_decay), _s(stream)))
 
 
 def sprint_apply_update_t(opt, w_in, w_out, wT_out, state, bufs, rows, cols, eta, nu_or_eps=0.0, stream=None,
-                          n_total=None):
+                          n_total=None, weight_decay=0.0):
     n = rows * cols if n_total is None else n_total
     return _check("sprint_apply_update_t", lib().sprint_apply_update_t(
         SPRINT_OPT.get(opt, opt), _p(w_in), _p(w_out), _p(wT_out), _p(state), _ptr_array(bufs), len(bufs), rows, cols,
-        n, float(eta), float(nu_or_eps), _s(stream)))
+        n, float(eta), float(nu_or_eps), float(weight_decay), _s(stream)))
 
 
 def sprint_fc_bwd_update_batched(x, w, wT, dy, relu_src, dx, dw, db, alpha, accumulate, N, fin, fout, opt, w_in, b_in,
                                  w_out, b_out, wT_out, w_state, b_state, eta, nu_or_eps, ws=None, ws_bytes=0,
-                                 stream=None, xT1=None, dyT=None, dxT=None):
+                                 stream=None, xT1=None, dyT=None, dxT=None, weight_decay=0.0):
     n = len(x)
     return _check("sprint_fc_bwd_update_batched", lib().sprint_fc_bwd_update_batched(
         _ptr_array(x), _opt_array(xT1), _ptr_array(w), _opt_array(wT), _ptr_array(dy), _opt_array(dyT),
         _opt_array(relu_src), _opt_array(dx), _opt_array(dxT), _ptr_array(dw), _opt_array(db), float(alpha),
         int(accumulate), n, N, fin, fout, SPRINT_OPT.get(opt, opt), _p(w_in), _p(b_in), _p(w_out), _p(b_out),
-        _p(wT_out), _p(w_state), _p(b_state), float(eta), float(nu_or_eps), _p(ws), ws_bytes, _s(stream)))
+        _p(wT_out), _p(w_state), _p(b_state), float(eta), float(nu_or_eps), float(weight_decay), _p(ws), ws_bytes,
+        _s(stream)))
 
 
 def sprint_softmax_xent_batched(logits, labels, loss, dlogits, N, C, reduction_sum=0, stream=None):

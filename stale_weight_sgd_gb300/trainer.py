@@ -48,14 +48,23 @@ import numpy as np
 import torch
 
 from . import sprint as S
-from .model import layer_shapes, pack, padded_size, unpack
+from .model import layer_shapes, pack, padded_size, stale_weight_percent, staleness_degrees, unpack
 
 
 class StaleSGD:
     def __init__(self, net, batch, *, replicas=1, max_delay=0, schedule_seed=0, stage_of_layer=None,
-                 stage_delays=None, optimizer="sgd", eta=0.01, nu=0.9, eps=1e-8, g0=0.1, concurrent=True,
-                 graphs="auto", device="cuda"):
-        """concurrent: run the per-layer updates on a second stream, overlapping
+                 stage_delays=None, hybrid_switch=None, n_fetch=None, n_push=None, optimizer="sgd", eta=0.01,
+                 nu=0.9, eps=1e-8, g0=0.1, weight_decay=0.0, concurrent=True, graphs="auto", device="cuda"):
+        """Delays: seeded per-replica delays up to max_delay (ASGD), fixed per-stage
+        delays (pipeline: stage_of_layer, stage_delays; hybrid_switch = N_p turns
+        them to 0 from step N_p on, "Pipelined training of deep CNNs with stale
+        weights" Sec. 4.2), or DistBelief's n_fetch / n_push (every replica
+        computes on the server's parameters of its last fetch step, t % n_fetch ==
+        0, accumulates its gradients in its GradBuf and pushes them at steps with
+        (t + 1) % n_push == 0, when the server applies the R buffers once).
+        optimizer: "sgd", "momentum", "nesterov" or "adagrad"; weight_decay adds
+        lambda*W to the summed gradient at the server.
+        concurrent: run the per-layer updates on a second stream, overlapping
         the rest of the backward pass (False: everything on one stream).
         graphs: replay captured CUDA graphs of the step ("auto": when the delay
         schedule is periodic — pipeline stages or no delay — so the same few
@@ -67,24 +76,37 @@ class StaleSGD:
         self.N = int(batch)
         self.R = int(replicas)
         self.pipeline = stage_delays is not None
+        self.fetch_push = n_fetch is not None or n_push is not None
+        self.hybrid_switch = None if hybrid_switch is None else int(hybrid_switch)
         if self.pipeline:
             assert stage_of_layer is not None and len(stage_of_layer) == len(self.shapes)
+            assert not self.fetch_push and max_delay == 0
             self.stage_of_layer = list(stage_of_layer)
             self.stage_delays = [int(s) for s in stage_delays]
             self.S = max(self.stage_delays)
+        elif self.fetch_push:
+            assert max_delay == 0 and self.hybrid_switch is None
+            self.n_fetch, self.n_push = int(n_fetch or 1), int(n_push or 1)
+            assert self.n_fetch >= 1 and self.n_push >= 1
+            # versions count server updates: at most D behind the current one
+            self.S = (self.n_fetch - 1) // self.n_push + 1
         else:
+            assert self.hybrid_switch is None
             self.S = int(max_delay)
+        self.RS = self.S + 2 if self.fetch_push else self.S + 1   # weight-version ring slots
         self.seed = int(schedule_seed)
         self.optimizer = optimizer
         self.eta, self.nu, self.eps, self.g0 = float(eta), float(nu), float(eps), float(g0)
+        self.weight_decay = float(weight_decay)
         self.dev = torch.device(device)
         f32 = dict(dtype=torch.float32, device=self.dev)
 
-        self.ring = torch.zeros((self.S + 1, self.n), **f32)
-        self.ringT = torch.zeros((self.S + 1, self.n), **f32)   # W^T of every layer that needs dX
-        self.gradbuf_sets = torch.zeros((2, self.R, self.n), **f32)   # step t writes set t % 2
+        self.ring = torch.zeros((self.RS, self.n), **f32)
+        self.ringT = torch.zeros((self.RS, self.n), **f32)   # W^T of every layer that needs dX
+        # the gradients pushed by update j live in set j % 2 (step t's update index: _cur(t))
+        self.gradbuf_sets = torch.zeros((2, self.R, self.n), **f32)
         self.gradbuf = self.gradbuf_sets[0]
-        if optimizer == "momentum":
+        if optimizer in ("momentum", "nesterov"):
             self.opt_state = torch.zeros(self.n, **f32)
         elif optimizer == "adagrad":
             self.opt_state = torch.full((self.n,), self.g0, **f32)
@@ -115,7 +137,7 @@ class StaleSGD:
         else:
             self.rep_streams = [main] * self.R
             self.rep_ws = [self.ws] * self.R
-        self.K = self.S + 3   # version v of layer l exists: ev_layer[l][v % K]
+        self.K = self.RS + 2   # version v of layer l exists: ev_layer[l][v % K]
         self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
         self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
         for evs in self.ev_layer:
@@ -126,7 +148,7 @@ class StaleSGD:
         self.batches_x = None
         self.batches_y = None
         self.t = 0
-        periodic = self.pipeline or self.S == 0
+        periodic = (self.pipeline or self.S == 0) and not self.fetch_push
         self.use_graphs = periodic if graphs == "auto" else bool(graphs)
         self._graphs = {}            # step key -> captured CUDA graph
         self._graph_steps = False    # the last step ran as a graph replay
@@ -206,7 +228,7 @@ class StaleSGD:
         self.ring[0].copy_(w.to(self.dev))
         for li in range(1, len(self.shapes)):
             self._transpose_layer(li, 0, self.main_stream)
-        if self.optimizer == "momentum":
+        if self.optimizer in ("momentum", "nesterov"):
             self.opt_state.zero_()
         elif self.optimizer == "adagrad":
             self.opt_state.fill_(self.g0)
@@ -235,10 +257,23 @@ class StaleSGD:
         self.inputs_pending = True
 
     def weights(self, version=None) -> np.ndarray:
-        """Dense copy of W(version) (default: the current version)."""
-        v = self.t if version is None else version
+        """Dense copy of W(version) (default: the current version). Versions are
+        steps (W(t) is the version before step t's update), or server updates
+        with n_fetch / n_push."""
+        v = self._cur(self.t) if version is None else version
         torch.cuda.synchronize(self.dev)
-        return unpack(self.shapes, self.ring[v % (self.S + 1)].cpu().numpy())
+        return unpack(self.shapes, self.ring[v % self.RS].cpu().numpy())
+
+    def staleness(self, t=None):
+        """Stale-weight metrics of a pipeline at step t (default: the next step),
+        "Pipelined training of deep CNNs with stale weights" Sec. 4.1: the degree
+        of staleness of every stage pair (the steps its weights lag) and the
+        percentage of the parameters held by stages with stale weights."""
+        assert self.pipeline
+        t = self.t if t is None else t
+        delays = [self._stage_delay(k, t) for k in range(len(self.stage_delays))]
+        return dict(degrees=staleness_degrees(delays),
+                    stale_weight_percent=stale_weight_percent(self.shapes, self.stage_of_layer, delays))
 
     def _transpose_layer(self, li, slot, stream):
         """W_l^T of version slot `slot` into ringT (layers after the first need dE/dX)."""
@@ -255,9 +290,30 @@ class StaleSGD:
         return self._sched[:steps]
 
     # ------------------------------------------------------------------ one step
+    def _stage_delay(self, k, t):
+        """Delay of pipeline stage k at step t (0 from the hybrid switch on)."""
+        if self.hybrid_switch is not None and t >= self.hybrid_switch:
+            return 0
+        return self.stage_delays[k]
+
+    def _cur(self, t):
+        """Index of the newest weight version before step t's update: steps, or
+        server updates with n_fetch / n_push (pushes end steps n_push-1, 2n_push-1, ...)."""
+        return t // self.n_push if self.fetch_push else t
+
+    def _pushes(self, t):
+        """Step t ends with a server update."""
+        return not self.fetch_push or (t + 1) % self.n_push == 0
+
+    def _first(self, t):
+        """Step t assigns (rather than adds to) the GradBufs: the first step of a push window."""
+        return not self.fetch_push or t % self.n_push == 0
+
     def _version(self, t, r, layer):
         if self.pipeline:
-            return max(0, t - self.stage_delays[self.stage_of_layer[layer]])
+            return max(0, t - self._stage_delay(self.stage_of_layer[layer], t))
+        if self.fetch_push:   # the server's version at the replica's last fetch step
+            return (t // self.n_fetch * self.n_fetch) // self.n_push
         s = int(self.schedule(t + 1)[t, r]) if self.S > 0 else 0
         return max(0, t - s)
 
@@ -266,34 +322,27 @@ class StaleSGD:
         ring slot t+1 in one launch, with W's transpose written in the same pass
         (layers after the first)."""
         off, cnt = self.span[li]
-        slot_in, slot_out = t % (self.S + 1), (t + 1) % (self.S + 1)
+        j = self._cur(t)
+        slot_in, slot_out = j % self.RS, (j + 1) % self.RS
         sh = stream.cuda_stream
         hp = self.eps if self.optimizer == "adagrad" else self.nu
-        gb = self.gradbuf_sets[t % 2]
+        gb = self.gradbuf_sets[j % 2]
 
         def ptrs(o):
             return (self.ring[slot_in].data_ptr() + 4 * o, self.ring[slot_out].data_ptr() + 4 * o,
                     self.opt_state.data_ptr() + 4 * o if self.opt_state is not None else None,
                     [gb[r].data_ptr() + 4 * o for r in range(self.R)])
 
-        def plain(o, n):
-            w_in, w_out, st, bufs = ptrs(o)
-            if self.optimizer == "sgd":
-                S.sprint_apply_update_sgd(w_in, w_out, bufs, n, self.eta, sh)
-            elif self.optimizer == "momentum":
-                S.sprint_apply_update_momentum(w_in, w_out, st, bufs, n, self.eta, self.nu, sh)
-            else:
-                S.sprint_apply_update_adagrad(w_in, w_out, st, bufs, n, self.eta, self.eps, sh)
-
+        w_in, w_out, st, bufs = ptrs(off)
         if li == 0:   # no input gradient: no transpose; W, b and padding in one pass
-            plain(off, cnt)
+            S.sprint_apply_update(self.optimizer, w_in, w_out, st, bufs, cnt, self.eta, hp, self.weight_decay, sh)
             return
         L = self.shapes[li]
         rows, cols = (L.cout, 9 * L.cin) if L.kind == "conv" else (L.cout, L.cin)
-        w_in, w_out, st, bufs = ptrs(off)
         wT = self.ringT[slot_out].data_ptr() + 4 * L.w_off
         # W (transposed copy too), then the rest of the span (b and padding) in the same launch
-        S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh, n_total=cnt)
+        S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh, n_total=cnt,
+                                weight_decay=self.weight_decay)
 
     def _per_replica(self, fn):
         """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica
@@ -317,10 +366,10 @@ class StaleSGD:
         """Everything a captured step bakes in: weight slots, GradBuf parity, batches."""
         nL = len(self.shapes)
         P = self.batches_x.shape[0]
-        slots = tuple(self._version(t, r, li) % (self.S + 1) for r in range(self.R) for li in range(nL))
+        slots = tuple(self._version(t, r, li) % self.RS for r in range(self.R) for li in range(nL))
         bx = tuple(self.batches_x[(t * self.R + r) % P].data_ptr() for r in range(self.R))
         by = tuple(self.batches_y[(t * self.R + r) % P].data_ptr() for r in range(self.R))
-        return slots, t % 2, bx, by
+        return slots, self._cur(t) % 2, self._first(t), self._pushes(t), bx, by
 
     def _capture(self, t, key):
         """Captures step t's graph (not run): on a stream of our own (capture needs
@@ -379,7 +428,7 @@ class StaleSGD:
                 g.replay()
             self.graph_launch_adjust += self._graph_kernels[key]
             self._graph_steps = True
-            self.gradbuf = self.gradbuf_sets[t % 2]
+            self.gradbuf = self.gradbuf_sets[self._cur(t) % 2]
             self.t = t + 1
             return
         self._issue(t, graph=False)
@@ -394,8 +443,10 @@ class StaleSGD:
         row = self.n * 4
         ring, ringT = self.ring.data_ptr(), self.ringT.data_ptr()
         ver = [[self._version(t, r, li) for li in range(nL)] for r in range(R)]
-        slot = [[v % (self.S + 1) for v in vr] for vr in ver]
-        gb = [self.gradbuf_sets[t % 2][r].data_ptr() for r in range(R)]
+        slot = [[v % self.RS for v in vr] for vr in ver]
+        j = self._cur(t)
+        gb = [self.gradbuf_sets[j % 2][r].data_ptr() for r in range(R)]
+        acc = 0 if self._first(t) else 1   # GradBuf: assign at a window's first step, add afterwards
         P = self.batches_x.shape[0]
         bidx = [(t * R + r) % P for r in range(R)]
         ws, wsb = self.ws, self.ws_bytes
@@ -442,9 +493,9 @@ class StaleSGD:
         for li in range(nL - 1, -1, -1):
             L = self.shapes[li]
             prev = self.shapes[li - 1] if li > 0 else None
-            # update t-2 (the last reader of GradBuf set t % 2) of this layer has finished
+            # update j-2 (the last reader of GradBuf set j % 2) of this layer has finished
             if not graph:
-                main.wait_event(self.ev_layer[li][max(t - 1, 0) % K])
+                main.wait_event(self.ev_layer[li][max(j - 1, 0) % K])
             dw = [gb[r] + 4 * L.w_off for r in range(R)]
             db = [gb[r] + 4 * L.b_off for r in range(R)]
             hT = None
@@ -458,12 +509,12 @@ class StaleSGD:
                     hT = hT_all   # the layer below is FC too: it reads dE/dy transposed
                 S.sprint_fc_bwd_batched(inp[li], [W(r, li) for r in range(R)],
                                         [WT(r, li) for r in range(R)] if prev is not None else None, g, relu_src,
-                                        h if prev is not None else None, dw, db, 1.0, 0, N, L.cin, L.cout, ws, wsb,
+                                        h if prev is not None else None, dw, db, 1.0, acc, N, L.cin, L.cout, ws, wsb,
                                         sh, xT1=xT1, dyT=gT, dxT=hT)
             else:
                 def bwd(r, st, rws, rwsb, li=li, L=L, prev=prev, g=g, h=h, dw=dw, db=db):
-                    S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, 0, N, L.h, L.w, L.cin, L.cout, 1, rws, rwsb,
-                                     st)
+                    S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1, rws,
+                                     rwsb, st)
                     if prev is not None:
                         relu_src = None if prev.pool else inp[li][r]
                         S.sprint_conv_dX(g[r], W(r, li), WT(r, li), relu_src, h[r], N, L.h, L.w, L.cin, L.cout, 1,
@@ -474,11 +525,12 @@ class StaleSGD:
                                               prev.w, prev.cout, st)
                 self._per_replica(bwd)
             # layer li's gradients are final: its update overlaps the layers below
-            self.ev_bwd[li].record(main)
-            upd.wait_event(self.ev_bwd[li])
-            self._update_layer(t, li, upd)
-            if not graph:
-                self.ev_layer[li][(t + 1) % K].record(upd)
+            if self._pushes(t):
+                self.ev_bwd[li].record(main)
+                upd.wait_event(self.ev_bwd[li])
+                self._update_layer(t, li, upd)
+                if not graph:
+                    self.ev_layer[li][(j + 1) % K].record(upd)
             if prev is None:
                 break
             if prev.kind == "conv" and prev.pool:
@@ -496,7 +548,7 @@ class StaleSGD:
             self.ev_graph_upd.record(upd)
             main.wait_event(self.ev_graph_upd)
             return
-        self.gradbuf = self.gradbuf_sets[t % 2]   # the GradBufs of the step just issued
+        self.gradbuf = self.gradbuf_sets[j % 2]   # the GradBufs of the step just issued
         self.t = t + 1
 
     def join(self, stream=None):
@@ -511,7 +563,7 @@ class StaleSGD:
                 st.wait_event(ev)
             return
         for evs in self.ev_layer:
-            st.wait_event(evs[self.t % self.K])
+            st.wait_event(evs[self._cur(self.t) % self.K])
 
     def step_loss(self) -> float:
         """Mean over replicas of the last step's loss (synchronises)."""

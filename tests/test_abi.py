@@ -54,12 +54,14 @@ def test_update_rejects_bad_arguments(S):
     assert L.sprint_apply_update_adagrad(16, 16, None, arr, 2, 10, ctypes.c_float(0.1), ctypes.c_float(1e-8), None) == 1
     f = ctypes.c_float
     n = ctypes.c_size_t
-    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 0, 8, n(0), f(0.1), f(0), None) == 2     # no rows
-    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 4, 8, n(31), f(0.1), f(0), None) == 2    # n < 4*8
-    assert L.sprint_apply_update_t(0, 16, 16, None, None, arr, 2, 4, 8, n(32), f(0.1), f(0), None) == 1  # NULL wT
-    assert L.sprint_apply_update_t(1, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0.9), None) == 1  # NULL v
-    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 17, 4, 8, n(32), f(0.1), f(0), None) == 4   # k > 16
-    assert L.sprint_apply_update_t(5, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0), None) == 1    # rule
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 0, 8, n(0), f(0.1), f(0), f(0), None) == 2     # no rows
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 2, 4, 8, n(31), f(0.1), f(0), f(0), None) == 2    # n < 4*8
+    assert L.sprint_apply_update_t(0, 16, 16, None, None, arr, 2, 4, 8, n(32), f(0.1), f(0), f(0), None) == 1  # NULL wT
+    assert L.sprint_apply_update_t(1, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0.9), f(0), None) == 1  # NULL v
+    assert L.sprint_apply_update_t(0, 16, 16, 16, None, arr, 17, 4, 8, n(32), f(0.1), f(0), f(0), None) == 4   # k > 16
+    assert L.sprint_apply_update_t(5, 16, 16, 16, None, arr, 2, 4, 8, n(32), f(0.1), f(0), f(0), None) == 1    # rule
+    assert L.sprint_apply_update(3, 16, 16, None, arr, 2, n(8), f(0.1), f(0.9), f(0), None) == 1   # Nesterov, NULL v
+    assert L.sprint_apply_update(4, 16, 16, 16, arr, 2, n(8), f(0.1), f(0.9), f(0), None) == 1     # unknown rule
 
 
 def test_shape_and_workspace_errors(S):
@@ -130,3 +132,15 @@ def test_no_cpu_fallback_in_product_path():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), f
                 assert not re.search(r"^\s*(import|from)\s+synth", src, re.M), f
+
+
+def test_stale_weight_metrics_match_the_oracle():
+    # host logic of the pipeline metrics against the oracle's own count (VGG-16, CIFAR shape)
+    import oracle as O
+    from stale_weight_sgd_gb300 import model
+    shapes = model.layer_shapes(model.NETWORKS["vgg_c"])
+    layers = O.build_layers(O.ARCHS["vgg_c"])
+    for delays in ([3, 2, 1, 0], [0, 0, 0, 0], [1, 0, 2, 0], [5, 5, 5, 5]):
+        assert model.stale_weight_percent(shapes, model.VGG_C_STAGES, delays) == pytest.approx(
+            O.stale_weight_percent(layers, model.VGG_C_STAGES, delays), rel=1e-15)
+        assert model.staleness_degrees(delays) == O.staleness_degrees(delays)

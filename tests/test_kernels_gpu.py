@@ -91,6 +91,47 @@ def test_update_transposed(S, rows, cols, tail, k, opt):
     assert rel_inf(a, ref) <= TOL_UPDATE
 
 
+@pytest.mark.parametrize("opt", ["sgd", "momentum", "nesterov", "adagrad"])
+@pytest.mark.parametrize("wd", [0.0, 0.004])
+@pytest.mark.parametrize("k", [1, 3])
+def test_update_rules_with_weight_decay(S, opt, wd, k):
+    """sprint_apply_update by rule, with weight decay, against the oracle; with
+    weight decay 0 bit for bit the rule-specific entry points."""
+    n = 10007
+    w = _f32(6, "w", n, 0.05)
+    bufs = [_f32(6, f"g{j}", n, 1e-3) for j in range(k)]
+    st0 = np.abs(_f32(6, "s", n, 1e-2)) + (0.1 if opt == "adagrad" else 0.0)
+    eta, hp = 0.01, (1e-8 if opt == "adagrad" else 0.9)
+    dbufs = [dev(b) for b in bufs]
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    st = dev(st0) if opt != "sgd" else None
+    S.sprint_apply_update(opt, dev(w), out, st, dbufs, n, eta, hp, wd)
+    ref, st_ref = O.apply_update(w, bufs, opt, eta, nu=hp, eps=hp, state=st0.astype(np.float64), weight_decay=wd)
+    assert rel_inf(host(out), ref) <= TOL_UPDATE
+    if opt != "sgd":
+        assert rel_inf(host(st), st_ref) <= TOL_UPDATE
+    if wd == 0.0 and opt != "nesterov":
+        out2 = torch.empty_like(out)
+        st2 = dev(st0) if opt != "sgd" else None
+        if opt == "sgd":
+            S.sprint_apply_update_sgd(dev(w), out2, dbufs, n, eta)
+        elif opt == "momentum":
+            S.sprint_apply_update_momentum(dev(w), out2, st2, dbufs, n, eta, hp)
+        else:
+            S.sprint_apply_update_adagrad(dev(w), out2, st2, dbufs, n, eta, hp)
+        assert np.array_equal(host(out), host(out2))
+    # the transposing form over a matrix (plus a bias tail): bit for bit the flat one
+    rows, cols = 97, 100
+    out_t = torch.empty(n, dtype=torch.float32, device="cuda")
+    wT = torch.empty(rows * cols, dtype=torch.float32, device="cuda")
+    st_t = dev(st0) if opt != "sgd" else None
+    S.sprint_apply_update_t(opt, dev(w), out_t, wT, st_t, dbufs, rows, cols, eta, hp, n_total=n, weight_decay=wd)
+    assert np.array_equal(host(out_t), host(out))
+    assert np.array_equal(host(wT).reshape(cols, rows), host(out)[:rows * cols].reshape(rows, cols).T)
+    if opt != "sgd":
+        assert np.array_equal(host(st_t), host(st))
+
+
 def test_update_in_place_and_order_invariance_exact(S):
     n, k = 4099, 8
     w = synth.dyadic(2, "w", n)

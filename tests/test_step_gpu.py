@@ -103,7 +103,8 @@ def _check_step_local(arch, run, kw):
     gl, hist, states, batches, gbufs, saves = run
     steps = len(gl)
     R, sched, okw = _oracle_kw(kw, steps)
-    opt = dict(optimizer=okw.pop("optimizer", "sgd"), eta=okw.pop("eta", 0.01))
+    opt = dict(optimizer=okw.pop("optimizer", "sgd"), eta=okw.pop("eta", 0.01),
+               weight_decay=okw.pop("weight_decay", 0.0))
     layers = O.build_layers(arch)
     offs, _ = O.param_offsets(layers)
     worst = dict(fwd=0.0, loss=0.0, loss_free=0.0, grad=0.0, update=0.0)
@@ -212,6 +213,62 @@ def test_vgg_i_asgd_eight_replicas_small():
     _check_step_local(VGG_I_SMALL, _run_gpu(VGG_I_SMALL, 4, 5, 16, 3, kw), kw)
 
 
+def test_nesterov_weight_decay():
+    """Tiny CNN, batch 8: SGD with Nesterov momentum 0.9 and weight decay 0.004 (the
+    pipelined-training page's appendix hyper-parameters), step-local."""
+    kw = dict(optimizer="nesterov", eta=0.01, weight_decay=0.004)
+    _check_step_local(TINY, _run_gpu(TINY, 8, 8, 6, 3, kw), kw)
+
+
+def test_hybrid_pipeline_switch_and_stale_metrics():
+    """VGG-16 (channels halved), 4 stages delayed 3,2,1,0 for steps 0..4, then
+    non-pipelined (hybrid training, Sec. 4.2), step-local; the stale-weight
+    metrics before and after the switch."""
+    from stale_weight_sgd_gb300.model import VGG_C_STAGES
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+    kw = dict(optimizer="momentum", eta=0.01, stage_of_layer=VGG_C_STAGES, stage_delays=[3, 2, 1, 0],
+              hybrid_switch=5)
+    _check_step_local(VGG_C_HALF, _run_gpu(VGG_C_HALF, 4, 8, 6, 3, kw), kw)
+    tr = StaleSGD(_product_net(VGG_C_HALF), 4, **kw)
+    layers = O.build_layers(VGG_C_HALF)
+    m0, m5 = tr.staleness(0), tr.staleness(5)
+    assert m0["degrees"] == [3, 2, 1, 0] and m5["degrees"] == [0, 0, 0, 0]
+    assert m0["stale_weight_percent"] == pytest.approx(O.stale_weight_percent(layers, VGG_C_STAGES, [3, 2, 1, 0]),
+                                                       rel=1e-12)
+    assert m5["stale_weight_percent"] == 0.0
+
+
+def test_fetch_push_against_oracle():
+    """DistBelief n_fetch = 2, n_push = 3, 2 replicas (SMLPs topology, units reduced):
+    the per-step loss along the oracle's fetch/push trajectory; every server update is
+    the oracle's update of the GPU's accumulated GradBufs; steps without a push leave
+    the server's weights unchanged."""
+    from stale_weight_sgd_gb300.model import layer_shapes, unpack
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+    arch, batch, steps, R = SMLPS_SMALL, 32, 9, 2
+    w0 = _dense_init(arch, 31)
+    batches = _batches(arch, 6, batch, 32)
+    tr = StaleSGD(_product_net(arch), batch, replicas=R, n_fetch=2, n_push=3, eta=0.002)
+    tr.load_weights(w0)
+    tr.load_batches(batches)
+    shapes = layer_shapes(_product_net(arch))
+    gl, ws = [], [w0.astype(np.float64)]
+    for t in range(steps):
+        tr.step()
+        gl.append(tr.step_loss())
+        if (t + 1) % 3 == 0:
+            bufs = [unpack(shapes, tr.gradbuf[r].cpu().numpy()).astype(np.float64) for r in range(R)]
+            w_new = tr.weights().astype(np.float64)
+            assert rel_inf(w_new, O.update_sgd(ws[-1], bufs, 0.002)) <= TOL_UPDATE, t
+            ws.append(w_new)
+        else:
+            assert (tr.weights() == ws[-1].astype(np.float32)).all(), t
+    ol, wo, vo = O.train_fetch_push(arch, w0, batches, steps, replicas=R, n_fetch=2, n_push=3, eta=0.002)
+    assert len(vo) == len(ws) == 4
+    rel = np.abs(np.array(gl) - np.array(ol)) / np.abs(np.array(ol))
+    assert rel.max() <= TOL_LOSS, rel
+
+
 def test_adagrad_asgd():
     kw = dict(replicas=2, max_delay=2, schedule_seed=2, optimizer="adagrad", eta=0.01)
     _check_step_local(SMLPS_SMALL, _run_gpu(SMLPS_SMALL, 32, 10, 6, 3, kw), kw)
@@ -255,7 +312,9 @@ def test_zero_delays_bitwise_equal_plain_sgd():
 @pytest.mark.parametrize("arch,batch,kw", [
     (TINY, 8, dict(optimizer="sgd", eta=0.01)),
     (VGG_C_HALF, 4, dict(optimizer="momentum", eta=0.01, stage_delays=[3, 2, 1, 0])),
-], ids=["tiny", "vgg_c_pipeline"])
+    (VGG_C_HALF, 4, dict(optimizer="nesterov", eta=0.001, weight_decay=5e-4, stage_delays=[3, 2, 1, 0],
+                         hybrid_switch=5)),
+], ids=["tiny", "vgg_c_pipeline", "vgg_c_hybrid_nesterov"])
 def test_graph_replay_matches_eager_bitwise(arch, batch, kw):
     """Periodic schedules replay captured CUDA graphs of the step; the same
     kernels in the same order: weights, losses and optimizer state bitwise equal
@@ -280,6 +339,7 @@ def test_graph_replay_matches_eager_bitwise(arch, batch, kw):
         out.append((tr.weights(), np.array(losses), state, len(tr._graphs)))
     (w_e, l_e, s_e, n_e), (w_g, l_g, s_g, n_g) = out
     assert n_e == 0 and n_g >= 1          # the second run did replay graphs
+    assert np.isfinite(l_e).all()
     assert np.array_equal(w_e, w_g)
     assert np.array_equal(l_e, l_g)
     if s_e is not None:
