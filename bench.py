@@ -46,6 +46,16 @@ CONFIGS = {
                   desc="VGG-16 CIFAR-shaped fp32, batch 128, momentum 0.9, 4 pipeline stages s_k=3,2,1,0"),
     "vgg_i": dict(net="vgg_i", batch=64, replicas=8, max_delay=7, optimizer="sgd", eta=0.005,
                   desc="VGG-16 ILSVRC-shaped fp32, batch 64/replica, ASGD 8 replicas, delays {0..7}, SGD eta=0.005"),
+    # the widened rows: hybrid pipelined -> non-pipelined training with Nesterov momentum and
+    # weight decay, and DistBelief n_fetch / n_push
+    "vgg_c_hybrid": dict(net="vgg_c", batch=128, replicas=1, max_delay=0, optimizer="nesterov", eta=0.01,
+                         weight_decay=5e-4, stage_delays=[3, 2, 1, 0], hybrid_switch=12,
+                         desc="VGG-16 CIFAR-shaped fp32, batch 128, Nesterov 0.9 + weight decay 5e-4, 4 pipeline "
+                              "stages s_k=3,2,1,0 switched to non-pipelined at step 12 (hybrid)"),
+    "smlps_fetch_push": dict(net="smlps", batch=512, replicas=4, max_delay=0, optimizer="adagrad", eta=0.001,
+                             n_fetch=3, n_push=2,
+                             desc="SMLPs MLP 3072-5000x5-10 fp32, batch 512/replica, 4 replicas, DistBelief "
+                                  "n_fetch=3 / n_push=2, Adagrad eta=0.001"),
 }
 
 
@@ -181,10 +191,13 @@ def run_ours(args, cfg, rank, world, local_rank):
     feat = c * h * w
     classes = shapes[-1].cout
     P = max(2 * R, 8)
-    kw = dict(replicas=R, max_delay=cfg["max_delay"], schedule_seed=1234, optimizer=cfg["optimizer"], eta=cfg["eta"])
+    kw = dict(replicas=R, max_delay=cfg["max_delay"], schedule_seed=1234, optimizer=cfg["optimizer"], eta=cfg["eta"],
+              weight_decay=cfg.get("weight_decay", 0.0))
     if "stage_delays" in cfg:
         kw = dict(stage_of_layer=model.VGG_C_STAGES, stage_delays=cfg["stage_delays"], optimizer=cfg["optimizer"],
-                  eta=cfg["eta"])
+                  eta=cfg["eta"], weight_decay=cfg.get("weight_decay", 0.0), hybrid_switch=cfg.get("hybrid_switch"))
+    if "n_fetch" in cfg:
+        kw.update(max_delay=0, n_fetch=cfg["n_fetch"], n_push=cfg["n_push"])
     tr = StaleSGD(net, N, concurrent=not args.serial, **kw)
     # synthetic data generated on the device (seeded), weights He-normal
     g = torch.Generator(device=dev)
@@ -297,7 +310,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) inputs, uniform labels, He-normal init)",
         "config": {"workload": cfg["desc"], "global_batch": R * N * world, "replicas_per_gpu": R,
                    "parallelism": f"replicas only x{world}" if world > 1 else "1 GPU",
-                   "l2": "working set (weights, 4 GradBufs) far larger than L2; no flush needed"},
+                   "l2": "working set (weights, 4 GradBufs) far larger than L2; no flush needed",
+                   **({"staleness_first_step": tr.staleness(0), "staleness_last_step": tr.staleness(tr.t - 1)}
+                      if tr.pipeline else {})},
         "e2e": {"value": round(e2e_value, 1), "unit": "images/s",
                 "h2d_bytes_per_step": int(hx.numel() * 4 + hy.numel() * 4),
                 "d2h_bytes_per_step": int(hloss[0].numel() * 4),
@@ -360,6 +375,8 @@ KERNELS = {
     "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
     "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
     "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
+    "update_nesterov_wd": "parameter-server Nesterov apply with weight decay, n = 16M, k = 4 buffers",
+    "update_t_sgd": "parameter-server SGD apply writing W' and W'^T, 5000 x 5000 (+ bias), k = 4 buffers",
 }
 
 
@@ -467,9 +484,21 @@ def run_kernel(args):
         if k == "update_sgd":
             fn = lambda i: S.sprint_apply_update_sgd(wv, wv, bufs, n, 0.01)
             work = (4.0 * kb + 8) * n
-        else:
+        elif k == "update_momentum":
             fn = lambda i: S.sprint_apply_update_momentum(wv, wv, st, bufs, n, 0.01, 0.9)
             work = (4.0 * kb + 16) * n
+        elif k == "update_nesterov_wd":
+            fn = lambda i: S.sprint_apply_update("nesterov", wv, wv, st, bufs, n, 0.01, 0.9, 5e-4)
+            work = (4.0 * kb + 16) * n
+        else:   # update_t_sgd: reads k buffers and W, writes W' and W'^T
+            rows, cols = 5000, 5000
+            n = rows * cols + rows
+            wv = rnd(n, std=0.01)
+            bufs = [rnd(n, std=1e-3) for _ in range(kb)]
+            wo = torch.empty(n, device="cuda")
+            wT = torch.empty(rows * cols, device="cuda")
+            fn = lambda i: S.sprint_apply_update_t("sgd", wv, wo, wT, None, bufs, rows, cols, 0.01, n_total=n)
+            work = (4.0 * kb + 8) * n + 4.0 * rows * cols
         unit = "GB/s"
     for i in range(args.warmup):
         fn(i)

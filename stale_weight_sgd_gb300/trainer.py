@@ -397,12 +397,17 @@ class StaleSGD:
         if not self.use_graphs:
             return 0
         P = self.batches_x.shape[0]
-        period = np.lcm.reduce([self.S + 1, 2, P // np.gcd(P, self.R) if P else 1])
+        period = int(np.lcm.reduce([self.S + 1, 2, P // np.gcd(P, self.R) if P else 1]))
         t0 = max(self.t, self.S)
-        for t in range(t0, t0 + int(period)):
-            key = self._graph_key(t)
-            if key not in self._graphs:
-                self._capture(t, key)
+        starts = [t0]
+        if self.hybrid_switch is not None and self.hybrid_switch + self.S > t0:
+            # the steps around and after the switch to non-pipelined training recur too
+            starts.append(max(t0, self.hybrid_switch))
+        for a in starts:
+            for t in range(a, a + period + self.S):
+                key = self._graph_key(t)
+                if key not in self._graphs:
+                    self._capture(t, key)
         return len(self._graphs)
 
     def step(self):
