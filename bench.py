@@ -561,6 +561,113 @@ def allreduce_max(v, world):
     return float(t.item())
 
 
+def run_cost_model(args):
+    """Refits the SPRINT report's SGEMM cost model (Eq. (6), per role) to this
+    library's calls on one GPU and checks its prediction of a replica's
+    forward + backward time (Eq. (4)); evaluates Eq. (9) / (10) for the
+    SMLPs workload with the measured update time. Prints one JSON line."""
+    import torch
+
+    from stale_weight_sgd_gb300 import costmodel as C
+    from stale_weight_sgd_gb300 import model
+    from stale_weight_sgd_gb300 import sprint as S
+    S.lib()
+    torch.cuda.set_device(0)
+    st = torch.cuda.Stream()
+    torch.cuda.set_stream(st)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    rnd = lambda *shape, std=1.0: torch.randn(shape, generator=g, device="cuda") * std
+
+    def timed(fn, reps=8):
+        for _ in range(2):
+            fn()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        e.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(e) / reps / 1e3
+
+    samples = {r: [] for r in C.ROLES}
+    measured = {}   # (net, N) -> sum of the measured per-layer call times (a replica's forward + backward GEMMs)
+    sweeps = (("smlps", (64, 128, 256, 512, 1024)), ("vgg_c", (8, 16, 32, 64, 128)))
+    for name, Ns in sweeps:
+        shapes = model.layer_shapes(model.NETWORKS[name])
+        for N in Ns:
+            total = 0.0
+            for i, L in enumerate(shapes):
+                dims = C.role_dims(L, N, i == 0)
+                if L.kind == "fc":
+                    x, w, b = rnd(N, L.cin).relu_(), rnd(L.cout, L.cin, std=0.02), rnd(L.cout)
+                    wT, y, dy = w.t().contiguous(), torch.empty(N, L.cout, device="cuda"), rnd(N, L.cout)
+                    dx, dw, db = torch.empty(N, L.cin, device="cuda"), torch.empty_like(w), torch.empty_like(b)
+                    nb = S.sprint_fc_workspace_size(N, L.cin, L.cout, 1)
+                    ws = torch.empty(nb // 4 + 64, device="cuda")
+                    t_f = timed(lambda: S.sprint_fc_fwd(x, w, b, y, N, L.cin, L.cout, 1, st.cuda_stream))
+                    t_w = timed(lambda: S.sprint_fc_bwd(x, w, wT, dy, None, None, dw, db, 1.0, 0, N, L.cin, L.cout,
+                                                        ws, nb, st.cuda_stream))
+                    samples["fc"].append((*dims["fc"], t_f))
+                    samples["dedw"].append((*dims["dedw"], t_w))
+                    total += t_f + t_w
+                    if i > 0:
+                        t_b = timed(lambda: S.sprint_fc_bwd(x, w, wT, dy, x, dx, dw, db, 1.0, 0, N, L.cin, L.cout,
+                                                            ws, nb, st.cuda_stream))
+                        samples["dedx_fc"].append((*dims["dedx_fc"], max(t_b - t_w, 0.0)))
+                        total += max(t_b - t_w, 0.0)
+                else:
+                    x = rnd(N, L.h, L.w, L.cin).relu_()
+                    w, b = rnd(L.cout, 3, 3, L.cin, std=0.05), rnd(L.cout)
+                    wT = w.reshape(L.cout, -1).t().contiguous()
+                    y, dy = torch.empty(N, L.h, L.w, L.cout, device="cuda"), rnd(N, L.h, L.w, L.cout)
+                    dx, dw, db = torch.empty_like(x), torch.empty_like(w), torch.empty_like(b)
+                    nb = max(S.sprint_conv_workspace_size(op, N, L.h, L.w, L.cin, L.cout, 1)
+                             for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX, S.SPRINT_CONV_DW))
+                    ws = torch.empty(nb // 4 + 64, device="cuda")
+                    t_f = timed(lambda: S.sprint_conv_fwd(x, w, b, y, N, L.h, L.w, L.cin, L.cout, 1, 1, ws, nb,
+                                                          st.cuda_stream))
+                    t_w = timed(lambda: S.sprint_conv_dW(x, dy, dw, db, 1.0, 0, N, L.h, L.w, L.cin, L.cout, 1, ws, nb,
+                                                         st.cuda_stream))
+                    samples["convolution"].append((*dims["convolution"], t_f))
+                    samples["dedw"].append((*dims["dedw"], t_w))
+                    total += t_f + t_w
+                    if i > 0:
+                        t_x = timed(lambda: S.sprint_conv_dX(dy, w, wT, x, dx, N, L.h, L.w, L.cin, L.cout, 1, ws, nb,
+                                                             st.cuda_stream))
+                        samples["dedx_conv"].append((*dims["dedx_conv"], t_x))
+                        total += t_x
+            measured[(name, N)] = total
+    coefs = {r: C.fit_role(samples[r]) for r in C.ROLES}
+    fit = {}
+    for r in C.ROLES:
+        y = np.array([t for *_, t in samples[r]])
+        p = np.array([C.predict(coefs[r], m, n, k) for m, n, k, _ in samples[r]])
+        fit[r] = {"samples": len(y), "max_rel_err": round(float(np.max(np.abs(p - y) / y)), 4),
+                  "r2": round(float(1 - np.sum((p - y) ** 2) / np.sum((y - y.mean()) ** 2)), 5),
+                  "coef": [float(f"{c:.4e}") for c in coefs[r]]}
+    pred = {}
+    for (name, N), t in measured.items():
+        tp = C.predict_t_gpu(model.layer_shapes(model.NETWORKS[name]), N, coefs)
+        pred[f"{name}@{N}"] = {"measured_ms": round(t * 1e3, 4), "predicted_ms": round(tp * 1e3, 4),
+                               "rel_err": round(abs(tp - t) / t, 4)}
+    # Eq. (9) / (10) for the SMLPs workload: 4 replicas on one GPU (N_Node = 1, N_GPU = 4),
+    # N_Subbatch = 512, T_GPU from the model, T_Update = the measured update of all layers
+    shapes = model.layer_shapes(model.NETWORKS["smlps"])
+    n = model.padded_size(shapes)
+    wv = rnd(n, std=0.01)
+    bufs = [rnd(n, std=1e-3) for _ in range(4)]
+    t_update = timed(lambda: S.sprint_apply_update_sgd(wv, wv, bufs, n, 0.01, st.cuda_stream))
+    t_gpu = C.predict_t_gpu(shapes, 512, coefs)
+    nmb = C.n_minibatch_avg(1, 4, 512, t_update, t_gpu)
+    out = {"cost_model": "SPRINT Eq. (6) per SGEMM role, refitted on this GPU", "fit": fit, "t_gpu": pred,
+           "smlps_eq9": {"t_update_ms": round(t_update * 1e3, 4), "t_gpu_ms": round(t_gpu * 1e3, 4),
+                         "n_minibatch_avg": round(nmb, 2),
+                         "t_epoch_s_cifar10": round(C.t_epoch(50000, t_update, nmb), 4)}}
+    print(json.dumps(out))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,9 +680,13 @@ def main(argv=None):
                     help="issue everything on one stream (no update overlap, no side-by-side replica convolutions)")
     ap.add_argument("--kernel", choices=sorted(KERNELS), default=None,
                     help="time one hot kernel at a workload shape instead of the training step")
+    ap.add_argument("--cost-model", action="store_true",
+                    help="refit the SPRINT report's SGEMM cost model to this GPU and check its T_GPU prediction")
     args = ap.parse_args(argv)
     if args.kernel:
         return run_kernel(args)
+    if args.cost_model:
+        return run_cost_model(args)
     cfg = CONFIGS[args.config]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
