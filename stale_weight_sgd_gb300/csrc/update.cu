@@ -91,6 +91,12 @@ __global__ void __launch_bounds__(kThreads) gradbuf_kernel(float* buf, const flo
 // group of 4 of its rows (every warp access a 512-byte row segment); W' goes
 // through shared memory and leaves as 32-float runs of W'^T rows. VEC: cols %
 // 4 == 0 and 16-byte aligned pointers (float4 accesses), else scalar ones.
+// The tile size also sets how the update shares the GPU with the tensor-core
+// GEMMs it overlaps on another stream: with 16.5 KB of shared memory exactly one
+// block fits beside a 256-wide pair GEMM CTA (~210 KB). Measured on the SMLPs
+// step: no block beside a GEMM CTA (padded tile) 729k images/s, one 767k, two
+// or more (32 x 32 tiles) 732k — more co-resident update blocks slow the GEMMs
+// more than they gain, none leaves the update to the gaps between GEMMs.
 constexpr int kUtRows = 32, kUtCols = 128;
 
 template <int OPT, int K, bool VEC>
