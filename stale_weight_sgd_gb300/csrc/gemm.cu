@@ -19,6 +19,9 @@ int colsum_chunks(long long rows, int cols);
 int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
                      long long dc, cudaStream_t s);
 int launch_transpose_group(const float* const* src, float* const* dst, int G, int R, int C, cudaStream_t s);
+int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr,
+                            long long db, long long dc, float* partial, float* out, float alpha, int accumulate,
+                            cudaStream_t s);
 int launch_colsum_group(const float* const* in, float* const* out, int G, long long rows, int cols, float alpha,
                         int accumulate, cudaStream_t s);
 
@@ -1089,11 +1092,14 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         return pl;
     }
     // dedw
-    const int chunks = colsum_chunks(P, Cout);
-    pl.ws_colsum = chunks > 1 ? fbytes(static_cast<long long>(chunks) * Cout) : 0;
     // x^T puts channels outermost, so any Cin works; outputs with Cin % 4 != 0
     // are written with direct stores
     pl.tc = (N % 4 == 0) && (Cout % 4 == 0) && Cout >= 16;
+    // dedb: partial column sums of the dy transpose (one per pixel and 32-image
+    // tile and channel) on the tensor-core path, else chunks of colsum
+    const int chunks = colsum_chunks(P, Cout);
+    pl.ws_colsum = pl.tc ? fbytes(static_cast<long long>(Cout) * Ho * Wo * ((N + 31) / 32))
+                         : (chunks > 1 ? fbytes(static_cast<long long>(chunks) * Cout) : 0);
     if (!pl.tc) {
         const long long nchunk = (P + kDwChunk - 1) / kDwChunk;
         pl.ws_partial = fbytes(nchunk * Cout * 9 * Cin);
@@ -1882,15 +1888,22 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
     float* dyT = reinterpret_cast<float*>(wsb + pl.ws_xT);
     float* part = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT);
     float* csum = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT + pl.ws_partial);
-    bool done = false;
+    bool done = false, db_done = false;
     if (pl.tc) {
         // x [N][H][W][Cin] -> x^T [Cin][H][W][N]; dy likewise (batch innermost, pixels = k)
         if ((rc = launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin, N,
                                    static_cast<long long>(H) * W * N, s)))
             return rc;
-        if ((rc = launch_transpose(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout, N,
-                                   static_cast<long long>(Ho) * Wo * N, s)))
+        // dy -> dy^T, with dedb from the same pass when asked for
+        if (db) {
+            if ((rc = launch_transpose_colsum(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout,
+                                              N, static_cast<long long>(Ho) * Wo * N, csum, db, alpha, accumulate, s)))
+                return rc;
+            db_done = true;
+        } else if ((rc = launch_transpose(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout, N,
+                                          static_cast<long long>(Ho) * Wo * N, s))) {
             return rc;
+        }
         CUtensorMap ta, tb;
         const uint64_t da[3] = {(uint64_t)Wo * N, (uint64_t)Ho, (uint64_t)Cout};
         const uint64_t sa[2] = {(uint64_t)Wo * N * 4, (uint64_t)Ho * Wo * N * 4};
@@ -1981,6 +1994,6 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         colsum_finish_k<<<(O + 255) / 256, 256, 0, s>>>(part, nchunk, O, dw, alpha, accumulate);
         if ((rc = check_launch("colsum_finish_k"))) return rc;
     }
-    if (db) return launch_colsum(dy, P, Cout, pl.ws_colsum ? csum : nullptr, db, alpha, accumulate, s);
+    if (db && !db_done) return launch_colsum(dy, P, Cout, pl.ws_colsum ? csum : nullptr, db, alpha, accumulate, s);
     return SPRINT_OK;
 }

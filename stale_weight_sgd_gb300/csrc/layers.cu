@@ -159,6 +159,71 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
     return check_launch("transpose_kernel");
 }
 
+// transpose_kernel plus the column sums the dedb role needs from the same
+// tile: after the transpose, the block's 32 rows (images) of each of its 32
+// columns (channels) are added in row order into partial[c * nparts + part],
+// part = batch index * row tiles + row tile; colsum_parts_finish then adds a
+// channel's parts in part order. One read of dy serves both dy^T and dedb.
+__global__ void __launch_bounds__(256) transpose_colsum_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                               int R, int C, long long sb, long long sr, long long db,
+                                                               long long dc, float* __restrict__ partial,
+                                                               long long nparts) {
+    __shared__ float tile[32][33];
+    const long long b = blockIdx.z;
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int r = r0 + j, c = c0 + tx;
+        tile[j][tx] = (r < R && c < C) ? src[b * sb + static_cast<long long>(r) * sr + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = ty; j < 32; j += 8) {
+        const int c = c0 + j, r = r0 + tx;
+        if (r < R && c < C) dst[b * db + static_cast<long long>(c) * dc + r] = tile[tx][j];
+    }
+    if (ty == 0 && c0 + tx < C) {
+        float t = 0.f;
+        for (int j = 0; j < 32; ++j) t += tile[j][tx];
+        partial[static_cast<long long>(c0 + tx) * nparts + b * gridDim.y + blockIdx.y] = t;
+    }
+}
+
+// out[c] = (accumulate ? out[c] : 0) + alpha * sum over the nparts parts of
+// channel c, added as 256 thread stripes (part = t, t + 256, ...) and then a
+// fixed pairwise tree: the same order on every run.
+__global__ void __launch_bounds__(256) colsum_parts_finish(const float* __restrict__ partial, long long nparts,
+                                                           float* __restrict__ out, float alpha, int accumulate) {
+    __shared__ float red[256];
+    const int c = blockIdx.x;
+    const float* p = partial + static_cast<long long>(c) * nparts;
+    float t = 0.f;
+    for (long long k = threadIdx.x; k < nparts; k += 256) t += p[k];
+    red[threadIdx.x] = t;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[c] = (accumulate ? out[c] : 0.f) + alpha * red[0];
+}
+
+// dst = src transposed as launch_transpose does, and out = dedb of src's columns
+// (partial: C * batch * ceil(R / 32) floats of workspace)
+int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr,
+                            long long db, long long dc, float* partial, float* out, float alpha, int accumulate,
+                            cudaStream_t s) {
+    if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
+    if (batch > 65535 || (R + 31) / 32 > 65535)
+        return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
+    const long long nparts = static_cast<long long>(batch) * ((R + 31) / 32);
+    dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
+    transpose_colsum_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, partial, nparts);
+    colsum_parts_finish<<<C, 256, 0, s>>>(partial, nparts, out, alpha, accumulate);
+    return check_launch("transpose_colsum", 2);
+}
+
 // One launch over up to kMaxGroup problems (blockIdx.z = problem g):
 // out[g] = in[g]^T, in[g] being R x C row-major.
 struct GroupPtrs {
