@@ -259,19 +259,29 @@ GemmPlan plan_gemm(long long m_tiles, long long n, long long z, int max_bn, int 
             double rounds = static_cast<double>(full);
             long long sp = 1;
             if (r > 0) {
-                sp = allow_tail ? slots / r : 1;
-                if (sp > num_kt / 4) sp = num_kt / 4;
-                if (sp >= 2) {
-                    // equal k-ranges of ceil(num_kt / sp) k-tiles: no range may be empty
-                    const long long kt = (num_kt + sp - 1) / sp;
-                    sp = (num_kt + kt - 1) / kt;
+                // the last round whole, or cut into s k-ranges plus the slab reduction, whose
+                // time (measured: ~4 us plus its slabs' traffic at ~4 TB/s) is counted in units
+                // of one unit's MMA time (~0.34 us per k-tile of a 256 x 256 pair tile at full
+                // rate, scaled by width / efficiency like the cost below)
+                const double e = pair ? eff_pair[i] : eff[i];
+                const double unit_us = static_cast<double>(num_kt) * 0.34 * (bn / 256.0) / e;
+                const double tile_bytes = (pair ? 256.0 : 128.0) * bn * 4.0;
+                double best_tail = 1.0;
+                long long smax = allow_tail ? slots / r : 1;
+                if (smax > num_kt / 4) smax = num_kt / 4;
+                for (long long c = 2; c <= smax; ++c) {
+                    // equal k-ranges of ceil(num_kt / c) k-tiles: no range may be empty
+                    const long long kt = (num_kt + c - 1) / c;
+                    const long long cs = (num_kt + kt - 1) / kt;
+                    if (cs < 2) continue;
+                    const double reduce_us = 4.0 + static_cast<double>(r) * cs * tile_bytes / 4e6;
+                    const double tail = 1.0 / static_cast<double>(cs) + reduce_us / unit_us;
+                    if (tail < best_tail - 1e-9) {
+                        best_tail = tail;
+                        sp = cs;
+                    }
                 }
-                if (sp >= 2)
-                    rounds += 1.0 / static_cast<double>(sp) + 0.03;   // + the slab reduction
-                else {
-                    sp = 1;
-                    rounds += 1.0;
-                }
+                rounds += best_tail;
             }
             const double cost = rounds * bn / (pair ? eff_pair[i] : eff[i]);
             if (cost < best_cost - 1e-9) {
