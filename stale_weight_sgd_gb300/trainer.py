@@ -51,6 +51,20 @@ from . import sprint as S
 from .model import layer_shapes, pack, padded_size, stale_weight_percent, staleness_degrees, unpack
 
 
+def fetch_push_version(t, n_fetch, n_push):
+    """DistBelief n_fetch / n_push: the server version (count of updates applied)
+    a replica computes on at step t — the one of its last fetch step, t rounded
+    down to a multiple of n_fetch; updates end steps n_push - 1, 2 n_push - 1, ..."""
+    return (t // n_fetch * n_fetch) // n_push
+
+
+def fetch_push_max_lag(n_fetch, n_push):
+    """A bound on how many server updates a replica's copy can be behind the
+    newest version (the versions of steps f .. f + n_fetch - 1 differ by at most
+    this; not always reached)."""
+    return (n_fetch - 1) // n_push + 1
+
+
 class StaleSGD:
     def __init__(self, net, batch, *, replicas=1, max_delay=0, schedule_seed=0, stage_of_layer=None,
                  stage_delays=None, hybrid_switch=None, n_fetch=None, n_push=None, optimizer="sgd", eta=0.01,
@@ -89,7 +103,7 @@ class StaleSGD:
             self.n_fetch, self.n_push = int(n_fetch or 1), int(n_push or 1)
             assert self.n_fetch >= 1 and self.n_push >= 1
             # versions count server updates: at most D behind the current one
-            self.S = (self.n_fetch - 1) // self.n_push + 1
+            self.S = fetch_push_max_lag(self.n_fetch, self.n_push)
         else:
             assert self.hybrid_switch is None
             self.S = int(max_delay)
@@ -313,7 +327,7 @@ class StaleSGD:
         if self.pipeline:
             return max(0, t - self._stage_delay(self.stage_of_layer[layer], t))
         if self.fetch_push:   # the server's version at the replica's last fetch step
-            return (t // self.n_fetch * self.n_fetch) // self.n_push
+            return fetch_push_version(t, self.n_fetch, self.n_push)
         s = int(self.schedule(t + 1)[t, r]) if self.S > 0 else 0
         return max(0, t - s)
 

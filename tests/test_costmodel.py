@@ -50,3 +50,21 @@ def test_minibatch_average_and_epoch_time():
     assert C.t_epoch(1281167, 0.2, nmb) == pytest.approx(1281167 * 0.2 / 96.0, rel=1e-15)
     # one GPU that updates after every step of its own: N_Minibatch_avg = N_Subbatch
     assert C.n_minibatch_avg(1, 1, 128, 0.3, 0.3) == pytest.approx(128.0)
+
+
+# ---- DistBelief n_fetch / n_push version arithmetic of the trainer (host logic)
+
+@pytest.mark.parametrize("n_fetch,n_push", [(1, 1), (2, 1), (1, 3), (3, 2), (5, 2), (4, 4), (7, 3)])
+def test_fetch_push_versions_match_a_step_by_step_server(n_fetch, n_push):
+    # brute force: run the server step by step, count its updates, snapshot at fetch steps
+    from stale_weight_sgd_gb300.trainer import fetch_push_max_lag, fetch_push_version
+    updates, fetched, worst = 0, None, 0
+    for t in range(60):
+        if t % n_fetch == 0:
+            fetched = updates
+        assert fetch_push_version(t, n_fetch, n_push) == fetched, t
+        worst = max(worst, updates - fetched)
+        if (t + 1) % n_push == 0:
+            updates += 1
+    # the ring (max_lag + 2 slots: the versions read plus the one being written) is enough
+    assert worst <= fetch_push_max_lag(n_fetch, n_push)
