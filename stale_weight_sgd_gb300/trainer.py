@@ -93,19 +93,29 @@ class StaleSGD:
         self.fetch_push = n_fetch is not None or n_push is not None
         self.hybrid_switch = None if hybrid_switch is None else int(hybrid_switch)
         if self.pipeline:
-            assert stage_of_layer is not None and len(stage_of_layer) == len(self.shapes)
-            assert not self.fetch_push and max_delay == 0
+            if stage_of_layer is None or len(stage_of_layer) != len(self.shapes):
+                raise ValueError("stage_delays needs stage_of_layer with one stage per layer")
+            if self.fetch_push or max_delay:
+                raise ValueError("pipeline stage delays exclude max_delay and n_fetch / n_push")
             self.stage_of_layer = list(stage_of_layer)
             self.stage_delays = [int(s) for s in stage_delays]
+            if min(self.stage_delays) < 0 or max(self.stage_of_layer) >= len(self.stage_delays):
+                raise ValueError("stage delays must be >= 0 and cover every stage of stage_of_layer")
             self.S = max(self.stage_delays)
         elif self.fetch_push:
-            assert max_delay == 0 and self.hybrid_switch is None
-            self.n_fetch, self.n_push = int(n_fetch or 1), int(n_push or 1)
-            assert self.n_fetch >= 1 and self.n_push >= 1
+            if max_delay or self.hybrid_switch is not None:
+                raise ValueError("n_fetch / n_push exclude max_delay and hybrid_switch")
+            self.n_fetch = 1 if n_fetch is None else int(n_fetch)
+            self.n_push = 1 if n_push is None else int(n_push)
+            if self.n_fetch < 1 or self.n_push < 1:
+                raise ValueError("n_fetch and n_push must be >= 1")
             # versions count server updates: at most D behind the current one
             self.S = fetch_push_max_lag(self.n_fetch, self.n_push)
         else:
-            assert self.hybrid_switch is None
+            if self.hybrid_switch is not None:
+                raise ValueError("hybrid_switch needs pipeline stage delays")
+            if max_delay < 0:
+                raise ValueError("max_delay must be >= 0")
             self.S = int(max_delay)
         self.RS = self.S + 2 if self.fetch_push else self.S + 1   # weight-version ring slots
         self.seed = int(schedule_seed)
@@ -283,7 +293,8 @@ class StaleSGD:
         "Pipelined training of deep CNNs with stale weights" Sec. 4.1: the degree
         of staleness of every stage pair (the steps its weights lag) and the
         percentage of the parameters held by stages with stale weights."""
-        assert self.pipeline
+        if not self.pipeline:
+            raise ValueError("staleness metrics are defined for pipeline stages")
         t = self.t if t is None else t
         delays = [self._stage_delay(k, t) for k in range(len(self.stage_delays))]
         return dict(degrees=staleness_degrees(delays),

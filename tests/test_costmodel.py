@@ -68,3 +68,18 @@ def test_fetch_push_versions_match_a_step_by_step_server(n_fetch, n_push):
             updates += 1
     # the ring (max_lag + 2 slots: the versions read plus the one being written) is enough
     assert worst <= fetch_push_max_lag(n_fetch, n_push)
+
+
+def test_trainer_rejects_inconsistent_schedules_before_touching_the_gpu():
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+    net = dict(input=(12, 1, 1), classes=4, layers=[("fc", 9, True), ("fc", 4, False)])
+    bad = [dict(stage_delays=[1, 0]),                                          # no stage map
+           dict(stage_delays=[1], stage_of_layer=[0, 1]),                      # stage without a delay
+           dict(stage_delays=[1, 0], stage_of_layer=[0, 1], max_delay=2),      # two delay models
+           dict(n_fetch=2, max_delay=1),
+           dict(n_fetch=0, n_push=1),
+           dict(hybrid_switch=3),                                              # hybrid without a pipeline
+           dict(max_delay=-1)]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            StaleSGD(net, 8, **kw)
