@@ -373,6 +373,8 @@ KERNELS = {
                       "x^T + ones row, dy^T given and dx^T written, as in the step",
     "conv_dw_224x64": "conv weight gradient, VGG conv1_2 shape 224x224x64->64, batch 16",
     "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
+    "conv_dw_224x3": "conv weight gradient + bias gradient, VGG conv1_1 shape 224x224x3->64, batch 16 "
+                     "(direct CUDA-core kernel)",
     "update_sgd": "parameter-server SGD apply, n = 16M, k = 16 buffers",
     "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
     "update_nesterov_wd": "parameter-server Nesterov apply with weight decay, n = 16M, k = 4 buffers",
@@ -438,7 +440,7 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
             work, unit = 4.0 * M * N * K, "TFLOP/s"
-    elif k in ("conv_dw_224x64", "conv_fwd_224x3"):
+    elif k in ("conv_dw_224x64", "conv_fwd_224x3", "conv_dw_224x3"):
         Nb, H, W = 16, 224, 224
         Ci = 64 if k == "conv_dw_224x64" else 3
         Co = 64
@@ -452,7 +454,7 @@ def run_kernel(args):
         dwt = torch.empty(Co, 3, 3, Ci, device="cuda")
         dbt = torch.empty(Co, device="cuda")
         work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
-        if k == "conv_dw_224x64":
+        if k in ("conv_dw_224x64", "conv_dw_224x3"):
             fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
         else:
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)

@@ -888,6 +888,183 @@ int launch_conv_smallc(const float* x, const float* w, const float* b, float* y,
     return check_launch("conv_smallc_fwd_kernel");
 }
 
+// dedw and dedb of a layer with few input channels (the RGB layer) on the CUDA
+// cores. As a GEMM it is [Cout] x [9 * Cin] over a k of every output pixel: a
+// 27-wide product that would fill few tensor-core columns and need both
+// operands re-laid out first. Here one warp walks kSmallcDwSeg output pixels of
+// a row; lane l owns channels l * CPL .. l * CPL + CPL - 1. The 3 x 3 x CIN
+// input patch slides one column per pixel, so each pixel loads 3 * CIN new
+// inputs (one address for the whole warp) and CPL dy values per lane, and adds
+// CPL * (9 * CIN + 1) products (the +1: dedb). A block adds its warps' sums in
+// warp order in shared memory and writes one partial of Cout * (9 * CIN + 1)
+// floats ([co][tap][ci], then [co]); smallc_dw_finish adds the partials in
+// block order, so the result depends only on the grid.
+constexpr int kSmallcDwSeg = 16;
+constexpr int kSmallcDwWarps = 8;
+
+// resident blocks per SM (the widest variant holds 2 x 36 + 36 live values per thread)
+constexpr int smallc_dw_per_sm(int cin, int cpl) { return cin * cpl > 6 ? 1 : 2; }
+
+int smallc_dw_blocks(int N, int Ho, int Wo, int Cin, int Cout) {
+    const long long tasks = static_cast<long long>(N) * Ho * ((Wo + kSmallcDwSeg - 1) / kSmallcDwSeg);
+    long long g = (tasks + kSmallcDwWarps - 1) / kSmallcDwWarps;
+    const long long cap = static_cast<long long>(smallc_dw_per_sm(Cin, Cout > 32 ? 2 : 1)) * num_sms();
+    if (g > cap) g = cap;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <int CIN, int CPL>
+__global__ void __launch_bounds__(kSmallcDwWarps * 32, smallc_dw_per_sm(CIN, CPL))
+    conv_smallc_dw_kernel(const float* __restrict__ x, const float* __restrict__ dy, float* __restrict__ partial,
+                          int N, int H, int W, int Cout, int pad) {
+    constexpr int K = 9 * CIN;
+    constexpr int KC = 3 * CIN;   // one input column of the patch, [kh][ci]
+    __shared__ float red[32 * CPL * (K + 1)];
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const int segs = (Wo + kSmallcDwSeg - 1) / kSmallcDwSeg;
+    const long long tasks = static_cast<long long>(N) * Ho * segs;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int co0 = lane * CPL;
+    const bool live = co0 < Cout;
+    float acc[CPL][K], accb[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        accb[j] = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc[j][k] = 0.f;
+    }
+    for (long long task = static_cast<long long>(blockIdx.x) * kSmallcDwWarps + warp; task < tasks;
+         task += static_cast<long long>(gridDim.x) * kSmallcDwWarps) {
+        const int seg = static_cast<int>(task % segs);
+        const long long r = task / segs;   // n * Ho + oh
+        const int oh = static_cast<int>(r % Ho);
+        const long long n = r / Ho;
+        const int ow0 = seg * kSmallcDwSeg;
+        const float* xr[3];
+#pragma unroll
+        for (int kh = 0; kh < 3; ++kh) {
+            const int ih = oh + kh - pad;
+            xr[kh] = (ih >= 0 && ih < H) ? x + (n * H + ih) * static_cast<long long>(W) * CIN : nullptr;
+        }
+        float win[3][KC];   // patch columns kw = 0, 1, 2 of the current pixel
+        auto load_col = [&](float* c, int iw) {
+            const bool in_w = iw >= 0 && iw < W;
+#pragma unroll
+            for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci)
+                    c[kh * CIN + ci] = (in_w && xr[kh]) ? __ldg(xr[kh] + static_cast<long long>(iw) * CIN + ci) : 0.f;
+        };
+        load_col(win[0], ow0 - pad);
+        load_col(win[1], ow0 - pad + 1);
+        const float* dyr = dy + (r * Wo + ow0) * Cout + co0;
+#pragma unroll
+        for (int q = 0; q < kSmallcDwSeg; ++q) {
+            load_col(win[2], ow0 + q - pad + 2);
+            float g[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) g[j] = 0.f;
+            if (live && ow0 + q < Wo) {
+                if constexpr (CPL == 2) {
+                    const float2 v = __ldcs(reinterpret_cast<const float2*>(dyr + static_cast<long long>(q) * Cout));
+                    g[0] = v.x;
+                    g[1] = v.y;
+                } else {
+                    g[0] = __ldcs(dyr + static_cast<long long>(q) * Cout);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                accb[j] += g[j];
+#pragma unroll
+                for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+                    for (int kw = 0; kw < 3; ++kw)
+#pragma unroll
+                        for (int ci = 0; ci < CIN; ++ci)
+                            acc[j][(kh * 3 + kw) * CIN + ci] =
+                                fmaf(g[j], win[kw][kh * CIN + ci], acc[j][(kh * 3 + kw) * CIN + ci]);
+            }
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+                win[0][c] = win[1][c];
+                win[1][c] = win[2][c];
+            }
+        }
+    }
+    // the block's sum, warp by warp in warp order: red[co][0..K-1] products, red[co][K] dedb
+    for (int w = 0; w < kSmallcDwWarps; ++w) {
+        if (warp == w && live) {
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                float* rr = red + (co0 + j) * (K + 1);
+#pragma unroll
+                for (int k = 0; k < K; ++k) rr[k] = w == 0 ? acc[j][k] : rr[k] + acc[j][k];
+                rr[K] = w == 0 ? accb[j] : rr[K] + accb[j];
+            }
+        }
+        __syncthreads();
+    }
+    const int O = Cout * (K + 1);
+    float* part = partial + static_cast<long long>(blockIdx.x) * O;
+    for (int i = threadIdx.x; i < O; i += blockDim.x) {
+        const bool is_b = i >= Cout * K;
+        const int co = is_b ? i - Cout * K : i / K, k = is_b ? K : i % K;
+        part[i] = red[co * (K + 1) + k];
+    }
+}
+
+// dw[o] / db[o - Cout * K] = (accumulate ? old : 0) + alpha * (sum of the
+// blocks' partials of output o): 32 outputs per block, 8 block stripes, then
+// a fixed pairwise sum of the stripes
+__global__ void __launch_bounds__(256) smallc_dw_finish(const float* __restrict__ partial, int nblocks, int Cout, int K,
+                                                        float* __restrict__ dw, float* __restrict__ db, float alpha,
+                                                        int accumulate) {
+    __shared__ float red[8][33];
+    const int O = Cout * (K + 1);
+    const int lane = threadIdx.x & 31, st = threadIdx.x >> 5;
+    const int o = blockIdx.x * 32 + lane;
+    float t = 0.f;
+    if (o < O)
+        for (int b = st; b < nblocks; b += 8) t += partial[static_cast<long long>(b) * O + o];
+    red[st][lane] = t;
+    __syncthreads();
+    if (st != 0 || o >= O) return;
+    const float s = ((red[0][lane] + red[1][lane]) + (red[2][lane] + red[3][lane])) +
+                    ((red[4][lane] + red[5][lane]) + (red[6][lane] + red[7][lane]));
+    if (o < Cout * K) {
+        dw[o] = (accumulate ? dw[o] : 0.f) + alpha * s;
+    } else if (db) {
+        const int c = o - Cout * K;
+        db[c] = (accumulate ? db[c] : 0.f) + alpha * s;
+    }
+}
+
+// Cin <= 4 and Cout <= 64 (Cout even above 32); partial: smallc_dw_blocks() *
+// Cout * (9 * Cin + 1) floats
+int launch_conv_smallc_dw(const float* x, const float* dy, float* partial, float* dw, float* db, float alpha,
+                          int accumulate, int N, int H, int W, int Cin, int Cout, int pad, cudaStream_t s) {
+    const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const int grid = smallc_dw_blocks(N, Ho, Wo, Cin, Cout);
+    const int threads = kSmallcDwWarps * 32;
+    const int key = Cin * 2 + (Cout > 32 ? 1 : 0);
+    switch (key) {
+        case 2: conv_smallc_dw_kernel<1, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 3: conv_smallc_dw_kernel<1, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 4: conv_smallc_dw_kernel<2, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 5: conv_smallc_dw_kernel<2, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 6: conv_smallc_dw_kernel<3, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 7: conv_smallc_dw_kernel<3, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        case 8: conv_smallc_dw_kernel<4, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+        default: conv_smallc_dw_kernel<4, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+    }
+    int rc = check_launch("conv_smallc_dw_kernel");
+    if (rc) return rc;
+    const int K = 9 * Cin;
+    smallc_dw_finish<<<(Cout * (K + 1) + 31) / 32, 256, 0, s>>>(partial, grid, Cout, K, dw, db, alpha, accumulate);
+    return check_launch("smallc_dw_finish");
+}
+
 // direct convolution, one thread per output element (co fastest)
 __global__ void __launch_bounds__(256) simt_conv_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ b, float* __restrict__ y, int N,
@@ -1054,7 +1231,7 @@ FcPlan plan_fc(int N, int in, int out, bool have_wT) {
 struct ConvPlan {
     bool tc = false;
     bool im2col = false;    // forward through an explicit padded im2col + 2-D GEMM
-    bool smallc = false;    // forward with Cin <= 4: direct CUDA-core kernel (conv_smallc_fwd_kernel)
+    bool smallc = false;    // Cin <= 4: direct CUDA-core kernel (conv_smallc_fwd_kernel / conv_smallc_dw_kernel)
     int kp = 0;             // padded k of that im2col
     size_t ws_col = 0, ws_wpad = 0;
     Tile tile{};
@@ -1102,6 +1279,12 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         return pl;
     }
     // dedw
+    if (Cin <= 4 && Cout <= 64 && (Cout <= 32 || Cout % 2 == 0)) {
+        // the RGB layer: direct CUDA-core kernel, dedb in the same pass
+        pl.smallc = true;
+        pl.ws_partial = fbytes(static_cast<long long>(smallc_dw_blocks(N, Ho, Wo, Cin, Cout)) * Cout * (9 * Cin + 1));
+        return pl;
+    }
     // x^T puts channels outermost, so any Cin works; outputs with Cin % 4 != 0
     // are written with direct stores
     pl.tc = (N % 4 == 0) && (Cout % 4 == 0) && Cout >= 16;
@@ -1898,6 +2081,8 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
     float* dyT = reinterpret_cast<float*>(wsb + pl.ws_xT);
     float* part = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT);
     float* csum = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT + pl.ws_partial);
+    if (pl.smallc)
+        return launch_conv_smallc_dw(x, dy, part, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, s);
     bool done = false, db_done = false;
     if (pl.tc) {
         // x [N][H][W][Cin] -> x^T [Cin][H][W][N]; dy likewise (batch innermost, pixels = k)

@@ -502,6 +502,10 @@ CONV_CASES = [
     (8, 9, 7, 3, 16),       # RGB layer, ragged spatial size
     (3, 7, 6, 1, 16),       # one input channel: direct CUDA-core forward, zero-filled tap boxes in dW
     (4, 8, 5, 4, 32),       # four input channels: direct forward (4-wide patch), CUDA-core dX
+    (2, 37, 35, 3, 48),     # RGB dW: ragged 16-pixel row segments, two channels per lane with idle lanes
+    (3, 20, 40, 2, 64),     # RGB dW: two input channels, full warp of channel pairs
+    (2, 11, 9, 4, 64),      # RGB dW: the widest patch (4 channels) with channel pairs
+    (1, 6, 17, 1, 40),      # RGB dW: one input channel, Cout between 32 and 64
 ]
 
 
@@ -561,6 +565,40 @@ def test_conv_dw(S, N, H, W, Cin, Cout, accumulate):
     S.sprint_conv_dW(dev(x), dev(dy), dw, db, 1.0, accumulate, N, H, W, Cin, Cout, 1, ws, nb)
     assert rel_inf(host(dw), dw_ref) <= TOL_TF32
     assert rel_inf(host(db), db_ref) <= TOL_FP32
+    _status_clean(S)
+
+
+@pytest.mark.parametrize("Cin,Cout", [(3, 64), (1, 16), (4, 32)])
+def test_conv_dw_rgb_pad0(S, Cin, Cout):
+    N, H, W = 3, 9, 21
+    x, _, _ = _conv_inputs(15, N, H, W, Cin, Cout)
+    dy = _f32(15, "dy", (N, H - 2, W - 2, Cout))
+    dw_ref, db_ref = O.conv3x3_dw(x, dy, pad=0)
+    dw = torch.full((Cout, 3, 3, Cin), 7.0, dtype=torch.float32, device="cuda")
+    n = S.sprint_conv_workspace_size(S.SPRINT_CONV_DW, N, H, W, Cin, Cout, 0)
+    ws = torch.empty(max(n // 4, 1) + 64, dtype=torch.float32, device="cuda")
+    S.sprint_conv_dW(dev(x), dev(dy), dw, None, 0.5, 0, N, H, W, Cin, Cout, 0, ws, n)
+    assert rel_inf(host(dw), 0.5 * dw_ref) <= TOL_FP32
+    _status_clean(S)
+
+
+def test_conv_dw_vgg_conv1_1(S):
+    """The ILSVRC-shaped VGG first layer (224 x 224 x 3 -> 64) at batch 2:
+    every output against the oracle, and the same bits on a second call."""
+    N, H, W, Cin, Cout = 2, 224, 224, 3, 64
+    x, _, _ = _conv_inputs(16, N, H, W, Cin, Cout)
+    dy = _f32(16, "dy", (N, H, W, Cout))
+    dw_ref, db_ref = O.conv3x3_dw(x, dy)
+    dw = torch.empty((Cout, 3, 3, Cin), dtype=torch.float32, device="cuda")
+    db = torch.empty(Cout, dtype=torch.float32, device="cuda")
+    ws, nb = _ws(S, S.SPRINT_CONV_DW, N, H, W, Cin, Cout)
+    xd, dyd = dev(x), dev(dy)
+    S.sprint_conv_dW(xd, dyd, dw, db, 1.0, 0, N, H, W, Cin, Cout, 1, ws, nb)
+    assert rel_inf(host(dw), dw_ref) <= TOL_FP32
+    assert rel_inf(host(db), db_ref) <= TOL_FP32
+    dw1, db1 = dw.clone(), db.clone()
+    S.sprint_conv_dW(xd, dyd, dw, db, 1.0, 0, N, H, W, Cin, Cout, 1, ws, nb)
+    assert torch.equal(dw, dw1) and torch.equal(db, db1)
     _status_clean(S)
 
 
