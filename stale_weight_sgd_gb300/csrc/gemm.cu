@@ -891,16 +891,28 @@ int launch_conv_smallc(const float* x, const float* w, const float* b, float* y,
 // dedw and dedb of a layer with few input channels (the RGB layer) on the CUDA
 // cores. As a GEMM it is [Cout] x [9 * Cin] over a k of every output pixel: a
 // 27-wide product that would fill few tensor-core columns and need both
-// operands re-laid out first. Here one warp walks kSmallcDwSeg output pixels of
-// a row; lane l owns channels l * CPL .. l * CPL + CPL - 1. The 3 x 3 x CIN
-// input patch slides one column per pixel, so each pixel loads 3 * CIN new
-// inputs (one address for the whole warp) and CPL dy values per lane, and adds
+// operands re-laid out first. Here one warp takes a segment of kSmallcDwSeg
+// output pixels of a row at a time; lane l owns channels l * CPL ..
+// l * CPL + CPL - 1. The warp stages the segment's inputs (3 rows of
+// kSmallcDwSeg + 2 patch columns, channels padded to 4) and dy rows in its own
+// shared buffers with cp.async, one segment ahead of the one it computes (a
+// warp's segments are consecutive, so their coordinates advance without a
+// division). The 3 x 3 x CIN patch then slides one column per pixel: 3 shared
+// loads of a column (one address for the warp) and one of dy per pixel for
 // CPL * (9 * CIN + 1) products (the +1: dedb). A block adds its warps' sums in
 // warp order in shared memory and writes one partial of Cout * (9 * CIN + 1)
 // floats ([co][tap][ci], then [co]); smallc_dw_finish adds the partials in
 // block order, so the result depends only on the grid.
 constexpr int kSmallcDwSeg = 16;
 constexpr int kSmallcDwWarps = 8;
+constexpr int kSmallcDwCols = kSmallcDwSeg + 2;      // patch columns of one segment
+constexpr int kSmallcDwXs = 3 * kSmallcDwCols * 4;   // staged inputs: [kh][column][4]
+
+// floats of one stage buffer of one warp (inputs, then kSmallcDwSeg dy rows of up to 32 * CPL channels)
+constexpr int smallc_dw_stage_floats(int cpl) { return kSmallcDwXs + kSmallcDwSeg * 32 * cpl; }
+constexpr size_t smallc_dw_smem(int cpl) {
+    return sizeof(float) * 2 * kSmallcDwWarps * static_cast<size_t>(smallc_dw_stage_floats(cpl));
+}
 
 // resident blocks per SM (the widest variant holds 2 x 36 + 36 live values per thread)
 constexpr int smallc_dw_per_sm(int cin, int cpl) { return cin * cpl > 6 ? 1 : 2; }
@@ -913,19 +925,66 @@ int smallc_dw_blocks(int N, int Ho, int Wo, int Cin, int Cout) {
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int NPENDING>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(NPENDING) : "memory");
+}
+
+// One warp stages the segment at output row r = n * Ho + oh, columns ow0 ..
+// ow0 + kSmallcDwSeg - 1, into xs / ds: xs[(kh * cols + c) * 4 + ci] =
+// x[n][oh + kh - pad][ow0 - pad + c][ci] (0 outside the image), ds[q * Cout + co]
+// = dy[n][oh][ow0 + q][co] (0 past the row's end). A lane copies whole patch
+// cells (CIN contiguous floats).
+template <int CIN>
+__device__ __forceinline__ void smallc_dw_stage(float* xs, float* ds, const float* __restrict__ x,
+                                                const float* __restrict__ dy, int n, int oh, int r, int ow0, int H,
+                                                int W, int Wo, int Cout, int pad, int lane) {
+    for (int cell = lane; cell < 3 * kSmallcDwCols; cell += 32) {
+        const int kh = cell / kSmallcDwCols, c = cell - kh * kSmallcDwCols;
+        const int ih = oh + kh - pad, iw = ow0 - pad + c;
+        float* d = xs + cell * 4;
+        if (ih >= 0 && ih < H && iw >= 0 && iw < W) {
+            const float* src = x + ((static_cast<long long>(n) * H + ih) * W + iw) * CIN;
+#pragma unroll
+            for (int ci = 0; ci < CIN; ++ci) cp_async4(d + ci, src + ci);
+        } else {
+#pragma unroll
+            for (int ci = 0; ci < CIN; ++ci) d[ci] = 0.f;
+        }
+    }
+    const int nq = Wo - ow0 < kSmallcDwSeg ? Wo - ow0 : kSmallcDwSeg;
+    const float* src = dy + (static_cast<long long>(r) * Wo + ow0) * Cout;
+    const int cnt = nq * Cout;
+    if ((Cout & 3) == 0) {
+        for (int e = lane * 4; e < cnt; e += 128) cp_async16(ds + e, src + e);
+    } else {
+        for (int e = lane; e < cnt; e += 32) cp_async4(ds + e, src + e);
+    }
+    for (int e = cnt + lane; e < kSmallcDwSeg * Cout; e += 32) ds[e] = 0.f;
+}
+
 template <int CIN, int CPL>
 __global__ void __launch_bounds__(kSmallcDwWarps * 32, smallc_dw_per_sm(CIN, CPL))
     conv_smallc_dw_kernel(const float* __restrict__ x, const float* __restrict__ dy, float* __restrict__ partial,
                           int N, int H, int W, int Cout, int pad) {
     constexpr int K = 9 * CIN;
-    constexpr int KC = 3 * CIN;   // one input column of the patch, [kh][ci]
+    constexpr int SF = smallc_dw_stage_floats(CPL);
+    extern __shared__ float4 smallc_dw_smem_raw[];
     __shared__ float red[32 * CPL * (K + 1)];
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const int segs = (Wo + kSmallcDwSeg - 1) / kSmallcDwSeg;
-    const long long tasks = static_cast<long long>(N) * Ho * segs;
+    const int tasks = N * Ho * segs;   // < 2^31: the launcher checks the pixel count
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int co0 = lane * CPL;
     const bool live = co0 < Cout;
+    float* const stage0 = reinterpret_cast<float*>(smallc_dw_smem_raw) + warp * 2 * SF;
     float acc[CPL][K], accb[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
@@ -933,44 +992,58 @@ __global__ void __launch_bounds__(kSmallcDwWarps * 32, smallc_dw_per_sm(CIN, CPL
 #pragma unroll
         for (int k = 0; k < K; ++k) acc[j][k] = 0.f;
     }
-    for (long long task = static_cast<long long>(blockIdx.x) * kSmallcDwWarps + warp; task < tasks;
-         task += static_cast<long long>(gridDim.x) * kSmallcDwWarps) {
-        const int seg = static_cast<int>(task % segs);
-        const long long r = task / segs;   // n * Ho + oh
-        const int oh = static_cast<int>(r % Ho);
-        const long long n = r / Ho;
-        const int ow0 = seg * kSmallcDwSeg;
-        const float* xr[3];
-#pragma unroll
-        for (int kh = 0; kh < 3; ++kh) {
-            const int ih = oh + kh - pad;
-            xr[kh] = (ih >= 0 && ih < H) ? x + (n * H + ih) * static_cast<long long>(W) * CIN : nullptr;
+    // warp gw takes the consecutive segments [t0, t1): row-major over (n, oh, segment)
+    const long long gw = static_cast<long long>(blockIdx.x) * kSmallcDwWarps + warp;
+    const long long nw = static_cast<long long>(gridDim.x) * kSmallcDwWarps;
+    const int t0 = static_cast<int>(gw * tasks / nw), t1 = static_cast<int>((gw + 1) * tasks / nw);
+    int seg = t0 % segs, r = t0 / segs;   // the next segment to stage; r = n * Ho + oh
+    int oh = r % Ho, n = r / Ho;
+    auto stage_next = [&](float* buf) {
+        smallc_dw_stage<CIN>(buf, buf + kSmallcDwXs, x, dy, n, oh, r, seg * kSmallcDwSeg, H, W, Wo, Cout, pad, lane);
+        if (++seg == segs) {
+            seg = 0;
+            ++r;
+            if (++oh == Ho) {
+                oh = 0;
+                ++n;
+            }
         }
-        float win[3][KC];   // patch columns kw = 0, 1, 2 of the current pixel
-        auto load_col = [&](float* c, int iw) {
-            const bool in_w = iw >= 0 && iw < W;
+    };
+    if (t0 < t1) stage_next(stage0);
+    cp_async_commit();
+    for (int t = t0, b = 0; t < t1; ++t, b ^= 1) {
+        if (t + 1 < t1) stage_next(stage0 + (b ^ 1) * SF);
+        cp_async_commit();
+        cp_async_wait<1>();   // this segment's copies are done; the next one's may still fly
+        __syncwarp();
+        const float* xs = stage0 + b * SF;
+        const float* ds = xs + kSmallcDwXs;
+        float win[3][3 * CIN];   // patch columns kw = 0, 1, 2 of the current pixel, [kh][ci]
+        auto load_col = [&](float* c, int col) {
 #pragma unroll
-            for (int kh = 0; kh < 3; ++kh)
-#pragma unroll
-                for (int ci = 0; ci < CIN; ++ci)
-                    c[kh * CIN + ci] = (in_w && xr[kh]) ? __ldg(xr[kh] + static_cast<long long>(iw) * CIN + ci) : 0.f;
+            for (int kh = 0; kh < 3; ++kh) {
+                const float4 v = *reinterpret_cast<const float4*>(xs + (kh * kSmallcDwCols + col) * 4);
+                c[kh * CIN + 0] = v.x;
+                if constexpr (CIN > 1) c[kh * CIN + 1] = v.y;
+                if constexpr (CIN > 2) c[kh * CIN + 2] = v.z;
+                if constexpr (CIN > 3) c[kh * CIN + 3] = v.w;
+            }
         };
-        load_col(win[0], ow0 - pad);
-        load_col(win[1], ow0 - pad + 1);
-        const float* dyr = dy + (r * Wo + ow0) * Cout + co0;
+        load_col(win[0], 0);
+        load_col(win[1], 1);
 #pragma unroll
         for (int q = 0; q < kSmallcDwSeg; ++q) {
-            load_col(win[2], ow0 + q - pad + 2);
+            load_col(win[2], q + 2);
             float g[CPL];
 #pragma unroll
             for (int j = 0; j < CPL; ++j) g[j] = 0.f;
-            if (live && ow0 + q < Wo) {
+            if (live) {
                 if constexpr (CPL == 2) {
-                    const float2 v = __ldcs(reinterpret_cast<const float2*>(dyr + static_cast<long long>(q) * Cout));
+                    const float2 v = *reinterpret_cast<const float2*>(ds + q * Cout + co0);
                     g[0] = v.x;
                     g[1] = v.y;
                 } else {
-                    g[0] = __ldcs(dyr + static_cast<long long>(q) * Cout);
+                    g[0] = ds[q * Cout + co0];
                 }
             }
 #pragma unroll
@@ -986,12 +1059,14 @@ __global__ void __launch_bounds__(kSmallcDwWarps * 32, smallc_dw_per_sm(CIN, CPL
                                 fmaf(g[j], win[kw][kh * CIN + ci], acc[j][(kh * 3 + kw) * CIN + ci]);
             }
 #pragma unroll
-            for (int c = 0; c < KC; ++c) {
+            for (int c = 0; c < 3 * CIN; ++c) {
                 win[0][c] = win[1][c];
                 win[1][c] = win[2][c];
             }
         }
+        __syncwarp();   // every lane is done with this buffer before it is staged again
     }
+    cp_async_wait<0>();
     // the block's sum, warp by warp in warp order: red[co][0..K-1] products, red[co][K] dedb
     for (int w = 0; w < kSmallcDwWarps; ++w) {
         if (warp == w && live) {
@@ -1040,25 +1115,43 @@ __global__ void __launch_bounds__(256) smallc_dw_finish(const float* __restrict_
     }
 }
 
+template <int CIN, int CPL>
+int launch_smallc_dw_variant(int grid, const float* x, const float* dy, float* partial, int N, int H, int W, int Cout,
+                             int pad, cudaStream_t s) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = smallc_dw_smem(CPL);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(conv_smallc_dw_kernel<CIN, CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return check_cuda("cudaFuncSetAttribute(conv_smallc_dw_kernel)");
+        attr_done[dev] = true;
+    }
+    conv_smallc_dw_kernel<CIN, CPL><<<grid, kSmallcDwWarps * 32, smem, s>>>(x, dy, partial, N, H, W, Cout, pad);
+    return check_launch("conv_smallc_dw_kernel");
+}
+
 // Cin <= 4 and Cout <= 64 (Cout even above 32); partial: smallc_dw_blocks() *
 // Cout * (9 * Cin + 1) floats
 int launch_conv_smallc_dw(const float* x, const float* dy, float* partial, float* dw, float* db, float alpha,
                           int accumulate, int N, int H, int W, int Cin, int Cout, int pad, cudaStream_t s) {
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    const long long P = static_cast<long long>(N) * Ho * Wo;
+    SPRINT_REQUIRE(P < (1ll << 31) - 32, SPRINT_ERR_SHAPE, "conv_dW: %lld output pixels", P);
     const int grid = smallc_dw_blocks(N, Ho, Wo, Cin, Cout);
-    const int threads = kSmallcDwWarps * 32;
-    const int key = Cin * 2 + (Cout > 32 ? 1 : 0);
-    switch (key) {
-        case 2: conv_smallc_dw_kernel<1, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 3: conv_smallc_dw_kernel<1, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 4: conv_smallc_dw_kernel<2, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 5: conv_smallc_dw_kernel<2, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 6: conv_smallc_dw_kernel<3, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 7: conv_smallc_dw_kernel<3, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        case 8: conv_smallc_dw_kernel<4, 1><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
-        default: conv_smallc_dw_kernel<4, 2><<<grid, threads, 0, s>>>(x, dy, partial, N, H, W, Cout, pad); break;
+    const bool pairs = Cout > 32;
+    int rc;
+    switch (Cin) {
+        case 1: rc = pairs ? launch_smallc_dw_variant<1, 2>(grid, x, dy, partial, N, H, W, Cout, pad, s)
+                           : launch_smallc_dw_variant<1, 1>(grid, x, dy, partial, N, H, W, Cout, pad, s); break;
+        case 2: rc = pairs ? launch_smallc_dw_variant<2, 2>(grid, x, dy, partial, N, H, W, Cout, pad, s)
+                           : launch_smallc_dw_variant<2, 1>(grid, x, dy, partial, N, H, W, Cout, pad, s); break;
+        case 3: rc = pairs ? launch_smallc_dw_variant<3, 2>(grid, x, dy, partial, N, H, W, Cout, pad, s)
+                           : launch_smallc_dw_variant<3, 1>(grid, x, dy, partial, N, H, W, Cout, pad, s); break;
+        default: rc = pairs ? launch_smallc_dw_variant<4, 2>(grid, x, dy, partial, N, H, W, Cout, pad, s)
+                            : launch_smallc_dw_variant<4, 1>(grid, x, dy, partial, N, H, W, Cout, pad, s); break;
     }
-    int rc = check_launch("conv_smallc_dw_kernel");
     if (rc) return rc;
     const int K = 9 * Cin;
     smallc_dw_finish<<<(Cout * (K + 1) + 31) / 32, 256, 0, s>>>(partial, grid, Cout, K, dw, db, alpha, accumulate);
