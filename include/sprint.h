@@ -138,6 +138,13 @@ size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Cin, int Cout
  *   dw[co,kh,kw,ci] = (accumulate ? dw : 0) + alpha * sum_{n,oh,ow} dy[n,oh,ow,co] x[n,oh+kh-pad,ow+kw-pad,ci]
  *   db[co]          = (accumulate ? db : 0) + alpha * sum_{n,oh,ow} dy[n,oh,ow,co]   (db may be NULL)
  * dy is the gradient w.r.t. the pre-activation (the ReLU mask already applied).
+ * x: device [N][H][W][Cin]; dy: device [N][Ho][Wo][Cout]; dw: device
+ * [Cout][3][3][Cin]; db: device [Cout]. With Cin <= 4 and Cout <= 64 (Cout even
+ * when above 32; the RGB input layer) both sums run in FP32 on the CUDA cores
+ * from x and dy as they are, and the workspace holds one partial per launched
+ * block (Cout * (9 * Cin + 1) floats each), added in block order; otherwise the
+ * workspace holds the transposed copies x^T [Cin][H][W][N], dy^T
+ * [Cout][Ho][Wo][N] of the TF32 tensor-core path and its partial sums.
  * ws: see sprint_conv_workspace_size(SPRINT_CONV_DW, ...). */
 int sprint_conv_dW(const float* x, const float* dy, float* dw, float* db, float alpha, int accumulate, int N, int H,
                    int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes, sprint_stream_t stream);

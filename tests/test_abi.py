@@ -78,6 +78,13 @@ def test_shape_and_workspace_errors(S):
     assert S.sprint_fc_workspace_size(64, 256, 512, 1) < need       # wT supplied: no transposed copy needed
     assert S.sprint_conv_workspace_size(2, 8, 16, 16, 64, 64, 1) > 0  # dedw: transposed copies
     assert S.sprint_conv_workspace_size(9, 8, 16, 16, 64, 64, 1) == 0
+    # the RGB layer's dedw: block partials of Cout * (9 * Cin + 1) floats, far
+    # below the transposed copies (x^T 9.6 MB + dy^T 205.5 MB at 16 x 224 x 224)
+    rgb = S.sprint_conv_workspace_size(2, 16, 224, 224, 3, 64, 1)
+    per_block = 64 * (9 * 3 + 1) * 4
+    assert rgb % per_block < 256 and 1 <= rgb // per_block <= 4 * 1024
+    assert rgb < 16 * 224 * 224 * (3 + 64) * 4 // 50
+    assert S.sprint_conv_workspace_size(2, 16, 224, 224, 3, 96, 1) > 16 * 224 * 224 * 96 * 4   # Cout > 64: copies
     assert L.sprint_transpose(16, 16, 4, 4, None) == 1               # aliasing
 
 
