@@ -1099,9 +1099,9 @@ __global__ void __launch_bounds__(256) smallc_dw_finish(const float* __restrict_
     const int O = Cout * (K + 1);
     const int lane = threadIdx.x & 31, st = threadIdx.x >> 5;
     const int o = blockIdx.x * 32 + lane;
-    float t = 0.f;
-    if (o < O)
-        for (int b = st; b < nblocks; b += 8) t += partial[static_cast<long long>(b) * O + o];
+    const float t = o < O && st < nblocks
+                        ? ordered_strided_sum(partial + static_cast<long long>(st) * O + o, (nblocks - st + 7) / 8, 8ll * O)
+                        : 0.f;
     red[st][lane] = t;
     __syncthreads();
     if (st != 0 || o >= O) return;
@@ -1257,9 +1257,8 @@ __global__ void dw_split_reduce(const float* __restrict__ partial, int splits, i
         const int ci = static_cast<int>(idx % Cin);
         const int tap = static_cast<int>((idx / Cin) % 9);
         const int co = static_cast<int>(idx / (9ll * Cin));
-        float t = 0.f;
-        for (int s = 0; s < splits; ++s)
-            t += partial[((static_cast<long long>(tap) * splits + s) * Cout + co) * Cin + ci];
+        const float t = ordered_strided_sum(partial + (static_cast<long long>(tap) * splits * Cout + co) * Cin + ci,
+                                            splits, static_cast<long long>(Cout) * Cin);
         dw[idx] = (accumulate ? dw[idx] : 0.f) + alpha * t;
     }
 }
@@ -1275,8 +1274,7 @@ __global__ void dw_packed_reduce(const float* __restrict__ partial, int splits, 
         const int ci = static_cast<int>(idx % Cin);
         const int tap = static_cast<int>((idx / Cin) % 9);
         const long long co = idx / (9ll * Cin);
-        float t = 0.f;
-        for (int s = 0; s < splits; ++s) t += partial[(s * static_cast<long long>(Cout) + co) * np + tap * rows + ci];
+        const float t = ordered_strided_sum(partial + co * np + tap * rows + ci, splits, Cout * np);
         dw[idx] = (accumulate ? dw[idx] : 0.f) + alpha * t;
     }
 }
@@ -1285,8 +1283,7 @@ __global__ void colsum_finish_k(const float* __restrict__ partial, int chunks, i
                                 float alpha, int accumulate) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= cols) return;
-    float t = 0.f;
-    for (int k = 0; k < chunks; ++k) t += partial[static_cast<long long>(k) * cols + c];
+    const float t = ordered_strided_sum(partial + c, chunks, cols);
     out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
 }
 

@@ -39,8 +39,7 @@ __global__ void colsum_finish(const float* __restrict__ partial, int chunks, int
                               float alpha, int accumulate) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= cols) return;
-    float t = 0.f;
-    for (int k = 0; k < chunks; ++k) t += partial[static_cast<long long>(k) * cols + c];
+    const float t = ordered_strided_sum(partial + c, chunks, cols);
     out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
 }
 
@@ -198,8 +197,9 @@ __global__ void __launch_bounds__(256) colsum_parts_finish(const float* __restri
     __shared__ float red[256];
     const int c = blockIdx.x;
     const float* p = partial + static_cast<long long>(c) * nparts;
-    float t = 0.f;
-    for (long long k = threadIdx.x; k < nparts; k += 256) t += p[k];
+    const float t = threadIdx.x < nparts
+                        ? ordered_strided_sum(p + threadIdx.x, static_cast<int>((nparts - threadIdx.x + 255) / 256), 256)
+                        : 0.f;
     red[threadIdx.x] = t;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
