@@ -137,6 +137,44 @@ def test_conv_adjoint_identities():
     np.testing.assert_allclose(db, y.sum(axis=(0, 1, 2)), rtol=1e-14)
 
 
+@pytest.mark.parametrize("pad", [0, 1])
+def test_conv_dw_brute_force(pad):
+    """dedw / dedb of [S] Sec. 3.3 by explicit loops over every output pixel and
+    tap, skipping taps that fall outside the image (the few-channel shapes of
+    the RGB layer, both paddings)."""
+    x = synth.normal(21, "x", (2, 5, 7, 3)).astype(np.float64)
+    n, h, wd, ci = x.shape
+    ho, wo = h + 2 * pad - 2, wd + 2 * pad - 2
+    dy = synth.normal(21, "dy", (n, ho, wo, 4)).astype(np.float64)
+    dw_ref = np.zeros((4, 3, 3, ci))
+    db_ref = np.zeros(4)
+    for a in range(n):
+        for oh in range(ho):
+            for ow in range(wo):
+                for co in range(4):
+                    g = dy[a, oh, ow, co]
+                    db_ref[co] += g
+                    for kh in range(3):
+                        for kw in range(3):
+                            ih, iw = oh + kh - pad, ow + kw - pad
+                            if 0 <= ih < h and 0 <= iw < wd:
+                                for c in range(ci):
+                                    dw_ref[co, kh, kw, c] += g * x[a, ih, iw, c]
+    dw, db = O.conv3x3_dw(x, dy, pad=pad)
+    np.testing.assert_allclose(dw, dw_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(db, db_ref, rtol=0, atol=1e-12)
+
+
+def test_conv_adjoint_identities_pad0():
+    x = synth.normal(22, "x", (2, 6, 5, 2)).astype(np.float64)
+    w = synth.normal(22, "w", (3, 3, 3, 2)).astype(np.float64)
+    y = synth.normal(22, "y", (2, 4, 3, 3)).astype(np.float64)
+    lhs = np.vdot(O.conv3x3_fwd(x, w, None, pad=0), y)
+    assert abs(lhs - np.vdot(x, O.conv3x3_dx(y, w, 6, 5, pad=0))) < 1e-12 * abs(lhs) + 1e-12
+    dw, _ = O.conv3x3_dw(x, y, pad=0)
+    assert abs(np.vdot(dw, w) - lhs) < 1e-12 * abs(lhs) + 1e-12
+
+
 def test_im2col_brute_force_index_map():
     x = synth.normal(6, "x", (2, 3, 4, 2))
     col, src = O.im2col(x)
