@@ -506,6 +506,7 @@ CONV_CASES = [
     (3, 20, 40, 2, 64),     # RGB dW: two input channels, full warp of channel pairs
     (2, 11, 9, 4, 64),      # RGB dW: the widest patch (4 channels) with channel pairs
     (1, 6, 17, 1, 40),      # RGB dW: one input channel, Cout between 32 and 64
+    (2, 7, 9, 3, 18),       # RGB dW with Cout % 4 != 0 (4-byte dy copies); CUDA-core forward and dX
 ]
 
 
