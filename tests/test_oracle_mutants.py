@@ -10,7 +10,7 @@ import oracle as O
 import oracle.oracle as OM
 import test_oracle_pins as P
 
-_ORIG = {k: getattr(OM, k) for k in ("conv3x3_dx", "conv3x3_fwd", "softmax_xent", "fc_bwd")}
+_ORIG = {k: getattr(OM, k) for k in ("conv3x3_dx", "conv3x3_fwd", "conv3x3_dw", "softmax_xent", "fc_bwd")}
 
 
 def _flipped_dx(dy, w, h, wd, pad=1):
@@ -23,6 +23,20 @@ def _no_bias_fwd(x, w, b, pad=1):
 
 def _swapped_taps_fwd(x, w, b, pad=1):
     return _ORIG["conv3x3_fwd"](x, np.swapaxes(w, 1, 2), b, pad)
+
+
+def _dw_taps_transposed(x, dy, pad=1):
+    dw, db = _ORIG["conv3x3_dw"](x, dy, pad)
+    return np.swapaxes(dw, 1, 2), db
+
+
+def _dw_pad_ignored(x, dy, pad=1):
+    return _ORIG["conv3x3_dw"](x, dy, 1)
+
+
+def _db_first_image_only(x, dy, pad=1):
+    dw, _ = _ORIG["conv3x3_dw"](x, dy, pad)
+    return dw, np.asarray(dy, float)[0].sum(axis=(0, 1))
 
 
 def _softmax_sum(z, labels, reduction="mean"):
@@ -92,6 +106,9 @@ MUTANTS = [
     ("conv3x3_dx", _flipped_dx, P.test_conv_adjoint_identities, ()),
     ("conv3x3_fwd", _no_bias_fwd, P.test_conv_fwd_brute_force, (1,)),
     ("conv3x3_fwd", _swapped_taps_fwd, P.test_conv_fwd_im2col_route, ()),
+    ("conv3x3_dw", _dw_taps_transposed, P.test_conv_dw_brute_force, (1,)),
+    ("conv3x3_dw", _dw_pad_ignored, P.test_conv_dw_brute_force, (0,)),
+    ("conv3x3_dw", _db_first_image_only, P.test_conv_dw_brute_force, (1,)),
     ("softmax_xent", _softmax_sum, P.test_softmax_fd_and_stability, ()),
     ("update_momentum", _momentum_sign, P.test_momentum_constant_gradient_closed_form, ()),
     ("update_adagrad", _adagrad_no_square, P.test_adagrad_constant_gradient_closed_form, ()),
