@@ -1,22 +1,27 @@
 """Throughput of the stale-weight SGD hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config smlps|tiny|vgg_c|vgg_i|ps]
+                    [--config vgg_i|vgg_c|smlps|tiny|vgg_c_hybrid|smlps_fetch_push|ps]
 
 A step is one pass of the whole hot path over one batch per logical replica:
 every replica's forward, softmax cross-entropy and backward (gradients fused
 into its GradBuf), then the parameter-server update that writes the next
-weight version. Default workload: the SMLPs MLP (3072 -> 5000 x5 -> 10),
-batch 512 per replica, 4 replicas with seeded delays in {0..3}, eta = 0.01.
+weight version. Default workload: the ILSVRC-shaped VGG-16 (3x224x224 input,
+13 conv3x3 layers, FC 25088-4096-4096-1000, N_Param 138,357,544), batch 64 per
+replica, 8 replicas with seeded delays in {0..7}, GradBuf sum then
+W -= eta * sum, eta = 0.005.
 
 Prints one JSON line (rank 0). `value` is images/s with inputs resident in HBM;
 `e2e` is the same metric with every step's inputs copied from pinned host
 memory and the loss read back inside the timed region. `roofline` is the
-dominant kernel's achieved TF32 FLOP/s (or HBM GB/s for the update sweep)
-from CUDA events around its launches, against the measured peak.
-`--impl reference` times the FP64 CPU oracle on the same workload (bounded
-sample per step). Multi-GPU (torchrun): every rank runs an independent replica
-of the workload (no data-path collective); value = the sum over ranks.
+dominant convolution kernel's achieved TF32 FLOP/s inside the timed steps
+(CUDA events around the layers' per-replica launch groups) against the
+measured peak. `breakdown` times one extra step issued serially, one event pair
+per library call, and splits it into the SGEMM roles of the SPRINT cost model
+(Eq. (4)). `--config ps` sweeps the parameter-server update instead (GB/s per
+point). `--impl reference` times the FP64 CPU oracle on the same workload, each
+step a bounded sample. Multi-GPU (torchrun): every rank runs an independent
+replica of the workload (no data-path collective); value = the sum over ranks.
 """
 from __future__ import annotations
 
@@ -33,19 +38,21 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+METRIC = "CNN train images/s on 1 GB300; conv-GEMM % TF32 peak; update GB/s vs HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense tensor ratio (tf32 1.1 PF vs bf16 2.25 PF)
 
 CONFIGS = {
+    "vgg_i": dict(net="vgg_i", batch=64, replicas=8, max_delay=7, optimizer="sgd", eta=0.005,
+                  desc="VGG-16 ILSVRC-shaped fp32 (3x224x224, N_Param 138,357,544), batch 64/replica, ASGD 8 "
+                       "replicas, seeded delays {0..7}, GradBuf sum then W -= eta*sum, SGD eta=0.005"),
+    "vgg_c": dict(net="vgg_c", batch=128, replicas=1, max_delay=0, optimizer="momentum", eta=0.01,
+                  stage_delays=[3, 2, 1, 0],
+                  desc="VGG-16 CIFAR-shaped fp32, batch 128, momentum 0.9, 4 pipeline stages s_k=3,2,1,0"),
     "smlps": dict(net="smlps", batch=512, replicas=4, max_delay=3, optimizer="sgd", eta=0.01,
                   desc="SMLPs MLP 3072-5000x5-10 fp32, batch 512/replica, ASGD 4 replicas, delays {0..3}, SGD eta=0.01"),
     "tiny": dict(net="tiny", batch=8, replicas=1, max_delay=0, optimizer="sgd", eta=0.01,
                  desc="tiny CNN (conv16-pool-conv32-pool-fc10), batch 8, SGD eta=0.01"),
-    "vgg_c": dict(net="vgg_c", batch=128, replicas=1, max_delay=0, optimizer="momentum", eta=0.01,
-                  stage_delays=[3, 2, 1, 0],
-                  desc="VGG-16 CIFAR-shaped fp32, batch 128, momentum 0.9, 4 pipeline stages s_k=3,2,1,0"),
-    "vgg_i": dict(net="vgg_i", batch=64, replicas=8, max_delay=7, optimizer="sgd", eta=0.005,
-                  desc="VGG-16 ILSVRC-shaped fp32, batch 64/replica, ASGD 8 replicas, delays {0..7}, SGD eta=0.005"),
     # the widened rows: hybrid pipelined -> non-pipelined training with Nesterov momentum and
     # weight decay, and DistBelief n_fetch / n_push
     "vgg_c_hybrid": dict(net="vgg_c", batch=128, replicas=1, max_delay=0, optimizer="nesterov", eta=0.01,
@@ -56,6 +63,17 @@ CONFIGS = {
                              n_fetch=3, n_push=2,
                              desc="SMLPs MLP 3072-5000x5-10 fp32, batch 512/replica, 4 replicas, DistBelief "
                                   "n_fetch=3 / n_push=2, Adagrad eta=0.001"),
+    "ps": dict(desc="parameter-server update sweep fp32: n = 1M / 16M / 138M parameters, k = 1, 2, 4, 8, 16 pending "
+                    "GradBufs, SGD / momentum 0.9 / Adagrad (eta 0.01, eps 1e-8, G0 0.1)"),
+}
+DEFAULT_CONFIG = "vgg_i"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# roofline kernel, from one ncu capture of that kernel on the same shape; must
+# be re-measured whenever that kernel or its tile choice changes (then absent).
+PROFILED_TRAFFIC = {
+    # one call: the GEMM kernel 461.8 + 47.0 MB and its tail reduction 17.1 MB (one ncu capture)
+    "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 525.9e6,
 }
 
 
@@ -66,6 +84,14 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tf32_peaks():
+    """(burst, sustained) TF32 TFLOP/s: the measured bf16 peaks times the nominal ratio."""
+    peaks, src = load_peaks()
+    burst = peaks["bf16_tflops"] * TF32_OVER_BF16
+    sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
+    return burst, sust, src
 
 
 class ClockSampler:
@@ -114,16 +140,6 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the probed kernel, from one ncu capture of the same kernel on the same shape
-# (bench.py --kernel fc_fwd_grouped); must be re-measured whenever that kernel
-# or its tile choice changes (then None).
-PROFILED_TRAFFIC = {
-    # one call: the GEMM kernel 461.8 + 47.0 MB and its tail reduction 17.1 MB (one ncu capture)
-    "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 525.9e6,
-}
-
-
 class GemmProbe:
     """Records CUDA events, on the launching stream, around the forward FC
     GEMM launches of the given (in, out) shapes: one grouped tensor-core
@@ -161,14 +177,150 @@ class GemmProbe:
         ms = np.array([a.elapsed_time(e) for a, e, _ in self.events])
         fl = np.array([f for _, _, f in self.events])
         return {"launches": len(ms), "mean_ms": float(ms.mean()), "total_ms": float(ms.sum()),
-                "tflops": float((fl / (ms / 1e3)).mean() / 1e12), "flops_per_launch": float(fl.mean()),
-                "kernel": self.desc}
+                "flops_per_launch": float(fl.mean()), "kernel": self.desc, "how": "events around each grouped call"}
+
+
+class ConvSpanProbe:
+    """Times the per-replica convolution forward groups of chosen layers inside
+    the timed steps: the trainer's span hook records an event on the main
+    stream before the replicas' launches are forked and one after they have
+    joined, so the pair brackets exactly the R launches of that layer (which
+    share the GPU: each persistent launch fills every SM). Per-launch time =
+    span / R; work = 2 * pixels * Cout * 9 * Cin per launch."""
+
+    def __init__(self, torch, tr, layers):
+        self.torch = torch
+        self.tr = tr
+        self.layers = set(layers)
+        self.active = False
+        self.open = {}
+        self.spans = []   # (layer, begin, end)
+        tr.span_hook = self.hook
+
+    def hook(self, tag, phase, stream):
+        kind, li = tag
+        if not self.active or kind != "fwd" or li not in self.layers:
+            return
+        ev = self.torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        if phase == 0:
+            self.open[li] = ev
+        else:
+            self.spans.append((li, self.open.pop(li), ev))
+
+    def summary(self, shapes, N, R, desc):
+        if not self.spans:
+            return None
+        ms = np.array([a.elapsed_time(e) for _, a, e in self.spans])
+        fl = np.array([2.0 * N * shapes[li].h * shapes[li].w * shapes[li].cout * 9 * shapes[li].cin
+                       for li, _, _ in self.spans])
+        per_layer = {}
+        for (li, _, _), m, f in zip(self.spans, ms, fl):
+            d = per_layer.setdefault(li, [0.0, 0.0, 0])
+            d[0] += m
+            d[1] += f * R
+            d[2] += 1
+        L = shapes
+        return {"launches": int(len(ms) * R), "mean_ms": float(ms.sum() / (len(ms) * R)),
+                "total_ms": float(ms.sum()), "flops_per_launch": float(fl.mean()), "kernel": desc,
+                "how": f"events on the main stream around each layer's {R} per-replica launches (fork to join); "
+                       "per-launch time = span / replicas",
+                "per_layer": {f"conv{li} {L[li].h}x{L[li].w}x{L[li].cin}->{L[li].cout}":
+                              {"tflops": round(v[1] / (v[0] / 1e3) / 1e12, 1), "ms_per_launch": round(v[0] / v[2] / R, 4)}
+                              for li, v in per_layer.items()}}
+
+
+# the roles of the SPRINT cost model's Eq. (4) / Sec. 3.3 table, per library call
+ROLE_OF_CALL = {
+    "sprint_conv_fwd": "convolution",
+    "sprint_conv_dW": "dedw+dedb conv",
+    "sprint_conv_dX": "dedx conv",
+    "sprint_fc_fwd_batched": "fc",
+    "sprint_fc_bwd_batched": "fc backward (dedx fc + dedw + dedb)",
+    "sprint_pool_fwd": "pool",
+    "sprint_pool_bwd": "pool",
+    "sprint_softmax_xent_batched": "softmax",
+    "sprint_apply_update": "update",
+    "sprint_apply_update_t": "update",
+}
+
+
+class CallProbe:
+    """Wraps every library call the trainer makes with a CUDA event pair on the
+    call's stream (a serial step: one stream, so the pairs are exact)."""
+
+    def __init__(self, sprint_mod, torch):
+        self.S = sprint_mod
+        self.torch = torch
+        self.active = False
+        self.calls = []   # (name, flops, a, e)
+        for name in list(ROLE_OF_CALL) + ["sprint_transpose"]:
+            self._wrap(name)
+
+    def _wrap(self, name):
+        orig = getattr(self.S, name)
+        torch = self.torch
+        probe = self
+
+        def wrapped(*args, **kw):
+            if not probe.active:
+                return orig(*args, **kw)
+            a = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            st = torch.cuda.current_stream()
+            a.record(st)
+            r = orig(*args, **kw)
+            e.record(st)
+            probe.calls.append((name, probe._flops(name, args), a, e))
+            return r
+        setattr(self.S, name, wrapped)
+
+    @staticmethod
+    def _flops(name, a):
+        if name == "sprint_conv_fwd" or name == "sprint_conv_dW":
+            N, H, W, Ci, Co = a[4:9] if name == "sprint_conv_fwd" else a[6:11]
+            return 2.0 * N * H * W * Co * 9 * Ci
+        if name == "sprint_conv_dX":
+            N, H, W, Ci, Co = a[5:10]
+            return 2.0 * N * H * W * Co * 9 * Ci
+        if name == "sprint_fc_fwd_batched":
+            return 2.0 * a[4] * a[5] * a[6] * len(a[0])
+        if name == "sprint_fc_bwd_batched":
+            N, fin, fout = a[10:13]
+            return (2.0 if a[5] is None else 4.0) * N * fin * fout * len(a[0])
+        return 0.0
+
+    def summary(self):
+        roles, flops = {}, {}
+        total = 0.0
+        for name, f, a, e in self.calls:
+            ms = a.elapsed_time(e)
+            r = ROLE_OF_CALL.get(name, "other")
+            roles[r] = roles.get(r, 0.0) + ms
+            flops[r] = flops.get(r, 0.0) + f
+            total += ms
+        return {"serial_ms_per_step": round(total, 3), "calls": len(self.calls),
+                "roles_ms": {r: round(v, 3) for r, v in sorted(roles.items(), key=lambda kv: -kv[1])},
+                "roles_share": {r: round(v / total, 4) for r, v in roles.items()} if total else {},
+                "roles_tflops": {r: round(flops[r] / (roles[r] / 1e3) / 1e12, 1) for r in roles if flops.get(r)}}
 
 
 def dense_init(shapes, seed):
     import synth
     return np.concatenate([np.concatenate([synth.normal(seed, f"w{i}", (L.w_numel,), np.sqrt(2.0 / L.fan_in)),
                                            np.zeros(L.cout, np.float32)]) for i, L in enumerate(shapes)])
+
+
+def make_trainer(cfg, N, R, concurrent, StaleSGD, model):
+    net = model.NETWORKS[cfg["net"]]
+    kw = dict(replicas=R, max_delay=cfg["max_delay"], schedule_seed=1234, optimizer=cfg["optimizer"], eta=cfg["eta"],
+              weight_decay=cfg.get("weight_decay", 0.0))
+    if "stage_delays" in cfg:
+        kw = dict(stage_of_layer=model.VGG_C_STAGES, stage_delays=cfg["stage_delays"], optimizer=cfg["optimizer"],
+                  eta=cfg["eta"], weight_decay=cfg.get("weight_decay", 0.0), hybrid_switch=cfg.get("hybrid_switch"))
+    if "n_fetch" in cfg:
+        kw.update(max_delay=0, n_fetch=cfg["n_fetch"], n_push=cfg["n_push"])
+    return StaleSGD(net, N, concurrent=concurrent, **kw)
 
 
 def run_ours(args, cfg, rank, world, local_rank):
@@ -180,7 +332,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     # a dedicated stream (not the legacy default stream) for the whole run: the
-    # trainer issues on it, and the probe's events are recorded on it. It runs at
+    # trainer issues on it, and the probes' events are recorded on it. It runs at
     # high priority so that the training step's kernels (the critical path) are
     # scheduled ahead of the trainer's low-priority update stream
     torch.cuda.set_stream(torch.cuda.Stream(dev, priority=-1))
@@ -191,14 +343,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     feat = c * h * w
     classes = shapes[-1].cout
     P = max(2 * R, 8)
-    kw = dict(replicas=R, max_delay=cfg["max_delay"], schedule_seed=1234, optimizer=cfg["optimizer"], eta=cfg["eta"],
-              weight_decay=cfg.get("weight_decay", 0.0))
-    if "stage_delays" in cfg:
-        kw = dict(stage_of_layer=model.VGG_C_STAGES, stage_delays=cfg["stage_delays"], optimizer=cfg["optimizer"],
-                  eta=cfg["eta"], weight_decay=cfg.get("weight_decay", 0.0), hybrid_switch=cfg.get("hybrid_switch"))
-    if "n_fetch" in cfg:
-        kw.update(max_delay=0, n_fetch=cfg["n_fetch"], n_push=cfg["n_push"])
-    tr = StaleSGD(net, N, concurrent=not args.serial, **kw)
+    tr = make_trainer(cfg, N, R, not args.serial, StaleSGD, model)
     # synthetic data generated on the device (seeded), weights He-normal
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + rank)
@@ -208,19 +353,31 @@ def run_ours(args, cfg, rank, world, local_rank):
     wd = dense_init(shapes, 7)
     tr.load_weights(wd)
 
+    has_conv = any(L.kind == "conv" for L in shapes)
+    # roofline probe: the implicit-GEMM conv forward of the tensor-core layers without a
+    # pool (their per-replica group holds conv launches only), or the grouped FC forward
+    conv_layers = [i for i, L in enumerate(shapes) if L.kind == "conv" and not L.pool and
+                   sprint.sprint_conv_plan(sprint.SPRINT_CONV_FWD, N, L.h, L.w, L.cin, L.cout)["path"] == "tc"]
+    span_probe = ConvSpanProbe(torch, tr, conv_layers) if (has_conv and not tr.use_graphs and conv_layers) else None
     big = [(L.cin, L.cout) for L in shapes if L.kind == "fc" and L.cin * L.cout >= 20_000_000]
-    probe = GemmProbe(sprint, torch, big)
+    gemm_probe = GemmProbe(sprint, torch, big) if not has_conv else None
 
-    for _ in range(args.warmup):
+    first_nonfinite = None
+    for i in range(args.warmup):
         tr.step()
+        if first_nonfinite is None and not math.isfinite(tr.step_loss()):
+            first_nonfinite = i
     tr.prepare_graphs()   # periodic schedules: capture every step graph of a period now, replay later
     torch.cuda.synchronize()
     barrier(world)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    probe.active = True
+    for p in (span_probe, gemm_probe):
+        if p is not None:
+            p.active = True
     launches0 = sprint.sprint_launch_count() + tr.graph_launch_adjust
+    t_first = tr.t
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -232,13 +389,17 @@ def run_ours(args, cfg, rank, world, local_rank):
     tr.join()   # the last step's per-layer updates are inside the timed region
     end.record(tr.main_stream)
     torch.cuda.synchronize()
-    probe.active = False
+    for p in (span_probe, gemm_probe):
+        if p is not None:
+            p.active = False
     launches = sprint.sprint_launch_count() + tr.graph_launch_adjust - launches0   # replayed graph kernels included
     clk = clocks.stop()
     ms = start.elapsed_time(end)
     ms_max = allreduce_max(ms, world)
     barrier(world)
     loss = tr.step_loss()
+    if first_nonfinite is None and not math.isfinite(loss):
+        first_nonfinite = f"between step {args.warmup} and step {tr.t - 1} (the timed steps)"
 
     # end to end, pipelined like a training loop: every step's inputs are copied from
     # pinned host memory (on a copy stream, into one of two device buffers, while the
@@ -287,31 +448,60 @@ def run_ours(args, cfg, rank, world, local_rank):
     e2e_s = time.perf_counter() - t0
     e2e_s = allreduce_max(e2e_s, world)
 
+    # one more step issued serially (one stream, eager, no update overlap) with an event
+    # pair around every library call: the per-role split of the SPRINT cost model, Eq. (4)
+    breakdown = None
+    if not args.no_breakdown:
+        tr.join()
+        torch.cuda.synchronize()
+        call_probe = CallProbe(sprint, torch)
+        saved = (tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook)
+        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook = False, tr.main_stream, False, None
+        tr._graph_steps = False
+        with torch.cuda.stream(tr.main_stream):
+            call_probe.active = True
+            tr.step()
+            tr.join()
+            call_probe.active = False
+        torch.cuda.synchronize()
+        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook = saved
+        breakdown = call_probe.summary()
+
     imgs = R * N * args.steps * world
     value, _ = weak_scaling_value(R * N * args.steps, ms / 1e3, world)
     e2e_value = imgs / e2e_s
-    peaks, peak_src = load_peaks()
-    summ = probe.summary()
+    burst, sust, peak_src = tf32_peaks()
+    if span_probe is not None:
+        summ = span_probe.summary(shapes, N, R, "tc_gemm_kernel<CONV_IMPL> (implicit-GEMM conv forward, TF32), "
+                                                "every tensor-core layer without a pool")
+    else:
+        summ = gemm_probe.summary() if gemm_probe is not None else None
     roof = None
     if summ:
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
         achieved = summ["flops_per_launch"] / (summ["mean_ms"] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": PROFILED_TRAFFIC.get(summ["kernel"]),
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(burst, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / burst, 4), "traffic": PROFILED_TRAFFIC.get(summ["kernel"]),
                 "kernel": summ["kernel"],
-                "peak_source": f"{peak_src}: bf16 sustained x 1.1/2.25 (nominal tf32/bf16 dense ratio)",
-                "launches": summ["launches"], "mean_ms": round(summ["mean_ms"], 4)}
+                "peak_source": f"{peak_src}: bf16 burst x 1.1/2.25 (nominal tf32/bf16 dense ratio); the timed "
+                               "steps ran at the clocks below",
+                "peak_sustained": round(sust, 1), "frac_of_sustained": round(achieved / sust, 4),
+                "launches": summ["launches"], "mean_ms": round(summ["mean_ms"], 4), "how": summ["how"]}
+        if "per_layer" in summ:
+            roof["per_layer"] = summ["per_layer"]
+    elif breakdown:
+        roof = {"note": "no in-step probe for CUDA-graph replays; see breakdown.roles_tflops (serial step)"}
     flops_step = model.train_flops_per_image(net) * R * N
+    step_tflops = flops_step * args.steps / (ms_max / 1e3) / 1e12 * world
     out = {
-        "metric": "CNN train images/s on 1 GB300; conv-GEMM % TF32 peak; update GB/s vs HBM peak",
+        "metric": METRIC,
         "value": round(value, 1), "unit": "images/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 (tf32 tensor-core GEMMs, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) inputs, uniform labels, He-normal init)",
         "config": {"workload": cfg["desc"], "global_batch": R * N * world, "replicas_per_gpu": R,
                    "parallelism": f"replicas only x{world}" if world > 1 else "1 GPU",
-                   "l2": "working set (weights, 4 GradBufs) far larger than L2; no flush needed",
-                   **({"staleness_first_step": tr.staleness(0), "staleness_last_step": tr.staleness(tr.t - 1)}
+                   "l2": "working set (weights, GradBufs, activations) far larger than L2; no flush needed",
+                   **({"staleness_first_step": tr.staleness(t_first), "staleness_last_step": tr.staleness(tr.t - 1)}
                       if tr.pipeline else {})},
         "e2e": {"value": round(e2e_value, 1), "unit": "images/s",
                 "h2d_bytes_per_step": int(hx.numel() * 4 + hy.numel() * 4),
@@ -320,44 +510,239 @@ def run_ours(args, cfg, rank, world, local_rank):
                 "host_ms_per_step": round(e2e_s * 1e3 / args.steps, 3)},
         "gpu_launches": int(launches),
         "roofline": roof,
-        "achieved_step_tflops": round(flops_step * args.steps / (ms_max / 1e3) / 1e12 * world, 1),
+        "achieved_step_tflops": round(step_tflops, 1),
+        "step_frac_of_tf32_burst": round(step_tflops / world / burst, 4),
+        "breakdown": breakdown,
         "clocks": clk,
-        # a diverged run (the ILSVRC-shaped config with 8 summed replica gradients at eta 0.005
-        # overflows after a few steps) has no finite loss: JSON has no NaN
+        # JSON has no NaN: a diverged run reports null
         "loss_last": loss if math.isfinite(loss) else None,
         "kernels_per_step": int(launches // args.steps),
         "host_issue_ms_per_step": round(host_issue_ms, 3),
     }
+    if first_nonfinite is not None:
+        out["numerics"] = {
+            "loss_first_nonfinite_step": first_nonfinite,
+            "note": "the configured eta with the replicas' gradients summed (no normalisation, no batch norm) "
+                    "diverges; the FP64 oracle diverges the same way on the reduced net. Steps after that run on "
+                    "non-finite values; the kernels' work and time do not depend on the values"}
     return out
 
 
-def cpu_oracle_rate(cfg, budget_s=12.0):
-    """Images/s of the FP64 oracle's forward+backward for one replica batch,
-    on a bounded sample of images at the workload's full layer sizes."""
+# ---------------------------------------------------------------- the FP64 oracle on the host
+
+def _oracle_sample_step(O, layers, w0, n_img, frac_update, R, opt, arch, tag):
+    """One bounded sample of a training step: forward + backward of n_img images
+    of one replica, and the parameter-server update of the same share
+    (n_img / (R * batch)) of the parameter vector over R buffers."""
+    import synth
+    c, h, w = arch["input"]
+    x = synth.images_nhwc(3, f"cpu{tag}", n_img, c, h, w)
+    if layers[0].kind == "fc":
+        x = x.reshape(n_img, -1)
+    y = synth.labels(3, f"cpuy{tag}", n_img, layers[-1].cout)
+    n_upd = max(1, int(round(w0.size * frac_update)))
+    t0 = time.perf_counter()
+    _, grads = O.gradient(layers, w0, x, y)
+    g = np.asarray(grads, np.float64)[:n_upd]
+    O.apply_update(w0[:n_upd], [g] * R, optimizer=opt["optimizer"], eta=opt["eta"],
+                   state=O.initial_state(opt["optimizer"], n_upd))
+    return time.perf_counter() - t0
+
+
+def oracle_rate(cfg, budget_s):
+    """Images/s of the FP64 oracle's training step on bounded samples at the
+    workload's full layer sizes (forward + backward of a few images of one
+    replica plus the same share of the update), over about budget_s seconds."""
     import oracle as O
     import synth
     arch = O.ARCHS[cfg["net"]]
     layers = O.build_layers(arch)
-    c, h, w = arch["input"]
     w0 = np.concatenate([np.concatenate([synth.normal(7, f"w{i}", (int(np.prod(L.w_shape)),), O.he_std(L)),
                                          np.zeros(L.cout, np.float32)]) for i, L in enumerate(layers)]).astype(np.float64)
-    n = 2
-    done, elapsed = 0, 0.0
+    opt = dict(optimizer=cfg["optimizer"], eta=cfg["eta"])
+    per_step = cfg["replicas"] * cfg["batch"]
+    _oracle_sample_step(O, layers, w0, 1, 1 / per_step, cfg["replicas"], opt, arch, "warm")   # page faults
+    n, done, elapsed = 1, 0, 0.0
     while True:
-        x = synth.images_nhwc(3, f"cpu{n}", n, c, h, w)
-        if layers[0].kind == "fc":
-            x = x.reshape(n, -1)
-        y = synth.labels(3, f"cpuy{n}", n, layers[-1].cout)
-        t0 = time.perf_counter()
-        O.gradient(layers, w0, x, y)
-        dt = time.perf_counter() - t0
+        dt = _oracle_sample_step(O, layers, w0, n, n / per_step, cfg["replicas"], opt, arch, f"{n}.{done}")
         done += n
         elapsed += dt
         if elapsed >= budget_s or dt * 4 + elapsed > budget_s * 2:
             break
         n = min(n * 2, cfg["batch"])
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return done / elapsed, cores, f"{done} images of one replica's forward+backward at full layer sizes ({elapsed:.1f} s)"
+    return done / elapsed, done, elapsed
+
+
+def host_threads():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def oracle_rate_one_thread(config, budget_s):
+    """The same rate with the numpy BLAS limited to one thread (a child process:
+    the thread count is fixed when numpy's BLAS is loaded)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-rate", config, str(budget_s)],
+                           env=env, capture_output=True, text=True, timeout=budget_s * 6 + 60)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return d
+    except Exception as e:   # reported, never fatal
+        return {"error": str(e)[:200]}
+
+
+def cpu_baseline(cfg, config_name, budget_s=10.0):
+    rate, done, elapsed = oracle_rate(cfg, budget_s)
+    one = oracle_rate_one_thread(config_name, budget_s * 0.6)
+    return {"value": round(rate, 3), "unit": "images/s", "cores": host_threads(), "kind": "oracle",
+            "sample": f"{done} images of one replica's forward + backward at full layer sizes, plus the matching "
+                      f"share of the update ({elapsed:.1f} s)",
+            "one_thread": ({"value": round(one["rate"], 3), "unit": "images/s", "cores": 1,
+                            "sample": f"{one['images']} images ({one['seconds']:.1f} s)"} if "rate" in one else one)}
+
+
+REF_IMAGES = {"tiny": 8, "smlps": 256, "vgg_c": 8, "vgg_i": 1}
+
+
+def run_reference(args, cfg, config_name):
+    """The reference arm: the FP64 oracle as it stands, W warm-up and K timed
+    steps, each a bounded sample of the workload (a few images of one replica's
+    forward + backward and the matching share of the update)."""
+    import oracle as O
+    import synth
+    if config_name == "ps":
+        return run_reference_ps(args, cfg)
+    arch = O.ARCHS[cfg["net"]]
+    layers = O.build_layers(arch)
+    w0 = np.concatenate([np.concatenate([synth.normal(7, f"w{i}", (int(np.prod(L.w_shape)),), O.he_std(L)),
+                                         np.zeros(L.cout, np.float32)]) for i, L in enumerate(layers)]).astype(np.float64)
+    opt = dict(optimizer=cfg["optimizer"], eta=cfg["eta"])
+    per_step = cfg["replicas"] * cfg["batch"]
+    # images per sample step, fixed per workload (about 0.5-3 s of oracle work on 16
+    # host cores): the oracle has a fixed cost per call (it converts and copies every
+    # parameter), so an MLP sample needs many images to time the per-image work
+    n = min(cfg["batch"], REF_IMAGES.get(cfg["net"], 1))
+    _oracle_sample_step(O, layers, w0, 1, 1 / per_step, cfg["replicas"], opt, arch, "c0")   # page faults
+    for i in range(args.warmup):
+        _oracle_sample_step(O, layers, w0, n, n / per_step, cfg["replicas"], opt, arch, f"w{i}")
+    times = [_oracle_sample_step(O, layers, w0, n, n / per_step, cfg["replicas"], opt, arch, f"s{i}")
+             for i in range(args.steps)]
+    total = float(sum(times))
+    rate = n * args.steps / total
+    sample = (f"each step: {n} image(s) of one replica's forward + backward at full layer sizes plus "
+              f"{n}/{per_step} of the parameter-server update ({args.steps} steps, {total:.1f} s)")
+    return {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "images/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 1),
+            "images_per_step": n, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg["desc"], "global_batch": per_step,
+                                            "replicas_per_gpu": cfg["replicas"], "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(rate, 3), "unit": "images/s", "cores": host_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(rate, 3), "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- parameter-server update sweep
+
+PS_SIZES = (1_000_000, 16_000_000, 138_000_000)
+PS_KS = (1, 2, 4, 8, 16)
+PS_OPTS = ("sgd", "momentum", "adagrad")
+
+
+def ps_bytes(opt, k, n):
+    """Algorithmic bytes of one apply: k buffers and W read, W' written, plus the
+    optimizer state read and written (momentum's v, Adagrad's G)."""
+    return (4.0 * k + 8.0 + (8.0 if opt != "sgd" else 0.0)) * n
+
+
+def run_ps(args, world, rank, local_rank):
+    """Times sprint_apply_update over the sweep: W ~ N(0, 0.01^2), buffers ~ N(0,
+    1e-6), per point W warm-up and K timed launches, each timed alone (events on
+    the launching stream) after a 256 MB write that evicts L2."""
+    import torch
+
+    from stale_weight_sgd_gb300 import sprint as S
+    S.lib()
+    torch.cuda.set_device(local_rank)
+    st = torch.cuda.Stream()
+    torch.cuda.set_stream(st)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17 + rank)
+    nmax, kmax = max(PS_SIZES), max(PS_KS)
+    W = torch.randn(nmax, generator=g, device="cuda") * 0.01
+    Wout = torch.empty(nmax, device="cuda")
+    bufs = [torch.randn(nmax, generator=g, device="cuda") * 1e-3 for _ in range(kmax)]
+    state = torch.empty(nmax, device="cuda")
+    flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
+    hp = {"sgd": 0.0, "momentum": 0.9, "adagrad": 1e-8}
+    peaks, src = load_peaks()
+    points = []
+    barrier(world)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    launches0 = S.sprint_launch_count()
+    tot_bytes, tot_ms = 0.0, 0.0
+    for n in PS_SIZES:
+        for k in PS_KS:
+            for opt in PS_OPTS:
+                state[:n].fill_(0.1 if opt == "adagrad" else 0.0)
+                ms_l = []
+                for i in range(args.warmup + args.steps):
+                    flush.zero_()
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(st)
+                    S.sprint_apply_update(opt, W, Wout, state if opt != "sgd" else None, bufs[:k], n, 0.01, hp[opt],
+                                          0.0, st)
+                    e.record(st)
+                    if i >= args.warmup:
+                        ms_l.append((a, e))
+                torch.cuda.synchronize()
+                ms = float(np.mean([a.elapsed_time(e) for a, e in ms_l]))
+                b = ps_bytes(opt, k, n)
+                gbs = b / (ms / 1e3) / 1e9
+                tot_bytes += b * args.steps
+                tot_ms += ms * args.steps
+                points.append({"n": n, "k": k, "opt": opt, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                               "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+    clk = clocks.stop()
+    launches = S.sprint_launch_count() - launches0
+    big = [p for p in points if p["n"] >= 16_000_000]
+    value = tot_bytes / (tot_ms / 1e3) / 1e9
+    return {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.01^2) W, "
+            "N(0,1e-6) buffers)",
+            "config": {"workload": CONFIGS["ps"]["desc"], "l2": "a 256 MB write evicts L2 before every timed launch",
+                       "value": "all points' algorithmic bytes over their summed launch times"},
+            "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(value / peaks["hbm_gbs"], 4), "traffic": None,
+                         "kernel": "update_kernel (all points)", "peak_source": f"{src}: hbm copy",
+                         "frac_min_n_ge_16M": min(p["frac_hbm"] for p in big),
+                         "frac_median_n_ge_16M": float(np.median([p["frac_hbm"] for p in big]))},
+            "sweep": points, "gpu_launches": int(launches), "clocks": clk}
+
+
+def run_reference_ps(args, cfg):
+    """The reference arm of the update sweep: the oracle's SGD apply over k = 4
+    buffers on a 1M-element sample, W warm-up and K timed steps."""
+    import oracle as O
+    n, k = 1_000_000, 4
+    rng = np.random.default_rng(3)
+    w = rng.normal(0, 0.01, n)
+    bufs = [rng.normal(0, 1e-3, n) for _ in range(k)]
+    for _ in range(args.warmup):
+        O.apply_update(w, bufs, optimizer="sgd", eta=0.01)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.apply_update(w, bufs, optimizer="sgd", eta=0.01)
+    dt = time.perf_counter() - t0
+    gbs = ps_bytes("sgd", k, n) * args.steps / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["desc"]},
+            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+                             "sample": f"SGD apply, n = 1M, k = 4 (of the sweep), {args.steps} steps"},
+            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 KERNELS = {
@@ -379,6 +764,11 @@ KERNELS = {
     "update_momentum": "parameter-server momentum apply, n = 16M, k = 4 buffers",
     "update_nesterov_wd": "parameter-server Nesterov apply with weight decay, n = 16M, k = 4 buffers",
     "update_t_sgd": "parameter-server SGD apply writing W' and W'^T, 5000 x 5000 (+ bias), k = 4 buffers",
+    "pool_fwd": "2x2 max-pool forward with argmax, VGG-I pool1 64x224x224x64 -> 112x112",
+    "pool_bwd": "max-pool backward routed by argmax with the ReLU mask, VGG-I pool1 shape",
+    "softmax_xent": "softmax cross-entropy (loss + dlogits) of 8 replicas x 64 x 1000 classes",
+    "transpose": "2-D transpose [16*56*56][256] -> [256][16*56*56] (the bytes of one conv weight-gradient operand "
+                 "re-layout at the VGG conv3_2 shape, batch 16)",
 }
 
 
@@ -477,6 +867,38 @@ def run_kernel(args):
             fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, y, Nb, H, W, C, C, 1, ws, nbytes)
         else:
             fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
+    elif k in ("pool_fwd", "pool_bwd"):
+        Nb, H, W, C = 64, 224, 224, 64
+        x = rnd(Nb, H, W, C).relu_()
+        y = torch.empty(Nb, H // 2, W // 2, C, device="cuda")
+        arg = torch.empty(Nb, H // 2, W // 2, C, dtype=torch.uint8, device="cuda")
+        S.sprint_pool_fwd(x, y, arg, Nb, H, W, C)
+        big, small = 4.0 * Nb * H * W * C, 4.0 * Nb * (H // 2) * (W // 2) * C
+        if k == "pool_fwd":   # reads x, writes y and the uint8 argmax
+            fn = lambda i: S.sprint_pool_fwd(x, y, arg, Nb, H, W, C)
+            work = big + small + small / 4
+        else:                 # reads dy, argmax and the pooled output (ReLU mask), writes dx
+            dy = rnd(Nb, H // 2, W // 2, C)
+            dx = torch.empty_like(x)
+            fn = lambda i: S.sprint_pool_bwd(dy, arg, y, dx, Nb, H, W, C)
+            work = big + 2 * small + small / 4
+        unit = "GB/s"
+    elif k == "softmax_xent":
+        R, Nb, C = 8, 64, 1000
+        z = [rnd(Nb, C) for _ in range(R)]
+        lab = [torch.randint(0, C, (Nb,), generator=g, device="cuda", dtype=torch.int32) for _ in range(R)]
+        loss = [torch.empty(4, device="cuda") for _ in range(R)]
+        dz = [torch.empty(Nb, C, device="cuda") for _ in range(R)]
+        fn = lambda i: S.sprint_softmax_xent_batched(z, lab, loss, dz, Nb, C)
+        work = R * (8.0 * Nb * C + 4.0 * Nb)
+        unit = "GB/s"
+    elif k == "transpose":
+        rows, cols = 16 * 56 * 56, 256
+        src = [rnd(rows, cols) for _ in range(2)]     # two sources: > L2 between launches
+        dst = torch.empty(cols, rows, device="cuda")
+        fn = lambda i: S.sprint_transpose(src[i % 2], dst, rows, cols)
+        work = 8.0 * rows * cols
+        unit = "GB/s"
     else:
         n = 16_000_000
         kb = 16 if k == "update_sgd" else 4
@@ -676,15 +1098,22 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(CONFIGS), default="smlps")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-breakdown", action="store_true", help="skip the serial per-role breakdown step")
     ap.add_argument("--serial", action="store_true",
                     help="issue everything on one stream (no update overlap, no side-by-side replica convolutions)")
     ap.add_argument("--kernel", choices=sorted(KERNELS), default=None,
                     help="time one hot kernel at a workload shape instead of the training step")
     ap.add_argument("--cost-model", action="store_true",
                     help="refit the SPRINT report's SGEMM cost model to this GPU and check its T_GPU prediction")
+    ap.add_argument("--oracle-rate", nargs=2, metavar=("CONFIG", "SECONDS"), default=None,
+                    help=argparse.SUPPRESS)   # child process of the one-thread oracle timing
     args = ap.parse_args(argv)
+    if args.oracle_rate:
+        rate, done, elapsed = oracle_rate(CONFIGS[args.oracle_rate[0]], float(args.oracle_rate[1]))
+        print(json.dumps({"rate": rate, "images": done, "seconds": elapsed}))
+        return 0
     if args.kernel:
         return run_kernel(args)
     if args.cost_model:
@@ -697,26 +1126,17 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        rate, cores, sample = cpu_oracle_rate(cfg, budget_s=8.0)
-        step_imgs = cfg["replicas"] * cfg["batch"]
-        out = {"impl": "reference", "metric": "CNN train images/s on 1 GB300; conv-GEMM % TF32 peak; update GB/s vs HBM peak",
-               "value": round(rate, 3), "unit": "images/s", "n_gpus": args.gpus, "steps": args.steps,
-               "warmup": args.warmup, "ms_per_step": round(step_imgs / rate * 1e3, 1), "higher_is_better": True,
-               "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-               "config": {"workload": cfg["desc"], "global_batch": step_imgs},
-               "cpu_baseline": {"value": round(rate, 3), "unit": "images/s", "cores": cores, "kind": "oracle",
-                                "sample": sample},
-               "e2e": {"value": round(rate, 3), "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(out))
+        print(json.dumps(run_reference(args, cfg, args.config)))
         return 0
 
     init_dist(world, local_rank)
-    out = run_ours(args, cfg, rank, world, local_rank)
+    if args.config == "ps":
+        out = run_ps(args, world, rank, local_rank)
+    else:
+        out = run_ours(args, cfg, rank, world, local_rank)
+        if rank == 0 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(cfg, args.config)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            rate, cores, sample = cpu_oracle_rate(cfg)
-            out["cpu_baseline"] = {"value": round(rate, 3), "unit": "images/s", "cores": cores, "kind": "oracle",
-                                   "sample": sample}
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist

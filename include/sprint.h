@@ -76,6 +76,42 @@ uint64_t sprint_launch_count(void);
  * was set, SPRINT_OK otherwise. */
 int sprint_device_status(int* flags_out, int reset);
 
+/* Plan queries (no page counterpart; for tests and tuning): how the library
+ * would run a call, without running it. out[0 .. SPRINT_PLAN_FIELDS-1] (host):
+ *   [0] path: SPRINT_PATH_TC (tcgen05 implicit GEMM / weight-gradient GEMM),
+ *       SPRINT_PATH_SMALLC (direct CUDA-core kernel for <= 4 input channels),
+ *       SPRINT_PATH_IM2COL (padded explicit im2col + tensor-core GEMM),
+ *       SPRINT_PATH_SIMT (CUDA-core fallback)
+ *   [1] tile width BN   [2] CTA pair (1) or single CTA (0)
+ *   [3] split-K count of the weight gradient (1: none)
+ *   [4] k-ranges of the last, partial round's tiles (1: no tail split; it is
+ *       used only when the workspace holds its slabs)
+ *   [5] taps per n-tile of the weight gradient (0: one tap per tile)
+ *   [6] channel rows per packed tap   [7] k-tiles of 32 in the reduction
+ *   [8..10] output-pixel box of the implicit GEMM (w, h, images)
+ * Returns SPRINT_ERR_SHAPE / SPRINT_ERR_INVALID_ARG like the calls they
+ * describe. sprint_conv_plan: op, shape and have_wT as for the conv calls.
+ * sprint_gemm_plan: the grouped tensor-core GEMM D[M][N] = A[M][K] B[N][K]^T
+ * over `batch` problems (the batched FC calls), allow_tail as when the
+ * workspace holds the tail slabs. */
+#define SPRINT_PLAN_FIELDS 11
+#define SPRINT_PATH_SIMT 0
+#define SPRINT_PATH_TC 1
+#define SPRINT_PATH_SMALLC 2
+#define SPRINT_PATH_IM2COL 3
+int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, int pad, int have_wT, int32_t* out, int n_out);
+int sprint_gemm_plan(int M, int N, int K, int batch, int allow_tail, int32_t* out, int n_out);
+
+/* Self-test of the failure path above (no page counterpart): launches one
+ * block on `stream` whose thread waits, with the same bounded wait the
+ * pipelined kernels use, on an mbarrier phase that nothing ever completes (no
+ * copy or MMA is in flight). After limit_ns nanoseconds of wall time the wait
+ * gives up, ORs 8 into the device status word and the kernel returns, so the
+ * context stays usable; sprint_device_status then reports
+ * SPRINT_ERR_DEVICE_FLAG with bit 8 set. limit_ns in [1e3, 1e10], else
+ * SPRINT_ERR_INVALID_ARG. */
+int sprint_selftest_bounded_wait(uint64_t limit_ns, sprint_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * im2col — the explicit unrolling of [S] Sec. 3.3, Eq. (5): rows x_l^2 * N,
  * columns c^2 * m_{l-1}.
@@ -188,9 +224,11 @@ size_t sprint_fc_workspace_size(int N, int in, int out, int have_wT);
  *    shape whose sprint_fc_workspace_size(N, in, out, wT != NULL || dx == NULL)
  *    exceeds it is rejected with SPRINT_ERR_WORKSPACE before any launch.
  *  - The array is held by every GPU that loads the library until the process
- *    exits. The first call on a device looks up the array's device address on
- *    that device (cudaGetSymbolAddress) and caches it; make that first call
- *    before any stream capture.
+ *    exits. The first call in a CUDA context looks up the array's device
+ *    address there (cudaGetSymbolAddress) and caches it under the context's
+ *    unique ID; make that first call before any stream capture. A context
+ *    created later on the device (e.g. after cudaDeviceReset) gets its own
+ *    lookup on its first call, which should also precede any capture.
  *  - No cudaMalloc, cudaFree or other allocating routine is called.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero (each call writes what it reads).

@@ -38,6 +38,7 @@ enum : int {
     DEV_FLAG_WAIT_PRODUCER = 1,   // TMA producer gave up waiting for a free stage
     DEV_FLAG_WAIT_MMA = 2,        // MMA issuer gave up waiting for a loaded stage
     DEV_FLAG_WAIT_EPILOGUE = 4,   // epilogue gave up waiting for the accumulator
+    DEV_FLAG_WAIT_SELFTEST = 8,   // sprint_selftest_bounded_wait's wait ran out (as it should)
 };
 
 // largest number of problems one grouped launch takes (batched entry points

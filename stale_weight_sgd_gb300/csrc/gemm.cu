@@ -2282,3 +2282,47 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
     if (db && !db_done) return launch_colsum(dy, P, Cout, pl.ws_colsum ? csum : nullptr, db, alpha, accumulate, s);
     return SPRINT_OK;
 }
+
+// ====================================================================== plan queries
+extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, int pad, int have_wT, int32_t* out,
+                                int n_out) {
+    SPRINT_REQUIRE(op >= SPRINT_CONV_FWD && op <= SPRINT_CONV_DW, SPRINT_ERR_INVALID_ARG, "%s: bad op %d", __func__, op);
+    int rc = check_conv_shape(__func__, N, H, W, Cin, Cout, pad);
+    if (rc) return rc;
+    SPRINT_NONNULL(out, "out");
+    SPRINT_REQUIRE(n_out >= SPRINT_PLAN_FIELDS, SPRINT_ERR_INVALID_ARG, "%s: out holds %d fields, need %d", __func__,
+                   n_out, SPRINT_PLAN_FIELDS);
+    const ConvPlan pl = plan_conv(op, N, H, W, Cin, Cout, pad, have_wT != 0);
+    for (int i = 0; i < n_out; ++i) out[i] = 0;
+    out[0] = pl.smallc ? SPRINT_PATH_SMALLC : (pl.im2col ? SPRINT_PATH_IM2COL : (pl.tc ? SPRINT_PATH_TC : SPRINT_PATH_SIMT));
+    out[1] = pl.tile.bn;
+    out[2] = pl.tile.pair ? 1 : 0;
+    out[3] = pl.splits;
+    out[4] = pl.gp.tail_splits;
+    out[5] = pl.wg_tpt;
+    out[6] = pl.wg_rows;
+    out[7] = pl.num_kt;
+    out[8] = pl.box.bw;
+    out[9] = pl.box.bh;
+    out[10] = pl.box.bimg;
+    return SPRINT_OK;
+}
+
+extern "C" int sprint_gemm_plan(int M, int N, int K, int batch, int allow_tail, int32_t* out, int n_out) {
+    SPRINT_REQUIRE(M >= 1 && N >= 1 && K >= 1 && batch >= 1, SPRINT_ERR_SHAPE, "%s: need M, N, K, batch >= 1", __func__);
+    SPRINT_NONNULL(out, "out");
+    SPRINT_REQUIRE(n_out >= SPRINT_PLAN_FIELDS, SPRINT_ERR_INVALID_ARG, "%s: out holds %d fields, need %d", __func__,
+                   n_out, SPRINT_PLAN_FIELDS);
+    const long long m_tiles = (M + TC_BM - 1) / TC_BM;
+    const int per_launch = batch < kMaxGroup ? batch : kMaxGroup;
+    const GemmPlan plan =
+        plan_gemm(m_tiles, N, per_launch, N >= 256 ? 256 : (N >= 128 ? 128 : 64), (K + TC_BK - 1) / TC_BK, allow_tail != 0);
+    for (int i = 0; i < n_out; ++i) out[i] = 0;
+    out[0] = SPRINT_PATH_TC;
+    out[1] = plan.tile.bn;
+    out[2] = plan.tile.pair ? 1 : 0;
+    out[3] = 1;
+    out[4] = plan.tail_splits;
+    out[7] = (K + TC_BK - 1) / TC_BK;
+    return SPRINT_OK;
+}

@@ -96,6 +96,33 @@ extern "C" int sprint_device_status(int* flags_out, int reset) {
     return SPRINT_OK;
 }
 
+// One thread waits, with the library's bounded wait, on an mbarrier phase that
+// nothing completes (no arrival, no copy, no MMA in flight): the wait gives up
+// after limit_ns and sets DEV_FLAG_WAIT_SELFTEST in the status word, and the
+// kernel returns. Exercises the failure path every pipelined kernel relies on.
+namespace sprint {
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, status, DEV_FLAG_WAIT_SELFTEST, limit_ns);
+    __syncthreads();
+}
+}  // namespace sprint
+
+extern "C" int sprint_selftest_bounded_wait(uint64_t limit_ns, sprint_stream_t stream) {
+    SPRINT_REQUIRE(limit_ns >= 1000 && limit_ns <= 10000000000ull, SPRINT_ERR_INVALID_ARG,
+                   "sprint_selftest_bounded_wait: limit_ns must be in [1e3, 1e10] (got %llu)",
+                   static_cast<unsigned long long>(limit_ns));
+    int* st = device_status_ptr();
+    SPRINT_REQUIRE(st != nullptr, SPRINT_ERR_CUDA, "sprint_selftest_bounded_wait: no device status word");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st, static_cast<unsigned long long>(limit_ns));
+    return check_launch("selftest_wait_kernel");
+}
+
 // SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): the state advances by the
 // golden-ratio gamma, and each output is the state passed through the mix.
 static inline uint64_t splitmix64_output(uint64_t seed, uint64_t index) {

@@ -11,9 +11,12 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its kScratchBytes until the process exits. Host code cannot use
-// the array's name as a device pointer, so the first call on each device looks
-// up its device address (cudaGetSymbolAddress, with that device current) and
-// caches it; later calls reuse the cached address.
+// the array's name as a device pointer, so the first call in each CUDA context
+// looks up the array's device address there (cudaGetSymbolAddress, with that
+// context's device current) and caches it with the context's unique ID. A
+// context created later on the same device (after cudaDeviceReset, say) has a
+// new ID and may hold the array at another address, so its first call looks
+// the address up again instead of reusing a stale one.
 #include <mutex>
 
 #include "common.cuh"
@@ -26,23 +29,68 @@ constexpr size_t kScratchBytes = static_cast<size_t>(24) << 20;  // 24 MiB per d
 static __device__ __align__(256) unsigned char g_fc_bwd_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {nullptr};
+struct ScratchSlot {
+    unsigned long long ctx_id;   // unique ID of the context the address belongs to (0: none yet)
+    void* addr;
+};
+ScratchSlot g_scratch[64] = {};
 
-// Device address of g_fc_bwd_scratch on the current device (looked up once).
+// cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points (no
+// link against libcuda); null if the driver lacks them
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+void ctx_fns(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
+    static CtxGetCurrentFn f_cur = nullptr;
+    static CtxGetIdFn f_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    *cur = f_cur;
+    *id = f_id;
+}
+
+// Device address of g_fc_bwd_scratch in the current context (looked up once per context).
 int scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(SPRINT_ERR_CUDA, "sprint_fc_bwd_static_scratch: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(SPRINT_ERR_UNSUPPORTED, "sprint_fc_bwd_static_scratch: device %d out of range", dev);
+    CtxGetCurrentFn get_cur;
+    CtxGetIdFn get_id;
+    ctx_fns(&get_cur, &get_id);
+    if (!get_cur || !get_id)
+        return fail(SPRINT_ERR_CUDA, "sprint_fc_bwd_static_scratch: driver lacks cuCtxGetCurrent / cuCtxGetId");
+    CUcontext ctx = nullptr;
+    if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) {
+        // no context current yet: the runtime sets up the device's primary context on this lookup
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fc_bwd_scratch);
+        if (e != cudaSuccess || get_cur(&ctx) != CUDA_SUCCESS || !ctx)
+            return fail(SPRINT_ERR_CUDA, "sprint_fc_bwd_static_scratch: no CUDA context on device %d", dev);
+    }
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS || id == 0)
+        return fail(SPRINT_ERR_CUDA, "sprint_fc_bwd_static_scratch: cannot identify the current CUDA context");
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchSlot& slot = g_scratch[dev];
+    if (slot.ctx_id != id || !slot.addr) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_fc_bwd_scratch);
         if (e != cudaSuccess || !p)
             return fail(SPRINT_ERR_CUDA, "sprint_fc_bwd_static_scratch: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        slot.ctx_id = id;
+        slot.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return SPRINT_OK;
 }
 

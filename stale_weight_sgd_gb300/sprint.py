@@ -42,6 +42,9 @@ _SIGS = {
     "sprint_version": ([], I),
     "sprint_launch_count": ([], ctypes.c_uint64),
     "sprint_device_status": ([ctypes.POINTER(I), I], I),
+    "sprint_selftest_bounded_wait": ([ctypes.c_uint64, P], I),
+    "sprint_conv_plan": ([I, I, I, I, I, I, I, I, P, I], I),
+    "sprint_gemm_plan": ([I, I, I, I, I, P, I], I),
     "sprint_im2col": ([P, I, I, I, I, I, P, P, P], I),
     "sprint_conv_fwd": ([P, P, P, P, I, I, I, I, I, I, I, P, SZ, P], I),
     "sprint_conv_dX": ([P, P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
@@ -128,6 +131,31 @@ def sprint_version() -> int:
 
 def sprint_launch_count() -> int:
     return int(lib().sprint_launch_count())
+
+
+PLAN_FIELDS = ("path", "bn", "pair", "splits", "tail_splits", "wg_tpt", "wg_rows", "num_kt", "box_w", "box_h",
+               "box_img")
+PATH_NAMES = {0: "simt", 1: "tc", 2: "smallc", 3: "im2col"}
+
+
+def _plan(name, *args):
+    buf = (ctypes.c_int32 * len(PLAN_FIELDS))()
+    _check(name, getattr(lib(), name)(*args, ctypes.cast(buf, P), len(PLAN_FIELDS)))
+    d = dict(zip(PLAN_FIELDS, list(buf)))
+    d["path"] = PATH_NAMES[d["path"]]
+    return d
+
+
+def sprint_conv_plan(op, N, H, W, Cin, Cout, pad=1, have_wT=True) -> dict:
+    return _plan("sprint_conv_plan", op, N, H, W, Cin, Cout, pad, int(bool(have_wT)))
+
+
+def sprint_gemm_plan(M, N, K, batch=1, allow_tail=True) -> dict:
+    return _plan("sprint_gemm_plan", M, N, K, batch, int(bool(allow_tail)))
+
+
+def sprint_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    _check("sprint_selftest_bounded_wait", lib().sprint_selftest_bounded_wait(int(limit_ns), _s(stream)))
 
 
 def sprint_device_status(reset: bool = True) -> int:

@@ -180,6 +180,7 @@ class StaleSGD:
         self.graph_launch_adjust = 0  # kernels replayed minus kernels counted while capturing
         self.ev_graph_upd = torch.cuda.Event()
         self._cap_stream = None
+        self.span_hook = None   # optional timing hook around each layer's per-replica convolution group
 
     # ------------------------------------------------------------------ buffers
     def _alloc_acts(self):
@@ -369,23 +370,30 @@ class StaleSGD:
         S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh, n_total=cnt,
                                 weight_decay=self.weight_decay)
 
-    def _per_replica(self, fn):
+    def _per_replica(self, fn, tag=None):
         """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica
         streams (forked from and joined back into the main stream) or in order
-        on the main stream."""
+        on the main stream. If span_hook is set, it is called with (tag, 0,
+        main stream) before the group and (tag, 1, main stream) after it has
+        joined, so events it records there bracket the whole group."""
         main = self.main_stream
+        hook = self.span_hook if tag is not None else None
+        if hook:
+            hook(tag, 0, main)
         if not self.fork:
             for r in range(self.R):
                 fn(r, main.cuda_stream, self.ws, self.ws_bytes)
-            return
-        self.ev_fork.record(main)
-        for r in range(self.R):
-            st = self.rep_streams[r]
-            st.wait_event(self.ev_fork)
-            fn(r, st.cuda_stream, self.rep_ws[r], self.rep_ws[r].numel() * 4)
-            self.ev_join[r].record(st)
-        for r in range(self.R):
-            main.wait_event(self.ev_join[r])
+        else:
+            self.ev_fork.record(main)
+            for r in range(self.R):
+                st = self.rep_streams[r]
+                st.wait_event(self.ev_fork)
+                fn(r, st.cuda_stream, self.rep_ws[r], self.rep_ws[r].numel() * 4)
+                self.ev_join[r].record(st)
+            for r in range(self.R):
+                main.wait_event(self.ev_join[r])
+        if hook:
+            hook(tag, 1, main)
 
     def _graph_key(self, t):
         """Everything a captured step bakes in: weight slots, GradBuf parity, batches."""
@@ -504,7 +512,7 @@ class StaleSGD:
                                       rwsb, st)
                     if L.pool:
                         S.sprint_pool_fwd(outs[r], self.pooled[li][r], self.argmax[li][r], N, L.h, L.w, L.cout, st)
-                self._per_replica(fwd)
+                self._per_replica(fwd, ("fwd", li))
                 cur = [self.pooled[li][r].data_ptr() for r in range(R)] if L.pool else outs
             else:
                 yT = None if self.outsT[li] is None else [self.outsT[li][r].data_ptr() for r in range(R)]
@@ -553,7 +561,7 @@ class StaleSGD:
                             # g[r] (free) <- routed gradient of the pre-pool ReLU output, masked
                             S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], g[r], N, prev.h,
                                               prev.w, prev.cout, st)
-                self._per_replica(bwd)
+                self._per_replica(bwd, ("bwd", li))
             # layer li's gradients are final: its update overlaps the layers below
             if self._pushes(t):
                 self.ev_bwd[li].record(main)

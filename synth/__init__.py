@@ -30,6 +30,7 @@ __all__ = [
     "images_nhwc",
     "dyadic",
     "batch_pool",
+    "device_normal",
 ]
 
 
@@ -78,3 +79,16 @@ def batch_pool(seed: int, count: int, n: int, c: int, h: int, w: int, classes: i
             x = x.reshape(n, -1)
         out.append((x, labels(seed, f"y/{j}", n, classes)))
     return out
+
+
+def device_normal(seed: int, tag: str, shape, std: float = 1.0, device="cuda"):
+    """N(0, std^2) fp32 samples drawn on a GPU by a torch generator keyed by
+    (seed, tag): the large full-size tensors (hundreds of MB) of the parity
+    tests, which both sides then read from the same device buffer."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) * 1000003 + zlib.crc32(tag.encode("utf-8"))) & 0x7FFFFFFFFFFFFFFF)
+    t = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t

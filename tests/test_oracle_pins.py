@@ -551,3 +551,42 @@ def test_fetch_slower_than_push_uses_stale_local_copies():
         g = O.gradient(layers, local, *b[t % len(b)])[1]
         w = w - 0.01 * g
     np.testing.assert_allclose(f[1], w, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- training FLOPs per image
+
+def _flops_by_sgemm_roles(arch):
+    """2*m*n*k summed over the SGEMM roles of the SPRINT report's Sec. 3.3 table
+    for one image (N = 1): convolution / fc, dedw (+ dedb as the k-sum, not a
+    GEMM), dedx (none for the first layer)."""
+    total = 0
+    for i, L in enumerate(O.build_layers(arch)):
+        if L.kind == "conv":
+            x2 = L.h * L.w
+            roles = [(x2, L.cout, 9 * L.cin),           # convolution
+                     (9 * L.cin, L.cout, x2)]           # dedw
+            if i > 0:
+                roles.append((x2, 9 * L.cin, L.cout))   # dedx conv (col2im of dY . W)
+        else:
+            roles = [(1, L.cout, L.cin), (L.cin, L.cout, 1)]
+            if i > 0:
+                roles.append((1, L.cin, L.cout))
+        total += sum(2 * m * n * k for m, n, k in roles)
+    return total
+
+
+def test_flops_per_image_pinned():
+    # tiny CNN by hand: conv1 32*32*16*27 MACs, conv2 16*16*32*144, fc 2048*10; the first layer has no dX
+    assert O.flops_per_image(O.ARCHS["tiny"]) == 2 * (2 * 442368 + 3 * 1179648 + 3 * 20480) == 8970240
+    # the per-image figures the workload table states (8.97 MFLOP, 0.662 / 1.879 / 92.65 GFLOP)
+    for name, stated in (("tiny", 8.97e6), ("smlps", 0.662e9), ("vgg_c", 1.879e9), ("vgg_i", 92.65e9)):
+        f = O.flops_per_image(O.ARCHS[name])
+        assert abs(f - stated) <= 1e-3 * stated, (name, f)
+        assert f == _flops_by_sgemm_roles(O.ARCHS[name]), name
+
+
+def test_product_flops_count_equals_oracle():
+    """The bench's achieved-FLOP/s denominators (product host code) count what the oracle counts."""
+    from stale_weight_sgd_gb300 import model
+    for name in ("tiny", "smlps", "vgg_c", "vgg_i"):
+        assert model.train_flops_per_image(model.NETWORKS[name]) == O.flops_per_image(O.ARCHS[name]), name

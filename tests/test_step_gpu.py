@@ -40,9 +40,10 @@ def _oracle_kw(kw, steps):
     return R, sched, okw
 
 
-def _run_gpu(arch, batch, steps, pool, seed, kw):
+def _run_gpu(arch, batch, steps, pool, seed, kw, keep_steps=None):
     """Free-running GPU training; returns per-step losses, the weight history
-    W(0..T) and the optimizer state before every step (dense, fp64)."""
+    W(0..T) and the optimizer state before every step (dense, fp64), and the
+    GradBufs and saved activations of every step (or only of keep_steps)."""
     from stale_weight_sgd_gb300.model import layer_shapes, unpack
     from stale_weight_sgd_gb300.trainer import StaleSGD
     w0 = _dense_init(arch, seed)
@@ -83,12 +84,14 @@ def _run_gpu(arch, batch, steps, pool, seed, kw):
         gl.append(tr.step_loss())
         hist.append(tr.weights(t + 1).astype(np.float64))
         states.append(state())
-        gbufs.append([unpack(shapes, tr.gradbuf[r].cpu().numpy()).astype(np.float64) for r in range(tr.R)])
-        saves.append([saved(t, r) for r in range(tr.R)])
+        keep = keep_steps is None or t in keep_steps
+        gbufs.append([unpack(shapes, tr.gradbuf[r].cpu().numpy()).astype(np.float64) for r in range(tr.R)]
+                     if keep else None)
+        saves.append([saved(t, r) for r in range(tr.R)] if keep else None)
     return np.array(gl), hist, states, batches, gbufs, saves
 
 
-def _check_step_local(arch, run, kw):
+def _check_step_local(arch, run, kw, check_steps=None):
     """Step-local, layer-local parity of every step against the oracle, on the
     GPU's own weight history:
       * forward: each layer's output vs the oracle layer applied to the GPU's
@@ -108,7 +111,7 @@ def _check_step_local(arch, run, kw):
     layers = O.build_layers(arch)
     offs, _ = O.param_offsets(layers)
     worst = dict(fwd=0.0, loss=0.0, loss_free=0.0, grad=0.0, update=0.0)
-    for t in range(steps):
+    for t in (range(steps) if check_steps is None else check_steps):
         lsum, lsum_free = 0.0, 0.0
         for r in range(R):
             params = O.replica_params(layers, hist, t, r, schedule=sched, **okw)
