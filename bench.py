@@ -831,7 +831,7 @@ def run_kernel(args):
             fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
             work, unit = 4.0 * M * N * K, "TFLOP/s"
     elif k in ("conv_dw_224x64", "conv_fwd_224x3", "conv_dw_224x3"):
-        Nb, H, W = 16, 224, 224
+        Nb, H, W = args.batch or 16, 224, 224
         Ci = 64 if k == "conv_dw_224x64" else 3
         Co = 64
         x = rnd(Nb, H, W, Ci).relu_()
@@ -849,7 +849,7 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
     elif k.startswith("conv"):
-        Nb, H, W, C = 16, 56, 56, 256
+        Nb, H, W, C = args.batch or 16, 56, 56, 256
         x = rnd(Nb, H, W, C).relu_()
         w = rnd(C, 3, 3, C, std=(2.0 / (9 * C)) ** 0.5)
         wT = w.reshape(C, 9 * C).t().contiguous()
@@ -894,9 +894,9 @@ def run_kernel(args):
         unit = "GB/s"
     elif k == "transpose":
         rows, cols = 16 * 56 * 56, 256
-        src = [rnd(rows, cols) for _ in range(2)]     # two sources: > L2 between launches
+        srcs = [rnd(rows, cols) for _ in range(2)]     # two sources: > L2 between launches
         dst = torch.empty(cols, rows, device="cuda")
-        fn = lambda i: S.sprint_transpose(src[i % 2], dst, rows, cols)
+        fn = lambda i: S.sprint_transpose(srcs[i % 2], dst, rows, cols)
         work = 8.0 * rows * cols
         unit = "GB/s"
     else:
@@ -942,7 +942,8 @@ def run_kernel(args):
     else:
         peak = peaks["hbm_gbs"]
         psrc = f"{src}: hbm copy"
-    print(json.dumps({"kernel": k, "workload": KERNELS[k], "ms": round(ms, 4), "achieved": round(achieved, 1),
+    print(json.dumps({"kernel": k, "workload": KERNELS[k] + (f" (batch {args.batch})" if args.batch else ""),
+                      "ms": round(ms, 4), "achieved": round(achieved, 1),
                       "unit": unit, "peak": round(peak, 1), "frac": round(achieved / peak, 4), "peak_source": psrc,
                       "flags": S.sprint_device_status()}))
     return 0
@@ -1105,6 +1106,8 @@ def main(argv=None):
                     help="issue everything on one stream (no update overlap, no side-by-side replica convolutions)")
     ap.add_argument("--kernel", choices=sorted(KERNELS), default=None,
                     help="time one hot kernel at a workload shape instead of the training step")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="--kernel conv_*: batch size in place of the case's 16")
     ap.add_argument("--cost-model", action="store_true",
                     help="refit the SPRINT report's SGEMM cost model to this GPU and check its T_GPU prediction")
     ap.add_argument("--oracle-rate", nargs=2, metavar=("CONFIG", "SECONDS"), default=None,

@@ -102,8 +102,8 @@ def test_plans_cover_every_kernel_path(S):
     dw = [p for (_, _, op), p in PLANS.items() if op == S.SPRINT_CONV_DW and p["path"] == "tc"]
     print("forward / input-gradient plans:", sorted({(p["bn"], p["pair"], p["tail_splits"]) for p in fwd_dx}))
     print("weight-gradient plans:", sorted({(p["bn"], p["pair"], p["splits"], p["wg_tpt"]) for p in dw}))
-    assert any(p["pair"] for p in fwd_dx) and any(not p["pair"] for p in fwd_dx)
-    assert any(p["tail_splits"] > 1 for p in fwd_dx)
+    assert any(p["pair"] for p in fwd_dx + dw) and any(not p["pair"] for p in fwd_dx + dw)
+    assert any(p["tail_splits"] > 1 for p in fwd_dx) and any(p["tail_splits"] == 1 for p in fwd_dx)
     assert any(p["splits"] > 1 for p in dw)
     assert any(p["wg_tpt"] > 0 for p in dw) and any(p["wg_tpt"] == 0 for p in dw)
     assert any(p["path"] == "smallc" for (_, _, op), p in PLANS.items())
