@@ -17,11 +17,11 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
                   cudaStream_t s);
 int colsum_chunks(long long rows, int cols);
 int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
-                     long long dc, cudaStream_t s);
+                     long long dc, cudaStream_t s, long long drt = 32);
 int launch_transpose_group(const float* const* src, float* const* dst, int G, int R, int C, cudaStream_t s);
 int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr,
                             long long db, long long dc, float* partial, float* out, float alpha, int accumulate,
-                            cudaStream_t s);
+                            cudaStream_t s, long long drt = 32);
 int launch_colsum_group(const float* const* in, float* const* out, int G, long long rows, int cols, float alpha,
                         int accumulate, cudaStream_t s);
 
@@ -1332,6 +1332,7 @@ struct ConvPlan {
     size_t ws_partial = 0;  // dedw: split-K partial sums (or the padded output of packed taps)
     size_t ws_colsum = 0;   // dedw: partial bias sums
     int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
+    bool wg_blocked = false;       // dedw copies blocked [H][W*N/32][C][32] (N % 32 == 0)
     GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
     size_t ws_tail = 0;            // fwd / dedx: slabs of that split (last in the workspace)
     size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad + ws_tail; }
@@ -1390,6 +1391,7 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     }
     pl.ws_xT = fbytes(static_cast<long long>(N) * H * W * Cin);
     pl.ws_dyT = fbytes(P * Cout);
+    pl.wg_blocked = N % 32 == 0;
     pl.box = PixBox{0, 0, 0, static_cast<int>((static_cast<long long>(Wo) * N + TC_BK - 1) / TC_BK), Ho, 1};
     pl.num_kt = pl.box.tw * Ho;   // per output row: ceil(Wo*N / 32) k-tiles
     const long long m_tiles = (Cout + TC_BM - 1) / TC_BM;
@@ -2175,29 +2177,46 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         return launch_conv_smallc_dw(x, dy, part, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, s);
     bool done = false, db_done = false;
     if (pl.tc) {
-        // x [N][H][W][Cin] -> x^T [Cin][H][W][N]; dy likewise (batch innermost, pixels = k)
-        if ((rc = launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin, N,
-                                   static_cast<long long>(H) * W * N, s)))
+        // x [N][H][W][Cin] -> x^T, dy likewise (pixels (h, w, n) = k, n fastest): blocked
+        // [H][W*N/32][C][32] when N % 32 == 0, else [C][H][W][N]
+        const bool blk = pl.wg_blocked;
+        const long long x_db = blk ? static_cast<long long>(N) * Cin : N;
+        const long long x_dc = blk ? 32 : static_cast<long long>(H) * W * N;
+        const long long y_db = blk ? static_cast<long long>(N) * Cout : N;
+        const long long y_dc = blk ? 32 : static_cast<long long>(Ho) * Wo * N;
+        if ((rc = launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin, x_db, x_dc, s,
+                                   blk ? 32ll * Cin : 32)))
             return rc;
         // dy -> dy^T, with dedb from the same pass when asked for
         if (db) {
             if ((rc = launch_transpose_colsum(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout,
-                                              N, static_cast<long long>(Ho) * Wo * N, csum, db, alpha, accumulate, s)))
+                                              y_db, y_dc, csum, db, alpha, accumulate, s, blk ? 32ll * Cout : 32)))
                 return rc;
             db_done = true;
-        } else if ((rc = launch_transpose(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout, N,
-                                          static_cast<long long>(Ho) * Wo * N, s))) {
+        } else if ((rc = launch_transpose(dy, dyT, Ho * Wo, N, Cout, Cout, static_cast<long long>(Ho) * Wo * Cout, y_db,
+                                          y_dc, s, blk ? 32ll * Cout : 32))) {
             return rc;
         }
         CUtensorMap ta, tb;
-        const uint64_t da[3] = {(uint64_t)Wo * N, (uint64_t)Ho, (uint64_t)Cout};
-        const uint64_t sa[2] = {(uint64_t)Wo * N * 4, (uint64_t)Ho * Wo * N * 4};
-        const uint64_t dbm[3] = {(uint64_t)W * N, (uint64_t)H, (uint64_t)Cin};
-        const uint64_t sbm[2] = {(uint64_t)W * N * 4, (uint64_t)H * W * N * 4};
-        const uint32_t ba[3] = {32, 1, 128};
         // packed taps: one box = one tap's wg_rows channel rows; else BN (or half) channel rows
-        const uint32_t bb[3] = {32, 1, pl.wg_tpt > 0 ? static_cast<uint32_t>(pl.wg_rows) : pl.tile.b_rows()};
-        if (make_tmap(&ta, dyT, 3, da, sa, ba) && make_tmap(&tb, xT, 3, dbm, sbm, bb)) {
+        const uint32_t b_rows = pl.wg_tpt > 0 ? static_cast<uint32_t>(pl.wg_rows) : pl.tile.b_rows();
+        bool maps_ok;
+        if (blk) {
+            const uint64_t da[4] = {32, (uint64_t)Cout, (uint64_t)Wo * N / 32, (uint64_t)Ho};
+            const uint64_t sa[3] = {128, (uint64_t)Cout * 128, (uint64_t)Wo * N / 32 * Cout * 128};
+            const uint64_t dbm[4] = {32, (uint64_t)Cin, (uint64_t)W * N / 32, (uint64_t)H};
+            const uint64_t sbm[3] = {128, (uint64_t)Cin * 128, (uint64_t)W * N / 32 * Cin * 128};
+            const uint32_t ba[4] = {32, 128, 1, 1}, bb[4] = {32, b_rows, 1, 1};
+            maps_ok = make_tmap(&ta, dyT, 4, da, sa, ba) && make_tmap(&tb, xT, 4, dbm, sbm, bb);
+        } else {
+            const uint64_t da[3] = {(uint64_t)Wo * N, (uint64_t)Ho, (uint64_t)Cout};
+            const uint64_t sa[2] = {(uint64_t)Wo * N * 4, (uint64_t)Ho * Wo * N * 4};
+            const uint64_t dbm[3] = {(uint64_t)W * N, (uint64_t)H, (uint64_t)Cin};
+            const uint64_t sbm[2] = {(uint64_t)W * N * 4, (uint64_t)H * W * N * 4};
+            const uint32_t ba[3] = {32, 1, 128}, bb[3] = {32, 1, b_rows};
+            maps_ok = make_tmap(&ta, dyT, 3, da, sa, ba) && make_tmap(&tb, xT, 3, dbm, sbm, bb);
+        }
+        if (maps_ok) {
             TcParams p = base_params();
             p.M = Cout;
             p.N = Cin;
@@ -2210,6 +2229,8 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
             p.pad = pad;
             p.tiles_w = pl.box.tw;
             p.tiles_h = pl.box.th;
+            p.wg_blocked = blk ? 1 : 0;
+            p.wg_cshift = N / 32;
             p.epi = EPI_ACCUM;
             p.D = dw;
             p.ldd = 9ll * Cin;
@@ -2305,6 +2326,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[8] = pl.box.bw;
     out[9] = pl.box.bh;
     out[10] = pl.box.bimg;
+    out[11] = pl.wg_blocked ? 1 : 0;
     return SPRINT_OK;
 }
 

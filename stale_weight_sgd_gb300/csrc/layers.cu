@@ -126,11 +126,13 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
 }
 
 // Strided batched transpose through 32x32 shared-memory tiles, coalesced on
-// both sides: dst[b*db + c*dc + r] = src[b*sb + r*sr + c] for r < R, c < C,
-// b = blockIdx.z. Used for w -> w^T (one batch) and NHWC -> [C][H][W][N]
-// (batch = pixel).
+// both sides: dst[b*db + c*dc + (r/32)*drt + r%32] = src[b*sb + r*sr + c] for
+// r < R, c < C, b = blockIdx.z (drt = 32: dst[b*db + c*dc + r]). Used for
+// w -> w^T (one batch), NHWC -> [C][H][W][N] (batch = pixel) and NHWC ->
+// [H][W*N/32][C][32] (batch = pixel, dc = 32, drt = 32*C).
 __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int R,
-                                                        int C, long long sb, long long sr, long long db, long long dc) {
+                                                        int C, long long sb, long long sr, long long db, long long dc,
+                                                        long long drt) {
     __shared__ float tile[32][33];
     const long long b = blockIdx.z;
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
@@ -141,20 +143,21 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict_
         if (r < R && c < C) tile[j][tx] = src[b * sb + static_cast<long long>(r) * sr + c];
     }
     __syncthreads();
+    const long long dst0 = b * db + blockIdx.y * drt;
 #pragma unroll
     for (int j = ty; j < 32; j += 8) {
         const int c = c0 + j, r = r0 + tx;
-        if (r < R && c < C) dst[b * db + static_cast<long long>(c) * dc + r] = tile[tx][j];
+        if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[tx][j];
     }
 }
 
 int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
-                     long long dc, cudaStream_t s) {
+                     long long dc, cudaStream_t s, long long drt = 32) {
     if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
     dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
-    transpose_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc);
+    transpose_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
     return check_launch("transpose_kernel");
 }
 
@@ -165,7 +168,7 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
 // channel's parts in part order. One read of dy serves both dy^T and dedb.
 __global__ void __launch_bounds__(256) transpose_colsum_kernel(const float* __restrict__ src, float* __restrict__ dst,
                                                                int R, int C, long long sb, long long sr, long long db,
-                                                               long long dc, float* __restrict__ partial,
+                                                               long long dc, long long drt, float* __restrict__ partial,
                                                                long long nparts) {
     __shared__ float tile[32][33];
     const long long b = blockIdx.z;
@@ -177,10 +180,11 @@ __global__ void __launch_bounds__(256) transpose_colsum_kernel(const float* __re
         tile[j][tx] = (r < R && c < C) ? src[b * sb + static_cast<long long>(r) * sr + c] : 0.f;
     }
     __syncthreads();
+    const long long dst0 = b * db + blockIdx.y * drt;
 #pragma unroll
     for (int j = ty; j < 32; j += 8) {
         const int c = c0 + j, r = r0 + tx;
-        if (r < R && c < C) dst[b * db + static_cast<long long>(c) * dc + r] = tile[tx][j];
+        if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[tx][j];
     }
     if (ty == 0 && c0 + tx < C) {
         float t = 0.f;
@@ -213,13 +217,13 @@ __global__ void __launch_bounds__(256) colsum_parts_finish(const float* __restri
 // (partial: C * batch * ceil(R / 32) floats of workspace)
 int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr,
                             long long db, long long dc, float* partial, float* out, float alpha, int accumulate,
-                            cudaStream_t s) {
+                            cudaStream_t s, long long drt = 32) {
     if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
     const long long nparts = static_cast<long long>(batch) * ((R + 31) / 32);
     dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
-    transpose_colsum_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, partial, nparts);
+    transpose_colsum_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
     colsum_parts_finish<<<C, 256, 0, s>>>(partial, nparts, out, alpha, accumulate);
     return check_launch("transpose_colsum", 2);
 }

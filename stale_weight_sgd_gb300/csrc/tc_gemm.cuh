@@ -42,10 +42,15 @@
 //               shifted by the tap, halo zero-filled by TMA), B = the tap's
 //               weight slice (3-D box). Forward: A = x, B = w[co][tap][ci];
 //               dedx conv: A = dy at the mirrored tap, B = w^T[tap][ci][co].
-//   CONV_WGRAD: dedw conv, per tap: A = dy^T [Cout][H][W][N], B = x^T
-//               [Cin][H][W][N] shifted by the tap; a k-tile is 32 consecutive
-//               (w, n) positions of one row (every TMA box here is 128 B wide
-//               along its inner dimension, the 128-byte swizzle span).
+//   CONV_WGRAD: dedw conv, per tap: A = dy^T, B = x^T shifted by the tap; a
+//               k-tile is 32 consecutive (w, n) positions of one row, n fastest,
+//               so the tap's w-shift is N positions. The copies are either
+//               [C][H][W][N] or, when N % 32 == 0, blocked [H][W*N/32][C][32]:
+//               there a k-tile of C channel rows is one contiguous C x 128-byte
+//               block (the first form spreads its rows H*W*N*4 bytes apart, a
+//               page or more each on wide images) and the w-shift is N/32 whole
+//               blocks. Every TMA box here is 128 B wide along its inner
+//               dimension, the 128-byte swizzle span.
 #pragma once
 
 #include "common.cuh"
@@ -135,6 +140,11 @@ struct TcParams {
     // D[co][tap * wg_rows + ci]; z is the k split only. wg_tpt == 0: one tap per
     // n-tile column range, taps and splits in z.
     int wg_tpt, wg_rows;
+    // CONV_WGRAD operand layout: 0 = [C][H][W][N] (maps {W*N, H, C}); 1 = blocked
+    // [H][W*N/32][C][32] (maps {32, C, W*N/32, H}: a k-tile box is C rows of 128
+    // contiguous bytes, and the tap's w-shift of N elements is wg_cshift = N/32
+    // whole blocks)
+    int wg_blocked, wg_cshift;
     // grouped launches: per-problem bias, mask and output (direct stores)
     const float* g_bias[TC_MAX_GROUP];
     const float* g_mask[TC_MAX_GROUP];
@@ -352,6 +362,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     tma_load_3d_pair(b_dst, mB, c0, n0, tp, bar);
                                 else
                                     tma_load_3d_pair(b_dst, mB, c0, tp, n0, bar);
+                            } else if (p.wg_blocked) {   // blocked [H][W*N/32][C][32] copies
+                                const int h = kt / p.tiles_w;
+                                const int ck = kt % p.tiles_w;
+                                tma_load_4d_pair(a_dst, mA, 0, m0, ck, h, bar);
+                                if (p.wg_tpt > 0) {
+                                    const int per = p.wg_tpt / 2, first = tc.nt * p.wg_tpt + static_cast<int>(rank) * per;
+                                    for (int j = 0; j < per && first + j < 9; ++j) {
+                                        const int tp = first + j;
+                                        tma_load_4d_pair(b_dst + j * p.wg_rows * 128, mB, 0, 0,
+                                                         ck + (tp % 3 - p.pad) * p.wg_cshift, h + tp / 3 - p.pad, bar);
+                                    }
+                                } else {
+                                    tma_load_4d_pair(b_dst, mB, 0, n0, ck + (tap % 3 - p.pad) * p.wg_cshift,
+                                                     h + tap / 3 - p.pad, bar);
+                                }
                             } else {
                                 const int h = kt / p.tiles_w;
                                 const int c0 = (kt % p.tiles_w) * TC_BK;
@@ -380,6 +405,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 tma_load_3d(b_dst, mB, c0, n0, tp, &full[s]);
                             else
                                 tma_load_3d(b_dst, mB, c0, tp, n0, &full[s]);
+                        } else if (p.wg_blocked) {  // CONV_WGRAD, blocked: dy^T {32, Cout, Wo*N/32, Ho}, x^T {32, Cin, W*N/32, H}
+                            const int h = kt / p.tiles_w;
+                            const int ck = kt % p.tiles_w;
+                            tma_load_4d(a_dst, mA, 0, m0, ck, h, &full[s]);
+                            if (p.wg_tpt > 0) {
+                                const int first = tc.nt * p.wg_tpt;
+                                for (int j = 0; j < p.wg_tpt && first + j < 9; ++j) {
+                                    const int tp = first + j;
+                                    tma_load_4d(b_dst + j * p.wg_rows * 128, mB, 0, 0, ck + (tp % 3 - p.pad) * p.wg_cshift,
+                                                h + tp / 3 - p.pad, &full[s]);
+                                }
+                            } else {
+                                tma_load_4d(b_dst, mB, 0, n0, ck + (tap % 3 - p.pad) * p.wg_cshift, h + tap / 3 - p.pad,
+                                            &full[s]);
+                            }
                         } else {  // CONV_WGRAD: dy^T {Wo*N, Ho, Cout}, x^T {W*N, H, Cin}
                             const int h = kt / p.tiles_w;
                             const int c0 = (kt % p.tiles_w) * TC_BK;
