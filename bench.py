@@ -271,7 +271,7 @@ class CallProbe:
             a.record(st)
             r = orig(*args, **kw)
             e.record(st)
-            probe.calls.append((name, probe._flops(name, args), a, e))
+            probe.calls.append((name, probe._flops(name, args), a, e, probe._conv_key(name, args)))
             return r
         setattr(self.S, name, wrapped)
 
@@ -290,19 +290,35 @@ class CallProbe:
             return (2.0 if a[5] is None else 4.0) * N * fin * fout * len(a[0])
         return 0.0
 
+    @staticmethod
+    def _conv_key(name, a):
+        op = {"sprint_conv_fwd": "fwd", "sprint_conv_dX": "dX", "sprint_conv_dW": "dW"}.get(name)
+        if op is None:
+            return None
+        i = {"fwd": 4, "dX": 5, "dW": 6}[op]
+        N, H, W, Ci, Co = a[i:i + 5]
+        return f"{op} {H}x{W}x{Ci}->{Co}"
+
     def summary(self):
-        roles, flops = {}, {}
+        roles, flops, conv = {}, {}, {}
         total = 0.0
-        for name, f, a, e in self.calls:
+        for name, f, a, e, key in self.calls:
             ms = a.elapsed_time(e)
             r = ROLE_OF_CALL.get(name, "other")
             roles[r] = roles.get(r, 0.0) + ms
             flops[r] = flops.get(r, 0.0) + f
             total += ms
+            if key:
+                c = conv.setdefault(key, [0.0, 0.0])
+                c[0] += ms
+                c[1] += f
         return {"serial_ms_per_step": round(total, 3), "calls": len(self.calls),
                 "roles_ms": {r: round(v, 3) for r, v in sorted(roles.items(), key=lambda kv: -kv[1])},
                 "roles_share": {r: round(v / total, 4) for r, v in roles.items()} if total else {},
-                "roles_tflops": {r: round(flops[r] / (roles[r] / 1e3) / 1e12, 1) for r in roles if flops.get(r)}}
+                "roles_tflops": {r: round(flops[r] / (roles[r] / 1e3) / 1e12, 1) for r in roles if flops.get(r)},
+                # every conv call of the step by op and layer shape (all replicas together)
+                "conv_calls": {k: {"ms": round(v[0], 3), "tflops": round(v[1] / (v[0] / 1e3) / 1e12, 1)}
+                               for k, v in sorted(conv.items(), key=lambda kv: -kv[1][0])}}
 
 
 def dense_init(shapes, seed):

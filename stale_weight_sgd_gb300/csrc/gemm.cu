@@ -1279,6 +1279,18 @@ __global__ void dw_packed_reduce(const float* __restrict__ partial, int splits, 
     }
 }
 
+// The factored weight gradient's slabs (Cin = Cout = 64): dw[i] = (acc ? dw : 0) + alpha * sum_s
+// slab_s[i], the slabs added in split order
+__global__ void dw_fact_reduce(const float* __restrict__ partial, int splits, float* __restrict__ dw, float alpha,
+                               int accumulate) {
+    constexpr long long slab = 9ll * 64 * 64;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < slab;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float t = ordered_strided_sum(partial + idx, splits, slab);
+        dw[idx] = (accumulate ? dw[idx] : 0.f) + alpha * t;
+    }
+}
+
 __global__ void colsum_finish_k(const float* __restrict__ partial, int chunks, int cols, float* __restrict__ out,
                                 float alpha, int accumulate) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1333,10 +1345,14 @@ struct ConvPlan {
     size_t ws_colsum = 0;   // dedw: partial bias sums
     int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
     bool wg_blocked = false;       // dedw copies blocked [H][W*N/32][C][32] (N % 32 == 0)
+    bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64; db from the GEMM)
     GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
     size_t ws_tail = 0;            // fwd / dedx: slabs of that split (last in the workspace)
     size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad + ws_tail; }
 };
+
+// floats per split of the factored weight gradient (Cin = Cout = 64): dW [64][9][64]
+constexpr long long wg_fact_slab() { return 9ll * 64 * 64; }
 
 ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool have_wT) {
     ConvPlan pl;
@@ -1397,7 +1413,15 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     const long long m_tiles = (Cout + TC_BM - 1) / TC_BM;
     const bool pair_m = m_tiles >= 2 && (m_tiles % 2 == 0 || m_tiles >= 6);
     long long base;
-    if (Cin <= 128 && (Cin % 8 == 0 || Cin < 8)) {
+    if (pl.wg_blocked && Cin == 64 && Cout == 64 && pad == 1) {
+        // Cout = 64 would fill half of every 128-row tile: D = [(dh, ci)] x [(dw, co)] on a
+        // CTA pair (192 of its 256 rows used, all nine taps from 9 boxes per k-tile), one unit
+        // per k split
+        pl.wg_fact = true;
+        pl.tile.bn = 192;
+        pl.tile.pair = true;
+        base = 1;
+    } else if (Cin <= 128 && (Cin % 8 == 0 || Cin < 8)) {
         // Few input channels: an n-tile holds whole taps (rows of x^T at their
         // shifts), wg_rows rows each (8 for Cin < 8: the box rows past Cin are TMA
         // zero fill), instead of one tap of a few columns; D = [Cout][9 * wg_rows].
@@ -1458,7 +1482,9 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     }
     pl.kt_per_split = static_cast<int>((pl.num_kt + want - 1) / want);
     pl.splits = (pl.num_kt + pl.kt_per_split - 1) / pl.kt_per_split;
-    if (pl.wg_tpt > 0) {
+    if (pl.wg_fact) {
+        pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * wg_fact_slab());
+    } else if (pl.wg_tpt > 0) {
         if (pl.splits > 1 || pl.wg_rows != Cin)
             pl.ws_partial = fbytes(static_cast<long long>(pl.splits) * Cout * 9 * pl.wg_rows);
     } else if (pl.splits > 1) {
@@ -2201,7 +2227,40 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         // packed taps: one box = one tap's wg_rows channel rows; else BN (or half) channel rows
         const uint32_t b_rows = pl.wg_tpt > 0 ? static_cast<uint32_t>(pl.wg_rows) : pl.tile.b_rows();
         bool maps_ok;
-        if (blk) {
+        if (pl.wg_fact) {
+            // A = x^T in boxes of Cin = 64 rows, B = dy^T in boxes of 32 rows
+            const uint64_t da[4] = {32, (uint64_t)Cin, (uint64_t)W * N / 32, (uint64_t)H};
+            const uint64_t sa[3] = {128, (uint64_t)Cin * 128, (uint64_t)W * N / 32 * Cin * 128};
+            const uint64_t dbm[4] = {32, (uint64_t)Cout, (uint64_t)Wo * N / 32, (uint64_t)Ho};
+            const uint64_t sbm[3] = {128, (uint64_t)Cout * 128, (uint64_t)Wo * N / 32 * Cout * 128};
+            const uint32_t ba[4] = {32, 64, 1, 1}, bb[4] = {32, 32, 1, 1};
+            maps_ok = make_tmap(&ta, xT, 4, da, sa, ba) && make_tmap(&tb, dyT, 4, dbm, sbm, bb);
+            if (maps_ok) {
+                TcParams p = base_params();
+                p.M = 2 * TC_BM;
+                p.N = 192;
+                p.num_kt = pl.num_kt;
+                p.kt_per_split = pl.kt_per_split;
+                p.splits = pl.splits;
+                p.img_n = N;
+                p.out_h = Ho;
+                p.out_w = Wo;
+                p.pad = pad;
+                p.tiles_w = pl.box.tw;
+                p.tiles_h = pl.box.th;
+                p.wg_blocked = 1;
+                p.wg_cshift = N / 32;
+                p.wg_fact = 1;
+                p.wg_slab = wg_fact_slab();
+                p.epi = EPI_ACCUM;
+                p.store = ST_DIRECT;
+                p.partial = part;
+                if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, ta, p, 2, 1, pl.splits, s))) return rc;
+                dw_fact_reduce<<<grid_cap(wg_fact_slab()), 256, 0, s>>>(part, pl.splits, dw, alpha, accumulate);
+                if ((rc = check_launch("dw_fact_reduce"))) return rc;
+                done = true;
+            }
+        } else if (blk) {
             const uint64_t da[4] = {32, (uint64_t)Cout, (uint64_t)Wo * N / 32, (uint64_t)Ho};
             const uint64_t sa[3] = {128, (uint64_t)Cout * 128, (uint64_t)Wo * N / 32 * Cout * 128};
             const uint64_t dbm[4] = {32, (uint64_t)Cin, (uint64_t)W * N / 32, (uint64_t)H};
@@ -2216,7 +2275,7 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
             const uint32_t ba[3] = {32, 1, 128}, bb[3] = {32, 1, b_rows};
             maps_ok = make_tmap(&ta, dyT, 3, da, sa, ba) && make_tmap(&tb, xT, 3, dbm, sbm, bb);
         }
-        if (maps_ok) {
+        if (maps_ok && !done) {
             TcParams p = base_params();
             p.M = Cout;
             p.N = Cin;
@@ -2327,6 +2386,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[9] = pl.box.bh;
     out[10] = pl.box.bimg;
     out[11] = pl.wg_blocked ? 1 : 0;
+    out[12] = pl.wg_fact ? 1 : 0;
     return SPRINT_OK;
 }
 

@@ -145,6 +145,17 @@ struct TcParams {
     // contiguous bytes, and the tap's w-shift of N elements is wg_cshift = N/32
     // whole blocks)
     int wg_blocked, wg_cshift;
+    // CONV_WGRAD factored over the kernel rows and columns (wg_fact = 1; CTA
+    // pairs, BN = 192, Cin = Cout = 64, pad 1, blocked copies): the identity
+    // dW[co][dh][dw][ci] = sum_q dy[q - (0, dw-1)][co] x[q + (dh-1, 0)][ci]
+    // makes D = [(dh, ci)] x [(dw, co)], A = x^T shifted by dh (the even CTA's
+    // rows dh 0 and 1, the odd CTA's dh 2), B = dy^T shifted by -(dw-1): all nine
+    // taps from 3 + 6 boxes per k-tile, no half-empty tile for Cout = 64. The odd
+    // CTA's A rows 64-127 are zeros (no copy writes them). Each split writes one
+    // slab of wg_slab floats (dW in its [co][tap][ci] layout) at
+    // partial + split * wg_slab.
+    int wg_fact;
+    long long wg_slab;
     // grouped launches: per-problem bias, mask and output (direct stores)
     const float* g_bias[TC_MAX_GROUP];
     const float* g_mask[TC_MAX_GROUP];
@@ -260,6 +271,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tmem_relinquish();
         }
     }
+    if constexpr (ROLE == ROLE_CONV_WGRAD && PAIR) {
+        // factored weight gradient: the odd CTA's A rows 64-127 are zeros in every ring slot (no
+        // copy ever writes them), visible to the tensor core before the first MMA
+        if (p.wg_fact && rank == 1 && warp < 4) {
+            for (int slot = 0; slot < STAGES * KS; ++slot) {
+                float4* a1 = reinterpret_cast<float4*>(sA + slot * TC_A_STAGE + 64 * 128);
+                for (int i = threadIdx.x; i < 64 * 128 / 16; i += 128) a1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            fence_async_smem();
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if constexpr (PAIR) cluster_sync();   // the peer's barriers are initialised before any remote arrive
@@ -285,7 +307,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int split = G > 1 ? 0 : tc.z;   // grouped: z is the problem, not a k split
         tap = 0;
         if constexpr (ROLE == ROLE_CONV_WGRAD) {
-            if (p.wg_tpt == 0) {
+            if (p.wg_tpt == 0 && !p.wg_fact) {
                 tap = tc.z / p.splits;
                 split = tc.z % p.splits;
             }
@@ -331,7 +353,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int nq = nkt - i < KS ? nkt - i : KS;   // k-tiles in this stage
                     uint32_t ktile_bytes = KTILE_BYTES;
                     if constexpr (ROLE == ROLE_CONV_WGRAD) {
-                        if (p.wg_tpt > 0) {   // A boxes of both CTAs + the taps that exist in this n-tile
+                        if (p.wg_fact) {   // x^T boxes: 2 (even CTA) + 1 (odd) of 64 rows; dy^T: 6 of 32 rows
+                            ktile_bytes = 3u * 64u * 128u + 6u * 32u * 128u;
+                        } else if (p.wg_tpt > 0) {   // A boxes of both CTAs + the taps that exist in this n-tile
                             const int per = PAIR ? p.wg_tpt / 2 : p.wg_tpt;
                             int taps = 0;
                             for (int rk = 0; rk < (PAIR ? 2 : 1); ++rk) {
@@ -362,6 +386,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     tma_load_3d_pair(b_dst, mB, c0, n0, tp, bar);
                                 else
                                     tma_load_3d_pair(b_dst, mB, c0, tp, n0, bar);
+                            } else if (p.wg_fact) {   // factored: A = x^T rows (dh, ci), B = dy^T rows (dw, co)
+                                const int h = kt / p.tiles_w;
+                                const int ck = kt % p.tiles_w;
+                                if (rank == 0) {
+                                    tma_load_4d_pair(a_dst, mA, 0, 0, ck, h - 1, bar);
+                                    tma_load_4d_pair(a_dst + 64 * 128, mA, 0, 0, ck, h, bar);
+                                } else {
+                                    tma_load_4d_pair(a_dst, mA, 0, 0, ck, h + 1, bar);
+                                }
+#pragma unroll
+                                for (int q2 = 0; q2 < 3; ++q2) {
+                                    const int g0 = static_cast<int>(rank) * 96 + 32 * q2;   // B row = dw * 64 + co
+                                    const int dwt = g0 / 64;
+                                    tma_load_4d_pair(b_dst + q2 * 32 * 128, mB, 0, g0 % 64,
+                                                     ck - (dwt - 1) * p.wg_cshift, h, bar);
+                                }
                             } else if (p.wg_blocked) {   // blocked [H][W*N/32][C][32] copies
                                 const int h = kt / p.tiles_w;
                                 const int ck = kt % p.tiles_w;
@@ -552,6 +592,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                         __uint_as_float(v[q + 3]));
                 }
                 continue;
+            }
+            if constexpr (ROLE == ROLE_CONV_WGRAD && PAIR && BN == 192) {
+                if (p.wg_fact) {
+                    // factored weight gradient (Cin = Cout = 64): row r is (dh, ci) = (r / 64, r % 64) in the
+                    // even CTA and (2, r) for r < 64 in the odd one; column c is (dw, co) = (c / 64, c % 64)
+                    float* slab = p.partial + static_cast<long long>(tc.z) * p.wg_slab;
+                    const int dh = rank == 0 ? r / 64 : 2, ci = r % 64;
+                    const bool w_row = rank == 0 || r < 64;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(warp * 32) << 16) + c,
+                                           v);
+                        tmem_wait_ld();
+                        if (c + 32 >= BN) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                        }
+                        if (nkt == 0) {
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) v[q] = 0u;
+                        }
+                        const int dw = c / 64, co0 = c % 64;
+                        if (w_row) {
+                            // dW[co][dh * 3 + dw][ci]: lanes hold consecutive ci, one 128-byte store per column
+                            float* dst = slab + (static_cast<long long>(co0) * 9 + dh * 3 + dw) * 64 + ci;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) dst[q * 9 * 64] = __uint_as_float(v[q]);
+                        }
+                    }
+                    continue;
+                }
             }
             // output row of this thread (direct stores, mask loads); -1 if outside
             long long row_off = -1, mask_off = -1;

@@ -101,9 +101,11 @@ def test_plans_cover_every_kernel_path(S):
     fwd_dx = [p for (_, _, op), p in PLANS.items() if op != S.SPRINT_CONV_DW and p["path"] == "tc"]
     dw = [p for (_, _, op), p in PLANS.items() if op == S.SPRINT_CONV_DW and p["path"] == "tc"]
     print("forward / input-gradient plans:", sorted({(p["bn"], p["pair"], p["tail_splits"]) for p in fwd_dx}))
-    print("weight-gradient plans:", sorted({(p["bn"], p["pair"], p["splits"], p["wg_tpt"]) for p in dw}))
+    print("weight-gradient plans:", sorted({(p["bn"], p["pair"], p["splits"], p["wg_tpt"], p["wg_fact"]) for p in dw}))
     assert any(p["pair"] for p in fwd_dx + dw) and any(not p["pair"] for p in fwd_dx + dw)
     assert any(p["tail_splits"] > 1 for p in fwd_dx) and any(p["tail_splits"] == 1 for p in fwd_dx)
     assert any(p["splits"] > 1 for p in dw)
-    assert any(p["wg_tpt"] > 0 for p in dw) and any(p["wg_tpt"] == 0 for p in dw)
+    assert any(p["wg_tpt"] > 0 for p in dw) and any(p["wg_tpt"] == 0 and not p["wg_fact"] for p in dw)
+    assert any(p["wg_fact"] for p in dw)          # the Cout = 64 layers: factored on CTA pairs
+    assert all(p["wg_blocked"] for p in dw)       # batch 64 and 128: blocked operand copies
     assert any(p["path"] == "smallc" for (_, _, op), p in PLANS.items())

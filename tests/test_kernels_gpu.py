@@ -508,7 +508,8 @@ CONV_CASES = [
     (1, 6, 17, 1, 40),      # RGB dW: one input channel, Cout between 32 and 64
     (2, 7, 9, 3, 18),       # RGB dW with Cout % 4 != 0 (4-byte dy copies); CUDA-core forward and dX
     # batch % 32 == 0: the weight gradient's blocked [H][W*N/32][C][32] copies
-    (32, 6, 5, 64, 64),     # packed taps (3 per tile), Cout < 128, ragged rows, w-shift = one block
+    (32, 6, 5, 64, 64),     # Cin = Cout = 64: factored over kernel rows x columns on a CTA pair, w-shift one block
+    (64, 9, 20, 64, 64),    # factored, w-shift = two blocks, several k-tiles per split
     (64, 3, 3, 32, 48),     # w-shift = two blocks, Cout % 32 != 0
     (32, 5, 7, 256, 128),   # one tap per tile, split-K
     (32, 4, 6, 6, 32),      # Cin < 8: tap boxes of 8 channel rows, rows past Cin zero-filled
