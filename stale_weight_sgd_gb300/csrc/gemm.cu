@@ -2245,13 +2245,15 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         const uint32_t b_rows = pl.wg_tpt > 0 ? static_cast<uint32_t>(pl.wg_rows) : pl.tile.b_rows();
         bool maps_ok;
         if (pl.wg_fact) {
-            // A = x^T in boxes of Cin = 64 rows, B = dy^T in boxes of 32 rows
+            // A = x^T in boxes of 2 rows x Cin = 64 channels, B = dy^T in boxes of 64 and 32 channels
             const uint64_t da[4] = {32, (uint64_t)Cin, (uint64_t)W * N / 32, (uint64_t)H};
             const uint64_t sa[3] = {128, (uint64_t)Cin * 128, (uint64_t)W * N / 32 * Cin * 128};
             const uint64_t dbm[4] = {32, (uint64_t)Cout, (uint64_t)Wo * N / 32, (uint64_t)Ho};
             const uint64_t sbm[3] = {128, (uint64_t)Cout * 128, (uint64_t)Wo * N / 32 * Cout * 128};
-            const uint32_t ba[4] = {32, 64, 1, 1}, bb[4] = {32, 32, 1, 1};
-            maps_ok = make_tmap(&ta, xT, 4, da, sa, ba) && make_tmap(&tb, dyT, 4, dbm, sbm, bb);
+            const uint32_t ba[4] = {32, 64, 1, 2}, bb[4] = {32, 64, 1, 1}, bd[4] = {32, 32, 1, 1};
+            CUtensorMap tb32;
+            maps_ok = make_tmap(&ta, xT, 4, da, sa, ba) && make_tmap(&tb, dyT, 4, dbm, sbm, bb) &&
+                      make_tmap(&tb32, dyT, 4, dbm, sbm, bd);
             if (maps_ok) {
                 TcParams p = base_params();
                 p.M = 2 * TC_BM;
@@ -2272,7 +2274,7 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
                 p.epi = EPI_ACCUM;
                 p.store = ST_DIRECT;
                 p.partial = part;
-                if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, ta, p, 2, 1, pl.splits, s))) return rc;
+                if ((rc = launch_tc<ROLE_CONV_WGRAD>(pl.tile, ta, tb, tb32, p, 2, 1, pl.splits, s))) return rc;
                 dw_fact_reduce<<<grid_cap(wg_fact_slab()), 256, 0, s>>>(part, pl.splits, dw, alpha, accumulate);
                 if ((rc = check_launch("dw_fact_reduce"))) return rc;
                 done = true;

@@ -150,10 +150,11 @@ struct TcParams {
     // dW[co][dh][dw][ci] = sum_q dy[q - (0, dw-1)][co] x[q + (dh-1, 0)][ci]
     // makes D = [(dh, ci)] x [(dw, co)], A = x^T shifted by dh (the even CTA's
     // rows dh 0 and 1, the odd CTA's dh 2), B = dy^T shifted by -(dw-1): all nine
-    // taps from 3 + 6 boxes per k-tile, no half-empty tile for Cout = 64. The odd
-    // CTA's A rows 64-127 are zeros (no copy writes them). Each split writes one
-    // slab of wg_slab floats (dW in its [co][tap][ci] layout) at
-    // partial + split * wg_slab.
+    // taps from 2 + 4 boxes per k-tile, no half-empty tile for Cout = 64 (the odd
+    // CTA's A rows 64-127, x^T two rows down, are never stored). maps.a holds
+    // x^T boxes of 2 rows x 64 channels, maps.b dy^T boxes of 64 channels and
+    // maps.d of 32. Each split writes one slab of wg_slab floats (dW in its
+    // [co][tap][ci] layout) at partial + split * wg_slab.
     int wg_fact;
     long long wg_slab;
     // grouped launches: per-problem bias, mask and output (direct stores)
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int g = 0; g < G && g < p.z_tiles; ++g) {
             tma_prefetch_desc(&maps.a[g]);
             tma_prefetch_desc(&maps.b[g]);
-            if (p.store != ST_DIRECT) tma_prefetch_desc(&maps.d[g]);
+            if (p.store != ST_DIRECT || p.wg_fact) tma_prefetch_desc(&maps.d[g]);
         }
     }
     if (warp == 5) {
@@ -269,17 +270,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         } else {
             tmem_alloc(tmem_slot, TMEM_COLS);
             tmem_relinquish();
-        }
-    }
-    if constexpr (ROLE == ROLE_CONV_WGRAD && PAIR) {
-        // factored weight gradient: the odd CTA's A rows 64-127 are zeros in every ring slot (no
-        // copy ever writes them), visible to the tensor core before the first MMA
-        if (p.wg_fact && rank == 1 && warp < 4) {
-            for (int slot = 0; slot < STAGES * KS; ++slot) {
-                float4* a1 = reinterpret_cast<float4*>(sA + slot * TC_A_STAGE + 64 * 128);
-                for (int i = threadIdx.x; i < 64 * 128 / 16; i += 128) a1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            fence_async_smem();
         }
     }
     tc_fence_before();
@@ -353,8 +343,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int nq = nkt - i < KS ? nkt - i : KS;   // k-tiles in this stage
                     uint32_t ktile_bytes = KTILE_BYTES;
                     if constexpr (ROLE == ROLE_CONV_WGRAD) {
-                        if (p.wg_fact) {   // x^T boxes: 2 (even CTA) + 1 (odd) of 64 rows; dy^T: 6 of 32 rows
-                            ktile_bytes = 3u * 64u * 128u + 6u * 32u * 128u;
+                        if (p.wg_fact) {   // x^T: one 128-row box per CTA; dy^T: 64 + 32 rows per CTA
+                            ktile_bytes = 2u * 128u * 128u + 2u * 96u * 128u;
                         } else if (p.wg_tpt > 0) {   // A boxes of both CTAs + the taps that exist in this n-tile
                             const int per = PAIR ? p.wg_tpt / 2 : p.wg_tpt;
                             int taps = 0;
@@ -389,18 +379,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             } else if (p.wg_fact) {   // factored: A = x^T rows (dh, ci), B = dy^T rows (dw, co)
                                 const int h = kt / p.tiles_w;
                                 const int ck = kt % p.tiles_w;
+                                // A: the 2-row box of x^T rows h - 1, h (even CTA) or h + 1, h + 2 (odd CTA,
+                                // whose second half, rows 64-127, is never stored)
+                                tma_load_4d_pair(a_dst, mA, 0, 0, ck, h - 1 + 2 * static_cast<int>(rank), bar);
+                                // B rows (dw, co): even CTA dw 0 (a 64-row box of maps.b) and dw 1 co 0-31, odd
+                                // CTA dw 1 co 32-63 and dw 2 (32-row boxes of maps.d)
+                                const CUtensorMap* mB32 = &maps.d[0];
                                 if (rank == 0) {
-                                    tma_load_4d_pair(a_dst, mA, 0, 0, ck, h - 1, bar);
-                                    tma_load_4d_pair(a_dst + 64 * 128, mA, 0, 0, ck, h, bar);
+                                    tma_load_4d_pair(b_dst, mB, 0, 0, ck + p.wg_cshift, h, bar);
+                                    tma_load_4d_pair(b_dst + 64 * 128, mB32, 0, 0, ck, h, bar);
                                 } else {
-                                    tma_load_4d_pair(a_dst, mA, 0, 0, ck, h + 1, bar);
-                                }
-#pragma unroll
-                                for (int q2 = 0; q2 < 3; ++q2) {
-                                    const int g0 = static_cast<int>(rank) * 96 + 32 * q2;   // B row = dw * 64 + co
-                                    const int dwt = g0 / 64;
-                                    tma_load_4d_pair(b_dst + q2 * 32 * 128, mB, 0, g0 % 64,
-                                                     ck - (dwt - 1) * p.wg_cshift, h, bar);
+                                    tma_load_4d_pair(b_dst, mB32, 0, 32, ck, h, bar);
+                                    tma_load_4d_pair(b_dst + 32 * 128, mB, 0, 0, ck - p.wg_cshift, h, bar);
                                 }
                             } else if (p.wg_blocked) {   // blocked [H][W*N/32][C][32] copies
                                 const int h = kt / p.tiles_w;
