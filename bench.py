@@ -81,6 +81,9 @@ ROOF_CONV_KERNEL = ("tc_gemm_kernel<CONV_IMPL> (implicit-GEMM conv forward, TF32
 PROFILED_TRAFFIC = {
     # one call: the GEMM kernel 461.8 + 47.0 MB and its tail reduction 17.1 MB (one ncu capture)
     "tc_gemm_kernel (grouped FC forward, 4 x 512x5000x5000, TF32)": 525.9e6,
+    # the GEMM kernel alone: 210.3 MB read + 170.8 MB written (one ncu capture, --set full;
+    # algorithmic 412 MB: x and y 205.5 MB each, the weights 2.4 MB)
+    ROOF_CONV_KERNEL: 381.1e6,
 }
 
 
