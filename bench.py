@@ -793,6 +793,8 @@ KERNELS = {
     "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T, "
                       "x^T + ones row, dy^T given and dx^T written, as in the step",
     "conv_dw_224x64": "conv weight gradient, VGG conv1_2 shape 224x224x64->64, batch 16",
+    "conv_fwd_224x64": "conv forward, VGG conv1_2 shape 224x224x64->64, batch 16",
+    "conv_dx_224x64": "conv input gradient (ReLU mask), VGG conv1_2 shape 224x224x64->64, batch 16",
     "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
     "conv_dw_224x3": "conv weight gradient + bias gradient, VGG conv1_1 shape 224x224x3->64, batch 16 "
                      "(direct CUDA-core kernel)",
@@ -866,9 +868,9 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
             work, unit = 4.0 * M * N * K, "TFLOP/s"
-    elif k in ("conv_dw_224x64", "conv_fwd_224x3", "conv_dw_224x3"):
+    elif k in ("conv_dw_224x64", "conv_fwd_224x64", "conv_dx_224x64", "conv_fwd_224x3", "conv_dw_224x3"):
         Nb, H, W = args.batch or 16, 224, 224
-        Ci = 64 if k == "conv_dw_224x64" else 3
+        Ci = 64 if k.endswith("224x64") else 3
         Co = 64
         x = rnd(Nb, H, W, Ci).relu_()
         w = rnd(Co, 3, 3, Ci, std=(2.0 / (9 * Ci)) ** 0.5)
@@ -882,6 +884,9 @@ def run_kernel(args):
         work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
         if k in ("conv_dw_224x64", "conv_dw_224x3"):
             fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
+        elif k == "conv_dx_224x64":
+            dx = torch.empty(Nb, H, W, Ci, device="cuda")
+            fn = lambda i: S.sprint_conv_dX(dy, w, None, x, dx, Nb, H, W, Ci, Co, 1, ws, nbytes)
         else:
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
     elif k.startswith("conv"):

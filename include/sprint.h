@@ -92,13 +92,16 @@ int sprint_device_status(int* flags_out, int reset);
  *   [11] layout of the weight gradient's transposed copies: 1 = blocked
  *       [H][W*N/32][C][32] (N % 32 == 0), 0 = [C][H][W][N]
  *   [12] 1 = weight gradient factored over kernel rows x columns on CTA pairs
- *       (Cin = Cout = 64, pad 1, N % 32 == 0; dedb from the same GEMM)
+ *       (Cin = Cout = 64, pad 1, N % 32 == 0)
+ *   [13] 1 = forward / input gradient factored over the kernel columns on CTA
+ *       pairs (64 output channels, input channels % 32 == 0, pad 1, rows of
+ *       >= 96 pixels; uses the workspace for permuted weights)
  * Returns SPRINT_ERR_SHAPE / SPRINT_ERR_INVALID_ARG like the calls they
  * describe. sprint_conv_plan: op, shape and have_wT as for the conv calls.
  * sprint_gemm_plan: the grouped tensor-core GEMM D[M][N] = A[M][K] B[N][K]^T
  * over `batch` problems (the batched FC calls), allow_tail as when the
  * workspace holds the tail slabs. */
-#define SPRINT_PLAN_FIELDS 13
+#define SPRINT_PLAN_FIELDS 14
 #define SPRINT_PATH_SIMT 0
 #define SPRINT_PATH_TC 1
 #define SPRINT_PATH_SMALLC 2

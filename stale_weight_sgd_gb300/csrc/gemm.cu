@@ -1316,6 +1316,33 @@ __global__ void colsum_finish_k(const float* __restrict__ partial, int chunks, i
     out[c] = (accumulate ? out[c] : 0.f) + alpha * t;
 }
 
+// The factored convolution's B operand: forward (dx = 0) B'[(dw, co)][(dh, ci)], input
+// gradient (dx = 1) B''[(dw, ci)][(dh, co)], both = w[co][dh][dw][ci] (row-major, k fastest)
+__global__ void fact_weights_kernel(const float* __restrict__ w, float* __restrict__ out, int Cin, int Cout, int dx) {
+    const long long total = 9ll * Cin * Cout;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        int co, ci, dh, dw;
+        long long r;
+        if (!dx) {   // idx = ((dw * Cout + co) * 3 + dh) * Cin + ci
+            ci = static_cast<int>(idx % Cin);
+            r = idx / Cin;
+            dh = static_cast<int>(r % 3);
+            r /= 3;
+            co = static_cast<int>(r % Cout);
+            dw = static_cast<int>(r / Cout);
+        } else {     // idx = ((dw * Cin + ci) * 3 + dh) * Cout + co
+            co = static_cast<int>(idx % Cout);
+            r = idx / Cout;
+            dh = static_cast<int>(r % 3);
+            r /= 3;
+            ci = static_cast<int>(r % Cin);
+            dw = static_cast<int>(r / Cin);
+        }
+        out[idx] = w[((static_cast<long long>(co) * 3 + dh) * 3 + dw) * Cin + ci];
+    }
+}
+
 int grid_cap(long long work) {
     long long g = (work + 255) / 256;
     const long long cap = static_cast<long long>(num_sms()) * 16;
@@ -1362,10 +1389,14 @@ struct ConvPlan {
     size_t ws_colsum = 0;   // dedw: partial bias sums
     int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
     bool wg_blocked = false;       // dedw copies blocked [H][W*N/32][C][32] (N % 32 == 0)
-    bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64; db from the GEMM)
+    bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64)
+    bool fact = false;             // fwd / dedx factored over the kernel columns (64 output channels, wide rows)
+    size_t ws_wfact = 0;           // its permuted weights
     GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
     size_t ws_tail = 0;            // fwd / dedx: slabs of that split (last in the workspace)
-    size_t ws_total() const { return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad + ws_tail; }
+    size_t ws_total() const {
+        return ws_wT + ws_xT + ws_dyT + ws_partial + ws_colsum + ws_col + ws_wpad + ws_wfact + ws_tail;
+    }
 };
 
 // floats per split of the factored weight gradient (Cin = Cout = 64): dW [64][9][64]
@@ -1391,6 +1422,20 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     if (op == SPRINT_CONV_FWD || op == SPRINT_CONV_DX) {
         pl.tc = (Cin % 4 == 0) && (Cout % 4 == 0) && Cin >= 8 && Cout >= 16;
         if (!pl.tc) return pl;
+        // 64 output channels on rows wide enough for 126-pixel tiles: factored over the kernel
+        // columns, a 192-wide GEMM instead of a 64-wide one
+        const int nout = op == SPRINT_CONV_FWD ? Cout : Cin, kch = op == SPRINT_CONV_FWD ? Cin : Cout;
+        const int fw = op == SPRINT_CONV_FWD ? Wo : W;
+        if (pad == 1 && nout == 64 && kch % 32 == 0 && fw >= 96) {
+            pl.fact = true;
+            pl.tile.bn = 192;
+            pl.tile.pair = true;
+            pl.num_kt = 3 * (kch / 32);
+            pl.kt_per_split = pl.num_kt;
+            pl.box = PixBox{TC_FACT_OUT, 1, 1, (fw + TC_FACT_OUT - 1) / TC_FACT_OUT, op == SPRINT_CONV_FWD ? Ho : H, N};
+            pl.ws_wfact = fbytes(3ll * nout * 3 * kch);
+            return pl;
+        }
         const int gw = op == SPRINT_CONV_FWD ? Wo : W, gh = op == SPRINT_CONV_FWD ? Ho : H;
         pl.box = pick_box(TC_BM, gw, gh, N);
         const int ncols = op == SPRINT_CONV_FWD ? Cout : Cin;
@@ -2072,6 +2117,46 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
     return launch_tail_reduce<ROLE_CONV_IMPL>(pl.gp, p, m_units, n_tiles, 1, s);
 }
 
+// The factored implicit GEMM (CONV_FACT, CTA pairs, BN = 192): A = act (NHWC, act_c channels) in
+// boxes of 128 pixels of one row, B = the permuted weights [3 * nout][3 * act_c].
+static int conv_fact_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, int nout,
+                        const float* wfact, TcParams p, cudaStream_t s, bool* done) {
+    *done = false;
+    CUtensorMap ta, tb;
+    const uint64_t da[4] = {(uint64_t)act_c, (uint64_t)act_w, (uint64_t)act_h, (uint64_t)p.img_n};
+    const uint64_t sa[3] = {(uint64_t)act_c * 4, (uint64_t)act_w * act_c * 4, (uint64_t)act_h * act_w * act_c * 4};
+    const uint32_t ba[4] = {32, 32, 1, 1};   // one 32-pixel window
+    const int kp = 3 * act_c;
+    const uint64_t db[2] = {(uint64_t)kp, (uint64_t)3 * nout};
+    const uint64_t sb[1] = {(uint64_t)kp * 4};
+    const uint32_t bb[2] = {32, pl.tile.b_rows()};
+    if (!make_tmap(&ta, act, 4, da, sa, ba) || !make_tmap(&tb, wfact, 2, db, sb, bb)) return SPRINT_OK;
+    p.chunks = act_c / 32;
+    p.num_kt = pl.num_kt;
+    p.kt_per_split = pl.num_kt;
+    p.tiles_w = pl.box.tw;
+    // the output through 30-pixel TMA boxes (NHWC, ldd channels per pixel)
+    CUtensorMap td = ta;
+    const uint64_t dd[4] = {(uint64_t)nout, (uint64_t)p.out_w, (uint64_t)p.out_h, (uint64_t)p.img_n};
+    const uint64_t sd[3] = {(uint64_t)p.ldd * 4, (uint64_t)p.out_w * p.ldd * 4, (uint64_t)p.out_h * p.out_w * p.ldd * 4};
+    const uint32_t bd[4] = {32, TC_FACT_WIN, 1, 1};
+    p.store = ST_DIRECT;
+    if ((p.ldd & 3) == 0 && aligned16(p.D) && make_tmap(&td, p.D, 4, dd, sd, bd, false)) p.store = ST_PIX4D;
+    TcMaps<1> maps;
+    maps.a[0] = ta;
+    maps.b[0] = tb;
+    maps.d[0] = td;
+    const long long tiles = static_cast<long long>(p.img_n) * p.out_h * p.tiles_w;
+    const long long units = (tiles + 1) / 2;
+    SPRINT_REQUIRE(units < (1ll << 31), SPRINT_ERR_SHAPE, "conv: %lld factored tiles is too many", tiles);
+    p.m_tiles = static_cast<int>(units);
+    p.n_tiles = 1;
+    p.z_tiles = 1;
+    p.num_tiles = static_cast<int>(units);
+    *done = true;
+    return launch_tc_bn<ROLE_CONV_FACT, 192, true, 1>(maps, p, s);
+}
+
 extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
                                int Cout, int pad, int relu, void* ws, size_t ws_bytes, sprint_stream_t stream) {
     int rc = check_conv_shape(__func__, N, H, W, Cin, Cout, pad);
@@ -2091,6 +2176,26 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     if (pl.smallc) return launch_conv_smallc(x, w, b, y, N, H, W, Cin, Cout, pad, relu, s);
+    if (pl.fact) {
+        float* wf = static_cast<float*>(ws);
+        fact_weights_kernel<<<grid_cap(9ll * Cin * Cout), 256, 0, s>>>(w, wf, Cin, Cout, 0);
+        if ((rc = check_launch("fact_weights_kernel"))) return rc;
+        TcParams p = base_params();
+        p.img_n = N;
+        p.out_h = Ho;
+        p.out_w = Wo;
+        p.pad = pad;
+        p.tap_sign = 1;
+        p.epi = EPI_STORE;
+        p.D = y;
+        p.ldd = Cout;
+        p.bias = b;
+        p.relu = relu;
+        bool done = false;
+        rc = conv_fact_tc(pl, x, Cin, W, H, Cout, wf, p, s, &done);
+        if (rc || done) return rc;
+        return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
+    }
     if (pl.tc && pl.im2col) {
         float* col = static_cast<float*>(ws);
         float* wpad = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_col);
@@ -2158,6 +2263,26 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
     const bool tail_room = pl.ws_tail && ws && ws_bytes >= pl.ws_total();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
+    if (pl.fact) {
+        float* wf = static_cast<float*>(ws);
+        fact_weights_kernel<<<grid_cap(9ll * Cin * Cout), 256, 0, s>>>(w, wf, Cin, Cout, 1);
+        if ((rc = check_launch("fact_weights_kernel"))) return rc;
+        TcParams p = base_params();
+        p.img_n = N;
+        p.out_h = H;
+        p.out_w = W;
+        p.pad = pad;
+        p.tap_sign = -1;
+        p.epi = EPI_MASK;
+        p.D = dx;
+        p.ldd = Cin;
+        p.mask = relu_src;
+        p.ldm = Cin;
+        bool done = false;
+        rc = conv_fact_tc(pl, dy, Cout, Wo, Ho, Cin, wf, p, s, &done);
+        if (rc || done) return rc;
+        return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
+    }
     if (pl.tc) {
         const float* wt = wT;
         if (!wt) {
@@ -2406,6 +2531,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[10] = pl.box.bimg;
     out[11] = pl.wg_blocked ? 1 : 0;
     out[12] = pl.wg_fact ? 1 : 0;
+    out[13] = pl.fact ? 1 : 0;
     return SPRINT_OK;
 }
 

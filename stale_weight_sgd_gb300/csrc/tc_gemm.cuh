@@ -42,6 +42,15 @@
 //               shifted by the tap, halo zero-filled by TMA), B = the tap's
 //               weight slice (3-D box). Forward: A = x, B = w[co][tap][ci];
 //               dedx conv: A = dy at the mirrored tap, B = w^T[tap][ci][co].
+//   CONV_FACT : forward or input gradient of a layer whose output has 64
+//               channels, factored over the kernel columns (CTA pairs, BN =
+//               192): D'[q][(dw, c)] = sum over (dh, k) of A[q + s*(dh-1, 0)][k]
+//               * B'[(dw, c)][(dh, k)], with q = four windows of 32 consecutive
+//               pixels of one image row (each window one pixel wider on both
+//               sides than its 30 outputs), A = x (s = +1) or dy (s = -1) and B'
+//               the weights permuted by the host; the epilogue adds the three
+//               column blocks of neighbouring rows within the warp's window:
+//               out[q] = D'[q - s][dw 0] + D'[q][dw 1] + D'[q + s][dw 2].
 //   CONV_WGRAD: dedw conv, per tap: A = dy^T, B = x^T shifted by the tap; a
 //               k-tile is 32 consecutive (w, n) positions of one row, n fastest,
 //               so the tap's w-shift is N positions. The copies are either
@@ -57,12 +66,17 @@
 
 namespace sprint {
 
-enum Role : int { ROLE_GEMM_2D = 0, ROLE_CONV_IMPL = 1, ROLE_CONV_WGRAD = 2 };
+enum Role : int { ROLE_GEMM_2D = 0, ROLE_CONV_IMPL = 1, ROLE_CONV_WGRAD = 2, ROLE_CONV_FACT = 3 };
 enum Epi : int { EPI_STORE = 0, EPI_MASK = 1, EPI_ACCUM = 2 };
 // how the epilogue writes: direct stores, or TMA through a store map of shape
 enum Store : int { ST_DIRECT = 0, ST_2D = 1, ST_PIX4D = 2, ST_WGRAD3D = 3, ST_PARTIAL3D = 4 };
 
 constexpr int TC_BM = 128;
+// CONV_FACT: each epilogue warp's 32 rows are a window of 32 consecutive
+// pixels of which the middle 30 are outputs (its first and last rows are the
+// halo its neighbours need), so a 128-row tile yields 120 outputs
+constexpr int TC_FACT_WIN = 30;
+constexpr int TC_FACT_OUT = 4 * TC_FACT_WIN;
 constexpr int TC_BK = 32;                      // fp32 elements per 128-byte swizzle row
 constexpr int TC_THREADS = 192;
 constexpr int TC_A_STAGE = TC_BM * TC_BK * 4;  // 16 KB
@@ -209,6 +223,16 @@ __host__ __device__ __forceinline__ TileCoord tile_coord(int t, const TcParams& 
     return c;
 }
 
+// CONV_FACT tile mt: image n, row h, first output pixel w0 (tiles_w tiles of
+// TC_FACT_OUT outputs per image row); n >= img_n past the last tile
+__host__ __device__ __forceinline__ void fact_tile(const TcParams& p, int mt, int& n, int& h, int& w0) {
+    const int per_img = p.out_h * p.tiles_w;
+    n = mt / per_img;
+    const int rem = mt % per_img;
+    h = rem / p.tiles_w;
+    w0 = (rem % p.tiles_w) * TC_FACT_OUT;
+}
+
 template <int ROLE, int BN, bool PAIR, int G>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps<G> maps, const TcParams p) {
@@ -332,6 +356,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     pw0 = (tc.mt % p.tiles_w) * p.bw;
                     ph0 = ((tc.mt / p.tiles_w) % p.tiles_h) * p.bh;
                     pn0 = (tc.mt / (p.tiles_w * p.tiles_h)) * p.bimg;
+                } else if constexpr (ROLE == ROLE_CONV_FACT) {
+                    fact_tile(p, tc.mt, pn0, ph0, pw0);
                 }
                 for (int i = 0; i < nkt; i += KS, ++it) {
                     const uint32_t s = it % STAGES;
@@ -376,6 +402,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     tma_load_3d_pair(b_dst, mB, c0, n0, tp, bar);
                                 else
                                     tma_load_3d_pair(b_dst, mB, c0, tp, n0, bar);
+                            } else if constexpr (ROLE == ROLE_CONV_FACT) {
+                                // A: the four 32-pixel windows of the row shifted by the kernel row (zero fill
+                                // outside the image, and past the last tile); B': the permuted weights, k =
+                                // (dh, channel)
+                                const int dh = kt / p.chunks;
+                                const int c0 = (kt % p.chunks) * TC_BK;
+#pragma unroll
+                                for (int wi = 0; wi < 4; ++wi)
+                                    tma_load_4d_pair(a_dst + wi * 32 * 128, mA, c0, pw0 + wi * TC_FACT_WIN - 1,
+                                                     ph0 + p.tap_sign * (dh - 1), pn0, bar);
+                                tma_load_2d_pair(b_dst, mB, kt * TC_BK, n0, bar);
                             } else if (p.wg_fact) {   // factored: A = x^T rows (dh, ci), B = dy^T rows (dw, co)
                                 const int h = kt / p.tiles_w;
                                 const int ck = kt % p.tiles_w;
@@ -580,6 +617,105 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         *reinterpret_cast<float4*>(slab + c + q) =
                             make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
                                         __uint_as_float(v[q + 3]));
+                }
+                continue;
+            }
+            if constexpr (ROLE == ROLE_CONV_FACT) {
+                // lane l of warp k is pixel w0 + 30k - 1 + l of the tile's image row; lanes 1-30
+                // output the sum of block dw1 of their own row and blocks dw0 / dw2 of rows l - s
+                // and l + s of the same window (shuffles), then go out as one 30-pixel TMA box
+                int fn, fh, fw0;
+                fact_tile(p, tc.mt, fn, fh, fw0);
+                const int wfirst = fw0 + warp * TC_FACT_WIN;   // the window's first output pixel
+                const int w = wfirst - 1 + lane;
+                const bool out_row = fn < p.img_n && lane >= 1 && lane <= TC_FACT_WIN && w < p.out_w;
+                const long long pix = (static_cast<long long>(fn) * p.out_h + fh) * p.out_w + w;
+                const int lo_blk = p.tap_sign > 0 ? 0 : 2;   // block taken from row l - 1
+                const int hi_blk = 2 - lo_blk;                // block taken from row l + 1
+                const bool box_inside = fn < p.img_n && wfirst < p.out_w;
+#pragma unroll 1
+                for (int jb = 0; jb < 2; ++jb) {   // the two 32-channel halves of the 64 outputs
+                    uint32_t vl[32], vm[32], vh[32];
+                    const uint32_t tb = tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(warp * 32) << 16);
+                    tmem_ld_32x32b_x32(tb + lo_blk * 64 + jb * 32, vl);
+                    tmem_ld_32x32b_x32(tb + 64 + jb * 32, vm);
+                    tmem_ld_32x32b_x32(tb + hi_blk * 64 + jb * 32, vh);
+                    tmem_wait_ld();
+                    if (jb == 1) {   // accumulator fully read: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                    }
+                    const int c0 = jb * 32;
+                    float o[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        o[q] = __shfl_up_sync(0xffffffffu, __uint_as_float(vl[q]), 1) + __uint_as_float(vm[q]) +
+                               __shfl_down_sync(0xffffffffu, __uint_as_float(vh[q]), 1);
+                    if (p.epi == EPI_STORE) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const float x = o[q] + (p.bias ? p.bias[c0 + q] : 0.f);
+                            o[q] = p.relu ? fmaxf(x, 0.f) : x;
+                        }
+                    } else if (p.mask) {
+                        // EPI_MASK: the ReLU mask of the layer below. The window's 32 pixel rows x 32
+                        // channels are read row-contiguously by the warp (8 lanes per 128-byte row) into
+                        // the staging rows, then each lane takes its own row
+                        if (pending) {
+                            if (lane == 0) bulk_wait_read0();
+                            __syncwarp();
+                            pending = false;
+                        }
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int row = it * 4 + (lane >> 3), cq = lane & 7;
+                            const int wr = wfirst - 1 + row;
+                            float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (fn < p.img_n && wr >= 0 && wr < p.out_w)
+                                mv = *reinterpret_cast<const float4*>(
+                                    p.mask + ((static_cast<long long>(fn) * p.out_h + fh) * p.out_w + wr) * p.ldm + c0 +
+                                    4 * cq);
+                            *reinterpret_cast<float4*>(stage + row * 128 + ((cq ^ (row & 7)) << 4)) = mv;
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 mv = *reinterpret_cast<const float4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4));
+                            o[4 * q] = mv.x > 0.f ? o[4 * q] : 0.f;
+                            o[4 * q + 1] = mv.y > 0.f ? o[4 * q + 1] : 0.f;
+                            o[4 * q + 2] = mv.z > 0.f ? o[4 * q + 2] : 0.f;
+                            o[4 * q + 3] = mv.w > 0.f ? o[4 * q + 3] : 0.f;
+                        }
+                        __syncwarp();   // the output staging below rewrites these rows
+                    }
+                    if (p.store == ST_PIX4D) {
+                        // rows 1-30 staged as smem rows 0-29 (128B-swizzled), one TMA box of 30 pixels;
+                        // TMA clips the pixels past the image
+                        if (pending) {
+                            if (lane == 0) bulk_wait_read0();
+                            __syncwarp();
+                        }
+                        if (lane >= 1 && lane <= TC_FACT_WIN) {
+                            const int sr = lane - 1;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4*>(stage + sr * 128 + ((q ^ (sr & 7)) << 4)) =
+                                    make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        }
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && box_inside) {
+                            tma_store_4d(mD, c0, wfirst, fh, fn, stage);
+                            bulk_commit();
+                        }
+                        pending = true;
+                    } else if (out_row) {
+                        float* dst = p.D + pix * p.ldd + c0;
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4)
+                            *reinterpret_cast<float4*>(dst + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+                    }
                 }
                 continue;
             }

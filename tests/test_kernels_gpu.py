@@ -514,6 +514,10 @@ CONV_CASES = [
     (32, 5, 7, 256, 128),   # one tap per tile, split-K
     (32, 4, 6, 6, 32),      # Cin < 8: tap boxes of 8 channel rows, rows past Cin zero-filled
     (32, 3, 4, 128, 256),   # CTA pairs over Cout, packed taps of 128 rows
+    # 64 output channels on rows of >= 96 pixels: forward / input gradient factored over the kernel columns
+    (2, 4, 100, 64, 64),    # forward and input gradient factored; one 126-pixel tile per row
+    (2, 5, 130, 32, 64),    # forward factored, two tiles per row (the second holds 4 pixels)
+    (1, 3, 253, 64, 96),    # input gradient factored (k = 3 x 96), three tiles per row, odd tile count
 ]
 
 
