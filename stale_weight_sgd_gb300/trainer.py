@@ -161,6 +161,17 @@ class StaleSGD:
         else:
             self.rep_streams = [main] * self.R
             self.rep_ws = [self.ws] * self.R
+        # without replica streams, a conv layer's weight gradient runs on a stream of its
+        # own (with its own workspace) beside the input-gradient chain of the layers below,
+        # and the gradient buffers rotate through three so that it can still read its dy
+        # while the next two layers' gradients are written
+        self.split_bwd = concurrent and not self.fork and any(L.kind == "conv" for L in self.shapes)
+        if self.split_bwd:
+            self.dw_stream = torch.cuda.Stream(self.dev)
+            self.ws_dw = torch.empty(max(self.conv_ws_bytes // 4 + 64, 64), **f32)
+            self.gspare = torch.empty_like(self.g)
+            self.ev_gready = [torch.cuda.Event() for _ in self.shapes]
+            self.ev_dw = [torch.cuda.Event() for _ in self.shapes]
         self.K = self.RS + 2   # version v of layer l exists: ev_layer[l][v % K]
         self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
         self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
@@ -521,6 +532,12 @@ class StaleSGD:
                 cur = outs
         g = [self.g[r].data_ptr() for r in range(R)]
         h = [self.h[r].data_ptr() for r in range(R)]
+        # split backward: the three gradient buffers, and for each the event of the weight
+        # gradient still reading it (waited for before the buffer is written again)
+        bufs = [g, h, [self.gspare[r].data_ptr() for r in range(R)]] if self.split_bwd else None
+        readers = [None, None, None]
+        gi, hi, si = 0, 1, 2
+        dw_last = None
         gT = None   # g transposed, when the layer above wrote it
         hT_all = [self.hT[r].data_ptr() for r in range(R)]
         gT_all = [self.gT[r].data_ptr() for r in range(R)]
@@ -549,6 +566,38 @@ class StaleSGD:
                                         [WT(r, li) for r in range(R)] if prev is not None else None, g, relu_src,
                                         h if prev is not None else None, dw, db, 1.0, acc, N, L.cin, L.cout, ws, wsb,
                                         sh, xT1=xT1, dyT=gT, dxT=hT)
+            elif self.split_bwd:
+                if dw_last is None:   # the first conv layer: pick up the buffers the FC layers left
+                    gi = next(i for i, bb in enumerate(bufs) if bb is g)
+                    hi = next(i for i, bb in enumerate(bufs) if bb is h)
+                    si = 3 - gi - hi
+                g, h = bufs[gi], bufs[hi]
+                self.ev_gready[li].record(main)
+                self.dw_stream.wait_event(self.ev_gready[li])
+                dws = self.dw_stream.cuda_stream
+                for r in range(R):
+                    S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1,
+                                     self.ws_dw, self.ws_dw.numel() * 4, dws)
+                self.ev_dw[li].record(self.dw_stream)
+                readers[gi] = dw_last = self.ev_dw[li]
+                if prev is not None:
+                    if readers[hi] is not None:
+                        main.wait_event(readers[hi])
+                        readers[hi] = None
+                    for r in range(R):
+                        relu_src = None if prev.pool else inp[li][r]
+                        S.sprint_conv_dX(g[r], W(r, li), WT(r, li), relu_src, h[r], N, L.h, L.w, L.cin, L.cout, 1,
+                                         ws, wsb, sh)
+                    if prev.kind == "conv" and prev.pool:
+                        if readers[si] is not None:
+                            main.wait_event(readers[si])
+                            readers[si] = None
+                        for r in range(R):
+                            S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], bufs[si][r], N,
+                                              prev.h, prev.w, prev.cout, sh)
+                        gi, si = si, gi            # the routed gradient is next; h is free again
+                    else:
+                        gi, hi, si = hi, si, gi    # dx is next; the spare takes the next dx
             else:
                 def bwd(r, st, rws, rwsb, li=li, L=L, prev=prev, g=g, h=h, dw=dw, db=db):
                     S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1, rws,
@@ -566,11 +615,15 @@ class StaleSGD:
             if self._pushes(t):
                 self.ev_bwd[li].record(main)
                 upd.wait_event(self.ev_bwd[li])
+                if self.split_bwd and L.kind == "conv":
+                    upd.wait_event(self.ev_dw[li])
                 self._update_layer(t, li, upd)
                 if not graph:
                     self.ev_layer[li][(j + 1) % K].record(upd)
             if prev is None:
                 break
+            if self.split_bwd and L.kind == "conv":
+                continue   # the buffers rotated above
             if prev.kind == "conv" and prev.pool:
                 if L.kind == "fc":
                     # the FC input gradient (in h) routed through the pool into g (free), masked
@@ -581,6 +634,9 @@ class StaleSGD:
             else:
                 g, h = h, g
                 gT, hT_all, gT_all = hT, gT_all, hT_all
+        if dw_last is not None:
+            # the next step overwrites activations the weight gradients read
+            main.wait_event(dw_last)
         if graph:
             # join the update stream: the next replay starts after this step's updates
             self.ev_graph_upd.record(upd)

@@ -348,3 +348,36 @@ def test_graph_replay_matches_eager_bitwise(arch, batch, kw):
     if s_e is not None:
         assert np.array_equal(s_e, s_g)
 
+
+
+@pytest.mark.parametrize("arch,batch,kw", [
+    (TINY, 8, dict(optimizer="sgd", eta=0.01)),
+    (VGG_C_HALF, 4, dict(optimizer="momentum", eta=0.01, stage_delays=[3, 2, 1, 0])),
+], ids=["tiny", "vgg_c_pipeline"])
+def test_split_backward_matches_serial_bitwise(arch, batch, kw):
+    """Without replica streams the conv weight gradients run on a stream of their
+    own beside the input-gradient chain (three rotating gradient buffers): the
+    same kernels on the same data, so weights and losses equal the all-on-one-
+    stream run bit for bit, eager and graph-replayed."""
+    from stale_weight_sgd_gb300.model import VGG_C_STAGES
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+    kw = dict(kw)
+    if "stage_delays" in kw:
+        kw["stage_of_layer"] = VGG_C_STAGES
+    w0 = _dense_init(arch, 31)
+    batches = _batches(arch, 3, batch, 32)
+    out = []
+    for concurrent, graphs in ((False, False), (True, False), (True, True)):
+        tr = StaleSGD(_product_net(arch), batch, concurrent=concurrent, graphs=graphs, **kw)
+        assert tr.split_bwd == concurrent
+        tr.load_weights(w0)
+        tr.load_batches(batches)
+        losses = []
+        for _ in range(7):
+            tr.step()
+            losses.append(tr.step_loss())
+        out.append((tr.weights(), np.array(losses)))
+    for w, l in out[1:]:
+        assert np.isfinite(l).all()
+        assert np.array_equal(w, out[0][0])
+        assert np.array_equal(l, out[0][1])
