@@ -485,8 +485,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         tr.join()
         torch.cuda.synchronize()
         call_probe = CallProbe(sprint, torch)
-        saved = (tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook)
-        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook = False, tr.main_stream, False, None
+        saved = (tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd)
+        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd = False, tr.main_stream, False, None, False
         tr._graph_steps = False
         with torch.cuda.stream(tr.main_stream):
             call_probe.active = True
@@ -494,7 +494,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             tr.join()
             call_probe.active = False
         torch.cuda.synchronize()
-        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook = saved
+        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd = saved
         breakdown = call_probe.summary()
 
     imgs = R * N * args.steps * world

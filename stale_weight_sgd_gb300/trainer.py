@@ -161,17 +161,17 @@ class StaleSGD:
         else:
             self.rep_streams = [main] * self.R
             self.rep_ws = [self.ws] * self.R
-        # without replica streams, a conv layer's weight gradient runs on a stream of its
-        # own (with its own workspace) beside the input-gradient chain of the layers below,
-        # and the gradient buffers rotate through three so that it can still read its dy
-        # while the next two layers' gradients are written
-        self.split_bwd = concurrent and not self.fork and any(L.kind == "conv" for L in self.shapes)
+        # a conv layer's weight gradient runs on a stream of its own (per replica, with its
+        # own workspace) beside the input-gradient chain of the layers below, and the
+        # gradient buffers rotate through three so that it can still read its dy while the
+        # next two layers' gradients are written
+        self.split_bwd = concurrent and any(L.kind == "conv" for L in self.shapes)
         if self.split_bwd:
-            self.dw_stream = torch.cuda.Stream(self.dev)
-            self.ws_dw = torch.empty(max(self.conv_ws_bytes // 4 + 64, 64), **f32)
+            self.dw_streams = [torch.cuda.Stream(self.dev) for _ in range(self.R)]
+            self.ws_dw = [torch.empty(max(self.conv_ws_bytes // 4 + 64, 64), **f32) for _ in range(self.R)]
             self.gspare = torch.empty_like(self.g)
-            self.ev_gready = [torch.cuda.Event() for _ in self.shapes]
-            self.ev_dw = [torch.cuda.Event() for _ in self.shapes]
+            self.ev_gready = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
+            self.ev_dw = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
         self.K = self.RS + 2   # version v of layer l exists: ev_layer[l][v % K]
         self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
         self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
@@ -572,29 +572,36 @@ class StaleSGD:
                     hi = next(i for i, bb in enumerate(bufs) if bb is h)
                     si = 3 - gi - hi
                 g, h = bufs[gi], bufs[hi]
-                self.ev_gready[li].record(main)
-                self.dw_stream.wait_event(self.ev_gready[li])
-                dws = self.dw_stream.cuda_stream
-                for r in range(R):
+                rd_h, rd_s = readers[hi], readers[si]
+
+                def bwd(r, st, rws, rwsb, li=li, L=L, prev=prev, g=g, h=h, s_=bufs[si], dw=dw, db=db, rd_h=rd_h,
+                        rd_s=rd_s):
+                    stream = self.rep_streams[r] if self.fork else main
+                    dws = self.dw_streams[r]
+                    ev = self.ev_gready[li][r]
+                    ev.record(stream)
+                    dws.wait_event(ev)
                     S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1,
-                                     self.ws_dw, self.ws_dw.numel() * 4, dws)
-                self.ev_dw[li].record(self.dw_stream)
+                                     self.ws_dw[r], self.ws_dw[r].numel() * 4, dws.cuda_stream)
+                    self.ev_dw[li][r].record(dws)
+                    if prev is None:
+                        return
+                    if rd_h is not None:
+                        stream.wait_event(rd_h[r])
+                    relu_src = None if prev.pool else inp[li][r]
+                    S.sprint_conv_dX(g[r], W(r, li), WT(r, li), relu_src, h[r], N, L.h, L.w, L.cin, L.cout, 1,
+                                     rws, rwsb, st)
+                    if prev.kind == "conv" and prev.pool:
+                        if rd_s is not None:
+                            stream.wait_event(rd_s[r])
+                        S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], s_[r], N, prev.h,
+                                          prev.w, prev.cout, st)
+                self._per_replica(bwd, ("bwd", li))
                 readers[gi] = dw_last = self.ev_dw[li]
                 if prev is not None:
-                    if readers[hi] is not None:
-                        main.wait_event(readers[hi])
-                        readers[hi] = None
-                    for r in range(R):
-                        relu_src = None if prev.pool else inp[li][r]
-                        S.sprint_conv_dX(g[r], W(r, li), WT(r, li), relu_src, h[r], N, L.h, L.w, L.cin, L.cout, 1,
-                                         ws, wsb, sh)
+                    readers[hi] = None
                     if prev.kind == "conv" and prev.pool:
-                        if readers[si] is not None:
-                            main.wait_event(readers[si])
-                            readers[si] = None
-                        for r in range(R):
-                            S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], bufs[si][r], N,
-                                              prev.h, prev.w, prev.cout, sh)
+                        readers[si] = None
                         gi, si = si, gi            # the routed gradient is next; h is free again
                     else:
                         gi, hi, si = hi, si, gi    # dx is next; the spare takes the next dx
@@ -616,7 +623,8 @@ class StaleSGD:
                 self.ev_bwd[li].record(main)
                 upd.wait_event(self.ev_bwd[li])
                 if self.split_bwd and L.kind == "conv":
-                    upd.wait_event(self.ev_dw[li])
+                    for ev in self.ev_dw[li]:
+                        upd.wait_event(ev)
                 self._update_layer(t, li, upd)
                 if not graph:
                     self.ev_layer[li][(j + 1) % K].record(upd)
@@ -636,7 +644,8 @@ class StaleSGD:
                 gT, hT_all, gT_all = hT, gT_all, hT_all
         if dw_last is not None:
             # the next step overwrites activations the weight gradients read
-            main.wait_event(dw_last)
+            for ev in dw_last:
+                main.wait_event(ev)
         if graph:
             # join the update stream: the next replay starts after this step's updates
             self.ev_graph_upd.record(upd)

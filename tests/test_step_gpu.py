@@ -353,12 +353,15 @@ def test_graph_replay_matches_eager_bitwise(arch, batch, kw):
 @pytest.mark.parametrize("arch,batch,kw", [
     (TINY, 8, dict(optimizer="sgd", eta=0.01)),
     (VGG_C_HALF, 4, dict(optimizer="momentum", eta=0.01, stage_delays=[3, 2, 1, 0])),
-], ids=["tiny", "vgg_c_pipeline"])
+    (VGG_I_SMALL, 32, dict(replicas=3, max_delay=2, schedule_seed=4, eta=0.001)),
+], ids=["tiny", "vgg_c_pipeline", "vgg_i_small_3_replicas"])
 def test_split_backward_matches_serial_bitwise(arch, batch, kw):
-    """Without replica streams the conv weight gradients run on a stream of their
-    own beside the input-gradient chain (three rotating gradient buffers): the
-    same kernels on the same data, so weights and losses equal the all-on-one-
-    stream run bit for bit, eager and graph-replayed."""
+    """The conv weight gradients run on streams of their own (one per replica)
+    beside the input-gradient chain (three rotating gradient buffers), with or
+    without replica streams: the same kernels on the same data, so weights and
+    losses equal the all-on-one-stream run bit for bit, eager and (periodic
+    schedules) graph-replayed. Batch 32 takes the blocked weight-gradient copies
+    and the factored paths."""
     from stale_weight_sgd_gb300.model import VGG_C_STAGES
     from stale_weight_sgd_gb300.trainer import StaleSGD
     kw = dict(kw)
@@ -367,7 +370,8 @@ def test_split_backward_matches_serial_bitwise(arch, batch, kw):
     w0 = _dense_init(arch, 31)
     batches = _batches(arch, 3, batch, 32)
     out = []
-    for concurrent, graphs in ((False, False), (True, False), (True, True)):
+    runs = ((False, False), (True, False), (True, True)) if not kw.get("max_delay") else ((False, False), (True, False))
+    for concurrent, graphs in runs:
         tr = StaleSGD(_product_net(arch), batch, concurrent=concurrent, graphs=graphs, **kw)
         assert tr.split_bwd == concurrent
         tr.load_weights(w0)
