@@ -186,11 +186,31 @@ size_t sprint_conv_workspace_size(int op, int N, int H, int W, int Cin, int Cout
  * when above 32; the RGB input layer) both sums run in FP32 on the CUDA cores
  * from x and dy as they are, and the workspace holds one partial per launched
  * block (Cout * (9 * Cin + 1) floats each), added in block order; otherwise the
- * workspace holds the transposed copies x^T [Cin][H][W][N], dy^T
- * [Cout][Ho][Wo][N] of the TF32 tensor-core path and its partial sums.
+ * workspace holds the transposed copies x^T, dy^T of the TF32 tensor-core
+ * path ([C][H][W][N], or blocked [H][W*N/32][C][32] when N % 32 == 0) and its
+ * partial sums.
  * ws: see sprint_conv_workspace_size(SPRINT_CONV_DW, ...). */
 int sprint_conv_dW(const float* x, const float* dy, float* dw, float* db, float alpha, int accumulate, int N, int H,
                    int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes, sprint_stream_t stream);
+
+/* The weight gradient's copy of its input made ahead of time (no page
+ * counterpart: the re-layout the k-contiguous TF32 operands need, so a caller
+ * can make it while the forward pass runs). When the tensor-core weight
+ * gradient of this shape reads blocked copies (N % 32 == 0; plan field 11),
+ * sprint_conv_xT_size returns the bytes of x^T = x as [H][W*N/32][C][32]
+ * (pixels (h, w, n) with n fastest in blocks of 32 images, channel-major inside
+ * a block), else 0. sprint_conv_xT writes that copy of x (device [N][H][W][C])
+ * into xT (device, caller-owned; must not alias x); SPRINT_ERR_UNSUPPORTED when
+ * the size is 0. sprint_conv_dW_xT is sprint_conv_dW reading x^T from xT
+ * instead of forming it (xT must hold sprint_conv_xT's copy of this x; x is
+ * still read by the paths that do not use copies); its workspace is the same
+ * as sprint_conv_dW's (the x^T part is then left unused). */
+size_t sprint_conv_xT_size(int N, int H, int W, int Cin, int Cout, int pad);
+int sprint_conv_xT(const float* x, float* xT, int N, int H, int W, int Cin, int Cout, int pad,
+                   sprint_stream_t stream);
+int sprint_conv_dW_xT(const float* x, const float* xT, const float* dy, float* dw, float* db, float alpha,
+                      int accumulate, int N, int H, int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes,
+                      sprint_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * FC forward — the "fc" role of [S] Sec. 3.3 (m = N, n = m_l, k = m_{l-1}):

@@ -2319,10 +2319,51 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
     return check_launch(__func__);
 }
 
+static int conv_dW_impl(const char* fn, const float* x, const float* xT_given, const float* dy, float* dw, float* db,
+                        float alpha, int accumulate, int N, int H, int W, int Cin, int Cout, int pad, void* ws,
+                        size_t ws_bytes, sprint_stream_t stream);
+
 extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float* db, float alpha, int accumulate,
                               int N, int H, int W, int Cin, int Cout, int pad, void* ws, size_t ws_bytes,
                               sprint_stream_t stream) {
+    return conv_dW_impl(__func__, x, nullptr, dy, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, ws, ws_bytes,
+                        stream);
+}
+
+extern "C" size_t sprint_conv_xT_size(int N, int H, int W, int Cin, int Cout, int pad) {
+    if (check_conv_shape(__func__, N, H, W, Cin, Cout, pad) != SPRINT_OK) return 0;
+    const ConvPlan pl = plan_conv(SPRINT_CONV_DW, N, H, W, Cin, Cout, pad, false);
+    return pl.tc && pl.wg_blocked ? pl.ws_xT : 0;
+}
+
+extern "C" int sprint_conv_xT(const float* x, float* xT, int N, int H, int W, int Cin, int Cout, int pad,
+                              sprint_stream_t stream) {
     int rc = check_conv_shape(__func__, N, H, W, Cin, Cout, pad);
+    if (rc) return rc;
+    SPRINT_NONNULL(x, "x");
+    SPRINT_NONNULL(xT, "xT");
+    SPRINT_ALIGNED(x, "x");
+    SPRINT_ALIGNED(xT, "xT");
+    const ConvPlan pl = plan_conv(SPRINT_CONV_DW, N, H, W, Cin, Cout, pad, false);
+    SPRINT_REQUIRE(pl.tc && pl.wg_blocked, SPRINT_ERR_UNSUPPORTED,
+                   "%s: this shape's weight gradient reads no blocked copy (N %% 32 != 0 or no tensor-core path)",
+                   __func__);
+    return launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin,
+                            static_cast<long long>(N) * Cin, 32, static_cast<cudaStream_t>(stream), 32ll * Cin);
+}
+
+extern "C" int sprint_conv_dW_xT(const float* x, const float* xT, const float* dy, float* dw, float* db, float alpha,
+                                 int accumulate, int N, int H, int W, int Cin, int Cout, int pad, void* ws,
+                                 size_t ws_bytes, sprint_stream_t stream) {
+    SPRINT_NONNULL(xT, "xT");
+    return conv_dW_impl(__func__, x, xT, dy, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, ws, ws_bytes,
+                        stream);
+}
+
+static int conv_dW_impl(const char* fn, const float* x, const float* xT_given, const float* dy, float* dw, float* db,
+                        float alpha, int accumulate, int N, int H, int W, int Cin, int Cout, int pad, void* ws,
+                        size_t ws_bytes, sprint_stream_t stream) {
+    int rc = check_conv_shape(fn, N, H, W, Cin, Cout, pad);
     if (rc) return rc;
     SPRINT_NONNULL(x, "x");
     SPRINT_NONNULL(dy, "dy");
@@ -2331,13 +2372,16 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
     SPRINT_ALIGNED(dy, "dy");
     SPRINT_ALIGNED(dw, "dw");
     SPRINT_ALIGNED(db, "db");
+    SPRINT_ALIGNED(xT_given, "xT");
     const ConvPlan pl = plan_conv(SPRINT_CONV_DW, N, H, W, Cin, Cout, pad, false);
-    if ((rc = check_ws(__func__, ws, ws_bytes, pl.ws_total()))) return rc;
+    SPRINT_REQUIRE(!xT_given || (pl.tc && pl.wg_blocked), SPRINT_ERR_UNSUPPORTED,
+                   "%s: this shape's weight gradient reads no blocked copy of x", fn);
+    if ((rc = check_ws(fn, ws, ws_bytes, pl.ws_total()))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const long long P = static_cast<long long>(N) * Ho * Wo;
     char* wsb = static_cast<char*>(ws);
-    float* xT = reinterpret_cast<float*>(wsb);
+    float* xT = xT_given ? const_cast<float*>(xT_given) : reinterpret_cast<float*>(wsb);
     float* dyT = reinterpret_cast<float*>(wsb + pl.ws_xT);
     float* part = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT);
     float* csum = reinterpret_cast<float*>(wsb + pl.ws_xT + pl.ws_dyT + pl.ws_partial);
@@ -2352,8 +2396,8 @@ extern "C" int sprint_conv_dW(const float* x, const float* dy, float* dw, float*
         const long long x_dc = blk ? 32 : static_cast<long long>(H) * W * N;
         const long long y_db = blk ? static_cast<long long>(N) * Cout : N;
         const long long y_dc = blk ? 32 : static_cast<long long>(Ho) * Wo * N;
-        if ((rc = launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin, x_db, x_dc, s,
-                                   blk ? 32ll * Cin : 32)))
+        if (!xT_given && (rc = launch_transpose(x, xT, H * W, N, Cin, Cin, static_cast<long long>(H) * W * Cin, x_db,
+                                                x_dc, s, blk ? 32ll * Cin : 32)))
             return rc;
         // dy -> dy^T, with dedb from the same pass when asked for
         if (db) {

@@ -50,6 +50,9 @@ _SIGS = {
     "sprint_conv_dX": ([P, P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
     "sprint_conv_workspace_size": ([I, I, I, I, I, I, I], SZ),
     "sprint_conv_dW": ([P, P, P, P, F, I, I, I, I, I, I, I, P, SZ, P], I),
+    "sprint_conv_xT_size": ([I, I, I, I, I, I], SZ),
+    "sprint_conv_xT": ([P, P, I, I, I, I, I, I, P], I),
+    "sprint_conv_dW_xT": ([P, P, P, P, P, F, I, I, I, I, I, I, I, P, SZ, P], I),
     "sprint_fc_fwd": ([P, P, P, P, I, I, I, I, P], I),
     "sprint_fc_bwd": ([P, P, P, P, P, P, P, P, F, I, I, I, I, P, SZ, P], I),
     "sprint_fc_workspace_size": ([I, I, I, I], SZ),
@@ -188,6 +191,21 @@ def sprint_conv_dW(x, dy, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, ws
     return _check("sprint_conv_dW", lib().sprint_conv_dW(_p(x), _p(dy), _p(dw), _p(db), float(alpha),
                                                          int(accumulate), N, H, W, Cin, Cout, pad, _p(ws), ws_bytes,
                                                          _s(stream)))
+
+
+def sprint_conv_xT_size(N, H, W, Cin, Cout, pad=1) -> int:
+    return lib().sprint_conv_xT_size(N, H, W, Cin, Cout, pad)
+
+
+def sprint_conv_xT(x, xT, N, H, W, Cin, Cout, pad=1, stream=None):
+    return _check("sprint_conv_xT", lib().sprint_conv_xT(_p(x), _p(xT), N, H, W, Cin, Cout, pad, _s(stream)))
+
+
+def sprint_conv_dW_xT(x, xT, dy, dw, db, alpha, accumulate, N, H, W, Cin, Cout, pad, ws=None, ws_bytes=0,
+                      stream=None):
+    return _check("sprint_conv_dW_xT", lib().sprint_conv_dW_xT(_p(x), _p(xT), _p(dy), _p(dw), _p(db), float(alpha),
+                                                               int(accumulate), N, H, W, Cin, Cout, pad, _p(ws),
+                                                               ws_bytes, _s(stream)))
 
 
 def sprint_fc_fwd(x, w, b, y, N, in_, out, relu, stream=None):

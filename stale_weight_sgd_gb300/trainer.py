@@ -172,6 +172,13 @@ class StaleSGD:
             self.gspare = torch.empty_like(self.g)
             self.ev_gready = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
             self.ev_dw = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
+            # the weight gradients' copies of their inputs (blocked x^T), made on the weight-
+            # gradient streams during the forward pass, beside the forward GEMMs
+            self.xT_bufs = []
+            self.ev_xready = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
+            for L in self.shapes:
+                nb = S.sprint_conv_xT_size(self.N, L.h, L.w, L.cin, L.cout, 1) if L.kind == "conv" else 0
+                self.xT_bufs.append(torch.empty((self.R, (nb // 4 + 63) // 64 * 64), **f32) if nb else None)
         self.K = self.RS + 2   # version v of layer l exists: ev_layer[l][v % K]
         self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
         self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
@@ -519,6 +526,12 @@ class StaleSGD:
             outs = [self.outs[li][r].data_ptr() for r in range(R)]
             if L.kind == "conv":
                 def fwd(r, st, rws, rwsb, li=li, L=L, src=cur, outs=outs):
+                    if self.split_bwd and self.xT_bufs[li] is not None:
+                        ev = self.ev_xready[li][r]
+                        ev.record(self.rep_streams[r] if self.fork else main)
+                        dws = self.dw_streams[r]
+                        dws.wait_event(ev)
+                        S.sprint_conv_xT(src[r], self.xT_bufs[li][r], N, L.h, L.w, L.cin, L.cout, 1, dws.cuda_stream)
                     S.sprint_conv_fwd(src[r], W(r, li), B(r, li), outs[r], N, L.h, L.w, L.cin, L.cout, 1, 1, rws,
                                       rwsb, st)
                     if L.pool:
@@ -581,8 +594,13 @@ class StaleSGD:
                     ev = self.ev_gready[li][r]
                     ev.record(stream)
                     dws.wait_event(ev)
-                    S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1,
-                                     self.ws_dw[r], self.ws_dw[r].numel() * 4, dws.cuda_stream)
+                    if self.xT_bufs[li] is not None:   # x^T made during the forward pass, on this stream
+                        S.sprint_conv_dW_xT(inp[li][r], self.xT_bufs[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h,
+                                            L.w, L.cin, L.cout, 1, self.ws_dw[r], self.ws_dw[r].numel() * 4,
+                                            dws.cuda_stream)
+                    else:
+                        S.sprint_conv_dW(inp[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h, L.w, L.cin, L.cout, 1,
+                                         self.ws_dw[r], self.ws_dw[r].numel() * 4, dws.cuda_stream)
                     self.ev_dw[li][r].record(dws)
                     if prev is None:
                         return

@@ -638,3 +638,39 @@ def test_conv_pad0(S):
     y = torch.empty((N, H - 2, W - 2, Cout), dtype=torch.float32, device="cuda")
     S.sprint_conv_fwd(dev(x), dev(w), dev(b), y, N, H, W, Cin, Cout, 0, 0, None, 0)
     assert rel_inf(host(y), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("N,H,W,Cin,Cout", [(32, 6, 5, 64, 64), (64, 3, 3, 32, 48), (32, 5, 7, 256, 128),
+                                            (32, 3, 4, 128, 256), (32, 4, 6, 6, 32)])
+def test_conv_dw_with_precomputed_xT(S, N, H, W, Cin, Cout):
+    """sprint_conv_xT + sprint_conv_dW_xT: the copy made ahead of time is the one
+    the weight gradient would make, so dW and db equal sprint_conv_dW bit for bit."""
+    x, _, _ = _conv_inputs(12, N, H, W, Cin, Cout)
+    dy = _f32(12, "dy", (N, H, W, Cout))
+    n = S.sprint_conv_xT_size(N, H, W, Cin, Cout, 1)
+    assert n == 4 * N * H * W * Cin
+    xT = torch.empty(n // 4, dtype=torch.float32, device="cuda")
+    xd, dyd = dev(x), dev(dy)
+    S.sprint_conv_xT(xd, xT, N, H, W, Cin, Cout, 1)
+    ws, nb = _ws(S, S.SPRINT_CONV_DW, N, H, W, Cin, Cout)
+    out = []
+    for use_xT in (False, True):
+        dw = torch.full((Cout, 3, 3, Cin), 7.0, dtype=torch.float32, device="cuda")
+        db = torch.full((Cout,), 7.0, dtype=torch.float32, device="cuda")
+        if use_xT:
+            S.sprint_conv_dW_xT(xd, xT, dyd, dw, db, 1.0, 0, N, H, W, Cin, Cout, 1, ws, nb)
+        else:
+            S.sprint_conv_dW(xd, dyd, dw, db, 1.0, 0, N, H, W, Cin, Cout, 1, ws, nb)
+        out.append((host(dw), host(db)))
+    assert np.array_equal(out[0][0], out[1][0]) and np.array_equal(out[0][1], out[1][1])
+    dw_ref, _ = O.conv3x3_dw(x, dy)
+    assert rel_inf(out[1][0], dw_ref) <= TOL_TF32
+    _status_clean(S)
+
+
+def test_conv_xT_needs_blocked_copies(S):
+    """No blocked copy when the batch is not a multiple of 32: size 0, and the calls refuse."""
+    assert S.sprint_conv_xT_size(16, 8, 8, 64, 64, 1) == 0
+    x = torch.zeros(16 * 8 * 8 * 64, dtype=torch.float32, device="cuda")
+    with pytest.raises(S.SprintError):
+        S.sprint_conv_xT(x, x, 16, 8, 8, 64, 64, 1)
