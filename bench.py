@@ -452,24 +452,47 @@ def run_ours(args, cfg, rank, world, local_rank):
             dxs[b].copy_(hx, non_blocking=True)
             dys[b].copy_(hy, non_blocking=True)
 
-    for b in range(2):   # the step graphs read the batch buffers: capture for both
-        tr.set_batch_pool(dxs[b], dys[b])
+    if tr.lookahead:
+        # step i also issues step i + 1's forward pass: one pool of two batch slots
+        # (step t reads slot t % 2), step i + 1's copy made before step i is issued. The
+        # forward pass the last timed step issued ahead read the old pool: dropped, so
+        # the first step here computes its own (from its copied inputs)
+        tr.drop_lookahead()
+        pool_x = torch.empty((2 * R, N, feat), dtype=torch.float32, device=dev)
+        pool_y = torch.empty((2 * R, N), dtype=torch.int32, device=dev)
+        dxs = [pool_x[b * R:(b + 1) * R] for b in range(2)]
+        dys = [pool_y[b * R:(b + 1) * R] for b in range(2)]
+        tr.set_batch_pool(pool_x, pool_y)
         tr.prepare_graphs()
+    else:
+        for b in range(2):   # the step graphs read the batch buffers: capture for both
+            tr.set_batch_pool(dxs[b], dys[b])
+            tr.prepare_graphs()
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    h2d(0)
+    s0 = tr.t
+    if tr.lookahead:   # step t reads slot t % 2
+        h2d(s0 % 2)
+        h2d((s0 + 1) % 2)
+    else:              # step i reads buffer i % 2
+        h2d(0)
     for i in range(args.steps):
         b = i % 2
-        tr.set_batch_pool(dxs[b], dys[b])
-        tr.mark_inputs(cs)          # step i waits for its copy
+        if not tr.lookahead:
+            tr.set_batch_pool(dxs[b], dys[b])
+        tr.mark_inputs(cs)          # step i waits for its copy (and, ahead, step i + 1's)
         tr.step()
         tr.join()
         ev_done[b].record(main)
         with torch.cuda.stream(main):
             hloss[b].copy_(tr.loss, non_blocking=True)   # contiguous [R][4]; column 0 = replica loss
         ev_loss[b].record(main)
-        if i + 1 < args.steps:
+        if tr.lookahead:
+            if i + 2 <= args.steps:
+                cs.wait_event(ev_done[b])   # step i no longer reads its slot: step i + 2's goes there
+                h2d((s0 + i) % 2)
+        elif i + 1 < args.steps:
             cs.wait_event(ev_done[1 - b])   # step i-1 no longer reads the other buffer
             h2d(1 - b)
         if i > 0:
@@ -485,8 +508,12 @@ def run_ours(args, cfg, rank, world, local_rank):
         tr.join()
         torch.cuda.synchronize()
         call_probe = CallProbe(sprint, torch)
-        saved = (tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd)
+        saved = (tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd, tr.lookahead)
         tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd = False, tr.main_stream, False, None, False
+        # one whole step on one stream: the forward pass the last step issued ahead is
+        # dropped (finished above) and issued again inside the probed step
+        tr.drop_lookahead()
+        tr.lookahead = False
         tr._graph_steps = False
         with torch.cuda.stream(tr.main_stream):
             call_probe.active = True
@@ -494,7 +521,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             tr.join()
             call_probe.active = False
         torch.cuda.synchronize()
-        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd = saved
+        tr.fork, tr.upd_stream, tr.use_graphs, tr.span_hook, tr.split_bwd, tr.lookahead = saved
         breakdown = call_probe.summary()
 
     imgs = R * N * args.steps * world

@@ -372,8 +372,9 @@ int sprint_pool_bwd(const float* dy, const uint8_t* argmax, const float* pooled,
  *   loss    = (1/N) sum_n [log sum_c exp(z[n][c]) - z[n][label[n]]]
  *   dlogits = (softmax(z) - onehot(label)) / N
  * With reduction_sum != 0 the 1/N factors are dropped (literal Eq. (1) sum).
- * logits: device [N][C]; labels: device int32 [N], each in [0, C) (not
- * checked on the device: a label out of range gives an undefined row);
+ * logits: device [N][C]; labels: device int32 [N], each in [0, C) (a label
+ * out of range is not read through: that row adds nothing to the loss, its
+ * dlogits row is zero, and sprint_device_status reports flag 16);
  * loss: device fp32 scalar; dlogits: device [N][C] (may alias logits). */
 int sprint_softmax_xent(const float* logits, const int32_t* labels, int N, int C, float* loss, float* dlogits,
                         int reduction_sum, sprint_stream_t stream);

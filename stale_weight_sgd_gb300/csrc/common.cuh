@@ -39,6 +39,7 @@ enum : int {
     DEV_FLAG_WAIT_MMA = 2,        // MMA issuer gave up waiting for a loaded stage
     DEV_FLAG_WAIT_EPILOGUE = 4,   // epilogue gave up waiting for the accumulator
     DEV_FLAG_WAIT_SELFTEST = 8,   // sprint_selftest_bounded_wait's wait ran out (as it should)
+    DEV_FLAG_BAD_LABEL = 16,      // a class label outside [0, C): that row was left out of the loss
 };
 
 // largest number of problems one grouped launch takes (batched entry points

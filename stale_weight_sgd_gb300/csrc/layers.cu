@@ -527,7 +527,9 @@ struct XentTable {
     float* dlogits[kMaxGroup];
 };
 
-__global__ void __launch_bounds__(1024) softmax_xent_kernel(XentTable tab, int N, int C, float scale) {
+// A label outside [0, C) is not read through: that row's loss and gradient are
+// zero and DEV_FLAG_BAD_LABEL is set in the device status word.
+__global__ void __launch_bounds__(1024) softmax_xent_kernel(XentTable tab, int N, int C, float scale, int* status) {
     const float* logits = tab.logits[blockIdx.x];
     const int32_t* __restrict__ labels = tab.labels[blockIdx.x];
     float* __restrict__ loss = tab.loss[blockIdx.x];
@@ -546,17 +548,19 @@ __global__ void __launch_bounds__(1024) softmax_xent_kernel(XentTable tab, int N
 #pragma unroll
         for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         const int y = labels[r];
-        const float zy = z[y];
+        const bool ok = y >= 0 && y < C;
+        if (!ok && lane == 0 && status) atomicOr(status, DEV_FLAG_BAD_LABEL);
+        const float zy = ok ? z[y] : 0.f;
         const float lse = m + logf(s);
         const float inv = 1.f / s;
         float* d = dlogits + static_cast<long long>(r) * C;
         __syncwarp();
         for (int c = lane; c < C; c += 32) {
             const float p = expf(z[c] - m) * inv;
-            d[c] = (p - (c == y ? 1.f : 0.f)) * scale;
+            d[c] = ok ? (p - (c == y ? 1.f : 0.f)) * scale : 0.f;
         }
         __syncwarp();
-        acc += lse - zy;
+        if (ok) acc += lse - zy;
     }
     if (lane == 0) warp_loss[warp] = acc;
     __syncthreads();
@@ -569,7 +573,8 @@ __global__ void __launch_bounds__(1024) softmax_xent_kernel(XentTable tab, int N
 
 // Few classes (C <= 32): one row per thread; per-row losses are added by each
 // warp in row order and the warp sums in warp order (deterministic).
-__global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(XentTable tab, int N, int C, float scale) {
+__global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(XentTable tab, int N, int C, float scale,
+                                                                  int* status) {
     const float* logits = tab.logits[blockIdx.x];
     const int32_t* __restrict__ labels = tab.labels[blockIdx.x];
     float* __restrict__ loss = tab.loss[blockIdx.x];
@@ -588,10 +593,15 @@ __global__ void __launch_bounds__(1024) softmax_xent_rows_kernel(XentTable tab, 
             float s = 0.f;
             for (int c = 0; c < C; ++c) s += expf(z[c] - m);
             const int y = labels[r];
-            const float zy = z[y];
-            const float inv = 1.f / s;
-            row_loss = m + logf(s) - zy;
-            for (int c = 0; c < C; ++c) d[c] = (expf(z[c] - m) * inv - (c == y ? 1.f : 0.f)) * scale;
+            if (y >= 0 && y < C) {
+                const float zy = z[y];
+                const float inv = 1.f / s;
+                row_loss = m + logf(s) - zy;
+                for (int c = 0; c < C; ++c) d[c] = (expf(z[c] - m) * inv - (c == y ? 1.f : 0.f)) * scale;
+            } else {   // a label outside [0, C): not read through
+                if (status) atomicOr(status, DEV_FLAG_BAD_LABEL);
+                for (int c = 0; c < C; ++c) d[c] = 0.f;
+            }
         }
         // add this pass's 32 rows of the warp in row order
 #pragma unroll
@@ -708,9 +718,9 @@ int launch_xent(const float* const* logits, const int32_t* const* labels, float*
             t.dlogits[i] = dlogits[g0 + i];
         }
         if (C <= 32)
-            softmax_xent_rows_kernel<<<n, 1024, 0, s>>>(t, N, C, scale);
+            softmax_xent_rows_kernel<<<n, 1024, 0, s>>>(t, N, C, scale, device_status_ptr());
         else
-            softmax_xent_kernel<<<n, 1024, 0, s>>>(t, N, C, scale);
+            softmax_xent_kernel<<<n, 1024, 0, s>>>(t, N, C, scale, device_status_ptr());
         const int rc = check_launch("softmax_xent");
         if (rc) return rc;
     }

@@ -68,7 +68,8 @@ def fetch_push_max_lag(n_fetch, n_push):
 class StaleSGD:
     def __init__(self, net, batch, *, replicas=1, max_delay=0, schedule_seed=0, stage_of_layer=None,
                  stage_delays=None, hybrid_switch=None, n_fetch=None, n_push=None, optimizer="sgd", eta=0.01,
-                 nu=0.9, eps=1e-8, g0=0.1, weight_decay=0.0, concurrent=True, graphs="auto", device="cuda"):
+                 nu=0.9, eps=1e-8, g0=0.1, weight_decay=0.0, concurrent=True, graphs="auto", lookahead="auto",
+                 device="cuda"):
         """Delays: seeded per-replica delays up to max_delay (ASGD), fixed per-stage
         delays (pipeline: stage_of_layer, stage_delays; hybrid_switch = N_p turns
         them to 0 from step N_p on, "Pipelined training of deep CNNs with stale
@@ -82,7 +83,16 @@ class StaleSGD:
         the rest of the backward pass (False: everything on one stream).
         graphs: replay captured CUDA graphs of the step ("auto": when the delay
         schedule is periodic — pipeline stages or no delay — so the same few
-        steps recur; the seeded random ASGD schedule is issued step by step)."""
+        steps recur; the seeded random ASGD schedule is issued step by step).
+        lookahead: with pipeline stage delays, step t also issues the forward
+        pass of step t + 1, on a stream of its own beside step t's backward
+        pass: a stage whose weights are s_k >= 1 steps old needs none of step
+        t's updates ("Pipelined training of deep CNNs with stale weights"
+        Sec. 4.1: the stages of different minibatches run at the same time);
+        layers with s_k = 0 wait for step t's update of their weights. Two
+        activation sets alternate by step parity. The softmax then opens the
+        backward pass. Step t + 1's batch must be in the pool when step t is
+        issued ("auto": on for pipeline delays without replica streams)."""
         S.lib()  # fail loudly if the CUDA library is missing
         self.net = net
         self.shapes = layer_shapes(net)
@@ -143,6 +153,8 @@ class StaleSGD:
         # parameter span of each layer (W then b, padded): the per-layer update range
         ends = [L.w_off for L in self.shapes[1:]] + [self.n]
         self.span = [(L.w_off, e - L.w_off) for L, e in zip(self.shapes, ends)]
+        self.lookahead = (self.pipeline and concurrent and not (self.R > 1 and any(L.kind == "conv" for L in self.shapes))
+                          if lookahead == "auto" else bool(lookahead))
         self._alloc_acts()
 
         main = torch.cuda.current_stream(self.dev)
@@ -174,11 +186,12 @@ class StaleSGD:
             self.ev_dw = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
             # the weight gradients' copies of their inputs (blocked x^T), made on the weight-
             # gradient streams during the forward pass, beside the forward GEMMs
-            self.xT_bufs = []
             self.ev_xready = [[torch.cuda.Event() for _ in range(self.R)] for _ in self.shapes]
-            for L in self.shapes:
-                nb = S.sprint_conv_xT_size(self.N, L.h, L.w, L.cin, L.cout, 1) if L.kind == "conv" else 0
-                self.xT_bufs.append(torch.empty((self.R, (nb // 4 + 63) // 64 * 64), **f32) if nb else None)
+            for A in self._sets:
+                for li, L in enumerate(self.shapes):
+                    nb = S.sprint_conv_xT_size(self.N, L.h, L.w, L.cin, L.cout, 1) if L.kind == "conv" else 0
+                    A["xT"][li] = torch.empty((self.R, (nb // 4 + 63) // 64 * 64), **f32) if nb else None
+            self.xT_bufs = self._sets[0]["xT"]
         self.K = self.RS + 2   # version v of layer l exists: ev_layer[l][v % K]
         self.ev_layer = [[torch.cuda.Event() for _ in range(self.K)] for _ in self.shapes]
         self.ev_bwd = [torch.cuda.Event() for _ in self.shapes]
@@ -186,6 +199,17 @@ class StaleSGD:
             evs[0].record(main)
         self.ev_inputs = torch.cuda.Event()
         self.inputs_pending = False
+        # lookahead: the forward pass of step t + 1 on its own stream; _ahead = the step whose
+        # forward pass has been issued already (or None)
+        self.ahead_stream = torch.cuda.Stream(self.dev) if self.lookahead else None
+        self._ahead = None
+        self._ahead_graph = False   # that forward pass is part of a replayed (joined) step
+        self.ev_fwd_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_fwd_cap = torch.cuda.Event()
+        self.ev_dw_cap = [torch.cuda.Event() for _ in range(self.R)]
+        self.ev_bwd_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_ahead_fork = torch.cuda.Event()
+        self.ev_upd_cap = [torch.cuda.Event() for _ in self.shapes]   # per layer, inside one captured step
         self._sched = np.zeros((0, self.R), np.int32)
         self.batches_x = None
         self.batches_y = None
@@ -212,43 +236,50 @@ class StaleSGD:
             stride = (numel + 255) // 256 * 256
             return torch.empty((R, stride), dtype=dtype, device=self.dev)[:, :numel]
 
-        self.outs, self.pooled, self.argmax = [], [], []
-        # FC layers followed by an FC layer also keep their output transposed,
-        # [out + 1][N] with a last row of ones (the next layer's xT1 operand:
-        # its weight-gradient GEMM reads it as is and yields db in the same pass)
-        self.outsT = []
+        # one activation set per step parity when the next step's forward pass runs ahead
+        self._sets = []
         big = 0
         ws_bytes = 0
         conv_ws = 0
-        for li, L in enumerate(self.shapes):
-            if L.kind == "conv":
-                numel = N * L.h * L.w * L.cout
-                big = max(big, numel, N * L.h * L.w * L.cin)
-                self.outs.append(rows(numel))
-                if L.pool:
-                    ph, pw = L.out_hw
-                    self.pooled.append(rows(N * ph * pw * L.cout))
-                    self.argmax.append(rows(N * ph * pw * L.cout, torch.uint8))
+        for _ in range(2 if self.lookahead else 1):
+            outs, pooled, argmax = [], [], []
+            # FC layers followed by an FC layer also keep their output transposed,
+            # [out + 1][N] with a last row of ones (the next layer's xT1 operand:
+            # its weight-gradient GEMM reads it as is and yields db in the same pass)
+            outsT = []
+            for li, L in enumerate(self.shapes):
+                if L.kind == "conv":
+                    numel = N * L.h * L.w * L.cout
+                    big = max(big, numel, N * L.h * L.w * L.cin)
+                    outs.append(rows(numel))
+                    if L.pool:
+                        ph, pw = L.out_hw
+                        pooled.append(rows(N * ph * pw * L.cout))
+                        argmax.append(rows(N * ph * pw * L.cout, torch.uint8))
+                    else:
+                        pooled.append(None)
+                        argmax.append(None)
+                    for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX, S.SPRINT_CONV_DW):
+                        conv_ws = max(conv_ws, S.sprint_conv_workspace_size(op, N, L.h, L.w, L.cin, L.cout, 1))
                 else:
-                    self.pooled.append(None)
-                    self.argmax.append(None)
-                for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX, S.SPRINT_CONV_DW):
-                    conv_ws = max(conv_ws, S.sprint_conv_workspace_size(op, N, L.h, L.w, L.cin, L.cout, 1))
-            else:
-                numel = N * L.cout
-                big = max(big, numel, N * L.cin)
-                self.outs.append(rows(numel))
-                self.pooled.append(None)
-                self.argmax.append(None)
-                ws_bytes = max(ws_bytes, S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 1),
-                               S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 0))
-            nxt = self.shapes[li + 1] if li + 1 < len(self.shapes) else None
-            if L.kind == "fc" and nxt is not None and nxt.kind == "fc":
-                t = rows((L.cout + 1) * N)
-                t[:, L.cout * N:].fill_(1.0)
-                self.outsT.append(t)
-            else:
-                self.outsT.append(None)
+                    numel = N * L.cout
+                    big = max(big, numel, N * L.cin)
+                    outs.append(rows(numel))
+                    pooled.append(None)
+                    argmax.append(None)
+                    ws_bytes = max(ws_bytes, S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 1),
+                                   S.sprint_fc_batched_workspace_size(R, N, L.cin, L.cout, 0))
+                nxt = self.shapes[li + 1] if li + 1 < len(self.shapes) else None
+                if L.kind == "fc" and nxt is not None and nxt.kind == "fc":
+                    t = rows((L.cout + 1) * N)
+                    t[:, L.cout * N:].fill_(1.0)
+                    outsT.append(t)
+                else:
+                    outsT.append(None)
+            self._sets.append(dict(outs=outs, pooled=pooled, argmax=argmax, outsT=outsT, xT=[None] * len(outs)))
+        self.outs, self.pooled, self.argmax, self.outsT = (self._sets[0][k] for k in ("outs", "pooled", "argmax",
+                                                                                       "outsT"))
+        self._acts_par = 0   # the set holding the last issued step's forward pass
         self.g = rows(big)
         self.h = rows(big)
         # dE/dy of FC layers transposed ([out][N]), written by the dX GEMM of the layer above
@@ -256,12 +287,19 @@ class StaleSGD:
         self.hT = rows(big)
         self.ws = torch.empty(max(max(ws_bytes, conv_ws) // 4 + 64, 64), **f32)
         self.ws_bytes = self.ws.numel() * 4
+        # the forward pass that runs ahead has a workspace of its own
+        self.ws_ahead = torch.empty_like(self.ws) if self.lookahead else None
         self.conv_ws_bytes = conv_ws
-        # per-replica views (what a replica's pass reads and writes)
-        self.acts = [dict(outs=[o[r] for o in self.outs],
-                          pooled=[p[r] if p is not None else None for p in self.pooled],
-                          argmax=[a[r] if a is not None else None for a in self.argmax])
-                     for r in range(R)]
+
+    @property
+    def acts(self):
+        """Per-replica views of the last step's forward tensors (what replica r's
+        pass read and wrote): outs, pooled and argmax per layer."""
+        A = self._sets[self._acts_par]
+        return [dict(outs=[o[r] for o in A["outs"]],
+                     pooled=[p[r] if p is not None else None for p in A["pooled"]],
+                     argmax=[a[r] if a is not None else None for a in A["argmax"]])
+                for r in range(self.R)]
 
     # ------------------------------------------------------------------ data / weights
     def load_weights(self, dense: np.ndarray):
@@ -388,19 +426,21 @@ class StaleSGD:
         S.sprint_apply_update_t(self.optimizer, w_in, w_out, wT, st, bufs, rows, cols, self.eta, hp, sh, n_total=cnt,
                                 weight_decay=self.weight_decay)
 
-    def _per_replica(self, fn, tag=None):
+    def _per_replica(self, fn, tag=None, main=None, ws=None):
         """fn(r, stream_handle, ws, ws_bytes) for every replica: on the replica
         streams (forked from and joined back into the main stream) or in order
-        on the main stream. If span_hook is set, it is called with (tag, 0,
-        main stream) before the group and (tag, 1, main stream) after it has
-        joined, so events it records there bracket the whole group."""
-        main = self.main_stream
+        on the main stream (default: self.main_stream; ws: its workspace, default
+        self.ws). If span_hook is set, it is called with (tag, 0, main stream)
+        before the group and (tag, 1, main stream) after it has joined, so events
+        it records there bracket the whole group."""
+        main = self.main_stream if main is None else main
+        ws = self.ws if ws is None else ws
         hook = self.span_hook if tag is not None else None
         if hook:
             hook(tag, 0, main)
         if not self.fork:
             for r in range(self.R):
-                fn(r, main.cuda_stream, self.ws, self.ws_bytes)
+                fn(r, main.cuda_stream, ws, ws.numel() * 4)
         else:
             self.ev_fork.record(main)
             for r in range(self.R):
@@ -420,7 +460,12 @@ class StaleSGD:
         slots = tuple(self._version(t, r, li) % self.RS for r in range(self.R) for li in range(nL))
         bx = tuple(self.batches_x[(t * self.R + r) % P].data_ptr() for r in range(self.R))
         by = tuple(self.batches_y[(t * self.R + r) % P].data_ptr() for r in range(self.R))
-        return slots, self._cur(t) % 2, self._first(t), self._pushes(t), bx, by
+        key = (slots, self._cur(t) % 2, self._first(t), self._pushes(t), bx, by)
+        if self.lookahead:   # the captured step also holds step t + 1's forward pass
+            slots1 = tuple(self._version(t + 1, r, li) % self.RS for r in range(self.R) for li in range(nL))
+            bx1 = tuple(self.batches_x[((t + 1) * self.R + r) % P].data_ptr() for r in range(self.R))
+            key = key + (slots1, bx1, t % 2)
+        return key
 
     def _capture(self, t, key):
         """Captures step t's graph (not run): on a stream of our own (capture needs
@@ -431,11 +476,13 @@ class StaleSGD:
         g = torch.cuda.CUDAGraph()
         n0 = S.sprint_launch_count()
         self.main_stream = self._cap_stream
+        state = (self._ahead, self._ahead_graph, self._acts_par)   # issuing records them; capturing runs nothing
         try:
             with torch.cuda.graph(g, stream=self._cap_stream, capture_error_mode="relaxed"):
                 self._issue(t, graph=True)
         finally:
             self.main_stream = main
+            self._ahead, self._ahead_graph, self._acts_par = state
         self._graphs[key] = g
         self._graph_kernels[key] = S.sprint_launch_count() - n0
         self.graph_launch_adjust -= self._graph_kernels[key]   # captured, not run
@@ -468,7 +515,19 @@ class StaleSGD:
         main = self.main_stream
         if self.inputs_pending:
             main.wait_event(self.ev_inputs)
+            if self.lookahead:
+                self.ahead_stream.wait_event(self.ev_inputs)
             self.inputs_pending = False
+        if self._ahead == t:
+            if not self._ahead_graph:   # (a replayed step joined its forward pass ahead itself)
+                main.wait_event(self.ev_fwd_done[t % 2])   # this step's forward pass ran ahead
+        elif self.lookahead:
+            # prologue: the first step (or one after a step without lookahead) issues its
+            # own forward pass first
+            if self._graph_steps:
+                self.join()
+            self._issue_forward(t, False, main, self.ws)
+            self._ahead = None
         # Periodic schedules: once past the first S steps (whose versions are clamped
         # at 0) a step is a replay of the graph captured for its key. A captured step
         # ends with the update stream joined into the main stream, so replays are
@@ -484,28 +543,35 @@ class StaleSGD:
                 g.replay()
             self.graph_launch_adjust += self._graph_kernels[key]
             self._graph_steps = True
+            if self.lookahead:
+                self._ahead = t + 1
+                self._ahead_graph = True
+                self._acts_par = t % 2
+            self.gradbuf = self.gradbuf_sets[self._cur(t) % 2]
+            self.t = t + 1
+            return
+        if self._ahead == t and not self.lookahead:
+            # forward pass ahead issued while lookahead was on: this step has it already
+            self._ahead = None
+            dw_last = self._issue_backward(t, False)
+            if dw_last is not None:
+                for ev in dw_last:
+                    main.wait_event(ev)
             self.gradbuf = self.gradbuf_sets[self._cur(t) % 2]
             self.t = t + 1
             return
         self._issue(t, graph=False)
 
-    def _issue(self, t, graph):
-        """Issues step t (graph: being captured — no waits on events recorded by
-        earlier steps, no per-layer version events, the update stream joined at the end)."""
-        R, N, K = self.R, self.N, self.K
-        main, upd = self.main_stream, self.upd_stream
-        sh = main.cuda_stream
-        nL = len(self.shapes)
+    def _step_refs(self, t):
+        """Per-step constants: weight-version slots per replica and layer, the batch
+        indices, and pointer helpers into the weight ring."""
+        R, nL = self.R, len(self.shapes)
         row = self.n * 4
         ring, ringT = self.ring.data_ptr(), self.ringT.data_ptr()
         ver = [[self._version(t, r, li) for li in range(nL)] for r in range(R)]
         slot = [[v % self.RS for v in vr] for vr in ver]
-        j = self._cur(t)
-        gb = [self.gradbuf_sets[j % 2][r].data_ptr() for r in range(R)]
-        acc = 0 if self._first(t) else 1   # GradBuf: assign at a window's first step, add afterwards
         P = self.batches_x.shape[0]
         bidx = [(t * R + r) % P for r in range(R)]
-        ws, wsb = self.ws, self.ws_bytes
 
         def W(r, li):
             return ring + slot[r][li] * row + 4 * self.shapes[li].w_off
@@ -516,33 +582,78 @@ class StaleSGD:
         def WT(r, li):
             return ringT + slot[r][li] * row + 4 * self.shapes[li].w_off
 
-        # forward
+        return ver, bidx, W, B, WT
+
+    def _fwd_ptrs(self, t):
+        """Step t's layer inputs (per layer, per replica) and logits, in activation
+        set t % sets (no work issued)."""
+        R = self.R
+        A = self._sets[t % len(self._sets)]
+        _, bidx, _, _, _ = self._step_refs(t)
         cur = [self.batches_x[b].data_ptr() for b in bidx]
-        inp = [None] * nL
+        inp = []
+        for li, L in enumerate(self.shapes):
+            inp.append(cur)
+            if L.kind == "conv" and L.pool:
+                cur = [A["pooled"][li][r].data_ptr() for r in range(R)]
+            else:
+                cur = [A["outs"][li][r].data_ptr() for r in range(R)]
+        return inp, cur
+
+    def _issue_forward(self, t, graph, stream, ws, cap_waits=None):
+        """Forward pass of step t on `stream` into activation set t % sets (the
+        softmax opens the backward pass). Eagerly every layer first waits for the
+        version of its weights it reads; inside a capture, cap_waits {layer: event}
+        holds the updates of the same captured step it must follow."""
+        R, N, K = self.R, self.N, self.K
+        sh = stream.cuda_stream
+        A = self._sets[t % len(self._sets)]
+        ver, bidx, W, B, WT = self._step_refs(t)
+        wsb = ws.numel() * 4
+        cur = [self.batches_x[b].data_ptr() for b in bidx]
         for li, L in enumerate(self.shapes):
             if not graph:
-                main.wait_event(self.ev_layer[li][max(ver[r][li] for r in range(R)) % K])
-            inp[li] = cur
-            outs = [self.outs[li][r].data_ptr() for r in range(R)]
+                stream.wait_event(self.ev_layer[li][max(ver[r][li] for r in range(R)) % K])
+            elif cap_waits and li in cap_waits:
+                stream.wait_event(cap_waits[li])
+            outs = [A["outs"][li][r].data_ptr() for r in range(R)]
             if L.kind == "conv":
                 def fwd(r, st, rws, rwsb, li=li, L=L, src=cur, outs=outs):
-                    if self.split_bwd and self.xT_bufs[li] is not None:
+                    if self.split_bwd and A["xT"][li] is not None:
                         ev = self.ev_xready[li][r]
-                        ev.record(self.rep_streams[r] if self.fork else main)
+                        ev.record(self.rep_streams[r] if self.fork else stream)
                         dws = self.dw_streams[r]
                         dws.wait_event(ev)
-                        S.sprint_conv_xT(src[r], self.xT_bufs[li][r], N, L.h, L.w, L.cin, L.cout, 1, dws.cuda_stream)
+                        S.sprint_conv_xT(src[r], A["xT"][li][r], N, L.h, L.w, L.cin, L.cout, 1, dws.cuda_stream)
                     S.sprint_conv_fwd(src[r], W(r, li), B(r, li), outs[r], N, L.h, L.w, L.cin, L.cout, 1, 1, rws,
                                       rwsb, st)
                     if L.pool:
-                        S.sprint_pool_fwd(outs[r], self.pooled[li][r], self.argmax[li][r], N, L.h, L.w, L.cout, st)
-                self._per_replica(fwd, ("fwd", li))
-                cur = [self.pooled[li][r].data_ptr() for r in range(R)] if L.pool else outs
+                        S.sprint_pool_fwd(outs[r], A["pooled"][li][r], A["argmax"][li][r], N, L.h, L.w, L.cout, st)
+                self._per_replica(fwd, ("fwd", li), main=stream, ws=ws)
+                cur = [A["pooled"][li][r].data_ptr() for r in range(R)] if L.pool else outs
             else:
-                yT = None if self.outsT[li] is None else [self.outsT[li][r].data_ptr() for r in range(R)]
+                yT = None if A["outsT"][li] is None else [A["outsT"][li][r].data_ptr() for r in range(R)]
                 S.sprint_fc_fwd_batched(cur, [W(r, li) for r in range(R)], [B(r, li) for r in range(R)], outs, N,
                                         L.cin, L.cout, int(L.relu), ws, wsb, sh, yT=yT)
                 cur = outs
+        self._acts_par = t % len(self._sets)
+
+    def _issue_backward(self, t, graph):
+        """Softmax cross-entropy and backward pass of step t (reading activation set
+        t % sets), each layer's update on the update stream as soon as its
+        gradients are final. Returns the events of the weight-gradient streams the
+        step's end must wait for (or None)."""
+        R, N, K = self.R, self.N, self.K
+        main, upd = self.main_stream, self.upd_stream
+        sh = main.cuda_stream
+        nL = len(self.shapes)
+        A = self._sets[t % len(self._sets)]
+        ver, bidx, W, B, WT = self._step_refs(t)
+        inp, logits = self._fwd_ptrs(t)
+        j = self._cur(t)
+        gb = [self.gradbuf_sets[j % 2][r].data_ptr() for r in range(R)]
+        acc = 0 if self._first(t) else 1   # GradBuf: assign at a window's first step, add afterwards
+        ws, wsb = self.ws, self.ws_bytes
         g = [self.g[r].data_ptr() for r in range(R)]
         h = [self.h[r].data_ptr() for r in range(R)]
         # split backward: the three gradient buffers, and for each the event of the weight
@@ -554,7 +665,7 @@ class StaleSGD:
         gT = None   # g transposed, when the layer above wrote it
         hT_all = [self.hT[r].data_ptr() for r in range(R)]
         gT_all = [self.gT[r].data_ptr() for r in range(R)]
-        S.sprint_softmax_xent_batched(cur, [self.batches_y[b].data_ptr() for b in bidx],
+        S.sprint_softmax_xent_batched(logits, [self.batches_y[b].data_ptr() for b in bidx],
                                       [self.loss[r].data_ptr() for r in range(R)], g, N, self.classes, 0, sh)
 
         # backward (g holds dE/d(pre-activation output) of layer li)
@@ -572,8 +683,8 @@ class StaleSGD:
                 if prev is not None and not (prev.kind == "conv" and prev.pool) and prev.relu:
                     relu_src = inp[li]
                 xT1 = None
-                if prev is not None and self.outsT[li - 1] is not None:
-                    xT1 = [self.outsT[li - 1][r].data_ptr() for r in range(R)]
+                if prev is not None and A["outsT"][li - 1] is not None:
+                    xT1 = [A["outsT"][li - 1][r].data_ptr() for r in range(R)]
                     hT = hT_all   # the layer below is FC too: it reads dE/dy transposed
                 S.sprint_fc_bwd_batched(inp[li], [W(r, li) for r in range(R)],
                                         [WT(r, li) for r in range(R)] if prev is not None else None, g, relu_src,
@@ -594,8 +705,8 @@ class StaleSGD:
                     ev = self.ev_gready[li][r]
                     ev.record(stream)
                     dws.wait_event(ev)
-                    if self.xT_bufs[li] is not None:   # x^T made during the forward pass, on this stream
-                        S.sprint_conv_dW_xT(inp[li][r], self.xT_bufs[li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h,
+                    if A["xT"][li] is not None:   # x^T made during the forward pass, on this stream
+                        S.sprint_conv_dW_xT(inp[li][r], A["xT"][li][r], g[r], dw[r], db[r], 1.0, acc, N, L.h,
                                             L.w, L.cin, L.cout, 1, self.ws_dw[r], self.ws_dw[r].numel() * 4,
                                             dws.cuda_stream)
                     else:
@@ -612,7 +723,7 @@ class StaleSGD:
                     if prev.kind == "conv" and prev.pool:
                         if rd_s is not None:
                             stream.wait_event(rd_s[r])
-                        S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], s_[r], N, prev.h,
+                        S.sprint_pool_bwd(h[r], A["argmax"][li - 1][r], A["pooled"][li - 1][r], s_[r], N, prev.h,
                                           prev.w, prev.cout, st)
                 self._per_replica(bwd, ("bwd", li))
                 readers[gi] = dw_last = self.ev_dw[li]
@@ -633,7 +744,7 @@ class StaleSGD:
                                          rws, rwsb, st)
                         if prev.kind == "conv" and prev.pool:
                             # g[r] (free) <- routed gradient of the pre-pool ReLU output, masked
-                            S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], g[r], N, prev.h,
+                            S.sprint_pool_bwd(h[r], A["argmax"][li - 1][r], A["pooled"][li - 1][r], g[r], N, prev.h,
                                               prev.w, prev.cout, st)
                 self._per_replica(bwd, ("bwd", li))
             # layer li's gradients are final: its update overlaps the layers below
@@ -646,6 +757,8 @@ class StaleSGD:
                 self._update_layer(t, li, upd)
                 if not graph:
                     self.ev_layer[li][(j + 1) % K].record(upd)
+                else:
+                    self.ev_upd_cap[li].record(upd)   # the forward pass running ahead may wait for it
             if prev is None:
                 break
             if self.split_bwd and L.kind == "conv":
@@ -654,17 +767,57 @@ class StaleSGD:
                 if L.kind == "fc":
                     # the FC input gradient (in h) routed through the pool into g (free), masked
                     for r in range(R):
-                        S.sprint_pool_bwd(h[r], self.argmax[li - 1][r], self.pooled[li - 1][r], g[r], N, prev.h,
+                        S.sprint_pool_bwd(h[r], A["argmax"][li - 1][r], A["pooled"][li - 1][r], g[r], N, prev.h,
                                           prev.w, prev.cout, sh)
                 # the conv branch routed into g already: g holds the next layer's gradient
             else:
                 g, h = h, g
                 gT, hT_all, gT_all = hT, gT_all, hT_all
+        return dw_last
+
+    def _issue(self, t, graph):
+        """Issues step t (graph: being captured — no waits on events recorded by
+        earlier steps, no per-layer version events, the update stream joined at the
+        end). With lookahead, step t's forward pass was issued before (ahead, or as
+        the prologue) and step t + 1's is issued here beside the backward pass."""
+        main, upd = self.main_stream, self.upd_stream
+        j = self._cur(t)
+        if not self.lookahead:
+            self._issue_forward(t, graph, main, self.ws)
+            dw_last = self._issue_backward(t, graph)
+        else:
+            ahead = self.ahead_stream
+            if graph:
+                self.ev_ahead_fork.record(main)   # the forward pass ahead depends on nothing before it
+            dw_last = self._issue_backward(t, graph)
+            if graph:
+                ahead.wait_event(self.ev_ahead_fork)
+                # layers whose step-(t + 1) weights are this step's update follow it
+                waits = {li: self.ev_upd_cap[li] for li in range(len(self.shapes))
+                         if self._pushes(t) and max(self._version(t + 1, r, li) for r in range(self.R)) > j}
+            else:
+                ahead.wait_event(self.ev_bwd_done[(t + 1) % 2])   # step t - 1 no longer reads that set
+                waits = None
+            self._issue_forward(t + 1, graph, ahead, self.ws_ahead, waits)
+            # (an event recorded inside a capture cannot be waited for outside it: captures
+            # join the forward pass ahead through an event of their own)
+            (self.ev_fwd_cap if graph else self.ev_fwd_done[(t + 1) % 2]).record(ahead)
+            self._ahead = t + 1
+            self._ahead_graph = graph
+            self._acts_par = t % 2   # tr.acts: the step being issued
         if dw_last is not None:
             # the next step overwrites activations the weight gradients read
             for ev in dw_last:
                 main.wait_event(ev)
+        if self.lookahead and not graph:
+            self.ev_bwd_done[t % 2].record(main)
         if graph:
+            if self.lookahead:   # join the forward pass ahead (and its x^T copies)
+                main.wait_event(self.ev_fwd_cap)
+                if self.split_bwd:
+                    for r in range(self.R):
+                        self.ev_dw_cap[r].record(self.dw_streams[r])
+                        main.wait_event(self.ev_dw_cap[r])
             # join the update stream: the next replay starts after this step's updates
             self.ev_graph_upd.record(upd)
             main.wait_event(self.ev_graph_upd)
@@ -677,6 +830,8 @@ class StaleSGD:
         issued so far (the last step's updates may still run on the update
         stream when step() returns)."""
         st = self.main_stream if stream is None else stream
+        if self._ahead is not None and not self._ahead_graph:   # the forward pass running ahead
+            st.wait_event(self.ev_fwd_done[self._ahead % 2])
         if self._graph_steps:   # graph replays end with the update stream joined
             if st is not self.main_stream:
                 ev = torch.cuda.Event()
@@ -685,6 +840,15 @@ class StaleSGD:
             return
         for evs in self.ev_layer:
             st.wait_event(evs[self._cur(self.t) % self.K])
+
+    def drop_lookahead(self):
+        """Waits for the forward pass issued ahead (if any) and forgets it: the next
+        step issues its own forward pass again (after the batch pool or the weights
+        were changed from outside, or to time one whole step)."""
+        self.join()
+        self.main_stream.synchronize()
+        self._ahead = None
+        self._ahead_graph = False
 
     def step_loss(self) -> float:
         """Mean over replicas of the last step's loss (synchronises)."""

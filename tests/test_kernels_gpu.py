@@ -674,3 +674,25 @@ def test_conv_xT_needs_blocked_copies(S):
     x = torch.zeros(16 * 8 * 8 * 64, dtype=torch.float32, device="cuda")
     with pytest.raises(S.SprintError):
         S.sprint_conv_xT(x, x, 16, 8, 8, 64, 64, 1)
+
+
+@pytest.mark.parametrize("C", [10, 1000])
+def test_softmax_xent_label_out_of_range(S, C):
+    """A label outside [0, C) is not read through: the row adds nothing to the
+    loss, its gradient row is zero, the other rows are as usual, and the device
+    status word reports it (flag 16)."""
+    N = 6
+    z = _f32(15, f"zb{C}", (N, C), 2.0)
+    y = synth.labels(15, f"yb{C}", N, C)
+    bad = y.copy()
+    bad[2], bad[4] = C, -1
+    loss = torch.zeros(4, dtype=torch.float32, device="cuda")
+    dz = torch.empty((N, C), dtype=torch.float32, device="cuda")
+    S.sprint_device_status(reset=True)
+    S.sprint_softmax_xent(dev(z), dev(bad), N, C, loss, dz)
+    assert S.sprint_device_status(reset=True) == 16
+    good = [0, 1, 3, 5]
+    loss_ref, dz_ref = O.softmax_xent(z[good], y[good])
+    assert abs(host(loss)[0] - loss_ref * len(good) / N) <= 1e-5 * abs(loss_ref)
+    assert rel_inf(host(dz)[good], dz_ref * len(good) / N) <= TOL_FP32
+    assert not host(dz)[[2, 4]].any()

@@ -385,3 +385,39 @@ def test_split_backward_matches_serial_bitwise(arch, batch, kw):
         assert np.isfinite(l).all()
         assert np.array_equal(w, out[0][0])
         assert np.array_equal(l, out[0][1])
+
+
+@pytest.mark.parametrize("graphs,batch", [(False, 4), (True, 4), (True, 32)],
+                         ids=["eager", "graphs", "graphs_batch32"])
+def test_lookahead_forward_matches_in_order_bitwise(graphs, batch):
+    """Pipeline stage delays let step t + 1's forward pass run beside step t's
+    backward pass (two activation sets by step parity; layers with delay 0 wait
+    for step t's update). Same kernels on the same data and weight versions:
+    weights, losses and saved activations equal the in-order run bit for bit,
+    also across the hybrid switch to zero delays. Batch 32 adds the weight
+    gradients' x^T copies made during the forward pass that runs ahead."""
+    from stale_weight_sgd_gb300.model import VGG_C_STAGES
+    from stale_weight_sgd_gb300.trainer import StaleSGD
+    arch = VGG_C_HALF
+    kw = dict(optimizer="momentum", eta=0.01, stage_of_layer=VGG_C_STAGES, stage_delays=[3, 2, 1, 0],
+              hybrid_switch=6)
+    w0 = _dense_init(arch, 41)
+    batches = _batches(arch, 3, batch, 42)
+    out = []
+    for lookahead in (False, True):
+        tr = StaleSGD(_product_net(arch), batch, graphs=graphs, lookahead=lookahead, **kw)
+        assert tr.lookahead == lookahead
+        tr.load_weights(w0)
+        tr.load_batches(batches)
+        losses, acts = [], []
+        for _ in range(10):
+            tr.step()
+            losses.append(tr.step_loss())
+            acts.append(np.concatenate([a.cpu().numpy().ravel() for a in tr.acts[0]["outs"]]))
+        out.append((tr.weights(), np.array(losses), acts))
+    (w0_, l0, a0), (w1, l1, a1) = out
+    assert np.isfinite(l0).all()
+    assert np.array_equal(w0_, w1)
+    assert np.array_equal(l0, l1)
+    for x, y in zip(a0, a1):
+        assert np.array_equal(x, y)
