@@ -791,17 +791,19 @@ int launch_smallk_dx4(const float* const* dy, const float* const* w, const float
 // Forward convolution with very few input channels (the RGB layer, CIN <= 4,
 // Cout % 16 == 0). Its 9*CIN-long reduction makes it bound by writing y, not by
 // arithmetic (~14 FLOP per output byte), so it runs on the CUDA cores: a
-// thread owns two horizontally adjacent output pixels x 16 consecutive output
-// channels, loads their shared 3x4xCIN input window once (zero outside the
-// image), and reads the weights — staged per block in shared memory as
-// [tap*CIN+ci][co] — as four float4 per tap, each used for both pixels; bias
-// and ReLU are fused and y is written as float4. The 32 lanes of a warp take 32
-// consecutive pixel pairs of the same channel group, so every weight read is a
-// shared-memory broadcast (lanes of different groups in one warp read rows 64 B
-// apart: bank conflicts, measured 10x slower). With one pixel per thread the
-// weight reads kept the shared-memory pipe 89% busy (ncu) at ~1.3 TB/s of
-// output; two pixels per read halve them.
-template <int CIN>
+// thread owns PX horizontally adjacent output pixels x 16 consecutive output
+// channels, loads their shared 3 x (PX+2) x CIN input window once (zero
+// outside the image), and reads the weights — staged per block in shared
+// memory as [tap*CIN+ci][co] — as four float4 per tap, each used for all PX
+// pixels; bias and ReLU are fused and y is written as float4. The 32 lanes of
+// a warp take 32 consecutive pixel groups of the same channel group, so every
+// weight read is a shared-memory broadcast (lanes of different groups in one
+// warp read rows 64 B apart: bank conflicts, measured 10x slower). With one
+// pixel per thread the weight reads kept the shared-memory pipe 89% busy (ncu)
+// at ~1.3 TB/s of output; PX pixels per read divide them by PX. PX = 2:
+// 0.58 -> 0.46 ms at VGG-I's conv1_1, batch 64; PX = 4 needs 188 registers (one
+// block per SM) and took 0.49 ms.
+template <int CIN, int PX>
 __global__ void __launch_bounds__(256) conv_smallc_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                               const float* __restrict__ b, float* __restrict__ y, int N,
                                                               int H, int W, int Cout, int pad, int relu) {
@@ -814,65 +816,67 @@ __global__ void __launch_bounds__(256) conv_smallc_fwd_kernel(const float* __res
     for (int i = threadIdx.x; i < Cout; i += blockDim.x) bs[i] = b ? b[i] : 0.f;
     __syncthreads();
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
-    const int Wp = (Wo + 1) / 2;                     // pixel pairs per output row
+    const int Wp = (Wo + PX - 1) / PX;               // pixel groups per output row
     const int groups = Cout / 16;
     const int P2 = N * Ho * Wp;                      // < 2^31 (checked by the caller)
-    const int pair_blocks = (P2 + 31) / 32;          // 32-pair warp tasks per channel group
-    const int tasks = pair_blocks * groups;
+    const int grp_blocks = (P2 + 31) / 32;           // 32-group warp tasks per channel group
+    const int tasks = grp_blocks * groups;
     const int warp_gid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int task = warp_gid; task < tasks; task += warps) {
         const int g = task % groups;
         const int pp = (task / groups) * 32 + lane;
         if (pp >= P2) continue;
-        const int ow = (pp % Wp) * 2;
+        const int ow = (pp % Wp) * PX;
         const int t = pp / Wp;
         const int oh = t % Ho;
         const long long n = t / Ho;
-        float in[3][4][CIN];   // input rows oh-pad .. +2, columns ow-pad .. +3
+        float in[3][PX + 2][CIN];   // input rows oh-pad .. +2, columns ow-pad .. ow-pad+PX+1
 #pragma unroll
         for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < PX + 2; ++c) {
                 const int ih = oh + kh - pad, iw = ow + c - pad;
                 const bool ok = ih >= 0 && ih < H && iw >= 0 && iw < W;
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) in[kh][c][ci] = ok ? __ldg(x + ((n * H + ih) * W + iw) * CIN + ci) : 0.f;
             }
         const int co0 = g * 16;
-        float acc0[16], acc1[16];
+        float acc[PX][16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc0[q] = acc1[q] = bs[co0 + q];
+        for (int q = 0; q < 16; ++q) {
+            const float bq = bs[co0 + q];
+#pragma unroll
+            for (int u = 0; u < PX; ++u) acc[u][q] = bq;
+        }
 #pragma unroll
         for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
             for (int kw = 0; kw < 3; ++kw)
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) {
-                    const float a0 = in[kh][kw][ci], a1 = in[kh][kw + 1][ci];
                     const float4* wr = reinterpret_cast<const float4*>(ws + ((kh * 3 + kw) * CIN + ci) * Cout + co0);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
                         const float4 wv = wr[v4];
-                        acc0[4 * v4 + 0] = fmaf(a0, wv.x, acc0[4 * v4 + 0]);
-                        acc0[4 * v4 + 1] = fmaf(a0, wv.y, acc0[4 * v4 + 1]);
-                        acc0[4 * v4 + 2] = fmaf(a0, wv.z, acc0[4 * v4 + 2]);
-                        acc0[4 * v4 + 3] = fmaf(a0, wv.w, acc0[4 * v4 + 3]);
-                        acc1[4 * v4 + 0] = fmaf(a1, wv.x, acc1[4 * v4 + 0]);
-                        acc1[4 * v4 + 1] = fmaf(a1, wv.y, acc1[4 * v4 + 1]);
-                        acc1[4 * v4 + 2] = fmaf(a1, wv.z, acc1[4 * v4 + 2]);
-                        acc1[4 * v4 + 3] = fmaf(a1, wv.w, acc1[4 * v4 + 3]);
+#pragma unroll
+                        for (int u = 0; u < PX; ++u) {
+                            const float a = in[kh][kw + u][ci];
+                            acc[u][4 * v4 + 0] = fmaf(a, wv.x, acc[u][4 * v4 + 0]);
+                            acc[u][4 * v4 + 1] = fmaf(a, wv.y, acc[u][4 * v4 + 1]);
+                            acc[u][4 * v4 + 2] = fmaf(a, wv.z, acc[u][4 * v4 + 2]);
+                            acc[u][4 * v4 + 3] = fmaf(a, wv.w, acc[u][4 * v4 + 3]);
+                        }
                     }
                 }
         const long long pix = (n * Ho + oh) * Wo + ow;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (u == 1 && ow + 1 >= Wo) break;
-            const float* acc = u == 0 ? acc0 : acc1;
+        for (int u = 0; u < PX; ++u) {
+            if (ow + u >= Wo) break;
             float4* dst = reinterpret_cast<float4*>(y + (pix + u) * Cout + co0);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
-                float4 o = make_float4(acc[4 * v4], acc[4 * v4 + 1], acc[4 * v4 + 2], acc[4 * v4 + 3]);
+                float4 o = make_float4(acc[u][4 * v4], acc[u][4 * v4 + 1], acc[u][4 * v4 + 2], acc[u][4 * v4 + 3]);
                 if (relu) {
                     o.x = fmaxf(o.x, 0.f);
                     o.y = fmaxf(o.y, 0.f);
@@ -885,22 +889,26 @@ __global__ void __launch_bounds__(256) conv_smallc_fwd_kernel(const float* __res
     }
 }
 
+// pixels per thread of the RGB-layer forward
+constexpr int kSmallcFwdPx = 2;
+
 int launch_conv_smallc(const float* x, const float* w, const float* b, float* y, int N, int H, int W, int Cin,
                        int Cout, int pad, int relu, cudaStream_t s) {
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const long long P = static_cast<long long>(N) * Ho * Wo;
     SPRINT_REQUIRE(P < (1ll << 31) - 32, SPRINT_ERR_SHAPE, "conv_fwd: %lld output pixels", P);
-    const long long pairs = static_cast<long long>(N) * Ho * ((Wo + 1) / 2);
-    const long long total = ((pairs + 31) / 32) * 32 * (Cout / 16);   // threads: one per pixel pair and group
+    constexpr int PX = kSmallcFwdPx;
+    const long long pairs = static_cast<long long>(N) * Ho * ((Wo + PX - 1) / PX);
+    const long long total = ((pairs + 31) / 32) * 32 * (Cout / 16);   // threads: one per pixel group and channel group
     const size_t smem = (static_cast<size_t>(9) * Cin * Cout + Cout) * sizeof(float);
     long long g = (total + 255) / 256;
     if (g > 16ll * num_sms()) g = 16ll * num_sms();
     const int grid = static_cast<int>(g < 1 ? 1 : g);
     switch (Cin) {
-        case 1: conv_smallc_fwd_kernel<1><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
-        case 2: conv_smallc_fwd_kernel<2><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
-        case 3: conv_smallc_fwd_kernel<3><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
-        default: conv_smallc_fwd_kernel<4><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        case 1: conv_smallc_fwd_kernel<1, PX><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        case 2: conv_smallc_fwd_kernel<2, PX><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        case 3: conv_smallc_fwd_kernel<3, PX><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
+        default: conv_smallc_fwd_kernel<4, PX><<<grid, 256, smem, s>>>(x, w, b, y, N, H, W, Cout, pad, relu); break;
     }
     return check_launch("conv_smallc_fwd_kernel");
 }
