@@ -815,11 +815,15 @@ KERNELS = {
     "conv_fwd": "conv forward, VGG conv3_2 shape 56x56x256->256, batch 16 (TF32 implicit GEMM)",
     "conv_dx": "conv input gradient, VGG conv3_2 shape, batch 16",
     "conv_dw": "conv weight gradient, VGG conv3_2 shape, batch 16",
+    "conv_dw_xT": "conv weight gradient with the x^T copy made ahead (as the training step calls it, "
+                  "sprint_conv_dW_xT), VGG conv3_2 shape, batch 16 (use --batch 64 for the blocked copies)",
     "fc_fwd_grouped": "grouped FC forward of the SMLPs hidden layer over 4 replicas, 4 x 512 x 5000 x 5000 (TF32), "
                       "with bias and the transposed output copy, as in the step",
     "fc_bwd_grouped": "grouped FC backward (dX + dW + db) of the SMLPs hidden layer over 4 replicas, with w^T, "
                       "x^T + ones row, dy^T given and dx^T written, as in the step",
     "conv_dw_224x64": "conv weight gradient, VGG conv1_2 shape 224x224x64->64, batch 16",
+    "conv_dw_224x64_xT": "conv weight gradient with the x^T copy made ahead (sprint_conv_dW_xT), VGG conv1_2 "
+                         "shape 224x224x64->64, batch 16 (use --batch 64)",
     "conv_fwd_224x64": "conv forward, VGG conv1_2 shape 224x224x64->64, batch 16",
     "conv_dx_224x64": "conv input gradient (ReLU mask), VGG conv1_2 shape 224x224x64->64, batch 16",
     "conv_fwd_224x3": "conv forward, VGG conv1_1 shape 224x224x3->64, batch 16",
@@ -895,9 +899,10 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_fc_bwd(x, w[i % 2], wT[i % 2], dy, x, dx, dw, db, 1.0, 0, M, K, N, ws, nb)
             work, unit = 4.0 * M * N * K, "TFLOP/s"
-    elif k in ("conv_dw_224x64", "conv_fwd_224x64", "conv_dx_224x64", "conv_fwd_224x3", "conv_dw_224x3"):
+    elif k in ("conv_dw_224x64", "conv_dw_224x64_xT", "conv_fwd_224x64", "conv_dx_224x64", "conv_fwd_224x3",
+               "conv_dw_224x3"):
         Nb, H, W = args.batch or 16, 224, 224
-        Ci = 64 if k.endswith("224x64") else 3
+        Ci = 64 if "224x64" in k else 3
         Co = 64
         x = rnd(Nb, H, W, Ci).relu_()
         w = rnd(Co, 3, 3, Ci, std=(2.0 / (9 * Ci)) ** 0.5)
@@ -911,6 +916,10 @@ def run_kernel(args):
         work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
         if k in ("conv_dw_224x64", "conv_dw_224x3"):
             fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
+        elif k == "conv_dw_224x64_xT":
+            xT = torch.empty(max(S.sprint_conv_xT_size(Nb, H, W, Ci, Co, 1) // 4, 1), device="cuda")
+            S.sprint_conv_xT(x, xT, Nb, H, W, Ci, Co, 1)
+            fn = lambda i: S.sprint_conv_dW_xT(x, xT, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
         elif k == "conv_dx_224x64":
             dx = torch.empty(Nb, H, W, Ci, device="cuda")
             fn = lambda i: S.sprint_conv_dX(dy, w, None, x, dx, Nb, H, W, Ci, Co, 1, ws, nbytes)
@@ -933,6 +942,10 @@ def run_kernel(args):
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, C, C, 1, 1, ws, nbytes)
         elif k == "conv_dx":
             fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, y, Nb, H, W, C, C, 1, ws, nbytes)
+        elif k == "conv_dw_xT":
+            xT = torch.empty(max(S.sprint_conv_xT_size(Nb, H, W, C, C, 1) // 4, 1), device="cuda")
+            S.sprint_conv_xT(x, xT, Nb, H, W, C, C, 1)
+            fn = lambda i: S.sprint_conv_dW_xT(x, xT, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
         else:
             fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
     elif k in ("pool_fwd", "pool_bwd"):
