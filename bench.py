@@ -926,28 +926,30 @@ def run_kernel(args):
         else:
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
     elif k.startswith("conv"):
-        Nb, H, W, C = args.batch or 16, 56, 56, 256
-        x = rnd(Nb, H, W, C).relu_()
-        w = rnd(C, 3, 3, C, std=(2.0 / (9 * C)) ** 0.5)
-        wT = w.reshape(C, 9 * C).t().contiguous()
-        b = torch.zeros(C, device="cuda")
-        y = torch.empty(Nb, H, W, C, device="cuda")
-        dy = rnd(Nb, H, W, C)
-        nbytes = max(S.sprint_conv_workspace_size(op, Nb, H, W, C, C, 1) for op in range(3))
+        Nb = args.batch or 16
+        H, W, Ci, Co = (int(v) for v in args.conv_shape.split(",")) if args.conv_shape else (56, 56, 256, 256)
+        x = rnd(Nb, H, W, Ci).relu_()
+        w = rnd(Co, 3, 3, Ci, std=(2.0 / (9 * Ci)) ** 0.5)
+        wT = w.reshape(Co, 9 * Ci).t().contiguous()
+        b = torch.zeros(Co, device="cuda")
+        y = torch.empty(Nb, H, W, Co, device="cuda")
+        dx = torch.empty(Nb, H, W, Ci, device="cuda")
+        dy = rnd(Nb, H, W, Co)
+        nbytes = max(S.sprint_conv_workspace_size(op, Nb, H, W, Ci, Co, 1) for op in range(3))
         ws = torch.empty(nbytes // 4 + 64, device="cuda")
-        dwt = torch.empty(C, 3, 3, C, device="cuda")
-        dbt = torch.empty(C, device="cuda")
-        work, unit = 2.0 * Nb * H * W * C * 9 * C, "TFLOP/s"
+        dwt = torch.empty(Co, 3, 3, Ci, device="cuda")
+        dbt = torch.empty(Co, device="cuda")
+        work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
         if k == "conv_fwd":
-            fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, C, C, 1, 1, ws, nbytes)
+            fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
         elif k == "conv_dx":
-            fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, y, Nb, H, W, C, C, 1, ws, nbytes)
+            fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, dx, Nb, H, W, Ci, Co, 1, ws, nbytes)
         elif k == "conv_dw_xT":
-            xT = torch.empty(max(S.sprint_conv_xT_size(Nb, H, W, C, C, 1) // 4, 1), device="cuda")
-            S.sprint_conv_xT(x, xT, Nb, H, W, C, C, 1)
-            fn = lambda i: S.sprint_conv_dW_xT(x, xT, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
+            xT = torch.empty(max(S.sprint_conv_xT_size(Nb, H, W, Ci, Co, 1) // 4, 1), device="cuda")
+            S.sprint_conv_xT(x, xT, Nb, H, W, Ci, Co, 1)
+            fn = lambda i: S.sprint_conv_dW_xT(x, xT, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
         else:
-            fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, C, C, 1, ws, nbytes)
+            fn = lambda i: S.sprint_conv_dW(x, dy, dwt, dbt, 1.0, 0, Nb, H, W, Ci, Co, 1, ws, nbytes)
     elif k in ("pool_fwd", "pool_bwd"):
         Nb, H, W, C = 64, 224, 224, 64
         x = rnd(Nb, H, W, C).relu_()
@@ -1023,7 +1025,8 @@ def run_kernel(args):
     else:
         peak = peaks["hbm_gbs"]
         psrc = f"{src}: hbm copy"
-    print(json.dumps({"kernel": k, "workload": KERNELS[k] + (f" (batch {args.batch})" if args.batch else ""),
+    shape = f" (shape {args.conv_shape})" if args.conv_shape and k.startswith("conv") else ""
+    print(json.dumps({"kernel": k, "workload": KERNELS[k] + (f" (batch {args.batch})" if args.batch else "") + shape,
                       "ms": round(ms, 4), "achieved": round(achieved, 1),
                       "unit": unit, "peak": round(peak, 1), "frac": round(achieved / peak, 4), "peak_source": psrc,
                       "flags": S.sprint_device_status()}))
@@ -1189,6 +1192,8 @@ def main(argv=None):
                     help="time one hot kernel at a workload shape instead of the training step")
     ap.add_argument("--batch", type=int, default=None,
                     help="--kernel conv_*: batch size in place of the case's 16")
+    ap.add_argument("--conv-shape", default=None, metavar="H,W,CIN,COUT",
+                    help="--kernel conv_fwd / conv_dx / conv_dw / conv_dw_xT: layer shape in place of 56,56,256,256")
     ap.add_argument("--cost-model", action="store_true",
                     help="refit the SPRINT report's SGEMM cost model to this GPU and check its T_GPU prediction")
     ap.add_argument("--oracle-rate", nargs=2, metavar=("CONFIG", "SECONDS"), default=None,

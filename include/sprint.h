@@ -96,12 +96,18 @@ int sprint_device_status(int* flags_out, int reset);
  *   [13] 1 = forward / input gradient factored over the kernel columns on CTA
  *       pairs (64 output channels, input channels % 32 == 0, pad 1, rows of
  *       >= 96 pixels; uses the workspace for permuted weights)
+ *   [14] 1 = forward / input gradient on halo-staged tiles (CTA pairs, pad
+ *       1, input channels % 32 == 0; 64 outputs (forward or input gradient)
+ *       with BN = 192, factored over the kernel columns, or 128 outputs of
+ *       the forward pass with BN = 128): a tile is [9] rows of [8] output
+ *       pixels, read once per 32-channel chunk with its one-pixel border;
+ *       used where such tiles fill >= 80% of the 128 MMA rows
  * Returns SPRINT_ERR_SHAPE / SPRINT_ERR_INVALID_ARG like the calls they
  * describe. sprint_conv_plan: op, shape and have_wT as for the conv calls.
  * sprint_gemm_plan: the grouped tensor-core GEMM D[M][N] = A[M][K] B[N][K]^T
  * over `batch` problems (the batched FC calls), allow_tail as when the
  * workspace holds the tail slabs. */
-#define SPRINT_PLAN_FIELDS 14
+#define SPRINT_PLAN_FIELDS 15
 #define SPRINT_PATH_SIMT 0
 #define SPRINT_PATH_TC 1
 #define SPRINT_PATH_SMALLC 2

@@ -190,6 +190,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// The same with relaxed semantics: orders none of the thread's earlier memory operations, so it
+// does not wait for its global stores to become visible (a release at cluster scope does). For
+// handing a TMEM accumulator back after tcgen05.wait::ld, which has already completed the reads.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // TMA loads into this CTA's shared memory whose completion is signalled on an
 // mbarrier of either CTA of the pair (shared::cluster address `bar`).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, int c0, int c1, uint32_t bar) {

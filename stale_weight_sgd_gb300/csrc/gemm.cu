@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "tc_gemm.cuh"
+#include "tc_halo.cuh"
 
 namespace sprint {
 
@@ -1398,6 +1399,7 @@ struct ConvPlan {
     int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
     bool wg_blocked = false;       // dedw copies blocked [H][W*N/32][C][32] (N % 32 == 0)
     bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64)
+    bool halo = false;             // fwd / dedx on halo-staged tiles of whole output rows (64 or 128 output channels)
     bool fact = false;             // fwd / dedx factored over the kernel columns (64 output channels, wide rows)
     size_t ws_wfact = 0;           // its permuted weights
     GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
@@ -1434,6 +1436,33 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         // columns, a 192-wide GEMM instead of a 64-wide one
         const int nout = op == SPRINT_CONV_FWD ? Cout : Cin, kch = op == SPRINT_CONV_FWD ? Cin : Cout;
         const int fw = op == SPRINT_CONV_FWD ? Wo : W;
+        // (the input gradient with 128 outputs stays tap by tap: measured faster there, its ReLU-mask
+        // reads weigh more in the halo epilogue)
+        if (pad == 1 && (nout == 64 || (nout == 128 && op == SPRINT_CONV_FWD)) && kch % 32 == 0) {
+            // halo-staged tiles: bh output rows of bw pixels (bw + 2 <= 115, so a 128-row MMA
+            // covers them and the buffer fits its stage), used when they fill >= 80% of the rows
+            const int fh = op == SPRINT_CONV_FWD ? Ho : H;
+            const int per_row = (fw + 112) / 113;
+            const int bw = (fw + per_row - 1) / per_row;
+            int bh = per_row == 1 ? TC_BM / (bw + 2) : 1;
+            if (bh > fh) bh = fh;
+            const int th = (fh + bh - 1) / bh;
+            const double fill = static_cast<double>(fw) * fh / (static_cast<double>(per_row) * th * TC_BM);
+            if (bh >= 1 && halo_rows_needed(bw, bh) <= HALO_A_ROWS && fill >= 0.8) {
+                // 64 outputs: factored over the kernel columns (a 192-wide MMA on permuted weights)
+                pl.halo = true;
+                pl.tile.bn = nout == 64 ? 192 : 128;
+                pl.tile.pair = true;
+                pl.box = PixBox{bw, bh, 1, per_row, th, N};
+                pl.num_kt = 9 * (kch / 32);
+                pl.kt_per_split = pl.num_kt;
+                if (nout == 64)
+                    pl.ws_wfact = fbytes(9ll * nout * kch);
+                else if (op == SPRINT_CONV_DX && !have_wT)
+                    pl.ws_wT = fbytes(9ll * Cin * Cout);
+                return pl;
+            }
+        }
         if (pad == 1 && nout == 64 && kch % 32 == 0 && fw >= 96) {
             pl.fact = true;
             pl.tile.bn = 192;
@@ -2125,6 +2154,93 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
     return launch_tail_reduce<ROLE_CONV_IMPL>(pl.gp, p, m_units, n_tiles, 1, s);
 }
 
+// Persistent CTA pairs of the halo-staged convolution (at most as many as can be resident).
+template <int BN>
+int launch_halo_bn(const TcMaps<1>& maps, const TcParams& p, cudaStream_t s) {
+    static bool attr_done[64] = {};
+    static int slots[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(HALO_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = halo_smem_bytes(BN);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(tc_halo_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, halo_smem_bytes(BN)) !=
+            cudaSuccess)
+            return check_cuda("cudaFuncSetAttribute(tc_halo_kernel)");
+        cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_halo_kernel<BN>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        slots[dev] = n;
+        attr_done[dev] = true;
+    }
+    const int pairs = p.num_tiles < slots[dev] ? p.num_tiles : slots[dev];
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.stream = s;
+    cudaLaunchKernelEx(&cfg, tc_halo_kernel<BN>, maps, p);
+    return check_launch("tc_halo_kernel");
+}
+
+// The halo-staged implicit GEMM (CTA pairs, BN = ncols = 64 or 128): A = act (NHWC, act_c
+// channels) in boxes of (bh + 2) x (bw + 2) pixels around each tile, B through *tb (the map of
+// the tap-by-tap implicit GEMM, boxes of BN / 2 rows).
+static int conv_halo_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, const CUtensorMap* tb,
+                        TcParams p, int ncols, cudaStream_t s, bool* done) {
+    *done = false;
+    CUtensorMap ta;
+    const uint64_t da[4] = {(uint64_t)act_c, (uint64_t)act_w, (uint64_t)act_h, (uint64_t)p.img_n};
+    const uint64_t sa[3] = {(uint64_t)act_c * 4, (uint64_t)act_w * act_c * 4, (uint64_t)act_h * act_w * act_c * 4};
+    const uint32_t ba[4] = {32, (uint32_t)pl.box.bw + 2, (uint32_t)pl.box.bh + 2, 1};
+    if (!make_tmap(&ta, act, 4, da, sa, ba)) return SPRINT_OK;
+    p.N = ncols;
+    p.bw = pl.box.bw;
+    p.bh = pl.box.bh;
+    p.bimg = 1;
+    p.tiles_w = pl.box.tw;
+    p.tiles_h = pl.box.th;
+    p.chunks = act_c / 32;
+    p.num_kt = pl.num_kt;
+    p.kt_per_split = pl.num_kt;
+    p.store = ST_DIRECT;
+    const long long units = (pl.box.tiles() + 1) / 2, n_tiles = (ncols + pl.tile.bn - 1) / pl.tile.bn;
+    SPRINT_REQUIRE(units * n_tiles < (1ll << 31), SPRINT_ERR_SHAPE, "conv: %lld halo tiles is too many",
+                   units * n_tiles);
+    p.m_tiles = static_cast<int>(units);
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.z_tiles = 1;
+    p.num_tiles = static_cast<int>(units * n_tiles);
+    TcMaps<1> maps;
+    maps.a[0] = ta;
+    maps.b[0] = *tb;
+    maps.d[0] = ta;
+    *done = true;
+    return pl.tile.bn == 192 ? launch_halo_bn<192>(maps, p, s) : launch_halo_bn<128>(maps, p, s);
+}
+
+// The halo-staged GEMM factored over the kernel columns (64 outputs): B' = the permuted weights
+// [3 * nout][3 * act_c] (fact_weights_kernel), boxes of 96 rows.
+static int conv_halo_fact_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, int nout,
+                             const float* wfact, TcParams p, cudaStream_t s, bool* done) {
+    *done = false;
+    CUtensorMap tb;
+    const uint64_t db[2] = {(uint64_t)3 * act_c, (uint64_t)3 * nout};
+    const uint64_t sb[1] = {(uint64_t)3 * act_c * 4};
+    const uint32_t bb[2] = {32, pl.tile.b_rows()};
+    if (!make_tmap(&tb, wfact, 2, db, sb, bb)) return SPRINT_OK;
+    return conv_halo_tc(pl, act, act_c, act_w, act_h, &tb, p, nout, s, done);
+}
+
 // The factored implicit GEMM (CONV_FACT, CTA pairs, BN = 192): A = act (NHWC, act_c channels) in
 // boxes of 128 pixels of one row, B = the permuted weights [3 * nout][3 * act_c].
 static int conv_fact_tc(const ConvPlan& pl, const float* act, int act_c, int act_w, int act_h, int nout,
@@ -2184,7 +2300,7 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     if (pl.smallc) return launch_conv_smallc(x, w, b, y, N, H, W, Cin, Cout, pad, relu, s);
-    if (pl.fact) {
+    if (pl.fact || (pl.halo && pl.tile.bn == 192)) {
         float* wf = static_cast<float*>(ws);
         fact_weights_kernel<<<grid_cap(9ll * Cin * Cout), 256, 0, s>>>(w, wf, Cin, Cout, 0);
         if ((rc = check_launch("fact_weights_kernel"))) return rc;
@@ -2200,7 +2316,8 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
         p.bias = b;
         p.relu = relu;
         bool done = false;
-        rc = conv_fact_tc(pl, x, Cin, W, H, Cout, wf, p, s, &done);
+        rc = pl.halo ? conv_halo_fact_tc(pl, x, Cin, W, H, Cout, wf, p, s, &done)
+                     : conv_fact_tc(pl, x, Cin, W, H, Cout, wf, p, s, &done);
         if (rc || done) return rc;
         return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
     }
@@ -2243,7 +2360,8 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
             bool done = false;
             float* tail_ws =
                 tail_room ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_total() - pl.ws_tail) : nullptr;
-            rc = conv_impl_tc(pl, x, Cin, W, H, &tb, p, Cout, s, &done, tail_ws);
+            rc = pl.halo ? conv_halo_tc(pl, x, Cin, W, H, &tb, p, Cout, s, &done)
+                         : conv_impl_tc(pl, x, Cin, W, H, &tb, p, Cout, s, &done, tail_ws);
             if (rc || done) return rc;
         }
     }
@@ -2271,7 +2389,7 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
     const bool tail_room = pl.ws_tail && ws && ws_bytes >= pl.ws_total();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
-    if (pl.fact) {
+    if (pl.fact || (pl.halo && pl.tile.bn == 192)) {
         float* wf = static_cast<float*>(ws);
         fact_weights_kernel<<<grid_cap(9ll * Cin * Cout), 256, 0, s>>>(w, wf, Cin, Cout, 1);
         if ((rc = check_launch("fact_weights_kernel"))) return rc;
@@ -2287,7 +2405,8 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
         p.mask = relu_src;
         p.ldm = Cin;
         bool done = false;
-        rc = conv_fact_tc(pl, dy, Cout, Wo, Ho, Cin, wf, p, s, &done);
+        rc = pl.halo ? conv_halo_fact_tc(pl, dy, Cout, Wo, Ho, Cin, wf, p, s, &done)
+                     : conv_fact_tc(pl, dy, Cout, Wo, Ho, Cin, wf, p, s, &done);
         if (rc || done) return rc;
         return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
     }
@@ -2318,7 +2437,8 @@ extern "C" int sprint_conv_dX(const float* dy, const float* w, const float* wT, 
             bool done = false;
             float* tail_ws =
                 tail_room ? reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_total() - pl.ws_tail) : nullptr;
-            rc = conv_impl_tc(pl, dy, Cout, Wo, Ho, &tb, p, Cin, s, &done, tail_ws);
+            rc = pl.halo ? conv_halo_tc(pl, dy, Cout, Wo, Ho, &tb, p, Cin, s, &done)
+                         : conv_impl_tc(pl, dy, Cout, Wo, Ho, &tb, p, Cin, s, &done, tail_ws);
             if (rc || done) return rc;
         }
     }
@@ -2584,6 +2704,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[11] = pl.wg_blocked ? 1 : 0;
     out[12] = pl.wg_fact ? 1 : 0;
     out[13] = pl.fact ? 1 : 0;
+    out[14] = pl.halo ? 1 : 0;
     return SPRINT_OK;
 }
 

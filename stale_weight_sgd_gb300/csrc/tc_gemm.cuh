@@ -19,7 +19,9 @@
 //              GradBuf accumulate); ragged edges are clipped by TMA. Outputs TMA
 //              cannot describe (row pitch not a multiple of 16 bytes) are
 //              written by the threads directly instead.
-// So the epilogue of tile i overlaps the MMAs of tile i+1.
+// So the epilogue of tile i overlaps the MMAs of tile i+1. The hand-back is a
+// relaxed arrive: a release would first wait for the warp's earlier direct
+// stores (transposed copies, vector columns) to become visible.
 //
 // CTA pairs (PAIR = true, clusters of two): a work unit is two vertically
 // adjacent tiles (m-tiles 2u and 2u+1) computed by one tcgen05.mma of M = 256
@@ -603,9 +605,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) {
                             if constexpr (PAIR)
-                                mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                                mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[b]), 0));
                             else
-                                mbar_arrive(&tmem_empty[b]);
+                                mbar_arrive_cluster_relaxed(smem_u32(&tmem_empty[b]));
                         }
                     }
                     if (nkt == 0) {   // an empty k-range contributes zeros (the accumulator was never written)
@@ -644,7 +646,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (jb == 1) {   // accumulator fully read: hand it back to the MMA warp
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[b]), 0));
                     }
                     const int c0 = jb * 32;
                     float o[32];
@@ -735,7 +737,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         if (c + 32 >= BN) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[b]), 0));
                         }
                         if (nkt == 0) {
 #pragma unroll
@@ -785,9 +787,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if constexpr (PAIR)
-                            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[b]), 0));
+                            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[b]), 0));
                         else
-                            mbar_arrive(&tmem_empty[b]);
+                            mbar_arrive_cluster_relaxed(smem_u32(&tmem_empty[b]));
                     }
                 }
                 const int ncol0 = n0 + c;

@@ -88,6 +88,29 @@ def test_shape_and_workspace_errors(S):
     assert L.sprint_transpose(16, 16, 4, 4, None) == 1               # aliasing
 
 
+def test_halo_tile_plans(S):
+    """Host-side tile choice of the halo-staged forward / input gradient: 64 or
+    128 output channels, tiles of whole output rows that fill >= 80% of the 128
+    MMA rows, the halo buffer within its stage."""
+    def plan(op, N, H, W, Cin, Cout):
+        return S.sprint_conv_plan(op, N, H, W, Cin, Cout, 1, True)
+    for N, H, W, Cin, Cout, bw, bh in [(64, 224, 224, 64, 64, 112, 1), (64, 112, 112, 64, 128, 112, 1),
+                                       (64, 112, 112, 128, 128, 112, 1), (2, 15, 28, 64, 128, 28, 4),
+                                       (1, 3, 221, 64, 64, 111, 1)]:
+        p = plan(0, N, H, W, Cin, Cout)
+        # 64 outputs factored over the kernel columns: a 192-wide MMA
+        assert p["conv_halo"] == 1 and p["pair"] == 1 and p["bn"] == (192 if Cout == 64 else Cout), p
+        assert (p["box_w"], p["box_h"], p["box_img"]) == (bw, bh, 1)
+        assert p["num_kt"] == 9 * Cin // 32
+        assert (bw + 2) * bh <= 128 and 2 * (bw + 2) + 130 <= 360   # the last tap's window inside the buffer
+    assert plan(1, 64, 112, 112, 64, 128)["conv_halo"] == 1           # dX of conv2_1: 64 output channels
+    assert plan(1, 64, 56, 56, 128, 256)["conv_halo"] == 0            # dX with 128 output channels: tap by tap
+    assert plan(0, 64, 56, 56, 128, 256)["conv_halo"] == 0            # 256 output channels: tap by tap
+    assert plan(0, 64, 14, 14, 64, 64)["conv_halo"] == 0              # 196 of 256 rows: tap by tap
+    assert plan(0, 2, 4, 100, 64, 64)["conv_fact"] == 1               # 100 of 128 rows: factored
+    assert plan(0, 2, 8, 8, 48, 64)["conv_halo"] == 0                 # input channels % 32 != 0
+
+
 def test_batched_entry_points_validate(S):
     L = S.lib()
     f1 = ctypes.c_float(1)

@@ -107,6 +107,7 @@ def test_plans_cover_every_kernel_path(S):
     assert any(p["splits"] > 1 for p in dw)
     assert any(p["wg_tpt"] > 0 for p in dw) and any(p["wg_tpt"] == 0 and not p["wg_fact"] for p in dw)
     assert any(p["wg_fact"] for p in dw)          # the Cout = 64 layers: factored on CTA pairs
-    assert any(p["conv_fact"] for p in fwd_dx) and any(not p["conv_fact"] for p in fwd_dx)
+    # the 64- and 128-channel outputs of the wide VGG-I layers: halo-staged tiles
+    assert any(p["conv_halo"] for p in fwd_dx) and any(not p["conv_halo"] for p in fwd_dx)
     assert all(p["wg_blocked"] for p in dw)       # batch 64 and 128: blocked operand copies
     assert any(p["path"] == "smallc" for (_, _, op), p in PLANS.items())

@@ -518,7 +518,19 @@ CONV_CASES = [
     (2, 4, 100, 64, 64),    # forward and input gradient factored; one 126-pixel tile per row
     (2, 5, 130, 32, 64),    # forward factored, two tiles per row (the second holds 4 pixels)
     (1, 3, 253, 64, 96),    # input gradient factored (k = 3 x 96), three tiles per row, odd tile count
+    # 64 or 128 output channels: halo-staged tiles of whole output rows
+    (2, 6, 112, 64, 128),   # forward BN 128, input gradient BN 64; one 112-pixel row per tile
+    (2, 6, 56, 128, 64),    # two rows of 56 pixels per tile, four input chunks (forward), BN 128 (dX)
+    (1, 4, 224, 64, 64),    # two tiles per row (the VGG conv1_2 width)
+    (1, 6, 56, 64, 64),     # odd tile count: the last pair's second CTA has no tile
+    (2, 15, 28, 64, 128),   # four rows per tile, the last tile row holds three
+    (1, 3, 221, 64, 64),    # two tiles per row, the second one pixel short
 ]
+
+# the cases above whose 64-channel outputs (forward or input gradient) and 128-channel forward
+# outputs take the halo-staged tiles
+HALO_CASES = {(2, 6, 112, 64, 128), (2, 6, 56, 128, 64), (1, 4, 224, 64, 64), (1, 6, 56, 64, 64),
+              (2, 15, 28, 64, 128), (1, 3, 221, 64, 64)}
 
 
 def _conv_inputs(seed, N, H, W, Cin, Cout):
@@ -531,6 +543,21 @@ def _conv_inputs(seed, N, H, W, Cin, Cout):
 def _ws(S, op, *shape):
     n = S.sprint_conv_workspace_size(op, *shape, 1)
     return (torch.empty(max(n // 4, 1) + 64, dtype=torch.float32, device="cuda"), n)
+
+
+def test_conv_plans_of_the_cases(S):
+    """The small cases reach both the halo-staged and the factored forward /
+    input-gradient tiles (whole-tensor parity below covers every tile edge)."""
+    for case in CONV_CASES:
+        N, H, W, Cin, Cout = case
+        for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX):
+            pl = S.sprint_conv_plan(op, N, H, W, Cin, Cout, 1, True)
+            nout = Cout if op == S.SPRINT_CONV_FWD else Cin
+            want = case in HALO_CASES and (nout == 64 or op == S.SPRINT_CONV_FWD)
+            assert bool(pl["conv_halo"]) == (want and pl["path"] == "tc"), (case, op, pl)
+            if pl["conv_halo"]:
+                assert pl["pair"] == 1 and pl["bn"] == (192 if nout == 64 else 128)
+    assert any(S.sprint_conv_plan(op, *c, 1, True)["conv_fact"] for c in CONV_CASES for op in (0, 1))
 
 
 @pytest.mark.parametrize("N,H,W,Cin,Cout", CONV_CASES)
