@@ -836,6 +836,8 @@ KERNELS = {
     "pool_fwd": "2x2 max-pool forward with argmax, VGG-I pool1 64x224x224x64 -> 112x112",
     "pool_bwd": "max-pool backward routed by argmax with the ReLU mask, VGG-I pool1 shape",
     "softmax_xent": "softmax cross-entropy (loss + dlogits) of 8 replicas x 64 x 1000 classes",
+    "conv_xT": "the weight gradient's blocked copy x -> [H][W*N/32][C][32] (sprint_conv_xT), VGG conv3_2 input "
+               "56x56x256, batch 16 (use --batch 64, --conv-shape)",
     "transpose": "2-D transpose [16*56*56][256] -> [256][16*56*56] (the bytes of one conv weight-gradient operand "
                  "re-layout at the VGG conv3_2 shape, batch 16)",
 }
@@ -940,7 +942,11 @@ def run_kernel(args):
         dwt = torch.empty(Co, 3, 3, Ci, device="cuda")
         dbt = torch.empty(Co, device="cuda")
         work, unit = 2.0 * Nb * H * W * Co * 9 * Ci, "TFLOP/s"
-        if k == "conv_fwd":
+        if k == "conv_xT":   # reads x, writes its blocked copy
+            xT = torch.empty(max(S.sprint_conv_xT_size(Nb, H, W, Ci, Co, 1) // 4, 1), device="cuda")
+            fn = lambda i: S.sprint_conv_xT(x, xT, Nb, H, W, Ci, Co, 1)
+            work, unit = 8.0 * Nb * H * W * Ci, "GB/s"
+        elif k == "conv_fwd":
             fn = lambda i: S.sprint_conv_fwd(x, w, b, y, Nb, H, W, Ci, Co, 1, 1, ws, nbytes)
         elif k == "conv_dx":
             fn = lambda i: S.sprint_conv_dX(dy, w, wT, x, dx, Nb, H, W, Ci, Co, 1, ws, nbytes)
