@@ -94,8 +94,8 @@ int pair_slots() {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-        cfg.blockDim = dim3(TC_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = tc_smem_bytes(BN, true);
+        cfg.blockDim = dim3(tc_threads<ROLE>(), 1, 1);
+        cfg.dynamicSmemBytes = tc_smem_bytes_r<ROLE>(BN, true);
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
@@ -115,7 +115,7 @@ int launch_tc_bn(const TcMaps<G>& maps, const TcParams& p, cudaStream_t s) {
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         if (cudaFuncSetAttribute(tc_gemm_kernel<ROLE, BN, PAIR, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc_smem_bytes(BN, PAIR)) != cudaSuccess)
+                                 tc_smem_bytes_r<ROLE>(BN, PAIR)) != cudaSuccess)
             return check_cuda("cudaFuncSetAttribute(tc_gemm_kernel)");
         attr_done[dev] = true;
     }
@@ -123,7 +123,7 @@ int launch_tc_bn(const TcMaps<G>& maps, const TcParams& p, cudaStream_t s) {
     if constexpr (!PAIR) {
         // persistent: one CTA per SM at most, each walking tiles blockIdx.x, +gridDim.x, ...
         const int grid = work < num_sms() ? work : num_sms();
-        tc_gemm_kernel<ROLE, BN, false, G><<<grid, TC_THREADS, tc_smem_bytes(BN, false), s>>>(maps, p);
+        tc_gemm_kernel<ROLE, BN, false, G><<<grid, tc_threads<ROLE>(), tc_smem_bytes_r<ROLE>(BN, false), s>>>(maps, p);
         return check_launch("tc_gemm_kernel");
     } else {
         // persistent pairs: at most as many clusters as can be resident together
@@ -136,8 +136,8 @@ int launch_tc_bn(const TcMaps<G>& maps, const TcParams& p, cudaStream_t s) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
-        cfg.blockDim = dim3(TC_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = tc_smem_bytes(BN, true);
+        cfg.blockDim = dim3(tc_threads<ROLE>(), 1, 1);
+        cfg.dynamicSmemBytes = tc_smem_bytes_r<ROLE>(BN, true);
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -1399,6 +1399,7 @@ struct ConvPlan {
     int wg_tpt = 0, wg_rows = 0;   // dedw with taps packed along N (0: one tap per tile)
     bool wg_blocked = false;       // dedw copies blocked [H][W*N/32][C][32] (N % 32 == 0)
     bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64)
+    bool rgb = false;              // fwd of the RGB layer (3 -> 64 channels): im2col rows built in shared memory
     bool halo = false;             // fwd / dedx on halo-staged tiles of whole output rows (64 or 128 output channels)
     bool fact = false;             // fwd / dedx factored over the kernel columns (64 output channels, wide rows)
     size_t ws_wfact = 0;           // its permuted weights
@@ -1416,6 +1417,17 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
     ConvPlan pl;
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     const long long P = static_cast<long long>(N) * Ho * Wo;
+    if (op == SPRINT_CONV_FWD && Cin == 3 && Cout == 64 && pad == 1) {
+        // the RGB layer: each 128-pixel tile's 27 products per output as one 32-deep k-tile on the
+        // tensor cores, its im2col rows written into shared memory by the producer warp (bound by
+        // writing y; the CUDA-core kernel below is bound by its shared-memory weight reads)
+        pl.tc = pl.rgb = true;
+        pl.tile.bn = 64;
+        pl.num_kt = 1;
+        pl.kt_per_split = 1;
+        pl.ws_wpad = fbytes(64ll * TC_BK);
+        return pl;
+    }
     if (op == SPRINT_CONV_FWD && Cin <= 4 && Cout % 16 == 0 && (9 * Cin + 1) * Cout * 4 <= 48 * 1024) {
         // the RGB layer: direct CUDA-core convolution at output-write speed (no workspace)
         pl.smallc = true;
@@ -2300,6 +2312,44 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Ho = H + 2 * pad - 2, Wo = W + 2 * pad - 2;
     if (pl.smallc) return launch_conv_smallc(x, w, b, y, N, H, W, Cin, Cout, pad, relu, s);
+    if (pl.rgb) {
+        float* wpad = static_cast<float*>(ws);
+        pad_cols_kernel<<<(Cout * TC_BK + 255) / 256, 256, 0, s>>>(w, Cout, 9 * Cin, TC_BK, wpad);
+        if ((rc = check_launch("pad_cols_kernel"))) return rc;
+        const long long P = static_cast<long long>(N) * H * W;
+        SPRINT_REQUIRE(P < (1ll << 31) - TC_BM, SPRINT_ERR_SHAPE, "%s: too many output pixels", __func__);
+        CUtensorMap tb, td;
+        const uint64_t db[2] = {(uint64_t)TC_BK, (uint64_t)Cout}, sb[1] = {(uint64_t)TC_BK * 4};
+        const uint32_t bb[2] = {32, 64};
+        const uint64_t dd[2] = {(uint64_t)Cout, (uint64_t)P}, sd[1] = {(uint64_t)Cout * 4};
+        const uint32_t bd[2] = {32, 32};
+        if (!make_tmap(&tb, wpad, 2, db, sb, bb) || !make_tmap(&td, y, 2, dd, sd, bd, false))
+            return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
+        TcParams p = base_params();
+        p.M = static_cast<int>(P);
+        p.N = Cout;
+        p.num_kt = 1;
+        p.kt_per_split = 1;
+        p.epi = EPI_STORE;
+        p.store = ST_2D;
+        p.D = y;
+        p.ldd = Cout;
+        p.bias = b;
+        p.relu = relu;
+        p.img_n = N;
+        p.out_h = H;
+        p.out_w = W;
+        p.act = x;
+        TcMaps<1> maps;
+        maps.a[0] = tb;   // (no A map: the producer writes A)
+        maps.b[0] = tb;
+        maps.d[0] = td;
+        p.m_tiles = static_cast<int>((P + TC_BM - 1) / TC_BM);
+        p.n_tiles = 1;
+        p.z_tiles = 1;
+        p.num_tiles = p.m_tiles;
+        return launch_tc_bn<ROLE_CONV_RGB, 64, false, 1>(maps, p, s);
+    }
     if (pl.fact || (pl.halo && pl.tile.bn == 192)) {
         float* wf = static_cast<float*>(ws);
         fact_weights_kernel<<<grid_cap(9ll * Cin * Cout), 256, 0, s>>>(w, wf, Cin, Cout, 0);
@@ -2705,6 +2755,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[12] = pl.wg_fact ? 1 : 0;
     out[13] = pl.fact ? 1 : 0;
     out[14] = pl.halo ? 1 : 0;
+    out[15] = pl.rgb ? 1 : 0;
     return SPRINT_OK;
 }
 

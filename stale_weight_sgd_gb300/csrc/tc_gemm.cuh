@@ -53,6 +53,13 @@
 //               the weights permuted by the host; the epilogue adds the three
 //               column blocks of neighbouring rows within the warp's window:
 //               out[q] = D'[q - s][dw 0] + D'[q][dw 1] + D'[q + s][dw 2].
+//   CONV_RGB  : forward of a layer with 3 input channels (the RGB layer, pad 1):
+//               one k-tile per 128-pixel tile, A = the tile's im2col rows
+//               ((dh * 3 + dw) * 3 + c, zero past 27) written into shared memory
+//               from x (act, NHWC) by four more warps (6-9, one row per lane),
+//               B = the weights padded to 32 columns (TMA, warp 4); the stage's
+//               barrier takes the TMA bytes and one arrival per im2col warp; the
+//               epilogue as for GEMM_2D over D = y [pixels][N].
 //   CONV_WGRAD: dedw conv, per tap: A = dy^T, B = x^T shifted by the tap; a
 //               k-tile is 32 consecutive (w, n) positions of one row, n fastest,
 //               so the tap's w-shift is N positions. The copies are either
@@ -68,7 +75,7 @@
 
 namespace sprint {
 
-enum Role : int { ROLE_GEMM_2D = 0, ROLE_CONV_IMPL = 1, ROLE_CONV_WGRAD = 2, ROLE_CONV_FACT = 3 };
+enum Role : int { ROLE_GEMM_2D = 0, ROLE_CONV_IMPL = 1, ROLE_CONV_WGRAD = 2, ROLE_CONV_FACT = 3, ROLE_CONV_RGB = 4 };
 enum Epi : int { EPI_STORE = 0, EPI_MASK = 1, EPI_ACCUM = 2 };
 // how the epilogue writes: direct stores, or TMA through a store map of shape
 enum Store : int { ST_DIRECT = 0, ST_2D = 1, ST_PIX4D = 2, ST_WGRAD3D = 3, ST_PARTIAL3D = 4 };
@@ -108,6 +115,25 @@ __host__ __device__ constexpr int tc_smem_bytes(int bn, bool pair) {
     return 1024 /* alignment slack */ +
            tc_stages(bn, pair) * tc_ks(bn, pair) * (TC_A_STAGE + tc_b_stage(bn, pair)) + TC_STAGING +
            256 /* barriers */;
+}
+
+// CONV_RGB (one k-tile per tile) takes stages of one k-tile and four staging buffers per epilogue
+// warp, so that a warp does not wait for its last TMA store to read its buffer; every other role
+// the shapes above.
+template <int ROLE>
+__host__ __device__ constexpr int tc_nstg() { return ROLE == ROLE_CONV_RGB ? 4 : 1; }
+template <int ROLE>
+__host__ __device__ constexpr int tc_ks_r(int bn, bool pair) { return ROLE == ROLE_CONV_RGB ? 1 : tc_ks(bn, pair); }
+template <int ROLE>
+__host__ __device__ constexpr int tc_stages_r(int bn, bool pair) {
+    return ROLE == ROLE_CONV_RGB ? 4 : tc_stages(bn, pair);
+}
+template <int ROLE>
+__host__ __device__ constexpr int tc_smem_bytes_r(int bn, bool pair) {
+    return ROLE == ROLE_CONV_RGB ? 1024 + tc_stages_r<ROLE>(bn, pair) * tc_ks_r<ROLE>(bn, pair) *
+                                              (TC_A_STAGE + tc_b_stage(bn, pair)) +
+                                       tc_nstg<ROLE>() * TC_STAGING + 256
+                                 : tc_smem_bytes(bn, pair);
 }
 
 // Up to TC_MAX_GROUP independent GEMMs of one shape in one launch (the work
@@ -192,6 +218,8 @@ struct TcParams {
     // units of one n-tile together, so each B tile comes from HBM once);
     // 0: m, then n, then z
     int z_mid;
+    // CONV_RGB: the layer input x [img_n][out_h][out_w][3]
+    const float* act;
 };
 
 #if defined(__CUDACC__)
@@ -235,12 +263,17 @@ __host__ __device__ __forceinline__ void fact_tile(const TcParams& p, int mt, in
     w0 = (rem % p.tiles_w) * TC_FACT_OUT;
 }
 
+// CONV_RGB adds warps 6-9, which write the im2col rows
+template <int ROLE>
+__host__ __device__ constexpr int tc_threads() { return ROLE == ROLE_CONV_RGB ? TC_THREADS + 128 : TC_THREADS; }
+
 template <int ROLE, int BN, bool PAIR, int G>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(tc_threads<ROLE>(), 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps<G> maps, const TcParams p) {
     static_assert(G == 1 || ROLE == ROLE_GEMM_2D, "only plain GEMMs are grouped");
-    constexpr int STAGES = tc_stages(BN, PAIR);
-    constexpr int KS = tc_ks(BN, PAIR);          // k-tiles per stage
+    constexpr int STAGES = tc_stages_r<ROLE>(BN, PAIR);
+    constexpr int KS = tc_ks_r<ROLE>(BN, PAIR);  // k-tiles per stage
+    constexpr int NSTG = tc_nstg<ROLE>();        // staging buffers per epilogue warp
     constexpr int B_ROWS = tc_b_rows(BN, PAIR);
     constexpr int B_STAGE = tc_b_stage(BN, PAIR);  // one k-tile of B
     constexpr uint32_t IDESC = idesc_tf32(BN, false, false, PAIR ? 256 : 128);
@@ -249,7 +282,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr uint32_t KTILE_BYTES = (TC_A_STAGE + B_STAGE) * (PAIR ? 2 : 1);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
     static_assert(!PAIR || BN >= 64, "a pair splits BN into two halves of at least 32 rows");
-    static_assert(tc_smem_bytes(BN, PAIR) <= 232448, "shared memory budget exceeded");
+    static_assert(tc_smem_bytes_r<ROLE>(BN, PAIR) <= 232448, "shared memory budget exceeded");
     constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;   // second accumulator at a power-of-two column offset
 
     extern __shared__ uint8_t smem_raw[];
@@ -257,8 +290,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * KS * TC_A_STAGE;
-    uint8_t* sStage = sB + STAGES * KS * B_STAGE;   // 4 x 4 KB epilogue staging, 1024-aligned
-    uint64_t* full = reinterpret_cast<uint64_t*>(sStage + TC_STAGING);
+    uint8_t* sStage = sB + STAGES * KS * B_STAGE;   // 4 x NSTG x 4 KB epilogue staging, 1024-aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(sStage + NSTG * TC_STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* tmem_full = empty + STAGES;     // [2]
     uint64_t* tmem_empty = tmem_full + 2;     // [2]
@@ -274,7 +307,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 4 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], ROLE == ROLE_CONV_RGB ? 5 : 1);   // CONV_RGB: + one arrival per im2col warp
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -342,7 +375,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 4) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if constexpr (ROLE == ROLE_CONV_RGB) {
+            // the weights of each tile's stage (warps 6-9 write its im2col rows)
+            if (lane == 0) {
+                uint32_t it = 0;
+                for (int t = unit0; t < p.num_tiles; t += units, ++it) {
+                    const uint32_t s = it % STAGES;
+                    if (!mbar_wait_bounded(&empty[s], ((it / STAGES) & 1) ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) break;
+                    mbar_arrive_expect_tx(&full[s], B_STAGE);
+                    tma_load_2d(sB + s * KS * B_STAGE, &maps.b[0], 0, 0, &full[s]);
+                }
+                // every weight copy issued above has landed before the CTA may exit
+                for (uint32_t k = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u; k < it; ++k)
+                    if (!mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1, p.status, DEV_FLAG_WAIT_PRODUCER))
+                        break;
+            }
+        } else if (lane == 0) {
             uint32_t it = 0;
             bool alive = true;
             for (int t = unit0; t < p.num_tiles && alive; t += units) {
@@ -573,10 +621,55 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_wait_bounded(mma_done, 0, p.status, DEV_FLAG_WAIT_MMA);
         }
         __syncwarp();
+    } else if (ROLE == ROLE_CONV_RGB && warp >= 6) {
+        // ---------------------------------------------------------------- CONV_RGB im2col rows (warps 6-9)
+        // lane l of warp 6 + i writes tile row 32 i + l: ((dh * 3 + dw) * 3 + c) -> x at (h + dh - 1,
+        // w + dw - 1), zero outside the image and past k = 27, 128B-swizzled as TMA would; the
+        // generic-proxy stores are fenced before the warp's arrival on the stage
+        uint32_t it = 0;
+        const long long npix = p.M;
+        const int hw = p.out_h * p.out_w;
+        const int r = (warp - 6) * 32 + lane;
+        for (int t = unit0; t < p.num_tiles; t += units, ++it) {
+            const uint32_t s = it % STAGES;
+            if (!mbar_wait_bounded(&empty[s], ((it / STAGES) & 1) ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) break;
+            const int pix = (t % p.m_tiles) * TC_BM + r;   // < 2^31 (checked by the host)
+            float v[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0.f;
+            if (pix < npix) {
+                const int n = pix / hw;
+                const int rem = pix - n * hw;
+                const int h = rem / p.out_w, w = rem - h * p.out_w;
+                const float* xi = p.act + static_cast<long long>(n) * hw * 3;
+#pragma unroll
+                for (int dh = 0; dh < 3; ++dh) {
+                    const int hh = h + dh - 1;
+                    if (hh < 0 || hh >= p.out_h) continue;
+                    const float* xr = xi + static_cast<long long>(hh) * p.out_w * 3;
+#pragma unroll
+                    for (int dw = 0; dw < 3; ++dw) {
+                        const int ww = w + dw - 1;
+                        if (ww < 0 || ww >= p.out_w) continue;
+#pragma unroll
+                        for (int c = 0; c < 3; ++c) v[(dh * 3 + dw) * 3 + c] = xr[ww * 3 + c];
+                    }
+                }
+            }
+            uint8_t* a_dst = sA + s * KS * TC_A_STAGE;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4*>(a_dst + r * 128 + ((k ^ (r & 7)) << 4)) =
+                    make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
+        }
     } else {
         // ---------------------------------------------------------------- epilogue (warps 0-3)
-        uint8_t* stage = sStage + warp * 4096;
+        uint8_t* stage = sStage + warp * NSTG * 4096;
         bool pending = false;     // a TMA store of this warp may still read `stage`
+        uint32_t nst = 0;         // chunks this warp has staged (buffer nst % NSTG)
         uint32_t j = 0;
         for (int t = unit0; t < p.num_tiles; t += units, ++j) {
             const TileCoord tc = own_coord(t);
@@ -854,14 +947,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
                 if (p.store != ST_DIRECT) {
-                    // stage the 32 x 32 chunk (128B-swizzled rows) and hand it to TMA
-                    if (pending) {
-                        if (lane == 0) bulk_wait_read0();
+                    // stage the 32 x 32 chunk (128B-swizzled rows) and hand it to TMA; the buffer's
+                    // previous store (NSTG chunks ago) must have read it
+                    uint8_t* sbuf = stage + (nst % NSTG) * 4096;
+                    if (nst >= static_cast<uint32_t>(NSTG)) {
+                        if (lane == 0) bulk_wait_read<NSTG - 1>();
                         __syncwarp();
                     }
+                    ++nst;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        float4* dst = reinterpret_cast<float4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4));
+                        float4* dst = reinterpret_cast<float4*>(sbuf + lane * 128 + ((q ^ (lane & 7)) << 4));
                         *dst = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     }
                     fence_async_smem();
@@ -879,24 +975,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const bool add = (p.epi == EPI_ACCUM) && p.accumulate && !to_partial;
                         if (p.store == ST_2D) {
                             if (add)
-                                tma_reduce_add_2d(mD, ncol0, m0 + warp * 32, stage);
+                                tma_reduce_add_2d(mD, ncol0, m0 + warp * 32, sbuf);
                             else
-                                tma_store_2d(mD, ncol0, m0 + warp * 32, stage);
+                                tma_store_2d(mD, ncol0, m0 + warp * 32, sbuf);
                         } else if (p.store == ST_PIX4D) {
                             const int row0 = warp * 32;
                             const int wo = row0 % p.bw, ho = (row0 / p.bw) % p.bh, no = row0 / (p.bw * p.bh);
-                            tma_store_4d(mD, ncol0, pw0 + wo, ph0 + ho, pn0 + no, stage);
+                            tma_store_4d(mD, ncol0, pw0 + wo, ph0 + ho, pn0 + no, sbuf);
                         } else if (p.store == ST_WGRAD3D) {
                             if (add)
-                                tma_reduce_add_3d(mD, ncol0, tap, m0 + warp * 32, stage);
+                                tma_reduce_add_3d(mD, ncol0, tap, m0 + warp * 32, sbuf);
                             else
-                                tma_store_3d(mD, ncol0, tap, m0 + warp * 32, stage);
+                                tma_store_3d(mD, ncol0, tap, m0 + warp * 32, sbuf);
                         } else {  // ST_PARTIAL3D
-                            tma_store_3d(mD, ncol0, m0 + warp * 32, tc.z, stage);
+                            tma_store_3d(mD, ncol0, m0 + warp * 32, tc.z, sbuf);
                         }
                         bulk_commit();
                     }
-                    pending = true;
                     continue;
                 }
                 // direct stores (outputs TMA cannot describe)

@@ -111,6 +111,18 @@ def test_halo_tile_plans(S):
     assert plan(0, 2, 8, 8, 48, 64)["conv_halo"] == 0                 # input channels % 32 != 0
 
 
+def test_rgb_layer_plans(S):
+    """The RGB layer's forward (3 -> 64 channels, pad 1) takes the tensor cores with its
+    im2col rows built in shared memory; other few-channel forwards stay on the CUDA cores."""
+    for shape in [(64, 224, 224, 3, 64), (128, 32, 32, 3, 64), (3, 7, 9, 3, 64)]:
+        p = S.sprint_conv_plan(0, *shape, 1, True)
+        assert p["path"] == "tc" and p["conv_rgb"] == 1 and p["bn"] == 64 and p["num_kt"] == 1
+        assert S.sprint_conv_workspace_size(0, *shape, 1) == 64 * 32 * 4   # the padded weights
+    for shape in [(8, 32, 32, 3, 16), (2, 11, 9, 4, 64), (2, 37, 35, 3, 48)]:
+        p = S.sprint_conv_plan(0, *shape, 1, True)
+        assert p["conv_rgb"] == 0 and p["path"] == "smallc"
+
+
 def test_batched_entry_points_validate(S):
     L = S.lib()
     f1 = ctypes.c_float(1)

@@ -55,8 +55,10 @@ def test_conv_at_configured_size(S, net, li, N, H, W, Cin, Cout):
     ws = torch.empty(nb // 4 + 64, dtype=torch.float32, device="cuda")
     for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX, S.SPRINT_CONV_DW):
         PLANS[(net, li, op)] = S.sprint_conv_plan(op, N, H, W, Cin, Cout, 1, True)
-    # the plans the training step gets: the tensor cores for every layer but the RGB one
-    assert PLANS[(net, li, S.SPRINT_CONV_FWD)]["path"] == ("smallc" if Cin <= 4 else "tc")
+    # the plans the training step gets: the tensor cores for every layer (the RGB layer's forward
+    # with its im2col rows built in shared memory) but the RGB layer's weight gradient
+    assert PLANS[(net, li, S.SPRINT_CONV_FWD)]["path"] == "tc"
+    assert PLANS[(net, li, S.SPRINT_CONV_FWD)]["conv_rgb"] == (Cin == 3)
     assert PLANS[(net, li, S.SPRINT_CONV_DW)]["path"] == ("smallc" if Cin <= 4 else "tc")
 
     y = torch.empty((N, H, W, Cout), dtype=torch.float32, device="cuda")

@@ -498,7 +498,9 @@ CONV_CASES = [
     (4, 8, 8, 32, 64),      # tensor-core weight gradient, W*N = 32 per row
     (12, 7, 5, 64, 32),     # ragged rows (W*N = 60), Cout < 128
     (32, 4, 4, 128, 256),   # wide channels, split-K
-    (4, 12, 12, 3, 64),     # RGB layer, batch % 4 == 0: padded im2col forward, tensor-core weight gradient
+    (4, 12, 12, 3, 64),     # RGB layer 3 -> 64: im2col rows in shared memory (tensor cores), tensor-core dW
+    (3, 7, 9, 3, 64),       # the same with a ragged last pixel tile (189 pixels)
+    (2, 37, 35, 3, 64),     # the same across image rows and images (2590 pixels)
     (8, 9, 7, 3, 16),       # RGB layer, ragged spatial size
     (3, 7, 6, 1, 16),       # one input channel: direct CUDA-core forward, zero-filled tap boxes in dW
     (4, 8, 5, 4, 32),       # four input channels: direct forward (4-wide patch), CUDA-core dX
