@@ -2168,7 +2168,7 @@ static int conv_impl_tc(const ConvPlan& pl, const float* act, int act_c, int act
 
 // Persistent CTA pairs of the halo-staged convolution (at most as many as can be resident).
 template <int BN>
-int launch_halo_bn(const TcMaps<1>& maps, const TcParams& p, cudaStream_t s) {
+int launch_halo_bn(const HaloMaps& maps, const TcParams& p, cudaStream_t s) {
     static bool attr_done[64] = {};
     static int slots[64] = {};
     int dev = 0;
@@ -2232,10 +2232,28 @@ static int conv_halo_tc(const ConvPlan& pl, const float* act, int act_c, int act
     p.n_tiles = static_cast<int>(n_tiles);
     p.z_tiles = 1;
     p.num_tiles = static_cast<int>(units * n_tiles);
-    TcMaps<1> maps;
-    maps.a[0] = ta;
-    maps.b[0] = *tb;
-    maps.d[0] = ta;
+    HaloMaps maps;
+    maps.a = ta;
+    maps.b = *tb;
+    maps.d = maps.dt = maps.m = maps.mt = ta;
+    p.halo_tma = 0;
+    if (pl.tile.bn == 192 && pl.box.bh == 1 && (p.ldd & 3) == 0 && aligned16(p.D) &&
+        (!p.mask || ((p.ldm & 3) == 0 && aligned16(p.mask)))) {
+        // one-row tiles: each epilogue warp's 32 (or the row's last bw % 32) pixels as TMA boxes of
+        // 32 channels, for its stores and its mask block
+        const int tw = pl.box.bw % 32;
+        const uint64_t dd[4] = {(uint64_t)ncols, (uint64_t)p.out_w, (uint64_t)p.out_h, (uint64_t)p.img_n};
+        const uint64_t sd[3] = {(uint64_t)p.ldd * 4, (uint64_t)p.out_w * p.ldd * 4,
+                                (uint64_t)p.out_h * p.out_w * p.ldd * 4};
+        const uint64_t sm[3] = {(uint64_t)p.ldm * 4, (uint64_t)p.out_w * p.ldm * 4,
+                                (uint64_t)p.out_h * p.out_w * p.ldm * 4};
+        const uint32_t b32[4] = {32, 32, 1, 1}, btw[4] = {32, (uint32_t)(tw ? tw : 32), 1, 1};
+        bool ok = make_tmap(&maps.d, p.D, 4, dd, sd, b32, false) && make_tmap(&maps.dt, p.D, 4, dd, sd, btw, false);
+        if (ok && p.mask)
+            ok = make_tmap(&maps.m, p.mask, 4, dd, sm, b32, false) && make_tmap(&maps.mt, p.mask, 4, dd, sm, btw, false);
+        if (ok) p.halo_tma = 1;
+        else maps.d = maps.dt = maps.m = maps.mt = ta;
+    }
     *done = true;
     return pl.tile.bn == 192 ? launch_halo_bn<192>(maps, p, s) : launch_halo_bn<128>(maps, p, s);
 }

@@ -220,6 +220,9 @@ struct TcParams {
     int z_mid;
     // CONV_RGB: the layer input x [img_n][out_h][out_w][3]
     const float* act;
+    // halo-staged kernel, factored tiles of one output row: each epilogue warp loads its mask block
+    // and stores its outputs by TMA (maps d / m: 32-pixel boxes, dt / mt: the row's last bw % 32)
+    int halo_tma;
 };
 
 #if defined(__CUDACC__)

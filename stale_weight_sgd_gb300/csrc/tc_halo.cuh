@@ -60,7 +60,7 @@ __host__ __device__ constexpr int halo_rows_needed(int bw, int bh) {
     return ((bh + 2) * (bw + 2) > 2 * (bw + 2) + 2 + TC_BM ? (bh + 2) * (bw + 2) : 2 * (bw + 2) + 2 + TC_BM);
 }
 // ring depths: halo buffers, and B stages of three k-tiles (a pair's half of the BN rows each)
-__host__ __device__ constexpr int halo_a_stages(int bn) { return bn == 192 ? 3 : (bn >= 128 ? 2 : 3); }
+__host__ __device__ constexpr int halo_a_stages(int bn) { return bn == 192 ? 2 : (bn >= 128 ? 2 : 3); }
 __host__ __device__ constexpr int halo_b_stage(int bn) { return 3 * (bn / 2) * TC_BK * 4; }
 __host__ __device__ constexpr int halo_b_stages(int bn) { return bn == 192 ? 2 : (bn >= 128 ? 5 : 6); }
 // BN = 192: the edge rows the epilogue warps pass on (two co halves x 4 warps x 3 rows x 32 floats)
@@ -68,12 +68,19 @@ constexpr int HALO_XCH_BYTES = 2 * 4 * 3 * 32 * 4;
 // warps 0-7 drain the accumulator (warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 and split
 // its columns), warp 8 loads, warp 9 issues the MMAs
 constexpr int HALO_THREADS = 320;
-// per epilogue warp: 8 rows of 128 B through which its stores (and mask loads) go out as whole rows
-constexpr int HALO_STG_BYTES = 8 * 8 * 128;
+// per epilogue warp: rows of 128 B through which its stores (and mask loads) go out as whole rows;
+// BN = 192 has a 32-row (4 KB) box per warp for its TMA mask loads and stores
+__host__ __device__ constexpr int halo_stg_warp(int bn) { return bn == 192 ? 32 * 128 : 8 * 128; }
 __host__ __device__ constexpr int halo_smem_bytes(int bn) {
-    return 1024 + halo_a_stages(bn) * HALO_A_BYTES + halo_b_stages(bn) * halo_b_stage(bn) + 512 +
-           HALO_STG_BYTES + (bn == 192 ? HALO_XCH_BYTES : 0);
+    return 1024 + halo_a_stages(bn) * HALO_A_BYTES + halo_b_stages(bn) * halo_b_stage(bn) + 1024 +
+           8 * halo_stg_warp(bn) + (bn == 192 ? HALO_XCH_BYTES : 0);
 }
+
+// Tensor maps of a halo launch: A (input, halo boxes), B (weights); BN = 192 with halo_tma: D and the
+// ReLU mask in boxes of 32 pixels (d, m) and of the row's last bw % 32 (dt, mt), 32 channels each.
+struct HaloMaps {
+    CUtensorMap a, b, d, dt, m, mt;
+};
 
 // CTA tile mt of a halo launch: image n, first output row h0 and pixel w0 (n >= img_n past the
 // last tile)
@@ -165,7 +172,7 @@ __device__ __forceinline__ void halo_mask_rows(float (&o)[32], long long moff, c
 // EPI_MASK: x 0 where mask <= 0), D / ldd, bias, mask / ldm, N (output channels), status.
 template <int BN>
 __global__ void __launch_bounds__(HALO_THREADS, 1)
-    tc_halo_kernel(const __grid_constant__ TcMaps<1> maps, const TcParams p) {
+    tc_halo_kernel(const __grid_constant__ HaloMaps maps, const TcParams p) {
     constexpr bool FACT = BN == 192;             // factored over the kernel columns (64 output channels)
     constexpr int SA = halo_a_stages(BN);
     constexpr int SB = halo_b_stages(BN);
@@ -184,16 +191,17 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + SA * HALO_A_BYTES;
-    uint64_t* a_full = reinterpret_cast<uint64_t*>(sB + SB * B_STAGE);   // barriers: 512 bytes
+    uint64_t* a_full = reinterpret_cast<uint64_t*>(sB + SB * B_STAGE);   // barriers: 1024 bytes
     uint64_t* a_empty = a_full + SA;
     uint64_t* b_full = a_empty + SA;
     uint64_t* b_empty = b_full + SB;
     uint64_t* tmem_full = b_empty + SB;    // [2]
     uint64_t* tmem_empty = tmem_full + 2;  // [2]
     uint64_t* mma_done = tmem_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-    uint8_t* sStg = smem + SA * HALO_A_BYTES + SB * B_STAGE + 512;
-    float* xch = reinterpret_cast<float*>(sStg + HALO_STG_BYTES);                                // BN = 192
+    uint64_t* mask_bar = mma_done + 1;     // [8]: an epilogue warp's TMA mask box
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mask_bar + 8);
+    uint8_t* sStg = smem + SA * HALO_A_BYTES + SB * B_STAGE + 1024;   // 1024-aligned (128B-swizzled TMA boxes)
+    float* xch = reinterpret_cast<float*>(sStg + 8 * halo_stg_warp(BN));                          // BN = 192
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -218,9 +226,10 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
             mbar_init(&tmem_empty[b], 16);   // one arrival per epilogue warp of both CTAs
         }
         mbar_init(mma_done, 1);
+        for (int w = 0; w < 8; ++w) mbar_init(&mask_bar[w], 1);
         fence_mbar_init();
-        tma_prefetch_desc(&maps.a[0]);
-        tma_prefetch_desc(&maps.b[0]);
+        tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.b);
     }
     if (warp == 9) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -237,8 +246,8 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
         if (lane == 0) {
             uint32_t ia = 0, ib = 0;
             bool alive = true;
-            const CUtensorMap* mA = &maps.a[0];
-            const CUtensorMap* mB = &maps.b[0];
+            const CUtensorMap* mA = &maps.a;
+            const CUtensorMap* mB = &maps.b;
             for (int t = unit0; t < p.num_tiles && alive; t += units) {
                 const int mt = 2 * (t % p.m_tiles) + static_cast<int>(rank);
                 const int n0 = (t / p.m_tiles) * BN + static_cast<int>(rank) * B_ROWS;
@@ -344,7 +353,13 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
         const int quarter = warp & 3, grp = warp >> 2;   // TMEM lanes 32 * quarter .., column group
         const int r = quarter * 32 + lane;               // tile position = TMEM lane
         const int hr = r / pitch, wc = r % pitch;
-        uint8_t* stg = sStg + warp * (HALO_STG_BYTES / 8);
+        uint8_t* stg = sStg + warp * halo_stg_warp(BN);
+        // TMA epilogue (BN = 192, one-row tiles): this warp's pixels w0 + 32 quarter .. (cnt of them)
+        const int cnt = p.bw - 32 * quarter < 32 ? p.bw - 32 * quarter : 32;
+        const CUtensorMap* mapd = cnt == 32 ? &maps.d : &maps.dt;
+        const CUtensorMap* mapm = cnt == 32 ? &maps.m : &maps.mt;
+        uint32_t nmask = 0, nmask_issued = 0;   // mask boxes waited for (the barrier's phase) / issued
+        bool mask_ok = true;                     // no mask wait has run out
         uint32_t j = 0;
         for (int t = unit0; t < p.num_tiles; t += units, ++j) {
             const int mt = 2 * (t % p.m_tiles) + static_cast<int>(rank);
@@ -362,9 +377,19 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
                 for (int c = (FACT ? 0 : nt * BN) + 32 * grp; c < (FACT ? 64 : nt * BN + BN) && c < p.N; c += 64)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.mask + moff + c) : "memory");
             }
+            // TMA epilogue: the warp's box lies in the image (TMA clips its end at the image edge)
+            const bool tbox = FACT && p.halo_tma && cnt > 0 && n < p.img_n && h0 < p.out_h && w0 + 32 * quarter < p.out_w;
+            if (tbox && masked) {   // the mask block on its way while the MMAs run
+                if (lane == 0) {
+                    bulk_wait_read0();   // the buffer's last store has read it
+                    mbar_arrive_expect_tx(&mask_bar[warp], static_cast<uint32_t>(cnt) * 128u);
+                    tma_load_4d(stg, mapm, 32 * grp, w0 + 32 * quarter, h0, n, &mask_bar[warp]);
+                }
+                ++nmask_issued;
+            }
             const uint32_t b = j & 1, tph = (j >> 1) & 1;
             bool ok = mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE);
-            if constexpr (FACT) ok = epi_all(grp, ok);   // the group's four warps go on, or none
+            if constexpr (FACT) ok = epi_all(grp, ok && mask_ok);   // the group's four warps go on, or none
             if (!ok) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -432,10 +457,41 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
                             const float x = o[q] + (p.bias ? p.bias[col + q] : 0.f);
                             o[q] = p.relu ? fmaxf(x, 0.f) : x;
                         }
-                    } else if (masked) {
+                    } else if (masked && !p.halo_tma) {
                         halo_mask_rows(o, moff >= 0 ? moff + col : -1, p.mask, stg, lane);
                     }
-                    halo_store_rows(o, off >= 0 ? off + col : -1, p.D, stg, lane);
+                    if (!p.halo_tma) {
+                        halo_store_rows(o, off >= 0 ? off + col : -1, p.D, stg, lane);
+                        continue;
+                    }
+                    if (!tbox) continue;
+                    if (masked) {   // lane l's mask row l of the box, 128B-swizzled as TMA wrote it
+                        if (!mbar_wait_bounded(&mask_bar[warp], nmask & 1, p.status, DEV_FLAG_WAIT_EPILOGUE))
+                            mask_ok = false;   // the group stops at the next tile
+                        ++nmask;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float4 m = *reinterpret_cast<const float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4));
+                            o[4 * k] = m.x > 0.f ? o[4 * k] : 0.f;
+                            o[4 * k + 1] = m.y > 0.f ? o[4 * k + 1] : 0.f;
+                            o[4 * k + 2] = m.z > 0.f ? o[4 * k + 2] : 0.f;
+                            o[4 * k + 3] = m.w > 0.f ? o[4 * k + 3] : 0.f;
+                        }
+                        __syncwarp();   // every lane has read its mask row before the rows are rewritten
+                    } else {
+                        if (lane == 0) bulk_wait_read0();   // the buffer's last store has read it
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                            make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(mapd, col, w0 + 32 * quarter, h0, n, stg);
+                        bulk_commit();
+                    }
                 }
                 continue;
             }
@@ -467,6 +523,10 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
                 halo_store_rows(o, off >= 0 ? off + col : -1, p.D, stg, lane);
             }
         }
+        // a mask box still in flight (a group that stopped early) lands before the CTA exits
+        for (; nmask < nmask_issued; ++nmask) mbar_wait_bounded(&mask_bar[warp], nmask & 1, p.status, DEV_FLAG_WAIT_EPILOGUE);
+        if (lane == 0) bulk_wait0();   // every TMA store of this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before();
