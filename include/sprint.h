@@ -102,6 +102,9 @@ int sprint_device_status(int* flags_out, int reset);
  *       the forward pass with BN = 128): a tile is [9] rows of [8] output
  *       pixels, read once per 32-channel chunk with its one-pixel border;
  *       used where such tiles fill >= 80% of the 128 MMA rows
+ *   [16] 1 = the halo-staged tiles of 128 outputs in their flipped form: the
+ *       weights as the 128-row MMA operand and 256 tile positions ([9] rows
+ *       of [8] pixels) as its N side, one CTA per tile ([1] = 128, [2] = 0)
  *   [15] 1 = forward of the RGB layer (3 input, 64 output channels, pad 1)
  *       on the tensor cores, its im2col rows written into shared memory (no
  *       workspace beyond the weights padded to 32 columns)
@@ -110,7 +113,7 @@ int sprint_device_status(int* flags_out, int reset);
  * sprint_gemm_plan: the grouped tensor-core GEMM D[M][N] = A[M][K] B[N][K]^T
  * over `batch` problems (the batched FC calls), allow_tail as when the
  * workspace holds the tail slabs. */
-#define SPRINT_PLAN_FIELDS 16
+#define SPRINT_PLAN_FIELDS 17
 #define SPRINT_PATH_SIMT 0
 #define SPRINT_PATH_TC 1
 #define SPRINT_PATH_SMALLC 2

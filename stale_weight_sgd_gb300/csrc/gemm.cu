@@ -1401,6 +1401,7 @@ struct ConvPlan {
     bool wg_fact = false;          // dedw factored over kernel rows x columns (Cin = Cout = 64)
     bool rgb = false;              // fwd of the RGB layer (3 -> 64 channels): im2col rows built in shared memory
     bool halo = false;             // fwd / dedx on halo-staged tiles of whole output rows (64 or 128 output channels)
+    bool hflip = false;            // that with 128 outputs, weights as M and 256 tile positions as N (one CTA)
     bool fact = false;             // fwd / dedx factored over the kernel columns (64 output channels, wide rows)
     size_t ws_wfact = 0;           // its permuted weights
     GemmPlan gp{};                 // fwd / dedx: tile shape and the k-split of the last, partial round
@@ -1448,8 +1449,30 @@ ConvPlan plan_conv(int op, int N, int H, int W, int Cin, int Cout, int pad, bool
         // columns, a 192-wide GEMM instead of a 64-wide one
         const int nout = op == SPRINT_CONV_FWD ? Cout : Cin, kch = op == SPRINT_CONV_FWD ? Cin : Cout;
         const int fw = op == SPRINT_CONV_FWD ? Wo : W;
-        // (the input gradient with 128 outputs stays tap by tap: measured faster there, its ReLU-mask
-        // reads weigh more in the halo epilogue)
+        if (pad == 1 && nout == 128 && kch % 32 == 0 && fw + 2 <= HALO_F_POS &&
+            (op == SPRINT_CONV_FWD || kch >= 256)) {
+            // 128 outputs: tiles of 256 positions (bh rows of the whole row width) against the weights
+            // as the 128-row operand, used when they fill >= 80% of the positions (for the input
+            // gradient only with >= 8 chunks of reduction: with 4, a tile's MMAs are too short to hide
+            // its mask reads, and the tap-by-tap tiles measured faster)
+            const int fh = op == SPRINT_CONV_FWD ? Ho : H;
+            int bh = HALO_F_POS / (fw + 2);
+            if (bh > fh) bh = fh;
+            const int th = (fh + bh - 1) / bh;
+            const double fill = static_cast<double>(fw) * fh / (static_cast<double>(th) * HALO_F_POS);
+            if (halo_f_rows_needed(fw, bh) * 128 <= HALO_F_A_BYTES && fill >= 0.8) {
+                pl.tc = pl.halo = pl.hflip = true;
+                pl.tile.bn = 128;
+                pl.tile.pair = false;
+                pl.box = PixBox{fw, bh, 1, 1, th, N};
+                pl.num_kt = 9 * (kch / 32);
+                pl.kt_per_split = pl.num_kt;
+                if (op == SPRINT_CONV_DX && !have_wT) pl.ws_wT = fbytes(9ll * Cin * Cout);
+                return pl;
+            }
+        }
+        // (the input gradient with 128 outputs stays tap by tap otherwise: measured faster than the
+        // pair tiles below, its ReLU-mask reads weigh more in their epilogue)
         if (pad == 1 && (nout == 64 || (nout == 128 && op == SPRINT_CONV_FWD)) && kch % 32 == 0) {
             // halo-staged tiles: bh output rows of bw pixels (bw + 2 <= 115, so a 128-row MMA
             // covers them and the buffer fits its stage), used when they fill >= 80% of the rows
@@ -2204,6 +2227,23 @@ int launch_halo_bn(const HaloMaps& maps, const TcParams& p, cudaStream_t s) {
     return check_launch("tc_halo_kernel");
 }
 
+// Persistent CTAs of the flipped halo-staged convolution (one per SM at most).
+int launch_halo_flip(const HaloMaps& maps, const TcParams& p, cudaStream_t s) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(tc_halo_flip_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, HALO_F_SMEM) !=
+            cudaSuccess)
+            return check_cuda("cudaFuncSetAttribute(tc_halo_flip_kernel)");
+        attr_done[dev] = true;
+    }
+    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+    tc_halo_flip_kernel<<<grid, HALO_THREADS, HALO_F_SMEM, s>>>(maps, p);
+    return check_launch("tc_halo_flip_kernel");
+}
+
 // The halo-staged implicit GEMM (CTA pairs, BN = ncols = 64 or 128): A = act (NHWC, act_c
 // channels) in boxes of (bh + 2) x (bw + 2) pixels around each tile, B through *tb (the map of
 // the tap-by-tap implicit GEMM, boxes of BN / 2 rows).
@@ -2225,6 +2265,18 @@ static int conv_halo_tc(const ConvPlan& pl, const float* act, int act_c, int act
     p.num_kt = pl.num_kt;
     p.kt_per_split = pl.num_kt;
     p.store = ST_DIRECT;
+    if (pl.hflip) {   // one CTA per tile, all 128 output channels
+        SPRINT_REQUIRE(pl.box.tiles() < (1ll << 31), SPRINT_ERR_SHAPE, "conv: %lld halo tiles is too many",
+                       pl.box.tiles());
+        p.m_tiles = p.num_tiles = static_cast<int>(pl.box.tiles());
+        p.n_tiles = p.z_tiles = 1;
+        HaloMaps maps;
+        maps.a = ta;
+        maps.b = *tb;
+        maps.d = maps.dt = maps.m = maps.mt = ta;
+        *done = true;
+        return launch_halo_flip(maps, p, s);
+    }
     const long long units = (pl.box.tiles() + 1) / 2, n_tiles = (ncols + pl.tile.bn - 1) / pl.tile.bn;
     SPRINT_REQUIRE(units * n_tiles < (1ll << 31), SPRINT_ERR_SHAPE, "conv: %lld halo tiles is too many",
                    units * n_tiles);
@@ -2774,6 +2826,7 @@ extern "C" int sprint_conv_plan(int op, int N, int H, int W, int Cin, int Cout, 
     out[13] = pl.fact ? 1 : 0;
     out[14] = pl.halo ? 1 : 0;
     out[15] = pl.rgb ? 1 : 0;
+    out[16] = pl.hflip ? 1 : 0;
     return SPRINT_OK;
 }
 

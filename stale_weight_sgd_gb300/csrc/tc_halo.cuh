@@ -540,4 +540,260 @@ __global__ void __launch_bounds__(HALO_THREADS, 1)
 
 #endif  // __CUDACC__
 
+// ---------------------------------------------------------------------------------------------
+// 128 output channels with the roles swapped ("flipped"): the weights are the MMA's M = 128
+// operand and 256 tile positions its N side, one CTA per tile (M = 128, N = 256: the math rate,
+// where the pair tile of N = 128 above sits at the ~123-cycle floor of a narrow MMA). A tile is
+// bh output rows of bw pixels with bh * (bw + 2) <= 256 positions; per 32-channel chunk one halo
+// box of (bh + 2) x (bw + 2) input pixels, and per tap the B operand is the 256-row window of it
+// that starts dh * pitch + dw rows in (the mirrored tap for the input gradient), the A operand the
+// tap's 128 x 32 weight slice. The accumulator holds [channel][position]: epilogue warp w reads
+// channels 32 (w % 4) .. + 31 (its TMEM lanes) and position chunks w / 4, w / 4 + 2, ..., and
+// stores each position's 32 channels as one 128-byte row (bias: one value per lane).
+constexpr int HALO_F_POS = 256;                   // tile positions (the MMA's N)
+constexpr int HALO_F_A_BYTES = 61 * 1024;         // halo buffer: at most 488 pixel rows
+constexpr int HALO_F_SA = 2, HALO_F_SW = 6;       // halo stages; weight stages (one tap each)
+constexpr int HALO_F_W_STAGE = TC_BM * TC_BK * 4; // 128 channels x 32 k
+constexpr int HALO_F_SMEM = 1024 + HALO_F_SA * HALO_F_A_BYTES + HALO_F_SW * HALO_F_W_STAGE + 1024;
+__host__ __device__ constexpr int halo_f_rows_needed(int bw, int bh) {
+    return ((bh + 2) * (bw + 2) > 2 * (bw + 2) + 2 + HALO_F_POS ? (bh + 2) * (bw + 2)
+                                                                 : 2 * (bw + 2) + 2 + HALO_F_POS);
+}
+
+#if defined(__CUDACC__)
+
+// p as for tc_halo_kernel; tiles m_tiles (= num_tiles), N = 128 output channels.
+__global__ void __launch_bounds__(HALO_THREADS, 1)
+    tc_halo_flip_kernel(const __grid_constant__ HaloMaps maps, const TcParams p) {
+    constexpr int SA = HALO_F_SA, SW = HALO_F_SW;
+    constexpr uint32_t IDESC = idesc_tf32(HALO_F_POS, false, false, TC_BM);
+    constexpr uint32_t TMEM_COLS = 512, ACC_STRIDE = 256;
+    static_assert(HALO_F_SMEM <= 232448, "shared memory budget exceeded");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* sH = smem;
+    uint8_t* sW = smem + SA * HALO_F_A_BYTES;
+    uint64_t* h_full = reinterpret_cast<uint64_t*>(sW + SW * HALO_F_W_STAGE);
+    uint64_t* h_empty = h_full + SA;
+    uint64_t* w_full = h_empty + SA;
+    uint64_t* w_empty = w_full + SW;
+    uint64_t* tmem_full = w_empty + SW;     // [2]
+    uint64_t* tmem_empty = tmem_full + 2;   // [2]
+    uint64_t* mma_done = tmem_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int pitch = p.bw + 2;
+    const uint32_t h_bytes = static_cast<uint32_t>((p.bh + 2) * pitch) * 128u;
+
+    if (warp == 8 && lane == 0) {
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&h_full[s], 1);
+            mbar_init(&h_empty[s], 1);
+        }
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tmem_full[b], 1);
+            mbar_init(&tmem_empty[b], 8);   // one arrival per epilogue warp
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.b);
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 8) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t ih = 0, iw = 0;
+            bool alive = true;
+            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x) {
+                int n, h0, w0;
+                halo_tile(p, t, n, h0, w0);
+                for (int c = 0; c < p.chunks && alive; ++c) {
+                    const uint32_t sa = ih % SA;
+                    if (!mbar_wait_bounded(&h_empty[sa], ((ih / SA) & 1) ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&h_full[sa], h_bytes);
+                    tma_load_4d(sH + sa * HALO_F_A_BYTES, &maps.a, c * TC_BK, w0 - 1, h0 - 1, n, &h_full[sa]);
+                    ++ih;
+                    for (int tap = 0; tap < 9; ++tap) {
+                        const uint32_t sw = iw % SW;
+                        if (!mbar_wait_bounded(&w_empty[sw], ((iw / SW) & 1) ^ 1, p.status, DEV_FLAG_WAIT_PRODUCER)) {
+                            alive = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&w_full[sw], HALO_F_W_STAGE);
+                        if (p.b_tap_outer)
+                            tma_load_3d(sW + sw * HALO_F_W_STAGE, &maps.b, c * TC_BK, 0, tap, &w_full[sw]);
+                        else
+                            tma_load_3d(sW + sw * HALO_F_W_STAGE, &maps.b, c * TC_BK, tap, 0, &w_full[sw]);
+                        ++iw;
+                    }
+                }
+            }
+            // every copy issued above has landed before the CTA may exit
+            for (uint32_t k = ih > static_cast<uint32_t>(SA) ? ih - SA : 0u; k < ih; ++k)
+                if (!mbar_wait_bounded(&h_full[k % SA], (k / SA) & 1, p.status, DEV_FLAG_WAIT_PRODUCER)) break;
+            for (uint32_t k = iw > static_cast<uint32_t>(SW) ? iw - SW : 0u; k < iw; ++k)
+                if (!mbar_wait_bounded(&w_full[k % SW], (k / SW) & 1, p.status, DEV_FLAG_WAIT_PRODUCER)) break;
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t ih = 0, iw = 0, j = 0;
+            bool alive = true;
+            for (int t = blockIdx.x; t < p.num_tiles && alive; t += gridDim.x, ++j) {
+                const uint32_t b = j & 1, tph = (j >> 1) & 1;
+                if (!mbar_wait_bounded(&tmem_empty[b], tph ^ 1, p.status, DEV_FLAG_WAIT_MMA)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * ACC_STRIDE;
+                for (int c = 0; c < p.chunks && alive; ++c) {
+                    const uint32_t sa = ih % SA;
+                    if (!mbar_wait_bounded(&h_full[sa], (ih / SA) & 1, p.status, DEV_FLAG_WAIT_MMA)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t h_base = smem_u32(sH + sa * HALO_F_A_BYTES);
+                    for (int tap = 0; tap < 9; ++tap) {
+                        const uint32_t sw = iw % SW;
+                        if (!mbar_wait_bounded(&w_full[sw], (iw / SW) & 1, p.status, DEV_FLAG_WAIT_MMA)) {
+                            alive = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int dh = tap / 3, dw = tap % 3;
+                        const int off = p.tap_sign > 0 ? dh * pitch + dw : (2 - dh) * pitch + (2 - dw);
+                        const uint32_t b_win = h_base + static_cast<uint32_t>(off) * 128u;
+                        const uint32_t a_base = smem_u32(sW + sw * HALO_F_W_STAGE);
+#pragma unroll
+                        for (int kk = 0; kk < TC_BK / 8; ++kk) {
+                            const uint64_t da = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                            const uint64_t db = smem_desc_sw128(b_win + kk * 32, 16, 1024);
+                            mma_tf32(d_tmem, da, db, IDESC, (c > 0 || tap > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&w_empty[sw]);
+                        ++iw;
+                    }
+                    if (!alive) break;
+                    mma_commit(&h_empty[sa]);
+                    ++ih;
+                }
+                mma_commit(&tmem_full[b]);
+            }
+            mma_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, p.status, DEV_FLAG_WAIT_MMA);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- epilogue (warps 0-7)
+        const int quarter = warp & 3, grp = warp >> 2;
+        const int co = quarter * 32 + lane;   // this lane's output channel (TMEM lane)
+        const bool masked = p.epi == EPI_MASK && p.mask;
+        const float bias_co = (p.epi == EPI_STORE && p.bias) ? p.bias[co] : 0.f;
+        uint32_t j = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++j) {
+            int n, h0, w0;
+            halo_tile(p, t, n, h0, w0);
+            if (masked) {   // this warp's mask lines (position lane of each of its chunks) on their way to L2
+#pragma unroll
+                for (int k = 0; k < HALO_F_POS / 64; ++k) {
+                    const int pos = (grp + 2 * k) * 32 + lane, hr = pos / pitch, wc = pos - hr * pitch;
+                    if (hr < p.bh && wc < p.bw && h0 + hr < p.out_h && w0 + wc < p.out_w)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                            p.mask + ((static_cast<long long>(n) * p.out_h + h0 + hr) * p.out_w + w0 + wc) * p.ldm +
+                            quarter * 32)
+                                     : "memory");
+                }
+            }
+            const uint32_t b = j & 1, tph = (j >> 1) & 1;
+            if (!mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+            for (int k = 0; k < HALO_F_POS / 64; ++k) {
+                const int chunk = grp + 2 * k;   // positions 32 chunk .. + 31
+                uint32_t v[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(tb + chunk * 32, v);
+                tmem_wait_ld();
+                if (k == HALO_F_POS / 64 - 1) {   // this warp's part of the accumulator is read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(smem_u32(&tmem_empty[b]));
+                }
+                // position -> (row, column) of the tile, stepped along the chunk (warp-uniform)
+                int hr = (chunk * 32) / pitch, wc = chunk * 32 - hr * pitch;
+                long long pix = (static_cast<long long>(n) * p.out_h + h0 + hr) * p.out_w + w0 + wc;
+                float mv[32];
+                if (masked) {   // the chunk's mask values, all in flight before they are used
+                    int hr2 = hr, wc2 = wc;
+                    long long px2 = pix;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const bool ok = hr2 < p.bh && wc2 < p.bw && h0 + hr2 < p.out_h && w0 + wc2 < p.out_w &&
+                                        n < p.img_n;
+                        mv[q] = ok ? p.mask[px2 * p.ldm + co] : 0.f;
+                        if (++wc2 == pitch) {
+                            wc2 = 0;
+                            ++hr2;
+                            px2 += p.out_w - pitch + 1;
+                        } else {
+                            ++px2;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const bool ok = hr < p.bh && wc < p.bw && h0 + hr < p.out_h && w0 + wc < p.out_w && n < p.img_n;
+                    if (ok) {
+                        float x = __uint_as_float(v[q]);
+                        if (p.epi == EPI_STORE) {
+                            x += bias_co;
+                            if (p.relu) x = fmaxf(x, 0.f);
+                        } else if (masked) {
+                            x = mv[q] > 0.f ? x : 0.f;
+                        }
+                        p.D[pix * p.ldd + co] = x;
+                    }
+                    if (++wc == pitch) {
+                        wc = 0;
+                        ++hr;
+                        pix += p.out_w - pitch + 1;
+                    } else {
+                        ++pix;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+#endif  // __CUDACC__
+
 }  // namespace sprint

@@ -137,7 +137,7 @@ def sprint_launch_count() -> int:
 
 
 PLAN_FIELDS = ("path", "bn", "pair", "splits", "tail_splits", "wg_tpt", "wg_rows", "num_kt", "box_w", "box_h",
-               "box_img", "wg_blocked", "wg_fact", "conv_fact", "conv_halo", "conv_rgb")
+               "box_img", "wg_blocked", "wg_fact", "conv_fact", "conv_halo", "conv_rgb", "conv_hflip")
 PATH_NAMES = {0: "simt", 1: "tc", 2: "smallc", 3: "im2col"}
 
 

@@ -89,24 +89,31 @@ def test_shape_and_workspace_errors(S):
 
 
 def test_halo_tile_plans(S):
-    """Host-side tile choice of the halo-staged forward / input gradient: 64 or
-    128 output channels, tiles of whole output rows that fill >= 80% of the 128
-    MMA rows, the halo buffer within its stage."""
+    """Host-side tile choice of the halo-staged forward / input gradient: 64 outputs on CTA
+    pairs, factored to 192 columns, tiles of whole output rows filling >= 80% of the 128 MMA
+    rows; 128 outputs flipped (weights as the 128-row operand, 256 tile positions as N, one
+    CTA per tile) when such tiles fill >= 80% of the positions; the halo buffer within its stage."""
     def plan(op, N, H, W, Cin, Cout):
         return S.sprint_conv_plan(op, N, H, W, Cin, Cout, 1, True)
-    for N, H, W, Cin, Cout, bw, bh in [(64, 224, 224, 64, 64, 112, 1), (64, 112, 112, 64, 128, 112, 1),
-                                       (64, 112, 112, 128, 128, 112, 1), (2, 15, 28, 64, 128, 28, 4),
-                                       (1, 3, 221, 64, 64, 111, 1)]:
+    for N, H, W, Cin, Cout, bw, bh in [(64, 224, 224, 64, 64, 112, 1), (1, 3, 221, 64, 64, 111, 1)]:
         p = plan(0, N, H, W, Cin, Cout)
-        # 64 outputs factored over the kernel columns: a 192-wide MMA
-        assert p["conv_halo"] == 1 and p["pair"] == 1 and p["bn"] == (192 if Cout == 64 else Cout), p
+        assert p["conv_halo"] == 1 and p["conv_hflip"] == 0 and p["pair"] == 1 and p["bn"] == 192, p
         assert (p["box_w"], p["box_h"], p["box_img"]) == (bw, bh, 1)
         assert p["num_kt"] == 9 * Cin // 32
         assert (bw + 2) * bh <= 128 and 2 * (bw + 2) + 130 <= 360   # the last tap's window inside the buffer
-    assert plan(1, 64, 112, 112, 64, 128)["conv_halo"] == 1           # dX of conv2_1: 64 output channels
-    assert plan(1, 64, 56, 56, 128, 256)["conv_halo"] == 0            # dX with 128 output channels: tap by tap
+    for op, N, H, W, Cin, Cout, bw, bh in [(0, 64, 112, 112, 64, 128, 112, 2), (0, 64, 112, 112, 128, 128, 112, 2),
+                                           (1, 64, 56, 56, 128, 256, 56, 4), (0, 2, 15, 28, 64, 128, 28, 8)]:
+        p = plan(op, N, H, W, Cin, Cout)
+        assert p["conv_halo"] == 1 and p["conv_hflip"] == 1 and p["pair"] == 0 and p["bn"] == 128, p
+        assert (p["box_w"], p["box_h"]) == (bw, bh)
+        assert (bw + 2) * bh <= 256 and max((bh + 2) * (bw + 2), 2 * (bw + 2) + 258) <= 488
+    assert plan(1, 64, 112, 112, 64, 128)["conv_halo"] == 1           # dX of conv2_1: 64 outputs, factored
+    assert plan(1, 64, 112, 112, 128, 128)["conv_halo"] == 0          # dX, 128 outputs, 4 chunks: tap by tap
+    p = plan(0, 1, 2, 452, 32, 128)                                   # rows too wide to flip: pair tiles
+    assert p["conv_halo"] == 1 and p["conv_hflip"] == 0 and p["pair"] == 1 and p["bn"] == 128
     assert plan(0, 64, 56, 56, 128, 256)["conv_halo"] == 0            # 256 output channels: tap by tap
     assert plan(0, 64, 14, 14, 64, 64)["conv_halo"] == 0              # 196 of 256 rows: tap by tap
+    assert plan(0, 128, 16, 16, 128, 128)["conv_halo"] == 0           # 256 of 512 positions: tap by tap
     assert plan(0, 2, 4, 100, 64, 64)["conv_fact"] == 1               # 100 of 128 rows: factored
     assert plan(0, 2, 8, 8, 48, 64)["conv_halo"] == 0                 # input channels % 32 != 0
 

@@ -522,17 +522,15 @@ CONV_CASES = [
     (1, 3, 253, 64, 96),    # input gradient factored (k = 3 x 96), three tiles per row, odd tile count
     # 64 or 128 output channels: halo-staged tiles of whole output rows
     (2, 6, 112, 64, 128),   # forward BN 128, input gradient BN 64; one 112-pixel row per tile
-    (2, 6, 56, 128, 64),    # two rows of 56 pixels per tile, four input chunks (forward), BN 128 (dX)
+    (2, 8, 56, 128, 64),    # two rows of 56 pixels per tile, four input chunks (forward)
+    (2, 8, 56, 128, 256),   # input gradient with 128 outputs and 8 chunks: flipped, four 56-pixel rows per tile
+    (1, 2, 452, 32, 128),   # rows too wide to flip: forward on pair tiles of 113 pixels, N = 128
     (1, 4, 224, 64, 64),    # two tiles per row (the VGG conv1_2 width)
     (1, 6, 56, 64, 64),     # odd tile count: the last pair's second CTA has no tile
     (2, 15, 28, 64, 128),   # four rows per tile, the last tile row holds three
     (1, 3, 221, 64, 64),    # two tiles per row, the second one pixel short
 ]
 
-# the cases above whose 64-channel outputs (forward or input gradient) and 128-channel forward
-# outputs take the halo-staged tiles
-HALO_CASES = {(2, 6, 112, 64, 128), (2, 6, 56, 128, 64), (1, 4, 224, 64, 64), (1, 6, 56, 64, 64),
-              (2, 15, 28, 64, 128), (1, 3, 221, 64, 64)}
 
 
 def _conv_inputs(seed, N, H, W, Cin, Cout):
@@ -548,18 +546,33 @@ def _ws(S, op, *shape):
 
 
 def test_conv_plans_of_the_cases(S):
-    """The small cases reach both the halo-staged and the factored forward /
-    input-gradient tiles (whole-tensor parity below covers every tile edge)."""
+    """The small cases reach every forward / input-gradient tiling of the 64- and 128-channel
+    outputs (whole-tensor parity below covers every tile edge): halo-staged pairs factored to
+    192 columns (one-row tiles with TMA epilogue boxes, and multi-row tiles), the flipped
+    128-channel tiles (forward and input gradient), pair tiles of N = 128, and the factored
+    tap windows."""
+    seen = set()
     for case in CONV_CASES:
         N, H, W, Cin, Cout = case
         for op in (S.SPRINT_CONV_FWD, S.SPRINT_CONV_DX):
             pl = S.sprint_conv_plan(op, N, H, W, Cin, Cout, 1, True)
             nout = Cout if op == S.SPRINT_CONV_FWD else Cin
-            want = case in HALO_CASES and (nout == 64 or op == S.SPRINT_CONV_FWD)
-            assert bool(pl["conv_halo"]) == (want and pl["path"] == "tc"), (case, op, pl)
             if pl["conv_halo"]:
-                assert pl["pair"] == 1 and pl["bn"] == (192 if nout == 64 else 128)
-    assert any(S.sprint_conv_plan(op, *c, 1, True)["conv_fact"] for c in CONV_CASES for op in (0, 1))
+                assert nout in (64, 128) and pl["path"] == "tc", (case, op, pl)
+                if nout == 64:
+                    assert pl["pair"] == 1 and pl["bn"] == 192 and not pl["conv_hflip"]
+                    seen.add(("fact192", pl["box_h"] == 1))
+                elif pl["conv_hflip"]:
+                    assert pl["pair"] == 0 and pl["bn"] == 128 and (pl["box_w"] + 2) * pl["box_h"] <= 256
+                    seen.add(("flip", op))
+                else:
+                    assert pl["pair"] == 1 and pl["bn"] == 128 and op == S.SPRINT_CONV_FWD
+                    seen.add(("pair128", op))
+            if pl["conv_fact"]:
+                seen.add(("fact", op))
+    want = {("fact192", True), ("fact192", False), ("flip", S.SPRINT_CONV_FWD), ("flip", S.SPRINT_CONV_DX),
+            ("pair128", S.SPRINT_CONV_FWD), ("fact", S.SPRINT_CONV_FWD), ("fact", S.SPRINT_CONV_DX)}
+    assert want <= seen, want - seen
 
 
 @pytest.mark.parametrize("N,H,W,Cin,Cout", CONV_CASES)
