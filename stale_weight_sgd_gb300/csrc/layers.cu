@@ -129,26 +129,32 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
 // both sides: dst[b*db + c*dc + (r/32)*drt + r%32] = src[b*sb + r*sr + c] for
 // r < R, c < C, b = blockIdx.z (drt = 32: dst[b*db + c*dc + r]). Used for
 // w -> w^T (one batch), NHWC -> [C][H][W][N] (batch = pixel) and NHWC ->
-// [H][W*N/32][C][32] (batch = pixel, dc = 32, drt = 32*C).
+// [H][W*N/32][C][32] (batch = pixel, dc = 32, drt = 32*C). A block takes CT
+// tiles side by side along c, so that each thread has 4 * CT loads in flight.
+template <int CT>
 __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int R,
                                                         int C, long long sb, long long sr, long long db, long long dc,
                                                         long long drt) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[CT][32][33];
     const long long b = blockIdx.z;
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int r0 = blockIdx.y * 32, cb = blockIdx.x * 32 * CT;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
 #pragma unroll
-    for (int j = ty; j < 32; j += 8) {
-        const int r = r0 + j, c = c0 + tx;
-        if (r < R && c < C) tile[j][tx] = src[b * sb + static_cast<long long>(r) * sr + c];
-    }
+    for (int ct = 0; ct < CT; ++ct)
+#pragma unroll
+        for (int j = ty; j < 32; j += 8) {
+            const int r = r0 + j, c = cb + 32 * ct + tx;
+            if (r < R && c < C) tile[ct][j][tx] = src[b * sb + static_cast<long long>(r) * sr + c];
+        }
     __syncthreads();
     const long long dst0 = b * db + blockIdx.y * drt;
 #pragma unroll
-    for (int j = ty; j < 32; j += 8) {
-        const int c = c0 + j, r = r0 + tx;
-        if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[tx][j];
-    }
+    for (int ct = 0; ct < CT; ++ct)
+#pragma unroll
+        for (int j = ty; j < 32; j += 8) {
+            const int c = cb + 32 * ct + j, r = r0 + tx;
+            if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[ct][tx][j];
+        }
 }
 
 int launch_transpose(const float* src, float* dst, int batch, int R, int C, long long sb, long long sr, long long db,
@@ -156,8 +162,13 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
     if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
-    dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
-    transpose_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
+    if (C >= 64) {
+        dim3 grid((C + 63) / 64, (R + 31) / 32, batch);
+        transpose_kernel<2><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
+    } else {
+        dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
+        transpose_kernel<1><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
+    }
     return check_launch("transpose_kernel");
 }
 
@@ -166,30 +177,35 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
 // columns (channels) are added in row order into partial[c * nparts + part],
 // part = batch index * row tiles + row tile; colsum_parts_finish then adds a
 // channel's parts in part order. One read of dy serves both dy^T and dedb.
+template <int CT>
 __global__ void __launch_bounds__(256) transpose_colsum_kernel(const float* __restrict__ src, float* __restrict__ dst,
                                                                int R, int C, long long sb, long long sr, long long db,
                                                                long long dc, long long drt, float* __restrict__ partial,
                                                                long long nparts) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[CT][32][33];
     const long long b = blockIdx.z;
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int r0 = blockIdx.y * 32, cb = blockIdx.x * 32 * CT;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
 #pragma unroll
-    for (int j = ty; j < 32; j += 8) {
-        const int r = r0 + j, c = c0 + tx;
-        tile[j][tx] = (r < R && c < C) ? src[b * sb + static_cast<long long>(r) * sr + c] : 0.f;
-    }
+    for (int ct = 0; ct < CT; ++ct)
+#pragma unroll
+        for (int j = ty; j < 32; j += 8) {
+            const int r = r0 + j, c = cb + 32 * ct + tx;
+            tile[ct][j][tx] = (r < R && c < C) ? src[b * sb + static_cast<long long>(r) * sr + c] : 0.f;
+        }
     __syncthreads();
     const long long dst0 = b * db + blockIdx.y * drt;
 #pragma unroll
-    for (int j = ty; j < 32; j += 8) {
-        const int c = c0 + j, r = r0 + tx;
-        if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[tx][j];
-    }
-    if (ty == 0 && c0 + tx < C) {
+    for (int ct = 0; ct < CT; ++ct)
+#pragma unroll
+        for (int j = ty; j < 32; j += 8) {
+            const int c = cb + 32 * ct + j, r = r0 + tx;
+            if (r < R && c < C) dst[dst0 + static_cast<long long>(c) * dc + tx] = tile[ct][tx][j];
+        }
+    if (ty < CT && cb + 32 * ty + tx < C) {   // warp ct adds sub-tile ct's columns
         float t = 0.f;
-        for (int j = 0; j < 32; ++j) t += tile[j][tx];
-        partial[static_cast<long long>(c0 + tx) * nparts + b * gridDim.y + blockIdx.y] = t;
+        for (int j = 0; j < 32; ++j) t += tile[ty][j][tx];
+        partial[static_cast<long long>(cb + 32 * ty + tx) * nparts + b * gridDim.y + blockIdx.y] = t;
     }
 }
 
@@ -222,8 +238,13 @@ int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int 
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
     const long long nparts = static_cast<long long>(batch) * ((R + 31) / 32);
-    dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
-    transpose_colsum_kernel<<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
+    if (C >= 64) {
+        dim3 grid((C + 63) / 64, (R + 31) / 32, batch);
+        transpose_colsum_kernel<2><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
+    } else {
+        dim3 grid((C + 31) / 32, (R + 31) / 32, batch);
+        transpose_colsum_kernel<1><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
+    }
     colsum_parts_finish<<<C, 256, 0, s>>>(partial, nparts, out, alpha, accumulate);
     return check_launch("transpose_colsum", 2);
 }
