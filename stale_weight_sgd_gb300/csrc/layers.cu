@@ -130,7 +130,8 @@ int launch_colsum(const float* in, long long rows, int cols, float* partial, flo
 // r < R, c < C, b = blockIdx.z (drt = 32: dst[b*db + c*dc + r]). Used for
 // w -> w^T (one batch), NHWC -> [C][H][W][N] (batch = pixel) and NHWC ->
 // [H][W*N/32][C][32] (batch = pixel, dc = 32, drt = 32*C). A block takes CT
-// tiles side by side along c, so that each thread has 4 * CT loads in flight.
+// tiles side by side along c (2 for C >= 64, 4 for C >= 128), so that each
+// thread has 4 * CT loads in flight: the copy is bound by the bytes in flight.
 template <int CT>
 __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int R,
                                                         int C, long long sb, long long sr, long long db, long long dc,
@@ -162,7 +163,10 @@ int launch_transpose(const float* src, float* dst, int batch, int R, int C, long
     if (batch <= 0 || R <= 0 || C <= 0) return SPRINT_OK;
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
-    if (C >= 64) {
+    if (C >= 128) {
+        dim3 grid((C + 127) / 128, (R + 31) / 32, batch);
+        transpose_kernel<4><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
+    } else if (C >= 64) {
         dim3 grid((C + 63) / 64, (R + 31) / 32, batch);
         transpose_kernel<2><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt);
     } else {
@@ -238,7 +242,10 @@ int launch_transpose_colsum(const float* src, float* dst, int batch, int R, int 
     if (batch > 65535 || (R + 31) / 32 > 65535)
         return fail(SPRINT_ERR_SHAPE, "transpose: batch %d / rows %d exceed the grid limits", batch, R);
     const long long nparts = static_cast<long long>(batch) * ((R + 31) / 32);
-    if (C >= 64) {
+    if (C >= 128) {
+        dim3 grid((C + 127) / 128, (R + 31) / 32, batch);
+        transpose_colsum_kernel<4><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
+    } else if (C >= 64) {
         dim3 grid((C + 63) / 64, (R + 31) / 32, batch);
         transpose_colsum_kernel<2><<<grid, 256, 0, s>>>(src, dst, R, C, sb, sr, db, dc, drt, partial, nparts);
     } else {
