@@ -2392,7 +2392,7 @@ extern "C" int sprint_conv_fwd(const float* x, const float* w, const float* b, f
         const uint64_t db[2] = {(uint64_t)TC_BK, (uint64_t)Cout}, sb[1] = {(uint64_t)TC_BK * 4};
         const uint32_t bb[2] = {32, 64};
         const uint64_t dd[2] = {(uint64_t)Cout, (uint64_t)P}, sd[1] = {(uint64_t)Cout * 4};
-        const uint32_t bd[2] = {32, 32};
+        const uint32_t bd[2] = {32, TC_BM};   // a tile's 128 rows x 32 channels per store
         if (!make_tmap(&tb, wpad, 2, db, sb, bb) || !make_tmap(&td, y, 2, dd, sd, bd, false))
             return fail(SPRINT_ERR_CUDA, "%s: tensor map setup failed", __func__);
         TcParams p = base_params();

@@ -59,7 +59,8 @@
 //               from x (act, NHWC) by four more warps (6-9, one row per lane),
 //               B = the weights padded to 32 columns (TMA, warp 4); the stage's
 //               barrier takes the TMA bytes and one arrival per im2col warp; the
-//               epilogue as for GEMM_2D over D = y [pixels][N].
+//               epilogue writes y [pixels][64] as two TMA boxes of 128 rows x 32
+//               channels per tile (double-buffered), the four warps' rows together.
 //   CONV_WGRAD: dedw conv, per tap: A = dy^T, B = x^T shifted by the tap; a
 //               k-tile is 32 consecutive (w, n) positions of one row, n fastest,
 //               so the tap's w-shift is N positions. The copies are either
@@ -679,7 +680,18 @@ __global__ void __launch_bounds__(tc_threads<ROLE>(), 1)
             int kt0, nkt, tap;
             k_range(tc, kt0, nkt, tap);
             const uint32_t b = j & 1, tph = (j >> 1) & 1;
-            if (!mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE)) break;
+            bool ok = mbar_wait_bounded(&tmem_full[b], tph, p.status, DEV_FLAG_WAIT_EPILOGUE);
+            if constexpr (ROLE == ROLE_CONV_RGB) {   // the four warps go on together, or none
+                uint32_t all;
+                asm volatile(
+                    "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 2, 128, p;\n\t"
+                    "selp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(all)
+                    : "r"(ok ? 1u : 0u)
+                    : "memory");
+                ok = all != 0;
+            }
+            if (!ok) break;
             tc_fence_after();
             const int n0 = tc.nt * BN, m0 = tc.mt * TC_BM;
             const CUtensorMap* mD = &maps.d[G > 1 ? tc.z : 0];
@@ -715,6 +727,45 @@ __global__ void __launch_bounds__(tc_threads<ROLE>(), 1)
                         *reinterpret_cast<float4*>(slab + c + q) =
                             make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
                                         __uint_as_float(v[q + 3]));
+                }
+                continue;
+            }
+            if constexpr (ROLE == ROLE_CONV_RGB) {
+                // the tile's 128 rows x 64 channels leave as two TMA boxes of 128 rows x 32 channels,
+                // written by the four warps into one of two 32 KB buffers (tile parity); warp 0 waits
+                // for the buffer's stores of two tiles ago and issues the new ones
+                uint8_t* buf = sStage + (j & 1) * 32768;
+                if (warp == 0 && lane == 0 && j >= 2) bulk_wait_read<1>();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + b * ACC_STRIDE + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+                    tmem_wait_ld();
+                    if (c == 32) {   // accumulator fully read: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster_relaxed(smem_u32(&tmem_empty[b]));
+                    }
+                    float o[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        float x = __uint_as_float(v[q]);
+                        if (bias) x += bias[c + q];
+                        o[q] = p.relu ? fmaxf(x, 0.f) : x;
+                    }
+                    uint8_t* half = buf + (c / 32) * 16384;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(half + r * 128 + ((q ^ (r & 7)) << 4)) =
+                            make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                }
+                fence_async_smem();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (warp == 0 && lane == 0) {
+                    tma_store_2d(mD, 0, m0, buf);
+                    tma_store_2d(mD, 32, m0, buf + 16384);
+                    bulk_commit();
                 }
                 continue;
             }
